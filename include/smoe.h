@@ -1,0 +1,216 @@
+/*
+ * smoe.h -- C ABI of the int4 routed-expert MoE layer for one GB300 (sm_103a).
+ *
+ * The layer is the sparse Mixture-of-Experts block of the Qwen3-Next /
+ * Qwen3.5-3.6 hybrid models that the Swiftlet runtime runs on Apple devices
+ * (pages: "Swiftlet Packs 80B Qwen Into Mac With 4.3GB Memory..." on xix.ai,
+ * paragraph on how it works; "Swiftletは低RAM使用量で..." on agentlenshq.com,
+ * section on how expert streaming works). For each token x (bf16, length H):
+ *
+ *   z  = W_r x (+ optional per-expert logit offset)       router, E logits
+ *   p  = softmax(z); ids = the k largest p (ties: lower id first)
+ *   w_j = p_{ids_j} / sum_j' p_{ids_j'}                     renormalised
+ *   f_e(x) = D_e (silu(G_e x) * (U_e x))                   SwiGLU expert
+ *   out = sum_{j<k} w_j f_{ids_j}(x) + sigmoid(w_s . x) f_shared(x)
+ *
+ * The routed and shared experts hold MLX-style affine 4-bit weights: groups of
+ * 64 along the input dimension, an fp16 scale s and bias b per group,
+ * w = s*q + b (same xix.ai page, last paragraph: "MLX-style int4/int8 group
+ * quantisation ... 64-bit offsets"). The routed experts of every layer live in
+ * one pool of fixed-stride blobs, one blob per expert, reached through a slot
+ * table (same page, paragraph on how it works: fixed-stride blobs, one read
+ * per expert, a bounded slot pool).
+ *
+ * Conventions for every call:
+ *  - Return value: SMOE_OK (0) or a negative SMOE_E* status. Nothing aborts,
+ *    prints, or throws across this ABI.
+ *  - Device memory is always owned by the caller. The library never allocates
+ *    device memory; smoe_workspace_bytes() says how much scratch to pass.
+ *  - "stream" is a cudaStream_t (NULL = legacy default stream). moe_route and
+ *    moe_forward only enqueue work on it: they never synchronise, so they can
+ *    be issued back to back and captured into a CUDA graph.
+ *  - bf16 / fp16 tensors are passed as uint16_t bit patterns.
+ *  - All tensors are dense and row-major (C order), 16-byte aligned.
+ */
+#ifndef SMOE_H
+#define SMOE_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SMOE_API __attribute__((visibility("default")))
+#else
+#define SMOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+#define SMOE_OK 0
+#define SMOE_EINVAL (-1)   /* bad argument: null pointer, bad size, misaligned */
+#define SMOE_ERANGE (-2)   /* slot or expert id out of range, duplicate slot */
+#define SMOE_ENOMEM (-3)   /* pool or workspace smaller than required */
+#define SMOE_ECUDA (-4)    /* a CUDA runtime call failed */
+#define SMOE_EDEVICE (-5)  /* a kernel reported a problem in the error word */
+#define SMOE_ENOTSUP (-6)  /* shape outside what the kernels support */
+
+/* Codes a kernel may store in the device error word (first one wins). */
+#define SMOE_DEV_BAD_SLOT 1     /* a selected expert's slot is < 0 or >= n_slots */
+#define SMOE_DEV_BAD_EXPERT 2   /* an id in ids[] is < 0 or >= E */
+#define SMOE_DEV_TIMEOUT 3      /* a bounded wait inside a kernel gave up */
+
+/* ------------------------------------------------------------------ shapes */
+/* H: hidden size; E: routed experts per layer; k: experts per token;
+ * I: routed expert intermediate size; I_shared: shared expert intermediate
+ * size; group: quantisation group (must be 64); bits: 4.
+ * Supported: H % 256 == 0, I % 64 == 0, 64 <= I <= 512, I_shared == I,
+ * 1 <= k <= 16, k <= E <= 1024. Others return SMOE_ENOTSUP. */
+typedef struct smoe_shape {
+    int32_t H, E, k, I, I_shared, group, bits;
+} smoe_shape;
+
+/* ------------------------------------------------------------- blob layout */
+/* One expert blob (fixed stride, no padding at H=2048, I=512:
+ * 1,769,472 bytes = 432 * 4 KiB). It is made of 576-byte "atoms"; an atom
+ * holds 16 logical rows x one group of 64 input columns:
+ *   bytes [0,512): 32 lanes x 16 bytes; lane L = 4g+t (g < 8, t < 4) holds the
+ *     four uint32 words (row g, cols 16t..16t+7), (row g, cols 16t+8..16t+15),
+ *     (row g+8, cols 16t..16t+7), (row g+8, cols 16t+8..16t+15) of the group;
+ *     a word for columns c0..c0+7 keeps column c0+2m in bits 4m..4m+3 and
+ *     column c0+2m+1 in bits 16+4m..16+4m+3 (m < 4): even columns in the low
+ *     half-word, odd columns in the high half-word;
+ *   bytes [512,576): for g < 8, fp16 (s, b) of row g followed by (s, b) of
+ *     row g+8 (8 bytes per g).
+ * Gate/up part (first): atom index rb*(H/64) + kb for row block rb < I/8 and
+ *   input group kb < H/64; logical row g < 8 is gate row 8rb+g and logical row
+ *   g+8 is up row 8rb+g (the two rows SwiGLU multiplies sit together).
+ * Down part (second, at offset down_offset): atom index rd*(I/64) + kb for
+ *   row block rd < H/16 and input group kb < I/64; logical row i is down row
+ *   16rd+i.
+ * The 16x64 atom is the operand fragment of one 16x8x16 tensor-core step per
+ * lane, so the decode kernel loads a lane's share with one 128-bit load. */
+typedef struct smoe_layout {
+    uint64_t blob_bytes;    /* stride between slots */
+    uint64_t gu_offset;     /* 0 */
+    uint64_t gu_bytes;      /* (I/8)*(H/64)*576 */
+    uint64_t down_offset;   /* == gu_bytes */
+    uint64_t down_bytes;    /* (H/16)*(I/64)*576 */
+    uint32_t atom_bytes;    /* 576 */
+    uint32_t atom_rows;     /* 16 */
+    uint32_t group;         /* 64 */
+    uint32_t reserved;
+} smoe_layout;
+
+/* Fills *out for shape. Errors: SMOE_EINVAL (null), SMOE_ENOTSUP (shape). */
+SMOE_API int smoe_layout_of(const smoe_shape *shape, smoe_layout *out);
+
+/* ------------------------------------------------------------ pack_experts */
+/* MLX triples of one expert (as produced by MLX's affine quantisation):
+ * q[0] gate uint32 [I][H/8], q[1] up [I][H/8], q[2] down [H][I/8], column c of
+ * a row in bits 4*(c%8).. of word c/8; s[m], b[m] fp16 bits [rows][cols/64]. */
+typedef struct smoe_expert_src {
+    const uint32_t *q[3];
+    const uint16_t *s[3];
+    const uint16_t *b[3];
+} smoe_expert_src;
+
+#define SMOE_HOST 0     /* src triples and pool are host memory; runs on the CPU */
+#define SMOE_DEVICE 1   /* src triples and pool are device memory; a kernel on stream */
+
+/* Writes expert i's blob at pool + dst_slots[i] * layout.blob_bytes (64-bit
+ * offsets; the pool may span tens of GB) for i < n. src and dst_slots are
+ * host arrays of n entries; the pointers inside src point to memory of kind
+ * `where`. The pool must hold at least (max slot + 1) * blob_bytes bytes
+ * (pool_bytes). With SMOE_DEVICE the copies are enqueued on stream and the
+ * triples must stay valid until they complete. Corresponds to the pages'
+ * repack step ("swiftlet-repack" builds fixed-stride containers from MLX
+ * checkpoints), done in memory.
+ * Errors: SMOE_EINVAL, SMOE_ENOTSUP, SMOE_ERANGE (slot < 0), SMOE_ENOMEM
+ * (slot past pool_bytes), SMOE_ECUDA. */
+SMOE_API int pack_experts(const smoe_shape *shape, const smoe_expert_src *src, int32_t n,
+                 const int64_t *dst_slots, void *pool, uint64_t pool_bytes,
+                 int32_t where, void *stream);
+
+/* ---------------------------------------------------------------- context */
+typedef struct smoe_ctx smoe_ctx;
+
+/* Creates a host-side context on the current CUDA device for shape, a stack
+ * of n_layers layers and a pool of n_slots slots. table_dev is caller-owned
+ * device memory of n_layers*E int32 (the slot table; filled by
+ * set_slot_table). The context allocates no device memory.
+ * Errors: SMOE_EINVAL, SMOE_ENOTSUP, SMOE_ECUDA. */
+SMOE_API int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_t n_slots,
+                    int32_t *table_dev, smoe_ctx **out);
+SMOE_API int smoe_ctx_destroy(smoe_ctx *ctx);
+
+/* ---------------------------------------------------------- set_slot_table */
+/* Sets layer's row of the slot table: expert e of that layer lives in slot
+ * host_table[e] (host array of E int32). Every entry must be in [0, n_slots)
+ * and the E entries distinct; else SMOE_ERANGE and nothing is written. The
+ * copy is enqueued on stream and this call waits for it, so host_table may be
+ * reused on return. Corresponds to the pages' slot pool: which slot holds
+ * which expert. Changing the table never changes results (bit-identical). */
+SMOE_API int set_slot_table(smoe_ctx *ctx, int32_t layer, const int32_t *host_table, void *stream);
+
+/* Bytes of scratch that moe_route / moe_forward need for T tokens. The caller
+ * allocates it on the device and zero-fills it once before first use; every
+ * call leaves its counters at zero again, so it can be reused without
+ * clearing. Calls that use the same workspace must not overlap on the GPU. */
+SMOE_API uint64_t smoe_workspace_bytes(const smoe_ctx *ctx, int32_t T);
+
+/* --------------------------------------------------------------- moe_route */
+/* Router for T tokens: logits z = W_r x (+ logit_bias), softmax, top-k with
+ * ties to the lower id, renormalised weights, and the shared-expert gate.
+ *   W_r   bf16 [E][H] device   router rows
+ *   w_s   bf16 [H]    device   shared-expert gate vector
+ *   x     bf16 [T][H] device   token activations
+ *   logit_bias fp32 [E] device or NULL, added to the logits
+ *   ids   int32 [T][k] device  out: chosen experts, descending probability
+ *   w     fp32  [T][k] device  out: renormalised weights (sum to 1 per token)
+ *   gate  fp32  [T]    device  out: sigmoid(w_s . x)
+ * Logits are accumulated in fp32. Errors: SMOE_EINVAL, SMOE_ENOMEM
+ * (workspace), SMOE_ECUDA (launch). */
+SMOE_API int moe_route(const smoe_ctx *ctx, const uint16_t *W_r, const uint16_t *w_s,
+              const uint16_t *x, int32_t T, const float *logit_bias,
+              int32_t *ids, float *w, float *gate,
+              void *workspace, uint64_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------- moe_forward */
+/* The expert part of the layer for T tokens given their routing:
+ *   out[t] = sum_{j<k} w[t][j] f_{ids[t][j]}(x_t) + gate[t] f_shared(x_t)
+ *            (+ residual[t] if residual != NULL), rounded once to bf16.
+ * Routed expert e of `layer` is read from pool + table[layer][e] * blob_bytes;
+ * the shared expert from shared_blob (one blob of the same layout).
+ *   x        bf16 [T][H] device
+ *   ids, w, gate   as written by moe_route (device)
+ *   pool     device, pool_bytes >= n_slots * blob_bytes
+ *   residual bf16 [T][H] device or NULL
+ *   out      bf16 [T][H] device (may alias residual, not x)
+ *   err      int32 device error word; the first device-side problem stores a
+ *            SMOE_DEV_* code there (the expert concerned contributes zero) and
+ *            nothing traps. Read it with smoe_check().
+ * Partial sums are fp32 and are combined in a fixed order (route order for
+ * each token, then the shared term), so the result does not depend on
+ * scheduling, slot placement or run: bit-identical across runs and slot
+ * permutations. T <= 8 takes the fused decode kernel; larger T the
+ * token-bucketed path. Errors: SMOE_EINVAL, SMOE_ENOMEM, SMOE_ECUDA. */
+SMOE_API int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x, int32_t T,
+                const int32_t *ids, const float *w, const float *gate,
+                const void *pool, uint64_t pool_bytes, const void *shared_blob,
+                const uint16_t *residual, uint16_t *out,
+                void *workspace, uint64_t workspace_bytes, int32_t *err, void *stream);
+
+/* Waits for stream, reads the error word (then clears it to 0) and returns
+ * SMOE_OK, SMOE_EDEVICE if a kernel stored a code (copied to *code if
+ * non-NULL), or SMOE_ECUDA. Not for use inside graph capture. */
+SMOE_API int smoe_check(int32_t *err_dev, int32_t *code, void *stream);
+
+/* Short English text for a status code (static storage). */
+SMOE_API const char *smoe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SMOE_H */

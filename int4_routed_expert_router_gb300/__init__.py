@@ -1,0 +1,196 @@
+"""Python binding of libsmoe.so, the int4 routed-expert MoE layer for GB300.
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels
+behind the C ABI (``include/smoe.h``). Device tensors are torch tensors (used
+for device memory and streams); host buffers are numpy arrays. If the library
+is not built this module raises on first use: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libsmoe.so")
+
+OK, EINVAL, ERANGE, ENOMEM, ECUDA, EDEVICE, ENOTSUP = 0, -1, -2, -3, -4, -5, -6
+DEV_BAD_SLOT, DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2, 3
+HOST, DEVICE = 0, 1
+EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destroy", "set_slot_table",
+           "smoe_workspace_bytes", "moe_route", "moe_forward", "smoe_check", "smoe_status_string"]
+
+
+class SmoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s failed: %s (%d)" % (what, status_string(status), status))
+        self.status = status
+
+
+class Shape(C.Structure):
+    _fields_ = [("H", C.c_int32), ("E", C.c_int32), ("k", C.c_int32), ("I", C.c_int32),
+                ("I_shared", C.c_int32), ("group", C.c_int32), ("bits", C.c_int32)]
+
+
+class Layout(C.Structure):
+    _fields_ = [("blob_bytes", C.c_uint64), ("gu_offset", C.c_uint64), ("gu_bytes", C.c_uint64),
+                ("down_offset", C.c_uint64), ("down_bytes", C.c_uint64), ("atom_bytes", C.c_uint32),
+                ("atom_rows", C.c_uint32), ("group", C.c_uint32), ("reserved", C.c_uint32)]
+
+
+class ExpertSrc(C.Structure):
+    _fields_ = [("q", C.c_void_p * 3), ("s", C.c_void_p * 3), ("b", C.c_void_p * 3)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libsmoe.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libsmoe.so is not built (run __graft_entry__.build() or "
+                               "python int4_routed_expert_router_gb300/_build.py)")
+        L = C.CDLL(LIB_PATH)
+        vp, i32, i64, u64 = C.c_void_p, C.c_int32, C.c_int64, C.c_uint64
+        L.smoe_layout_of.argtypes = [C.POINTER(Shape), C.POINTER(Layout)]
+        L.pack_experts.argtypes = [C.POINTER(Shape), C.POINTER(ExpertSrc), i32, C.POINTER(C.c_int64), vp, u64,
+                                   i32, vp]
+        L.smoe_ctx_create.argtypes = [C.POINTER(Shape), i32, i64, vp, C.POINTER(vp)]
+        L.smoe_ctx_destroy.argtypes = [vp]
+        L.set_slot_table.argtypes = [vp, i32, vp, vp]
+        L.smoe_workspace_bytes.argtypes = [vp, i32]
+        L.smoe_workspace_bytes.restype = u64
+        L.moe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, u64, vp]
+        L.moe_forward.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, u64, vp, vp, vp, vp, u64, vp, vp]
+        L.smoe_check.argtypes = [vp, C.POINTER(C.c_int32), vp]
+        L.smoe_status_string.argtypes = [C.c_int]
+        L.smoe_status_string.restype = C.c_char_p
+        for name in EXPORTS:
+            if name not in ("smoe_workspace_bytes", "smoe_status_string"):
+                getattr(L, name).restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().smoe_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise SmoeError(rc, what)
+
+
+def _ptr(t) -> int | None:
+    """Raw address of a torch tensor / numpy array (None stays NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except Exception:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_shape(H, E, k, I, I_shared=None) -> Shape:
+    return Shape(H, E, k, I, I if I_shared is None else I_shared, 64, 4)
+
+
+def layout_of(shape: Shape) -> Layout:
+    out = Layout()
+    _check(lib().smoe_layout_of(C.byref(shape), C.byref(out)), "smoe_layout_of")
+    return out
+
+
+def expert_src(arrays) -> ExpertSrc:
+    """9 arrays/tensors in the order gate q,s,b, up q,s,b, down q,s,b."""
+    st = ExpertSrc()
+    for m in range(3):
+        st.q[m] = _ptr(arrays[3 * m])
+        st.s[m] = _ptr(arrays[3 * m + 1])
+        st.b[m] = _ptr(arrays[3 * m + 2])
+    return st
+
+
+def pack_experts(shape: Shape, experts, slots, pool, pool_bytes: int, where: int, stream=None):
+    """experts: list of 9-array lists (host numpy or device torch, per `where`)."""
+    n = len(experts)
+    srcs = (ExpertSrc * n)(*[expert_src(e) for e in experts])
+    sl = (C.c_int64 * n)(*[int(s) for s in slots])
+    st = None if where == HOST else _stream(stream)
+    _check(lib().pack_experts(C.byref(shape), srcs, n, sl, _ptr(pool), int(pool_bytes), where, st),
+           "pack_experts")
+
+
+class Context:
+    """Host-side context for one shape / layer stack / slot pool (smoe_ctx)."""
+
+    def __init__(self, shape: Shape, n_layers: int, n_slots: int, table_dev):
+        self.shape = shape
+        self.n_layers = n_layers
+        self.n_slots = n_slots
+        self.table = table_dev          # keep the caller's tensor alive
+        h = C.c_void_p()
+        _check(lib().smoe_ctx_create(C.byref(shape), n_layers, n_slots, _ptr(table_dev), C.byref(h)),
+               "smoe_ctx_create")
+        self.handle = h.value
+        self.layout = layout_of(shape)
+
+    def close(self):
+        if self.handle:
+            lib().smoe_ctx_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_bytes(self, T: int) -> int:
+        return int(lib().smoe_workspace_bytes(self.handle, int(T)))
+
+
+def set_slot_table(ctx: Context, layer: int, host_table: np.ndarray, stream=None):
+    tab = np.ascontiguousarray(host_table, np.int32)
+    _check(lib().set_slot_table(ctx.handle, int(layer), tab.ctypes.data, _stream(stream)), "set_slot_table")
+
+
+def moe_route(ctx: Context, W_r, w_s, x, ids, w, gate, workspace, logit_bias=None, stream=None):
+    T = x.shape[0]
+    _check(lib().moe_route(ctx.handle, _ptr(W_r), _ptr(w_s), _ptr(x), T, _ptr(logit_bias), _ptr(ids), _ptr(w),
+                           _ptr(gate), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(stream)), "moe_route")
+
+
+def moe_forward(ctx: Context, layer: int, x, ids, w, gate, pool, shared_blob, out, workspace, err,
+                residual=None, stream=None):
+    T = x.shape[0]
+    _check(lib().moe_forward(ctx.handle, int(layer), _ptr(x), T, _ptr(ids), _ptr(w), _ptr(gate), _ptr(pool),
+                             pool.numel() * pool.element_size(), _ptr(shared_blob), _ptr(residual), _ptr(out),
+                             _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
+                             _stream(stream)), "moe_forward")
+
+
+def check(err, stream=None) -> int:
+    """Synchronises, returns the device error code (0 if none) and clears it."""
+    code = C.c_int32(0)
+    rc = lib().smoe_check(_ptr(err), C.byref(code), _stream(stream))
+    if rc not in (OK, EDEVICE):
+        raise SmoeError(rc, "smoe_check")
+    return int(code.value)

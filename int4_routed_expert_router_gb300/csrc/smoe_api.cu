@@ -1,0 +1,360 @@
+// smoe_api.cu -- the C ABI declared in include/smoe.h: blob layout, packing of
+// MLX triples into fixed-stride blobs, context and slot table, workspace
+// carving, and dispatch of the router / expert kernels.
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "smoe_dev.cuh"
+#include "smoe_internal.h"
+
+using namespace smoe;
+
+namespace smoe {
+
+// ------------------------------------------------------------------ packing
+// Blob word for MLX word mw (columns c0..c0+7 of one row, column c0+j in bits
+// 4j..4j+3): column c0+2m goes to bits 4m.., column c0+2m+1 to bits 16+4m..
+__host__ __device__ inline uint32_t blob_word(uint32_t mw)
+{
+    uint32_t out = 0;
+    for (int m = 0; m < 4; ++m) {
+        out |= ((mw >> (8 * m)) & 0xFu) << (4 * m);
+        out |= ((mw >> (8 * m + 4)) & 0xFu) << (16 + 4 * m);
+    }
+    return out;
+}
+
+// Source (matrix, row) of logical row lr (0..15) of atom row block rb.
+__host__ __device__ inline void atom_row(bool down, int rb, int lr, int *mat, int *row)
+{
+    if (!down) {
+        *mat = lr < 8 ? 0 : 1;            // gate rows then up rows
+        *row = 8 * rb + (lr & 7);
+    } else {
+        *mat = 2;
+        *row = 16 * rb + lr;
+    }
+}
+
+// The 16 bytes of lane L of atom (part, rb, kb).
+__host__ __device__ inline uint4 atom_lane(const smoe_expert_src &src, int H, int I, bool down, int rb, int kb,
+                                           int L)
+{
+    const int g = L >> 2, t = L & 3;
+    const int wpr = down ? I / 8 : H / 8;
+    const int w0 = kb * 8 + 2 * t;     // MLX word of columns kb*64 + 16t ..
+    uint32_t out[4];
+    for (int half = 0; half < 2; ++half) {     // row g, row g+8
+        int mat, row;
+        atom_row(down, rb, g + 8 * half, &mat, &row);
+        const uint32_t *q = src.q[mat] + size_t(row) * wpr;
+        out[2 * half] = blob_word(q[w0]);
+        out[2 * half + 1] = blob_word(q[w0 + 1]);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// The 8 bytes (s_g, b_g, s_g8, b_g8) of scale entry g of atom (part, rb, kb).
+__host__ __device__ inline uint2 atom_sb(const smoe_expert_src &src, int H, int I, bool down, int rb, int kb, int g)
+{
+    const int gpr = down ? I / kGroup : H / kGroup;
+    uint32_t v[2];
+    for (int half = 0; half < 2; ++half) {
+        int mat, row;
+        atom_row(down, rb, g + 8 * half, &mat, &row);
+        const size_t i = size_t(row) * gpr + kb;
+        v[half] = uint32_t(src.s[mat][i]) | (uint32_t(src.b[mat][i]) << 16);
+    }
+    return make_uint2(v[0], v[1]);
+}
+
+void pack_host(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst)
+{
+    const Layout L = layout_of(s.H, s.I);
+    for (int part = 0; part < 2; ++part) {
+        const bool down = part == 1;
+        const int nrb = down ? s.H / 16 : s.I / 8, nkb = down ? s.I / kGroup : s.H / kGroup;
+        uint8_t *base = dst + (down ? L.down_off : L.gu_off);
+        for (int rb = 0; rb < nrb; ++rb)
+            for (int kb = 0; kb < nkb; ++kb) {
+                uint8_t *atom = base + (size_t(rb) * nkb + kb) * kAtomBytes;
+                for (int lane = 0; lane < 32; ++lane) {
+                    const uint4 v = atom_lane(src, s.H, s.I, down, rb, kb, lane);
+                    std::memcpy(atom + 16 * lane, &v, 16);
+                }
+                for (int g = 0; g < 8; ++g) {
+                    const uint2 v = atom_sb(src, s.H, s.I, down, rb, kb, g);
+                    std::memcpy(atom + kAtomQBytes + 8 * g, &v, 8);
+                }
+            }
+    }
+}
+
+// One thread per (atom, lane): 16 bytes of nibbles, and for lanes < 8 the 8
+// bytes of scales/biases.
+__global__ void pack_kernel(const smoe_expert_src src, int H, int I, uint8_t *dst, uint64_t down_off,
+                            long long n_gu_atoms, long long n_atoms)
+{
+    const long long total = n_atoms * 32;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long a = i >> 5;
+        const int lane = int(i & 31);
+        const bool down = a >= n_gu_atoms;
+        const long long ai = down ? a - n_gu_atoms : a;
+        const int nkb = down ? I / kGroup : H / kGroup;
+        const int rb = int(ai / nkb), kb = int(ai % nkb);
+        uint8_t *atom = dst + (down ? down_off : 0) + ai * kAtomBytes;
+        *reinterpret_cast<uint4 *>(atom + 16 * lane) = atom_lane(src, H, I, down, rb, kb, lane);
+        if (lane < 8) *reinterpret_cast<uint2 *>(atom + kAtomQBytes + 8 * lane) = atom_sb(src, H, I, down, rb, kb, lane);
+    }
+}
+
+cudaError_t launch_pack_device(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst, cudaStream_t st)
+{
+    const Layout L = layout_of(s.H, s.I);
+    const long long ngu = (long long)(s.I / 8) * (s.H / kGroup);
+    const long long nd = (long long)(s.H / 16) * (s.I / kGroup);
+    const long long threads = (ngu + nd) * 32;
+    const int block = 256;
+    const long long grid = (threads + block - 1) / block;
+    pack_kernel<<<unsigned(grid < 65535 ? grid : 65535), block, 0, st>>>(src, s.H, s.I, dst, L.down_off, ngu,
+                                                                         ngu + nd);
+    return cudaGetLastError();
+}
+
+Workspace workspace_layout(const smoe_shape &s, int T)
+{
+    auto al = [](uint64_t v) { return (v + 255) & ~uint64_t(255); };
+    Workspace w;
+    uint64_t o = 0;
+    w.route_counter = o; o = al(o + 64);
+    w.fwd_counters = o;  o = al(o + 64 * 4);
+    w.logits = o;        o = al(o + uint64_t(T) * (s.E + 1) * 4);
+    const uint64_t umax = uint64_t(s.E < T * s.k ? s.E : T * s.k) + 1;
+    w.ypair = o;
+    if (T <= kDecodeMaxT) o = al(o + umax * T * s.H * 4);
+    w.total = o;
+    return w;
+}
+
+}  // namespace smoe
+
+// ====================================================================== C ABI
+static int shape_check(const smoe_shape *s)
+{
+    if (!s) return SMOE_EINVAL;
+    if (s->group != 64 || s->bits != 4) return SMOE_ENOTSUP;
+    if (s->H <= 0 || s->E <= 0 || s->k <= 0 || s->I <= 0) return SMOE_EINVAL;
+    if (s->H % 256 || s->H > 4096) return SMOE_ENOTSUP;
+    if (s->I % 64 || s->I < 64 || s->I > 512 || s->I_shared != s->I) return SMOE_ENOTSUP;
+    if (s->k > 16 || s->k > s->E || s->E > 1024) return SMOE_ENOTSUP;
+    return SMOE_OK;
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SMOE_OK : SMOE_ECUDA; }
+
+extern "C" int smoe_layout_of(const smoe_shape *shape, smoe_layout *out)
+{
+    int rc = shape_check(shape);
+    if (rc) return rc;
+    if (!out) return SMOE_EINVAL;
+    const Layout L = layout_of(shape->H, shape->I);
+    out->blob_bytes = L.blob;
+    out->gu_offset = L.gu_off;
+    out->gu_bytes = L.gu_bytes;
+    out->down_offset = L.down_off;
+    out->down_bytes = L.down_bytes;
+    out->atom_bytes = kAtomBytes;
+    out->atom_rows = kAtomRows;
+    out->group = kGroup;
+    out->reserved = 0;
+    return SMOE_OK;
+}
+
+extern "C" int pack_experts(const smoe_shape *shape, const smoe_expert_src *src, int32_t n,
+                            const int64_t *dst_slots, void *pool, uint64_t pool_bytes, int32_t where,
+                            void *stream)
+{
+    int rc = shape_check(shape);
+    if (rc) return rc;
+    if (n < 0 || (n > 0 && (!src || !dst_slots || !pool))) return SMOE_EINVAL;
+    if (where != SMOE_HOST && where != SMOE_DEVICE) return SMOE_EINVAL;
+    const Layout L = layout_of(shape->H, shape->I);
+    for (int i = 0; i < n; ++i) {
+        for (int m = 0; m < 3; ++m)
+            if (!src[i].q[m] || !src[i].s[m] || !src[i].b[m]) return SMOE_EINVAL;
+        if (dst_slots[i] < 0) return SMOE_ERANGE;
+        const uint64_t end = (uint64_t(dst_slots[i]) + 1) * L.blob;
+        if (end / L.blob != uint64_t(dst_slots[i]) + 1 || end > pool_bytes) return SMOE_ENOMEM;
+    }
+    uint8_t *base = static_cast<uint8_t *>(pool);
+    for (int i = 0; i < n; ++i) {
+        uint8_t *dst = base + uint64_t(dst_slots[i]) * L.blob;
+        if (where == SMOE_HOST) {
+            pack_host(*shape, src[i], dst);
+        } else {
+            cudaError_t e = launch_pack_device(*shape, src[i], dst, static_cast<cudaStream_t>(stream));
+            if (e != cudaSuccess) return SMOE_ECUDA;
+        }
+    }
+    return SMOE_OK;
+}
+
+extern "C" int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_t n_slots, int32_t *table_dev,
+                               smoe_ctx **out)
+{
+    int rc = shape_check(shape);
+    if (rc) return rc;
+    if (!out || n_layers <= 0 || n_slots <= 0 || !table_dev) return SMOE_EINVAL;
+    *out = nullptr;
+    smoe_ctx *c = new (std::nothrow) smoe_ctx();
+    if (!c) return SMOE_ENOMEM;
+    c->shape = *shape;
+    c->layout = layout_of(shape->H, shape->I);
+    c->n_layers = n_layers;
+    c->n_slots = n_slots;
+    c->table_dev = table_dev;
+    c->cs = shape->I / kSlice;
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    if (e == cudaSuccess) e = route_config();
+    if (e == cudaSuccess) e = decode_config(c);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete c;
+        return e == cudaErrorInvalidConfiguration || e == cudaErrorInvalidValue ? SMOE_ENOTSUP : SMOE_ECUDA;
+    }
+    *out = c;
+    return SMOE_OK;
+}
+
+extern "C" int smoe_ctx_destroy(smoe_ctx *ctx)
+{
+    delete ctx;
+    return SMOE_OK;
+}
+
+extern "C" int set_slot_table(smoe_ctx *ctx, int32_t layer, const int32_t *host_table, void *stream)
+{
+    if (!ctx || !host_table || layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
+    const int E = ctx->shape.E;
+    std::vector<int32_t> tmp(host_table, host_table + E);
+    for (int e = 0; e < E; ++e)
+        if (tmp[e] < 0 || tmp[e] >= ctx->n_slots) return SMOE_ERANGE;
+    std::qsort(tmp.data(), tmp.size(), sizeof(int32_t), [](const void *a, const void *b) {
+        const int32_t x = *static_cast<const int32_t *>(a), y = *static_cast<const int32_t *>(b);
+        return (x > y) - (x < y);
+    });
+    for (size_t i = 1; i < tmp.size(); ++i)
+        if (tmp[i] == tmp[i - 1]) return SMOE_ERANGE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(ctx->table_dev + size_t(layer) * E, host_table, sizeof(int32_t) * E,
+                                    cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return cuda_status(e);
+}
+
+extern "C" uint64_t smoe_workspace_bytes(const smoe_ctx *ctx, int32_t T)
+{
+    if (!ctx || T <= 0) return 0;
+    return workspace_layout(ctx->shape, T).total;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+extern "C" int moe_route(const smoe_ctx *ctx, const uint16_t *W_r, const uint16_t *w_s, const uint16_t *x,
+                         int32_t T, const float *logit_bias, int32_t *ids, float *w, float *gate, void *workspace,
+                         uint64_t workspace_bytes, void *stream)
+{
+    if (!ctx || !W_r || !w_s || !x || !ids || !w || !gate || !workspace || T < 0) return SMOE_EINVAL;
+    if (T == 0) return SMOE_OK;
+    if (!aligned16(W_r) || !aligned16(w_s) || !aligned16(x) || !aligned16(workspace)) return SMOE_EINVAL;
+    const Workspace W = workspace_layout(ctx->shape, T);
+    if (workspace_bytes < W.total) return SMOE_ENOMEM;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    RouteParams p = {};
+    p.Wr = W_r;
+    p.ws = w_s;
+    p.x = x;
+    p.bias = logit_bias;
+    p.logits = reinterpret_cast<float *>(ws + W.logits);
+    p.ids = ids;
+    p.w = w;
+    p.gate = gate;
+    p.counter = reinterpret_cast<uint32_t *>(ws + W.route_counter);
+    p.err = nullptr;
+    p.T = T;
+    p.H = ctx->shape.H;
+    p.E = ctx->shape.E;
+    p.k = ctx->shape.k;
+    return cuda_status(launch_route(p, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x, int32_t T, const int32_t *ids,
+                           const float *w, const float *gate, const void *pool, uint64_t pool_bytes,
+                           const void *shared_blob, const uint16_t *residual, uint16_t *out, void *workspace,
+                           uint64_t workspace_bytes, int32_t *err, void *stream)
+{
+    if (!ctx || !x || !ids || !w || !gate || !pool || !shared_blob || !out || !workspace || !err || T < 0)
+        return SMOE_EINVAL;
+    if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
+    if (T == 0) return SMOE_OK;
+    if (!aligned16(x) || !aligned16(pool) || !aligned16(shared_blob) || !aligned16(workspace)) return SMOE_EINVAL;
+    if (pool_bytes < uint64_t(ctx->n_slots) * ctx->layout.blob) return SMOE_ENOMEM;
+    const Workspace W = workspace_layout(ctx->shape, T);
+    if (workspace_bytes < W.total) return SMOE_ENOMEM;
+    if (T > kDecodeMaxT) return SMOE_ENOTSUP;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    DecodeParams p = {};
+    p.x = x;
+    p.ids = ids;
+    p.w = w;
+    p.gate = gate;
+    p.pool = static_cast<const uint8_t *>(pool);
+    p.shared_blob = static_cast<const uint8_t *>(shared_blob);
+    p.table_row = ctx->table_dev + size_t(layer) * ctx->shape.E;
+    p.residual = residual;
+    p.out = out;
+    p.ypair = reinterpret_cast<float *>(ws + W.ypair);
+    p.counters = reinterpret_cast<uint32_t *>(ws + W.fwd_counters);
+    p.err = err;
+    p.stride = ctx->layout.blob;
+    p.n_slots = ctx->n_slots;
+    p.T = T;
+    p.H = ctx->shape.H;
+    p.E = ctx->shape.E;
+    p.k = ctx->shape.k;
+    p.I = ctx->shape.I;
+    return cuda_status(launch_decode(ctx, p, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int smoe_check(int32_t *err_dev, int32_t *code, void *stream)
+{
+    if (!err_dev) return SMOE_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, err_dev, sizeof h, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess && h != 0) e = cudaMemsetAsync(err_dev, 0, sizeof h, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return SMOE_ECUDA;
+    if (code) *code = h;
+    return h ? SMOE_EDEVICE : SMOE_OK;
+}
+
+extern "C" const char *smoe_status_string(int status)
+{
+    switch (status) {
+    case SMOE_OK: return "ok";
+    case SMOE_EINVAL: return "invalid argument";
+    case SMOE_ERANGE: return "slot or expert id out of range";
+    case SMOE_ENOMEM: return "pool or workspace too small";
+    case SMOE_ECUDA: return "CUDA runtime error";
+    case SMOE_EDEVICE: return "kernel reported an error";
+    case SMOE_ENOTSUP: return "shape not supported";
+    default: return "unknown status";
+    }
+}

@@ -1,0 +1,111 @@
+// smoe_internal.h -- library-internal definitions shared by the host code and
+// the kernels (blob format constants, context, kernel parameter blocks).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/smoe.h"
+
+namespace smoe {
+
+constexpr int kGroup = 64;          // quantisation group along the input dim
+constexpr int kAtomRows = 16;       // rows per atom
+constexpr int kAtomQBytes = 512;    // packed nibbles of one atom
+constexpr int kAtomBytes = 576;     // nibbles + 16 (s, b) fp16 pairs
+
+// Decode kernel (fused experts, T <= kDecodeMaxT).
+constexpr int kDecodeMaxT = 8;
+constexpr int kSlice = 32;                        // intermediates per CTA
+constexpr int kChunkCols = 256;                   // H columns per streamed chunk
+constexpr int kRowBlocksA = kSlice / 8;           // gate/up row blocks per CTA
+constexpr int kChunkBytes = kRowBlocksA * (kChunkCols / kGroup) * kAtomBytes;   // 9216
+constexpr int kDecodeConsumerWarps = 8;
+constexpr int kDecodeThreads = (kDecodeConsumerWarps + 1) * 32;
+
+struct Layout {
+    uint64_t blob, gu_off, gu_bytes, down_off, down_bytes;
+};
+
+inline Layout layout_of(int H, int I)
+{
+    Layout L;
+    L.gu_off = 0;
+    L.gu_bytes = uint64_t(I / 8) * (H / kGroup) * kAtomBytes;
+    L.down_off = L.gu_bytes;
+    L.down_bytes = uint64_t(H / 16) * (I / kGroup) * kAtomBytes;
+    L.blob = L.gu_bytes + L.down_bytes;
+    return L;
+}
+
+struct DecodeCfg {
+    int nst = 0;            // ring stages
+    int smem = 0;           // dynamic shared memory bytes
+    int max_clusters = 0;   // co-resident clusters
+};
+
+}  // namespace smoe
+
+struct smoe_ctx {
+    smoe_shape shape;
+    smoe::Layout layout;
+    int32_t n_layers;
+    int64_t n_slots;
+    int32_t *table_dev;
+    int device;
+    int num_sms;
+    int cs;                                  // cluster size of the decode kernel = I / kSlice
+    smoe::DecodeCfg decode[smoe::kDecodeMaxT + 1];
+};
+
+namespace smoe {
+
+struct RouteParams {
+    const uint16_t *Wr;
+    const uint16_t *ws;
+    const uint16_t *x;
+    const float *bias;
+    float *logits;          // [T][E+1] (column E: shared-gate logit)
+    int32_t *ids;
+    float *w;
+    float *gate;
+    uint32_t *counter;
+    int32_t *err;
+    int T, H, E, k;
+    int fused_topk;
+};
+
+struct DecodeParams {
+    const uint16_t *x;
+    const int32_t *ids;
+    const float *w;
+    const float *gate;
+    const uint8_t *pool;
+    const uint8_t *shared_blob;
+    const int32_t *table_row;   // slot table row of this layer
+    const uint16_t *residual;
+    uint16_t *out;
+    float *ypair;               // [(U_max + 1)][T][H] fp32, expert outputs (unweighted)
+    uint32_t *counters;         // [cs] arrival tickets per row chunk
+    int32_t *err;
+    uint64_t stride;
+    int64_t n_slots;
+    int T, H, E, k, I;
+    int cs, nst;
+};
+
+// workspace carving (all offsets 256-byte aligned)
+struct Workspace {
+    uint64_t route_counter, logits, fwd_counters, ypair, total;
+};
+
+Workspace workspace_layout(const smoe_shape &s, int T);
+
+cudaError_t route_config();
+cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
+cudaError_t launch_decode(const smoe_ctx *ctx, const DecodeParams &p, cudaStream_t st);
+cudaError_t decode_config(smoe_ctx *ctx);
+cudaError_t launch_pack_device(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst,
+                               cudaStream_t st);
+void pack_host(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst);
+
+}  // namespace smoe

@@ -1,0 +1,123 @@
+"""C-ABI library checks that need no GPU: it loads, exports every declared
+symbol, reports the blob layout, and its host packer writes blobs that the
+oracle's independently written reader parses back to the source triples."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import int4_routed_expert_router_gb300 as smoe
+import oracle
+import synthetic
+from int4_routed_expert_router_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "smoe.h")).read()
+    return re.findall(r"SMOE_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert set(names) >= {"pack_experts", "set_slot_table", "moe_route", "moe_forward"}
+    L = smoe.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(smoe.EXPORTS)
+
+
+def test_layout_sizes():
+    lay = smoe.layout_of(smoe.make_shape(2048, 512, 10, 512))
+    assert lay.blob_bytes == 1769472 == 432 * 4096
+    assert lay.gu_bytes == 2 * 589824 and lay.down_offset == lay.gu_bytes and lay.down_bytes == 589824
+    assert (lay.atom_bytes, lay.atom_rows, lay.group) == (576, 16, 64)
+    tiny = smoe.layout_of(smoe.make_shape(256, 16, 4, 64))
+    assert tiny.blob_bytes == 27648 == oracle.blob_bytes(256, 64)
+
+
+@pytest.mark.parametrize("shape,status", [
+    ((2048, 512, 10, 512, 256), smoe.ENOTSUP),     # I_shared != I
+    ((2000, 512, 10, 512, 512), smoe.ENOTSUP),     # H not a multiple of 256
+    ((2048, 512, 10, 1024, 1024), smoe.ENOTSUP),   # I too large for the kernels
+    ((2048, 8, 10, 512, 512), smoe.ENOTSUP),       # k > E
+    ((2048, 512, 0, 512, 512), smoe.EINVAL),
+])
+def test_layout_rejects_bad_shapes(shape, status):
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.layout_of(smoe.make_shape(*shape))
+    assert ei.value.status == status
+
+
+def _triples(wl, layer, e):
+    return synthetic.expert_triples(wl.seed, layer, e, wl.H, wl.I).arrays()
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode80b"])
+def test_host_pack_round_trips_through_oracle_reader(name):
+    wl = synthetic.WORKLOADS[name]
+    shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I)
+    stride = smoe.layout_of(shape).blob_bytes
+    srcs = [_triples(wl, 0, e) for e in (3, 7)]
+    pool = np.zeros(3 * stride, np.uint8)
+    smoe.pack_experts(shape, srcs, [2, 0], pool, pool.size, smoe.HOST)
+    for src, slot in zip(srcs, [2, 0]):
+        back = oracle.blob_to_mlx(pool[slot * stride:(slot + 1) * stride], wl.H, wl.I)
+        for a, b in zip(src, back):
+            assert np.array_equal(a, b)
+    assert not pool[stride:2 * stride].any()        # slot 1 untouched
+
+
+def test_host_pack_beyond_4GiB_offsets():
+    wl = synthetic.WORKLOADS["decode80b"]
+    shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I)
+    stride = smoe.layout_of(shape).blob_bytes
+    slot = (1 << 32) // stride + 5                  # offset past 4 GiB
+    pool = np.empty((slot + 1) * stride, np.uint8)  # untouched pages cost no memory
+    src = _triples(wl, 1, 42)
+    smoe.pack_experts(shape, [src], [slot], pool, pool.size, smoe.HOST)
+    back = oracle.blob_to_mlx(pool[slot * stride:], wl.H, wl.I)
+    for a, b in zip(src, back):
+        assert np.array_equal(a, b)
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.pack_experts(shape, [src], [slot + 1], pool, pool.size, smoe.HOST)
+    assert ei.value.status == smoe.ENOMEM
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.pack_experts(shape, [src], [-1], pool, pool.size, smoe.HOST)
+    assert ei.value.status == smoe.ERANGE
+
+
+def test_oracle_pool_path_is_slot_permutation_invariant():
+    """Cache or disk, same answer: the oracle reading experts through any slot
+    permutation of the pool gives bit-identical output, equal to reading the
+    triples directly."""
+    wl = synthetic.WORKLOADS["tiny"]
+    shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I)
+    stride = smoe.layout_of(shape).blob_bytes
+    x = synthetic.activations(wl.seed, wl.T, wl.H)
+    Wr = synthetic.router_weights(wl.seed, 0, wl.E, wl.H)
+    ws = synthetic.shared_gate_weights(wl.seed, 0, wl.H)
+    ids, w, gate = oracle.route(x, Wr, ws, wl.k)
+    direct = oracle.layer(wl, 0, x, Wr, ws)
+    shared = np.zeros(stride, np.uint8)
+    smoe.pack_experts(shape, [synthetic.expert_triples(wl.seed, 0, None, wl.H, wl.I).arrays()], [0],
+                      shared, stride, smoe.HOST)
+    outs = []
+    for seed in range(3):
+        table = np.random.default_rng(seed).permutation(2 * wl.E)[:wl.E].astype(np.int32)
+        pool = np.zeros(2 * wl.E * stride, np.uint8)
+        smoe.pack_experts(shape, [_triples(wl, 0, e) for e in range(wl.E)], table.tolist(), pool, pool.size,
+                          smoe.HOST)
+        o64, ob = oracle.combine_pool(x, ids, w, gate, pool, stride, 2 * wl.E, table, shared, wl.E, wl.I)
+        outs.append(o64)
+        assert np.array_equal(ob, direct["out_bf16"])
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+    assert np.array_equal(outs[0], direct["out64"])
