@@ -1,0 +1,380 @@
+#!/usr/bin/env python
+"""Benchmark of the int4 routed-expert MoE layer on GB300.
+
+A step is one pass of the whole hot path over one batch: for the default
+workload (35B-A3B-shaped decode, T=1, a stack of 40 independent layers),
+per layer the router (moe_route) and the fused expert kernel (moe_forward,
+residual fused), all layers captured in one CUDA graph and replayed.
+
+Prints one JSON line. value = MoE-layer tokens/s = T * layers * steps / time
+(whole job: summed over ranks). The expert pool (18 GB at this shape) is far
+larger than the 129 MB L2 and each step streams 637 MB of distinct expert
+blobs, so no L2 flush is needed between steps.
+
+--impl reference times the CPU oracle (oracle/, one thread) on the same
+workload and metric, each step one layer for one token.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_SOURCES = ["int4_routed_expert_router_gb300/csrc/decode.cu",
+                  "int4_routed_expert_router_gb300/csrc/smoe_dev.cuh",
+                  "int4_routed_expert_router_gb300/csrc/smoe_internal.h"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode35b")
+    ap.add_argument("--layers", type=int, default=0, help="override the stack depth (profiling of small cases)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# --------------------------------------------------------------- clock sampler
+
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+           0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+           0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler(threading.Thread):
+    """Reads the SM clock, the max SM clock and the clock-event reasons
+    through NVML (read only) every few ms while running."""
+
+    def __init__(self, period=0.002):
+        super().__init__(daemon=True)
+        self.period = period
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.ok = False
+        try:
+            import torch
+            nv = C.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            props = torch.cuda.get_device_properties(torch.cuda.current_device())
+            bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+            h = C.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), C.byref(h)) != 0:
+                return
+            self.nv, self.h = nv, h
+            mx = C.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, 1, C.byref(mx))
+            self.max_mhz = mx.value
+            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except Exception:                                 # noqa: BLE001
+            self.ok = False
+
+    def run(self):
+        if not self.ok:
+            return
+        mhz, mask = C.c_uint(), C.c_ulonglong()
+        while not self.stop_flag.is_set():
+            self.nv.nvmlDeviceGetClockInfo(self.h, 1, C.byref(mhz))
+            self.reasons_fn(self.h, C.byref(mask))
+            self.samples.append((mhz.value, mask.value))
+            time.sleep(self.period)
+
+    def stop(self):
+        self.stop_flag.set()
+        if self.is_alive():
+            self.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": [],
+                    "samples": len(self.samples), "source": "nvml" if self.ok else "unavailable"}
+        bits = 0
+        for _, m in self.samples:
+            bits |= m
+        return {"sm_mhz": statistics.median(s for s, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in REASONS.items() if bits & b and n != "gpu_idle"],
+                "samples": len(self.samples), "source": "nvml"}
+
+
+# ---------------------------------------------------------------- helpers
+
+def src_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, only if the kernel sources are unchanged since it was taken."""
+    p = os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_sha256") != src_hash(DECODE_SOURCES) or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def config_of(wl, note=""):
+    blobs = wl.n_layers * (wl.k * wl.T + 1)
+    return {"workload": wl.name + ": " + wl.description, "H": wl.H, "E": wl.E, "k": wl.k, "I": wl.I,
+            "I_shared": wl.I_shared, "T": wl.T, "layers": wl.n_layers, "seed": wl.seed,
+            "l2": ("no flush: each step streams %d distinct expert blobs (%.0f MB) through the 129 MB L2"
+                   % (blobs, blobs * 1769472 / 1e6)) if wl.T == 1 else "see DESIGN.md",
+            "note": note}
+
+
+def cpu_baseline(wl, budget_s: float):
+    """The oracle as it stands (one thread) on a bounded sample of the
+    workload: one token through consecutive layers until the budget is used."""
+    import numpy as np
+
+    import oracle
+    import synthetic
+    x = synthetic.activations(wl.seed, wl.T, wl.H, tag=4242)
+    done, spent, layer = 0, 0.0, 0
+    while spent < budget_s and layer < wl.n_layers:
+        Wr = synthetic.router_weights(wl.seed, layer, wl.E, wl.H)
+        ws = synthetic.shared_gate_weights(wl.seed, layer, wl.H)
+        bias = synthetic.zipf_bias(wl.seed, wl.E) if wl.zipf else None
+        t0 = time.perf_counter()
+        ids, w, gate = oracle.route(x, Wr, ws, wl.k, bias=bias)
+        t_route = time.perf_counter() - t0
+        experts = {int(e): synthetic.expert_triples(wl.seed, layer, int(e), wl.H, wl.I) for e in np.unique(ids)}
+        shared = synthetic.expert_triples(wl.seed, layer, None, wl.H, wl.I_shared)
+        t0 = time.perf_counter()
+        out64, _ = oracle.combine(x, ids, w, gate, experts, shared, wl.E, wl.I, wl.I_shared)
+        spent += t_route + time.perf_counter() - t0
+        x = oracle.residual(x, out64)
+        done += wl.T
+        layer += 1
+    return {"value": done / spent, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d token(s) through %d of %d layers (expert regeneration excluded), %.1f s on one core"
+                      % (wl.T, layer, wl.n_layers, spent)}
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, wl, world, rank):
+    """The oracle timed on the host cores: each step one layer for one token."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import synthetic
+    pre = []
+    x = synthetic.activations(wl.seed, wl.T, wl.H, tag=4242)
+    for i in range(min(args.warmup + args.steps, wl.n_layers)):
+        Wr = synthetic.router_weights(wl.seed, i, wl.E, wl.H)
+        ws = synthetic.shared_gate_weights(wl.seed, i, wl.H)
+        bias = synthetic.zipf_bias(wl.seed, wl.E) if wl.zipf else None
+        ids, w, gate = oracle.route(x, Wr, ws, wl.k, bias=bias)
+        experts = {int(e): synthetic.expert_triples(wl.seed, i, int(e), wl.H, wl.I) for e in np.unique(ids)}
+        shared = synthetic.expert_triples(wl.seed, i, None, wl.H, wl.I_shared)
+        pre.append((x, Wr, ws, bias, experts, shared))
+        out64, _ = oracle.combine(x, ids, w, gate, experts, shared, wl.E, wl.I, wl.I_shared)
+        x = oracle.residual(x, out64)
+
+    def step(i):
+        x, Wr, ws, bias, experts, shared = pre[i % len(pre)]
+        ids, w, gate = oracle.route(x, Wr, ws, wl.k, bias=bias)
+        oracle.combine(x, ids, w, gate, experts, shared, wl.E, wl.I, wl.I_shared)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = args.steps * wl.T / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(wl, "oracle: one layer for one token per step"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "each step: one layer for one token (router + experts); expert "
+                                       "regeneration outside the timed region"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl, world, rank, dist):
+    import numpy as np
+    import torch
+
+    import int4_routed_expert_router_gb300 as smoe
+    import synthetic
+    import workload as W
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    pool = W.DevicePool(wl)
+    inp = W.LayerInputs(wl, wl.n_layers)
+    st = W.Stack(pool, inp, wl.T)
+    x0 = synthetic.activations(wl.seed, wl.T, wl.H, tag=4242)
+    st.xs[0].copy_(W.bf16_tensor(x0))
+    g = st.capture()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    if smoe.check(st.err) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- timed region: K replays of the whole step
+    sampler = ClockSampler()
+    sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    sampler.stop()
+    ms = t0.elapsed_time(t1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if smoe.check(st.err) != 0:
+        raise RuntimeError("device error word set during the timed region")
+    step_s = ms / 1e3 / args.steps
+    value = world * wl.T * wl.n_layers / step_s
+
+    # ---- the dominant kernel (moe_forward) bracketed by event nodes in a graph
+    kern_ms = None
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(wl.n_layers)]
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        gi = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gi, stream=s):
+            for l in range(wl.n_layers):
+                smoe.moe_route(pool.ctx, inp.Wr[l], inp.ws[l], st.xs[l], st.ids[l], st.w[l], st.gate[l], st.ws,
+                               logit_bias=inp.bias, stream=s)
+                evs[l][0].record(s)
+                smoe.moe_forward(pool.ctx, l, st.xs[l], st.ids[l], st.w[l], st.gate[l], pool.pool, pool.shared[l],
+                                 st.xs[l + 1], st.ws, st.err, residual=st.xs[l], stream=s)
+                evs[l][1].record(s)
+        reps = max(3, min(args.steps, 100))
+        tot = []
+        for _ in range(reps):
+            gi.replay()
+            torch.cuda.synchronize()
+            tot.extend(a.elapsed_time(b) for a, b in evs)
+        kern_ms = float(np.mean(tot))
+    except Exception as e:                               # noqa: BLE001
+        print("kernel timing unavailable: %r" % (e,), file=sys.stderr)
+
+    # ---- end to end: x from pinned host memory, the step, the result back
+    xh = torch.from_numpy(x0.view(np.int16)).view(torch.bfloat16).pin_memory()
+    oh = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        st.xs[0].copy_(xh, non_blocking=True)
+        g.replay()
+        oh.copy_(st.xs[wl.n_layers], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": round(world * wl.T * wl.n_layers * args.steps / (e2e_ms / 1e3), 1), "unit": UNIT,
+           "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2}
+
+    if rank != 0:
+        return
+    pk, pk_src = peaks()
+    blob = int(pool.layout.blob_bytes)
+    alg_bytes = (wl.k * wl.T + 1) * blob if wl.T == 1 else None
+    roof = None
+    if kern_ms and alg_bytes:
+        ach = alg_bytes / (kern_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": recorded_traffic(wl.name),
+                "kernel": "decode_kernel (moe_forward)", "bytes_per_launch": alg_bytes,
+                "us_per_launch": round(kern_ms * 1e3, 3),
+                "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk_src == "measured"
+                else "fallback 6.8 TB/s"}
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(wl, "CUDA graph of %d x (moe_route + moe_forward); us per layer %.3f"
+                                % (wl.n_layers, 1e3 * ms / args.steps / wl.n_layers)),
+            "roofline": roof, "e2e": e2e, "gpu_launches": 2 * wl.n_layers * args.steps,
+            "clocks": sampler.summary()}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    import synthetic
+    wl = synthetic.WORKLOADS[args.workload]
+    if args.layers:
+        wl = dataclasses.replace(wl, n_layers=args.layers)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+        dist = tdist
+    try:
+        if args.impl == "reference":
+            run_reference(args, wl, world, rank)
+        else:
+            run_ours(args, wl, world, rank, dist)
+    finally:
+        if dist:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -65,7 +65,7 @@ extern "C" {
 /* H: hidden size; E: routed experts per layer; k: experts per token;
  * I: routed expert intermediate size; I_shared: shared expert intermediate
  * size; group: quantisation group (must be 64); bits: 4.
- * Supported: H % 256 == 0, I % 64 == 0, 64 <= I <= 512, I_shared == I,
+ * Supported: H % 256 == 0, H <= 4096, I % 64 == 0, 64 <= I <= 512, I_shared == I,
  * 1 <= k <= 16, k <= E <= 1024. Others return SMOE_ENOTSUP. */
 typedef struct smoe_shape {
     int32_t H, E, k, I, I_shared, group, bits;
@@ -206,6 +206,11 @@ SMOE_API int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x, 
  * SMOE_OK, SMOE_EDEVICE if a kernel stored a code (copied to *code if
  * non-NULL), or SMOE_ECUDA. Not for use inside graph capture. */
 SMOE_API int smoe_check(int32_t *err_dev, int32_t *code, void *stream);
+
+/* Writes a one-line description of the kernel configuration the context
+ * chose (cluster size, ring stages, shared memory, co-resident clusters) into
+ * buf (NUL-terminated, at most len bytes). Errors: SMOE_EINVAL. */
+SMOE_API int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len);
 
 /* Short English text for a status code (static storage). */
 SMOE_API const char *smoe_status_string(int status);

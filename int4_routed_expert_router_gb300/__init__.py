@@ -19,7 +19,8 @@ OK, EINVAL, ERANGE, ENOMEM, ECUDA, EDEVICE, ENOTSUP = 0, -1, -2, -3, -4, -5, -6
 DEV_BAD_SLOT, DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2, 3
 HOST, DEVICE = 0, 1
 EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destroy", "set_slot_table",
-           "smoe_workspace_bytes", "moe_route", "moe_forward", "smoe_check", "smoe_status_string"]
+           "smoe_workspace_bytes", "moe_route", "moe_forward", "smoe_check", "smoe_ctx_describe",
+           "smoe_status_string"]
 
 
 class SmoeError(RuntimeError):
@@ -66,6 +67,7 @@ def lib():
         L.moe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, u64, vp]
         L.moe_forward.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, u64, vp, vp, vp, vp, u64, vp, vp]
         L.smoe_check.argtypes = [vp, C.POINTER(C.c_int32), vp]
+        L.smoe_ctx_describe.argtypes = [vp, C.c_char_p, i32]
         L.smoe_status_string.argtypes = [C.c_int]
         L.smoe_status_string.restype = C.c_char_p
         for name in EXPORTS:
@@ -161,6 +163,11 @@ class Context:
             self.close()
         except Exception:
             pass
+
+    def describe(self) -> str:
+        buf = C.create_string_buffer(1024)
+        _check(lib().smoe_ctx_describe(self.handle, buf, 1024), "smoe_ctx_describe")
+        return buf.value.decode()
 
     def workspace_bytes(self, T: int) -> int:
         return int(lib().smoe_workspace_bytes(self.handle, int(T)))

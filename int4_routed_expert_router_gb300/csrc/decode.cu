@@ -154,35 +154,51 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
             bulk_g2s_plain(x_s + t * xstride, p.x + size_t(t) * H, uint32_t(H * 2), xbar);
     }
 
-    // ---- routing bookkeeping: unique experts (ascending) and pair -> unique index
+    // ---- routing bookkeeping: unique experts and pair -> unique index (1..U).
+    // One token has distinct experts, so its route order serves directly;
+    // several tokens are deduplicated (ascending id) so a shared expert is
+    // streamed once. Either way the mapping only decides which cluster
+    // computes what; every pair still reads its own expert's output.
     const int npairs = T * k;
-    if (tid < npairs) ids_s[tid] = p.ids[tid];
-    __syncthreads();
-    if (tid < npairs) {
-        const int v = ids_s[tid];
-        const bool ok = v >= 0 && v < p.E;
-        if (!ok) set_error(p.err, SMOE_DEV_BAD_EXPERT);
-        bool first = ok;
-        for (int j = 0; j < tid; ++j)
-            if (ids_s[j] == v) first = false;
-        flags[2 + tid] = first ? 1 : 0;
+    if (T == 1) {
+        if (tid < k) {
+            const int v = p.ids[tid];
+            const bool ok = v >= 0 && v < p.E;
+            if (!ok) set_error(p.err, SMOE_DEV_BAD_EXPERT);
+            uniq[tid] = ok ? v : 0;
+            uidx[tid] = ok ? 1 + tid : 0;
+        }
+        if (tid == 0) flags[0] = k;
+        __syncthreads();
+    } else {
+        if (tid < npairs) ids_s[tid] = p.ids[tid];
+        __syncthreads();
+        if (tid < npairs) {
+            const int v = ids_s[tid];
+            const bool ok = v >= 0 && v < p.E;
+            if (!ok) set_error(p.err, SMOE_DEV_BAD_EXPERT);
+            bool first = ok;
+            for (int j = 0; j < tid; ++j)
+                if (ids_s[j] == v) first = false;
+            flags[2 + tid] = first ? 1 : 0;
+        }
+        __syncthreads();
+        if (tid < npairs) {
+            const int v = ids_s[tid];
+            int r = 0;
+            const bool ok = v >= 0 && v < p.E;
+            for (int j = 0; j < npairs; ++j)
+                if (flags[2 + j] && ids_s[j] < v) ++r;
+            uidx[tid] = ok ? 1 + r : 0;
+            if (flags[2 + tid]) uniq[r] = v;
+        }
+        if (tid == 0) {
+            int U = 0;
+            for (int j = 0; j < npairs; ++j) U += flags[2 + j];
+            flags[0] = U;
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    if (tid < npairs) {
-        const int v = ids_s[tid];
-        int r = 0;
-        bool ok = v >= 0 && v < p.E;
-        for (int j = 0; j < npairs; ++j)
-            if (flags[2 + j] && ids_s[j] < v) ++r;
-        uidx[tid] = ok ? 1 + r : 0;
-        if (flags[2 + tid]) uniq[r] = v;
-    }
-    if (tid == 0) {
-        int U = 0;
-        for (int j = 0; j < npairs; ++j) U += flags[2 + j];
-        flags[0] = U;
-    }
-    __syncthreads();
     const int U_total = flags[0] + 1;
 
     int it = 0;
@@ -246,13 +262,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
                         }
                         const uint32_t xl[4] = {xa.x, xa.y, xa.z, xa.w};
                         const uint32_t xh4[4] = {xb.x, xb.y, xb.z, xb.w};
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const uint32_t a[4] = {nib_pair(A.x, m), nib_pair(A.z, m), nib_pair(A.y, m),
-                                                   nib_pair(A.w, m)};
-                            mma_bf16(acc, a, xl[m], xh4[m]);
+                        for (int m = 0; m < 4; m += 2) {   // two independent chains of two
+                            const uint32_t a0[4] = {nib_pair(A.x, m), nib_pair(A.z, m), nib_pair(A.y, m),
+                                                    nib_pair(A.w, m)};
+                            const uint32_t a1[4] = {nib_pair(A.x, m + 1), nib_pair(A.z, m + 1),
+                                                    nib_pair(A.y, m + 1), nib_pair(A.w, m + 1)};
+                            mma_bf16(acc, a0, xl[m], xh4[m]);
+                            mma_bf16(acc2, a1, xl[m + 1], xh4[m + 1]);
                         }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
                         const float2 X = *reinterpret_cast<const float2 *>(xsum + grp * kDecodeMaxT + 2 * t4);
                         const float sg = half_bits_to_f32(uint16_t(SB.x & 0xffff));
                         const float bg = half_bits_to_f32(uint16_t(SB.x >> 16));
@@ -324,38 +345,57 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
             for (int rbB = warp; rbB < nrbB; rbB += kDecodeConsumerWarps) {
                 float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
                 if (run && !bad) {
-                    for (int kb = 0; kb < ngI; ++kb) {
-                        const uint8_t *atom = wB + (rbB * ngI + kb) * kAtomBytes;
-                        const uint4 A = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
-                        const uint2 SB = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
-                        const int col = kb * kGroup + 16 * t4;
-                        uint4 ha = make_uint4(0, 0, 0, 0), hb = ha, la = ha, lb = ha;
-                        if (g < T) {
-                            ha = *reinterpret_cast<const uint4 *>(hhi + g * (I + 8) + col);
-                            hb = *reinterpret_cast<const uint4 *>(hhi + g * (I + 8) + col + 8);
-                            la = *reinterpret_cast<const uint4 *>(hlo + g * (I + 8) + col);
-                            lb = *reinterpret_cast<const uint4 *>(hlo + g * (I + 8) + col + 8);
-                        }
-                        const uint32_t ha_[4] = {ha.x, ha.y, ha.z, ha.w}, hb_[4] = {hb.x, hb.y, hb.z, hb.w};
-                        const uint32_t la_[4] = {la.x, la.y, la.z, la.w}, lb_[4] = {lb.x, lb.y, lb.z, lb.w};
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    // groups two at a time; per group the hi and lo halves of h
+                    // accumulate in separate chains (four independent chains)
+                    for (int kb0 = 0; kb0 < ngI; kb0 += 2) {
+                        float acc[2][2][4];
+                        uint4 A[2];
+                        uint2 SB[2];
 #pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const uint32_t a[4] = {nib_pair(A.x, m), nib_pair(A.z, m), nib_pair(A.y, m),
-                                                   nib_pair(A.w, m)};
-                            mma_bf16(acc, a, ha_[m], hb_[m]);
-                            mma_bf16(acc, a, la_[m], lb_[m]);
+                        for (int q = 0; q < 2; ++q) {
+                            const int kb = kb0 + q < ngI ? kb0 + q : kb0;
+                            const uint8_t *atom = wB + (rbB * ngI + kb) * kAtomBytes;
+                            A[q] = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
+                            SB[q] = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) acc[q][0][i] = acc[q][1][i] = 0.f;
                         }
-                        const float2 X = *reinterpret_cast<const float2 *>(xh + kb * kDecodeMaxT + 2 * t4);
-                        const float s0 = half_bits_to_f32(uint16_t(SB.x & 0xffff));
-                        const float b0 = half_bits_to_f32(uint16_t(SB.x >> 16));
-                        const float s1 = half_bits_to_f32(uint16_t(SB.y & 0xffff));
-                        const float b1 = half_bits_to_f32(uint16_t(SB.y >> 16));
-                        const float bp0 = fmaf(-128.f, s0, b0), bp1 = fmaf(-128.f, s1, b1);
-                        y0 += fmaf(s0, acc[0], bp0 * X.x);
-                        y1 += fmaf(s0, acc[1], bp0 * X.y);
-                        y2 += fmaf(s1, acc[2], bp1 * X.x);
-                        y3 += fmaf(s1, acc[3], bp1 * X.y);
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const int kb = kb0 + q < ngI ? kb0 + q : kb0;
+                            const int col = kb * kGroup + 16 * t4;
+                            uint4 ha = make_uint4(0, 0, 0, 0), hb = ha, la = ha, lb = ha;
+                            if (g < T) {
+                                ha = *reinterpret_cast<const uint4 *>(hhi + g * (I + 8) + col);
+                                hb = *reinterpret_cast<const uint4 *>(hhi + g * (I + 8) + col + 8);
+                                la = *reinterpret_cast<const uint4 *>(hlo + g * (I + 8) + col);
+                                lb = *reinterpret_cast<const uint4 *>(hlo + g * (I + 8) + col + 8);
+                            }
+                            const uint32_t ha_[4] = {ha.x, ha.y, ha.z, ha.w}, hb_[4] = {hb.x, hb.y, hb.z, hb.w};
+                            const uint32_t la_[4] = {la.x, la.y, la.z, la.w}, lb_[4] = {lb.x, lb.y, lb.z, lb.w};
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const uint32_t a[4] = {nib_pair(A[q].x, m), nib_pair(A[q].z, m),
+                                                       nib_pair(A[q].y, m), nib_pair(A[q].w, m)};
+                                mma_bf16(acc[q][0], a, ha_[m], hb_[m]);
+                                mma_bf16(acc[q][1], a, la_[m], lb_[m]);
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            if (kb0 + q >= ngI) break;
+                            const int kb = kb0 + q;
+                            const float2 X = *reinterpret_cast<const float2 *>(xh + kb * kDecodeMaxT + 2 * t4);
+                            const float s0 = half_bits_to_f32(uint16_t(SB[q].x & 0xffff));
+                            const float b0 = half_bits_to_f32(uint16_t(SB[q].x >> 16));
+                            const float s1 = half_bits_to_f32(uint16_t(SB[q].y & 0xffff));
+                            const float b1 = half_bits_to_f32(uint16_t(SB[q].y >> 16));
+                            const float bp0 = fmaf(-128.f, s0, b0), bp1 = fmaf(-128.f, s1, b1);
+                            y0 += fmaf(s0, acc[q][0][0] + acc[q][1][0], bp0 * X.x);
+                            y1 += fmaf(s0, acc[q][0][1] + acc[q][1][1], bp0 * X.y);
+                            y2 += fmaf(s1, acc[q][0][2] + acc[q][1][2], bp1 * X.x);
+                            y3 += fmaf(s1, acc[q][0][3] + acc[q][1][3], bp1 * X.y);
+                        }
                     }
                 }
                 const int row = int(rank) * rowsB + rbB * 16 + g;
@@ -377,13 +417,27 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
                 for (int i = tid; i < T * rowsB; i += kDecodeConsumerWarps * 32) {
                     const int tok = i / rowsB;
                     const int row = int(rank) * rowsB + i % rowsB;
-                    float acc = 0.f;
-                    for (int j = 0; j < k; ++j) {
-                        const int uu = uidx[tok * k + j];
-                        if (uu > 0)
-                            acc = fmaf(p.w[tok * k + j], __ldcg(p.ypair + (size_t(uu) * T + tok) * H + row), acc);
+                    // all loads first (k <= 16), then the sum in route order
+                    float yv[16], wv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        yv[j] = 0.f;
+                        wv[j] = 0.f;
+                        if (j < k) {
+                            const int uu = uidx[tok * k + j];
+                            if (uu > 0) {
+                                yv[j] = __ldcg(p.ypair + (size_t(uu) * T + tok) * H + row);
+                                wv[j] = p.w[tok * k + j];
+                            }
+                        }
                     }
-                    acc = fmaf(p.gate[tok], __ldcg(p.ypair + size_t(tok) * H + row), acc);
+                    const float ys = __ldcg(p.ypair + size_t(tok) * H + row);
+                    const float gt = p.gate[tok];
+                    float acc = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < k) acc = fmaf(wv[j], yv[j], acc);
+                    acc = fmaf(gt, ys, acc);
                     if (p.residual) acc += __uint_as_float(uint32_t(p.residual[size_t(tok) * H + row]) << 16);
                     p.out[size_t(tok) * H + row] = f32_to_bf16_bits(acc);
                 }

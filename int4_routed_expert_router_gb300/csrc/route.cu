@@ -12,8 +12,9 @@
 // rows (router rows, plus the shared-gate vector as row E) and the tokens are
 // bulk-copied into shared memory, one warp per row forms the fp32 dot products.
 // With fused_topk the last CTA to finish (arrival ticket) then runs the top-k
-// for every token, so a decode step costs one launch; otherwise topk_kernel
-// runs one warp per token.
+// for every token with all its warps (two levels of warp max-reductions over
+// order-preserving integer keys), so a decode step costs one launch;
+// otherwise topk_kernel runs one warp per token.
 #include "smoe_dev.cuh"
 #include "smoe_internal.h"
 
@@ -21,7 +22,6 @@ namespace smoe {
 
 constexpr int kRouteRows = 8;
 constexpr int kRouteToks = 8;
-constexpr int kTopkMaxPerLane = 32;   // E <= 1024
 
 __device__ __forceinline__ void bulk_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
@@ -29,55 +29,129 @@ __device__ __forceinline__ void bulk_plain(void *dst, const void *src, uint32_t 
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-// Top-k of one token by one warp: logits row z[0..E) (+bias), gate logit zg.
-__device__ void topk_warp(const float *z, const float *bias, float zg, int E, int k, int32_t *ids_out,
-                          float *w_out, float *gate_out, int lane)
+// Order-preserving map float -> uint32 (larger float, larger key); key 0 is
+// reserved for "taken / empty" (no finite or infinite float maps to it).
+__device__ __forceinline__ uint32_t fkey(float f)
 {
-    float v[kTopkMaxPerLane];
-    const int per = (E + 31) / 32;
-#pragma unroll
-    for (int j = 0; j < kTopkMaxPerLane; ++j) {
-        const int e = lane + 32 * j;
-        float val = -INFINITY;
-        if (j < per && e < E) val = __ldcg(z + e) + (bias ? bias[e] : 0.f);
-        v[j] = val;
-    }
-    uint32_t taken = 0;
-    float zsel[16];
-    int isel[16];
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float fkey_inv(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// One warp picks the k largest keys among its lanes' PER values, in
+// descending order, ties to the lower id. Each round: warp max of the lanes'
+// current bests, then the lowest id holding that key; the winner removes it.
+template <int PER>
+__device__ void warp_topk(uint32_t (&key)[PER], int32_t (&id)[PER], int k, uint32_t *okey, int32_t *oid,
+                          int lane)
+{
     for (int s = 0; s < k; ++s) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+        uint32_t bk = 0;
+        int32_t bi = 0x7fffffff;
 #pragma unroll
-        for (int j = 0; j < kTopkMaxPerLane; ++j) {
-            const int e = lane + 32 * j;
-            if (j < per && e < E && !((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < bi))) {
-                bv = v[j];
-                bi = e;
+        for (int j = 0; j < PER; ++j)
+            if (key[j] > bk || (key[j] == bk && key[j] != 0u && id[j] < bi)) {
+                bk = key[j];
+                bi = id[j];
             }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const int32_t mi = int32_t(__reduce_min_sync(0xffffffffu, uint32_t(bk == mk ? bi : 0x7fffffff)));
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+            if (id[j] == mi && key[j] == mk) key[j] = 0u;
+        if (lane == 0) {
+            okey[s] = mk;
+            oid[s] = mk ? mi : -1;
         }
-        for (int o = 16; o; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        zsel[s] = bv;
-        isel[s] = bi;
     }
-    if (lane == 0) {
-        const float zmax = zsel[0];
-        float den = 0.f;
-        float ex[16];
-        for (int s = 0; s < k; ++s) {
-            ex[s] = expf(zsel[s] - zmax);
-            den += ex[s];
+}
+
+// Level 1 for one token slice: values z[e] (+bias) for e in [e0, e1).
+template <int PER>
+__device__ void slice_topk(const float *z, const float *bias, int e0, int e1, int k, uint32_t *okey, int32_t *oid,
+                           int lane)
+{
+    uint32_t key[PER];
+    int32_t id[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int e = e0 + lane + 32 * j;
+        key[j] = 0u;
+        id[j] = 0x7fffffff;
+        if (e < e1) {
+            key[j] = fkey(__ldcg(z + e) + (bias ? bias[e] : 0.f));
+            id[j] = e;
         }
-        for (int s = 0; s < k; ++s) {
-            ids_out[s] = isel[s];
-            w_out[s] = ex[s] / den;
+    }
+    warp_topk<PER>(key, id, k, okey, oid, lane);
+}
+
+__device__ void slice_topk_any(int per, const float *z, const float *bias, int e0, int e1, int k, uint32_t *ok,
+                               int32_t *oi, int lane)
+{
+    if (per <= 1) slice_topk<1>(z, bias, e0, e1, k, ok, oi, lane);
+    else if (per <= 2) slice_topk<2>(z, bias, e0, e1, k, ok, oi, lane);
+    else if (per <= 4) slice_topk<4>(z, bias, e0, e1, k, ok, oi, lane);
+    else if (per <= 8) slice_topk<8>(z, bias, e0, e1, k, ok, oi, lane);
+    else if (per <= 16) slice_topk<16>(z, bias, e0, e1, k, ok, oi, lane);
+    else slice_topk<32>(z, bias, e0, e1, k, ok, oi, lane);
+}
+
+// Final weights of one token from its k chosen keys (descending).
+__device__ void write_choice(const RouteParams &p, int t, const uint32_t *fk, const int32_t *fi)
+{
+    const float zmax = fkey_inv(fk[0]);
+    float ex[16], den = 0.f;
+    for (int s = 0; s < p.k; ++s) {
+        ex[s] = expf(fkey_inv(fk[s]) - zmax);
+        den += ex[s];
+    }
+    for (int s = 0; s < p.k; ++s) {
+        p.ids[size_t(t) * p.k + s] = fi[s];
+        p.w[size_t(t) * p.k + s] = ex[s] / den;
+    }
+    p.gate[t] = 1.0f / (1.0f + expf(-__ldcg(p.logits + size_t(t) * (p.E + 1) + p.E)));
+}
+
+// Top-k of T <= 8 tokens by the 8 warps of a CTA (the CTA that finishes the
+// logits last). Each token gets 8/T' warps (T' = T rounded up to a power of
+// two); each of them takes a slice of the experts (level 1), then one warp
+// merges the slices' candidates (level 2). ckey/cid: 2 * 8 * 16 entries.
+__device__ void block_topk(const RouteParams &p, uint32_t *ckey, int32_t *cid)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = p.T, E = p.E, k = p.k;
+    int tp = 1;
+    while (tp < T) tp <<= 1;
+    const int wpt = 8 / tp;                     // warps per token
+    const int t = warp / wpt, sl = warp % wpt;
+    if (t < T) {
+        const int span = (E + wpt - 1) / wpt;
+        const int e0 = sl * span, e1 = min(E, e0 + span);
+        slice_topk_any((span + 31) / 32, p.logits + size_t(t) * (E + 1), p.bias, e0, e1, k, ckey + warp * 16,
+                       cid + warp * 16, lane);
+    }
+    __syncthreads();
+    if (t < T && sl == 0) {
+        uint32_t key[4];
+        int32_t id[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {       // wpt * k <= 8 * 16 = 128 candidates, 4 per lane
+            const int c = lane + 32 * j;
+            const int w = warp + c / k, r = c % k;
+            const bool ok = c < wpt * k;
+            key[j] = ok ? ckey[w * 16 + r] : 0u;
+            id[j] = ok && key[j] ? cid[w * 16 + r] : 0x7fffffff;
         }
-        *gate_out = 1.0f / (1.0f + expf(-zg));
+        uint32_t *fk = ckey + 8 * 16 + warp * 16;
+        int32_t *fi = cid + 8 * 16 + warp * 16;
+        warp_topk<4>(key, id, k, fk, fi, lane);
+        __syncwarp();
+        if (lane == 0) write_choice(p, t, fk, fi);
     }
 }
 
@@ -149,24 +223,26 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const RouteParams p)
     __syncthreads();
     if (!last) return;
     __threadfence();
-    for (int t = warp; t < T; t += 8) {
-        const float *z = p.logits + size_t(t) * (E + 1);
-        topk_warp(z, p.bias, __ldcg(z + E), E, p.k, p.ids + size_t(t) * p.k, p.w + size_t(t) * p.k,
-                  p.gate + t, lane);
-    }
+    __shared__ uint32_t ckey[2 * 8 * 16];
+    __shared__ int32_t cid[2 * 8 * 16];
+    block_topk(p, ckey, cid);
     if (tid == 0) atomicExch(p.counter, 0u);
 }
 
+// One warp per token (large T): a single level over all E experts.
 __global__ void __launch_bounds__(256) topk_kernel(const RouteParams p)
 {
+    __shared__ uint32_t ckey[8 * 16];
+    __shared__ int32_t cid[8 * 16];
     pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= p.T) return;
-    const float *z = p.logits + size_t(t) * (p.E + 1);
-    topk_warp(z, p.bias, __ldcg(z + p.E), p.E, p.k, p.ids + size_t(t) * p.k, p.w + size_t(t) * p.k,
-              p.gate + t, lane);
+    slice_topk_any((p.E + 31) / 32, p.logits + size_t(t) * (p.E + 1), p.bias, 0, p.E, p.k, ckey + warp * 16,
+                   cid + warp * 16, lane);
+    __syncwarp();
+    if (lane == 0) write_choice(p, t, ckey + warp * 16, cid + warp * 16);
 }
 
 cudaError_t route_config()

@@ -1,6 +1,7 @@
 // smoe_api.cu -- the C ABI declared in include/smoe.h: blob layout, packing of
 // MLX triples into fixed-stride blobs, context and slot table, workspace
 // carving, and dispatch of the router / expert kernels.
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -343,6 +344,16 @@ extern "C" int smoe_check(int32_t *err_dev, int32_t *code, void *stream)
     if (e != cudaSuccess) return SMOE_ECUDA;
     if (code) *code = h;
     return h ? SMOE_EDEVICE : SMOE_OK;
+}
+
+extern "C" int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len)
+{
+    if (!ctx || !buf || len <= 0) return SMOE_EINVAL;
+    int o = std::snprintf(buf, size_t(len), "sms=%d decode: cluster=%d", ctx->num_sms, ctx->cs);
+    for (int T = 1; T <= kDecodeMaxT && o < len; ++T)
+        o += std::snprintf(buf + o, size_t(len - o), " T%d:{stages=%d smem=%d clusters=%d}", T,
+                           ctx->decode[T].nst, ctx->decode[T].smem, ctx->decode[T].max_clusters);
+    return SMOE_OK;
 }
 
 extern "C" const char *smoe_status_string(int status)
