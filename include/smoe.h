@@ -65,7 +65,7 @@ extern "C" {
 /* H: hidden size; E: routed experts per layer; k: experts per token;
  * I: routed expert intermediate size; I_shared: shared expert intermediate
  * size; group: quantisation group (must be 64); bits: 4.
- * Supported: H % 256 == 0, H <= 4096, I % 64 == 0, 64 <= I <= 512, I_shared == I,
+ * Supported: H % 256 == 0, H <= 2048, I % 64 == 0, 64 <= I <= 512, I_shared == I,
  * 1 <= k <= 16, k <= E <= 1024. Others return SMOE_ENOTSUP. */
 typedef struct smoe_shape {
     int32_t H, E, k, I, I_shared, group, bits;

@@ -19,8 +19,8 @@ OK, EINVAL, ERANGE, ENOMEM, ECUDA, EDEVICE, ENOTSUP = 0, -1, -2, -3, -4, -5, -6
 DEV_BAD_SLOT, DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2, 3
 HOST, DEVICE = 0, 1
 EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destroy", "set_slot_table",
-           "smoe_workspace_bytes", "moe_route", "moe_forward", "smoe_check", "smoe_ctx_describe",
-           "smoe_status_string"]
+           "smoe_workspace_bytes", "moe_route", "moe_forward", "smoe_check",
+           "smoe_ctx_describe", "smoe_status_string"]
 
 
 class SmoeError(RuntimeError):

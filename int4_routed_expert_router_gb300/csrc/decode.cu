@@ -1,8 +1,8 @@
 // decode.cu -- fused expert kernel for small token counts (T <= 8).
 //
 // One thread-block cluster of cs = I/32 CTAs works on one expert at a time
-// (shared expert first, then the routed experts the tokens selected, in
-// ascending id); clusters loop over experts. Inside a cluster:
+// (shared expert first, then the routed experts the tokens selected); the
+// clusters loop over experts. Inside a cluster:
 //   phase A: CTA r computes gate/up for intermediates [32r, 32r+32) over all
 //            H inputs and applies SwiGLU -> h slice (fp32, in its shared memory);
 //   exchange: every CTA reads the cs slices through distributed shared memory
@@ -11,12 +11,16 @@
 //   combine: the expert outputs go to a workspace buffer; per row chunk an
 //            arrival ticket picks the last CTA to arrive, which sums, per token,
 //            w_j * y_j in route order plus gate * y_shared and writes bf16.
-// The weights stream once from HBM with 1-D bulk copies into a ring of shared
-// memory stages; each 576-byte atom is the A-operand fragment of 16x8x16 bf16
-// tensor-core steps, dequantised in registers: a nibble pair becomes
-// bf16x2 (128+q) with one shift and one LOP3, the MMA sums (128+q) x over a
-// 64-column group, and the group epilogue applies s and b:
+// Weights stream once from HBM with 1-D bulk copies into a ring of shared
+// memory slots, one slot per 256-column chunk of phase A, all requested at
+// once; phase B's weights then fill the first slots as phase A frees them.
+// Each 576-byte atom is the A-operand fragment of 16x8x16 bf16 tensor-core
+// steps, dequantised in registers: a nibble pair becomes bf16x2 (128 + q) with
+// one shift and one LOP3, the MMA sums (128 + q) x over a 64-column group, and
+// the group epilogue applies s and b:
 //   sum_c (s q_c + b) x_c = s * sum_c (128 + q_c) x_c + (b - 128 s) * sum_c x_c.
+// NCW consumer warps per CTA: 16 when the clusters fit one CTA per SM, 8 when
+// two CTAs must share an SM.
 // Pages: fixed-stride expert blobs and MLX int4 group quantisation (xix.ai
 // article, paragraphs on how it works and on the Metal kernels); combining
 // the shared expert (agentlenshq article, how expert streaming works).
@@ -26,26 +30,37 @@
 namespace smoe {
 
 struct DecodeSmem {
-    int x_s, xsum, wB, ring, hslice, hhi, hlo, xh, red, ints, bars, total;
+    int x_s, xsum, ring, hslice, hhi, hlo, xh, red, ints, bars, total, nst;
 };
 
 __host__ __device__ inline int align128(int v) { return (v + 127) & ~127; }
 
-__host__ __device__ inline DecodeSmem decode_smem(int T, int H, int I, int cs, int nst)
+// float4 entries of the cross-warp reduction buffer (per lane)
+__host__ __device__ inline int red_entries(int ncw, int H, int cs)
+{
+    const int a = (ncw / 4 - 1) * kRowBlocksA;            // phase A partials
+    const int nrbB = H / cs / 16;
+    const int splitB = ncw > nrbB ? ncw / nrbB : 1;
+    const int b = (splitB - 1) * nrbB;                     // phase B partials
+    const int m = a > b ? a : b;
+    return m > 1 ? m : 1;
+}
+
+__host__ __device__ inline DecodeSmem decode_smem(int T, int H, int I, int cs, int ncw)
 {
     DecodeSmem L;
+    L.nst = H / kChunkCols;
     int o = 0;
     L.x_s = o;    o = align128(o + T * (2 * H + 16));
     L.xsum = o;   o = align128(o + (H / kGroup) * kDecodeMaxT * 4);
-    L.wB = o;     o = align128(o + (H / cs / 16) * (I / kGroup) * kAtomBytes);
-    L.ring = o;   o = align128(o + nst * kChunkBytes);
+    L.ring = o;   o = align128(o + L.nst * kChunkBytes);
     L.hslice = o; o = align128(o + kDecodeMaxT * kSlice * 4);
     L.hhi = o;    o = align128(o + T * (I + 8) * 2);
     L.hlo = o;    o = align128(o + T * (I + 8) * 2);
     L.xh = o;     o = align128(o + (I / kGroup) * kDecodeMaxT * 4);
-    L.red = o;    o = align128(o + kRowBlocksA * 32 * 16);
+    L.red = o;    o = align128(o + red_entries(ncw, H, cs) * 32 * 16);
     L.ints = o;   o = align128(o + 640 * 4);
-    L.bars = o;   o = align128(o + (2 * nst + 2) * 8);
+    L.bars = o;   o = align128(o + (2 * L.nst + 1) * 8);
     L.total = o;
     return L;
 }
@@ -58,93 +73,157 @@ __device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint3
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-__global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeParams p)
+// s (low half) and b (high half) of one fp16 pair as floats: s and b - 128 s.
+__device__ __forceinline__ void scale_bias(uint32_t sb, float &s, float &bp)
 {
+    s = half_bits_to_f32(uint16_t(sb & 0xffff));
+    bp = fmaf(-128.f, s, half_bits_to_f32(uint16_t(sb >> 16)));
+}
+
+// Phase B for one 16-row block over groups [kbeg, kend) of h (bf16 hi + lo).
+// y = rows (g, g+8) x tokens (2 t4, 2 t4 + 1). Groups two at a time; per group
+// the hi and lo halves of h accumulate in separate chains.
+__device__ __forceinline__ void down_rows(const uint8_t *wB, int rbB, int ngI, int kbeg, int kend,
+                                          const uint16_t *hhi, const uint16_t *hlo, const float *xh, int I,
+                                          int T, int lane, float (&y)[4])
+{
+    const int g = lane >> 2, t4 = lane & 3;
+    for (int kb0 = kbeg; kb0 < kend; kb0 += 2) {
+        float acc[2][2][4];
+        uint4 A[2];
+        uint2 SB[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int kb = kb0 + q < kend ? kb0 + q : kb0;
+            const uint8_t *atom = wB + (rbB * ngI + kb) * kAtomBytes;
+            A[q] = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
+            SB[q] = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[q][0][i] = acc[q][1][i] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int kb = kb0 + q < kend ? kb0 + q : kb0;
+            const int col = kb * kGroup + 16 * t4;
+            uint4 ha = make_uint4(0, 0, 0, 0), hb = ha, la = ha, lb = ha;
+            if (g < T) {
+                ha = *reinterpret_cast<const uint4 *>(hhi + g * (I + 8) + col);
+                hb = *reinterpret_cast<const uint4 *>(hhi + g * (I + 8) + col + 8);
+                la = *reinterpret_cast<const uint4 *>(hlo + g * (I + 8) + col);
+                lb = *reinterpret_cast<const uint4 *>(hlo + g * (I + 8) + col + 8);
+            }
+            const uint32_t ha_[4] = {ha.x, ha.y, ha.z, ha.w}, hb_[4] = {hb.x, hb.y, hb.z, hb.w};
+            const uint32_t la_[4] = {la.x, la.y, la.z, la.w}, lb_[4] = {lb.x, lb.y, lb.z, lb.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t a[4] = {nib_pair(A[q].x, m), nib_pair(A[q].z, m), nib_pair(A[q].y, m),
+                                       nib_pair(A[q].w, m)};
+                mma_bf16(acc[q][0], a, ha_[m], hb_[m]);
+                mma_bf16(acc[q][1], a, la_[m], lb_[m]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            if (kb0 + q >= kend) break;
+            const int kb = kb0 + q;
+            const float2 X = *reinterpret_cast<const float2 *>(xh + kb * kDecodeMaxT + 2 * t4);
+            float s0, bp0, s1, bp1;
+            scale_bias(SB[q].x, s0, bp0);
+            scale_bias(SB[q].y, s1, bp1);
+            y[0] += fmaf(s0, acc[q][0][0] + acc[q][1][0], bp0 * X.x);
+            y[1] += fmaf(s0, acc[q][0][1] + acc[q][1][1], bp0 * X.y);
+            y[2] += fmaf(s1, acc[q][0][2] + acc[q][1][2], bp1 * X.x);
+            y[3] += fmaf(s1, acc[q][0][3] + acc[q][1][3], bp1 * X.y);
+        }
+    }
+}
+
+template <int NCW>
+__global__ void __launch_bounds__((NCW + 1) * 32, 16 / NCW) decode_kernel(const DecodeParams p)
+{
+    constexpr int kCons = NCW * 32;                 // consumer threads (named barrier 1)
+    constexpr int kGQ = NCW / 4;                    // warps sharing one gate/up row block
+    constexpr int kGPW = (kChunkCols / kGroup) / kGQ;   // groups per chunk per warp
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int T = p.T, H = p.H, I = p.I, k = p.k, nst = p.nst;
-    const DecodeSmem L = decode_smem(T, H, I, p.cs, nst);
+    const int T = p.T, H = p.H, I = p.I, k = p.k;
+    const DecodeSmem L = decode_smem(T, H, I, p.cs, NCW);
+    const int nst = L.nst;
     uint16_t *x_s = reinterpret_cast<uint16_t *>(smem + L.x_s);
     float *xsum = reinterpret_cast<float *>(smem + L.xsum);      // [H/64][8]
-    uint8_t *wB = smem + L.wB;
     uint8_t *ring = smem + L.ring;
     float *hslice = reinterpret_cast<float *>(smem + L.hslice);  // [8][32]
     uint16_t *hhi = reinterpret_cast<uint16_t *>(smem + L.hhi);  // [T][I+8]
     uint16_t *hlo = reinterpret_cast<uint16_t *>(smem + L.hlo);
     float *xh = reinterpret_cast<float *>(smem + L.xh);          // [I/64][8]
-    float4 *red = reinterpret_cast<float4 *>(smem + L.red);      // [4][32]
+    float4 *red = reinterpret_cast<float4 *>(smem + L.red);      // [entries][32]
     int *ints = reinterpret_cast<int *>(smem + L.ints);
     int *ids_s = ints;            // [128]
     int *uidx = ints + 128;       // [128] unique index (1..U) of each pair, 0 if invalid
-    int *uniq = ints + 256;       // [<=128] unique expert ids, ascending
+    int *uniq = ints + 256;       // [<=128] unique expert ids
     int *flags = ints + 384;      // [0] U, [1] is-last, [2..130) first-occurrence marks
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + nst;
     uint64_t *xbar = empty + nst;
-    uint64_t *wbar = xbar + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const uint32_t rank = cluster_ctarank();
     const uint32_t clus = cluster_id_x(), nclus = ncluster_x();
-    const int nchunks = H / kChunkCols;
     const int ngH = H / kGroup, ngI = I / kGroup;
     const int rowsB = H / p.cs;
     const int nrbB = rowsB / 16;
+    const int splitB = NCW > nrbB ? NCW / nrbB : 1;      // NCW, nrbB powers of two
     const uint32_t wB_bytes = uint32_t(nrbB * ngI * kAtomBytes);
+    const int nB = int((wB_bytes + kChunkBytes - 1) / kChunkBytes);   // phase B slots (<= nst)
     const uint64_t down_off = uint64_t(I / 8) * ngH * kAtomBytes;
-    const bool producer = warp == kDecodeConsumerWarps;
+    const bool producer = warp == NCW;
     const int xstride = H + 8;
 
     if (tid == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kDecodeConsumerWarps);
+            mbar_init(&empty[s], NCW);
         }
         mbar_init(xbar, 1);
-        mbar_init(wbar, 1);
         fence_mbar_init();
     }
     __syncthreads();
 
     const uint64_t pol_stream = policy_evict_first();
-    uint32_t qnext = 0;      // producer: chunks issued so far (ring sequence)
-    uint32_t qdone = 0;      // consumers: chunks consumed so far
-    uint32_t nw = 0;         // phase-B weight loads consumed
+    // Slot s is filled 1 + (s < nB) times per valid expert, so before the
+    // expert with valid-index vit it has been filled vit * (1 + (s < nB)) times.
+    auto fills = [&](int vit, int s) { return uint32_t(vit * (1 + (s < nB ? 1 : 0))); };
     bool x_ready = false;    // uniform across the CTA: x rows were waited for
     bool bad = false;        // this thread's bounded wait gave up: skip later waits
                              // (never used to skip a barrier, so all threads still
                              // reach every barrier and the kernel finishes)
-    int pre_chunks = 0;
-    bool pre_w = false;
 
-    auto issue_chunk = [&](const uint8_t *blob, int c) {
-        const uint32_t slot = qnext % nst;
-        if (qnext >= (uint32_t)nst && !mbar_wait(&empty[slot], ((qnext / nst) - 1) & 1, p.err))
-            return false;
-        mbar_arrive_expect_tx(&full[slot], kChunkBytes);
-        uint8_t *dst = ring + slot * kChunkBytes;
-        const int per_rb = (kChunkCols / kGroup) * kAtomBytes;
-        for (int rb = 0; rb < kRowBlocksA; ++rb) {
-            const uint64_t atom = uint64_t(rank * kRowBlocksA + rb) * ngH + uint64_t(c) * (kChunkCols / kGroup);
-            bulk_g2s(dst + rb * per_rb, blob + atom * kAtomBytes, per_rb, &full[slot], pol_stream);
+    // producer: fill f of slot s (waits for the consumers to free the previous fill)
+    auto fill_slot = [&](int s, uint32_t f, const uint8_t *blob, bool phaseA) {
+        if (f >= 1 && !mbar_wait(&empty[s], (f - 1) & 1, p.err)) return false;
+        uint8_t *dst = ring + s * kChunkBytes;
+        if (phaseA) {
+            mbar_arrive_expect_tx(&full[s], kChunkBytes);
+            const int per_rb = (kChunkCols / kGroup) * kAtomBytes;
+            for (int rb = 0; rb < kRowBlocksA; ++rb) {
+                const uint64_t atom = uint64_t(rank * kRowBlocksA + rb) * ngH + uint64_t(s) * (kChunkCols / kGroup);
+                bulk_g2s(dst + rb * per_rb, blob + atom * kAtomBytes, per_rb, &full[s], pol_stream);
+            }
+        } else {
+            const uint32_t off = uint32_t(s) * kChunkBytes;
+            const uint32_t bytes = wB_bytes - off < uint32_t(kChunkBytes) ? wB_bytes - off : uint32_t(kChunkBytes);
+            mbar_arrive_expect_tx(&full[s], bytes);
+            bulk_g2s(dst, blob + down_off + uint64_t(rank) * wB_bytes + off, bytes, &full[s], pol_stream);
         }
-        ++qnext;
         return true;
-    };
-    auto issue_w = [&](const uint8_t *blob) {
-        mbar_arrive_expect_tx(wbar, wB_bytes);
-        bulk_g2s(wB, blob + down_off + uint64_t(rank) * wB_bytes, wB_bytes, wbar, pol_stream);
     };
 
     // The shared expert (u = 0) needs no routing, so cluster 0 starts streaming
-    // it before waiting for the kernel that produced the routing.
+    // its phase-A weights before waiting for the kernel that produced the routing.
+    bool pre = false;
     if (producer && lane == 0 && clus == 0) {
-        issue_w(p.shared_blob);
-        pre_w = true;
-        for (int c = 0; c < nchunks && c < nst; ++c) {
-            issue_chunk(p.shared_blob, c);
-            ++pre_chunks;
-        }
+        for (int s = 0; s < nst; ++s) fill_slot(s, 0, p.shared_blob, true);
+        pre = true;
     }
     pdl_wait();
     pdl_trigger();
@@ -201,7 +280,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     }
     const int U_total = flags[0] + 1;
 
-    int it = 0;
+    int it = 0, vit = 0;
     for (int u = int(clus); u < U_total; u += int(nclus), ++it) {
         if (it > 0) cluster_wait();   // peers are done reading our previous h slice
 
@@ -222,34 +301,35 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 
         if (producer) {
             if (lane == 0 && valid && !bad) {
-                if (!(it == 0 && pre_w)) issue_w(blob);
-                for (int c = (it == 0 ? pre_chunks : 0); c < nchunks; ++c)
-                    if (!issue_chunk(blob, c)) { bad = true; break; }
+                if (!(it == 0 && pre))
+                    for (int s = 0; s < nst && !bad; ++s)
+                        if (!fill_slot(s, fills(vit, s), blob, true)) bad = true;
+                for (int s = 0; s < nB && !bad; ++s)           // phase B into freed slots
+                    if (!fill_slot(s, fills(vit, s) + 1, blob, false)) bad = true;
             }
             __syncwarp();
         } else {
-            const int rb = warp & 3, gh = warp >> 2;
+            const int rb = warp & 3, gq = warp >> 2;
             float aG0 = 0.f, aG1 = 0.f, aU0 = 0.f, aU1 = 0.f;
             if (valid) {
                 if (!x_ready) {
                     if (!bad && !mbar_wait(xbar, 0, p.err)) bad = true;
-                    // per-group sums of x for the bias term: warp w sums groups w, w+8, ...
-                    for (int grp = warp; grp < ngH; grp += kDecodeConsumerWarps)
+                    // per-group sums of x for the bias term
+                    for (int grp = warp; grp < ngH; grp += NCW)
                         for (int t = 0; t < T; ++t) {
                             const uint32_t v = *reinterpret_cast<const uint32_t *>(x_s + t * xstride + grp * 64 + 2 * lane);
                             float s = bf16lo(v) + bf16hi(v);
                             for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                             if (lane == 0) xsum[grp * kDecodeMaxT + t] = s;
                         }
-                    named_bar(1, kDecodeConsumerWarps * 32);
+                    named_bar(1, kCons);
                 }
-                for (int c = 0; c < nchunks; ++c, ++qdone) {
-                    const uint32_t slot = qdone % nst;
-                    if (!bad && !mbar_wait(&full[slot], (qdone / nst) & 1, p.err)) bad = true;
-                    const uint8_t *base = ring + slot * kChunkBytes + rb * (kChunkCols / kGroup) * kAtomBytes;
+                for (int c = 0; c < nst; ++c) {
+                    if (!bad && !mbar_wait(&full[c], fills(vit, c) & 1, p.err)) bad = true;
+                    const uint8_t *base = ring + c * kChunkBytes + rb * (kChunkCols / kGroup) * kAtomBytes;
 #pragma unroll
-                    for (int gg = 0; gg < 2; ++gg) {
-                        const int gl = 2 * gh + gg;
+                    for (int gg = 0; gg < kGPW; ++gg) {
+                        const int gl = gq * kGPW + gg;
                         const uint8_t *atom = base + gl * kAtomBytes;
                         const uint4 A = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
                         const uint2 SB = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
@@ -272,36 +352,34 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
                             mma_bf16(acc, a0, xl[m], xh4[m]);
                             mma_bf16(acc2, a1, xl[m + 1], xh4[m + 1]);
                         }
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
                         const float2 X = *reinterpret_cast<const float2 *>(xsum + grp * kDecodeMaxT + 2 * t4);
-                        const float sg = half_bits_to_f32(uint16_t(SB.x & 0xffff));
-                        const float bg = half_bits_to_f32(uint16_t(SB.x >> 16));
-                        const float su = half_bits_to_f32(uint16_t(SB.y & 0xffff));
-                        const float bu = half_bits_to_f32(uint16_t(SB.y >> 16));
-                        const float bpg = fmaf(-128.f, sg, bg), bpu = fmaf(-128.f, su, bu);
-                        aG0 += fmaf(sg, acc[0], bpg * X.x);
-                        aG1 += fmaf(sg, acc[1], bpg * X.y);
-                        aU0 += fmaf(su, acc[2], bpu * X.x);
-                        aU1 += fmaf(su, acc[3], bpu * X.y);
+                        float sg, bpg, su, bpu;
+                        scale_bias(SB.x, sg, bpg);
+                        scale_bias(SB.y, su, bpu);
+                        aG0 += fmaf(sg, acc[0] + acc2[0], bpg * X.x);
+                        aG1 += fmaf(sg, acc[1] + acc2[1], bpg * X.y);
+                        aU0 += fmaf(su, acc[2] + acc2[2], bpu * X.x);
+                        aU1 += fmaf(su, acc[3] + acc2[3], bpu * X.y);
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[slot]);
+                    if (lane == 0) mbar_arrive(&empty[c]);
                 }
             }
-            // combine the two K halves, SwiGLU, h slice -> own shared memory
-            if (gh == 1) red[rb * 32 + lane] = make_float4(aG0, aG1, aU0, aU1);
-            named_bar(1, kDecodeConsumerWarps * 32);
-            if (gh == 0) {
-                const float4 v = red[rb * 32 + lane];
-                aG0 += v.x; aG1 += v.y; aU0 += v.z; aU1 += v.w;
+            // add the K parts of each row block, SwiGLU, h slice -> own shared memory
+            if (gq > 0) red[((gq - 1) * kRowBlocksA + rb) * 32 + lane] = make_float4(aG0, aG1, aU0, aU1);
+            named_bar(1, kCons);
+            if (gq == 0) {
+#pragma unroll
+                for (int q = 1; q < kGQ; ++q) {
+                    const float4 v = red[((q - 1) * kRowBlocksA + rb) * 32 + lane];
+                    aG0 += v.x; aG1 += v.y; aU0 += v.z; aU1 += v.w;
+                }
                 const int il = rb * 8 + g;
                 const int t0 = 2 * t4, t1 = t0 + 1;
                 if (t0 < T) hslice[t0 * kSlice + il] = (valid && !bad) ? silu(aG0) * aU0 : 0.f;
                 if (t1 < T) hslice[t1 * kSlice + il] = (valid && !bad) ? silu(aG1) * aU1 : 0.f;
             }
         }
-
         if (valid) x_ready = true;   // every thread: valid is uniform in the cluster
 
         // ---- exchange h slices inside the cluster
@@ -309,7 +387,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         cluster_wait();
         if (!producer) {
             const int nitems = p.cs * T * (kSlice / 4);
-            for (int i = tid; i < nitems; i += kDecodeConsumerWarps * 32) {
+            for (int i = tid; i < nitems; i += kCons) {
                 const int q4 = i % (kSlice / 4);
                 const int rest = i / (kSlice / 4);
                 const int tok = rest % T, peer = rest / T;
@@ -321,8 +399,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
                 *reinterpret_cast<uint2 *>(hhi + tok * (I + 8) + col) = make_uint2(h01, h23);
                 *reinterpret_cast<uint2 *>(hlo + tok * (I + 8) + col) = make_uint2(l01, l23);
             }
-            named_bar(1, kDecodeConsumerWarps * 32);
-            for (int grp = warp; grp < ngI; grp += kDecodeConsumerWarps)
+            named_bar(1, kCons);
+            for (int grp = warp; grp < ngI; grp += NCW)
                 for (int t = 0; t < T; ++t) {
                     const uint32_t vh = *reinterpret_cast<const uint32_t *>(hhi + t * (I + 8) + grp * 64 + 2 * lane);
                     const uint32_t vl = *reinterpret_cast<const uint32_t *>(hlo + t * (I + 8) + grp * 64 + 2 * lane);
@@ -330,91 +408,68 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
                     for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                     if (lane == 0) xh[grp * kDecodeMaxT + t] = s;
                 }
-            named_bar(1, kDecodeConsumerWarps * 32);
+            named_bar(1, kCons);
         }
         cluster_arrive();   // done reading peers' slices; matched by the wait at the next iteration / exit
 
-        // ---- phase B: down rows of this CTA, full K = I
+        // ---- phase B: down rows of this CTA, full K = I, from ring slots 0..nB-1
         if (!producer) {
-            const bool run = valid && !bad;
-            if (run) {
-                if (!mbar_wait(wbar, nw & 1, p.err)) bad = true;
-                ++nw;
-            }
+            if (valid)
+                for (int s = 0; s < nB; ++s)
+                    if (!bad && !mbar_wait(&full[s], (fills(vit, s) + 1) & 1, p.err)) bad = true;
             float *yp = p.ypair + size_t(u) * T * H;
-            for (int rbB = warp; rbB < nrbB; rbB += kDecodeConsumerWarps) {
-                float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
-                if (run && !bad) {
-                    // groups two at a time; per group the hi and lo halves of h
-                    // accumulate in separate chains (four independent chains)
-                    for (int kb0 = 0; kb0 < ngI; kb0 += 2) {
-                        float acc[2][2][4];
-                        uint4 A[2];
-                        uint2 SB[2];
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const int kb = kb0 + q < ngI ? kb0 + q : kb0;
-                            const uint8_t *atom = wB + (rbB * ngI + kb) * kAtomBytes;
-                            A[q] = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
-                            SB[q] = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) acc[q][0][i] = acc[q][1][i] = 0.f;
-                        }
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const int kb = kb0 + q < ngI ? kb0 + q : kb0;
-                            const int col = kb * kGroup + 16 * t4;
-                            uint4 ha = make_uint4(0, 0, 0, 0), hb = ha, la = ha, lb = ha;
-                            if (g < T) {
-                                ha = *reinterpret_cast<const uint4 *>(hhi + g * (I + 8) + col);
-                                hb = *reinterpret_cast<const uint4 *>(hhi + g * (I + 8) + col + 8);
-                                la = *reinterpret_cast<const uint4 *>(hlo + g * (I + 8) + col);
-                                lb = *reinterpret_cast<const uint4 *>(hlo + g * (I + 8) + col + 8);
-                            }
-                            const uint32_t ha_[4] = {ha.x, ha.y, ha.z, ha.w}, hb_[4] = {hb.x, hb.y, hb.z, hb.w};
-                            const uint32_t la_[4] = {la.x, la.y, la.z, la.w}, lb_[4] = {lb.x, lb.y, lb.z, lb.w};
-#pragma unroll
-                            for (int m = 0; m < 4; ++m) {
-                                const uint32_t a[4] = {nib_pair(A[q].x, m), nib_pair(A[q].z, m),
-                                                       nib_pair(A[q].y, m), nib_pair(A[q].w, m)};
-                                mma_bf16(acc[q][0], a, ha_[m], hb_[m]);
-                                mma_bf16(acc[q][1], a, la_[m], lb_[m]);
-                            }
-                        }
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            if (kb0 + q >= ngI) break;
-                            const int kb = kb0 + q;
-                            const float2 X = *reinterpret_cast<const float2 *>(xh + kb * kDecodeMaxT + 2 * t4);
-                            const float s0 = half_bits_to_f32(uint16_t(SB[q].x & 0xffff));
-                            const float b0 = half_bits_to_f32(uint16_t(SB[q].x >> 16));
-                            const float s1 = half_bits_to_f32(uint16_t(SB[q].y & 0xffff));
-                            const float b1 = half_bits_to_f32(uint16_t(SB[q].y >> 16));
-                            const float bp0 = fmaf(-128.f, s0, b0), bp1 = fmaf(-128.f, s1, b1);
-                            y0 += fmaf(s0, acc[q][0][0] + acc[q][1][0], bp0 * X.x);
-                            y1 += fmaf(s0, acc[q][0][1] + acc[q][1][1], bp0 * X.y);
-                            y2 += fmaf(s1, acc[q][0][2] + acc[q][1][2], bp1 * X.x);
-                            y3 += fmaf(s1, acc[q][0][3] + acc[q][1][3], bp1 * X.y);
-                        }
-                    }
-                }
+            const int t0 = 2 * t4, t1 = t0 + 1;
+            auto store = [&](int rbB, const float (&y)[4]) {
                 const int row = int(rank) * rowsB + rbB * 16 + g;
-                const int t0 = 2 * t4, t1 = t0 + 1;
-                if (t0 < T) { yp[size_t(t0) * H + row] = y0; yp[size_t(t0) * H + row + 8] = y2; }
-                if (t1 < T) { yp[size_t(t1) * H + row] = y1; yp[size_t(t1) * H + row + 8] = y3; }
+                if (t0 < T) { yp[size_t(t0) * H + row] = y[0]; yp[size_t(t0) * H + row + 8] = y[2]; }
+                if (t1 < T) { yp[size_t(t1) * H + row] = y[1]; yp[size_t(t1) * H + row + 8] = y[3]; }
+            };
+            if (splitB > 1) {
+                // one (row block, K part) per warp; the K parts meet in shared memory
+                const int rbB = warp % nrbB, sp = warp / nrbB;
+                const int kb_per = (ngI + splitB - 1) / splitB;
+                const int kbeg = sp * kb_per < ngI ? sp * kb_per : ngI;
+                const int kend = kbeg + kb_per < ngI ? kbeg + kb_per : ngI;
+                float y[4] = {0.f, 0.f, 0.f, 0.f};
+                if (valid && !bad) down_rows(ring, rbB, ngI, kbeg, kend, hhi, hlo, xh, I, T, lane, y);
+                if (valid) {
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int s = 0; s < nB; ++s) mbar_arrive(&empty[s]);
+                }
+                if (sp > 0) red[((sp - 1) * nrbB + rbB) * 32 + lane] = make_float4(y[0], y[1], y[2], y[3]);
+                named_bar(1, kCons);
+                if (sp == 0) {
+                    for (int q = 1; q < splitB; ++q) {
+                        const float4 v = red[((q - 1) * nrbB + rbB) * 32 + lane];
+                        y[0] += v.x; y[1] += v.y; y[2] += v.z; y[3] += v.w;
+                    }
+                    store(rbB, y);
+                }
+            } else {
+                for (int rbB = warp; rbB < nrbB; rbB += NCW) {
+                    float y[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (valid && !bad) down_rows(ring, rbB, ngI, 0, ngI, hhi, hlo, xh, I, T, lane, y);
+                    store(rbB, y);
+                }
+                if (valid) {
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int s = 0; s < nB; ++s) mbar_arrive(&empty[s]);
+                }
             }
 
             // ---- arrival ticket for this row chunk; the last arrival combines
-            named_bar(1, kDecodeConsumerWarps * 32);
+            named_bar(1, kCons);
             if (tid == 0) {
                 __threadfence();
                 const uint32_t old = atomicAdd(&p.counters[rank], 1u);
                 flags[1] = (old == uint32_t(U_total - 1)) ? 1 : 0;
             }
-            named_bar(1, kDecodeConsumerWarps * 32);
+            named_bar(1, kCons);
             if (flags[1]) {
                 __threadfence();
-                for (int i = tid; i < T * rowsB; i += kDecodeConsumerWarps * 32) {
+                for (int i = tid; i < T * rowsB; i += kCons) {
                     const int tok = i / rowsB;
                     const int row = int(rank) * rowsB + i % rowsB;
                     // all loads first (k <= 16), then the sum in route order
@@ -441,10 +496,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
                     if (p.residual) acc += __uint_as_float(uint32_t(p.residual[size_t(tok) * H + row]) << 16);
                     p.out[size_t(tok) * H + row] = f32_to_bf16_bits(acc);
                 }
-                named_bar(1, kDecodeConsumerWarps * 32);
+                named_bar(1, kCons);
                 if (tid == 0) atomicExch(&p.counters[rank], 0u);
             }
         }
+        if (valid) ++vit;
         __syncthreads();
     }
     if (it > 0) cluster_wait();
@@ -454,36 +510,26 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     }
 }
 
-cudaError_t decode_config(smoe_ctx *ctx)
+template <int NCW>
+static cudaError_t config_one(smoe_ctx *ctx, int max_smem_optin, int *smem_out, int *clusters_out)
 {
     const smoe_shape &s = ctx->shape;
-    const int nchunks = s.H / kChunkCols;
-    int max_smem_optin = 0;
-    cudaError_t e = cudaDeviceGetAttribute(&max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device);
-    if (e != cudaSuccess) return e;
     int worst = 0;
     for (int T = 1; T <= kDecodeMaxT; ++T) {
-        int nst = nchunks < 8 ? nchunks : 8;
-        // prefer two CTAs per SM (<= 113 KB each) while keeping >= 4 stages in flight
-        while (nst > 4 && decode_smem(T, s.H, s.I, ctx->cs, nst).total > 113 * 1024) --nst;
-        while (nst > 2 && decode_smem(T, s.H, s.I, ctx->cs, nst).total > max_smem_optin) --nst;
-        const int sm = decode_smem(T, s.H, s.I, ctx->cs, nst).total;
-        if (sm > max_smem_optin) return cudaErrorInvalidValue;
-        ctx->decode[T].nst = nst;
-        ctx->decode[T].smem = sm;
+        const int sm = decode_smem(T, s.H, s.I, ctx->cs, NCW).total;
+        smem_out[T] = sm;
         if (sm > worst) worst = sm;
     }
-    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
+    if (worst > max_smem_optin) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<NCW>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
+    if (e == cudaSuccess && ctx->cs > 8)
+        e = cudaFuncSetAttribute(decode_kernel<NCW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    if (ctx->cs > 8) {
-        e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
     for (int T = 1; T <= kDecodeMaxT; ++T) {
         cudaLaunchConfig_t lc = {};
         lc.gridDim = dim3(ctx->cs * 64);
-        lc.blockDim = dim3(kDecodeThreads);
-        lc.dynamicSmemBytes = ctx->decode[T].smem;
+        lc.blockDim = dim3((NCW + 1) * 32);
+        lc.dynamicSmemBytes = smem_out[T];
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
         at[0].val.clusterDim.x = ctx->cs;
@@ -492,10 +538,30 @@ cudaError_t decode_config(smoe_ctx *ctx)
         lc.attrs = at;
         lc.numAttrs = 1;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, decode_kernel, &lc);
+        e = cudaOccupancyMaxActiveClusters(&n, decode_kernel<NCW>, &lc);
         if (e != cudaSuccess) return e;
-        if (n < 1) return cudaErrorInvalidConfiguration;
-        ctx->decode[T].max_clusters = n;
+        clusters_out[T] = n;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t decode_config(smoe_ctx *ctx)
+{
+    int max_smem_optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device);
+    if (e != cudaSuccess) return e;
+    int sm8[kDecodeMaxT + 1], cl8[kDecodeMaxT + 1], sm16[kDecodeMaxT + 1], cl16[kDecodeMaxT + 1];
+    e = config_one<8>(ctx, max_smem_optin, sm8, cl8);
+    if (e != cudaSuccess) return e;
+    e = config_one<16>(ctx, max_smem_optin, sm16, cl16);
+    if (e != cudaSuccess) return e;
+    for (int T = 1; T <= kDecodeMaxT; ++T) {
+        if (cl8[T] < 1) return cudaErrorInvalidConfiguration;
+        ctx->decode[T].nst = ctx->shape.H / kChunkCols;
+        ctx->decode[T].smem = sm8[T];
+        ctx->decode[T].max_clusters = cl8[T];
+        ctx->decode[T].smem16 = sm16[T];
+        ctx->decode[T].max_clusters16 = cl16[T];
     }
     return cudaSuccess;
 }
@@ -504,14 +570,17 @@ cudaError_t launch_decode(const smoe_ctx *ctx, const DecodeParams &p0, cudaStrea
 {
     DecodeParams p = p0;
     const DecodeCfg &cfg = ctx->decode[p.T];
-    p.nst = cfg.nst;
     p.cs = ctx->cs;
     const int umax = (p.E < p.T * p.k ? p.E : p.T * p.k) + 1;
-    const int nclus = umax < cfg.max_clusters ? umax : cfg.max_clusters;
+    // 16 consumer warps (one CTA per SM) when every expert gets its own
+    // co-resident cluster that way; otherwise 8 (two CTAs per SM).
+    const bool wide = umax * p.cs <= ctx->num_sms && cfg.max_clusters16 >= umax;
+    const int maxc = wide ? cfg.max_clusters16 : cfg.max_clusters;
+    const int nclus = umax < maxc ? umax : maxc;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(nclus * p.cs);
-    lc.blockDim = dim3(kDecodeThreads);
-    lc.dynamicSmemBytes = cfg.smem;
+    lc.blockDim = dim3(((wide ? 16 : 8) + 1) * 32);
+    lc.dynamicSmemBytes = wide ? cfg.smem16 : cfg.smem;
     lc.stream = st;
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -522,7 +591,7 @@ cudaError_t launch_decode(const smoe_ctx *ctx, const DecodeParams &p0, cudaStrea
     at[1].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = at;
     lc.numAttrs = 2;
-    return cudaLaunchKernelEx(&lc, decode_kernel, p);
+    return wide ? cudaLaunchKernelEx(&lc, decode_kernel<16>, p) : cudaLaunchKernelEx(&lc, decode_kernel<8>, p);
 }
 
 }  // namespace smoe

@@ -149,7 +149,7 @@ static int shape_check(const smoe_shape *s)
     if (!s) return SMOE_EINVAL;
     if (s->group != 64 || s->bits != 4) return SMOE_ENOTSUP;
     if (s->H <= 0 || s->E <= 0 || s->k <= 0 || s->I <= 0) return SMOE_EINVAL;
-    if (s->H % 256 || s->H > 4096) return SMOE_ENOTSUP;
+    if (s->H % 256 || s->H > 2048) return SMOE_ENOTSUP;
     if (s->I % 64 || s->I < 64 || s->I > 512 || s->I_shared != s->I) return SMOE_ENOTSUP;
     if (s->k > 16 || s->k > s->E || s->E > 1024) return SMOE_ENOTSUP;
     return SMOE_OK;
@@ -351,8 +351,9 @@ extern "C" int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len)
     if (!ctx || !buf || len <= 0) return SMOE_EINVAL;
     int o = std::snprintf(buf, size_t(len), "sms=%d decode: cluster=%d", ctx->num_sms, ctx->cs);
     for (int T = 1; T <= kDecodeMaxT && o < len; ++T)
-        o += std::snprintf(buf + o, size_t(len - o), " T%d:{stages=%d smem=%d clusters=%d}", T,
-                           ctx->decode[T].nst, ctx->decode[T].smem, ctx->decode[T].max_clusters);
+        o += std::snprintf(buf + o, size_t(len - o), " T%d:{slots=%d smem=%d/%d clusters=%d/%d}", T,
+                           ctx->decode[T].nst, ctx->decode[T].smem, ctx->decode[T].smem16,
+                           ctx->decode[T].max_clusters, ctx->decode[T].max_clusters16);
     return SMOE_OK;
 }
 

@@ -19,8 +19,6 @@ constexpr int kSlice = 32;                        // intermediates per CTA
 constexpr int kChunkCols = 256;                   // H columns per streamed chunk
 constexpr int kRowBlocksA = kSlice / 8;           // gate/up row blocks per CTA
 constexpr int kChunkBytes = kRowBlocksA * (kChunkCols / kGroup) * kAtomBytes;   // 9216
-constexpr int kDecodeConsumerWarps = 8;
-constexpr int kDecodeThreads = (kDecodeConsumerWarps + 1) * 32;
 
 struct Layout {
     uint64_t blob, gu_off, gu_bytes, down_off, down_bytes;
@@ -38,9 +36,11 @@ inline Layout layout_of(int H, int I)
 }
 
 struct DecodeCfg {
-    int nst = 0;            // ring stages
-    int smem = 0;           // dynamic shared memory bytes
-    int max_clusters = 0;   // co-resident clusters
+    int nst = 0;              // ring slots
+    int smem = 0;             // dynamic shared memory bytes, 8 consumer warps
+    int max_clusters = 0;     // co-resident clusters, 8 consumer warps
+    int smem16 = 0;           // the same with 16 consumer warps
+    int max_clusters16 = 0;
 };
 
 }  // namespace smoe

@@ -47,6 +47,7 @@ def test_layout_sizes():
 @pytest.mark.parametrize("shape,status", [
     ((2048, 512, 10, 512, 256), smoe.ENOTSUP),     # I_shared != I
     ((2000, 512, 10, 512, 512), smoe.ENOTSUP),     # H not a multiple of 256
+    ((4096, 512, 10, 512, 512), smoe.ENOTSUP),     # H above what the decode kernel stages
     ((2048, 512, 10, 1024, 1024), smoe.ENOTSUP),   # I too large for the kernels
     ((2048, 8, 10, 512, 512), smoe.ENOTSUP),       # k > E
     ((2048, 512, 0, 512, 512), smoe.EINVAL),

@@ -32,9 +32,10 @@ def built():
 
 # ------------------------------------------------------------------ helpers
 
-def routing_ok(ids_g, w_g, gate_g, ref, k, atol_w=2e-5, atol_gate=1e-5):
+def routing_ok(ids_g, w_g, gate_g, ref, k, atol_w=2e-5, atol_gate=1e-5, gap=1e-4):
     """Returns the tokens whose expert set matches the oracle's; asserts the
-    rule on every token where the oracle's decision is not a near-tie."""
+    rule on every token where the oracle's decision is not a near-tie (the
+    probabilities differ by more than `gap`)."""
     probs = ref["probs"]
     same = []
     for t in range(ids_g.shape[0]):
@@ -42,12 +43,12 @@ def routing_ok(ids_g, w_g, gate_g, ref, k, atol_w=2e-5, atol_gate=1e-5):
         order = np.argsort(-p, kind="stable")
         ps = p[order]
         gap_k = ps[k - 1] - ps[k] if k < len(p) else np.inf
-        if gap_k > 1e-4:
+        if gap_k > gap:
             assert set(ids_g[t].tolist()) == set(ref["ids"][t].tolist()), (t, ids_g[t], ref["ids"][t])
         for j in range(k):
             lo = ps[j] - ps[j + 1] if j + 1 < len(p) else np.inf
             hi = ps[j - 1] - ps[j] if j > 0 else np.inf
-            if lo > 1e-4 and hi > 1e-4:
+            if lo > gap and hi > gap:
                 assert ids_g[t, j] == ref["ids"][t, j], (t, j)
         if set(ids_g[t].tolist()) == set(ref["ids"][t].tolist()):
             same.append(t)
@@ -238,10 +239,13 @@ def test_full_stack_in_cuda_graph(which, request):
     Deeper layers compare two chains: each side rounds x_{l+1} = x_l + y_l to
     bf16, and where the two pre-rounding values straddle a rounding boundary
     the chains differ by one bf16 unit, which then rides the residual stream.
-    So layer l > 0 gets: the routing rule (weights/gate within 2e-3, since the
-    router inputs differ by such units), relative L2 <= 5e-3 of the stream, and
-    |gpu - oracle| <= (l + 1) bf16 units (of the larger binade of the two
-    values) + 2e-2 rms(y_l)."""
+    So layer l > 0 gets: the routing rule with a 1e-3 near-tie margin (weights
+    and gate within 2e-3 sqrt(l + 1), since the router inputs drift apart by
+    such units layer after layer),
+    relative L2 of the stream <= 5e-3 sqrt(l + 1) (independent per-layer
+    disagreements add in quadrature), and
+    per element |gpu - oracle| <= the sum over layers so far of one bf16 unit
+    (of the larger binade of the two values at that layer) + 2e-2 rms(y)."""
     pool, inp = request.getfixturevalue(which)
     wl = pool.wl
     st = W.Stack(pool, inp, 1)
@@ -252,26 +256,29 @@ def test_full_stack_in_cuda_graph(which, request):
     torch.cuda.synchronize()
     assert smoe.check(st.err) == 0
     x = x0
+    bound = np.zeros((1, wl.H))
     for l in range(pool.n_layers):
         ref = oracle_layer(wl, l, x, inp)
         ids = st.ids[l].cpu().numpy()
-        tol = (2e-5, 1e-5) if l == 0 else (2e-3, 2e-3)
+        # past layer 0 the router inputs differ by bf16 units: probabilities move
+        # by ~1e-4, so near-ties are judged with a 1e-3 margin there
+        c = np.sqrt(l + 1)
+        tol = (2e-5, 1e-5, 1e-4) if l == 0 else (2e-3 * c, 2e-3 * c, 1e-3)
         same = routing_ok(ids, st.w[l].cpu().numpy(), st.gate[l].cpu().numpy(), ref, wl.k, *tol)
         if not same:
             pytest.skip("near-tie routing at layer %d: the chains legitimately diverge" % l)
         xr = synthetic.bf16_bits_to_f32(x).astype(np.float64)
         want = oracle.residual(x, ref["out64"])
         got = W.bits_of(st.xs[l + 1])
+        g = synthetic.bf16_bits_to_f32(got).astype(np.float64)
+        o = synthetic.bf16_bits_to_f32(want).astype(np.float64)
+        big = np.maximum(np.maximum(np.abs(o), np.abs(g)), 1e-30)
+        bound += 2.0 ** (np.floor(np.log2(big)) - 7) + 2e-2 * np.sqrt(np.mean(ref["out64"] ** 2))
         if l == 0:
             assert_output_close(got, xr + ref["out64"], want, exact_frac=0.95)
         else:
-            g = synthetic.bf16_bits_to_f32(got).astype(np.float64)
-            o = synthetic.bf16_bits_to_f32(want).astype(np.float64)
-            assert np.linalg.norm(g - o) <= 5e-3 * np.linalg.norm(o)
-            big = np.maximum(np.maximum(np.abs(o), np.abs(g)), 1e-30)
-            unit = 2.0 ** (np.floor(np.log2(big)) - 7)    # bf16 spacing in the larger binade
-            rms_y = np.sqrt(np.mean(ref["out64"] ** 2))
-            assert np.all(np.abs(g - o) <= (l + 1) * unit + 2e-2 * rms_y)
+            assert np.linalg.norm(g - o) <= 5e-3 * np.sqrt(l + 1) * np.linalg.norm(o)
+            assert np.all(np.abs(g - o) <= bound)
         x = want                      # continue the oracle's own chain
 
 
