@@ -202,6 +202,27 @@ SMOE_API int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x, 
                 const uint16_t *residual, uint16_t *out,
                 void *workspace, uint64_t workspace_bytes, int32_t *err, void *stream);
 
+/* -------------------------------------------------- moe_forward_noalloc */
+/* moe_forward for T <= 8 without a workspace, for callers that cannot
+ * allocate device memory: code handed only its input and output buffers by a
+ * host framework that owns all device memory (plugin or custom-operator
+ * interfaces), or loops that must never allocate because an allocation can
+ * synchronise the device. The pages describe no such interface; it has no
+ * counterpart there. Arguments and results are those of moe_forward minus
+ * the workspace. The scratch (arrival tickets and per-expert outputs) lives
+ * in one fixed 8 MiB array inside the library, which every GPU that loads the
+ * library holds until the process exits; a call needing more than that
+ * ((min(E, T*k) + 1) * T * H * 4 bytes plus 256) returns SMOE_ENOMEM, and
+ * T > 8 returns SMOE_ENOTSUP. The first call on a device looks up the
+ * array's device address (make that first call before any stream capture);
+ * every call clears the tickets on `stream` before launching. All calls share
+ * the one array, so calls that overlap on the GPU (other streams, other
+ * threads) race and give wrong results: serialise them. */
+SMOE_API int moe_forward_noalloc(const smoe_ctx *ctx, int32_t layer, const uint16_t *x, int32_t T,
+                                 const int32_t *ids, const float *w, const float *gate,
+                                 const void *pool, uint64_t pool_bytes, const void *shared_blob,
+                                 const uint16_t *residual, uint16_t *out, int32_t *err, void *stream);
+
 /* Waits for stream, reads the error word (then clears it to 0) and returns
  * SMOE_OK, SMOE_EDEVICE if a kernel stored a code (copied to *code if
  * non-NULL), or SMOE_ECUDA. Not for use inside graph capture. */

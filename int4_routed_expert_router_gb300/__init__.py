@@ -19,7 +19,7 @@ OK, EINVAL, ERANGE, ENOMEM, ECUDA, EDEVICE, ENOTSUP = 0, -1, -2, -3, -4, -5, -6
 DEV_BAD_SLOT, DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2, 3
 HOST, DEVICE = 0, 1
 EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destroy", "set_slot_table",
-           "smoe_workspace_bytes", "moe_route", "moe_forward", "smoe_check",
+           "smoe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_noalloc", "smoe_check",
            "smoe_ctx_describe", "smoe_status_string"]
 
 
@@ -66,6 +66,7 @@ def lib():
         L.smoe_workspace_bytes.restype = u64
         L.moe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, u64, vp]
         L.moe_forward.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, u64, vp, vp, vp, vp, u64, vp, vp]
+        L.moe_forward_noalloc.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, u64, vp, vp, vp, vp, vp]
         L.smoe_check.argtypes = [vp, C.POINTER(C.c_int32), vp]
         L.smoe_ctx_describe.argtypes = [vp, C.c_char_p, i32]
         L.smoe_status_string.argtypes = [C.c_int]
@@ -192,6 +193,16 @@ def moe_forward(ctx: Context, layer: int, x, ids, w, gate, pool, shared_blob, ou
                              pool.numel() * pool.element_size(), _ptr(shared_blob), _ptr(residual), _ptr(out),
                              _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
                              _stream(stream)), "moe_forward")
+
+
+def moe_forward_noalloc(ctx: Context, layer: int, x, ids, w, gate, pool, shared_blob, out, err,
+                        residual=None, stream=None):
+    """moe_forward without a workspace (scratch inside the library); T <= 8."""
+    T = x.shape[0]
+    _check(lib().moe_forward_noalloc(ctx.handle, int(layer), _ptr(x), T, _ptr(ids), _ptr(w), _ptr(gate),
+                                     _ptr(pool), pool.numel() * pool.element_size(), _ptr(shared_blob),
+                                     _ptr(residual), _ptr(out), _ptr(err), _stream(stream)),
+           "moe_forward_noalloc")
 
 
 def check(err, stream=None) -> int:
