@@ -60,6 +60,7 @@ extern "C" {
 #define SMOE_DEV_BAD_SLOT 1     /* a selected expert's slot is < 0 or >= n_slots */
 #define SMOE_DEV_BAD_EXPERT 2   /* an id in ids[] is < 0 or >= E */
 #define SMOE_DEV_TIMEOUT 3      /* a bounded wait inside a kernel gave up */
+#define SMOE_DEV_RANGE 4        /* T > 8 path: |x| or |h| >= 65504 (outside its fp16 operands) */
 
 /* ------------------------------------------------------------------ shapes */
 /* H: hidden size; E: routed experts per layer; k: experts per token;
@@ -194,8 +195,11 @@ SMOE_API int moe_route(const smoe_ctx *ctx, const uint16_t *W_r, const uint16_t 
  * Partial sums are fp32 and are combined in a fixed order (route order for
  * each token, then the shared term), so the result does not depend on
  * scheduling, slot placement or run: bit-identical across runs and slot
- * permutations. T <= 8 takes the fused decode kernel; larger T the
- * token-bucketed path. Errors: SMOE_EINVAL, SMOE_ENOMEM, SMOE_ECUDA. */
+ * permutations. T <= 8 takes the fused decode kernel (weights exact, fp32
+ * intermediates); larger T the token-bucketed path, whose tensor-core GEMMs
+ * take fp16 operands (dequantised weights, x, h), so it needs |x| < 65504
+ * (else SMOE_DEV_RANGE in the error word). Errors: SMOE_EINVAL, SMOE_ENOMEM,
+ * SMOE_ECUDA. */
 SMOE_API int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x, int32_t T,
                 const int32_t *ids, const float *w, const float *gate,
                 const void *pool, uint64_t pool_bytes, const void *shared_blob,
@@ -232,6 +236,16 @@ SMOE_API int smoe_check(int32_t *err_dev, int32_t *code, void *stream);
  * chose (cluster size, ring stages, shared memory, co-resident clusters) into
  * buf (NUL-terminated, at most len bytes). Errors: SMOE_EINVAL. */
 SMOE_API int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len);
+
+/* Profiling hook. events: up to 4 caller-created cudaEvent_t (as void*), or
+ * NULL/n = 0 to turn it off. While set, each moe_forward on this context
+ * records them on its stream (as external events, so they also become event
+ * nodes when the stream is being captured): events[0] before the dominant
+ * kernel, events[1] after it -- the fused decode kernel for T <= 8, the
+ * grouped gate/up GEMM otherwise -- and, for T > 8, events[2] after the
+ * grouped down GEMM. The library keeps the pointers, not the events.
+ * Errors: SMOE_EINVAL. */
+SMOE_API int smoe_set_profile_events(smoe_ctx *ctx, void *const *events, int32_t n);
 
 /* Short English text for a status code (static storage). */
 SMOE_API const char *smoe_status_string(int status);

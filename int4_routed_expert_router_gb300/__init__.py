@@ -16,11 +16,11 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsmoe.so")
 
 OK, EINVAL, ERANGE, ENOMEM, ECUDA, EDEVICE, ENOTSUP = 0, -1, -2, -3, -4, -5, -6
-DEV_BAD_SLOT, DEV_BAD_EXPERT, DEV_TIMEOUT = 1, 2, 3
+DEV_BAD_SLOT, DEV_BAD_EXPERT, DEV_TIMEOUT, DEV_RANGE = 1, 2, 3, 4
 HOST, DEVICE = 0, 1
 EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destroy", "set_slot_table",
            "smoe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_noalloc", "smoe_check",
-           "smoe_ctx_describe", "smoe_status_string"]
+           "smoe_ctx_describe", "smoe_set_profile_events", "smoe_status_string"]
 
 
 class SmoeError(RuntimeError):
@@ -69,6 +69,7 @@ def lib():
         L.moe_forward_noalloc.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, u64, vp, vp, vp, vp, vp]
         L.smoe_check.argtypes = [vp, C.POINTER(C.c_int32), vp]
         L.smoe_ctx_describe.argtypes = [vp, C.c_char_p, i32]
+        L.smoe_set_profile_events.argtypes = [vp, C.POINTER(vp), i32]
         L.smoe_status_string.argtypes = [C.c_int]
         L.smoe_status_string.restype = C.c_char_p
         for name in EXPORTS:
@@ -169,6 +170,12 @@ class Context:
         buf = C.create_string_buffer(1024)
         _check(lib().smoe_ctx_describe(self.handle, buf, 1024), "smoe_ctx_describe")
         return buf.value.decode()
+
+    def set_profile_events(self, events):
+        """events: list of up to 4 torch.cuda.Event (already recorded once), or []."""
+        n = len(events)
+        arr = (C.c_void_p * max(n, 1))(*[e.cuda_event for e in events])
+        _check(lib().smoe_set_profile_events(self.handle, arr, n), "smoe_set_profile_events")
 
     def workspace_bytes(self, T: int) -> int:
         return int(lib().smoe_workspace_bytes(self.handle, int(T)))

@@ -254,7 +254,13 @@ cudaError_t route_config()
 cudaError_t launch_route(const RouteParams &p0, cudaStream_t st)
 {
     RouteParams p = p0;
-    p.fused_topk = p.T <= kDecodeMaxT ? 1 : 0;
+    if (p.T > kDecodeMaxT) {       // logits on tensor cores, then one warp per token
+        cudaError_t e = launch_router_gemm(p, st);
+        if (e != cudaSuccess) return e;
+        topk_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(p);
+        return cudaGetLastError();
+    }
+    p.fused_topk = 1;
     const int smem = (kRouteRows + kRouteToks) * p.H * 2 + 16;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((p.E + 1 + kRouteRows - 1) / kRouteRows, (p.T + kRouteToks - 1) / kRouteToks);
@@ -266,11 +272,7 @@ cudaError_t launch_route(const RouteParams &p0, cudaStream_t st)
     at[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = at;
     lc.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&lc, route_logits_kernel, p);
-    if (e != cudaSuccess || p.fused_topk) return e;
-    lc.gridDim = dim3((p.T + 7) / 8);
-    lc.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&lc, topk_kernel, p);
+    return cudaLaunchKernelEx(&lc, route_logits_kernel, p);
 }
 
 }  // namespace smoe

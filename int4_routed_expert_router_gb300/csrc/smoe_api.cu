@@ -129,14 +129,28 @@ cudaError_t launch_pack_device(const smoe_shape &s, const smoe_expert_src &src, 
 Workspace workspace_layout(const smoe_shape &s, int T)
 {
     auto al = [](uint64_t v) { return (v + 255) & ~uint64_t(255); };
-    Workspace w;
+    Workspace w = {};
     uint64_t o = 0;
     w.route_counter = o; o = al(o + 64);
     w.fwd_counters = o;  o = al(o + 64 * 4);
     w.logits = o;        o = al(o + uint64_t(T) * (s.E + 1) * 4);
-    const uint64_t umax = uint64_t(s.E < T * s.k ? s.E : T * s.k) + 1;
-    w.ypair = o;
-    if (T <= kDecodeMaxT) o = al(o + umax * T * s.H * 4);
+    if (T <= kDecodeMaxT) {
+        const uint64_t umax = uint64_t(s.E < T * s.k ? s.E : T * s.k) + 1;
+        w.ypair = o;     o = al(o + umax * T * s.H * 4);
+    } else {
+        const uint64_t P = uint64_t(T) * s.k, nch = (uint64_t(T) + 63) / 64;
+        w.counts = o;     o = al(o + nch * s.E * 4);
+        w.chunk_base = o; o = al(o + nch * s.E * 4);
+        w.offsets = o;    o = al(o + (uint64_t(s.E) + 1) * 4);
+        w.tiles = o;      o = al(o + uint64_t(prefill_max_tiles(T, s.k, s.E)) * sizeof(PfTile));
+        w.ntiles = o;     o = al(o + 4);
+        w.pair_token = o; o = al(o + P * 4);
+        w.pair_j = o;     o = al(o + P * 4);
+        w.pair_pos = o;   o = al(o + P * 4);
+        w.hbuf = o;       o = al(o + (P + T) * s.I * 2);
+        w.ybuf = o;       o = al(o + (P + T) * s.H * 4);
+        w.xh = o;         o = al(o + uint64_t(T) * s.H * 2);
+    }
     w.total = o;
     return w;
 }
@@ -222,6 +236,7 @@ extern "C" int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_
     cudaError_t e = cudaGetDevice(&c->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
     if (e == cudaSuccess) e = route_config();
+    if (e == cudaSuccess) e = prefill_config();
     if (e == cudaSuccess) e = decode_config(c);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -307,8 +322,53 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
     if (pool_bytes < uint64_t(ctx->n_slots) * ctx->layout.blob) return SMOE_ENOMEM;
     const Workspace W = workspace_layout(ctx->shape, T);
     if (workspace_bytes < W.total) return SMOE_ENOMEM;
-    if (T > kDecodeMaxT) return SMOE_ENOTSUP;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (T > kDecodeMaxT) {
+        PrefillParams q = {};
+        q.ids = ids;
+        q.counts = reinterpret_cast<int32_t *>(ws + W.counts);
+        q.chunk_base = reinterpret_cast<int32_t *>(ws + W.chunk_base);
+        q.offsets = reinterpret_cast<int32_t *>(ws + W.offsets);
+        q.tiles = reinterpret_cast<PfTile *>(ws + W.tiles);
+        q.ntiles = reinterpret_cast<int32_t *>(ws + W.ntiles);
+        q.pair_token = reinterpret_cast<int32_t *>(ws + W.pair_token);
+        q.pair_j = reinterpret_cast<int32_t *>(ws + W.pair_j);
+        q.pair_pos = reinterpret_cast<int32_t *>(ws + W.pair_pos);
+        q.ypair = reinterpret_cast<float *>(ws + W.ybuf);
+        q.residual = residual;
+        q.out = out;
+        q.err = err;
+        q.T = T;
+        q.H = ctx->shape.H;
+        q.E = ctx->shape.E;
+        q.k = ctx->shape.k;
+        q.P = T * ctx->shape.k;
+        GemmParams g = {};
+        g.pool = static_cast<const uint8_t *>(pool);
+        g.shared_blob = static_cast<const uint8_t *>(shared_blob);
+        g.table_row = ctx->table_dev + size_t(layer) * ctx->shape.E;
+        g.stride = ctx->layout.blob;
+        g.n_slots = ctx->n_slots;
+        g.x = reinterpret_cast<const uint16_t *>(ws + W.xh);
+        g.x_bf16 = x;
+        g.hbuf = reinterpret_cast<uint16_t *>(ws + W.hbuf);
+        g.ypair = reinterpret_cast<float *>(ws + W.ybuf);
+        g.pair_token = q.pair_token;
+        g.pair_j = q.pair_j;
+        g.ntiles = q.ntiles;
+        g.tiles = q.tiles;
+        g.w = w;
+        g.gate = gate;
+        g.err = err;
+        g.T = T;
+        g.H = q.H;
+        g.E = q.E;
+        g.k = q.k;
+        g.I = ctx->shape.I;
+        g.P = q.P;
+        return cuda_status(launch_prefill(q, g, st, ctx->prof, ctx->nprof));
+    }
     DecodeParams p = {};
     p.x = x;
     p.ids = ids;
@@ -329,7 +389,10 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
     p.E = ctx->shape.E;
     p.k = ctx->shape.k;
     p.I = ctx->shape.I;
-    return cuda_status(launch_decode(ctx, p, static_cast<cudaStream_t>(stream)));
+    cudaError_t e = prof_record(ctx->nprof > 0 ? ctx->prof[0] : nullptr, st);
+    if (e == cudaSuccess) e = launch_decode(ctx, p, st);
+    if (e == cudaSuccess) e = prof_record(ctx->nprof > 1 ? ctx->prof[1] : nullptr, st);
+    return cuda_status(e);
 }
 
 extern "C" int smoe_check(int32_t *err_dev, int32_t *code, void *stream)
@@ -344,6 +407,14 @@ extern "C" int smoe_check(int32_t *err_dev, int32_t *code, void *stream)
     if (e != cudaSuccess) return SMOE_ECUDA;
     if (code) *code = h;
     return h ? SMOE_EDEVICE : SMOE_OK;
+}
+
+extern "C" int smoe_set_profile_events(smoe_ctx *ctx, void *const *events, int32_t n)
+{
+    if (!ctx || n < 0 || n > 4 || (n > 0 && !events)) return SMOE_EINVAL;
+    for (int i = 0; i < 4; ++i) ctx->prof[i] = i < n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+    ctx->nprof = n;
+    return SMOE_OK;
 }
 
 extern "C" int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len)

@@ -54,6 +54,8 @@ struct smoe_ctx {
     int device;
     int num_sms;
     int cs;                                  // cluster size of the decode kernel = I / kSlice
+    cudaEvent_t prof[4];                     // profiling hook (smoe_set_profile_events)
+    int nprof;
     smoe::DecodeCfg decode[smoe::kDecodeMaxT + 1];
 };
 
@@ -93,9 +95,61 @@ struct DecodeParams {
     int cs, nst;
 };
 
+struct PfTile {
+    int32_t kind;     // 0: run of an expert's pairs; 1: run of tokens for the shared expert
+    int32_t expert;
+    int32_t p0;       // first pair (kind 0) or first token (kind 1)
+    int32_t n;        // rows in the run (<= 256)
+};
+
+// Token-bucketed path (T > 8): bucketing and combine.
+struct PrefillParams {
+    const int32_t *ids;
+    int32_t *counts;       // [chunks][E]
+    int32_t *chunk_base;   // [chunks][E]
+    int32_t *offsets;      // [E + 1]
+    PfTile *tiles;         // [max tiles]
+    int32_t *ntiles;
+    int32_t *pair_token;   // [T*k]
+    int32_t *pair_j;       // [T*k]
+    int32_t *pair_pos;     // [T*k] position of pair (t, j) in expert order, -1 if invalid
+    const float *ypair;    // [(T*k + T)][H]
+    const uint16_t *residual;
+    uint16_t *out;
+    int32_t *err;
+    int T, H, E, k, P;     // P = T*k (rows of routed pairs; shared rows follow)
+};
+
+struct GemmParams {
+    int mode;              // 0 gate/up, 1 down, 2 router logits
+    const uint8_t *pool;
+    const uint8_t *shared_blob;
+    const int32_t *table_row;
+    uint64_t stride;
+    int64_t n_slots;
+    const uint16_t *x;     // [T][H]: fp16 copy for the expert GEMMs, bf16 for the router
+    const uint16_t *x_bf16;  // the caller's bf16 x (converted to fp16 into x by the path)
+    uint16_t *hbuf;        // [(P + T)][I] fp16
+    float *ypair;          // [(P + T)][H] fp32, weighted
+    const int32_t *pair_token;
+    const int32_t *pair_j;
+    const int32_t *ntiles;
+    const PfTile *tiles;
+    const float *w;
+    const float *gate;
+    const uint16_t *Wr;    // router rows (mode 2)
+    const uint16_t *ws;
+    float *logits;         // [T][E + 1] (mode 2)
+    int32_t *err;
+    int T, H, E, k, I, P;
+    int m_tiles;
+};
+
 // workspace carving (all offsets 256-byte aligned)
 struct Workspace {
     uint64_t route_counter, logits, fwd_counters, ypair, total;
+    // token-bucketed path (T > kDecodeMaxT)
+    uint64_t counts, chunk_base, offsets, tiles, ntiles, pair_token, pair_j, pair_pos, hbuf, ybuf, xh;
 };
 
 Workspace workspace_layout(const smoe_shape &s, int T);
@@ -104,6 +158,16 @@ cudaError_t route_config();
 cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
 cudaError_t launch_decode(const smoe_ctx *ctx, const DecodeParams &p, cudaStream_t st);
 cudaError_t decode_config(smoe_ctx *ctx);
+cudaError_t prefill_config();
+int prefill_max_tiles(int T, int k, int E);
+cudaError_t launch_router_gemm(const RouteParams &r, cudaStream_t st);
+cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g, cudaStream_t st, const cudaEvent_t *prof,
+                           int nprof);
+// records ev (if any) on st as an external event
+inline cudaError_t prof_record(cudaEvent_t ev, cudaStream_t st)
+{
+    return ev ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal) : cudaSuccess;
+}
 cudaError_t launch_pack_device(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst,
                                cudaStream_t st);
 void pack_host(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst);

@@ -126,15 +126,20 @@ class Stack:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph = None
 
-    def enqueue(self, stream=None):
+    def enqueue(self, stream=None, prof_events=None):
+        """prof_events: optional per-layer lists of events for the profiling hook."""
         p, inp = self.pool, self.inputs
         for l in range(p.n_layers):
             smoe.moe_route(p.ctx, inp.Wr[l], inp.ws[l], self.xs[l], self.ids[l], self.w[l], self.gate[l],
                            self.ws, logit_bias=inp.bias, stream=stream)
+            if prof_events is not None:
+                p.ctx.set_profile_events(prof_events[l])
             smoe.moe_forward(p.ctx, l, self.xs[l], self.ids[l], self.w[l], self.gate[l], p.pool, p.shared[l],
                              self.xs[l + 1], self.ws, self.err, residual=self.xs[l], stream=stream)
+        if prof_events is not None:
+            p.ctx.set_profile_events([])
 
-    def capture(self):
+    def capture(self, prof_events=None):
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
@@ -143,7 +148,8 @@ class Stack:
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            self.enqueue(s)
+            self.enqueue(s, prof_events)
         torch.cuda.synchronize()
-        self.graph = g
+        if prof_events is None:
+            self.graph = g
         return g
