@@ -4,6 +4,9 @@
 //     expert (per-chunk counts, one scan, an ordered scatter), plus the list of
 //     GEMM tiles: per expert, runs of up to 256 of its pairs; the shared
 //     expert takes all T tokens;
+//   row gather: x rows in expert order (the routed pairs, then all T tokens for
+//     the shared expert), converted to fp16, with each row's routing weight
+//     (or shared-expert gate), so that every GEMM tile reads contiguous rows;
 //   gate/up GEMM: per tile, 128 weight rows (64 gate + 64 up rows, interleaved
 //     in blocks of 8 as the blob stores them) x its tokens, K = H; the int4
 //     atoms are dequantised to bf16 in shared memory (128-byte swizzled,
@@ -21,22 +24,34 @@
 // Pages: the sparse MoE layer (xix.ai article, paragraph on how it works);
 // prefill as the slow part on the pages' hardware (paper-digest, Community
 // Reactions).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "smoe_dev.cuh"
 #include "smoe_internal.h"
 
 namespace smoe {
 
 constexpr int kPfM = 128;          // weight rows per tile
-constexpr int kPfK = 64;           // K per pipeline stage (one quantisation group)
+constexpr int kPfK = 64;           // K per pipeline step (one quantisation group)
 constexpr int kPfMaxN = 256;       // tokens per tile
-constexpr int kPfStages = 3;
-constexpr int kPfWorkers = 8;      // warps: B loads, A dequant, epilogue
-constexpr int kPfThreads = (kPfWorkers + 2) * 32;   // + producer warp + MMA warp
-constexpr int kPfRawBytes = 5120;  // 8 atoms (4608 B) rounded up to 1 KiB
+constexpr int kPfRaw = 6;          // raw int4 atom slots (one K step each)
+constexpr int kPfAB = 4;           // A/B operand stages
+constexpr int kPfBoxRows = 64;     // B rows per TMA box
+constexpr int kPfWorkers = 8;      // warps: A (dequantisation, or router rows)
+constexpr int kPfEpi = 8;          // warps: epilogue (two per TMEM lane quadrant)
+constexpr int kPfRawWarp = kPfWorkers + kPfEpi;   // bulk copies of the raw atoms
+constexpr int kPfBWarp = kPfRawWarp + 1;          // TMA row gathers of B
+constexpr int kPfMma = kPfBWarp + 1;              // tcgen05.mma issuer
+constexpr int kPfThreads = (kPfMma + 1) * 32;
+constexpr int kPfRawBytes = 8 * kAtomBytes;         // 4608: 8 row blocks x one group
 constexpr int kPfABytes = kPfM * kPfK * 2;          // 16 KiB
 constexpr int kPfBBytes = kPfMaxN * kPfK * 2;       // 32 KiB
-constexpr int kPfStageBytes = kPfRawBytes + kPfABytes + kPfBBytes;
-constexpr int kPfSmem = kPfStages * kPfStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kPfStageBytes = kPfABytes + kPfBBytes;
+constexpr int kPfSmem = kPfAB * kPfStageBytes + kPfRaw * kPfRawBytes + 1024 /*align*/ + 512 /*barriers*/;
+static_assert(kPfSmem <= 232448, "shared memory per CTA");
 constexpr int kBucketTok = 64;     // tokens per bucketing chunk
 
 __device__ __forceinline__ uint32_t sw128(int r, int c)   // byte offset of (row, col) in a 64-col bf16 tile
@@ -76,24 +91,17 @@ __device__ __forceinline__ uint16_t f32_to_f16_bits(float v)
     return r;
 }
 
-// x (bf16) -> fp16 for the expert GEMMs: exact for |x| < 65504 (and subnormal
-// below 2^-14, an absolute error under 3e-8); larger values set the error word.
-__global__ void __launch_bounds__(256) x_to_half_kernel(const uint16_t *x, uint16_t *xh, long long n8, int32_t *err)
+// tmem_ld32: 32 lanes x 32 consecutive 32-bit columns into 32 registers per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
-        const uint4 v = reinterpret_cast<const uint4 *>(x)[i];
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
-        bool bad = false;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float a = bf16lo(in[j]), b = bf16hi(in[j]);
-            bad |= !(fabsf(a) < 65504.f) || !(fabsf(b) < 65504.f);
-            o[j] = pack_f16x2(a, b);
-        }
-        if (bad) set_error(err, SMOE_DEV_RANGE);
-        reinterpret_cast<uint4 *>(xh)[i] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+                   "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+                   "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void umma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
@@ -109,15 +117,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
                  ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
-{
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-                 : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // 16-byte cp.async into shared memory; src_bytes 0 fills zeros.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes)
 {
@@ -126,14 +125,16 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ float silu_f(float v) { return v / (1.0f + __expf(-v)); }
+__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // ---------------------------------------------------------------- bucketing
+// counts and chunk_base are [E][chunks] (expert-major) so the scan reads each
+// expert's row with vector loads.
 
 __global__ void __launch_bounds__(256) bucket_count_kernel(const PrefillParams p)
 {
     __shared__ int cnt[1024];
-    const int c = blockIdx.x;
+    const int c = blockIdx.x, nch = gridDim.x;
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     const int t0 = c * kBucketTok, t1 = min(p.T, t0 + kBucketTok);
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(256) bucket_count_kernel(const PrefillParams p
         else set_error(p.err, SMOE_DEV_BAD_EXPERT);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < p.E; e += blockDim.x) p.counts[size_t(c) * p.E + e] = cnt[e];
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) p.counts[size_t(e) * nch + c] = cnt[e];
 }
 
 // One CTA: per-expert chunk prefixes, expert offsets, and the tile list.
@@ -154,12 +155,20 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
     const int e = threadIdx.x;
     const int nch = (p.T + kBucketTok - 1) / kBucketTok;
     int total = 0;
-    if (e < p.E)
-        for (int c = 0; c < nch; ++c) {
-            const int v = p.counts[size_t(c) * p.E + e];
-            p.chunk_base[size_t(c) * p.E + e] = total;
-            total += v;
+    if (e < p.E) {
+        const int *row = p.counts + size_t(e) * nch;
+        int *brow = p.chunk_base + size_t(e) * nch;
+        for (int c0 = 0; c0 < nch; c0 += 32) {       // 32 loads in flight, then the running sum
+            int v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = c0 + j < nch ? row[c0 + j] : 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (c0 + j < nch) brow[c0 + j] = total;
+                total += v[j];
+            }
         }
+    }
     const int nt = e < p.E ? (total + kPfMaxN - 1) / kPfMaxN : 0;
     buf[e] = e < p.E ? total : 0;
     tbuf[e] = nt;
@@ -174,12 +183,12 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
     const int start = buf[e] - (e < p.E ? total : 0);     // exclusive
     const int tstart = tbuf[e] - nt;
     if (e < p.E) {
-        p.offsets[e] = start;
-        for (int c = 0; c < nch; ++c) p.chunk_base[size_t(c) * p.E + e] += start;
+        p.offsets[e] = start;                         // the scatter adds it to the chunk prefixes
         for (int i = 0; i < nt; ++i) {
             PfTile tl;
             tl.kind = 0;
-            tl.expert = e;
+            const int64_t slot = p.table_row[e];
+            tl.slot = (slot < 0 || slot >= p.n_slots) ? -1 : int(slot);
             tl.p0 = start + i * kPfMaxN;
             tl.n = min(kPfMaxN, total - i * kPfMaxN);
             p.tiles[tstart + i] = tl;
@@ -193,7 +202,7 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
         for (int i = 0; i < nts; ++i) {
             PfTile tl;
             tl.kind = 1;
-            tl.expert = -1;
+            tl.slot = 0;
             tl.p0 = i * kPfMaxN;
             tl.n = min(kPfMaxN, p.T - i * kPfMaxN);
             p.tiles[ntr + i] = tl;
@@ -203,17 +212,21 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
 }
 
 // One warp per chunk: pairs in token order, each to its expert's next slot.
+// The chunk's ids are staged in shared memory first so the ordered loop only
+// touches shared memory.
 __global__ void __launch_bounds__(32) bucket_scatter_kernel(const PrefillParams p)
 {
     __shared__ int base[1024];
-    const int c = blockIdx.x, lane = threadIdx.x;
-    for (int e = lane; e < p.E; e += 32) base[e] = p.chunk_base[size_t(c) * p.E + e];
-    __syncwarp();
+    __shared__ int ids_s[kBucketTok * 16];
+    const int c = blockIdx.x, nch = gridDim.x, lane = threadIdx.x;
+    for (int e = lane; e < p.E; e += 32) base[e] = p.offsets[e] + p.chunk_base[size_t(e) * nch + c];
     const int t0 = c * kBucketTok, t1 = min(p.T, t0 + kBucketTok);
+    for (int q = t0 * p.k + lane; q < t1 * p.k; q += 32) ids_s[q - t0 * p.k] = p.ids[q];
+    __syncwarp();
     for (int t = t0; t < t1; ++t) {
         const int q = t * p.k + lane;
         const bool act = lane < p.k;
-        const int e = act ? p.ids[q] : -1;
+        const int e = act ? ids_s[q - t0 * p.k] : -1;
         const bool ok = act && e >= 0 && e < p.E;
         // lanes naming the same expert take consecutive slots in lane order
         const uint32_t same = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
@@ -231,77 +244,195 @@ __global__ void __launch_bounds__(32) bucket_scatter_kernel(const PrefillParams 
     }
 }
 
+// ------------------------------------------------------------ row gather
+// One warp per row of xs: row pos < P is pair pos (expert order), row P + t
+// is token t for the shared expert. xs = fp16(x row), exact for |x| < 65504
+// (subnormal below 2^-14, an absolute error under 3e-8); larger values set
+// the error word. pair_w = the pair's routing weight, or the token's gate.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const GemmParams g)
+{
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= g.P + g.T) return;
+    int tok;
+    if (row < g.P) {
+        tok = g.pair_token[row];
+        if (lane == 0) g.pair_w[row] = g.w[size_t(tok) * g.k + g.pair_j[row]];
+    } else {
+        tok = row - g.P;
+        if (lane == 0) g.pair_w[row] = g.gate[tok];
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(g.x_bf16 + size_t(tok) * g.H);
+    uint4 *dst = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(g.x) + size_t(row) * g.H);
+    bool bad = false;
+    for (int i = lane; i < g.H / 8; i += 32) {
+        const uint4 v = __ldg(src + i);
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = bf16lo(in[j]), b = bf16hi(in[j]);
+            bad |= !(fabsf(a) < 65504.f) || !(fabsf(b) < 65504.f);
+            o[j] = pack_f16x2(a, b);
+        }
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (bad) set_error(g.err, SMOE_DEV_RANGE);
+}
+
 // ---------------------------------------------------------- grouped GEMM
 
-// mode 0 gate/up, 1 down, 2 router logits. Tile = blockIdx.x / m_tiles.
-__global__ void __launch_bounds__(kPfThreads, 1) grouped_gemm_kernel(const GemmParams p)
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b)
 {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kPfStages * kPfStageBytes);
-    uint64_t *rawfull = bars, *afull = bars + kPfStages, *bfull = bars + 2 * kPfStages, *empty = bars + 3 * kPfStages;
-    uint64_t *accfull = bars + 4 * kPfStages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4 * kPfStages + 1);
+    uint32_t r;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nt = blockIdx.x / p.m_tiles, mt = blockIdx.x % p.m_tiles;
-    PfTile tl;
-    if (p.mode == 2) {
-        tl.kind = 1;
-        tl.expert = -1;
-        tl.p0 = nt * kPfMaxN;
-        tl.n = min(kPfMaxN, p.T - tl.p0);
-    } else {
-        if (nt >= *p.ntiles) return;                  // uniform: more tiles were launched than exist
-        tl = p.tiles[nt];
-    }
-    if (tl.n <= 0) return;
-    const int n = tl.n, N = (n + 15) & ~15;
-    const int K = p.mode == 1 ? p.I : p.H;
-    const int nk = K / kPfK;
-    const int ngH = p.H / kGroup, ngI = p.I / kGroup;
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
 
-    const uint8_t *blob = nullptr;
-    bool valid = true;
-    if (p.mode != 2) {
-        if (tl.kind == 1) {
-            blob = p.shared_blob;
-        } else {
-            const int64_t slot = p.table_row[tl.expert];
-            if (slot < 0 || slot >= p.n_slots) {
-                valid = false;
-                set_error(p.err, SMOE_DEV_BAD_SLOT);
-            } else {
-                blob = p.pool + uint64_t(slot) * p.stride;
+// fp16x2 (q_even, q_odd) of nibble pair m of a blob word: 0x6400 is 1024.0 in
+// fp16, whose unit in the last place is 1, so OR-ing the nibble in gives
+// 1024 + q and subtracting 1024 is exact.
+__device__ __forceinline__ uint32_t nib_pair_f16(uint32_t w, int m)
+{
+    uint32_t r;
+    const uint32_t v = w >> (4 * m);
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(0x000F000Fu), "r"(0x64006400u));
+    return hsub2(r, 0x64006400u);
+}
+
+// Bounded wait for the persistent GEMM: gives up after about one second of
+// global time, and once any wait of the CTA has given up (*abort set) every
+// later wait returns at once, so a failed CTA drains in bounded time.
+__device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int32_t *err, volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 0) {
+            if (*abort) return false;
+            uint64_t t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            if (t - t0 > 1000000000ull) {
+                *abort = 1;
+                set_error(err, SMOE_DEV_TIMEOUT);
+                return false;
             }
         }
     }
-    // rows of the B operand / outputs: routed pairs at p0.., shared tokens at P + p0..
-    const int rowbase = tl.kind == 1 ? p.P + tl.p0 : tl.p0;
+}
 
-    if (!valid) {                                     // contributes zeros
-        if (p.mode == 0) {
-            for (int i = tid; i < n * 64; i += kPfThreads)
-                p.hbuf[size_t(rowbase + i / 64) * p.I + mt * 64 + i % 64] = 0;
-        } else {
-            for (int i = tid; i < n * kPfM; i += kPfThreads)
-                p.ypair[size_t(rowbase + i / kPfM) * p.H + mt * kPfM + i % kPfM] = 0.f;
-        }
-        return;
+struct TileInfo {
+    int n, N, rowbase, p0, kind;
+    int slot;              // pool slot of the tile's expert (0 for the shared expert)
+    bool valid;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile)
+{
+    TileInfo t;
+    PfTile tl;
+    if (p.mode == 2) {
+        tl.kind = 1;
+        tl.slot = 0;
+        tl.p0 = tile * kPfMaxN;
+        tl.n = min(kPfMaxN, p.T - tl.p0);
+    } else {
+        tl = p.tiles[tile];
     }
+    t.n = tl.n;
+    t.N = (tl.n + 15) & ~15;
+    t.p0 = tl.p0;
+    t.kind = tl.kind;
+    t.rowbase = tl.kind == 1 ? p.P + tl.p0 : tl.p0;   // rows of B / outputs: pairs, then shared tokens
+    t.slot = tl.slot;
+    t.valid = p.mode == 2 || tl.slot >= 0;
+    return t;
+}
+
+// TMA load of a box (64 columns x kPfBoxRows rows) of a 2-D tensor map at
+// (column col, row row) into shared memory, 128-byte swizzled.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int col, int row, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(map), "r"(col), "r"(row), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// The raw atoms of one K step: 8 row blocks (8 mt .. 8 mt + 7) x one group,
+// one box {144 words, 8 row blocks, 1 slot} of the pool's 3-D tensor map
+// [slot][row block][group x 144 words] (no swizzle), 4608 bytes.
+__device__ __forceinline__ void tma_raw(uint32_t dst, const CUtensorMap *map, int kb, int mt, int slot, uint64_t *bar,
+                                        uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+                 ::"r"(dst), "l"(map), "r"(kb * (kAtomBytes / 4)), "r"(8 * mt), "r"(slot), "r"(smem_u32(bar)),
+                   "l"(policy)
+                 : "memory");
+}
+
+// Persistent: CTA b handles tiles b, b + grid, ... (tile = row-run x m_tiles
+// weight-row blocks); every role walks the same flattened sequence of K steps.
+// mode 0 gate/up (K = H), 1 down (K = I), 2 router logits (K = H).
+// Roles: 8 warps fill A (dequantising raw atoms, or copying router rows),
+// 8 warps run the epilogue, one warp streams raw atoms from HBM (amap: the
+// pool's gate/up or down atoms, amap_shared: the shared expert's), one loads
+// B rows with TMA (bmap: xs for mode 0, h for mode 1, x for mode 2; tile rows
+// rowbase ..), one issues MMAs.
+__global__ void __launch_bounds__(kPfThreads, 1) grouped_gemm_kernel(const GemmParams p,
+                                                                     const __grid_constant__ CUtensorMap bmap,
+                                                                     const __grid_constant__ CUtensorMap amap,
+                                                                     const __grid_constant__ CUtensorMap amap_shared)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *ab = smem;                                           // kPfAB x (A 16 KiB | B 32 KiB)
+    uint8_t *raw = smem + kPfAB * kPfStageBytes;                  // kPfRaw x 4608 B
+    uint64_t *bars = reinterpret_cast<uint64_t *>(raw + kPfRaw * kPfRawBytes);
+    uint64_t *rawfull = bars, *rawempty = bars + kPfRaw;
+    uint64_t *afull = bars + 2 * kPfRaw, *bfull = afull + kPfAB, *empty = bfull + kPfAB;
+    uint64_t *accfull = empty + kPfAB, *accempty = accfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accempty + 2);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nrun = p.mode == 2 ? (p.T + kPfMaxN - 1) / kPfMaxN : *p.ntiles;
+    const int ntiles = nrun * p.m_tiles;
+    const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
+    if (my_tiles == 0) return;                                    // uniform
+    const int K = p.mode == 1 ? p.I : p.H;
+    const int nk = K / kPfK;
+    const int total = my_tiles * nk;                              // K steps of this CTA
+    auto tile_of = [&](int i) { return int(blockIdx.x) + i * int(gridDim.x); };
 
     if (tid == 0) {
-        for (int s = 0; s < kPfStages; ++s) {
-            mbar_init(&rawfull[s], 1);
+        for (int r = 0; r < kPfRaw; ++r) {
+            mbar_init(&rawfull[r], 1);
+            mbar_init(&rawempty[r], kPfWorkers);
+        }
+        for (int s = 0; s < kPfAB; ++s) {
             mbar_init(&afull[s], kPfWorkers * 32);
-            mbar_init(&bfull[s], kPfWorkers * 32);
+            mbar_init(&bfull[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accfull, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accfull[b], 1);
+            mbar_init(&accempty[b], kPfEpi * 32);
+        }
+        *abort = 0;
         fence_mbar_init();
     }
-    if (warp == kPfWorkers + 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(tmem_slot)));
+    if (warp == kPfMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -309,182 +440,245 @@ __global__ void __launch_bounds__(kPfThreads, 1) grouped_gemm_kernel(const GemmP
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kPfWorkers) {
-        // ---- producer: raw int4 atoms (8 row blocks x one group) per stage
+    if (warp == kPfRawWarp) {
+        // ---- raw int4 atoms (8 row blocks x one group) per K step: one TMA box each
         if (lane == 0 && p.mode != 2) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&amap) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&amap_shared) : "memory");
             const uint64_t pol = policy_evict_first();
-            const uint64_t down_off = uint64_t(p.I / 8) * ngH * kAtomBytes;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % kPfStages;
-                if (kb >= kPfStages && !mbar_wait(&empty[s], ((kb / kPfStages) - 1) & 1, p.err)) break;
-                mbar_arrive_expect_tx(&rawfull[s], 8 * kAtomBytes);
-                uint8_t *raw = smem + s * kPfStageBytes;
-                for (int a = 0; a < 8; ++a) {
-                    const int rb = 8 * mt + a;
-                    const uint64_t atom = p.mode == 0 ? uint64_t(rb) * ngH + kb : down_off / kAtomBytes + uint64_t(rb) * ngI + kb;
-                    bulk_g2s(raw + a * kAtomBytes, blob + atom * kAtomBytes, kAtomBytes, &rawfull[s], pol);
+            TileInfo ti;
+            int gk = 0;
+            for (; gk < total; ++gk) {
+                const int i = gk / nk, kb = gk % nk, r = gk % kPfRaw;
+                if (kb == 0) ti = tile_info(p, tile_of(i) / p.m_tiles);
+                const int mt = tile_of(i) % p.m_tiles;
+                if (gk >= kPfRaw && !pf_wait(&rawempty[r], ((gk / kPfRaw) - 1) & 1, p.err, abort)) break;
+                if (!ti.valid) {
+                    mbar_arrive(&rawfull[r]);                  // nothing to load; the epilogue writes zeros
+                    continue;
                 }
+                mbar_arrive_expect_tx(&rawfull[r], kPfRawBytes);
+                tma_raw(smem_u32(raw + r * kPfRawBytes), ti.kind == 1 ? &amap_shared : &amap, kb, mt, ti.slot,
+                        &rawfull[r], pol);
+            }
+            // let the last copy into each slot land before the CTA can exit
+            for (int g2 = gk - 1; g2 >= 0 && g2 >= gk - kPfRaw; --g2)
+                mbar_wait(&rawfull[g2 % kPfRaw], (g2 / kPfRaw) & 1, p.err);
+        }
+    } else if (warp == kPfBWarp) {
+        // ---- B: rows rowbase .. rowbase + N - 1 of bmap, in boxes of kPfBoxRows rows
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&bmap) : "memory");
+            TileInfo ti;
+            for (int gk = 0; gk < total; ++gk) {
+                const int i = gk / nk, kb = gk % nk, s = gk % kPfAB;
+                if (kb == 0) ti = tile_info(p, tile_of(i) / p.m_tiles);
+                const int nbox = (ti.N + kPfBoxRows - 1) / kPfBoxRows;
+                if (gk >= kPfAB) pf_wait(&empty[s], ((gk / kPfAB) - 1) & 1, p.err, abort);
+                mbar_arrive_expect_tx(&bfull[s], uint32_t(nbox) * kPfBoxRows * (kPfK * 2));
+                const uint32_t dst = smem_u32(ab + s * kPfStageBytes + kPfABytes);
+                for (int j = 0; j < nbox; ++j)
+                    tma_load_2d(dst + j * (kPfBoxRows * kPfK * 2), &bmap, kb * kPfK, ti.rowbase + j * kPfBoxRows, &bfull[s]);
             }
         }
-    } else if (warp == kPfWorkers + 1) {
-        // ---- MMA issuer
+    } else if (warp == kPfMma) {
+        // ---- MMA issuer: tile i accumulates in TMEM buffer i % 2 (256 columns each)
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc(N, p.mode == 2);
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % kPfStages;
-                const uint32_t par = (kb / kPfStages) & 1;
-                if (!mbar_wait(&afull[s], par, p.err) || !mbar_wait(&bfull[s], par, p.err)) break;
+            uint32_t idesc = 0;
+            int nextN = tile_info(p, tile_of(0) / p.m_tiles).N;
+            for (int gk = 0; gk < total; ++gk) {
+                const int i = gk / nk, kb = gk % nk, s = gk % kPfAB, b = i & 1;
+                if (kb == 0) {
+                    idesc = umma_idesc(nextN, p.mode == 2);
+                    if (i + 1 < my_tiles) nextN = tile_info(p, tile_of(i + 1) / p.m_tiles).N;   // used one tile later
+                    if (i >= 2) pf_wait(&accempty[b], ((i / 2) - 1) & 1, p.err, abort);
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                }
+                const uint32_t par = (gk / kPfAB) & 1;
+                pf_wait(&afull[s], par, p.err, abort);
+                pf_wait(&bfull[s], par, p.err, abort);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint8_t *sa = smem + s * kPfStageBytes + kPfRawBytes;
-                const uint8_t *sb = sa + kPfABytes;
+                const uint8_t *sa = ab + s * kPfStageBytes, *sb = sa + kPfABytes;
                 const uint64_t ad = umma_desc(smem_u32(sa)), bd = umma_desc(smem_u32(sb));
+                const uint32_t acc_t = tmem + uint32_t(b * 256);
 #pragma unroll
                 for (int k4 = 0; k4 < kPfK / 16; ++k4)
-                    umma(tmem, ad + uint64_t(k4 * 2), bd + uint64_t(k4 * 2), idesc, (kb | k4) ? 1u : 0u);
+                    umma(acc_t, ad + uint64_t(k4 * 2), bd + uint64_t(k4 * 2), idesc, (kb | k4) ? 1u : 0u);
                 umma_commit(&empty[s]);
+                if (kb == nk - 1) umma_commit(&accfull[b]);
             }
-            umma_commit(accfull);
+            // the tensor cores are done with TMEM and shared memory before the CTA exits
+            mbar_wait(&accfull[(my_tiles - 1) & 1], ((my_tiles - 1) / 2) & 1, p.err);
         }
-    } else {
-        // ---- workers: B rows by cp.async, A by dequantisation (or cp.async for the router)
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kPfStages;
-            const uint32_t par = (kb / kPfStages) & 1;
-            if (kb >= kPfStages) mbar_wait(&empty[s], par ^ 1, p.err);
-            uint8_t *st = smem + s * kPfStageBytes;
-            uint8_t *sa = st + kPfRawBytes, *sb = sa + kPfABytes;
-            const uint32_t sb_u = smem_u32(sb), sa_u = smem_u32(sa);
-            for (int i = tid; i < N * 8; i += kPfWorkers * 32) {
-                const int r = i >> 3, c8 = i & 7;
-                const int rr = r < n ? r : 0;         // padded rows repeat row 0; their outputs are dropped
-                const uint16_t *src;
-                if (p.mode == 1) {
-                    src = p.hbuf + size_t(rowbase + rr) * p.I + kb * kPfK + c8 * 8;
-                } else {
-                    const int tok = tl.kind == 1 ? tl.p0 + rr : p.pair_token[tl.p0 + rr];
-                    src = p.x + size_t(tok) * p.H + kb * kPfK + c8 * 8;
-                }
-                cp_async16(sb_u + sw128(r, c8 * 8), src, 16);
-            }
-            if (p.mode == 2) {                        // A = router rows (row E is the shared-gate vector)
-                for (int i = tid; i < kPfM * 8; i += kPfWorkers * 32) {
-                    const int r = i >> 3, c8 = i & 7;
-                    const int e = mt * kPfM + r;
-                    const uint16_t *src = e < p.E ? p.Wr + size_t(e) * p.H : p.ws;
-                    cp_async16(sa_u + sw128(r, c8 * 8), src + kb * kPfK + c8 * 8, e <= p.E ? 16u : 0u);
-                }
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-            if (p.mode != 2) {
-                if (!mbar_wait(&rawfull[s], par, p.err)) { /* bounded; continue */ }
-                // lane-chunk `tid`: atom a, lane L -> rows (g, g+8) of row block a, 16 columns
-                const int a = tid >> 5, L = tid & 31, g = L >> 2, t = L & 3;
-                const uint8_t *atom = st + a * kAtomBytes;
-                const uint4 q = *reinterpret_cast<const uint4 *>(atom + 16 * L);
+    } else if (warp < kPfWorkers) {
+        if (p.mode != 2) {
+            // ---- A by dequantisation: warp a takes atom a (row block 8 mt + a);
+            // lane L = 4g + t holds rows (g, g + 8) x 16 columns of it
+            const int a = warp, g = lane >> 2, t = lane & 3;
+            for (int gk = 0; gk < total; ++gk) {
+                const int s = gk % kPfAB, r = gk % kPfRaw;
+                pf_wait(&rawfull[r], (gk / kPfRaw) & 1, p.err, abort);
+                const uint8_t *atom = raw + r * kPfRawBytes + a * kAtomBytes;
+                const uint4 q = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
                 const uint2 sbp = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rawempty[r]);
                 const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+                uint32_t o[4][4];
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    const int half = w & 1, hi = w >> 1;      // column half, row g or g+8
-                    const uint32_t sbw = hi ? sbp.y : sbp.x;
-                    const float sc = half_bits_to_f32(uint16_t(sbw & 0xffff));
-                    const float bp = fmaf(-128.f, sc, half_bits_to_f32(uint16_t(sbw >> 16)));
-                    uint32_t o[4];
+                    const uint32_t sbw = (w >> 1) ? sbp.y : sbp.x;   // fp16 (s, b) of row g or g + 8
+                    const uint32_t s2 = __byte_perm(sbw, 0, 0x1010), b2 = __byte_perm(sbw, 0, 0x3232);
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const uint32_t pr = nib_pair(words[w], m);   // (128 + q_even, 128 + q_odd)
-                        o[m] = pack_f16x2(fmaf(bf16lo(pr), sc, bp), fmaf(bf16hi(pr), sc, bp));
-                    }
-                    const int row = 16 * a + g + 8 * hi;
-                    *reinterpret_cast<uint4 *>(sa + sw128(row, 16 * t + 8 * half)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    for (int m = 0; m < 4; ++m) o[w][m] = hfma2(nib_pair_f16(words[w], m), s2, b2);   // s q + b, one rounding
+                }
+                if (gk >= kPfAB) pf_wait(&empty[s], ((gk / kPfAB) - 1) & 1, p.err, abort);
+                uint8_t *sa = ab + s * kPfStageBytes;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int row = 16 * a + g + 8 * (w >> 1);       // word w: column half w & 1, row g or g + 8
+                    *reinterpret_cast<uint4 *>(sa + sw128(row, 16 * t + 8 * (w & 1))) =
+                        make_uint4(o[w][0], o[w][1], o[w][2], o[w][3]);
                 }
                 fence_async_smem();
                 mbar_arrive(&afull[s]);
             }
-            if (kb >= 1) {                            // the previous stage's cp.async data is complete
-                asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            // ---- A = router rows (row E: the shared-gate vector; rows past E zero), one step ahead
+            auto issue_a = [&](int gi) {
+                if (gi < total) {
+                    const int i = gi / nk, kb = gi % nk, s = gi % kPfAB;
+                    if (gi >= kPfAB) pf_wait(&empty[s], ((gi / kPfAB) - 1) & 1, p.err, abort);
+                    const int mt = tile_of(i) % p.m_tiles;
+                    const uint32_t sa_u = smem_u32(ab + s * kPfStageBytes);
+                    for (int q = tid; q < kPfM * 8; q += kPfWorkers * 32) {
+                        const int r = q >> 3, c8 = q & 7;
+                        const int e = mt * kPfM + r;
+                        const uint16_t *src = e < p.E ? p.Wr + size_t(e) * p.H : p.ws;
+                        cp_async16(sa_u + sw128(r, c8 * 8), src + kb * kPfK + c8 * 8, e <= p.E ? 16u : 0u);
+                    }
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");   // one group per step, even if empty
+            };
+            issue_a(0);
+            for (int gk = 0; gk < total; ++gk) {
+                issue_a(gk + 1);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");  // this step's rows have landed
                 fence_async_smem();
-                const int sp = (kb - 1) % kPfStages;
-                if (p.mode == 2) mbar_arrive(&afull[sp]);
-                mbar_arrive(&bfull[sp]);
+                mbar_arrive(&afull[gk % kPfAB]);
             }
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
         }
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        fence_async_smem();
-        if (p.mode == 2) mbar_arrive(&afull[(nk - 1) % kPfStages]);
-        mbar_arrive(&bfull[(nk - 1) % kPfStages]);
-
-        // ---- epilogue: TMEM lanes = tile rows, columns = tokens of the tile
-        mbar_wait(accfull, 0, p.err);
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const int q = warp & 3, colhalf = warp >> 2;
+    } else {
+        // ---- epilogue warps: warp e reads TMEM lanes 32q..32q+31 (q = e % 4, the
+        // quadrant its warp index allows) = tile rows, column chunks of 32 tokens
+        // j = 2u + e / 4
+        const int e = warp - kPfWorkers, q = e & 3, half = e >> 2;
         const int r = 32 * q + lane;
-        for (int c16 = colhalf; c16 < N / 16; c16 += 2) {
-            uint32_t v[16];
-            tmem_ld16(tmem + (uint32_t(32 * q) << 16) + uint32_t(c16 * 16), v);
-            if (p.mode == 0) {
-                const bool gate_row = (lane & 8) == 0;
-                const int inter = 64 * mt + 8 * (r >> 4) + (r & 7);
+        bool range_bad = false;
+        // mode 1: weight of column 32 j + lane; the next tile's are loaded one tile ahead
+        auto weights = [&](const TileInfo &t, float (&wv)[4]) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float gv = __uint_as_float(v[j]);
-                    const float uv = __shfl_xor_sync(0xffffffffu, gv, 8);
-                    const int c = c16 * 16 + j;
-                    if (gate_row && c < n) {
-                        const float h = silu_f(gv) * uv;
-                        if (!(fabsf(h) < 65504.f)) set_error(p.err, SMOE_DEV_RANGE);
-                        p.hbuf[size_t(rowbase + c) * p.I + inter] = f32_to_f16_bits(h);
-                    }
-                }
-            } else if (p.mode == 1) {
-                const int R = kPfM * mt + r;
+            for (int u = 0; u < 4; ++u) {
+                const int c = 32 * (2 * u + half) + lane;
+                wv[u] = (p.mode == 1 && c < t.n) ? p.pair_w[t.rowbase + c] : 0.f;
+            }
+        };
+        TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
+        float wnext[4];
+        weights(tnext, wnext);
+        for (int i = 0; i < my_tiles; ++i) {
+            const int b = i & 1;
+            const TileInfo ti = tnext;
+            float wv[4] = {wnext[0], wnext[1], wnext[2], wnext[3]};
+            const int mt = tile_of(i) % p.m_tiles;
+            if (i + 1 < my_tiles) {
+                tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
+                weights(tnext, wnext);
+            }
+            pf_wait(&accfull[b], (i / 2) & 1, p.err, abort);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (!ti.valid) set_error(p.err, SMOE_DEV_BAD_SLOT);
+            const float keep = ti.valid ? 1.f : 0.f;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c = c16 * 16 + j;
-                    if (c < n) {
-                        float wt;
-                        if (tl.kind == 1) {
-                            wt = p.gate[tl.p0 + c];
-                        } else {
-                            const int pp = tl.p0 + c;
-                            wt = p.w[size_t(p.pair_token[pp]) * p.k + p.pair_j[pp]];
+            for (int u = 0; u < 4; ++u) {
+                const int j = 2 * u + half;
+                if (32 * j < ti.N) {                      // uniform over the warp
+                    uint32_t v[32];
+                    tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(b * 256 + 32 * j), v);
+                    if (p.mode == 0) {
+                        // rows r (gate) and r ^ 8 (up) of one intermediate unit: per column
+                        // pair the gate lane takes the even column, the up lane the odd one
+                        const bool gate_row = (lane & 8) == 0;
+                        const int inter = 64 * mt + 8 * (r >> 4) + (r & 7);
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj += 2) {
+                            const float a0 = __uint_as_float(v[jj]) * keep, a1 = __uint_as_float(v[jj + 1]) * keep;
+                            const float other = __shfl_xor_sync(0xffffffffu, gate_row ? a1 : a0, 8);
+                            const float gv = gate_row ? a0 : other, uv = gate_row ? other : a1;
+                            const int c = 32 * j + jj + (gate_row ? 0 : 1);
+                            const float h = silu_f(gv) * uv;
+                            if (c < ti.n) {
+                                range_bad |= !(fabsf(h) < 65504.f);
+                                p.hbuf[size_t(ti.rowbase + c) * p.I + inter] = f32_to_f16_bits(h);
+                            }
                         }
-                        p.ypair[size_t(rowbase + c) * p.H + R] = __uint_as_float(v[j]) * wt;
-                    }
-                }
-            } else {
-                const int e = kPfM * mt + r;
+                    } else if (p.mode == 1) {
+                        const int R = kPfM * mt + r;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c = c16 * 16 + j;
-                    if (c < n && e <= p.E) p.logits[size_t(tl.p0 + c) * (p.E + 1) + e] = __uint_as_float(v[j]);
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const int c = 32 * j + jj;
+                            const float wt = __shfl_sync(0xffffffffu, wv[u], jj);
+                            if (c < ti.n) {
+                                const float y = __uint_as_float(v[jj]) * keep * wt;
+                                range_bad |= !(fabsf(y) < 65504.f);
+                                p.ypair[size_t(ti.rowbase + c) * p.H + R] = f32_to_f16_bits(y);
+                            }
+                        }
+                    } else {
+                        const int ex = kPfM * mt + r;
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const int c = 32 * j + jj;
+                            if (c < ti.n && ex <= p.E) p.logits[size_t(ti.p0 + c) * (p.E + 1) + ex] = __uint_as_float(v[jj]);
+                        }
+                    }
                 }
             }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            mbar_arrive(&accempty[b]);
         }
+        if (range_bad) set_error(p.err, SMOE_DEV_RANGE);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (warp == kPfWorkers + 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+    if (warp == kPfMma)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
 }
 
 // ---------------------------------------------------------------- combine
 
-// out[t] = sum_j ypair[pos(t, j)] (route order) + ypair[P + t] (+ residual).
+// out[t] = sum_j ypair[pos(t, j)] (route order) + ypair[P + t] (+ residual),
+// from the fp16 weighted pair outputs, summed in fp32.
 __global__ void __launch_bounds__(256) combine_kernel(const PrefillParams p)
 {
     const int t = blockIdx.y;
     const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (c >= p.H) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](int row) {
+        const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(p.ypair + size_t(row) * p.H + c));
+        float2 a, b;
+        asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}" : "=f"(a.x), "=f"(a.y) : "r"(v.x));
+        asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}" : "=f"(b.x), "=f"(b.y) : "r"(v.y));
+        acc.x += a.x; acc.y += a.y; acc.z += b.x; acc.w += b.y;
+    };
     for (int j = 0; j < p.k; ++j) {
         const int pos = p.pair_pos[size_t(t) * p.k + j];
-        if (pos < 0) continue;
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.ypair + size_t(pos) * p.H + c));
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        if (pos >= 0) add(pos);
     }
-    const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.ypair + size_t(p.P + t) * p.H + c));
-    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    add(p.P + t);
     if (p.residual) {
         const uint2 r = *reinterpret_cast<const uint2 *>(p.residual + size_t(t) * p.H + c);
         acc.x += bf16lo(r.x); acc.y += bf16hi(r.x); acc.z += bf16lo(r.y); acc.w += bf16hi(r.y);
@@ -501,6 +695,69 @@ cudaError_t prefill_config()
 
 int prefill_max_tiles(int T, int k, int E) { return (T * k + kPfMaxN - 1) / kPfMaxN + E + (T + kPfMaxN - 1) / kPfMaxN; }
 
+static int g_num_sms = 0;
+
+static int persistent_grid(int max_tiles)
+{
+    if (g_num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 1;
+    }
+    return max_tiles < g_num_sms ? (max_tiles > 0 ? max_tiles : 1) : g_num_sms;
+}
+
+// Tensor map of a row-major [rows][cols] 16-bit matrix for the B operand:
+// box 64 columns x kPfBoxRows rows, 128-byte swizzle (the MMA operand layout);
+// rows past the end read as zeros.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return encode;
+}
+
+// Tensor map of the raw atoms of a pool region as [slot][row block][group x
+// 144 words]: base = the pool (or shared blob) plus the region's offset, row
+// blocks atom_rows apart (groups x 576 bytes), slots `stride` bytes apart.
+static cudaError_t atoms_map(CUtensorMap *m, const void *base, int groups, int row_blocks, int64_t n_slots,
+                             uint64_t stride)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {uint64_t(groups) * (kAtomBytes / 4), uint64_t(row_blocks), uint64_t(n_slots)};
+    const cuuint64_t strides[2] = {uint64_t(groups) * kAtomBytes, stride};
+    const cuuint32_t box[3] = {kAtomBytes / 4, 8, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+static cudaError_t rows_map(CUtensorMap *m, const void *base, bool bf16, uint64_t cols, uint64_t rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {uint32_t(kPfK), uint32_t(kPfBoxRows)};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                              const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_router_gemm(const RouteParams &r, cudaStream_t st)
 {
     GemmParams g = {};
@@ -515,8 +772,11 @@ cudaError_t launch_router_gemm(const RouteParams &r, cudaStream_t st)
     g.E = r.E;
     g.k = r.k;
     g.m_tiles = (r.E + 1 + kPfM - 1) / kPfM;
+    CUtensorMap xmap;
+    cudaError_t e = rows_map(&xmap, r.x, true, uint64_t(r.H), uint64_t(r.T));
+    if (e != cudaSuccess) return e;
     const int ntile = (r.T + kPfMaxN - 1) / kPfMaxN;
-    grouped_gemm_kernel<<<ntile * g.m_tiles, kPfThreads, kPfSmem, st>>>(g);
+    grouped_gemm_kernel<<<persistent_grid(ntile * g.m_tiles), kPfThreads, kPfSmem, st>>>(g, xmap, xmap, xmap);
     return cudaGetLastError();
 }
 
@@ -524,22 +784,32 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
                            int nprof)
 {
     const int nch = (p.T + kBucketTok - 1) / kBucketTok;
-    const long long n8 = (long long)p.T * p.H / 8;
-    x_to_half_kernel<<<unsigned(n8 / 256 + 1 < 4096 ? n8 / 256 + 1 : 4096), 256, 0, st>>>(g0.x_bf16, const_cast<uint16_t *>(g0.x), n8, p.err);
+    CUtensorMap xmap, hmap;
+    cudaError_t e = rows_map(&xmap, g0.x, false, uint64_t(p.H), uint64_t(p.P + p.T));
+    if (e != cudaSuccess) return e;
+    if ((e = rows_map(&hmap, g0.hbuf, false, uint64_t(g0.I), uint64_t(p.P + p.T))) != cudaSuccess) return e;
+    // raw atoms: gate/up region [I/8 row blocks][H/64 groups], down region [H/16][I/64] at I/8 x H/64 atoms
+    const uint64_t down_off = uint64_t(g0.I / 8) * (p.H / kGroup) * kAtomBytes;
+    const uint8_t *shared_down = g0.shared_blob + down_off, *pool_down = g0.pool + down_off;
+    CUtensorMap gu_pool, gu_shared, dn_pool, dn_shared;
+    if ((e = atoms_map(&gu_pool, g0.pool, p.H / kGroup, g0.I / 8, g0.n_slots, g0.stride)) != cudaSuccess) return e;
+    if ((e = atoms_map(&gu_shared, g0.shared_blob, p.H / kGroup, g0.I / 8, 1, g0.stride)) != cudaSuccess) return e;
+    if ((e = atoms_map(&dn_pool, pool_down, g0.I / kGroup, p.H / 16, g0.n_slots, g0.stride)) != cudaSuccess) return e;
+    if ((e = atoms_map(&dn_shared, shared_down, g0.I / kGroup, p.H / 16, 1, g0.stride)) != cudaSuccess) return e;
     bucket_count_kernel<<<nch, 256, 0, st>>>(p);
     bucket_scan_kernel<<<1, 1024, 0, st>>>(p);
     bucket_scatter_kernel<<<nch, 32, 0, st>>>(p);
+    gather_rows_kernel<<<(p.P + p.T + 7) / 8, 256, 0, st>>>(g0);
     const int maxt = prefill_max_tiles(p.T, p.k, p.E);
     GemmParams g = g0;
     g.mode = 0;
     g.m_tiles = g.I / 64;
-    cudaError_t e = prof_record(nprof > 0 ? prof[0] : nullptr, st);
-    if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<<<maxt * g.m_tiles, kPfThreads, kPfSmem, st>>>(g);
+    if ((e = prof_record(nprof > 0 ? prof[0] : nullptr, st)) != cudaSuccess) return e;
+    grouped_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kPfThreads, kPfSmem, st>>>(g, xmap, gu_pool, gu_shared);
     if ((e = prof_record(nprof > 1 ? prof[1] : nullptr, st)) != cudaSuccess) return e;
     g.mode = 1;
     g.m_tiles = p.H / kPfM;
-    grouped_gemm_kernel<<<maxt * g.m_tiles, kPfThreads, kPfSmem, st>>>(g);
+    grouped_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kPfThreads, kPfSmem, st>>>(g, hmap, dn_pool, dn_shared);
     if ((e = prof_record(nprof > 2 ? prof[2] : nullptr, st)) != cudaSuccess) return e;
     combine_kernel<<<dim3((p.H / 4 + 255) / 256, p.T), 256, 0, st>>>(p);
     return cudaGetLastError();

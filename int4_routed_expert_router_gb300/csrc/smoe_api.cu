@@ -148,8 +148,9 @@ Workspace workspace_layout(const smoe_shape &s, int T)
         w.pair_j = o;     o = al(o + P * 4);
         w.pair_pos = o;   o = al(o + P * 4);
         w.hbuf = o;       o = al(o + (P + T) * s.I * 2);
-        w.ybuf = o;       o = al(o + (P + T) * s.H * 4);
-        w.xh = o;         o = al(o + uint64_t(T) * s.H * 2);
+        w.ybuf = o;       o = al(o + (P + T) * s.H * 2);
+        w.xh = o;         o = al(o + (P + T) * s.H * 2);
+        w.pair_w = o;     o = al(o + (P + T) * 4);
     }
     w.total = o;
     return w;
@@ -332,10 +333,12 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
         q.offsets = reinterpret_cast<int32_t *>(ws + W.offsets);
         q.tiles = reinterpret_cast<PfTile *>(ws + W.tiles);
         q.ntiles = reinterpret_cast<int32_t *>(ws + W.ntiles);
+        q.table_row = ctx->table_dev + size_t(layer) * ctx->shape.E;
+        q.n_slots = ctx->n_slots;
         q.pair_token = reinterpret_cast<int32_t *>(ws + W.pair_token);
         q.pair_j = reinterpret_cast<int32_t *>(ws + W.pair_j);
         q.pair_pos = reinterpret_cast<int32_t *>(ws + W.pair_pos);
-        q.ypair = reinterpret_cast<float *>(ws + W.ybuf);
+        q.ypair = reinterpret_cast<const uint16_t *>(ws + W.ybuf);
         q.residual = residual;
         q.out = out;
         q.err = err;
@@ -353,7 +356,8 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
         g.x = reinterpret_cast<const uint16_t *>(ws + W.xh);
         g.x_bf16 = x;
         g.hbuf = reinterpret_cast<uint16_t *>(ws + W.hbuf);
-        g.ypair = reinterpret_cast<float *>(ws + W.ybuf);
+        g.pair_w = reinterpret_cast<float *>(ws + W.pair_w);
+        g.ypair = reinterpret_cast<uint16_t *>(ws + W.ybuf);
         g.pair_token = q.pair_token;
         g.pair_j = q.pair_j;
         g.ntiles = q.ntiles;

@@ -97,7 +97,7 @@ struct DecodeParams {
 
 struct PfTile {
     int32_t kind;     // 0: run of an expert's pairs; 1: run of tokens for the shared expert
-    int32_t expert;
+    int32_t slot;     // pool slot of the expert (kind 0; -1 if the slot table entry is out of range), else 0
     int32_t p0;       // first pair (kind 0) or first token (kind 1)
     int32_t n;        // rows in the run (<= 256)
 };
@@ -105,15 +105,17 @@ struct PfTile {
 // Token-bucketed path (T > 8): bucketing and combine.
 struct PrefillParams {
     const int32_t *ids;
-    int32_t *counts;       // [chunks][E]
-    int32_t *chunk_base;   // [chunks][E]
+    int32_t *counts;       // [E][chunks]
+    int32_t *chunk_base;   // [E][chunks]
     int32_t *offsets;      // [E + 1]
     PfTile *tiles;         // [max tiles]
     int32_t *ntiles;
+    const int32_t *table_row;  // the layer's slot table row [E]
+    int64_t n_slots;
     int32_t *pair_token;   // [T*k]
     int32_t *pair_j;       // [T*k]
     int32_t *pair_pos;     // [T*k] position of pair (t, j) in expert order, -1 if invalid
-    const float *ypair;    // [(T*k + T)][H]
+    const uint16_t *ypair; // [(T*k + T)][H] fp16, weighted
     const uint16_t *residual;
     uint16_t *out;
     int32_t *err;
@@ -127,10 +129,11 @@ struct GemmParams {
     const int32_t *table_row;
     uint64_t stride;
     int64_t n_slots;
-    const uint16_t *x;     // [T][H]: fp16 copy for the expert GEMMs, bf16 for the router
-    const uint16_t *x_bf16;  // the caller's bf16 x (converted to fp16 into x by the path)
+    const uint16_t *x;     // expert GEMMs: xs [(P + T)][H] fp16 rows in expert order; router: x [T][H] bf16
+    const uint16_t *x_bf16;  // the caller's bf16 x (gathered and converted into xs by the path)
+    float *pair_w;         // [(P + T)] routing weight of each xs row (shared rows: the gate)
     uint16_t *hbuf;        // [(P + T)][I] fp16
-    float *ypair;          // [(P + T)][H] fp32, weighted
+    uint16_t *ypair;       // [(P + T)][H] fp16, weighted
     const int32_t *pair_token;
     const int32_t *pair_j;
     const int32_t *ntiles;
@@ -149,7 +152,7 @@ struct GemmParams {
 struct Workspace {
     uint64_t route_counter, logits, fwd_counters, ypair, total;
     // token-bucketed path (T > kDecodeMaxT)
-    uint64_t counts, chunk_base, offsets, tiles, ntiles, pair_token, pair_j, pair_pos, hbuf, ybuf, xh;
+    uint64_t counts, chunk_base, offsets, tiles, ntiles, pair_token, pair_j, pair_pos, hbuf, ybuf, xh, pair_w;
 };
 
 Workspace workspace_layout(const smoe_shape &s, int T);

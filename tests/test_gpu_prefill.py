@@ -1,9 +1,10 @@
 """GPU parity of the token-bucketed path (T > 8): bucketing, tcgen05 grouped
 gate/up and down GEMMs, ordered combine, and the tensor-core router.
 
-Weights are dequantised to bf16 tiles and h is bf16 (fp32 accumulation), so
-only the layer tolerance applies (relative L2 <= 5e-3, max abs <= 2e-2 rms
-against the oracle's fp64 output)."""
+Weights are dequantised to fp16 tiles (one rounding of s q + b), x and h
+are fp16, products accumulate in fp32 and the weighted pair outputs are
+stored as fp16, so only the layer tolerance applies (relative L2 <= 5e-3,
+max abs <= 2e-2 rms against the oracle's fp64 output)."""
 import numpy as np
 import pytest
 import torch
