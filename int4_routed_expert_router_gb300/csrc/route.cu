@@ -23,6 +23,14 @@ namespace smoe {
 constexpr int kRouteRows = 8;
 constexpr int kRouteToks = 8;
 
+// Bytes of the route kernel's main shared-memory region: the staged rows and
+// tokens, reused for the T x (E + 1) logits of the top-k.
+__host__ __device__ inline int route_region_bytes(int H, int E, int T)
+{
+    const int a = (kRouteRows + kRouteToks) * H * 2, b = T * (E + 1) * 4;
+    return ((a > b ? a : b) + 15) & ~15;
+}
+
 __device__ __forceinline__ void bulk_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -70,7 +78,8 @@ __device__ void warp_topk(uint32_t (&key)[PER], int32_t (&id)[PER], int k, uint3
     }
 }
 
-// Level 1 for one token slice: values z[e] (+bias) for e in [e0, e1).
+// Level 1 for one token slice: values z[e] (+bias) for e in [e0, e1); z may be
+// global (read through L2) or a shared-memory copy.
 template <int PER>
 __device__ void slice_topk(const float *z, const float *bias, int e0, int e1, int k, uint32_t *okey, int32_t *oid,
                            int lane)
@@ -83,7 +92,7 @@ __device__ void slice_topk(const float *z, const float *bias, int e0, int e1, in
         key[j] = 0u;
         id[j] = 0x7fffffff;
         if (e < e1) {
-            key[j] = fkey(__ldcg(z + e) + (bias ? bias[e] : 0.f));
+            key[j] = fkey(z[e] + (bias ? bias[e] : 0.f));
             id[j] = e;
         }
     }
@@ -101,30 +110,33 @@ __device__ void slice_topk_any(int per, const float *z, const float *bias, int e
     else slice_topk<32>(z, bias, e0, e1, k, ok, oi, lane);
 }
 
-// Final weights of one token from its k chosen keys (descending).
-__device__ void write_choice(const RouteParams &p, int t, const uint32_t *fk, const int32_t *fi)
+// Final weights of one token from its k chosen keys (descending), one lane per
+// choice (k <= 16); zs: the token's shared-gate logit. The denominator is
+// summed in choice order on every lane, so all lanes agree bit for bit.
+__device__ void write_choice(const RouteParams &p, int t, const uint32_t *fk, const int32_t *fi, float zs, int lane)
 {
     const float zmax = fkey_inv(fk[0]);
-    float ex[16], den = 0.f;
-    for (int s = 0; s < p.k; ++s) {
-        ex[s] = expf(fkey_inv(fk[s]) - zmax);
-        den += ex[s];
+    float den = 0.f;
+    for (int s = 0; s < p.k; ++s) den += expf(fkey_inv(fk[s]) - zmax);
+    if (lane < p.k) {
+        p.ids[size_t(t) * p.k + lane] = fi[lane];
+        p.w[size_t(t) * p.k + lane] = expf(fkey_inv(fk[lane]) - zmax) / den;
     }
-    for (int s = 0; s < p.k; ++s) {
-        p.ids[size_t(t) * p.k + s] = fi[s];
-        p.w[size_t(t) * p.k + s] = ex[s] / den;
-    }
-    p.gate[t] = 1.0f / (1.0f + expf(-__ldcg(p.logits + size_t(t) * (p.E + 1) + p.E)));
+    if (lane == 0) p.gate[t] = 1.0f / (1.0f + expf(-zs));
 }
 
 // Top-k of T <= 8 tokens by the 8 warps of a CTA (the CTA that finishes the
-// logits last). Each token gets 8/T' warps (T' = T rounded up to a power of
-// two); each of them takes a slice of the experts (level 1), then one warp
-// merges the slices' candidates (level 2). ckey/cid: 2 * 8 * 16 entries.
-__device__ void block_topk(const RouteParams &p, uint32_t *ckey, int32_t *cid)
+// logits last). The T x (E + 1) logits are first copied to shared memory by
+// all threads (one round trip to L2). Each token gets 8/T' warps (T' = T
+// rounded up to a power of two); each of them takes a slice of the experts
+// (level 1), then one warp merges the slices' candidates (level 2).
+// ckey/cid: 2 * 8 * 16 entries; zsm: T * (E + 1) floats.
+__device__ void block_topk(const RouteParams &p, uint32_t *ckey, int32_t *cid, float *zsm)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = p.T, E = p.E, k = p.k;
+    for (int i = threadIdx.x; i < T * (E + 1); i += blockDim.x) zsm[i] = __ldcg(p.logits + i);
+    __syncthreads();
     int tp = 1;
     while (tp < T) tp <<= 1;
     const int wpt = 8 / tp;                     // warps per token
@@ -132,8 +144,8 @@ __device__ void block_topk(const RouteParams &p, uint32_t *ckey, int32_t *cid)
     if (t < T) {
         const int span = (E + wpt - 1) / wpt;
         const int e0 = sl * span, e1 = min(E, e0 + span);
-        slice_topk_any((span + 31) / 32, p.logits + size_t(t) * (E + 1), p.bias, e0, e1, k, ckey + warp * 16,
-                       cid + warp * 16, lane);
+        slice_topk_any((span + 31) / 32, zsm + t * (E + 1), p.bias, e0, e1, k, ckey + warp * 16, cid + warp * 16,
+                       lane);
     }
     __syncthreads();
     if (t < T && sl == 0) {
@@ -151,7 +163,7 @@ __device__ void block_topk(const RouteParams &p, uint32_t *ckey, int32_t *cid)
         int32_t *fi = cid + 8 * 16 + warp * 16;
         warp_topk<4>(key, id, k, fk, fi, lane);
         __syncwarp();
-        if (lane == 0) write_choice(p, t, fk, fi);
+        write_choice(p, t, fk, fi, zsm[t * (E + 1) + E], lane);
     }
 }
 
@@ -159,9 +171,10 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const RouteParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int H = p.H, E = p.E, T = p.T;
+    // [router rows 8 x H | tokens 8 x H], later the logits for the top-k; barriers last
     uint16_t *wrow = reinterpret_cast<uint16_t *>(smem);                 // [8][H]
     uint16_t *xs = wrow + kRouteRows * H;                                 // [8][H]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(xs + kRouteToks * H);  // [2]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + route_region_bytes(H, E, T));   // [2]
     __shared__ int last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row0 = blockIdx.x * kRouteRows, tok0 = blockIdx.y * kRouteToks;
@@ -216,16 +229,14 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const RouteParams p)
 
     __syncthreads();
     if (tid == 0) {
-        __threadfence();
         const uint32_t n = gridDim.x * gridDim.y;
-        last = (atomicAdd(p.counter, 1u) == n - 1) ? 1 : 0;
+        last = (ticket_add(p.counter, 1u) == n - 1) ? 1 : 0;
     }
     __syncthreads();
     if (!last) return;
-    __threadfence();
     __shared__ uint32_t ckey[2 * 8 * 16];
     __shared__ int32_t cid[2 * 8 * 16];
-    block_topk(p, ckey, cid);
+    block_topk(p, ckey, cid, reinterpret_cast<float *>(wrow));   // the router rows are no longer needed
     if (tid == 0) atomicExch(p.counter, 0u);
 }
 
@@ -242,13 +253,13 @@ __global__ void __launch_bounds__(256) topk_kernel(const RouteParams p)
     slice_topk_any((p.E + 31) / 32, p.logits + size_t(t) * (p.E + 1), p.bias, 0, p.E, p.k, ckey + warp * 16,
                    cid + warp * 16, lane);
     __syncwarp();
-    if (lane == 0) write_choice(p, t, ckey + warp * 16, cid + warp * 16);
+    write_choice(p, t, ckey + warp * 16, cid + warp * 16, __ldcg(p.logits + size_t(t) * (p.E + 1) + p.E), lane);
 }
 
 cudaError_t route_config()
 {
     return cudaFuncSetAttribute(route_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (kRouteRows + kRouteToks) * 4096 * 2 + 16);
+                                route_region_bytes(2048, 1024, kDecodeMaxT) + 16);
 }
 
 cudaError_t launch_route(const RouteParams &p0, cudaStream_t st)
@@ -261,7 +272,7 @@ cudaError_t launch_route(const RouteParams &p0, cudaStream_t st)
         return cudaGetLastError();
     }
     p.fused_topk = 1;
-    const int smem = (kRouteRows + kRouteToks) * p.H * 2 + 16;
+    const int smem = route_region_bytes(p.H, p.E, p.T) + 16;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((p.E + 1 + kRouteRows - 1) / kRouteRows, (p.T + kRouteToks - 1) / kRouteToks);
     lc.blockDim = dim3(256);

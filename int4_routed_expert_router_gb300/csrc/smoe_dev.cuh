@@ -139,6 +139,16 @@ __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr)
     return v;
 }
 
+// Arrival ticket: atomic add with acquire-release semantics at GPU scope. The
+// caller's CTA barrier before it makes the CTA's earlier writes part of the
+// release; the barrier after it extends the acquire to the whole CTA.
+__device__ __forceinline__ uint32_t ticket_add(uint32_t *ctr, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(ctr), "r"(v) : "memory");
+    return old;
+}
+
 // ------------------------------------------------- programmatic dependent launch
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
