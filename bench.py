@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (profiling of small cases)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="stack", choices=["stack", "layers"],
+                    help="one-token steps: one moe_decode_stack launch (default) or moe_route + moe_forward per layer")
     return ap.parse_args()
 
 
@@ -132,6 +134,26 @@ def src_hash(files):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+STACK_SOURCES = ["int4_routed_expert_router_gb300/csrc/decode_stack.cu",
+                 "int4_routed_expert_router_gb300/csrc/decode_common.cuh",
+                 "int4_routed_expert_router_gb300/csrc/route_common.cuh",
+                 "int4_routed_expert_router_gb300/csrc/smoe_dev.cuh",
+                 "int4_routed_expert_router_gb300/csrc/smoe_internal.h"]
+
+
+def stack_traffic(workload: str):
+    """DRAM bytes per launch of the stack kernel from the committed ncu
+    summary, only if its sources are unchanged since it was taken."""
+    p = os.path.join(ROOT, "profiles", "decode_stack_kernel_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_sha256") != src_hash(STACK_SOURCES) or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_launch")
 
 
 def recorded_traffic(workload: str):
@@ -275,7 +297,9 @@ def run_ours(args, wl, world, rank, dist):
     torch.cuda.set_device(dev)
     pool = W.DevicePool(wl)
     inp = W.LayerInputs(wl, wl.n_layers)
-    st = W.Stack(pool, inp, wl.T)
+    # one-token steps run as one moe_decode_stack launch when the GPU supports it
+    stacked = wl.T == 1 and args.path == "stack" and pool.ctx.stack_workspace_bytes(wl.n_layers) > 0
+    st = W.DecodeStep(pool, inp) if stacked else W.Stack(pool, inp, wl.T)
     x0 = synthetic.activations(wl.seed, wl.T, wl.H, tag=4242)
     st.xs[0].copy_(W.bf16_tensor(x0))
     g = st.capture()
@@ -334,12 +358,13 @@ def run_ours(args, wl, world, rank, dist):
     kern_ms = down_ms = None
     try:
         nev = 3 if prefill else 2
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nev)] for _ in range(wl.n_layers)]
+        nrow = 1 if stacked else wl.n_layers
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nev)] for _ in range(nrow)]
         for row in evs:
             for e in row:
                 e.record()                      # creates the events
         torch.cuda.synchronize()
-        gi = st.capture(prof_events=evs)
+        gi = st.capture(prof_events=evs[0] if stacked else evs)
         reps = max(3, min(args.steps, 100))
         tot, tot_down = [], []
         for _ in range(reps):
@@ -381,11 +406,14 @@ def run_ours(args, wl, world, rank, dist):
     if kern_ms and not prefill:
         # algorithmic bytes: every distinct routed expert of the step plus the shared expert
         uniq = [len(np.unique(st.ids[l].cpu().numpy())) for l in range(wl.n_layers)]
-        alg_bytes = float(np.mean(uniq) + 1) * blob
+        alg_bytes = float(np.mean(uniq) + 1) * blob * (wl.n_layers if stacked else 1)
         ach = alg_bytes / (kern_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": recorded_traffic(wl.name),
-                "kernel": "decode_kernel (moe_forward, T <= 8)", "bytes_per_launch": int(alg_bytes),
+                "frac": round(ach / pk["hbm_gbs"], 4),
+                "traffic": stack_traffic(wl.name) if stacked else recorded_traffic(wl.name),
+                "kernel": ("decode_stack_kernel (moe_decode_stack: %d layers per launch)" % wl.n_layers) if stacked
+                else "decode_kernel (moe_forward, T <= 8)",
+                "bytes_per_launch": int(alg_bytes),
                 "us_per_launch": round(kern_ms * 1e3, 3),
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk_src == "measured"
                 else "fallback 6.8 TB/s"}
@@ -406,12 +434,13 @@ def run_ours(args, wl, world, rank, dist):
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp16" if prefill else "bf16", "data": "synthetic",
-            "config": config_of(wl, "CUDA graph of %d x (moe_route + moe_forward); us per layer %.3f"
-                                % (wl.n_layers, 1e3 * ms / args.steps / wl.n_layers), blobs, flush),
+            "config": config_of(wl, ("CUDA graph of one moe_decode_stack call (%d layers in one launch); us per layer "
+                                     "%.3f" if stacked else "CUDA graph of %d x (moe_route + moe_forward); us per "
+                                     "layer %.3f") % (wl.n_layers, 1e3 * ms / args.steps / wl.n_layers), blobs, flush),
             "roofline": roof, "e2e": e2e,
-            # per layer: decode = router + fused expert kernel; bucketed path = router GEMM + top-k,
-            # 3 bucketing kernels, row gather, 2 grouped GEMMs, combine
-            "gpu_launches": (9 if prefill else 2) * wl.n_layers * args.steps,
+            # per step: the one stack kernel; else per layer: decode = router + fused expert kernel;
+            # bucketed path = router GEMM + top-k, 3 bucketing kernels, row gather, 2 grouped GEMMs, combine
+            "gpu_launches": (1 if stacked else (9 if prefill else 2) * wl.n_layers) * args.steps,
             "clocks": sampler.summary()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)

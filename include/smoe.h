@@ -227,6 +227,51 @@ SMOE_API int moe_forward_noalloc(const smoe_ctx *ctx, int32_t layer, const uint1
                                  const void *pool, uint64_t pool_bytes, const void *shared_blob,
                                  const uint16_t *residual, uint16_t *out, int32_t *err, void *stream);
 
+/* ----------------------------------------------------- moe_decode_stack */
+/* One decode step for ONE token through n_layers consecutive layers
+ * (first_layer .. first_layer + n_layers - 1 of the context), each layer being
+ * moe_route followed by moe_forward with the residual added:
+ *   x_{l+1} = bf16(x_l + sum_j w_j f_{ids_j}(x_l) + gate f_shared(x_l)),
+ * the residual stacking of a decode step (the layers run one after the
+ * other for each new token: xix.ai article, paragraph on how it works). The
+ * whole step is one persistent launch (one CTA per SM, cooperative), the
+ * layers separated by grid-wide counters in the workspace instead of kernel
+ * boundaries; the routing rule and its fp32 arithmetic are moe_route's, so
+ * ids, w and gate equal what moe_route returns for the same x_l.
+ *   W_r, w_s      HOST arrays of n_layers device pointers: each layer's router
+ *                 rows (bf16 [E][H]) and shared-gate vector (bf16 [H]); the
+ *                 pointers are copied into the launch, the arrays may be
+ *                 freed when the call returns
+ *   shared_blobs  HOST array of n_layers device pointers to the layers'
+ *                 shared-expert blobs
+ *   logit_bias    fp32 [E] device or NULL (the same for every layer)
+ *   xs            bf16 [n_layers + 1][H] device: xs[0] is the input (read),
+ *                 xs[l + 1] receives layer l's output
+ *   ids, w        int32 / fp32 [n_layers][k] device, out: each layer's routing
+ *   gate          fp32 [n_layers] device, out
+ *   pool          as for moe_forward
+ *   workspace     device, >= smoe_stack_workspace_bytes(ctx, n_layers) bytes;
+ *                 the call clears the part it needs (its counters) itself
+ *   err           device error word as for moe_forward; a grid-wide wait
+ *                 that gives up (2 s) stores SMOE_DEV_TIMEOUT
+ * Expert arithmetic is the decode kernel's (exact weights, fp32 partials, h
+ * as bf16 hi + lo); the partial sums are combined in a fixed order, so the
+ * step is bit-identical across runs. Needs E % 4 == 0, 1 <= n_layers <= 64
+ * and a GPU with cooperative launch and enough shared memory (see
+ * smoe_ctx_describe); otherwise SMOE_ENOTSUP. Errors: SMOE_EINVAL,
+ * SMOE_ENOMEM, SMOE_ENOTSUP, SMOE_ECUDA. The pages describe one MoE layer at a
+ * time; running a step's layers in one launch is this library's. */
+SMOE_API int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_t n_layers,
+                              const uint16_t *const *W_r, const uint16_t *const *w_s,
+                              const void *const *shared_blobs, const float *logit_bias,
+                              uint16_t *xs, int32_t *ids, float *w, float *gate,
+                              const void *pool, uint64_t pool_bytes,
+                              void *workspace, uint64_t workspace_bytes, int32_t *err, void *stream);
+
+/* Workspace bytes moe_decode_stack needs for n_layers layers (0 if the
+ * context cannot run it). */
+SMOE_API uint64_t smoe_stack_workspace_bytes(const smoe_ctx *ctx, int32_t n_layers);
+
 /* Waits for stream, reads the error word (then clears it to 0) and returns
  * SMOE_OK, SMOE_EDEVICE if a kernel stored a code (copied to *code if
  * non-NULL), or SMOE_ECUDA. Not for use inside graph capture. */
@@ -243,7 +288,8 @@ SMOE_API int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len);
  * nodes when the stream is being captured): events[0] before the dominant
  * kernel, events[1] after it -- the fused decode kernel for T <= 8, the
  * grouped gate/up GEMM otherwise -- and, for T > 8, events[2] after the
- * grouped down GEMM. The library keeps the pointers, not the events.
+ * grouped down GEMM; moe_decode_stack records events[0] and events[1]
+ * around its one kernel. The library keeps the pointers, not the events.
  * Errors: SMOE_EINVAL. */
 SMOE_API int smoe_set_profile_events(smoe_ctx *ctx, void *const *events, int32_t n);
 

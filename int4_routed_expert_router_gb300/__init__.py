@@ -19,8 +19,9 @@ OK, EINVAL, ERANGE, ENOMEM, ECUDA, EDEVICE, ENOTSUP = 0, -1, -2, -3, -4, -5, -6
 DEV_BAD_SLOT, DEV_BAD_EXPERT, DEV_TIMEOUT, DEV_RANGE = 1, 2, 3, 4
 HOST, DEVICE = 0, 1
 EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destroy", "set_slot_table",
-           "smoe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_noalloc", "smoe_check",
-           "smoe_ctx_describe", "smoe_set_profile_events", "smoe_status_string"]
+           "smoe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_noalloc", "moe_decode_stack",
+           "smoe_stack_workspace_bytes", "smoe_check", "smoe_ctx_describe", "smoe_set_profile_events",
+           "smoe_status_string"]
 
 
 class SmoeError(RuntimeError):
@@ -67,6 +68,10 @@ def lib():
         L.moe_route.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, u64, vp]
         L.moe_forward.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, u64, vp, vp, vp, vp, u64, vp, vp]
         L.moe_forward_noalloc.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, u64, vp, vp, vp, vp, vp]
+        L.moe_decode_stack.argtypes = [vp, i32, i32, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp, vp, vp, vp,
+                                       vp, vp, u64, vp, u64, vp, vp]
+        L.smoe_stack_workspace_bytes.argtypes = [vp, i32]
+        L.smoe_stack_workspace_bytes.restype = u64
         L.smoe_check.argtypes = [vp, C.POINTER(C.c_int32), vp]
         L.smoe_ctx_describe.argtypes = [vp, C.c_char_p, i32]
         L.smoe_set_profile_events.argtypes = [vp, C.POINTER(vp), i32]
@@ -177,6 +182,10 @@ class Context:
         arr = (C.c_void_p * max(n, 1))(*[e.cuda_event for e in events])
         _check(lib().smoe_set_profile_events(self.handle, arr, n), "smoe_set_profile_events")
 
+    def stack_workspace_bytes(self, n_layers: int) -> int:
+        """Workspace bytes of moe_decode_stack over n_layers layers (0: not available)."""
+        return int(lib().smoe_stack_workspace_bytes(self.handle, int(n_layers)))
+
     def workspace_bytes(self, T: int) -> int:
         return int(lib().smoe_workspace_bytes(self.handle, int(T)))
 
@@ -210,6 +219,20 @@ def moe_forward_noalloc(ctx: Context, layer: int, x, ids, w, gate, pool, shared_
                                      _ptr(pool), pool.numel() * pool.element_size(), _ptr(shared_blob),
                                      _ptr(residual), _ptr(out), _ptr(err), _stream(stream)),
            "moe_forward_noalloc")
+
+
+def moe_decode_stack(ctx: Context, first_layer: int, Wr, ws, shared_blobs, xs, ids, w, gate, pool, workspace, err,
+                     logit_bias=None, stream=None):
+    """One token through len(Wr) layers in one launch. Wr, ws, shared_blobs:
+    per-layer device tensors; xs bf16 [L + 1, H] (xs[0] the input); ids, w
+    [L, k]; gate [L]."""
+    n = len(Wr)
+    arr = lambda ts: (C.c_void_p * n)(*[_ptr(t) for t in ts])
+    _check(lib().moe_decode_stack(ctx.handle, int(first_layer), n, arr(Wr), arr(ws), arr(shared_blobs),
+                                  _ptr(logit_bias), _ptr(xs), _ptr(ids), _ptr(w), _ptr(gate), _ptr(pool),
+                                  pool.numel() * pool.element_size(), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)),
+           "moe_decode_stack")
 
 
 def check(err, stream=None) -> int:

@@ -306,27 +306,22 @@ __device__ __forceinline__ uint32_t nib_pair_f16(uint32_t w, int m)
     return hsub2(r, 0x64006400u);
 }
 
-// Bounded wait for the persistent GEMM: gives up after about one second of
+// Bounded wait for the persistent GEMM: gives up after kWaitLimitNs of
 // global time, and once any wait of the CTA has given up (*abort set) every
 // later wait returns at once, so a failed CTA drains in bounded time.
 __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int32_t *err, volatile int *abort)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255) == 0) {
-            if (*abort) return false;
-            uint64_t t;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-            if (t - t0 > 1000000000ull) {
-                *abort = 1;
-                set_error(err, SMOE_DEV_TIMEOUT);
-                return false;
-            }
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            set_error(err, SMOE_DEV_TIMEOUT);
+            return false;
         }
     }
+    return true;
 }
 
 struct TileInfo {

@@ -15,8 +15,7 @@
 // for every token with all its warps (two levels of warp max-reductions over
 // order-preserving integer keys), so a decode step costs one launch;
 // otherwise topk_kernel runs one warp per token.
-#include "smoe_dev.cuh"
-#include "smoe_internal.h"
+#include "route_common.cuh"
 
 namespace smoe {
 
@@ -37,92 +36,16 @@ __device__ __forceinline__ void bulk_plain(void *dst, const void *src, uint32_t 
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-// Order-preserving map float -> uint32 (larger float, larger key); key 0 is
-// reserved for "taken / empty" (no finite or infinite float maps to it).
-__device__ __forceinline__ uint32_t fkey(float f)
-{
-    const uint32_t b = __float_as_uint(f);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-__device__ __forceinline__ float fkey_inv(uint32_t k)
-{
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// One warp picks the k largest keys among its lanes' PER values, in
-// descending order, ties to the lower id. Each round: warp max of the lanes'
-// current bests, then the lowest id holding that key; the winner removes it.
-template <int PER>
-__device__ void warp_topk(uint32_t (&key)[PER], int32_t (&id)[PER], int k, uint32_t *okey, int32_t *oid,
-                          int lane)
-{
-    for (int s = 0; s < k; ++s) {
-        uint32_t bk = 0;
-        int32_t bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < PER; ++j)
-            if (key[j] > bk || (key[j] == bk && key[j] != 0u && id[j] < bi)) {
-                bk = key[j];
-                bi = id[j];
-            }
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-        const int32_t mi = int32_t(__reduce_min_sync(0xffffffffu, uint32_t(bk == mk ? bi : 0x7fffffff)));
-#pragma unroll
-        for (int j = 0; j < PER; ++j)
-            if (id[j] == mi && key[j] == mk) key[j] = 0u;
-        if (lane == 0) {
-            okey[s] = mk;
-            oid[s] = mk ? mi : -1;
-        }
-    }
-}
-
-// Level 1 for one token slice: values z[e] (+bias) for e in [e0, e1); z may be
-// global (read through L2) or a shared-memory copy.
-template <int PER>
-__device__ void slice_topk(const float *z, const float *bias, int e0, int e1, int k, uint32_t *okey, int32_t *oid,
-                           int lane)
-{
-    uint32_t key[PER];
-    int32_t id[PER];
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-        const int e = e0 + lane + 32 * j;
-        key[j] = 0u;
-        id[j] = 0x7fffffff;
-        if (e < e1) {
-            key[j] = fkey(z[e] + (bias ? bias[e] : 0.f));
-            id[j] = e;
-        }
-    }
-    warp_topk<PER>(key, id, k, okey, oid, lane);
-}
-
-__device__ void slice_topk_any(int per, const float *z, const float *bias, int e0, int e1, int k, uint32_t *ok,
-                               int32_t *oi, int lane)
-{
-    if (per <= 1) slice_topk<1>(z, bias, e0, e1, k, ok, oi, lane);
-    else if (per <= 2) slice_topk<2>(z, bias, e0, e1, k, ok, oi, lane);
-    else if (per <= 4) slice_topk<4>(z, bias, e0, e1, k, ok, oi, lane);
-    else if (per <= 8) slice_topk<8>(z, bias, e0, e1, k, ok, oi, lane);
-    else if (per <= 16) slice_topk<16>(z, bias, e0, e1, k, ok, oi, lane);
-    else slice_topk<32>(z, bias, e0, e1, k, ok, oi, lane);
-}
-
-// Final weights of one token from its k chosen keys (descending), one lane per
-// choice (k <= 16); zs: the token's shared-gate logit. The denominator is
-// summed in choice order on every lane, so all lanes agree bit for bit.
+// Final outputs of one token from its k chosen keys (descending), one lane
+// per choice (k <= 16); zs: the token's shared-gate logit.
 __device__ void write_choice(const RouteParams &p, int t, const uint32_t *fk, const int32_t *fi, float zs, int lane)
 {
-    const float zmax = fkey_inv(fk[0]);
-    float den = 0.f;
-    for (int s = 0; s < p.k; ++s) den += expf(fkey_inv(fk[s]) - zmax);
+    const float wl = choice_weight(fk, p.k, lane);
     if (lane < p.k) {
         p.ids[size_t(t) * p.k + lane] = fi[lane];
-        p.w[size_t(t) * p.k + lane] = expf(fkey_inv(fk[lane]) - zmax) / den;
+        p.w[size_t(t) * p.k + lane] = wl;
     }
-    if (lane == 0) p.gate[t] = 1.0f / (1.0f + expf(-zs));
+    if (lane == 0) p.gate[t] = shared_gate(zs);
 }
 
 // Top-k of T <= 8 tokens by the 8 warps of a CTA (the CTA that finishes the
@@ -149,19 +72,9 @@ __device__ void block_topk(const RouteParams &p, uint32_t *ckey, int32_t *cid, f
     }
     __syncthreads();
     if (t < T && sl == 0) {
-        uint32_t key[4];
-        int32_t id[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {       // wpt * k <= 8 * 16 = 128 candidates, 4 per lane
-            const int c = lane + 32 * j;
-            const int w = warp + c / k, r = c % k;
-            const bool ok = c < wpt * k;
-            key[j] = ok ? ckey[w * 16 + r] : 0u;
-            id[j] = ok && key[j] ? cid[w * 16 + r] : 0x7fffffff;
-        }
         uint32_t *fk = ckey + 8 * 16 + warp * 16;
         int32_t *fi = cid + 8 * 16 + warp * 16;
-        warp_topk<4>(key, id, k, fk, fi, lane);
+        topk_merge(ckey + warp * 16, cid + warp * 16, wpt, k, fk, fi, lane);
         __syncwarp();
         write_choice(p, t, fk, fi, zsm[t * (E + 1) + E], lane);
     }
@@ -208,20 +121,7 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const RouteParams p)
     if (warp < nrows && ok) {
         const int row = row0 + warp;
         for (int t = 0; t < ntok; ++t) {
-            float acc = 0.f;
-            for (int c = 8 * lane; c < H; c += 256) {
-                const uint4 wv = *reinterpret_cast<const uint4 *>(wrow + warp * H + c);
-                const uint4 xv = *reinterpret_cast<const uint4 *>(xs + t * H + c);
-                acc = fmaf(bf16lo(wv.x), bf16lo(xv.x), acc);
-                acc = fmaf(bf16hi(wv.x), bf16hi(xv.x), acc);
-                acc = fmaf(bf16lo(wv.y), bf16lo(xv.y), acc);
-                acc = fmaf(bf16hi(wv.y), bf16hi(xv.y), acc);
-                acc = fmaf(bf16lo(wv.z), bf16lo(xv.z), acc);
-                acc = fmaf(bf16hi(wv.z), bf16hi(xv.z), acc);
-                acc = fmaf(bf16lo(wv.w), bf16lo(xv.w), acc);
-                acc = fmaf(bf16hi(wv.w), bf16hi(xv.w), acc);
-            }
-            for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            const float acc = router_dot(wrow + warp * H, xs + t * H, H, lane);
             if (lane == 0) p.logits[size_t(tok0 + t) * (E + 1) + row] = acc;
         }
     }

@@ -1,0 +1,145 @@
+// route_common.cuh -- routing arithmetic shared by the routing kernel
+// (route.cu) and the multi-layer decode kernel (decode_stack.cu), so that both
+// produce the same logits, ids and weights bit for bit.
+// Since exp is increasing, the k largest probabilities are the k largest
+// logits, and the renormalised weight of a chosen expert is
+//   w_j = exp(z_j - z_max) / sum_{chosen i} exp(z_i - z_max),
+// the full softmax denominator cancelling (xix.ai article, paragraph on how it
+// works: top-k routing over the experts).
+#pragma once
+
+#include "smoe_dev.cuh"
+#include "smoe_internal.h"
+
+namespace smoe {
+
+// One router row (bf16 [H]) dotted with one token (bf16 [H]) by a warp: lane l
+// takes columns 8 l .. 8 l + 7 of every 256, fp32 fused multiply-adds in that
+// order, then a butterfly sum. Every lane returns the total.
+__device__ __forceinline__ float router_dot(const uint16_t *row, const uint16_t *x, int H, int lane)
+{
+    float acc = 0.f;
+    for (int c = 8 * lane; c < H; c += 256) {
+        const uint4 wv = *reinterpret_cast<const uint4 *>(row + c);
+        const uint4 xv = *reinterpret_cast<const uint4 *>(x + c);
+        acc = fmaf(bf16lo(wv.x), bf16lo(xv.x), acc);
+        acc = fmaf(bf16hi(wv.x), bf16hi(xv.x), acc);
+        acc = fmaf(bf16lo(wv.y), bf16lo(xv.y), acc);
+        acc = fmaf(bf16hi(wv.y), bf16hi(xv.y), acc);
+        acc = fmaf(bf16lo(wv.z), bf16lo(xv.z), acc);
+        acc = fmaf(bf16hi(wv.z), bf16hi(xv.z), acc);
+        acc = fmaf(bf16lo(wv.w), bf16lo(xv.w), acc);
+        acc = fmaf(bf16hi(wv.w), bf16hi(xv.w), acc);
+    }
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc;
+}
+
+// Order-preserving map float -> uint32 (larger float, larger key); key 0 is
+// reserved for "taken / empty" (no finite or infinite float maps to it).
+__device__ __forceinline__ uint32_t fkey(float f)
+{
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float fkey_inv(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// One warp picks the k largest keys among its lanes' PER values, in
+// descending order, ties to the lower id. Each round: warp max of the lanes'
+// current bests, then the lowest id holding that key; the winner removes it.
+template <int PER>
+__device__ inline void warp_topk(uint32_t (&key)[PER], int32_t (&id)[PER], int k, uint32_t *okey, int32_t *oid,
+                          int lane)
+{
+    for (int s = 0; s < k; ++s) {
+        uint32_t bk = 0;
+        int32_t bi = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+            if (key[j] > bk || (key[j] == bk && key[j] != 0u && id[j] < bi)) {
+                bk = key[j];
+                bi = id[j];
+            }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const int32_t mi = int32_t(__reduce_min_sync(0xffffffffu, uint32_t(bk == mk ? bi : 0x7fffffff)));
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+            if (id[j] == mi && key[j] == mk) key[j] = 0u;
+        if (lane == 0) {
+            okey[s] = mk;
+            oid[s] = mk ? mi : -1;
+        }
+    }
+}
+
+// Level 1 for one token slice: values z[e] (+bias) for e in [e0, e1); z may be
+// global (read through L2) or a shared-memory copy.
+template <int PER>
+__device__ inline void slice_topk(const float *z, const float *bias, int e0, int e1, int k, uint32_t *okey, int32_t *oid,
+                           int lane)
+{
+    uint32_t key[PER];
+    int32_t id[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int e = e0 + lane + 32 * j;
+        key[j] = 0u;
+        id[j] = 0x7fffffff;
+        if (e < e1) {
+            key[j] = fkey(z[e] + (bias ? bias[e] : 0.f));
+            id[j] = e;
+        }
+    }
+    warp_topk<PER>(key, id, k, okey, oid, lane);
+}
+
+__device__ inline void slice_topk_any(int per, const float *z, const float *bias, int e0, int e1, int k, uint32_t *ok,
+                               int32_t *oi, int lane)
+{
+    if (per <= 1) slice_topk<1>(z, bias, e0, e1, k, ok, oi, lane);
+    else if (per <= 2) slice_topk<2>(z, bias, e0, e1, k, ok, oi, lane);
+    else if (per <= 4) slice_topk<4>(z, bias, e0, e1, k, ok, oi, lane);
+    else if (per <= 8) slice_topk<8>(z, bias, e0, e1, k, ok, oi, lane);
+    else if (per <= 16) slice_topk<16>(z, bias, e0, e1, k, ok, oi, lane);
+    else slice_topk<32>(z, bias, e0, e1, k, ok, oi, lane);
+}
+
+// Level 2 for one token: the k best of the nw * k candidates that nw level-1
+// warps left in ckey/cid (16 entries per warp, nw * k <= 128), by one warp,
+// into fk/fi in descending order.
+__device__ inline void topk_merge(const uint32_t *ckey, const int32_t *cid, int nw, int k, uint32_t *fk, int32_t *fi,
+                                  int lane)
+{
+    uint32_t key[4];
+    int32_t id[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int c = lane + 32 * j;
+        const int w = c / k, r = c % k;
+        const bool ok = c < nw * k;
+        key[j] = ok ? ckey[w * 16 + r] : 0u;
+        id[j] = ok && key[j] ? cid[w * 16 + r] : 0x7fffffff;
+    }
+    warp_topk<4>(key, id, k, fk, fi, lane);
+}
+
+// Renormalised weight of choice `lane` (lane < k) from the k chosen keys in
+// descending order: each lane forms exp(z_lane - z_max), then every lane sums
+// the k terms in choice order (gathered by shuffles), so all lanes agree bit
+// for bit. Called by a whole warp.
+__device__ __forceinline__ float choice_weight(const uint32_t *fk, int k, int lane)
+{
+    const float zmax = fkey_inv(fk[0]);
+    const float ex = lane < k ? expf(fkey_inv(fk[lane]) - zmax) : 0.f;
+    float den = 0.f;
+    for (int s = 0; s < k; ++s) den += __shfl_sync(0xffffffffu, ex, s);
+    return lane < k ? ex / den : 0.f;
+}
+
+__device__ __forceinline__ float shared_gate(float zs) { return 1.0f / (1.0f + expf(-zs)); }
+
+}  // namespace smoe

@@ -239,6 +239,7 @@ extern "C" int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_
     if (e == cudaSuccess) e = route_config();
     if (e == cudaSuccess) e = prefill_config();
     if (e == cudaSuccess) e = decode_config(c);
+    if (e == cudaSuccess) e = stack_config(c);
     if (e != cudaSuccess) {
         cudaGetLastError();
         delete c;
@@ -421,6 +422,77 @@ extern "C" int smoe_set_profile_events(smoe_ctx *ctx, void *const *events, int32
     return SMOE_OK;
 }
 
+// Workspace of moe_decode_stack: logits [n][E + 1], h [n][U][I] fp32, counters.
+struct StackWs {
+    uint64_t logits, h, sync, total;
+};
+
+static StackWs stack_ws(const smoe_ctx *ctx, int n)
+{
+    auto al = [](uint64_t v) { return (v + 255) & ~uint64_t(255); };
+    const smoe_shape &s = ctx->shape;
+    StackWs w = {};
+    uint64_t o = 0;
+    w.logits = o; o = al(o + uint64_t(n) * (s.E + 1) * 4);
+    w.h = o;      o = al(o + uint64_t(n) * ctx->stack.U * s.I * 4);
+    w.sync = o;   o = al(o + (3 * uint64_t(n) + 1) * 4);
+    w.total = o;
+    return w;
+}
+
+extern "C" uint64_t smoe_stack_workspace_bytes(const smoe_ctx *ctx, int32_t n_layers)
+{
+    if (!ctx || !ctx->stack.ok || n_layers < 1 || n_layers > kStackMaxLayers) return 0;
+    return stack_ws(ctx, n_layers).total;
+}
+
+extern "C" int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_t n_layers,
+                                const uint16_t *const *W_r, const uint16_t *const *w_s,
+                                const void *const *shared_blobs, const float *logit_bias, uint16_t *xs,
+                                int32_t *ids, float *w, float *gate, const void *pool, uint64_t pool_bytes,
+                                void *workspace, uint64_t workspace_bytes, int32_t *err, void *stream)
+{
+    if (!ctx || !W_r || !w_s || !shared_blobs || !xs || !ids || !w || !gate || !pool || !workspace || !err)
+        return SMOE_EINVAL;
+    if (n_layers < 1 || first_layer < 0 || first_layer + n_layers > ctx->n_layers) return SMOE_EINVAL;
+    if (n_layers > kStackMaxLayers || !ctx->stack.ok) return SMOE_ENOTSUP;
+    if (!aligned16(xs) || !aligned16(pool) || !aligned16(workspace)) return SMOE_EINVAL;
+    if (pool_bytes < uint64_t(ctx->n_slots) * ctx->layout.blob) return SMOE_ENOMEM;
+    const StackWs W = stack_ws(ctx, n_layers);
+    if (workspace_bytes < W.total) return SMOE_ENOMEM;
+    StackParams p = {};
+    for (int l = 0; l < n_layers; ++l) {
+        if (!W_r[l] || !w_s[l] || !shared_blobs[l]) return SMOE_EINVAL;
+        if (!aligned16(W_r[l]) || !aligned16(w_s[l]) || !aligned16(shared_blobs[l])) return SMOE_EINVAL;
+        p.Wr[l] = W_r[l];
+        p.ws[l] = w_s[l];
+        p.shared[l] = static_cast<const uint8_t *>(shared_blobs[l]);
+    }
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.bias = logit_bias;
+    p.xs = xs;
+    p.ids = ids;
+    p.w = w;
+    p.gate = gate;
+    p.pool = static_cast<const uint8_t *>(pool);
+    p.table = ctx->table_dev + size_t(first_layer) * ctx->shape.E;
+    p.stride = ctx->layout.blob;
+    p.n_slots = ctx->n_slots;
+    p.logits = reinterpret_cast<float *>(ws + W.logits);
+    p.h = reinterpret_cast<float *>(ws + W.h);
+    p.sync = reinterpret_cast<uint32_t *>(ws + W.sync);
+    p.err = err;
+    p.n_layers = n_layers;
+    p.H = ctx->shape.H;
+    p.E = ctx->shape.E;
+    p.k = ctx->shape.k;
+    p.I = ctx->shape.I;
+    p.U = ctx->stack.U;
+    p.nr = ctx->stack.nr;
+    p.nu = ctx->stack.nu;
+    return cuda_status(launch_stack(ctx, p, static_cast<cudaStream_t>(stream)));
+}
+
 extern "C" int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len)
 {
     if (!ctx || !buf || len <= 0) return SMOE_EINVAL;
@@ -429,6 +501,9 @@ extern "C" int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len)
         o += std::snprintf(buf + o, size_t(len - o), " T%d:{slots=%d smem=%d/%d clusters=%d/%d}", T,
                            ctx->decode[T].nst, ctx->decode[T].smem, ctx->decode[T].smem16,
                            ctx->decode[T].max_clusters, ctx->decode[T].max_clusters16);
+    if (o < len)
+        std::snprintf(buf + o, size_t(len - o), " stack:{ok=%d grid=%d rows=%d units=%d smem=%d}", int(ctx->stack.ok),
+                      ctx->stack.grid, ctx->stack.nr, ctx->stack.nu, ctx->stack.smem);
     return SMOE_OK;
 }
 

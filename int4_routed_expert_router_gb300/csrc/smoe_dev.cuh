@@ -11,7 +11,8 @@ namespace smoe {
 
 // Bounded waits: a spin that exceeds this many polls records
 // SMOE_DEV_TIMEOUT in the error word and gives up (about a second or more).
-constexpr uint32_t kSpinLimit = 1u << 26;
+constexpr uint32_t kSuspendNs = 100000;          // longest sleep of one mbarrier try_wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a bounded wait gives up after two seconds
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -45,24 +46,38 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One try_wait: the thread sleeps until the phase completes or kSuspendNs
+// pass (the suspend-time hint), so waiting warps do not take issue slots from
+// the warps doing the work.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs) : "memory");
     return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 // Waits for phase `parity` of bar to complete. Returns false (and records a
-// timeout) if it did not within kSpinLimit polls.
+// timeout) if it did not within kWaitLimitNs of global time.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err)
 {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    set_error(err, SMOE_DEV_TIMEOUT);
-    return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            set_error(err, SMOE_DEV_TIMEOUT);
+            return false;
+        }
+    return true;
 }
 
 // ------------------------------------------------------------ bulk copies

@@ -43,6 +43,38 @@ struct DecodeCfg {
     int max_clusters16 = 0;
 };
 
+// Multi-layer decode step (decode_stack.cu), one token.
+constexpr int kStackMaxLayers = 64;
+
+struct StackCfg {
+    bool ok = false;          // cooperative launch available and the shared memory fits
+    int grid = 0;             // CTAs (one per SM)
+    int U = 0;                // experts per layer: k routed + the shared expert
+    int nr = 0;               // most router rows of one CTA
+    int nu = 0;               // most gate/up units of one CTA
+    int smem = 0;
+};
+
+struct StackParams {
+    const uint16_t *Wr[kStackMaxLayers];       // router rows of each layer [E][H] bf16
+    const uint16_t *ws[kStackMaxLayers];       // shared-gate vector of each layer [H]
+    const uint8_t *shared[kStackMaxLayers];    // shared-expert blob of each layer
+    const float *bias;                         // [E] logit offsets or nullptr
+    uint16_t *xs;                              // [(n_layers + 1)][H] bf16: input, then each layer's output
+    int32_t *ids;                              // [n_layers][k]
+    float *w;                                  // [n_layers][k]
+    float *gate;                               // [n_layers]
+    const uint8_t *pool;
+    const int32_t *table;                      // slot table rows of the layers [n_layers][E]
+    uint64_t stride;
+    int64_t n_slots;
+    float *logits;                             // [n_layers][E + 1]
+    float *h;                                  // [n_layers][U][I]
+    uint32_t *sync;                            // [n_layers][3] arrival counters, then the abort word
+    int32_t *err;
+    int n_layers, H, E, k, I, U, nr, nu;
+};
+
 }  // namespace smoe
 
 struct smoe_ctx {
@@ -57,6 +89,7 @@ struct smoe_ctx {
     cudaEvent_t prof[4];                     // profiling hook (smoe_set_profile_events)
     int nprof;
     smoe::DecodeCfg decode[smoe::kDecodeMaxT + 1];
+    smoe::StackCfg stack;
 };
 
 namespace smoe {
@@ -161,6 +194,8 @@ cudaError_t route_config();
 cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
 cudaError_t launch_decode(const smoe_ctx *ctx, const DecodeParams &p, cudaStream_t st);
 cudaError_t decode_config(smoe_ctx *ctx);
+cudaError_t stack_config(smoe_ctx *ctx);
+cudaError_t launch_stack(const smoe_ctx *ctx, const StackParams &p, cudaStream_t st);
 cudaError_t prefill_config();
 int prefill_max_tiles(int T, int k, int E);
 cudaError_t launch_router_gemm(const RouteParams &r, cudaStream_t st);

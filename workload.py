@@ -153,3 +153,39 @@ class Stack:
         if prof_events is None:
             self.graph = g
         return g
+
+
+class DecodeStep:
+    """A one-token decode step through the whole stack as one moe_decode_stack
+    call (one persistent launch): xs_buf [L + 1][1][H] holds the input and
+    each layer's output; ids/w/gate [L][k], [L]."""
+
+    def __init__(self, pool: DevicePool, inputs: LayerInputs):
+        wl = pool.wl
+        L = pool.n_layers
+        self.pool, self.inputs, self.T = pool, inputs, 1
+        self.xs_buf = torch.zeros((L + 1, 1, wl.H), dtype=torch.bfloat16, device="cuda")
+        self.xs = [self.xs_buf[l] for l in range(L + 1)]      # [1][H] views, as in Stack
+        self.ids = torch.zeros((L, wl.k), dtype=torch.int32, device="cuda")
+        self.w = torch.zeros((L, wl.k), dtype=torch.float32, device="cuda")
+        self.gate = torch.zeros((L,), dtype=torch.float32, device="cuda")
+        n = pool.ctx.stack_workspace_bytes(L)
+        if n == 0:
+            raise RuntimeError("moe_decode_stack is not available for this shape / GPU")
+        self.ws = torch.zeros((n + 15) // 16 * 16, dtype=torch.uint8, device="cuda")
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.shared = [pool.shared[l] for l in range(L)]
+        self.graph = None
+
+    def enqueue(self, stream=None, prof_events=None):
+        """prof_events: optional [before, after] events for the profiling hook."""
+        p, inp = self.pool, self.inputs
+        if prof_events is not None:
+            p.ctx.set_profile_events(prof_events)
+        smoe.moe_decode_stack(p.ctx, 0, inp.Wr, inp.ws, self.shared, self.xs_buf, self.ids, self.w, self.gate, p.pool,
+                              self.ws, self.err, logit_bias=inp.bias, stream=stream)
+        if prof_events is not None:
+            p.ctx.set_profile_events([])
+
+    capture = Stack.capture
+
