@@ -144,8 +144,9 @@ STACK_SOURCES = ["int4_routed_expert_router_gb300/csrc/decode_stack.cu",
 
 
 def stack_traffic(workload: str):
-    """DRAM bytes per launch of the stack kernel from the committed ncu
-    summary, only if its sources are unchanged since it was taken."""
+    """DRAM bytes per layer of the stack kernel from the committed ncu summary
+    (captured on a shorter stack; the traffic is per layer), only if its
+    sources are unchanged since it was taken."""
     p = os.path.join(ROOT, "profiles", "decode_stack_kernel_traffic.json")
     if not os.path.exists(p):
         return None
@@ -153,7 +154,7 @@ def stack_traffic(workload: str):
         d = json.load(f)
     if d.get("source_sha256") != src_hash(STACK_SOURCES) or d.get("workload") != workload:
         return None
-    return d.get("dram_bytes_per_launch")
+    return d.get("dram_bytes_per_layer")
 
 
 def recorded_traffic(workload: str):
@@ -410,7 +411,8 @@ def run_ours(args, wl, world, rank, dist):
         ach = alg_bytes / (kern_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / pk["hbm_gbs"], 4),
-                "traffic": stack_traffic(wl.name) if stacked else recorded_traffic(wl.name),
+                "traffic": (stack_traffic(wl.name) * wl.n_layers if stack_traffic(wl.name) else None) if stacked
+                else recorded_traffic(wl.name),
                 "kernel": ("decode_stack_kernel (moe_decode_stack: %d layers per launch)" % wl.n_layers) if stacked
                 else "decode_kernel (moe_forward, T <= 8)",
                 "bytes_per_launch": int(alg_bytes),
