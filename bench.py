@@ -173,6 +173,17 @@ def recorded_traffic(workload: str):
 L2_BYTES = 129 * 10**6
 
 
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The largest value over all ranks (the slowest rank's time), or value
+    itself when there is one process."""
+    if not dist:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def config_of(wl, note="", blobs=None, flushed=False):
     """blobs: distinct expert blobs one step streams (routed + shared, all layers)."""
     if blobs is None:
@@ -344,10 +355,7 @@ def run_ours(args, wl, world, rank, dist):
     if dist:
         dist.barrier()
     sampler.stop()
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     if smoe.check(st.err) != 0:
         raise RuntimeError("device error word set during the timed region")
     step_s = ms / 1e3 / args.steps
@@ -392,10 +400,7 @@ def run_ours(args, wl, world, rank, dist):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     e2e = {"value": round(world * wl.T * wl.n_layers * args.steps / (e2e_ms / 1e3), 1), "unit": UNIT,
            "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2}
 
