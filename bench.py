@@ -432,7 +432,7 @@ def run_ours(args, wl, world, rank, dist):
         peak = pk["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(ach / peak, 4), "traffic": None,
-                "kernel": "grouped_gemm_kernel gate/up (fp16 operands, fp32 accumulate)",
+                "kernel": "expert_gemm_kernel gate/up (fp16 operands, A in TMEM, fp32 accumulate)",
                 "flops_per_launch": flops, "us_per_launch": round(kern_ms * 1e3, 3),
                 "down_gemm_us": round(down_ms * 1e3, 3) if down_ms else None,
                 "down_gemm_tflops": round(2.0 * pairs * wl.I * wl.H / (down_ms / 1e3) / 1e12, 1) if down_ms else None,

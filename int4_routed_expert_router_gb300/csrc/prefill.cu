@@ -8,10 +8,11 @@
 //     the shared expert), converted to fp16, with each row's routing weight
 //     (or shared-expert gate), so that every GEMM tile reads contiguous rows;
 //   gate/up GEMM: per tile, 128 weight rows (64 gate + 64 up rows, interleaved
-//     in blocks of 8 as the blob stores them) x its tokens, K = H; the int4
-//     atoms are dequantised to bf16 in shared memory (128-byte swizzled,
-//     K-major) and multiplied on tcgen05 tensor cores with the accumulator in
-//     TMEM; the epilogue applies SwiGLU and writes h;
+//     in blocks of 8 as the blob stores them) x its tokens (at most 192), K = H;
+//     the int4 atoms are dequantised to fp16 straight into tensor memory and
+//     multiplied on tcgen05 tensor cores (A from TMEM, B from 128-byte-swizzled
+//     shared memory) with the accumulator in TMEM; the epilogue applies SwiGLU
+//     and writes h;
 //   down GEMM: per tile, 128 down rows x its pairs, K = I, B = h rows; the
 //     epilogue scales by the routing weight (or the shared-expert gate);
 //   combine: per token, the k pair outputs in route order, then the shared
@@ -53,6 +54,20 @@ constexpr int kPfStageBytes = kPfABytes + kPfBBytes;
 constexpr int kPfSmem = kPfAB * kPfStageBytes + kPfRaw * kPfRawBytes + 1024 /*align*/ + 512 /*barriers*/;
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
 constexpr int kBucketTok = 64;     // tokens per bucketing chunk
+
+// Expert GEMMs (gate/up, down): A (the dequantised weights) lives in tensor
+// memory. TMEM columns: two accumulators of kXMaxN columns, then kXAStg A
+// stages of 32 columns (128 rows x 64 fp16 K values). Shared memory holds only
+// the B stages and the raw atoms.
+constexpr int kXMaxN = 192;        // tokens per expert tile
+constexpr int kXRaw = 12;          // raw atom slots
+constexpr int kXAStg = 4;          // A stages in TMEM
+constexpr int kXBStg = 6;          // B stages in shared memory
+constexpr int kXBBytes = kXMaxN * kPfK * 2;                 // 24 KiB
+constexpr uint32_t kXACol0 = 2 * kXMaxN;                    // first A column (384)
+constexpr int kXSmem = kXBStg * kXBBytes + kXRaw * kPfRawBytes + 1024 /*align*/ + 512 /*barriers*/;
+static_assert(kXSmem <= 232448, "shared memory per CTA");
+static_assert(kXACol0 + kXAStg * 32 <= 512, "TMEM columns");
 
 __device__ __forceinline__ uint32_t sw128(int r, int c)   // byte offset of (row, col) in a 64-col bf16 tile
 {
@@ -110,6 +125,33 @@ __device__ __forceinline__ void umma(uint32_t tmem, uint64_t a, uint64_t b, uint
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
                  ::"r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
+
+// tcgen05.mma with A read from tensor memory (a_tmem: column of the stage,
+// lane 0) and B from a shared-memory descriptor.
+__device__ __forceinline__ void umma_ts(uint32_t tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 ::"r"(tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// 16 lanes x 32 columns from registers: thread 4g + t's registers 4r .. 4r + 3
+// land at (lane g, column 8r + 2t), (g, 8r + 2t + 1), (g + 8, 8r + 2t),
+// (g + 8, 8r + 2t + 1) of the 16-lane block at taddr.
+__device__ __forceinline__ void tmem_st16x256x4(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+                   "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+
+// K order inside a 64-column group as the expert GEMMs see it: MMA position
+// 16 a + 4 b + c holds column 16 b + 4 a + c (the 4-column blocks transposed),
+// which is the order in which a thread's atom fragment meets the 16x256b
+// tensor-memory store. The map is its own inverse; B rows (x and h) are stored
+// in the same order so the products pair up.
+__device__ __forceinline__ int perm64(int c) { return ((c & 12) << 2) | ((c >> 2) & 12) | (c & 3); }
 
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
@@ -169,7 +211,7 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
             }
         }
     }
-    const int nt = e < p.E ? (total + kPfMaxN - 1) / kPfMaxN : 0;
+    const int nt = e < p.E ? (total + kXMaxN - 1) / kXMaxN : 0;
     buf[e] = e < p.E ? total : 0;
     tbuf[e] = nt;
     __syncthreads();
@@ -189,8 +231,8 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
             tl.kind = 0;
             const int64_t slot = p.table_row[e];
             tl.slot = (slot < 0 || slot >= p.n_slots) ? -1 : int(slot);
-            tl.p0 = start + i * kPfMaxN;
-            tl.n = min(kPfMaxN, total - i * kPfMaxN);
+            tl.p0 = start + int((int64_t(i) * total) / nt);               // runs of near-equal size
+            tl.n = int((int64_t(i + 1) * total) / nt) - int((int64_t(i) * total) / nt);
             p.tiles[tstart + i] = tl;
         }
     }
@@ -198,13 +240,13 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
         const int P = buf[1023];
         const int ntr = tbuf[1023];
         p.offsets[p.E] = P;
-        const int nts = (p.T + kPfMaxN - 1) / kPfMaxN;
+        const int nts = (p.T + kXMaxN - 1) / kXMaxN;
         for (int i = 0; i < nts; ++i) {
             PfTile tl;
             tl.kind = 1;
             tl.slot = 0;
-            tl.p0 = i * kPfMaxN;
-            tl.n = min(kPfMaxN, p.T - i * kPfMaxN);
+            tl.p0 = int((int64_t(i) * p.T) / nts);
+            tl.n = int((int64_t(i + 1) * p.T) / nts) - tl.p0;
             p.tiles[ntr + i] = tl;
         }
         *p.ntiles = ntr + nts;
@@ -246,7 +288,8 @@ __global__ void __launch_bounds__(32) bucket_scatter_kernel(const PrefillParams 
 
 // ------------------------------------------------------------ row gather
 // One warp per row of xs: row pos < P is pair pos (expert order), row P + t
-// is token t for the shared expert. xs = fp16(x row), exact for |x| < 65504
+// is token t for the shared expert, its columns in the expert GEMMs' K order
+// (perm64 inside each 64-column group). xs = fp16(x row), exact for |x| < 65504
 // (subnormal below 2^-14, an absolute error under 3e-8); larger values set
 // the error word. pair_w = the pair's routing weight, or the token's gate.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const GemmParams g)
@@ -264,6 +307,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GemmParams g)
     const uint4 *src = reinterpret_cast<const uint4 *>(g.x_bf16 + size_t(tok) * g.H);
     uint4 *dst = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(g.x) + size_t(row) * g.H);
     bool bad = false;
+    uint2 *dst2 = reinterpret_cast<uint2 *>(dst);
     for (int i = lane; i < g.H / 8; i += 32) {
         const uint4 v = __ldg(src + i);
         const uint32_t in[4] = {v.x, v.y, v.z, v.w};
@@ -274,7 +318,10 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GemmParams g)
             bad |= !(fabsf(a) < 65504.f) || !(fabsf(b) < 65504.f);
             o[j] = pack_f16x2(a, b);
         }
-        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        // columns 8 i .. 8 i + 7 are two 4-column blocks; each goes to its permuted place
+        const int c0 = 8 * i, base = c0 & ~63;
+        dst2[(base + perm64(c0 & 63)) / 4] = make_uint2(o[0], o[1]);
+        dst2[(base + perm64((c0 & 63) + 4)) / 4] = make_uint2(o[2], o[3]);
     }
     if (bad) set_error(g.err, SMOE_DEV_RANGE);
 }
@@ -652,6 +699,246 @@ __global__ void __launch_bounds__(kPfThreads, 1) grouped_gemm_kernel(const GemmP
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
 }
 
+// ------------------------------------------------- expert GEMMs, A in TMEM
+// Persistent like grouped_gemm_kernel (tiles b, b + grid, ...; every role walks
+// the same K steps) for mode 0 (gate/up, K = H) and mode 1 (down, K = I), but
+// the eight dequantising warps write A straight into tensor memory
+// (tcgen05.st) and the MMAs read it there, so shared memory carries only the
+// raw atoms and B. Worker warp w writes atom a = 2 (w % 4) + w / 4 (rows
+// 16 a .. 16 a + 15, inside the lane quadrant w % 4 that the warp may access).
+__global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmParams p,
+                                                                    const __grid_constant__ CUtensorMap bmap,
+                                                                    const __grid_constant__ CUtensorMap amap,
+                                                                    const __grid_constant__ CUtensorMap amap_shared)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *bst = smem;                                          // kXBStg x 24 KiB, 128-byte swizzled rows
+    uint8_t *raw = smem + kXBStg * kXBBytes;                      // kXRaw x 4608 B
+    uint64_t *bars = reinterpret_cast<uint64_t *>(raw + kXRaw * kPfRawBytes);
+    uint64_t *rawfull = bars, *rawempty = bars + kXRaw;
+    uint64_t *afull = bars + 2 * kXRaw, *aempty = afull + kXAStg;
+    uint64_t *bfull = aempty + kXAStg, *bempty = bfull + kXBStg;
+    uint64_t *accfull = bempty + kXBStg, *accempty = accfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accempty + 2);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ntiles = *p.ntiles * p.m_tiles;
+    const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
+    if (my_tiles == 0) return;                                    // uniform
+    const int nk = (p.mode == 1 ? p.I : p.H) / kPfK;
+    const int total = my_tiles * nk;
+    auto tile_of = [&](int i) { return int(blockIdx.x) + i * int(gridDim.x); };
+
+    if (tid == 0) {
+        for (int r = 0; r < kXRaw; ++r) {
+            mbar_init(&rawfull[r], 1);
+            mbar_init(&rawempty[r], kPfWorkers);
+        }
+        for (int s = 0; s < kXAStg; ++s) {
+            mbar_init(&afull[s], kPfWorkers * 32);
+            mbar_init(&aempty[s], 1);
+        }
+        for (int s = 0; s < kXBStg; ++s) {
+            mbar_init(&bfull[s], 1);
+            mbar_init(&bempty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accfull[b], 1);
+            mbar_init(&accempty[b], kPfEpi * 32);
+        }
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kPfMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kPfRawWarp) {
+        // ---- raw int4 atoms (8 row blocks x one group) per K step: one TMA box each
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&amap) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&amap_shared) : "memory");
+            const uint64_t pol = policy_evict_first();
+            TileInfo ti;
+            int gk = 0;
+            for (; gk < total; ++gk) {
+                const int i = gk / nk, kb = gk % nk, r = gk % kXRaw;
+                if (kb == 0) ti = tile_info(p, tile_of(i) / p.m_tiles);
+                const int mt = tile_of(i) % p.m_tiles;
+                if (gk >= kXRaw && !pf_wait(&rawempty[r], ((gk / kXRaw) - 1) & 1, p.err, abort)) break;
+                if (!ti.valid) {
+                    mbar_arrive(&rawfull[r]);                  // nothing to load; the epilogue writes zeros
+                    continue;
+                }
+                mbar_arrive_expect_tx(&rawfull[r], kPfRawBytes);
+                tma_raw(smem_u32(raw + r * kPfRawBytes), ti.kind == 1 ? &amap_shared : &amap, kb, mt, ti.slot,
+                        &rawfull[r], pol);
+            }
+            for (int g2 = gk - 1; g2 >= 0 && g2 >= gk - kXRaw; --g2)
+                mbar_wait(&rawfull[g2 % kXRaw], (g2 / kXRaw) & 1, p.err);
+        }
+    } else if (warp == kPfBWarp) {
+        // ---- B: rows rowbase .. rowbase + N - 1 of bmap, in boxes of kPfBoxRows rows
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&bmap) : "memory");
+            TileInfo ti;
+            for (int gk = 0; gk < total; ++gk) {
+                const int i = gk / nk, kb = gk % nk, s = gk % kXBStg;
+                if (kb == 0) ti = tile_info(p, tile_of(i) / p.m_tiles);
+                const int nbox = (ti.N + kPfBoxRows - 1) / kPfBoxRows;
+                if (gk >= kXBStg) pf_wait(&bempty[s], ((gk / kXBStg) - 1) & 1, p.err, abort);
+                mbar_arrive_expect_tx(&bfull[s], uint32_t(nbox) * kPfBoxRows * (kPfK * 2));
+                const uint32_t dst = smem_u32(bst + s * kXBBytes);
+                for (int j = 0; j < nbox; ++j)
+                    tma_load_2d(dst + j * (kPfBoxRows * kPfK * 2), &bmap, kb * kPfK, ti.rowbase + j * kPfBoxRows, &bfull[s]);
+            }
+        }
+    } else if (warp == kPfMma) {
+        // ---- MMA issuer: tile i accumulates in TMEM columns (i % 2) * kXMaxN ..
+        if (lane == 0) {
+            uint32_t idesc = 0;
+            int nextN = tile_info(p, tile_of(0) / p.m_tiles).N;
+            for (int gk = 0; gk < total; ++gk) {
+                const int i = gk / nk, kb = gk % nk, sa = gk % kXAStg, sb = gk % kXBStg, b = i & 1;
+                if (kb == 0) {
+                    idesc = umma_idesc(nextN, false);
+                    if (i + 1 < my_tiles) nextN = tile_info(p, tile_of(i + 1) / p.m_tiles).N;
+                    if (i >= 2) pf_wait(&accempty[b], ((i / 2) - 1) & 1, p.err, abort);
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                }
+                pf_wait(&afull[sa], (gk / kXAStg) & 1, p.err, abort);
+                pf_wait(&bfull[sb], (gk / kXBStg) & 1, p.err, abort);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint64_t bd = umma_desc(smem_u32(bst + sb * kXBBytes));
+                const uint32_t acc_t = tmem + uint32_t(b * kXMaxN), a_t = tmem + kXACol0 + uint32_t(32 * sa);
+#pragma unroll
+                for (int k4 = 0; k4 < kPfK / 16; ++k4)
+                    umma_ts(acc_t, a_t + uint32_t(8 * k4), bd + uint64_t(k4 * 2), idesc, (kb | k4) ? 1u : 0u);
+                umma_commit(&aempty[sa]);
+                umma_commit(&bempty[sb]);
+                if (kb == nk - 1) umma_commit(&accfull[b]);
+            }
+            mbar_wait(&accfull[(my_tiles - 1) & 1], ((my_tiles - 1) / 2) & 1, p.err);
+        }
+    } else if (warp < kPfWorkers) {
+        // ---- A: dequantise atom a of each K step into the fragment order of the
+        // 16x256b store: register 4r + {0, 1} = row g, columns 16 t + 4 r .. + 3;
+        // 4r + {2, 3} = row g + 8 (MMA K order: perm64)
+        const int a = 2 * (warp & 3) + (warp >> 2), g = lane >> 2;
+        const uint32_t lane_base = uint32_t(16 * a) << 16;
+        for (int gk = 0; gk < total; ++gk) {
+            const int r = gk % kXRaw, sa = gk % kXAStg;
+            pf_wait(&rawfull[r], (gk / kXRaw) & 1, p.err, abort);
+            const uint8_t *atom = raw + r * kPfRawBytes + a * kAtomBytes;
+            const uint4 q = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
+            const uint2 sbp = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rawempty[r]);
+            const uint32_t s0 = __byte_perm(sbp.x, 0, 0x1010), b0 = __byte_perm(sbp.x, 0, 0x3232);   // row g
+            const uint32_t s1 = __byte_perm(sbp.y, 0, 0x1010), b1 = __byte_perm(sbp.y, 0, 0x3232);   // row g + 8
+            const uint32_t wg[2] = {q.x, q.y}, wh[2] = {q.z, q.w};
+            uint32_t v[16];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const int m0 = 2 * (rr & 1);
+                v[4 * rr + 0] = hfma2(nib_pair_f16(wg[rr >> 1], m0), s0, b0);
+                v[4 * rr + 1] = hfma2(nib_pair_f16(wg[rr >> 1], m0 + 1), s0, b0);
+                v[4 * rr + 2] = hfma2(nib_pair_f16(wh[rr >> 1], m0), s1, b1);
+                v[4 * rr + 3] = hfma2(nib_pair_f16(wh[rr >> 1], m0 + 1), s1, b1);
+            }
+            if (gk >= kXAStg) pf_wait(&aempty[sa], ((gk / kXAStg) - 1) & 1, p.err, abort);
+            tmem_st16x256x4(tmem + lane_base + kXACol0 + uint32_t(32 * sa), v);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            mbar_arrive(&afull[sa]);
+        }
+    } else {
+        // ---- epilogue warps: warp e reads TMEM lanes 32q..32q+31 (q = e % 4) = tile
+        // rows, column chunks of 32 tokens j = 2u + e / 4
+        const int e = warp - kPfWorkers, q = e & 3, half = e >> 2;
+        const int r = 32 * q + lane;
+        bool range_bad = false;
+        auto weights = [&](const TileInfo &t, float (&wv)[3]) {
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+                const int c = 32 * (2 * u + half) + lane;
+                wv[u] = (p.mode == 1 && c < t.n) ? p.pair_w[t.rowbase + c] : 0.f;
+            }
+        };
+        TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
+        float wnext[3];
+        weights(tnext, wnext);
+        for (int i = 0; i < my_tiles; ++i) {
+            const int b = i & 1;
+            const TileInfo ti = tnext;
+            float wv[3] = {wnext[0], wnext[1], wnext[2]};
+            const int mt = tile_of(i) % p.m_tiles;
+            if (i + 1 < my_tiles) {
+                tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
+                weights(tnext, wnext);
+            }
+            pf_wait(&accfull[b], (i / 2) & 1, p.err, abort);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (!ti.valid) set_error(p.err, SMOE_DEV_BAD_SLOT);
+            const float keep = ti.valid ? 1.f : 0.f;
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+                const int j = 2 * u + half;
+                if (32 * j < ti.N) {                      // uniform over the warp
+                    uint32_t v[32];
+                    tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(b * kXMaxN + 32 * j), v);
+                    if (p.mode == 0) {
+                        // rows r (gate) and r ^ 8 (up) of one intermediate unit; h goes to
+                        // its column in the down GEMM's K order
+                        const bool gate_row = (lane & 8) == 0;
+                        const int inter = 64 * mt + 8 * (r >> 4) + (r & 7);
+                        const int hcol = (inter & ~63) | perm64(inter & 63);
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj += 2) {
+                            const float a0 = __uint_as_float(v[jj]) * keep, a1 = __uint_as_float(v[jj + 1]) * keep;
+                            const float other = __shfl_xor_sync(0xffffffffu, gate_row ? a1 : a0, 8);
+                            const float gv = gate_row ? a0 : other, uv = gate_row ? other : a1;
+                            const int c = 32 * j + jj + (gate_row ? 0 : 1);
+                            const float h = silu_f(gv) * uv;
+                            if (c < ti.n) {
+                                range_bad |= !(fabsf(h) < 65504.f);
+                                p.hbuf[size_t(ti.rowbase + c) * p.I + hcol] = f32_to_f16_bits(h);
+                            }
+                        }
+                    } else {
+                        const int R = kPfM * mt + r;
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const int c = 32 * j + jj;
+                            const float wt = __shfl_sync(0xffffffffu, wv[u], jj);
+                            if (c < ti.n) {
+                                const float y = __uint_as_float(v[jj]) * keep * wt;
+                                range_bad |= !(fabsf(y) < 65504.f);
+                                p.ypair[size_t(ti.rowbase + c) * p.H + R] = f32_to_f16_bits(y);
+                            }
+                        }
+                    }
+                }
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            mbar_arrive(&accempty[b]);
+        }
+        if (range_bad) set_error(p.err, SMOE_DEV_RANGE);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == kPfMma)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+}
+
 // ---------------------------------------------------------------- combine
 
 // out[t] = sum_j ypair[pos(t, j)] (route order) + ypair[P + t] (+ residual),
@@ -685,10 +972,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const PrefillParams p)
 
 cudaError_t prefill_config()
 {
-    return cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem);
+    return e;
 }
 
-int prefill_max_tiles(int T, int k, int E) { return (T * k + kPfMaxN - 1) / kPfMaxN + E + (T + kPfMaxN - 1) / kPfMaxN; }
+int prefill_max_tiles(int T, int k, int E) { return (T * k + kXMaxN - 1) / kXMaxN + E + (T + kXMaxN - 1) / kXMaxN; }
 
 static int g_num_sms = 0;
 
@@ -800,11 +1089,11 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
     g.mode = 0;
     g.m_tiles = g.I / 64;
     if ((e = prof_record(nprof > 0 ? prof[0] : nullptr, st)) != cudaSuccess) return e;
-    grouped_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kPfThreads, kPfSmem, st>>>(g, xmap, gu_pool, gu_shared);
+    expert_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kPfThreads, kXSmem, st>>>(g, xmap, gu_pool, gu_shared);
     if ((e = prof_record(nprof > 1 ? prof[1] : nullptr, st)) != cudaSuccess) return e;
     g.mode = 1;
     g.m_tiles = p.H / kPfM;
-    grouped_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kPfThreads, kPfSmem, st>>>(g, hmap, dn_pool, dn_shared);
+    expert_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kPfThreads, kXSmem, st>>>(g, hmap, dn_pool, dn_shared);
     if ((e = prof_record(nprof > 2 ? prof[2] : nullptr, st)) != cudaSuccess) return e;
     combine_kernel<<<dim3((p.H / 4 + 255) / 256, p.T), 256, 0, st>>>(p);
     return cudaGetLastError();
