@@ -38,8 +38,7 @@ namespace smoe {
 constexpr int kPfM = 128;          // weight rows per tile
 constexpr int kPfK = 64;           // K per pipeline step (one quantisation group)
 constexpr int kPfMaxN = 256;       // tokens per tile
-constexpr int kPfRaw = 6;          // raw int4 atom slots (one K step each)
-constexpr int kPfAB = 4;           // A/B operand stages
+constexpr int kPfAB = 4;           // router GEMM: A/B operand stages
 constexpr int kPfBoxRows = 64;     // B rows per TMA box
 constexpr int kPfWorkers = 8;      // warps: A (dequantisation, or router rows)
 constexpr int kPfEpi = 8;          // warps: epilogue (two per TMEM lane quadrant)
@@ -51,7 +50,7 @@ constexpr int kPfRawBytes = 8 * kAtomBytes;         // 4608: 8 row blocks x one 
 constexpr int kPfABytes = kPfM * kPfK * 2;          // 16 KiB
 constexpr int kPfBBytes = kPfMaxN * kPfK * 2;       // 32 KiB
 constexpr int kPfStageBytes = kPfABytes + kPfBBytes;
-constexpr int kPfSmem = kPfAB * kPfStageBytes + kPfRaw * kPfRawBytes + 1024 /*align*/ + 512 /*barriers*/;
+constexpr int kPfSmem = kPfAB * kPfStageBytes + 1024 /*align*/ + 512 /*barriers*/;
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
 constexpr int kBucketTok = 64;     // tokens per bucketing chunk
 
@@ -422,45 +421,34 @@ __device__ __forceinline__ void tma_raw(uint32_t dst, const CUtensorMap *map, in
                  : "memory");
 }
 
-// Persistent: CTA b handles tiles b, b + grid, ... (tile = row-run x m_tiles
-// weight-row blocks); every role walks the same flattened sequence of K steps.
-// mode 0 gate/up (K = H), 1 down (K = I), 2 router logits (K = H).
-// Roles: 8 warps fill A (dequantising raw atoms, or copying router rows),
-// 8 warps run the epilogue, one warp streams raw atoms from HBM (amap: the
-// pool's gate/up or down atoms, amap_shared: the shared expert's), one loads
-// B rows with TMA (bmap: xs for mode 0, h for mode 1, x for mode 2; tile rows
-// rowbase ..), one issues MMAs.
-__global__ void __launch_bounds__(kPfThreads, 1) grouped_gemm_kernel(const GemmParams p,
-                                                                     const __grid_constant__ CUtensorMap bmap,
-                                                                     const __grid_constant__ CUtensorMap amap,
-                                                                     const __grid_constant__ CUtensorMap amap_shared)
+// Router logits for large T on tensor cores: logits[t][e] = W_r[e] . x[t]
+// (row E: the shared-gate vector), bf16 operands, fp32 accumulation.
+// Persistent: CTA b handles tiles b, b + grid, ... (tile = 256 tokens x 128
+// router rows); roles: 8 warps copy the router rows into A stages
+// (cp.async, one step ahead), one warp loads the tokens (B) with TMA, one
+// issues the MMAs into a double-buffered TMEM accumulator, 8 warps store the
+// logits.
+__global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmParams p,
+                                                                    const __grid_constant__ CUtensorMap bmap)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ab = smem;                                           // kPfAB x (A 16 KiB | B 32 KiB)
-    uint8_t *raw = smem + kPfAB * kPfStageBytes;                  // kPfRaw x 4608 B
-    uint64_t *bars = reinterpret_cast<uint64_t *>(raw + kPfRaw * kPfRawBytes);
-    uint64_t *rawfull = bars, *rawempty = bars + kPfRaw;
-    uint64_t *afull = bars + 2 * kPfRaw, *bfull = afull + kPfAB, *empty = bfull + kPfAB;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kPfAB * kPfStageBytes);
+    uint64_t *afull = bars, *bfull = afull + kPfAB, *empty = bfull + kPfAB;
     uint64_t *accfull = empty + kPfAB, *accempty = accfull + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accempty + 2);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nrun = p.mode == 2 ? (p.T + kPfMaxN - 1) / kPfMaxN : *p.ntiles;
-    const int ntiles = nrun * p.m_tiles;
+    const int ntiles = (p.T + kPfMaxN - 1) / kPfMaxN * p.m_tiles;
     const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
     if (my_tiles == 0) return;                                    // uniform
-    const int K = p.mode == 1 ? p.I : p.H;
-    const int nk = K / kPfK;
-    const int total = my_tiles * nk;                              // K steps of this CTA
+    const int nk = p.H / kPfK;
+    const int total = my_tiles * nk;
     auto tile_of = [&](int i) { return int(blockIdx.x) + i * int(gridDim.x); };
 
     if (tid == 0) {
-        for (int r = 0; r < kPfRaw; ++r) {
-            mbar_init(&rawfull[r], 1);
-            mbar_init(&rawempty[r], kPfWorkers);
-        }
         for (int s = 0; s < kPfAB; ++s) {
             mbar_init(&afull[s], kPfWorkers * 32);
             mbar_init(&bfull[s], 1);
@@ -482,33 +470,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) grouped_gemm_kernel(const GemmP
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kPfRawWarp) {
-        // ---- raw int4 atoms (8 row blocks x one group) per K step: one TMA box each
-        if (lane == 0 && p.mode != 2) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&amap) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&amap_shared) : "memory");
-            const uint64_t pol = policy_evict_first();
-            TileInfo ti;
-            int gk = 0;
-            for (; gk < total; ++gk) {
-                const int i = gk / nk, kb = gk % nk, r = gk % kPfRaw;
-                if (kb == 0) ti = tile_info(p, tile_of(i) / p.m_tiles);
-                const int mt = tile_of(i) % p.m_tiles;
-                if (gk >= kPfRaw && !pf_wait(&rawempty[r], ((gk / kPfRaw) - 1) & 1, p.err, abort)) break;
-                if (!ti.valid) {
-                    mbar_arrive(&rawfull[r]);                  // nothing to load; the epilogue writes zeros
-                    continue;
-                }
-                mbar_arrive_expect_tx(&rawfull[r], kPfRawBytes);
-                tma_raw(smem_u32(raw + r * kPfRawBytes), ti.kind == 1 ? &amap_shared : &amap, kb, mt, ti.slot,
-                        &rawfull[r], pol);
-            }
-            // let the last copy into each slot land before the CTA can exit
-            for (int g2 = gk - 1; g2 >= 0 && g2 >= gk - kPfRaw; --g2)
-                mbar_wait(&rawfull[g2 % kPfRaw], (g2 / kPfRaw) & 1, p.err);
-        }
-    } else if (warp == kPfBWarp) {
-        // ---- B: rows rowbase .. rowbase + N - 1 of bmap, in boxes of kPfBoxRows rows
+    if (warp == kPfBWarp) {
+        // ---- B: tokens p0 .. p0 + N - 1 in boxes of kPfBoxRows rows
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&bmap) : "memory");
             TileInfo ti;
@@ -527,12 +490,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) grouped_gemm_kernel(const GemmP
         // ---- MMA issuer: tile i accumulates in TMEM buffer i % 2 (256 columns each)
         if (lane == 0) {
             uint32_t idesc = 0;
-            int nextN = tile_info(p, tile_of(0) / p.m_tiles).N;
             for (int gk = 0; gk < total; ++gk) {
                 const int i = gk / nk, kb = gk % nk, s = gk % kPfAB, b = i & 1;
                 if (kb == 0) {
-                    idesc = umma_idesc(nextN, p.mode == 2);
-                    if (i + 1 < my_tiles) nextN = tile_info(p, tile_of(i + 1) / p.m_tiles).N;   // used one tile later
+                    idesc = umma_idesc(tile_info(p, tile_of(i) / p.m_tiles).N, true);
                     if (i >= 2) pf_wait(&accempty[b], ((i / 2) - 1) & 1, p.err, abort);
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 }
@@ -549,141 +510,54 @@ __global__ void __launch_bounds__(kPfThreads, 1) grouped_gemm_kernel(const GemmP
                 umma_commit(&empty[s]);
                 if (kb == nk - 1) umma_commit(&accfull[b]);
             }
-            // the tensor cores are done with TMEM and shared memory before the CTA exits
             mbar_wait(&accfull[(my_tiles - 1) & 1], ((my_tiles - 1) / 2) & 1, p.err);
         }
     } else if (warp < kPfWorkers) {
-        if (p.mode != 2) {
-            // ---- A by dequantisation: warp a takes atom a (row block 8 mt + a);
-            // lane L = 4g + t holds rows (g, g + 8) x 16 columns of it
-            const int a = warp, g = lane >> 2, t = lane & 3;
-            for (int gk = 0; gk < total; ++gk) {
-                const int s = gk % kPfAB, r = gk % kPfRaw;
-                pf_wait(&rawfull[r], (gk / kPfRaw) & 1, p.err, abort);
-                const uint8_t *atom = raw + r * kPfRawBytes + a * kAtomBytes;
-                const uint4 q = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
-                const uint2 sbp = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&rawempty[r]);
-                const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-                uint32_t o[4][4];
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint32_t sbw = (w >> 1) ? sbp.y : sbp.x;   // fp16 (s, b) of row g or g + 8
-                    const uint32_t s2 = __byte_perm(sbw, 0, 0x1010), b2 = __byte_perm(sbw, 0, 0x3232);
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) o[w][m] = hfma2(nib_pair_f16(words[w], m), s2, b2);   // s q + b, one rounding
+        // ---- A = router rows (row E: the shared-gate vector; rows past E zero), one step ahead
+        auto issue_a = [&](int gi) {
+            if (gi < total) {
+                const int i = gi / nk, kb = gi % nk, s = gi % kPfAB;
+                if (gi >= kPfAB) pf_wait(&empty[s], ((gi / kPfAB) - 1) & 1, p.err, abort);
+                const int mt = tile_of(i) % p.m_tiles;
+                const uint32_t sa_u = smem_u32(ab + s * kPfStageBytes);
+                for (int q = tid; q < kPfM * 8; q += kPfWorkers * 32) {
+                    const int r = q >> 3, c8 = q & 7;
+                    const int e = mt * kPfM + r;
+                    const uint16_t *src = e < p.E ? p.Wr + size_t(e) * p.H : p.ws;
+                    cp_async16(sa_u + sw128(r, c8 * 8), src + kb * kPfK + c8 * 8, e <= p.E ? 16u : 0u);
                 }
-                if (gk >= kPfAB) pf_wait(&empty[s], ((gk / kPfAB) - 1) & 1, p.err, abort);
-                uint8_t *sa = ab + s * kPfStageBytes;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int row = 16 * a + g + 8 * (w >> 1);       // word w: column half w & 1, row g or g + 8
-                    *reinterpret_cast<uint4 *>(sa + sw128(row, 16 * t + 8 * (w & 1))) =
-                        make_uint4(o[w][0], o[w][1], o[w][2], o[w][3]);
-                }
-                fence_async_smem();
-                mbar_arrive(&afull[s]);
             }
-        } else {
-            // ---- A = router rows (row E: the shared-gate vector; rows past E zero), one step ahead
-            auto issue_a = [&](int gi) {
-                if (gi < total) {
-                    const int i = gi / nk, kb = gi % nk, s = gi % kPfAB;
-                    if (gi >= kPfAB) pf_wait(&empty[s], ((gi / kPfAB) - 1) & 1, p.err, abort);
-                    const int mt = tile_of(i) % p.m_tiles;
-                    const uint32_t sa_u = smem_u32(ab + s * kPfStageBytes);
-                    for (int q = tid; q < kPfM * 8; q += kPfWorkers * 32) {
-                        const int r = q >> 3, c8 = q & 7;
-                        const int e = mt * kPfM + r;
-                        const uint16_t *src = e < p.E ? p.Wr + size_t(e) * p.H : p.ws;
-                        cp_async16(sa_u + sw128(r, c8 * 8), src + kb * kPfK + c8 * 8, e <= p.E ? 16u : 0u);
-                    }
-                }
-                asm volatile("cp.async.commit_group;" ::: "memory");   // one group per step, even if empty
-            };
-            issue_a(0);
-            for (int gk = 0; gk < total; ++gk) {
-                issue_a(gk + 1);
-                asm volatile("cp.async.wait_group 1;" ::: "memory");  // this step's rows have landed
-                fence_async_smem();
-                mbar_arrive(&afull[gk % kPfAB]);
-            }
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            asm volatile("cp.async.commit_group;" ::: "memory");   // one group per step, even if empty
+        };
+        issue_a(0);
+        for (int gk = 0; gk < total; ++gk) {
+            issue_a(gk + 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");  // this step's rows have landed
+            fence_async_smem();
+            mbar_arrive(&afull[gk % kPfAB]);
         }
-    } else {
-        // ---- epilogue warps: warp e reads TMEM lanes 32q..32q+31 (q = e % 4, the
-        // quadrant its warp index allows) = tile rows, column chunks of 32 tokens
-        // j = 2u + e / 4
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+    } else if (warp < kPfWorkers + kPfEpi) {
+        // ---- epilogue warps: TMEM lanes 32q..32q+31 (q = e % 4) = router rows,
+        // column chunks of 32 tokens j = 2u + e / 4
         const int e = warp - kPfWorkers, q = e & 3, half = e >> 2;
         const int r = 32 * q + lane;
-        bool range_bad = false;
-        // mode 1: weight of column 32 j + lane; the next tile's are loaded one tile ahead
-        auto weights = [&](const TileInfo &t, float (&wv)[4]) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = 32 * (2 * u + half) + lane;
-                wv[u] = (p.mode == 1 && c < t.n) ? p.pair_w[t.rowbase + c] : 0.f;
-            }
-        };
-        TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
-        float wnext[4];
-        weights(tnext, wnext);
         for (int i = 0; i < my_tiles; ++i) {
             const int b = i & 1;
-            const TileInfo ti = tnext;
-            float wv[4] = {wnext[0], wnext[1], wnext[2], wnext[3]};
-            const int mt = tile_of(i) % p.m_tiles;
-            if (i + 1 < my_tiles) {
-                tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
-                weights(tnext, wnext);
-            }
+            const TileInfo ti = tile_info(p, tile_of(i) / p.m_tiles);
+            const int ex = kPfM * (tile_of(i) % p.m_tiles) + r;
             pf_wait(&accfull[b], (i / 2) & 1, p.err, abort);
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            if (!ti.valid) set_error(p.err, SMOE_DEV_BAD_SLOT);
-            const float keep = ti.valid ? 1.f : 0.f;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int j = 2 * u + half;
                 if (32 * j < ti.N) {                      // uniform over the warp
                     uint32_t v[32];
                     tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(b * 256 + 32 * j), v);
-                    if (p.mode == 0) {
-                        // rows r (gate) and r ^ 8 (up) of one intermediate unit: per column
-                        // pair the gate lane takes the even column, the up lane the odd one
-                        const bool gate_row = (lane & 8) == 0;
-                        const int inter = 64 * mt + 8 * (r >> 4) + (r & 7);
 #pragma unroll
-                        for (int jj = 0; jj < 32; jj += 2) {
-                            const float a0 = __uint_as_float(v[jj]) * keep, a1 = __uint_as_float(v[jj + 1]) * keep;
-                            const float other = __shfl_xor_sync(0xffffffffu, gate_row ? a1 : a0, 8);
-                            const float gv = gate_row ? a0 : other, uv = gate_row ? other : a1;
-                            const int c = 32 * j + jj + (gate_row ? 0 : 1);
-                            const float h = silu_f(gv) * uv;
-                            if (c < ti.n) {
-                                range_bad |= !(fabsf(h) < 65504.f);
-                                p.hbuf[size_t(ti.rowbase + c) * p.I + inter] = f32_to_f16_bits(h);
-                            }
-                        }
-                    } else if (p.mode == 1) {
-                        const int R = kPfM * mt + r;
-#pragma unroll
-                        for (int jj = 0; jj < 32; ++jj) {
-                            const int c = 32 * j + jj;
-                            const float wt = __shfl_sync(0xffffffffu, wv[u], jj);
-                            if (c < ti.n) {
-                                const float y = __uint_as_float(v[jj]) * keep * wt;
-                                range_bad |= !(fabsf(y) < 65504.f);
-                                p.ypair[size_t(ti.rowbase + c) * p.H + R] = f32_to_f16_bits(y);
-                            }
-                        }
-                    } else {
-                        const int ex = kPfM * mt + r;
-#pragma unroll
-                        for (int jj = 0; jj < 32; ++jj) {
-                            const int c = 32 * j + jj;
-                            if (c < ti.n && ex <= p.E) p.logits[size_t(ti.p0 + c) * (p.E + 1) + ex] = __uint_as_float(v[jj]);
-                        }
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int c = 32 * j + jj;
+                        if (c < ti.n && ex <= p.E) p.logits[size_t(ti.p0 + c) * (p.E + 1) + ex] = __uint_as_float(v[jj]);
                     }
                 }
             }
@@ -691,7 +565,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) grouped_gemm_kernel(const GemmP
             __syncwarp();
             mbar_arrive(&accempty[b]);
         }
-        if (range_bad) set_error(p.err, SMOE_DEV_RANGE);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -700,7 +573,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) grouped_gemm_kernel(const GemmP
 }
 
 // ------------------------------------------------- expert GEMMs, A in TMEM
-// Persistent like grouped_gemm_kernel (tiles b, b + grid, ...; every role walks
+// Persistent like router_gemm_kernel (tiles b, b + grid, ...; every role walks
 // the same K steps) for mode 0 (gate/up, K = H) and mode 1 (down, K = I), but
 // the eight dequantising warps write A straight into tensor memory
 // (tcgen05.st) and the MMAs read it there, so shared memory carries only the
@@ -972,7 +845,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const PrefillParams p)
 
 cudaError_t prefill_config()
 {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem);
     return e;
 }
@@ -1060,7 +933,7 @@ cudaError_t launch_router_gemm(const RouteParams &r, cudaStream_t st)
     cudaError_t e = rows_map(&xmap, r.x, true, uint64_t(r.H), uint64_t(r.T));
     if (e != cudaSuccess) return e;
     const int ntile = (r.T + kPfMaxN - 1) / kPfMaxN;
-    grouped_gemm_kernel<<<persistent_grid(ntile * g.m_tiles), kPfThreads, kPfSmem, st>>>(g, xmap, xmap, xmap);
+    router_gemm_kernel<<<persistent_grid(ntile * g.m_tiles), kPfThreads, kPfSmem, st>>>(g, xmap);
     return cudaGetLastError();
 }
 
