@@ -55,18 +55,17 @@ static_assert(kPfSmem <= 232448, "shared memory per CTA");
 constexpr int kBucketTok = 64;     // tokens per bucketing chunk
 
 // Expert GEMMs (gate/up, down): A (the dequantised weights) lives in tensor
-// memory. TMEM columns: two accumulators of kXMaxN columns, then kXAStg A
+// memory. TMEM columns: two accumulators of kXMaxN columns, then kXStg A
 // stages of 32 columns (128 rows x 64 fp16 K values). Shared memory holds only
 // the B stages and the raw atoms.
 constexpr int kXMaxN = 192;        // tokens per expert tile
-constexpr int kXRaw = 12;          // raw atom slots
-constexpr int kXAStg = 4;          // A stages in TMEM
-constexpr int kXBStg = 6;          // B stages in shared memory
+constexpr int kXRaw = 16;          // raw atom slots
+constexpr int kXStg = 4;           // operand stages: A in TMEM + B in shared memory, one barrier pair each
 constexpr int kXBBytes = kXMaxN * kPfK * 2;                 // 24 KiB
 constexpr uint32_t kXACol0 = 2 * kXMaxN;                    // first A column (384)
-constexpr int kXSmem = kXBStg * kXBBytes + kXRaw * kPfRawBytes + 1024 /*align*/ + 512 /*barriers*/;
+constexpr int kXSmem = kXStg * kXBBytes + kXRaw * kPfRawBytes + 1024 /*align*/ + 512 /*barriers*/;
 static_assert(kXSmem <= 232448, "shared memory per CTA");
-static_assert(kXACol0 + kXAStg * 32 <= 512, "TMEM columns");
+static_assert(kXACol0 + kXStg * 32 <= 512, "TMEM columns");
 
 __device__ __forceinline__ uint32_t sw128(int r, int c)   // byte offset of (row, col) in a 64-col bf16 tile
 {
@@ -370,6 +369,17 @@ __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, int32_t 
     return true;
 }
 
+// pf_wait that first polls without sleeping (the phase is usually complete
+// already, and a non-blocking test returns sooner than a suspending try).
+__device__ __forceinline__ bool pf_wait_fast(uint64_t *bar, uint32_t parity, int32_t *err, volatile int *abort)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok ? true : pf_wait(bar, parity, err, abort);
+}
+
 struct TileInfo {
     int n, N, rowbase, p0, kind;
     int slot;              // pool slot of the tile's expert (0 for the shared expert)
@@ -586,13 +596,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *bst = smem;                                          // kXBStg x 24 KiB, 128-byte swizzled rows
-    uint8_t *raw = smem + kXBStg * kXBBytes;                      // kXRaw x 4608 B
+    uint8_t *bst = smem;                                          // kXStg x 24 KiB, 128-byte swizzled rows
+    uint8_t *raw = smem + kXStg * kXBBytes;                       // kXRaw x 4608 B
     uint64_t *bars = reinterpret_cast<uint64_t *>(raw + kXRaw * kPfRawBytes);
     uint64_t *rawfull = bars, *rawempty = bars + kXRaw;
-    uint64_t *afull = bars + 2 * kXRaw, *aempty = afull + kXAStg;
-    uint64_t *bfull = aempty + kXAStg, *bempty = bfull + kXBStg;
-    uint64_t *accfull = bempty + kXBStg, *accempty = accfull + 2;
+    uint64_t *full = bars + 2 * kXRaw, *empty = full + kXStg;     // stage s: A (TMEM) + B (smem)
+    uint64_t *accfull = empty + kXStg, *accempty = accfull + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accempty + 2);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -609,13 +618,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
             mbar_init(&rawfull[r], 1);
             mbar_init(&rawempty[r], kPfWorkers);
         }
-        for (int s = 0; s < kXAStg; ++s) {
-            mbar_init(&afull[s], kPfWorkers * 32);
-            mbar_init(&aempty[s], 1);
-        }
-        for (int s = 0; s < kXBStg; ++s) {
-            mbar_init(&bfull[s], 1);
-            mbar_init(&bempty[s], 1);
+        for (int s = 0; s < kXStg; ++s) {
+            mbar_init(&full[s], kPfWorkers * 32 + 1);             // the A threads + the B producer (with bytes)
+            mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accfull[b], 1);
@@ -633,72 +638,88 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
+    // Ring positions advance by one per K step (index and phase bit); a producer
+    // waits for the slot's release with the opposite parity, which a fresh
+    // barrier passes, so the first round needs no special case.
     if (warp == kPfRawWarp) {
         // ---- raw int4 atoms (8 row blocks x one group) per K step: one TMA box each
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&amap) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(&amap_shared) : "memory");
             const uint64_t pol = policy_evict_first();
-            TileInfo ti;
-            int gk = 0;
-            for (; gk < total; ++gk) {
-                const int i = gk / nk, kb = gk % nk, r = gk % kXRaw;
-                if (kb == 0) ti = tile_info(p, tile_of(i) / p.m_tiles);
+            int r = 0, done = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int i = 0; i < my_tiles && ok; ++i) {
+                const TileInfo ti = tile_info(p, tile_of(i) / p.m_tiles);
                 const int mt = tile_of(i) % p.m_tiles;
-                if (gk >= kXRaw && !pf_wait(&rawempty[r], ((gk / kXRaw) - 1) & 1, p.err, abort)) break;
-                if (!ti.valid) {
-                    mbar_arrive(&rawfull[r]);                  // nothing to load; the epilogue writes zeros
-                    continue;
+                const CUtensorMap *map = ti.kind == 1 ? &amap_shared : &amap;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!pf_wait(&rawempty[r], ph ^ 1u, p.err, abort)) { ok = false; break; }
+                    if (ti.valid) {
+                        mbar_arrive_expect_tx(&rawfull[r], kPfRawBytes);
+                        tma_raw(smem_u32(raw + r * kPfRawBytes), map, kb, mt, ti.slot, &rawfull[r], pol);
+                    } else {
+                        mbar_arrive(&rawfull[r]);              // nothing to load; the epilogue writes zeros
+                    }
+                    ++done;
+                    if (++r == kXRaw) { r = 0; ph ^= 1u; }
                 }
-                mbar_arrive_expect_tx(&rawfull[r], kPfRawBytes);
-                tma_raw(smem_u32(raw + r * kPfRawBytes), ti.kind == 1 ? &amap_shared : &amap, kb, mt, ti.slot,
-                        &rawfull[r], pol);
             }
-            for (int g2 = gk - 1; g2 >= 0 && g2 >= gk - kXRaw; --g2)
+            // let the last copy into each slot land before the CTA can exit
+            for (int g2 = done - 1; g2 >= 0 && g2 >= done - kXRaw; --g2)
                 mbar_wait(&rawfull[g2 % kXRaw], (g2 / kXRaw) & 1, p.err);
         }
     } else if (warp == kPfBWarp) {
         // ---- B: rows rowbase .. rowbase + N - 1 of bmap, in boxes of kPfBoxRows rows
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&bmap) : "memory");
-            TileInfo ti;
-            for (int gk = 0; gk < total; ++gk) {
-                const int i = gk / nk, kb = gk % nk, s = gk % kXBStg;
-                if (kb == 0) ti = tile_info(p, tile_of(i) / p.m_tiles);
+            int sb = 0;
+            uint32_t ph = 0;
+            for (int i = 0; i < my_tiles; ++i) {
+                const TileInfo ti = tile_info(p, tile_of(i) / p.m_tiles);
                 const int nbox = (ti.N + kPfBoxRows - 1) / kPfBoxRows;
-                if (gk >= kXBStg) pf_wait(&bempty[s], ((gk / kXBStg) - 1) & 1, p.err, abort);
-                mbar_arrive_expect_tx(&bfull[s], uint32_t(nbox) * kPfBoxRows * (kPfK * 2));
-                const uint32_t dst = smem_u32(bst + s * kXBBytes);
-                for (int j = 0; j < nbox; ++j)
-                    tma_load_2d(dst + j * (kPfBoxRows * kPfK * 2), &bmap, kb * kPfK, ti.rowbase + j * kPfBoxRows, &bfull[s]);
+                const uint32_t bytes = uint32_t(nbox) * kPfBoxRows * (kPfK * 2);
+                for (int kb = 0; kb < nk; ++kb) {
+                    pf_wait(&empty[sb], ph ^ 1u, p.err, abort);
+                    mbar_arrive_expect_tx(&full[sb], bytes);
+                    const uint32_t dst = smem_u32(bst + sb * kXBBytes);
+                    for (int j = 0; j < nbox; ++j)
+                        tma_load_2d(dst + j * (kPfBoxRows * kPfK * 2), &bmap, kb * kPfK, ti.rowbase + j * kPfBoxRows,
+                                    &full[sb]);
+                    if (++sb == kXStg) { sb = 0; ph ^= 1u; }
+                }
             }
         }
     } else if (warp == kPfMma) {
         // ---- MMA issuer: tile i accumulates in TMEM columns (i % 2) * kXMaxN ..
         if (lane == 0) {
-            uint32_t idesc = 0;
+            int s = 0;
+            uint32_t ph = 0;
             int nextN = tile_info(p, tile_of(0) / p.m_tiles).N;
-            for (int gk = 0; gk < total; ++gk) {
-                const int i = gk / nk, kb = gk % nk, sa = gk % kXAStg, sb = gk % kXBStg, b = i & 1;
-                if (kb == 0) {
-                    idesc = umma_idesc(nextN, false);
-                    if (i + 1 < my_tiles) nextN = tile_info(p, tile_of(i + 1) / p.m_tiles).N;
-                    if (i >= 2) pf_wait(&accempty[b], ((i / 2) - 1) & 1, p.err, abort);
-                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                }
-                pf_wait(&afull[sa], (gk / kXAStg) & 1, p.err, abort);
-                pf_wait(&bfull[sb], (gk / kXBStg) & 1, p.err, abort);
+            for (int i = 0; i < my_tiles; ++i) {
+                const int b = i & 1;
+                const uint32_t idesc = umma_idesc(nextN, false);
+                if (i + 1 < my_tiles) nextN = tile_info(p, tile_of(i + 1) / p.m_tiles).N;   // used one tile later
+                pf_wait(&accempty[b], ((i >> 1) & 1) ^ 1u, p.err, abort);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint64_t bd = umma_desc(smem_u32(bst + sb * kXBBytes));
-                const uint32_t acc_t = tmem + uint32_t(b * kXMaxN), a_t = tmem + kXACol0 + uint32_t(32 * sa);
+                const uint32_t acc_t = tmem + uint32_t(b * kXMaxN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    pf_wait_fast(&full[s], ph, p.err, abort);
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint64_t bd = umma_desc(smem_u32(bst + s * kXBBytes));
+                    const uint32_t a_t = tmem + kXACol0 + uint32_t(32 * s);
+                    umma_ts(acc_t, a_t, bd, idesc, kb ? 1u : 0u);
 #pragma unroll
-                for (int k4 = 0; k4 < kPfK / 16; ++k4)
-                    umma_ts(acc_t, a_t + uint32_t(8 * k4), bd + uint64_t(k4 * 2), idesc, (kb | k4) ? 1u : 0u);
-                umma_commit(&aempty[sa]);
-                umma_commit(&bempty[sb]);
-                if (kb == nk - 1) umma_commit(&accfull[b]);
+                    for (int k4 = 1; k4 < kPfK / 16; ++k4)
+                        umma_ts(acc_t, a_t + uint32_t(8 * k4), bd + uint64_t(k4 * 2), idesc, 1u);
+                    umma_commit(&empty[s]);
+                    if (++s == kXStg) { s = 0; ph ^= 1u; }
+                }
+                umma_commit(&accfull[b]);
             }
-            mbar_wait(&accfull[(my_tiles - 1) & 1], ((my_tiles - 1) / 2) & 1, p.err);
+            // the tensor cores are done with TMEM and shared memory before the CTA exits
+            mbar_wait(&accfull[(my_tiles - 1) & 1], ((my_tiles - 1) >> 1) & 1, p.err);
         }
     } else if (warp < kPfWorkers) {
         // ---- A: dequantise atom a of each K step into the fragment order of the
@@ -706,14 +727,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
         // 4r + {2, 3} = row g + 8 (MMA K order: perm64)
         const int a = 2 * (warp & 3) + (warp >> 2), g = lane >> 2;
         const uint32_t lane_base = uint32_t(16 * a) << 16;
+        int r = 0, sa = 0;
+        uint32_t phr = 0, pha = 0;                                // raw ring, operand ring
         for (int gk = 0; gk < total; ++gk) {
-            const int r = gk % kXRaw, sa = gk % kXAStg;
-            pf_wait(&rawfull[r], (gk / kXRaw) & 1, p.err, abort);
+            pf_wait(&rawfull[r], phr, p.err, abort);
             const uint8_t *atom = raw + r * kPfRawBytes + a * kAtomBytes;
             const uint4 q = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
             const uint2 sbp = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
             __syncwarp();
             if (lane == 0) mbar_arrive(&rawempty[r]);
+            if (++r == kXRaw) { r = 0; phr ^= 1u; }
             const uint32_t s0 = __byte_perm(sbp.x, 0, 0x1010), b0 = __byte_perm(sbp.x, 0, 0x3232);   // row g
             const uint32_t s1 = __byte_perm(sbp.y, 0, 0x1010), b1 = __byte_perm(sbp.y, 0, 0x3232);   // row g + 8
             const uint32_t wg[2] = {q.x, q.y}, wh[2] = {q.z, q.w};
@@ -726,11 +749,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
                 v[4 * rr + 2] = hfma2(nib_pair_f16(wh[rr >> 1], m0), s1, b1);
                 v[4 * rr + 3] = hfma2(nib_pair_f16(wh[rr >> 1], m0 + 1), s1, b1);
             }
-            if (gk >= kXAStg) pf_wait(&aempty[sa], ((gk / kXAStg) - 1) & 1, p.err, abort);
+            pf_wait(&empty[sa], pha ^ 1u, p.err, abort);
             tmem_st16x256x4(tmem + lane_base + kXACol0 + uint32_t(32 * sa), v);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            mbar_arrive(&afull[sa]);
+            mbar_arrive(&full[sa]);
+            if (++sa == kXStg) { sa = 0; pha ^= 1u; }
         }
     } else {
         // ---- epilogue warps: warp e reads TMEM lanes 32q..32q+31 (q = e % 4) = tile
