@@ -60,7 +60,8 @@ extern "C" {
 #define SMOE_DEV_BAD_SLOT 1     /* a selected expert's slot is < 0 or >= n_slots */
 #define SMOE_DEV_BAD_EXPERT 2   /* an id in ids[] is < 0 or >= E */
 #define SMOE_DEV_TIMEOUT 3      /* a bounded wait inside a kernel gave up */
-#define SMOE_DEV_RANGE 4        /* T > 8 path: |x| or |h| >= 65504 (outside its fp16 operands) */
+#define SMOE_DEV_RANGE 4        /* T > 8 path: |x| or |h| >= 65504, or an expert output that rounds to
+                                   65504 or beyond in fp16 (outside its fp16 intermediates) */
 
 /* ------------------------------------------------------------------ shapes */
 /* H: hidden size; E: routed experts per layer; k: experts per token;
@@ -197,8 +198,9 @@ SMOE_API int moe_route(const smoe_ctx *ctx, const uint16_t *W_r, const uint16_t 
  * scheduling, slot placement or run: bit-identical across runs and slot
  * permutations. T <= 8 takes the fused decode kernel (weights exact, fp32
  * intermediates); larger T the token-bucketed path, whose tensor-core GEMMs
- * take fp16 operands (dequantised weights, x, h), so it needs |x| < 65504
- * (else SMOE_DEV_RANGE in the error word). Errors: SMOE_EINVAL, SMOE_ENOMEM,
+ * take fp16 operands (dequantised weights, x, h) and stores each expert's
+ * output in fp16 before the weighted combine, so it needs |x| < 65504 (else
+ * SMOE_DEV_RANGE in the error word). Errors: SMOE_EINVAL, SMOE_ENOMEM,
  * SMOE_ECUDA. */
 SMOE_API int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x, int32_t T,
                 const int32_t *ids, const float *w, const float *gate,

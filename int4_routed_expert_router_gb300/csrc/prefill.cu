@@ -2,21 +2,21 @@
 //
 //   bucketing: a deterministic counting sort of the T*k (token, slot) pairs by
 //     expert (per-chunk counts, one scan, an ordered scatter), plus the list of
-//     GEMM tiles: per expert, runs of up to 256 of its pairs; the shared
+//     GEMM tiles: per expert, runs of up to 192 of its pairs; the shared
 //     expert takes all T tokens;
-//   row gather: x rows in expert order (the routed pairs, then all T tokens for
-//     the shared expert), converted to fp16, with each row's routing weight
-//     (or shared-expert gate), so that every GEMM tile reads contiguous rows;
+//   token conversion: x to fp16 in the MMA's K order, one row per token;
 //   gate/up GEMM: per tile, 128 weight rows (64 gate + 64 up rows, interleaved
 //     in blocks of 8 as the blob stores them) x its tokens (at most 192), K = H;
-//     the int4 atoms are dequantised to fp16 straight into tensor memory and
-//     multiplied on tcgen05 tensor cores (A from TMEM, B from 128-byte-swizzled
-//     shared memory) with the accumulator in TMEM; the epilogue applies SwiGLU
-//     and writes h;
+//     the int4 atoms are dequantised to fp16 straight into tensor memory, the
+//     tile's token rows are gathered into 128-byte-swizzled shared memory, and
+//     tcgen05 tensor cores multiply them (A from TMEM, B from shared memory)
+//     into an accumulator in TMEM; the epilogue applies SwiGLU and writes h in
+//     expert order;
 //   down GEMM: per tile, 128 down rows x its pairs, K = I, B = h rows; the
-//     epilogue scales by the routing weight (or the shared-expert gate);
-//   combine: per token, the k pair outputs in route order, then the shared
-//     expert (and the residual), rounded once to bf16.
+//     epilogue stores each pair's expert output;
+//   combine: per token, the k pair outputs times their routing weights in route
+//     order, then the shared expert times its gate (and the residual), summed in
+//     fp32 and rounded once to bf16.
 // The expert GEMMs take fp16 operands (weights s q + b and h keep 11
 // significant bits; x converts exactly for |x| < 65504, else the error word is
 // set); the same kernel with bf16 router rows and bf16 x computes the router
@@ -66,6 +66,11 @@ constexpr uint32_t kXACol0 = 2 * kXMaxN;                    // first A column (3
 constexpr int kXSmem = kXStg * kXBBytes + kXRaw * kPfRawBytes + 1024 /*align*/ + 512 /*barriers*/;
 static_assert(kXSmem <= 232448, "shared memory per CTA");
 static_assert(kXACol0 + kXStg * 32 <= 512, "TMEM columns");
+constexpr int kXGatherW0 = 19;     // gate/up: warps 19 .. 22 gather the B rows (cp.async)
+constexpr int kXGatherWarps = 4;
+constexpr int kXThreads = (kXGatherW0 + kXGatherWarps) * 32;
+constexpr int kXGRows = kXMaxN / (kXGatherWarps * 32 / 8);   // rows per gather thread per K step (12)
+constexpr int kXGDepth = 2;        // K steps a gather thread keeps in flight past the one it signals
 
 __device__ __forceinline__ uint32_t sw128(int r, int c)   // byte offset of (row, col) in a 64-col bf16 tile
 {
@@ -168,13 +173,13 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // ---------------------------------------------------------------- bucketing
-// counts and chunk_base are [E][chunks] (expert-major) so the scan reads each
-// expert's row with vector loads.
+// counts and chunk_base are [chunks][E]: the scan's threads (one per expert)
+// and the scatter's lanes read one chunk's row together, coalesced.
 
 __global__ void __launch_bounds__(256) bucket_count_kernel(const PrefillParams p)
 {
     __shared__ int cnt[1024];
-    const int c = blockIdx.x, nch = gridDim.x;
+    const int c = blockIdx.x;
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     const int t0 = c * kBucketTok, t1 = min(p.T, t0 + kBucketTok);
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(256) bucket_count_kernel(const PrefillParams p
         else set_error(p.err, SMOE_DEV_BAD_EXPERT);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < p.E; e += blockDim.x) p.counts[size_t(e) * nch + c] = cnt[e];
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) p.counts[size_t(c) * p.E + e] = cnt[e];
 }
 
 // One CTA: per-expert chunk prefixes, expert offsets, and the tile list.
@@ -196,15 +201,13 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
     const int nch = (p.T + kBucketTok - 1) / kBucketTok;
     int total = 0;
     if (e < p.E) {
-        const int *row = p.counts + size_t(e) * nch;
-        int *brow = p.chunk_base + size_t(e) * nch;
         for (int c0 = 0; c0 < nch; c0 += 32) {       // 32 loads in flight, then the running sum
             int v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = c0 + j < nch ? row[c0 + j] : 0;
+            for (int j = 0; j < 32; ++j) v[j] = c0 + j < nch ? p.counts[size_t(c0 + j) * p.E + e] : 0;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                if (c0 + j < nch) brow[c0 + j] = total;
+                if (c0 + j < nch) p.chunk_base[size_t(c0 + j) * p.E + e] = total;
                 total += v[j];
             }
         }
@@ -234,32 +237,31 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
             p.tiles[tstart + i] = tl;
         }
     }
+    const int ntr = tbuf[1023];
+    const int nts = (p.T + kXMaxN - 1) / kXMaxN;
+    for (int i = e; i < nts; i += blockDim.x) {       // the shared expert: runs of near-equal size over T
+        PfTile tl;
+        tl.kind = 1;
+        tl.slot = 0;
+        tl.p0 = int((int64_t(i) * p.T) / nts);
+        tl.n = int((int64_t(i + 1) * p.T) / nts) - tl.p0;
+        p.tiles[ntr + i] = tl;
+    }
     if (e == 0) {
-        const int P = buf[1023];
-        const int ntr = tbuf[1023];
-        p.offsets[p.E] = P;
-        const int nts = (p.T + kXMaxN - 1) / kXMaxN;
-        for (int i = 0; i < nts; ++i) {
-            PfTile tl;
-            tl.kind = 1;
-            tl.slot = 0;
-            tl.p0 = int((int64_t(i) * p.T) / nts);
-            tl.n = int((int64_t(i + 1) * p.T) / nts) - tl.p0;
-            p.tiles[ntr + i] = tl;
-        }
+        p.offsets[p.E] = buf[1023];
         *p.ntiles = ntr + nts;
     }
 }
 
-// One warp per chunk: pairs in token order, each to its expert's next slot.
-// The chunk's ids are staged in shared memory first so the ordered loop only
-// touches shared memory.
+// One warp per chunk: pairs in token order, each to its expert's next slot,
+// with its token and routing weight. The chunk's ids are staged in shared
+// memory first so the ordered loop only touches shared memory.
 __global__ void __launch_bounds__(32) bucket_scatter_kernel(const PrefillParams p)
 {
     __shared__ int base[1024];
     __shared__ int ids_s[kBucketTok * 16];
-    const int c = blockIdx.x, nch = gridDim.x, lane = threadIdx.x;
-    for (int e = lane; e < p.E; e += 32) base[e] = p.offsets[e] + p.chunk_base[size_t(e) * nch + c];
+    const int c = blockIdx.x, lane = threadIdx.x;
+    for (int e = lane; e < p.E; e += 32) base[e] = p.offsets[e] + p.chunk_base[size_t(c) * p.E + e];
     const int t0 = c * kBucketTok, t1 = min(p.T, t0 + kBucketTok);
     for (int q = t0 * p.k + lane; q < t1 * p.k; q += 32) ids_s[q - t0 * p.k] = p.ids[q];
     __syncwarp();
@@ -277,35 +279,24 @@ __global__ void __launch_bounds__(32) bucket_scatter_kernel(const PrefillParams 
         if (ok && rank == __popc(same) - 1) base[e] = pos + 1;
         if (ok) {
             p.pair_token[pos] = t;
-            p.pair_j[pos] = lane;
         }
         if (act) p.pair_pos[q] = pos;
         __syncwarp();
     }
 }
 
-// ------------------------------------------------------------ row gather
-// One warp per row of xs: row pos < P is pair pos (expert order), row P + t
-// is token t for the shared expert, its columns in the expert GEMMs' K order
-// (perm64 inside each 64-column group). xs = fp16(x row), exact for |x| < 65504
-// (subnormal below 2^-14, an absolute error under 3e-8); larger values set
-// the error word. pair_w = the pair's routing weight, or the token's gate.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const GemmParams g)
+// ------------------------------------------------------ token conversion
+// One warp per token t: xt[t] = fp16(x[t]) with the columns in the expert
+// GEMMs' K order (perm64 inside each 64-column group); the gate/up GEMM gathers
+// its B rows from xt by token. fp16 is exact for |x| < 65504 (subnormal below
+// 2^-14, an absolute error under 3e-8); larger values set the error word.
+__global__ void __launch_bounds__(256) convert_x_kernel(const GemmParams g)
 {
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (row >= g.P + g.T) return;
-    int tok;
-    if (row < g.P) {
-        tok = g.pair_token[row];
-        if (lane == 0) g.pair_w[row] = g.w[size_t(tok) * g.k + g.pair_j[row]];
-    } else {
-        tok = row - g.P;
-        if (lane == 0) g.pair_w[row] = g.gate[tok];
-    }
+    const int tok = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (tok >= g.T) return;
     const uint4 *src = reinterpret_cast<const uint4 *>(g.x_bf16 + size_t(tok) * g.H);
-    uint4 *dst = reinterpret_cast<uint4 *>(const_cast<uint16_t *>(g.x) + size_t(row) * g.H);
+    uint2 *dst2 = reinterpret_cast<uint2 *>(const_cast<uint16_t *>(g.x) + size_t(tok) * g.H);
     bool bad = false;
-    uint2 *dst2 = reinterpret_cast<uint2 *>(dst);
     for (int i = lane; i < g.H / 8; i += 32) {
         const uint4 v = __ldg(src + i);
         const uint32_t in[4] = {v.x, v.y, v.z, v.w};
@@ -589,7 +580,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmPa
 // (tcgen05.st) and the MMAs read it there, so shared memory carries only the
 // raw atoms and B. Worker warp w writes atom a = 2 (w % 4) + w / 4 (rows
 // 16 a .. 16 a + 15, inside the lane quadrant w % 4 that the warp may access).
-__global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmParams p,
+__global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmParams p,
                                                                     const __grid_constant__ CUtensorMap bmap,
                                                                     const __grid_constant__ CUtensorMap amap,
                                                                     const __grid_constant__ CUtensorMap amap_shared)
@@ -619,7 +610,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
             mbar_init(&rawempty[r], kPfWorkers);
         }
         for (int s = 0; s < kXStg; ++s) {
-            mbar_init(&full[s], kPfWorkers * 32 + 1);             // the A threads + the B producer (with bytes)
+            // the A threads + the B producer(s): 128 gathering threads (gate/up) or one TMA issuer
+            mbar_init(&full[s], kPfWorkers * 32 + (p.mode == 0 ? kXGatherWarps * 32 : 1));
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -670,9 +662,67 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
             for (int g2 = done - 1; g2 >= 0 && g2 >= done - kXRaw; --g2)
                 mbar_wait(&rawfull[g2 % kXRaw], (g2 / kXRaw) & 1, p.err);
         }
+    } else if (warp >= kXGatherW0) {
+        if (p.mode == 0) {
+            // ---- B (gate/up): the tile's N token rows of xt, one 16-byte chunk per
+            // thread and row: thread g takes chunk g % 8 of rows g / 8 + 16 u. Rows
+            // n .. N - 1 repeat row n - 1 (their accumulator columns are never
+            // stored). A step is signalled once its copies have landed, kXGDepth
+            // steps later (cp.async groups), after a proxy fence for the MMA.
+            const int gt = tid - kXGatherW0 * 32, c8 = gt & 7, r0 = gt >> 3;
+            // byte offsets: source row u = token row start + chunk; destination row
+            // r0 + 16 u = sw128(r0, 8 c8) + 2048 u (16 u keeps the row's swizzle phase)
+            auto rows_of = [&](const TileInfo &t, uint32_t (&off)[kXGRows]) {
+#pragma unroll
+                for (int u = 0; u < kXGRows; ++u) {
+                    const int rr = min(r0 + 16 * u, t.n - 1);
+                    const int tok = t.kind == 1 ? t.p0 + rr : p.pair_token[t.p0 + rr];
+                    off[u] = uint32_t(tok) * uint32_t(2 * p.H) + uint32_t(16 * c8);
+                }
+            };
+            const char *xt = reinterpret_cast<const char *>(p.x);
+            const uint32_t dst0 = smem_u32(bst) + sw128(r0, 8 * c8);
+            uint32_t cur[kXGRows], nxt[kXGRows];
+            TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
+            rows_of(tnext, nxt);
+            int sb = 0, sd = 0, issued = 0;
+            uint32_t ph = 0;
+            for (int i = 0; i < my_tiles; ++i) {
+                const TileInfo ti = tnext;
+#pragma unroll
+                for (int u = 0; u < kXGRows; ++u) cur[u] = nxt[u];
+                if (i + 1 < my_tiles) {
+                    tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
+                    rows_of(tnext, nxt);
+                }
+                const int urows = (ti.N - r0 + 15) / 16;              // rows r0 + 16 u < N
+                for (int kb = 0; kb < nk; ++kb) {
+                    pf_wait(&empty[sb], ph ^ 1u, p.err, abort);
+                    const uint32_t dst = dst0 + uint32_t(sb * kXBBytes);
+                    const char *src = xt + kb * (kPfK * 2);
+#pragma unroll
+                    for (int u = 0; u < kXGRows; ++u)
+                        if (u < urows) cp_async16(dst + uint32_t(2048 * u), src + cur[u], 16u);
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                    if (++sb == kXStg) { sb = 0; ph ^= 1u; }
+                    if (++issued > kXGDepth) {
+                        asm volatile("cp.async.wait_group %0;" ::"n"(kXGDepth) : "memory");
+                        fence_async_smem();
+                        mbar_arrive(&full[sd]);
+                        if (++sd == kXStg) sd = 0;
+                    }
+                }
+            }
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            fence_async_smem();
+            for (int j = 0; j < min(issued, kXGDepth); ++j) {
+                mbar_arrive(&full[sd]);
+                if (++sd == kXStg) sd = 0;
+            }
+        }
     } else if (warp == kPfBWarp) {
-        // ---- B: rows rowbase .. rowbase + N - 1 of bmap, in boxes of kPfBoxRows rows
-        if (lane == 0) {
+        if (p.mode == 1 && lane == 0) {
+            // ---- B (down): rows rowbase .. rowbase + N - 1 of hbuf, in boxes of kPfBoxRows rows
             asm volatile("prefetch.tensormap [%0];" ::"l"(&bmap) : "memory");
             int sb = 0;
             uint32_t ph = 0;
@@ -762,25 +812,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
         const int e = warp - kPfWorkers, q = e & 3, half = e >> 2;
         const int r = 32 * q + lane;
         bool range_bad = false;
-        auto weights = [&](const TileInfo &t, float (&wv)[3]) {
-#pragma unroll
-            for (int u = 0; u < 3; ++u) {
-                const int c = 32 * (2 * u + half) + lane;
-                wv[u] = (p.mode == 1 && c < t.n) ? p.pair_w[t.rowbase + c] : 0.f;
-            }
-        };
+        uint32_t ymax = 0;                                        // largest |fp16 bits| of the down outputs
         TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
-        float wnext[3];
-        weights(tnext, wnext);
         for (int i = 0; i < my_tiles; ++i) {
             const int b = i & 1;
             const TileInfo ti = tnext;
-            float wv[3] = {wnext[0], wnext[1], wnext[2]};
             const int mt = tile_of(i) % p.m_tiles;
-            if (i + 1 < my_tiles) {
-                tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
-                weights(tnext, wnext);
-            }
+            if (i + 1 < my_tiles) tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
             pf_wait(&accfull[b], (i / 2) & 1, p.err, abort);
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             if (!ti.valid) set_error(p.err, SMOE_DEV_BAD_SLOT);
@@ -810,15 +848,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
                             }
                         }
                     } else {
-                        const int R = kPfM * mt + r;
+                        // the pair's expert output, row R of the down projection
+                        uint16_t *y = p.ypair + size_t(ti.rowbase + 32 * j) * p.H + (kPfM * mt + r);
+                        const int nc = ti.n - 32 * j;
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj) {
-                            const int c = 32 * j + jj;
-                            const float wt = __shfl_sync(0xffffffffu, wv[u], jj);
-                            if (c < ti.n) {
-                                const float y = __uint_as_float(v[jj]) * keep * wt;
-                                range_bad |= !(fabsf(y) < 65504.f);
-                                p.ypair[size_t(ti.rowbase + c) * p.H + R] = f32_to_f16_bits(y);
+                            if (jj < nc) {
+                                const uint32_t hb = f32_to_f16_bits(__uint_as_float(v[jj]) * keep);
+                                ymax = max(ymax, hb & 0x7fffu);
+                                y[size_t(jj) * p.H] = uint16_t(hb);
                             }
                         }
                     }
@@ -828,7 +866,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
             __syncwarp();
             mbar_arrive(&accempty[b]);
         }
-        if (range_bad) set_error(p.err, SMOE_DEV_RANGE);
+        // 0x7bff is 65504, the largest finite fp16; above it: infinities and NaN
+        if (range_bad || ymax >= 0x7bffu) set_error(p.err, SMOE_DEV_RANGE);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -838,26 +877,29 @@ __global__ void __launch_bounds__(kPfThreads, 1) expert_gemm_kernel(const GemmPa
 
 // ---------------------------------------------------------------- combine
 
-// out[t] = sum_j ypair[pos(t, j)] (route order) + ypair[P + t] (+ residual),
-// from the fp16 weighted pair outputs, summed in fp32.
+// out[t] = sum_j w[t][j] ypair[pos(t, j)] (route order) + gate[t] ypair[P + t]
+// (+ residual), from the fp16 expert outputs, in fp32.
 __global__ void __launch_bounds__(256) combine_kernel(const PrefillParams p)
 {
     const int t = blockIdx.y;
     const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (c >= p.H) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto add = [&](int row) {
+    auto add = [&](int row, float wt) {
         const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(p.ypair + size_t(row) * p.H + c));
         float2 a, b;
         asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}" : "=f"(a.x), "=f"(a.y) : "r"(v.x));
         asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}" : "=f"(b.x), "=f"(b.y) : "r"(v.y));
-        acc.x += a.x; acc.y += a.y; acc.z += b.x; acc.w += b.y;
+        acc.x = fmaf(wt, a.x, acc.x);
+        acc.y = fmaf(wt, a.y, acc.y);
+        acc.z = fmaf(wt, b.x, acc.z);
+        acc.w = fmaf(wt, b.y, acc.w);
     };
     for (int j = 0; j < p.k; ++j) {
         const int pos = p.pair_pos[size_t(t) * p.k + j];
-        if (pos >= 0) add(pos);
+        if (pos >= 0) add(pos, p.w[size_t(t) * p.k + j]);
     }
-    add(p.P + t);
+    add(p.P + t, p.gate[t]);
     if (p.residual) {
         const uint2 r = *reinterpret_cast<const uint2 *>(p.residual + size_t(t) * p.H + c);
         acc.x += bf16lo(r.x); acc.y += bf16hi(r.x); acc.z += bf16lo(r.y); acc.w += bf16hi(r.y);
@@ -966,7 +1008,7 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
 {
     const int nch = (p.T + kBucketTok - 1) / kBucketTok;
     CUtensorMap xmap, hmap;
-    cudaError_t e = rows_map(&xmap, g0.x, false, uint64_t(p.H), uint64_t(p.P + p.T));
+    cudaError_t e = rows_map(&xmap, g0.x, false, uint64_t(p.H), uint64_t(p.T));   // unused: gate/up gathers B itself
     if (e != cudaSuccess) return e;
     if ((e = rows_map(&hmap, g0.hbuf, false, uint64_t(g0.I), uint64_t(p.P + p.T))) != cudaSuccess) return e;
     // raw atoms: gate/up region [I/8 row blocks][H/64 groups], down region [H/16][I/64] at I/8 x H/64 atoms
@@ -980,17 +1022,17 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
     bucket_count_kernel<<<nch, 256, 0, st>>>(p);
     bucket_scan_kernel<<<1, 1024, 0, st>>>(p);
     bucket_scatter_kernel<<<nch, 32, 0, st>>>(p);
-    gather_rows_kernel<<<(p.P + p.T + 7) / 8, 256, 0, st>>>(g0);
+    convert_x_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(g0);
     const int maxt = prefill_max_tiles(p.T, p.k, p.E);
     GemmParams g = g0;
     g.mode = 0;
     g.m_tiles = g.I / 64;
     if ((e = prof_record(nprof > 0 ? prof[0] : nullptr, st)) != cudaSuccess) return e;
-    expert_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kPfThreads, kXSmem, st>>>(g, xmap, gu_pool, gu_shared);
+    expert_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kXThreads, kXSmem, st>>>(g, xmap, gu_pool, gu_shared);
     if ((e = prof_record(nprof > 1 ? prof[1] : nullptr, st)) != cudaSuccess) return e;
     g.mode = 1;
     g.m_tiles = p.H / kPfM;
-    expert_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kPfThreads, kXSmem, st>>>(g, hmap, dn_pool, dn_shared);
+    expert_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kXThreads, kXSmem, st>>>(g, hmap, dn_pool, dn_shared);
     if ((e = prof_record(nprof > 2 ? prof[2] : nullptr, st)) != cudaSuccess) return e;
     combine_kernel<<<dim3((p.H / 4 + 255) / 256, p.T), 256, 0, st>>>(p);
     return cudaGetLastError();

@@ -145,12 +145,10 @@ Workspace workspace_layout(const smoe_shape &s, int T)
         w.tiles = o;      o = al(o + uint64_t(prefill_max_tiles(T, s.k, s.E)) * sizeof(PfTile));
         w.ntiles = o;     o = al(o + 4);
         w.pair_token = o; o = al(o + P * 4);
-        w.pair_j = o;     o = al(o + P * 4);
         w.pair_pos = o;   o = al(o + P * 4);
         w.hbuf = o;       o = al(o + (P + T) * s.I * 2);
         w.ybuf = o;       o = al(o + (P + T) * s.H * 2);
-        w.xh = o;         o = al(o + (P + T) * s.H * 2);
-        w.pair_w = o;     o = al(o + (P + T) * 4);
+        w.xt = o;         o = al(o + uint64_t(T) * s.H * 2);
     }
     w.total = o;
     return w;
@@ -337,7 +335,8 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
         q.table_row = ctx->table_dev + size_t(layer) * ctx->shape.E;
         q.n_slots = ctx->n_slots;
         q.pair_token = reinterpret_cast<int32_t *>(ws + W.pair_token);
-        q.pair_j = reinterpret_cast<int32_t *>(ws + W.pair_j);
+        q.w = w;
+        q.gate = gate;
         q.pair_pos = reinterpret_cast<int32_t *>(ws + W.pair_pos);
         q.ypair = reinterpret_cast<const uint16_t *>(ws + W.ybuf);
         q.residual = residual;
@@ -354,17 +353,13 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
         g.table_row = ctx->table_dev + size_t(layer) * ctx->shape.E;
         g.stride = ctx->layout.blob;
         g.n_slots = ctx->n_slots;
-        g.x = reinterpret_cast<const uint16_t *>(ws + W.xh);
+        g.x = reinterpret_cast<const uint16_t *>(ws + W.xt);
         g.x_bf16 = x;
         g.hbuf = reinterpret_cast<uint16_t *>(ws + W.hbuf);
-        g.pair_w = reinterpret_cast<float *>(ws + W.pair_w);
         g.ypair = reinterpret_cast<uint16_t *>(ws + W.ybuf);
         g.pair_token = q.pair_token;
-        g.pair_j = q.pair_j;
         g.ntiles = q.ntiles;
         g.tiles = q.tiles;
-        g.w = w;
-        g.gate = gate;
         g.err = err;
         g.T = T;
         g.H = q.H;

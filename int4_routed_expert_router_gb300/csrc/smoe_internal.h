@@ -138,17 +138,18 @@ struct PfTile {
 // Token-bucketed path (T > 8): bucketing and combine.
 struct PrefillParams {
     const int32_t *ids;
-    int32_t *counts;       // [E][chunks]
-    int32_t *chunk_base;   // [E][chunks]
+    int32_t *counts;       // [chunks][E]
+    int32_t *chunk_base;   // [chunks][E]
     int32_t *offsets;      // [E + 1]
     PfTile *tiles;         // [max tiles]
     int32_t *ntiles;
     const int32_t *table_row;  // the layer's slot table row [E]
     int64_t n_slots;
     int32_t *pair_token;   // [T*k]
-    int32_t *pair_j;       // [T*k]
+    const float *w;        // [T][k] routing weights
+    const float *gate;     // [T] shared-expert gates
     int32_t *pair_pos;     // [T*k] position of pair (t, j) in expert order, -1 if invalid
-    const uint16_t *ypair; // [(T*k + T)][H] fp16, weighted
+    const uint16_t *ypair; // [(T*k + T)][H] fp16 expert outputs (unweighted)
     const uint16_t *residual;
     uint16_t *out;
     int32_t *err;
@@ -162,17 +163,13 @@ struct GemmParams {
     const int32_t *table_row;
     uint64_t stride;
     int64_t n_slots;
-    const uint16_t *x;     // expert GEMMs: xs [(P + T)][H] fp16 rows in expert order; router: x [T][H] bf16
-    const uint16_t *x_bf16;  // the caller's bf16 x (gathered and converted into xs by the path)
-    float *pair_w;         // [(P + T)] routing weight of each xs row (shared rows: the gate)
+    const uint16_t *x;     // expert GEMMs: xt [T][H] fp16 (x in the MMA K order); router: x [T][H] bf16
+    const uint16_t *x_bf16;  // the caller's bf16 x (converted into xt by the path)
     uint16_t *hbuf;        // [(P + T)][I] fp16
-    uint16_t *ypair;       // [(P + T)][H] fp16, weighted
+    uint16_t *ypair;       // [(P + T)][H] fp16 expert outputs (unweighted)
     const int32_t *pair_token;
-    const int32_t *pair_j;
     const int32_t *ntiles;
     const PfTile *tiles;
-    const float *w;
-    const float *gate;
     const uint16_t *Wr;    // router rows (mode 2)
     const uint16_t *ws;
     float *logits;         // [T][E + 1] (mode 2)
@@ -185,7 +182,7 @@ struct GemmParams {
 struct Workspace {
     uint64_t route_counter, logits, fwd_counters, ypair, total;
     // token-bucketed path (T > kDecodeMaxT)
-    uint64_t counts, chunk_base, offsets, tiles, ntiles, pair_token, pair_j, pair_pos, hbuf, ybuf, xh, pair_w;
+    uint64_t counts, chunk_base, offsets, tiles, ntiles, pair_token, pair_pos, hbuf, ybuf, xt;
 };
 
 Workspace workspace_layout(const smoe_shape &s, int T);

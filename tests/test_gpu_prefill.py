@@ -2,8 +2,8 @@
 gate/up and down GEMMs, ordered combine, and the tensor-core router.
 
 Weights are dequantised to fp16 tiles (one rounding of s q + b), x and h
-are fp16, products accumulate in fp32 and the weighted pair outputs are
-stored as fp16, so only the layer tolerance applies (relative L2 <= 5e-3,
+are fp16, products accumulate in fp32 and each pair's expert output is
+stored as fp16 before the fp32 weighted combine, so only the layer tolerance applies (relative L2 <= 5e-3,
 max abs <= 2e-2 rms against the oracle's fp64 output)."""
 import numpy as np
 import pytest
