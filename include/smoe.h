@@ -63,6 +63,10 @@ extern "C" {
 #define SMOE_DEV_RANGE 4        /* T > 8 path: |x| or |h| >= 65504, or an expert output that rounds to
                                    65504 or beyond in fp16 (outside its fp16 intermediates) */
 
+/* Most tokens of one moe_route / moe_forward call (T); larger T is
+ * SMOE_EINVAL and smoe_workspace_bytes returns 0. */
+#define SMOE_MAX_TOKENS (1 << 20)
+
 /* ------------------------------------------------------------------ shapes */
 /* H: hidden size; E: routed experts per layer; k: experts per token;
  * I: routed expert intermediate size; I_shared: shared expert intermediate

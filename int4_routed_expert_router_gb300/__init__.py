@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(PKG, "libsmoe.so")
 
 OK, EINVAL, ERANGE, ENOMEM, ECUDA, EDEVICE, ENOTSUP = 0, -1, -2, -3, -4, -5, -6
 DEV_BAD_SLOT, DEV_BAD_EXPERT, DEV_TIMEOUT, DEV_RANGE = 1, 2, 3, 4
+MAX_TOKENS = 1 << 20          # SMOE_MAX_TOKENS: most tokens of one moe_route / moe_forward call
 HOST, DEVICE = 0, 1
 EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destroy", "set_slot_table",
            "smoe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_noalloc", "moe_decode_stack",

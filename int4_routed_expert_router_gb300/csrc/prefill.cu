@@ -677,7 +677,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                 for (int u = 0; u < kXGRows; ++u) {
                     const int rr = min(r0 + 16 * u, t.n - 1);
                     const int tok = t.kind == 1 ? t.p0 + rr : p.pair_token[t.p0 + rr];
-                    off[u] = uint32_t(tok) * uint32_t(2 * p.H) + uint32_t(16 * c8);
+                    off[u] = uint32_t(tok) * uint32_t(2 * p.H) + uint32_t(16 * c8);   // < 2^32: T <= SMOE_MAX_TOKENS, H <= 2048
                 }
             };
             const char *xt = reinterpret_cast<const char *>(p.x);

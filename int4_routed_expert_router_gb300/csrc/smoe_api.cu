@@ -275,7 +275,7 @@ extern "C" int set_slot_table(smoe_ctx *ctx, int32_t layer, const int32_t *host_
 
 extern "C" uint64_t smoe_workspace_bytes(const smoe_ctx *ctx, int32_t T)
 {
-    if (!ctx || T <= 0) return 0;
+    if (!ctx || T <= 0 || T > SMOE_MAX_TOKENS) return 0;
     return workspace_layout(ctx->shape, T).total;
 }
 
@@ -285,7 +285,8 @@ extern "C" int moe_route(const smoe_ctx *ctx, const uint16_t *W_r, const uint16_
                          int32_t T, const float *logit_bias, int32_t *ids, float *w, float *gate, void *workspace,
                          uint64_t workspace_bytes, void *stream)
 {
-    if (!ctx || !W_r || !w_s || !x || !ids || !w || !gate || !workspace || T < 0) return SMOE_EINVAL;
+    if (!ctx || !W_r || !w_s || !x || !ids || !w || !gate || !workspace || T < 0 || T > SMOE_MAX_TOKENS)
+        return SMOE_EINVAL;
     if (T == 0) return SMOE_OK;
     if (!aligned16(W_r) || !aligned16(w_s) || !aligned16(x) || !aligned16(workspace)) return SMOE_EINVAL;
     const Workspace W = workspace_layout(ctx->shape, T);
@@ -314,7 +315,8 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
                            const void *shared_blob, const uint16_t *residual, uint16_t *out, void *workspace,
                            uint64_t workspace_bytes, int32_t *err, void *stream)
 {
-    if (!ctx || !x || !ids || !w || !gate || !pool || !shared_blob || !out || !workspace || !err || T < 0)
+    if (!ctx || !x || !ids || !w || !gate || !pool || !shared_blob || !out || !workspace || !err || T < 0 ||
+        T > SMOE_MAX_TOKENS)
         return SMOE_EINVAL;
     if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
     if (T == 0) return SMOE_OK;

@@ -134,3 +134,32 @@ def test_prefill_bad_slot_sets_error_word(tiny):
     finally:
         pool.table_dev[0, e] = saved
         torch.cuda.synchronize()
+
+
+def test_token_limit_is_rejected_before_any_work(tiny):
+    """T above SMOE_MAX_TOKENS (the limit that keeps every row offset of the
+    bucketed path inside 32 bits) is refused at the boundary: no workspace
+    size, and EINVAL from moe_route and moe_forward without touching memory."""
+    pool, inp = tiny
+    wl = pool.wl
+    T = smoe.MAX_TOKENS + 1
+    assert pool.ctx.workspace_bytes(smoe.MAX_TOKENS) > 0
+    assert pool.ctx.workspace_bytes(T) == 0
+    x = torch.zeros((8, wl.H), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((8, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((8, wl.k), dtype=torch.float32, device="cuda")
+    gate = torch.zeros(8, dtype=torch.float32, device="cuda")
+    out = torch.zeros_like(x)
+    ws = W.workspace(pool.ctx, 8)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L = smoe.lib()
+    p = smoe._ptr
+    st = L.moe_forward(pool.ctx.handle, 0, p(x), T, p(ids), p(w), p(gate), p(pool.pool),
+                       pool.pool.numel() * pool.pool.element_size(), p(pool.shared[0]), None, p(out), p(ws),
+                       ws.numel() * ws.element_size(), p(err), None)
+    assert st == smoe.EINVAL
+    st = L.moe_route(pool.ctx.handle, p(inp.Wr[0]), p(inp.ws[0]), p(x), T, None, p(ids), p(w), p(gate), p(ws),
+                     ws.numel() * ws.element_size(), None)
+    assert st == smoe.EINVAL
+    torch.cuda.synchronize()
+    assert smoe.check(err) == 0
