@@ -476,16 +476,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmPa
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&bmap) : "memory");
             TileInfo ti;
+            int issued = 0;
             for (int gk = 0; gk < total; ++gk) {
                 const int i = gk / nk, kb = gk % nk, s = gk % kPfAB;
                 if (kb == 0) ti = tile_info(p, tile_of(i) / p.m_tiles);
                 const int nbox = (ti.N + kPfBoxRows - 1) / kPfBoxRows;
-                if (gk >= kPfAB) pf_wait(&empty[s], ((gk / kPfAB) - 1) & 1, p.err, abort);
+                if (gk >= kPfAB && !pf_wait(&empty[s], ((gk / kPfAB) - 1) & 1, p.err, abort)) break;
                 mbar_arrive_expect_tx(&bfull[s], uint32_t(nbox) * kPfBoxRows * (kPfK * 2));
                 const uint32_t dst = smem_u32(ab + s * kPfStageBytes + kPfABytes);
                 for (int j = 0; j < nbox; ++j)
                     tma_load_2d(dst + j * (kPfBoxRows * kPfK * 2), &bmap, kb * kPfK, ti.rowbase + j * kPfBoxRows, &bfull[s]);
+                ++issued;
             }
+            // the last copy into each stage lands before the CTA can exit (also after an abort)
+            for (int g2 = issued - 1; g2 >= 0 && g2 >= issued - kPfAB; --g2)
+                mbar_wait(&bfull[g2 % kPfAB], (g2 / kPfAB) & 1, p.err);
         }
     } else if (warp == kPfMma) {
         // ---- MMA issuer: tile i accumulates in TMEM buffer i % 2 (256 columns each)
@@ -573,6 +578,82 @@ __global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmPa
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
 }
 
+// Epilogue of the expert GEMMs: warp w reads TMEM lanes 32 (w % 4) .. + 31
+// (tile rows; a warp may only access its own lane quadrant) and column chunks
+// of 32 tokens. Gate/up: 8 warps, 2 per quadrant, 3 chunks each; SwiGLU of each
+// unit's gate row r and up row r ^ 8, h written in the down GEMM's K order.
+// Down: 12 warps, 3 per quadrant, 2 chunks each; each pair's fp16 output, two
+// rows per 4-byte store (neighbouring lanes swap halves).
+template <typename TileOf>
+__device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uint64_t *accfull, uint64_t *accempty,
+                                         volatile int *abort, int warp, int lane, int my_tiles, TileOf tile_of)
+{
+    const int q = warp & 3;
+    const int nh = p.mode == 1 ? 3 : 2;                           // warps per quadrant
+    const int h = warp >= kXGatherW0 ? 2 : (warp - kPfWorkers) >> 2;
+    const int r = 32 * q + lane;
+    const int odd = lane & 1;
+    bool range_bad = false;
+    uint32_t ymax = 0;                                            // largest |fp16| bits of the down outputs, per half
+    TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
+    for (int i = 0; i < my_tiles; ++i) {
+        const int b = i & 1;
+        const TileInfo ti = tnext;
+        const int mt = tile_of(i) % p.m_tiles;
+        if (i + 1 < my_tiles) tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
+        pf_wait(&accfull[b], (i / 2) & 1, p.err, abort);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (!ti.valid) set_error(p.err, SMOE_DEV_BAD_SLOT);
+        const float keep = ti.valid ? 1.f : 0.f;
+        for (int j = h; 32 * j < ti.N; j += nh) {                 // uniform over the warp
+            uint32_t v[32];
+            tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(b * kXMaxN + 32 * j), v);
+            if (p.mode == 0) {
+                // rows r (gate) and r ^ 8 (up) of one intermediate unit; h goes to
+                // its column in the down GEMM's K order
+                const bool gate_row = (lane & 8) == 0;
+                const int inter = 64 * mt + 8 * (r >> 4) + (r & 7);
+                const int hcol = (inter & ~63) | perm64(inter & 63);
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 2) {
+                    const float a0 = __uint_as_float(v[jj]) * keep, a1 = __uint_as_float(v[jj + 1]) * keep;
+                    const float other = __shfl_xor_sync(0xffffffffu, gate_row ? a1 : a0, 8);
+                    const float gv = gate_row ? a0 : other, uv = gate_row ? other : a1;
+                    const int c = 32 * j + jj + (gate_row ? 0 : 1);
+                    const float hv = silu_f(gv) * uv;
+                    if (c < ti.n) {
+                        range_bad |= !(fabsf(hv) < 65504.f);
+                        p.hbuf[size_t(ti.rowbase + c) * p.I + hcol] = f32_to_f16_bits(hv);
+                    }
+                }
+            } else {
+                // columns 2m (even lane) and 2m + 1 (odd lane) of rows R, R + 1 (R even):
+                // each lane packs (col 2m, col 2m + 1) of its row, swaps with its
+                // neighbour, and stores one column of both rows
+                const int R0 = kPfM * mt + r - odd;
+                uint32_t *y = reinterpret_cast<uint32_t *>(p.ypair + size_t(ti.rowbase + 32 * j + odd) * p.H + R0);
+                const int nc = ti.n - 32 * j - odd;                 // stored when 2m < nc
+                const uint32_t sel = odd ? 0x3276u : 0x5410u;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const uint32_t h2 = pack_f16x2(__uint_as_float(v[2 * m]) * keep, __uint_as_float(v[2 * m + 1]) * keep);
+                    const uint32_t nb = __shfl_xor_sync(0xffffffffu, h2, 1);
+                    const uint32_t o = __byte_perm(h2, nb, sel);
+                    if (2 * m < nc) {
+                        ymax = __vmaxu2(ymax, o & 0x7fff7fffu);
+                        y[size_t(2 * m) * (p.H / 2)] = o;
+                    }
+                }
+            }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        mbar_arrive(&accempty[b]);
+    }
+    // 0x7bff is 65504, the largest finite fp16; above it: infinities and NaN
+    if (range_bad || (ymax & 0xffffu) >= 0x7bffu || (ymax >> 16) >= 0x7bffu) set_error(p.err, SMOE_DEV_RANGE);
+}
+
 // ------------------------------------------------- expert GEMMs, A in TMEM
 // Persistent like router_gemm_kernel (tiles b, b + grid, ...; every role walks
 // the same K steps) for mode 0 (gate/up, K = H) and mode 1 (down, K = I), but
@@ -593,7 +674,8 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     uint64_t *rawfull = bars, *rawempty = bars + kXRaw;
     uint64_t *full = bars + 2 * kXRaw, *empty = full + kXStg;     // stage s: A (TMEM) + B (smem)
     uint64_t *accfull = empty + kXStg, *accempty = accfull + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accempty + 2);
+    uint64_t *bfull = accempty + 2;                               // down: B copies of stage s (TMA)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bfull + kXStg);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -610,13 +692,15 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             mbar_init(&rawempty[r], kPfWorkers);
         }
         for (int s = 0; s < kXStg; ++s) {
-            // the A threads + the B producer(s): 128 gathering threads (gate/up) or one TMA issuer
-            mbar_init(&full[s], kPfWorkers * 32 + (p.mode == 0 ? kXGatherWarps * 32 : 1));
+            // the A threads, plus in gate/up the 128 gathering threads (the down
+            // GEMM's B copies complete on bfull instead)
+            mbar_init(&full[s], kPfWorkers * 32 + (p.mode == 0 ? kXGatherWarps * 32 : 0));
             mbar_init(&empty[s], 1);
+            mbar_init(&bfull[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accfull[b], 1);
-            mbar_init(&accempty[b], kPfEpi * 32);
+            mbar_init(&accempty[b], (p.mode == 1 ? kPfEpi + kXGatherWarps : kPfEpi) * 32);   // epilogue threads
         }
         *abort = 0;
         fence_mbar_init();
@@ -633,7 +717,11 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     // Ring positions advance by one per K step (index and phase bit); a producer
     // waits for the slot's release with the opposite parity, which a fresh
     // barrier passes, so the first round needs no special case.
-    if (warp == kPfRawWarp) {
+    // epilogue warps: 8..15, and in the down GEMM also the gather warps (idle there)
+    const bool epi_role = (warp >= kPfWorkers && warp < kPfWorkers + kPfEpi) || (p.mode == 1 && warp >= kXGatherW0);
+    if (epi_role) {
+        epilogue(p, tmem, accfull, accempty, abort, warp, lane, my_tiles, tile_of);
+    } else if (warp == kPfRawWarp) {
         // ---- raw int4 atoms (8 row blocks x one group) per K step: one TMA box each
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&amap) : "memory");
@@ -724,22 +812,27 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
         if (p.mode == 1 && lane == 0) {
             // ---- B (down): rows rowbase .. rowbase + N - 1 of hbuf, in boxes of kPfBoxRows rows
             asm volatile("prefetch.tensormap [%0];" ::"l"(&bmap) : "memory");
-            int sb = 0;
+            int sb = 0, issued = 0;
             uint32_t ph = 0;
-            for (int i = 0; i < my_tiles; ++i) {
+            bool ok = true;
+            for (int i = 0; i < my_tiles && ok; ++i) {
                 const TileInfo ti = tile_info(p, tile_of(i) / p.m_tiles);
                 const int nbox = (ti.N + kPfBoxRows - 1) / kPfBoxRows;
                 const uint32_t bytes = uint32_t(nbox) * kPfBoxRows * (kPfK * 2);
                 for (int kb = 0; kb < nk; ++kb) {
-                    pf_wait(&empty[sb], ph ^ 1u, p.err, abort);
-                    mbar_arrive_expect_tx(&full[sb], bytes);
+                    if (!pf_wait(&empty[sb], ph ^ 1u, p.err, abort)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&bfull[sb], bytes);
                     const uint32_t dst = smem_u32(bst + sb * kXBBytes);
                     for (int j = 0; j < nbox; ++j)
                         tma_load_2d(dst + j * (kPfBoxRows * kPfK * 2), &bmap, kb * kPfK, ti.rowbase + j * kPfBoxRows,
-                                    &full[sb]);
+                                    &bfull[sb]);
+                    ++issued;
                     if (++sb == kXStg) { sb = 0; ph ^= 1u; }
                 }
             }
+            // the last copy into each stage lands before the CTA can exit (also after an abort)
+            for (int g2 = issued - 1; g2 >= 0 && g2 >= issued - kXStg; --g2)
+                mbar_wait(&bfull[g2 % kXStg], (g2 / kXStg) & 1, p.err);
         }
     } else if (warp == kPfMma) {
         // ---- MMA issuer: tile i accumulates in TMEM columns (i % 2) * kXMaxN ..
@@ -756,6 +849,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                 const uint32_t acc_t = tmem + uint32_t(b * kXMaxN);
                 for (int kb = 0; kb < nk; ++kb) {
                     pf_wait_fast(&full[s], ph, p.err, abort);
+                    if (p.mode == 1) pf_wait_fast(&bfull[s], ph, p.err, abort);
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const uint64_t bd = umma_desc(smem_u32(bst + s * kXBBytes));
                     const uint32_t a_t = tmem + kXACol0 + uint32_t(32 * s);
@@ -806,68 +900,6 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             mbar_arrive(&full[sa]);
             if (++sa == kXStg) { sa = 0; pha ^= 1u; }
         }
-    } else {
-        // ---- epilogue warps: warp e reads TMEM lanes 32q..32q+31 (q = e % 4) = tile
-        // rows, column chunks of 32 tokens j = 2u + e / 4
-        const int e = warp - kPfWorkers, q = e & 3, half = e >> 2;
-        const int r = 32 * q + lane;
-        bool range_bad = false;
-        uint32_t ymax = 0;                                        // largest |fp16 bits| of the down outputs
-        TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
-        for (int i = 0; i < my_tiles; ++i) {
-            const int b = i & 1;
-            const TileInfo ti = tnext;
-            const int mt = tile_of(i) % p.m_tiles;
-            if (i + 1 < my_tiles) tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
-            pf_wait(&accfull[b], (i / 2) & 1, p.err, abort);
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            if (!ti.valid) set_error(p.err, SMOE_DEV_BAD_SLOT);
-            const float keep = ti.valid ? 1.f : 0.f;
-#pragma unroll
-            for (int u = 0; u < 3; ++u) {
-                const int j = 2 * u + half;
-                if (32 * j < ti.N) {                      // uniform over the warp
-                    uint32_t v[32];
-                    tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(b * kXMaxN + 32 * j), v);
-                    if (p.mode == 0) {
-                        // rows r (gate) and r ^ 8 (up) of one intermediate unit; h goes to
-                        // its column in the down GEMM's K order
-                        const bool gate_row = (lane & 8) == 0;
-                        const int inter = 64 * mt + 8 * (r >> 4) + (r & 7);
-                        const int hcol = (inter & ~63) | perm64(inter & 63);
-#pragma unroll
-                        for (int jj = 0; jj < 32; jj += 2) {
-                            const float a0 = __uint_as_float(v[jj]) * keep, a1 = __uint_as_float(v[jj + 1]) * keep;
-                            const float other = __shfl_xor_sync(0xffffffffu, gate_row ? a1 : a0, 8);
-                            const float gv = gate_row ? a0 : other, uv = gate_row ? other : a1;
-                            const int c = 32 * j + jj + (gate_row ? 0 : 1);
-                            const float h = silu_f(gv) * uv;
-                            if (c < ti.n) {
-                                range_bad |= !(fabsf(h) < 65504.f);
-                                p.hbuf[size_t(ti.rowbase + c) * p.I + hcol] = f32_to_f16_bits(h);
-                            }
-                        }
-                    } else {
-                        // the pair's expert output, row R of the down projection
-                        uint16_t *y = p.ypair + size_t(ti.rowbase + 32 * j) * p.H + (kPfM * mt + r);
-                        const int nc = ti.n - 32 * j;
-#pragma unroll
-                        for (int jj = 0; jj < 32; ++jj) {
-                            if (jj < nc) {
-                                const uint32_t hb = f32_to_f16_bits(__uint_as_float(v[jj]) * keep);
-                                ymax = max(ymax, hb & 0x7fffu);
-                                y[size_t(jj) * p.H] = uint16_t(hb);
-                            }
-                        }
-                    }
-                }
-            }
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncwarp();
-            mbar_arrive(&accempty[b]);
-        }
-        // 0x7bff is 65504, the largest finite fp16; above it: infinities and NaN
-        if (range_bad || ymax >= 0x7bffu) set_error(p.err, SMOE_DEV_RANGE);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
