@@ -423,7 +423,8 @@ __device__ __forceinline__ void tma_raw(uint32_t dst, const CUtensorMap *map, in
 }
 
 // Router logits for large T on tensor cores: logits[t][e] = W_r[e] . x[t]
-// (row E: the shared-gate vector), bf16 operands, fp32 accumulation.
+// for e < E, bf16 operands, fp32 accumulation (the shared-gate logit is one
+// warp dot per token in the top-k kernel).
 // Persistent: CTA b handles tiles b, b + grid, ... (tile = 256 tokens x 128
 // router rows); roles: 8 warps copy the router rows into A stages
 // (cp.async, one step ahead), one warp loads the tokens (B) with TMA, one
@@ -519,7 +520,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmPa
             mbar_wait(&accfull[(my_tiles - 1) & 1], ((my_tiles - 1) / 2) & 1, p.err);
         }
     } else if (warp < kPfWorkers) {
-        // ---- A = router rows (row E: the shared-gate vector; rows past E zero), one step ahead
+        // ---- A = router rows (rows past E zero), one step ahead
         auto issue_a = [&](int gi) {
             if (gi < total) {
                 const int i = gi / nk, kb = gi % nk, s = gi % kPfAB;
@@ -529,8 +530,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmPa
                 for (int q = tid; q < kPfM * 8; q += kPfWorkers * 32) {
                     const int r = q >> 3, c8 = q & 7;
                     const int e = mt * kPfM + r;
-                    const uint16_t *src = e < p.E ? p.Wr + size_t(e) * p.H : p.ws;
-                    cp_async16(sa_u + sw128(r, c8 * 8), src + kb * kPfK + c8 * 8, e <= p.E ? 16u : 0u);
+                    const uint16_t *src = p.Wr + size_t(e < p.E ? e : 0) * p.H;
+                    cp_async16(sa_u + sw128(r, c8 * 8), src + kb * kPfK + c8 * 8, e < p.E ? 16u : 0u);
                 }
             }
             asm volatile("cp.async.commit_group;" ::: "memory");   // one group per step, even if empty
@@ -563,7 +564,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmPa
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
                         const int c = 32 * j + jj;
-                        if (c < ti.n && ex <= p.E) p.logits[size_t(ti.p0 + c) * (p.E + 1) + ex] = __uint_as_float(v[jj]);
+                        if (c < ti.n && ex < p.E) p.logits[size_t(ti.p0 + c) * (p.E + 1) + ex] = __uint_as_float(v[jj]);
                     }
                 }
             }
@@ -1019,14 +1020,13 @@ cudaError_t launch_router_gemm(const RouteParams &r, cudaStream_t st)
     g.mode = 2;
     g.x = r.x;
     g.Wr = r.Wr;
-    g.ws = r.ws;
     g.logits = r.logits;
     g.err = r.err;
     g.T = r.T;
     g.H = r.H;
     g.E = r.E;
     g.k = r.k;
-    g.m_tiles = (r.E + 1 + kPfM - 1) / kPfM;
+    g.m_tiles = (r.E + kPfM - 1) / kPfM;
     CUtensorMap xmap;
     cudaError_t e = rows_map(&xmap, r.x, true, uint64_t(r.H), uint64_t(r.T));
     if (e != cudaSuccess) return e;

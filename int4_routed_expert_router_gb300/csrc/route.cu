@@ -140,20 +140,25 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const RouteParams p)
     if (tid == 0) atomicExch(p.counter, 0u);
 }
 
-// One warp per token (large T): a single level over all E experts.
+// One warp per token (large T): a single level over all E experts (the
+// threshold pass of warp_topk_thresh first), and the token's shared-gate logit
+// w_s . x_t by router_dot, as the small-T path computes it.
 __global__ void __launch_bounds__(256) topk_kernel(const RouteParams p)
 {
     __shared__ uint32_t ckey[8 * 16];
     __shared__ int32_t cid[8 * 16];
+    __shared__ uint32_t cand_k[8 * 64];
+    __shared__ int32_t cand_i[8 * 64];
     pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= p.T) return;
-    slice_topk_any((p.E + 31) / 32, p.logits + size_t(t) * (p.E + 1), p.bias, 0, p.E, p.k, ckey + warp * 16,
-                   cid + warp * 16, lane);
+    token_topk_any((p.E + 31) / 32, p.logits + size_t(t) * (p.E + 1), p.bias, p.E, p.k, ckey + warp * 16,
+                   cid + warp * 16, lane, cand_k + warp * 64, cand_i + warp * 64);
+    const float zs = router_dot(p.ws, p.x + size_t(t) * p.H, p.H, lane);
     __syncwarp();
-    write_choice(p, t, ckey + warp * 16, cid + warp * 16, __ldcg(p.logits + size_t(t) * (p.E + 1) + p.E), lane);
+    write_choice(p, t, ckey + warp * 16, cid + warp * 16, zs, lane);
 }
 
 cudaError_t route_config()

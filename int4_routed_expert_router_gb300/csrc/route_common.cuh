@@ -76,6 +76,57 @@ __device__ inline void warp_topk(uint32_t (&key)[PER], int32_t (&id)[PER], int k
     }
 }
 
+// warp_topk with a threshold pass first: the k-th largest of the 32 lanes'
+// maxima bounds the k-th largest key from below (k distinct keys reach it), so
+// only keys at or above it can be chosen, ties included. When at most 64 keys
+// qualify (the usual case) they are compacted into ck/ci (64 entries, this
+// warp's own) and selected from there; otherwise warp_topk runs on all keys.
+// The result equals warp_topk's. Needs k <= 32.
+template <int PER>
+__device__ inline void warp_topk_thresh(uint32_t (&key)[PER], int32_t (&id)[PER], int k, uint32_t *okey,
+                                        int32_t *oid, int lane, uint32_t *ck, int32_t *ci)
+{
+    uint32_t cur = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) cur = max(cur, key[j]);
+    uint32_t t0 = 0;
+    for (int s = 0; s < k; ++s) {                 // the k-th largest lane maximum
+        t0 = __reduce_max_sync(0xffffffffu, cur);
+        const uint32_t who = __ballot_sync(0xffffffffu, cur == t0);
+        if (lane == __ffs(who) - 1) cur = 0;
+    }
+    int n = 0;
+    if (t0 != 0u) {
+        const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const bool c = key[j] >= t0;
+            const uint32_t b = __ballot_sync(0xffffffffu, c);
+            const int pos = n + __popc(b & below);
+            if (c && pos < 64) {
+                ck[pos] = key[j];
+                ci[pos] = id[j];
+            }
+            n += __popc(b);
+        }
+    }
+    if (t0 == 0u || n > 64) {                    // empty slots among the maxima, or too many candidates
+        warp_topk<PER>(key, id, k, okey, oid, lane);
+        return;
+    }
+    __syncwarp();
+    uint32_t k2[2];
+    int32_t i2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int c = lane + 32 * u;
+        k2[u] = c < n ? ck[c] : 0u;
+        i2[u] = c < n ? ci[c] : 0x7fffffff;
+    }
+    __syncwarp();
+    warp_topk<2>(k2, i2, k, okey, oid, lane);
+}
+
 // Level 1 for one token slice: values z[e] (+bias) for e in [e0, e1); z may be
 // global (read through L2) or a shared-memory copy.
 template <int PER>
@@ -95,6 +146,37 @@ __device__ inline void slice_topk(const float *z, const float *bias, int e0, int
         }
     }
     warp_topk<PER>(key, id, k, okey, oid, lane);
+}
+
+// slice_topk over all E values of one token with the threshold pass.
+template <int PER>
+__device__ inline void token_topk(const float *z, const float *bias, int E, int k, uint32_t *okey, int32_t *oid,
+                                  int lane, uint32_t *ck, int32_t *ci)
+{
+    uint32_t key[PER];
+    int32_t id[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int e = lane + 32 * j;
+        key[j] = 0u;
+        id[j] = 0x7fffffff;
+        if (e < E) {
+            key[j] = fkey(z[e] + (bias ? bias[e] : 0.f));
+            id[j] = e;
+        }
+    }
+    warp_topk_thresh<PER>(key, id, k, okey, oid, lane, ck, ci);
+}
+
+__device__ inline void token_topk_any(int per, const float *z, const float *bias, int E, int k, uint32_t *ok,
+                                      int32_t *oi, int lane, uint32_t *ck, int32_t *ci)
+{
+    if (per <= 1) token_topk<1>(z, bias, E, k, ok, oi, lane, ck, ci);
+    else if (per <= 2) token_topk<2>(z, bias, E, k, ok, oi, lane, ck, ci);
+    else if (per <= 4) token_topk<4>(z, bias, E, k, ok, oi, lane, ck, ci);
+    else if (per <= 8) token_topk<8>(z, bias, E, k, ok, oi, lane, ck, ci);
+    else if (per <= 16) token_topk<16>(z, bias, E, k, ok, oi, lane, ck, ci);
+    else token_topk<32>(z, bias, E, k, ok, oi, lane, ck, ci);
 }
 
 __device__ inline void slice_topk_any(int per, const float *z, const float *bias, int e0, int e1, int k, uint32_t *ok,

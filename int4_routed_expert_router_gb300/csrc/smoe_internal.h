@@ -171,7 +171,6 @@ struct GemmParams {
     const int32_t *ntiles;
     const PfTile *tiles;
     const uint16_t *Wr;    // router rows (mode 2)
-    const uint16_t *ws;
     float *logits;         // [T][E + 1] (mode 2)
     int32_t *err;
     int T, H, E, k, I, P;
