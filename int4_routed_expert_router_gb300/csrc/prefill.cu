@@ -122,6 +122,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// tmem_ld16x256x8: 16 lanes x 64 columns; thread 4 g + t gets registers 4 r ..
+// 4 r + 3 = (lane g, column 8 r + 2 t), (g, 8 r + 2 t + 1), (g + 8, 8 r + 2 t),
+// (g + 8, 8 r + 2 t + 1), r = 0 .. 7 (lanes relative to the address's lane).
+__device__ __forceinline__ void tmem_ld16x256x8(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+                   "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+                   "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void umma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
 {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -580,22 +595,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmPa
 }
 
 // Epilogue of the expert GEMMs: warp w reads TMEM lanes 32 (w % 4) .. + 31
-// (tile rows; a warp may only access its own lane quadrant) and column chunks
-// of 32 tokens. Gate/up: 8 warps, 2 per quadrant, 3 chunks each; SwiGLU of each
-// unit's gate row r and up row r ^ 8, h written in the down GEMM's K order.
-// Down: 12 warps, 3 per quadrant, 2 chunks each; each pair's fp16 output, two
-// rows per 4-byte store (neighbouring lanes swap halves).
+// (tile rows; a warp may only access its own lane quadrant).
+// Gate/up: 8 warps, 2 per quadrant, each the 16 lanes of 8 units (rows g:
+// gate, g + 8: up) in chunks of 64 tokens, loaded so that a thread holds both
+// rows of its unit; h = silu(gate) * up, and units g, g + 1 (adjacent columns of
+// h in the down GEMM's K order) share a 4-byte store.
+// Down: 12 warps, 3 per quadrant, chunks of 32 tokens; each pair's fp16
+// output, two rows per 4-byte store (neighbouring lanes swap halves).
 template <typename TileOf>
 __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uint64_t *accfull, uint64_t *accempty,
                                          volatile int *abort, int warp, int lane, int my_tiles, TileOf tile_of)
 {
     const int q = warp & 3;
-    const int nh = p.mode == 1 ? 3 : 2;                           // warps per quadrant
-    const int h = warp >= kXGatherW0 ? 2 : (warp - kPfWorkers) >> 2;
-    const int r = 32 * q + lane;
-    const int odd = lane & 1;
-    bool range_bad = false;
-    uint32_t ymax = 0;                                            // largest |fp16| bits of the down outputs, per half
+    const int h = warp >= kXGatherW0 ? 2 : (warp - kPfWorkers) >> 2;   // warp within its quadrant
+    uint32_t ymax = 0;                                            // largest |fp16| bits stored, per half
     TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
     for (int i = 0; i < my_tiles; ++i) {
         const int b = i & 1;
@@ -604,42 +617,51 @@ __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uin
         if (i + 1 < my_tiles) tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
         pf_wait(&accfull[b], (i / 2) & 1, p.err, abort);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (!ti.valid) set_error(p.err, SMOE_DEV_BAD_SLOT);
-        const float keep = ti.valid ? 1.f : 0.f;
-        for (int j = h; 32 * j < ti.N; j += nh) {                 // uniform over the warp
-            uint32_t v[32];
-            tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(b * kXMaxN + 32 * j), v);
-            if (p.mode == 0) {
-                // rows r (gate) and r ^ 8 (up) of one intermediate unit; h goes to
-                // its column in the down GEMM's K order
-                const bool gate_row = (lane & 8) == 0;
-                const int inter = 64 * mt + 8 * (r >> 4) + (r & 7);
-                const int hcol = (inter & ~63) | perm64(inter & 63);
+        if (!ti.valid) set_error(p.err, SMOE_DEV_BAD_SLOT);       // and the tile's outputs are zeros
+        if (p.mode == 0) {
+            // units 8 (2 q + h) + g, g = lane / 4: h of unit g for tokens c0, c0 + 1
+            // (c0 = 64 cc + 8 r + 2 t, t = lane % 4); the even unit of a pair stores
+            // both units' h of token c0, the odd one those of token c0 + 1
+            const int g = lane >> 2, t = lane & 3, godd = g & 1;
+            const int inter = 64 * mt + 8 * (2 * q + h) + (g & ~1);
+            const int hcol = (inter & ~63) | perm64(inter & 63);        // units g & ~1, (g & ~1) + 1
+            const uint32_t sel = godd ? 0x3276u : 0x5410u;
+            for (int cc = 0; 64 * cc < ti.N; ++cc) {                    // uniform over the warp
+                uint32_t v[32];
+                tmem_ld16x256x8(tmem + (uint32_t(32 * q + 16 * h) << 16) + uint32_t(b * kXMaxN + 64 * cc), v);
+                const int c0 = 64 * cc + 2 * t + godd;                  // this thread's token, + 8 r
+                uint32_t *hp = reinterpret_cast<uint32_t *>(p.hbuf + size_t(ti.rowbase + c0) * p.I + hcol);
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 2) {
-                    const float a0 = __uint_as_float(v[jj]) * keep, a1 = __uint_as_float(v[jj + 1]) * keep;
-                    const float other = __shfl_xor_sync(0xffffffffu, gate_row ? a1 : a0, 8);
-                    const float gv = gate_row ? a0 : other, uv = gate_row ? other : a1;
-                    const int c = 32 * j + jj + (gate_row ? 0 : 1);
-                    const float hv = silu_f(gv) * uv;
-                    if (c < ti.n) {
-                        range_bad |= !(fabsf(hv) < 65504.f);
-                        p.hbuf[size_t(ti.rowbase + c) * p.I + hcol] = f32_to_f16_bits(hv);
+                for (int rr = 0; rr < 8; ++rr) {
+                    const float ha = silu_f(__uint_as_float(v[4 * rr])) * __uint_as_float(v[4 * rr + 2]);
+                    const float hb = silu_f(__uint_as_float(v[4 * rr + 1])) * __uint_as_float(v[4 * rr + 3]);
+                    const uint32_t h2 = pack_f16x2(ha, hb);
+                    const uint32_t nb = __shfl_xor_sync(0xffffffffu, h2, 4);
+                    const uint32_t o = ti.valid ? __byte_perm(h2, nb, sel) : 0u;
+                    if (c0 + 8 * rr < ti.n) {
+                        ymax = __vmaxu2(ymax, o & 0x7fff7fffu);
+                        hp[size_t(8 * rr) * (p.I / 2)] = o;
                     }
                 }
-            } else {
-                // columns 2m (even lane) and 2m + 1 (odd lane) of rows R, R + 1 (R even):
-                // each lane packs (col 2m, col 2m + 1) of its row, swaps with its
-                // neighbour, and stores one column of both rows
-                const int R0 = kPfM * mt + r - odd;
+            }
+        } else {
+            // chunks j of 32 tokens; lane = row R of the down projection. Tokens 2 m
+            // (even lane) and 2 m + 1 (odd lane) of rows R0, R0 + 1: each lane packs
+            // its row's two tokens, swaps with its neighbour, and stores one token
+            // of both rows
+            const int odd = lane & 1;
+            const int R0 = kPfM * mt + 32 * q + lane - odd;
+            const uint32_t sel = odd ? 0x3276u : 0x5410u;
+            for (int j = h; 32 * j < ti.N; j += 3) {                    // uniform over the warp
+                uint32_t v[32];
+                tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(b * kXMaxN + 32 * j), v);
                 uint32_t *y = reinterpret_cast<uint32_t *>(p.ypair + size_t(ti.rowbase + 32 * j + odd) * p.H + R0);
-                const int nc = ti.n - 32 * j - odd;                 // stored when 2m < nc
-                const uint32_t sel = odd ? 0x3276u : 0x5410u;
+                const int nc = ti.n - 32 * j - odd;                     // stored when 2 m < nc
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
-                    const uint32_t h2 = pack_f16x2(__uint_as_float(v[2 * m]) * keep, __uint_as_float(v[2 * m + 1]) * keep);
+                    const uint32_t h2 = pack_f16x2(__uint_as_float(v[2 * m]), __uint_as_float(v[2 * m + 1]));
                     const uint32_t nb = __shfl_xor_sync(0xffffffffu, h2, 1);
-                    const uint32_t o = __byte_perm(h2, nb, sel);
+                    const uint32_t o = ti.valid ? __byte_perm(h2, nb, sel) : 0u;
                     if (2 * m < nc) {
                         ymax = __vmaxu2(ymax, o & 0x7fff7fffu);
                         y[size_t(2 * m) * (p.H / 2)] = o;
@@ -652,7 +674,7 @@ __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uin
         mbar_arrive(&accempty[b]);
     }
     // 0x7bff is 65504, the largest finite fp16; above it: infinities and NaN
-    if (range_bad || (ymax & 0xffffu) >= 0x7bffu || (ymax >> 16) >= 0x7bffu) set_error(p.err, SMOE_DEV_RANGE);
+    if ((ymax & 0xffffu) >= 0x7bffu || (ymax >> 16) >= 0x7bffu) set_error(p.err, SMOE_DEV_RANGE);
 }
 
 // ------------------------------------------------- expert GEMMs, A in TMEM
