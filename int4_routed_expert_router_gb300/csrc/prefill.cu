@@ -52,7 +52,6 @@ constexpr int kPfBBytes = kPfMaxN * kPfK * 2;       // 32 KiB
 constexpr int kPfStageBytes = kPfABytes + kPfBBytes;
 constexpr int kPfSmem = kPfAB * kPfStageBytes + 1024 /*align*/ + 512 /*barriers*/;
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
-constexpr int kBucketTok = 64;     // tokens per bucketing chunk
 
 // Expert GEMMs (gate/up, down): A (the dequantised weights) lives in tensor
 // memory. TMEM columns: two accumulators of kXMaxN columns, then kXStg A
@@ -188,13 +187,13 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // ---------------------------------------------------------------- bucketing
-// counts and chunk_base are [chunks][E]: the scan's threads (one per expert)
-// and the scatter's lanes read one chunk's row together, coalesced.
+// counts and chunk_base are [E][chunks] (chunks of kBucketTok tokens): the
+// scan's warps (one per expert) read and write an expert's row coalesced.
 
 __global__ void __launch_bounds__(256) bucket_count_kernel(const PrefillParams p)
 {
     __shared__ int cnt[1024];
-    const int c = blockIdx.x;
+    const int c = blockIdx.x, nch = gridDim.x;
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     const int t0 = c * kBucketTok, t1 = min(p.T, t0 + kBucketTok);
@@ -204,31 +203,51 @@ __global__ void __launch_bounds__(256) bucket_count_kernel(const PrefillParams p
         else set_error(p.err, SMOE_DEV_BAD_EXPERT);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < p.E; e += blockDim.x) p.counts[size_t(c) * p.E + e] = cnt[e];
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) p.counts[size_t(e) * nch + c] = cnt[e];
 }
 
-// One CTA: per-expert chunk prefixes, expert offsets, and the tile list.
+// One warp per expert: chunk_base[e][c] = pairs of expert e in chunks before
+// c (warp scans of 32 chunks at a time), the expert's total into offsets[e].
+// The last CTA to finish (arrival ticket) turns the totals into the expert
+// offsets (exclusive prefix) and writes the tile list: per expert, runs of at
+// most kXMaxN pairs of near-equal size; then the shared expert's runs over T.
 __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p)
 {
     __shared__ int buf[1024];
     __shared__ int tbuf[1024];
-    const int e = threadIdx.x;
+    __shared__ int last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nch = (p.T + kBucketTok - 1) / kBucketTok;
-    int total = 0;
-    if (e < p.E) {
-        for (int c0 = 0; c0 < nch; c0 += 32) {       // 32 loads in flight, then the running sum
-            int v[32];
+    const int ew = blockIdx.x * 32 + warp;
+    if (ew < p.E) {
+        const int *row = p.counts + size_t(ew) * nch;
+        int *brow = p.chunk_base + size_t(ew) * nch;
+        int carry = 0;
+        for (int c0 = 0; c0 < nch; c0 += 32) {
+            const int c = c0 + lane;
+            const int v = c < nch ? row[c] : 0;
+            int incl = v;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = c0 + j < nch ? p.counts[size_t(c0 + j) * p.E + e] : 0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (c0 + j < nch) p.chunk_base[size_t(c0 + j) * p.E + e] = total;
-                total += v[j];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
             }
+            if (c < nch) brow[c] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            p.offsets[ew] = carry;
+            __threadfence();
         }
     }
-    const int nt = e < p.E ? (total + kXMaxN - 1) / kXMaxN : 0;
-    buf[e] = e < p.E ? total : 0;
+    __syncthreads();
+    if (tid == 0) last = ticket_add(p.ticket, 1u) == gridDim.x - 1 ? 1 : 0;
+    __syncthreads();
+    if (!last) return;
+    const int e = tid;
+    const int total = e < p.E ? __ldcg(p.offsets + e) : 0;
+    const int nt = (total + kXMaxN - 1) / kXMaxN;
+    buf[e] = total;
     tbuf[e] = nt;
     __syncthreads();
     for (int off = 1; off < 1024; off <<= 1) {       // inclusive scans of totals and tile counts
@@ -238,14 +257,14 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
         tbuf[e] += b;
         __syncthreads();
     }
-    const int start = buf[e] - (e < p.E ? total : 0);     // exclusive
+    const int start = buf[e] - total;                 // exclusive
     const int tstart = tbuf[e] - nt;
     if (e < p.E) {
         p.offsets[e] = start;                         // the scatter adds it to the chunk prefixes
+        const int64_t slot = p.table_row[e];
         for (int i = 0; i < nt; ++i) {
             PfTile tl;
             tl.kind = 0;
-            const int64_t slot = p.table_row[e];
             tl.slot = (slot < 0 || slot >= p.n_slots) ? -1 : int(slot);
             tl.p0 = start + int((int64_t(i) * total) / nt);               // runs of near-equal size
             tl.n = int((int64_t(i + 1) * total) / nt) - int((int64_t(i) * total) / nt);
@@ -265,6 +284,7 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
     if (e == 0) {
         p.offsets[p.E] = buf[1023];
         *p.ntiles = ntr + nts;
+        atomicExch(p.ticket, 0u);                     // ready for the next call
     }
 }
 
@@ -275,8 +295,8 @@ __global__ void __launch_bounds__(32) bucket_scatter_kernel(const PrefillParams 
 {
     __shared__ int base[1024];
     __shared__ int ids_s[kBucketTok * 16];
-    const int c = blockIdx.x, lane = threadIdx.x;
-    for (int e = lane; e < p.E; e += 32) base[e] = p.offsets[e] + p.chunk_base[size_t(c) * p.E + e];
+    const int c = blockIdx.x, nch = gridDim.x, lane = threadIdx.x;
+    for (int e = lane; e < p.E; e += 32) base[e] = p.offsets[e] + p.chunk_base[size_t(e) * nch + c];
     const int t0 = c * kBucketTok, t1 = min(p.T, t0 + kBucketTok);
     for (int q = t0 * p.k + lane; q < t1 * p.k; q += 32) ids_s[q - t0 * p.k] = p.ids[q];
     __syncwarp();
@@ -1074,7 +1094,7 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
     if ((e = atoms_map(&dn_pool, pool_down, g0.I / kGroup, p.H / 16, g0.n_slots, g0.stride)) != cudaSuccess) return e;
     if ((e = atoms_map(&dn_shared, shared_down, g0.I / kGroup, p.H / 16, 1, g0.stride)) != cudaSuccess) return e;
     bucket_count_kernel<<<nch, 256, 0, st>>>(p);
-    bucket_scan_kernel<<<1, 1024, 0, st>>>(p);
+    bucket_scan_kernel<<<(p.E + 31) / 32, 1024, 0, st>>>(p);
     bucket_scatter_kernel<<<nch, 32, 0, st>>>(p);
     convert_x_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(g0);
     const int maxt = prefill_max_tiles(p.T, p.k, p.E);

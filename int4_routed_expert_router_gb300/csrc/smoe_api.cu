@@ -138,7 +138,7 @@ Workspace workspace_layout(const smoe_shape &s, int T)
         const uint64_t umax = uint64_t(s.E < T * s.k ? s.E : T * s.k) + 1;
         w.ypair = o;     o = al(o + umax * T * s.H * 4);
     } else {
-        const uint64_t P = uint64_t(T) * s.k, nch = (uint64_t(T) + 63) / 64;
+        const uint64_t P = uint64_t(T) * s.k, nch = (uint64_t(T) + kBucketTok - 1) / kBucketTok;
         w.counts = o;     o = al(o + nch * s.E * 4);
         w.chunk_base = o; o = al(o + nch * s.E * 4);
         w.offsets = o;    o = al(o + (uint64_t(s.E) + 1) * 4);
@@ -320,7 +320,9 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
         return SMOE_EINVAL;
     if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
     if (T == 0) return SMOE_OK;
-    if (!aligned16(x) || !aligned16(pool) || !aligned16(shared_blob) || !aligned16(workspace)) return SMOE_EINVAL;
+    if (!aligned16(x) || !aligned16(pool) || !aligned16(shared_blob) || !aligned16(workspace) || !aligned16(out) ||
+        (residual && !aligned16(residual)))
+        return SMOE_EINVAL;
     if (pool_bytes < uint64_t(ctx->n_slots) * ctx->layout.blob) return SMOE_ENOMEM;
     const Workspace W = workspace_layout(ctx->shape, T);
     if (workspace_bytes < W.total) return SMOE_ENOMEM;
@@ -331,6 +333,7 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
         q.ids = ids;
         q.counts = reinterpret_cast<int32_t *>(ws + W.counts);
         q.chunk_base = reinterpret_cast<int32_t *>(ws + W.chunk_base);
+        q.ticket = reinterpret_cast<uint32_t *>(ws + W.fwd_counters);   // unused by the T <= 8 path of this call
         q.offsets = reinterpret_cast<int32_t *>(ws + W.offsets);
         q.tiles = reinterpret_cast<PfTile *>(ws + W.tiles);
         q.ntiles = reinterpret_cast<int32_t *>(ws + W.ntiles);

@@ -15,6 +15,7 @@ constexpr int kAtomBytes = 576;     // nibbles + 16 (s, b) fp16 pairs
 
 // Decode kernel (fused experts, T <= kDecodeMaxT).
 constexpr int kDecodeMaxT = 8;
+constexpr int kBucketTok = 32;     // tokens per bucketing chunk (T > kDecodeMaxT path)
 constexpr int kSlice = 32;                        // intermediates per CTA
 constexpr int kChunkCols = 256;                   // H columns per streamed chunk
 constexpr int kRowBlocksA = kSlice / 8;           // gate/up row blocks per CTA
@@ -138,8 +139,9 @@ struct PfTile {
 // Token-bucketed path (T > 8): bucketing and combine.
 struct PrefillParams {
     const int32_t *ids;
-    int32_t *counts;       // [chunks][E]
-    int32_t *chunk_base;   // [chunks][E]
+    int32_t *counts;       // [E][chunks]
+    int32_t *chunk_base;   // [E][chunks]
+    uint32_t *ticket;      // arrival ticket of the scan (zero between calls)
     int32_t *offsets;      // [E + 1]
     PfTile *tiles;         // [max tiles]
     int32_t *ntiles;
