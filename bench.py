@@ -170,6 +170,24 @@ def recorded_traffic(workload: str):
     return d.get("dram_bytes_per_launch")
 
 
+PREFILL_SOURCES = ["int4_routed_expert_router_gb300/csrc/prefill.cu",
+                   "int4_routed_expert_router_gb300/csrc/smoe_dev.cuh",
+                   "int4_routed_expert_router_gb300/csrc/smoe_internal.h"]
+
+
+def prefill_traffic(workload: str):
+    """DRAM bytes per launch of the gate/up expert GEMM from the committed ncu
+    summary, only if the prefill sources are unchanged since it was taken."""
+    p = os.path.join(ROOT, "profiles", "expert_gemm_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_sha256") != src_hash(PREFILL_SOURCES) or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
 L2_BYTES = 129 * 10**6
 
 
@@ -431,7 +449,7 @@ def run_ours(args, wl, world, rank, dist):
         ach = flops / (kern_ms / 1e3) / 1e12
         peak = pk["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4), "traffic": None,
+                "frac": round(ach / peak, 4), "traffic": prefill_traffic(wl.name),
                 "kernel": "expert_gemm_kernel gate/up (fp16 operands, A in TMEM, fp32 accumulate)",
                 "flops_per_launch": flops, "us_per_launch": round(kern_ms * 1e3, 3),
                 "down_gemm_us": round(down_ms * 1e3, 3) if down_ms else None,
