@@ -5,12 +5,13 @@
 //   1. x_l and this CTA's router rows (rows c, c + G, ...; row E is the
 //      shared-gate vector) are bulk-copied into shared memory; the CTA's
 //      logits go to the workspace; counter A.
-//   2. Every CTA reads all E + 1 logits and computes the same top-k,
-//      renormalised weights and shared gate (the routing kernel's arithmetic,
-//      route_common.cuh); CTA 0 also writes them out.
+//   2. Every CTA reads all E + 1 logits and computes the same top-k (by rank
+//      among the few logits that can be chosen), renormalised weights and
+//      shared gate (route_common.cuh's arithmetic); CTA 0 also writes them out.
 //   3. Gate/up: work units (expert u, 16-row block rb: intermediates
 //      8 rb .. 8 rb + 7, 32 contiguous atoms, one bulk copy) are spread over
-//      all CTAs; SwiGLU values go to the workspace as fp32; counter B.
+//      all CTAs; SwiGLU values go to the workspace as bf16 high and low
+//      parts with each unit's sum of them; counter B.
 //   4. Down and combine: CTA c < H/16 owns output rows 16 c .. 16 c + 15. Its
 //      down atoms of every expert were requested in step 3, so they stream in
 //      with the gate/up weights; after counter B it reads all h, computes the
@@ -33,7 +34,7 @@ constexpr int kStkWarps = 16;
 constexpr int kStkThreads = kStkWarps * 32;
 
 struct StkSmem {
-    int x_s, xsum, rows, zs, table, units, wdn, hraw, hh, hl, hsum, yp, red, cand, ints, bars, total;
+    int x_s, xsum, rows, zs, table, units, wdn, hps, hh, hl, hsum, yp, red, cand, ints, bars, total;
 };
 
 __host__ __device__ inline StkSmem stk_smem(int H, int E, int I, int U, int nr, int nu)
@@ -47,13 +48,13 @@ __host__ __device__ inline StkSmem stk_smem(int H, int E, int I, int U, int nr, 
     L.table = o; o = align128(o + E * 4);
     L.units = o; o = align128(o + nu * (H / kGroup) * kAtomBytes);
     L.wdn = o;   o = align128(o + U * (I / kGroup) * kAtomBytes);
-    L.hraw = o;  o = align128(o + U * I * 4);
+    L.hps = o;   o = align128(o + U * (I / 8) * 4);
     L.hh = o;    o = align128(o + U * (I + 8) * 2);
     L.hl = o;    o = align128(o + U * (I + 8) * 2);
     L.hsum = o;  o = align128(o + U * (I / kGroup) * kDecodeMaxT * 4);
     L.yp = o;    o = align128(o + U * 2 * 16 * 4);
     L.red = o;   o = align128(o + kStkWarps * 32 * 16);
-    L.cand = o;  o = align128(o + 2 * (8 * 16 + 16) * 4);
+    L.cand = o;  o = align128(o + (2 * E + 2 * 16 + 2 * 16) * 4);
     L.ints = o;  o = align128(o + 64 * 4);
     L.bars = o;  o = align128(o + (nu + U + 3) * 8);
     L.total = o;
@@ -71,10 +72,10 @@ __device__ __forceinline__ void prefetch_l2_bytes(const void *p, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
 {
     uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
@@ -86,29 +87,41 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 
 // Thread 0 waits until *ctr >= target (two seconds at most, or until another
-// CTA raised the abort word), then the CTA synchronises. Returns false if the
-// wait gave up; the results of the step are then garbage and the error word
-// says so, but every CTA still runs to the end.
+// CTA raised the abort word), then the CTA synchronises. The counter is polled
+// with relaxed loads, one in flight at a time and spaced by a short sleep (the
+// abort word and the clock every 16 polls), and an acquire fence then orders what the arrivals
+// released before this CTA's reads. Returns false if the wait gave up; the
+// results of the step are then garbage and the error word says so, but every
+// CTA still runs to the end.
 __device__ bool grid_wait(const uint32_t *ctr, uint32_t target, uint32_t *abortw, int32_t *err, int *flag_s)
 {
     if (threadIdx.x == 0) {
         int ok = 1;
         const uint64_t t0 = global_ns();
-        while (ld_acquire(ctr) < target) {
-            if (ld_acquire(abortw)) { ok = 0; break; }
-            if (global_ns() - t0 > 2000000000ull) {
-                atomicExch(abortw, 1u);
-                set_error(err, SMOE_DEV_TIMEOUT);
-                ok = 0;
-                break;
+        for (uint32_t it = 1; ld_relaxed(ctr) < target; ++it) {
+            __nanosleep(32);                     // polls spaced out: the arrivals hit the same line
+            if ((it & 15) == 0) {
+                if (ld_relaxed(abortw)) { ok = 0; break; }
+                if (global_ns() - t0 > 2000000000ull) {
+                    atomicExch(abortw, 1u);
+                    set_error(err, SMOE_DEV_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
             }
-            __nanosleep(32);
         }
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
         asm volatile("fence.proxy.async.global;" ::: "memory");   // later bulk copies read what we acquired
         *flag_s = ok;
     }
     __syncthreads();
     return *flag_s != 0;
+}
+
+// Composite order of the routing keys: larger key first, equal keys by lower id.
+__device__ __forceinline__ bool key_before(uint32_t ka, int32_t ia, uint32_t kb, int32_t ib)
+{
+    return ka > kb || (ka == kb && ia < ib);
 }
 
 __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __grid_constant__ StackParams p)
@@ -126,19 +139,24 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
     int *table = reinterpret_cast<int *>(smem + L.table);
     uint8_t *units = smem + L.units;
     uint8_t *wdn = smem + L.wdn;
-    float *hraw = reinterpret_cast<float *>(smem + L.hraw);
+    float *hps = reinterpret_cast<float *>(smem + L.hps);
     uint16_t *hh = reinterpret_cast<uint16_t *>(smem + L.hh);
     uint16_t *hl = reinterpret_cast<uint16_t *>(smem + L.hl);
     float *hsum = reinterpret_cast<float *>(smem + L.hsum);
     float *yp = reinterpret_cast<float *>(smem + L.yp);
     float4 *red = reinterpret_cast<float4 *>(smem + L.red);
-    uint32_t *ckey = reinterpret_cast<uint32_t *>(smem + L.cand);   // [8][16] level 1, [16] final
-    int32_t *cid = reinterpret_cast<int32_t *>(ckey + 8 * 16 + 16);
+    uint32_t *cand_k = reinterpret_cast<uint32_t *>(smem + L.cand);   // [E] candidates
+    int32_t *cand_i = reinterpret_cast<int32_t *>(cand_k + E);
+    uint32_t *mx_k = reinterpret_cast<uint32_t *>(cand_i + E);        // [16] slice maxima
+    int32_t *mx_i = reinterpret_cast<int32_t *>(mx_k + 16);
+    uint32_t *sel_k = reinterpret_cast<uint32_t *>(mx_i + 16);        // [16] chosen, in route order
+    int32_t *sel_i = reinterpret_cast<int32_t *>(sel_k + 16);
     int *ints = reinterpret_cast<int *>(smem + L.ints);
     int *ids_s = ints;                  // [16] route order
     float *w_s = reinterpret_cast<float *>(ints + 16);   // [16]
     float *gate_s = reinterpret_cast<float *>(ints + 32);
     int *flag_s = ints + 33;
+    int *ncand = ints + 34;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *ubar = bars, *dbar = bars + p.nu, *xbar = dbar + U, *rbar = xbar + 1, *hbar = rbar + 1;
 
@@ -194,27 +212,73 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
         __syncthreads();
         if (tid == 0) ticket_add(&cnt[0], 1u);
 
-        // ---- 2. routing, redundantly in every CTA
+        // ---- 2. routing, redundantly in every CTA. Warp w holds the keys of slice
+        // w (E / 16 logits); the k-th largest of the 16 slice maxima bounds the
+        // k-th largest key from below (k distinct keys reach it), so only keys at
+        // or above it can be chosen. Each such candidate's rank among the
+        // candidates (larger key first, ties to the lower id) is its place in
+        // route order.
         grid_wait(&cnt[0], uint32_t(G), abortw, p.err, flag_s);
         for (int e = tid; e <= E; e += kStkThreads) zs[e] = __ldcg(p.logits + size_t(l) * (E + 1) + e);
+        if (tid == 0) *ncand = 0;
         __syncthreads();
-        if (warp < 8) {
-            const int span = (E + 7) / 8;
-            const int e0 = warp * span, e1 = min(E, e0 + span);
-            slice_topk_any((span + 31) / 32, zs, p.bias, e0, e1, k, ckey + warp * 16, cid + warp * 16, lane);
+        {
+            const int spw = (E + kStkWarps - 1) / kStkWarps;        // keys per slice (<= 64)
+            uint32_t kk[2];
+            int32_t ki[2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int j = lane + 32 * h2, e = warp * spw + j;
+                const bool in = j < spw && e < E;
+                kk[h2] = in ? fkey(zs[e] + (p.bias ? p.bias[e] : 0.f)) : 0u;
+                ki[h2] = in ? e : 0x7fffffff;
+            }
+            const bool second = key_before(kk[1], ki[1], kk[0], ki[0]);
+            const uint32_t bk = second ? kk[1] : kk[0];
+            const int32_t bi = second ? ki[1] : ki[0];
+            const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+            const int32_t mi = int32_t(__reduce_min_sync(0xffffffffu, uint32_t(bk == mk ? bi : 0x7fffffff)));
+            if (lane == 0) {
+                mx_k[warp] = mk;
+                mx_i[warp] = mi;
+            }
+            __syncthreads();
+            // the k-th largest slice maximum (k <= 16 slices): the one with rank k - 1
+            int rank = 0;
+            if (lane < kStkWarps)
+                for (int j = 0; j < kStkWarps; ++j) rank += key_before(mx_k[j], mx_i[j], mx_k[lane], mx_i[lane]);
+            // (fewer than k slices with keys: no such rank; then every key is a candidate)
+            const int tl = __ffs(__ballot_sync(0xffffffffu, lane < kStkWarps && rank == k - 1)) - 1;
+            const uint32_t t_k = tl >= 0 ? mx_k[tl] : 0u;
+            const int32_t t_i = tl >= 0 ? mx_i[tl] : 0x7fffffff;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+                if (kk[h2] != 0u && !key_before(t_k, t_i, kk[h2], ki[h2])) {
+                    const int pos = atomicAdd(ncand, 1);
+                    cand_k[pos] = kk[h2];
+                    cand_i[pos] = ki[h2];
+                }
+            __syncthreads();
+            const int n = *ncand;
+            for (int q = tid; q < n; q += kStkThreads) {
+                const uint32_t ck = cand_k[q];
+                const int32_t ci = cand_i[q];
+                int r = 0;
+                for (int j = 0; j < n; ++j) r += key_before(cand_k[j], cand_i[j], ck, ci);
+                if (r < k) {
+                    sel_k[r] = ck;
+                    sel_i[r] = ci;
+                }
+            }
+            __syncthreads();
         }
-        __syncthreads();
         if (warp == 0) {
-            uint32_t *fk = ckey + 8 * 16;
-            int32_t *fi = cid + 8 * 16;
-            topk_merge(ckey, cid, 8, k, fk, fi, lane);
-            __syncwarp();
-            const float wl = choice_weight(fk, k, lane);
+            const float wl = choice_weight(sel_k, k, lane);
             if (lane < k) {
-                ids_s[lane] = fi[lane];
+                ids_s[lane] = sel_i[lane];
                 w_s[lane] = wl;
                 if (c == 0) {
-                    p.ids[size_t(l) * k + lane] = fi[lane];
+                    p.ids[size_t(l) * k + lane] = sel_i[lane];
                     p.w[size_t(l) * k + lane] = wl;
                 }
             }
@@ -310,9 +374,22 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                     aG += v.x;
                     aU += v.y;
                 }
-                // rows g (gate) and g + 8 (up) of the block are intermediate 8 rb + g; token = column 0
-                if (t4 == 0)
-                    __stcg(p.h + (size_t(l) * U + u) * I + 8 * rb + g, (valid && !bad) ? silu(aG) * aU : 0.f);
+                // rows g (gate) and g + 8 (up) of the block are intermediate 8 rb + g; token =
+                // column 0. h goes out as bf16 hi and lo = bf16(h - hi), with the unit's
+                // sum of hi + lo over its 8 intermediates (the down rows' bias term)
+                const float hv = (valid && !bad) ? silu(aG) * aU : 0.f;
+                const uint16_t hi = f32_to_bf16_bits(hv);
+                const uint16_t lo = f32_to_bf16_bits(hv - __uint_as_float(uint32_t(hi) << 16));
+                float sum = __uint_as_float(uint32_t(hi) << 16) + __uint_as_float(uint32_t(lo) << 16);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+                uint16_t *hrow = p.h + (size_t(l) * 2 * U + u) * I;
+                if (t4 == 0) {
+                    __stcg(hrow + 8 * rb + g, hi);
+                    __stcg(hrow + size_t(U) * I + 8 * rb + g, lo);
+                }
+                if (lane == 0) __stcg(p.hps + (size_t(l) * U + u) * nrb + rb, sum);
             }
             __syncthreads();
         }
@@ -321,30 +398,28 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
         // ---- 5. down rows of every expert for rows 16 c .. 16 c + 15, combine
         if (c < nrbB) {
             grid_wait(&cnt[1], uint32_t(G), abortw, p.err, flag_s);
-            if (tid == 0) {
-                mbar_arrive_expect_tx(hbar, uint32_t(U * I * 4));
-                bulk_nohint(hraw, p.h + size_t(l) * U * I, uint32_t(U * I * 4), hbar);
+            // h rows of every expert (hi, lo; padded rows), and the unit sums: one bulk
+            // copy per lane of warp 0
+            if (warp == 0) {
+                if (lane == 0) mbar_arrive_expect_tx(hbar, uint32_t(U * I * 4 + U * nrb * 4));
+                __syncwarp();
+                const uint16_t *hl_src = p.h + size_t(l) * 2 * U * I;
+                for (int j = lane; j < 2 * U + 1; j += 32) {
+                    if (j < U)
+                        bulk_nohint(hh + j * (I + 8), hl_src + size_t(j) * I, uint32_t(I * 2), hbar);
+                    else if (j < 2 * U)
+                        bulk_nohint(hl + (j - U) * (I + 8), hl_src + size_t(U + (j - U)) * I, uint32_t(I * 2), hbar);
+                    else
+                        bulk_nohint(hps, p.hps + size_t(l) * U * nrb, uint32_t(U * nrb * 4), hbar);
+                }
             }
             if (!bad && !mbar_wait(hbar, par, p.err)) bad = true;
-            const float4 *h4 = reinterpret_cast<const float4 *>(hraw);
-            for (int i = tid; i < U * I / 4; i += kStkThreads) {
-                const float4 v = h4[i];
-                const int u = (4 * i) / I, cc = (4 * i) % I;
-                const uint32_t h01 = pack_bf16x2(v.x, v.y), h23 = pack_bf16x2(v.z, v.w);
-                const uint32_t l01 = pack_bf16x2(v.x - bf16lo(h01), v.y - bf16hi(h01));
-                const uint32_t l23 = pack_bf16x2(v.z - bf16lo(h23), v.w - bf16hi(h23));
-                *reinterpret_cast<uint2 *>(hh + u * (I + 8) + cc) = make_uint2(h01, h23);
-                *reinterpret_cast<uint2 *>(hl + u * (I + 8) + cc) = make_uint2(l01, l23);
-            }
-            __syncthreads();
-            for (int it = warp; it < U * ngI; it += kStkWarps) {    // group sums of hi + lo
-                const int u = it / ngI, grp = it % ngI;
-                const int o = u * (I + 8) + grp * kGroup + 2 * lane;
-                const uint32_t vh = *reinterpret_cast<const uint32_t *>(hh + o);
-                const uint32_t vl = *reinterpret_cast<const uint32_t *>(hl + o);
-                float s = (bf16lo(vh) + bf16lo(vl)) + (bf16hi(vh) + bf16hi(vl));
-                for (int o2 = 16; o2; o2 >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o2);
-                if (lane == 0) hsum[(u * ngI + grp) * kDecodeMaxT] = s;
+            for (int it = tid; it < U * ngI; it += kStkThreads) {   // group sums: the 8 unit sums in order
+                const float *ps = hps + it * 8;
+                float s2 = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s2 += ps[j];
+                hsum[it * kDecodeMaxT] = s2;
             }
             __syncthreads();
             const int nkh = ngI >= 2 ? 2 : 1;

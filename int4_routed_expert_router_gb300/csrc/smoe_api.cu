@@ -424,7 +424,7 @@ extern "C" int smoe_set_profile_events(smoe_ctx *ctx, void *const *events, int32
 
 // Workspace of moe_decode_stack: logits [n][E + 1], h [n][U][I] fp32, counters.
 struct StackWs {
-    uint64_t logits, h, sync, total;
+    uint64_t logits, h, hps, sync, total;
 };
 
 static StackWs stack_ws(const smoe_ctx *ctx, int n)
@@ -435,6 +435,7 @@ static StackWs stack_ws(const smoe_ctx *ctx, int n)
     uint64_t o = 0;
     w.logits = o; o = al(o + uint64_t(n) * (s.E + 1) * 4);
     w.h = o;      o = al(o + uint64_t(n) * ctx->stack.U * s.I * 4);
+    w.hps = o;    o = al(o + uint64_t(n) * ctx->stack.U * (s.I / 8) * 4);
     w.sync = o;   o = al(o + (3 * uint64_t(n) + 1) * 4);
     w.total = o;
     return w;
@@ -479,7 +480,8 @@ extern "C" int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_
     p.stride = ctx->layout.blob;
     p.n_slots = ctx->n_slots;
     p.logits = reinterpret_cast<float *>(ws + W.logits);
-    p.h = reinterpret_cast<float *>(ws + W.h);
+    p.h = reinterpret_cast<uint16_t *>(ws + W.h);
+    p.hps = reinterpret_cast<float *>(ws + W.hps);
     p.sync = reinterpret_cast<uint32_t *>(ws + W.sync);
     p.err = err;
     p.n_layers = n_layers;

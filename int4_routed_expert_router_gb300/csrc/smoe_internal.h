@@ -70,7 +70,8 @@ struct StackParams {
     uint64_t stride;
     int64_t n_slots;
     float *logits;                             // [n_layers][E + 1]
-    float *h;                                  // [n_layers][U][I]
+    uint16_t *h;                               // [n_layers][2][U][I] bf16: h's high part, then h - high
+    float *hps;                                // [n_layers][U][I / 8] sum of hi + lo per 8-row unit
     uint32_t *sync;                            // [n_layers][3] arrival counters, then the abort word
     int32_t *err;
     int n_layers, H, E, k, I, U, nr, nu;
