@@ -215,5 +215,7 @@ WORKLOADS = {
                  "80B-shaped batched decode: T=64, Zipf(1.1) router offsets"),
         Workload("prefill80b", 2048, 512, 10, 512, 512, 8192, 1, False, False, 8192,
                  "80B-shaped prefill: T=8192, uniform router"),
+        Workload("prefill35b", 2048, 256, 8, 512, 512, 8192, 1, False, False, 3592,
+                 "35B-shaped prefill: T=8192, uniform router"),
     ]
 }
