@@ -49,8 +49,11 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (profiling of small cases)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", default="stack", choices=["stack", "layers"],
-                    help="one-token steps: one moe_decode_stack launch (default) or moe_route + moe_forward per layer")
+    ap.add_argument("--path", default="stack", choices=["stack", "layers", "cached"],
+                    help="one-token steps: one moe_decode_stack launch (default), moe_route + moe_forward per "
+                         "layer, or per layer through the streaming slot pool (cached)")
+    ap.add_argument("--cache-fraction", type=float, default=0.25,
+                    help="cached path: device slots as a fraction of all experts of the stack")
     return ap.parse_args()
 
 
@@ -472,6 +475,81 @@ def run_ours(args, wl, world, rank, dist):
     print(json.dumps(line), flush=True)
 
 
+def run_cached(args, wl, world, rank):
+    """One token per step through the stack, per layer: moe_route, its ids read
+    to the host, smoe_cache_prepare (misses copied from pinned host memory into
+    the bounded device pool), moe_forward. The steps cycle through 64 seeded
+    token inputs (a decoded sequence), so the routing changes from step to step."""
+    import numpy as np
+    import torch
+
+    import int4_routed_expert_router_gb300 as smoe
+    import synthetic
+    import workload as W
+
+    full = W.DevicePool(wl)
+    inp = W.LayerInputs(wl, wl.n_layers)
+    L, E, stride = wl.n_layers, wl.E, full.stride
+    idx = torch.from_numpy(full.table.astype(np.int64)).cuda().reshape(-1)
+    store = torch.empty(L * E * stride, dtype=torch.uint8).pin_memory()
+    for l in range(L):                                   # every expert's blob, [layer][expert] order
+        store[l * E * stride:(l + 1) * E * stride].copy_(full.pool.view(-1, stride).index_select(0, idx[l * E:(l + 1) * E]).reshape(-1))
+    shared = full.shared
+    del full
+    torch.cuda.empty_cache()
+    n_slots = max(4 * wl.k, int(args.cache_fraction * L * E))
+    pool = torch.empty(n_slots * stride, dtype=torch.uint8, device="cuda")
+    table = torch.zeros((L, E), dtype=torch.int32, device="cuda")
+    ctx = smoe.Context(smoe.make_shape(wl.H, wl.E, wl.k, wl.I, wl.I_shared), L, n_slots, table)
+    cache = smoe.Cache(ctx, store, pool)
+    xs = torch.zeros((L + 1, 1, wl.H), dtype=torch.bfloat16, device="cuda")
+    tokens = W.bf16_tensor(synthetic.activations(wl.seed, 64, wl.H, tag=4243))      # [64, H]
+    ids = torch.zeros((1, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((1, wl.k), dtype=torch.float32, device="cuda")
+    gate = torch.zeros((1,), dtype=torch.float32, device="cuda")
+    ws = W.workspace(ctx, 1)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ids_h = torch.zeros((1, wl.k), dtype=torch.int32).pin_memory()
+
+    def step(i):
+        xs[0].copy_(tokens[i % 64:i % 64 + 1])
+        for l in range(L):
+            smoe.moe_route(ctx, inp.Wr[l], inp.ws[l], xs[l], ids, w, gate, ws, logit_bias=inp.bias)
+            ids_h.copy_(ids)                                 # waits for the routing
+            cache.prepare(l, ids_h.numpy())
+            smoe.moe_forward(ctx, l, xs[l], ids, w, gate, pool, shared[l], xs[l + 1], ws, err, residual=xs[l])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    h0, m0, b0 = cache.stats()
+    sampler = ClockSampler()
+    sampler.start()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    sampler.stop()
+    if smoe.check(err) != 0:
+        raise RuntimeError("device error word set during the cached run")
+    h1, m1, b1 = cache.stats()
+    hits, misses, nbytes = h1 - h0, m1 - m0, b1 - b0
+    value = args.steps * L / el
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(wl, "streaming slot pool: %d of %d experts resident, per layer moe_route, ids to "
+                                    "the host, smoe_cache_prepare, moe_forward; steps cycle through 64 token "
+                                    "inputs" % (n_slots, L * E), None, False),
+            "cache": {"slots": n_slots, "experts": L * E, "hit_rate": round(hits / max(1, hits + misses), 4),
+                      "copied_bytes_per_step": nbytes // max(1, args.steps),
+                      "host_to_device_GBps": round(nbytes / el / 1e9, 2), "us_per_layer": round(1e6 * el / args.steps / L, 3)},
+            "gpu_launches": 2 * L * args.steps, "clocks": sampler.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     import synthetic
@@ -491,6 +569,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, wl, world, rank)
+        elif args.path == "cached":
+            run_cached(args, wl, world, rank)
         else:
             run_ours(args, wl, world, rank, dist)
     finally:

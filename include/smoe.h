@@ -299,6 +299,53 @@ SMOE_API int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len);
  * Errors: SMOE_EINVAL. */
 SMOE_API int smoe_set_profile_events(smoe_ctx *ctx, void *const *events, int32_t n);
 
+/* ------------------------------------------------------- streaming slot pool */
+/* A cache of experts: the context's n_slots device slots hold a changing
+ * subset of all n_layers * E experts, whose packed blobs (pack_experts layout,
+ * one stride each) sit in host memory in [layer][expert] order; pinned host
+ * memory lets the copies run at the link's rate. The cache owns the context's
+ * slot table from creation on: entries of experts that are not resident are
+ * -1, so a moe_forward that names one sets SMOE_DEV_BAD_SLOT instead of
+ * reading another expert's weights. Results are bit-identical to a fully
+ * resident pool (they do not depend on slot placement). Use per layer:
+ * moe_route, read its ids to the host (which waits for the stream), then
+ * smoe_cache_prepare, then moe_forward on the same stream. The pages' slot
+ * pool fed from storage with an LFU + recency cache (xix.ai article, how it
+ * works; agentlenshq article, how expert streaming works). */
+typedef struct smoe_cache smoe_cache;
+
+/* host_store: host, >= n_layers * E * stride bytes; pool: device, the
+ * context's n_slots slots (>= n_slots * stride bytes), both caller-owned and
+ * outliving the cache. Clears the context's slot table (asynchronously on
+ * stream). Errors: SMOE_EINVAL, SMOE_ENOMEM, SMOE_ECUDA. */
+SMOE_API int smoe_cache_create(smoe_ctx *ctx, const void *host_store, uint64_t host_bytes, void *pool,
+                               uint64_t pool_bytes, void *stream, smoe_cache **out);
+SMOE_API int smoe_cache_destroy(smoe_cache *cache);
+
+/* Makes experts ids[0..n) (host memory, any order, repeats allowed) of `layer`
+ * resident. A miss takes a free slot, else evicts the resident expert used
+ * least often, ties to the one used least recently, never one named by this
+ * request; its blob is copied host -> device (one cudaMemcpyAsync per blob)
+ * and the changed slot-table rows are rewritten, all asynchronously on
+ * stream. The host mirror of the table is reused by the next call, so call
+ * again only after the stream has passed this call's copies (reading the next
+ * layer's ids to the host ensures it). hits/misses (nullable): this call's
+ * counts, one per entry of ids. Errors: SMOE_EINVAL (layer or an id out of
+ * range), SMOE_ENOMEM (more distinct experts than slots), SMOE_ECUDA. */
+SMOE_API int smoe_cache_prepare(smoe_cache *cache, int32_t layer, const int32_t *ids, int32_t n, void *stream,
+                                int32_t *hits, int32_t *misses);
+
+/* Totals since creation: entries found resident, entries copied in, bytes copied. */
+SMOE_API int smoe_cache_stats(const smoe_cache *cache, uint64_t *hits, uint64_t *misses, uint64_t *bytes_copied);
+
+/* The replacement policy alone, on the host (no device, no copies): runs
+ * n_requests records [layer, n, id_0 .. id_{n-1}] (concatenated in requests)
+ * through a fresh policy with n_slots slots and writes the slot of every
+ * requested id, in order, to out_slots; hits/misses totals (nullable).
+ * Errors: SMOE_EINVAL, SMOE_ENOMEM. */
+SMOE_API int smoe_cache_simulate(int32_t n_layers, int32_t E, int64_t n_slots, const int32_t *requests,
+                                 int32_t n_requests, int32_t *out_slots, int64_t *hits, int64_t *misses);
+
 /* Short English text for a status code (static storage). */
 SMOE_API const char *smoe_status_string(int status);
 

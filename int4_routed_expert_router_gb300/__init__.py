@@ -22,7 +22,8 @@ HOST, DEVICE = 0, 1
 EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destroy", "set_slot_table",
            "smoe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_noalloc", "moe_decode_stack",
            "smoe_stack_workspace_bytes", "smoe_check", "smoe_ctx_describe", "smoe_set_profile_events",
-           "smoe_status_string"]
+           "smoe_status_string", "smoe_cache_create", "smoe_cache_destroy", "smoe_cache_prepare",
+           "smoe_cache_stats", "smoe_cache_simulate"]
 
 
 class SmoeError(RuntimeError):
@@ -71,6 +72,11 @@ def lib():
         L.moe_forward_noalloc.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, u64, vp, vp, vp, vp, vp]
         L.moe_decode_stack.argtypes = [vp, i32, i32, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp, vp, vp, vp,
                                        vp, vp, u64, vp, u64, vp, vp]
+        L.smoe_cache_create.argtypes = [vp, vp, u64, vp, u64, vp, C.POINTER(vp)]
+        L.smoe_cache_destroy.argtypes = [vp]
+        L.smoe_cache_prepare.argtypes = [vp, i32, vp, i32, vp, C.POINTER(i32), C.POINTER(i32)]
+        L.smoe_cache_stats.argtypes = [vp, C.POINTER(u64), C.POINTER(u64), C.POINTER(u64)]
+        L.smoe_cache_simulate.argtypes = [i32, i32, i64, vp, i32, vp, C.POINTER(i64), C.POINTER(i64)]
         L.smoe_stack_workspace_bytes.argtypes = [vp, i32]
         L.smoe_stack_workspace_bytes.restype = u64
         L.smoe_check.argtypes = [vp, C.POINTER(C.c_int32), vp]
@@ -234,6 +240,62 @@ def moe_decode_stack(ctx: Context, first_layer: int, Wr, ws, shared_blobs, xs, i
                                   pool.numel() * pool.element_size(), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)),
            "moe_decode_stack")
+
+
+class Cache:
+    """Streaming slot pool (smoe_cache): the context's device slots as a cache
+    over every expert's packed blob in host memory. host_store: a host uint8
+    tensor [n_layers * E * stride] (pinned for full-rate copies); pool: the
+    context's device pool. Both must outlive the cache."""
+
+    def __init__(self, ctx: Context, host_store, pool, stream=None):
+        self.ctx, self.host_store, self.pool = ctx, host_store, pool
+        h = C.c_void_p()
+        _check(lib().smoe_cache_create(ctx.handle, C.c_void_p(host_store.data_ptr()),
+                                       host_store.numel() * host_store.element_size(), _ptr(pool),
+                                       pool.numel() * pool.element_size(), _stream(stream), C.byref(h)),
+               "smoe_cache_create")
+        self.handle = h.value
+
+    def prepare(self, layer: int, ids: np.ndarray, stream=None) -> tuple[int, int]:
+        """Makes the experts in ids (host int array) of `layer` resident; returns (hits, misses)."""
+        a = np.ascontiguousarray(ids, np.int32).ravel()
+        hits, misses = C.c_int32(0), C.c_int32(0)
+        _check(lib().smoe_cache_prepare(self.handle, int(layer), a.ctypes.data, a.size, _stream(stream),
+                                        C.byref(hits), C.byref(misses)), "smoe_cache_prepare")
+        return int(hits.value), int(misses.value)
+
+    def stats(self) -> tuple[int, int, int]:
+        """(hits, misses, bytes copied) since creation."""
+        h, m, b = C.c_uint64(0), C.c_uint64(0), C.c_uint64(0)
+        _check(lib().smoe_cache_stats(self.handle, C.byref(h), C.byref(m), C.byref(b)), "smoe_cache_stats")
+        return int(h.value), int(m.value), int(b.value)
+
+    def close(self):
+        if self.handle:
+            lib().smoe_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def cache_simulate(n_layers: int, E: int, n_slots: int, requests) -> tuple[np.ndarray, int, int]:
+    """The replacement policy alone on the host. requests: list of (layer, ids).
+    Returns (slot of every requested id in order, hits, misses)."""
+    flat = []
+    for layer, ids in requests:
+        ids = list(map(int, ids))
+        flat += [int(layer), len(ids)] + ids
+    req = np.asarray(flat, np.int32)
+    out = np.zeros(sum(len(ids) for _, ids in requests), np.int32)
+    h, m = C.c_int64(0), C.c_int64(0)
+    _check(lib().smoe_cache_simulate(int(n_layers), int(E), int(n_slots), req.ctypes.data, len(requests),
+                                     out.ctypes.data, C.byref(h), C.byref(m)), "smoe_cache_simulate")
+    return out, int(h.value), int(m.value)
 
 
 def check(err, stream=None) -> int:
