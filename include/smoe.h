@@ -299,6 +299,17 @@ SMOE_API int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len);
  * Errors: SMOE_EINVAL. */
 SMOE_API int smoe_set_profile_events(smoe_ctx *ctx, void *const *events, int32_t n);
 
+/* The same layer as moe_forward, computed plainly for checking the fast
+ * kernels on the device: one CTA per token, each weight decoded on its own
+ * from the blob (s * q + b in fp32), fp32 dot products, the routed experts in
+ * route order then the shared expert, one bf16 rounding. Slow (about a
+ * millisecond per token at H = 2048); no workspace. Arguments and errors as
+ * for moe_forward (bad ids and slots set the error word and are skipped). */
+SMOE_API int moe_forward_debug(const smoe_ctx *ctx, int32_t layer, const uint16_t *x, int32_t T,
+                               const int32_t *ids, const float *w, const float *gate, const void *pool,
+                               uint64_t pool_bytes, const void *shared_blob, const uint16_t *residual,
+                               uint16_t *out, int32_t *err, void *stream);
+
 /* ------------------------------------------------------- streaming slot pool */
 /* A cache of experts: the context's n_slots device slots hold a changing
  * subset of all n_layers * E experts, whose packed blobs (pack_experts layout,

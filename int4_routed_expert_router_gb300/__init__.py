@@ -23,7 +23,7 @@ EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destro
            "smoe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_noalloc", "moe_decode_stack",
            "smoe_stack_workspace_bytes", "smoe_check", "smoe_ctx_describe", "smoe_set_profile_events",
            "smoe_status_string", "smoe_cache_create", "smoe_cache_destroy", "smoe_cache_prepare",
-           "smoe_cache_stats", "smoe_cache_simulate"]
+           "smoe_cache_stats", "smoe_cache_simulate", "moe_forward_debug"]
 
 
 class SmoeError(RuntimeError):
@@ -72,6 +72,7 @@ def lib():
         L.moe_forward_noalloc.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, u64, vp, vp, vp, vp, vp]
         L.moe_decode_stack.argtypes = [vp, i32, i32, C.POINTER(vp), C.POINTER(vp), C.POINTER(vp), vp, vp, vp, vp,
                                        vp, vp, u64, vp, u64, vp, vp]
+        L.moe_forward_debug.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp, u64, vp, vp, vp, vp, vp]
         L.smoe_cache_create.argtypes = [vp, vp, u64, vp, u64, vp, C.POINTER(vp)]
         L.smoe_cache_destroy.argtypes = [vp]
         L.smoe_cache_prepare.argtypes = [vp, i32, vp, i32, vp, C.POINTER(i32), C.POINTER(i32)]
@@ -216,6 +217,15 @@ def moe_forward(ctx: Context, layer: int, x, ids, w, gate, pool, shared_blob, ou
                              pool.numel() * pool.element_size(), _ptr(shared_blob), _ptr(residual), _ptr(out),
                              _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
                              _stream(stream)), "moe_forward")
+
+
+def moe_forward_debug(ctx: Context, layer: int, x, ids, w, gate, pool, shared_blob, out, err, residual=None,
+                      stream=None):
+    """The plain per-token CUDA path (for checking the fast kernels)."""
+    T = x.shape[0]
+    _check(lib().moe_forward_debug(ctx.handle, int(layer), _ptr(x), T, _ptr(ids), _ptr(w), _ptr(gate), _ptr(pool),
+                                   pool.numel() * pool.element_size(), _ptr(shared_blob), _ptr(residual), _ptr(out),
+                                   _ptr(err), _stream(stream)), "moe_forward_debug")
 
 
 def moe_forward_noalloc(ctx: Context, layer: int, x, ids, w, gate, pool, shared_blob, out, err,

@@ -1,0 +1,76 @@
+"""GPU: the plain per-token CUDA path (moe_forward_debug) against the oracle,
+and the fast kernels (the decode kernel for T <= 8, the bucketed tensor-core
+path above) against it, each within the layer tolerance; bad slots set the
+error word."""
+import numpy as np
+import pytest
+import torch
+
+import int4_routed_expert_router_gb300 as smoe
+import synthetic
+import workload as W
+from test_gpu_parity import assert_output_close, gpu_forward, oracle_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from int4_routed_expert_router_gb300 import _build
+    from synthetic import _build as sb
+    _build.build()
+    sb.build()
+
+
+def debug_forward(pool, layer, x_bits, ids, w, gate, residual=False):
+    wl = pool.wl
+    T = x_bits.shape[0]
+    x = W.bf16_tensor(x_bits)
+    out = torch.zeros((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    smoe.moe_forward_debug(pool.ctx, layer, x, torch.from_numpy(np.ascontiguousarray(ids, np.int32)).cuda(),
+                           torch.from_numpy(np.ascontiguousarray(w, np.float32)).cuda(),
+                           torch.from_numpy(np.ascontiguousarray(gate, np.float32)).cuda(), pool.pool,
+                           pool.shared[layer], out, err, residual=x if residual else None)
+    code = smoe.check(err)
+    return W.bits_of(out), code
+
+
+@pytest.mark.parametrize("name,Ts", [("tiny", (1, 4, 20)), ("decode35b", (2, 16))])
+def test_debug_path_matches_oracle_and_fast_kernels(name, Ts):
+    wl = synthetic.WORKLOADS[name]
+    pool, inp = W.DevicePool(wl, n_layers=1), W.LayerInputs(wl, 1)
+    for T in Ts:
+        x = synthetic.activations(wl.seed, T, wl.H, tag=900 + T)
+        ref = oracle_layer(wl, 0, x, inp)
+        dbg, code = debug_forward(pool, 0, x, ref["ids"], ref["w"], ref["gate"])
+        assert code == 0
+        assert_output_close(dbg, ref["out64"])
+        fast = gpu_forward(pool, 0, x, ref["ids"], ref["w"], ref["gate"])
+        assert_output_close(fast, ref["out64"])
+        # fast against debug: two approximations of the oracle, so twice the layer bounds
+        f = synthetic.bf16_bits_to_f32(fast).astype(np.float64)
+        d = synthetic.bf16_bits_to_f32(dbg).astype(np.float64)
+        rms = np.sqrt(np.mean(ref["out64"] ** 2))
+        assert np.linalg.norm(f - d) <= 2 * 5e-3 * np.linalg.norm(ref["out64"])
+        assert np.abs(f - d).max() <= 2 * 2e-2 * rms
+        dres, _ = debug_forward(pool, 0, x, ref["ids"], ref["w"], ref["gate"], residual=True)
+        xr = synthetic.bf16_bits_to_f32(x).astype(np.float64)
+        assert_output_close(dres, xr + ref["out64"])
+
+
+def test_debug_path_bad_slot_sets_error_word():
+    wl = synthetic.WORKLOADS["tiny"]
+    pool, inp = W.DevicePool(wl), W.LayerInputs(wl, 1)
+    x = synthetic.activations(wl.seed, 2, wl.H, tag=950)
+    ref = oracle_layer(wl, 0, x, inp)
+    e = int(ref["ids"][0, 0])
+    saved = pool.table_dev[0, e].item()
+    try:
+        pool.table_dev[0, e] = -1
+        out, code = debug_forward(pool, 0, x, ref["ids"], ref["w"], ref["gate"])
+        assert code == smoe.DEV_BAD_SLOT
+        assert np.isfinite(synthetic.bf16_bits_to_f32(out)).all()
+    finally:
+        pool.table_dev[0, e] = saved
+        torch.cuda.synchronize()
