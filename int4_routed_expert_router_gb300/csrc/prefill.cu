@@ -187,16 +187,16 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // ---------------------------------------------------------------- bucketing
-// counts and chunk_base are [E][chunks] (chunks of kBucketTok tokens): the
+// counts and chunk_base are [E][chunks] (chunks of bucket_tok(T) tokens): the
 // scan's warps (one per expert) read and write an expert's row coalesced.
 
 __global__ void __launch_bounds__(256) bucket_count_kernel(const PrefillParams p)
 {
     __shared__ int cnt[1024];
-    const int c = blockIdx.x, nch = gridDim.x;
+    const int c = blockIdx.x, nch = gridDim.x, ct = bucket_tok(p.T);
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
-    const int t0 = c * kBucketTok, t1 = min(p.T, t0 + kBucketTok);
+    const int t0 = c * ct, t1 = min(p.T, t0 + ct);
     for (int q = t0 * p.k + threadIdx.x; q < t1 * p.k; q += blockDim.x) {
         const int e = p.ids[q];
         if (e >= 0 && e < p.E) atomicAdd(&cnt[e], 1);
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
     __shared__ int tbuf[1024];
     __shared__ int last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nch = (p.T + kBucketTok - 1) / kBucketTok;
+    const int nch = (p.T + bucket_tok(p.T) - 1) / bucket_tok(p.T);
     const int ew = blockIdx.x * 32 + warp;
     if (ew < p.E) {
         const int *row = p.counts + size_t(ew) * nch;
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(32) bucket_scatter_kernel(const PrefillParams 
     __shared__ int ids_s[kBucketTok * 16];
     const int c = blockIdx.x, nch = gridDim.x, lane = threadIdx.x;
     for (int e = lane; e < p.E; e += 32) base[e] = p.offsets[e] + p.chunk_base[size_t(e) * nch + c];
-    const int t0 = c * kBucketTok, t1 = min(p.T, t0 + kBucketTok);
+    const int ct = bucket_tok(p.T), t0 = c * ct, t1 = min(p.T, t0 + ct);
     for (int q = t0 * p.k + lane; q < t1 * p.k; q += 32) ids_s[q - t0 * p.k] = p.ids[q];
     __syncwarp();
     for (int t = t0; t < t1; ++t) {
@@ -1080,7 +1080,7 @@ cudaError_t launch_router_gemm(const RouteParams &r, cudaStream_t st)
 cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStream_t st, const cudaEvent_t *prof,
                            int nprof)
 {
-    const int nch = (p.T + kBucketTok - 1) / kBucketTok;
+    const int nch = (p.T + bucket_tok(p.T) - 1) / bucket_tok(p.T);
     CUtensorMap xmap, hmap;
     cudaError_t e = rows_map(&xmap, g0.x, false, uint64_t(p.H), uint64_t(p.T));   // unused: gate/up gathers B itself
     if (e != cudaSuccess) return e;

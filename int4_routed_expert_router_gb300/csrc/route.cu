@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const RouteParams p)
     // [router rows 8 x H | tokens 8 x H], later the logits for the top-k; barriers last
     uint16_t *wrow = reinterpret_cast<uint16_t *>(smem);                 // [8][H]
     uint16_t *xs = wrow + kRouteRows * H;                                 // [8][H]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + route_region_bytes(H, E, T));   // [2]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + route_region_bytes(H, E, p.fused_topk ? T : 0));   // [2]
     __shared__ int last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int row0 = blockIdx.x * kRouteRows, tok0 = blockIdx.y * kRouteToks;
@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(256) topk_kernel(const RouteParams p)
     if (t >= p.T) return;
     token_topk_any((p.E + 31) / 32, p.logits + size_t(t) * (p.E + 1), p.bias, p.E, p.k, ckey + warp * 16,
                    cid + warp * 16, lane, cand_k + warp * 64, cand_i + warp * 64);
-    const float zs = router_dot(p.ws, p.x + size_t(t) * p.H, p.H, lane);
+    const float zs = p.gate_in_logits ? __ldcg(p.logits + size_t(t) * (p.E + 1) + p.E)
+                                      : router_dot(p.ws, p.x + size_t(t) * p.H, p.H, lane);
     __syncwarp();
     write_choice(p, t, ckey + warp * 16, cid + warp * 16, zs, lane);
 }
@@ -170,14 +171,18 @@ cudaError_t route_config()
 cudaError_t launch_route(const RouteParams &p0, cudaStream_t st)
 {
     RouteParams p = p0;
-    if (p.T > kDecodeMaxT) {       // logits on tensor cores, then one warp per token
+    if (p.T > kRouteGemvMaxT) {    // logits on tensor cores, then one warp per token
         cudaError_t e = launch_router_gemm(p, st);
         if (e != cudaSuccess) return e;
         topk_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(p);
         return cudaGetLastError();
     }
-    p.fused_topk = 1;
-    const int smem = route_region_bytes(p.H, p.E, p.T) + 16;
+    // small T: the GEMV kernel over (row block, token block) CTAs; above kDecodeMaxT
+    // it stops at the logits (row E: the shared-gate logit) and one warp per token
+    // takes the top-k
+    p.fused_topk = p.T <= kDecodeMaxT ? 1 : 0;
+    p.gate_in_logits = 1;
+    const int smem = route_region_bytes(p.H, p.E, p.fused_topk ? p.T : 0) + 16;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((p.E + 1 + kRouteRows - 1) / kRouteRows, (p.T + kRouteToks - 1) / kRouteToks);
     lc.blockDim = dim3(256);
@@ -188,7 +193,10 @@ cudaError_t launch_route(const RouteParams &p0, cudaStream_t st)
     at[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = at;
     lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, route_logits_kernel, p);
+    cudaError_t e = cudaLaunchKernelEx(&lc, route_logits_kernel, p);
+    if (e != cudaSuccess || p.fused_topk) return e;
+    topk_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace smoe

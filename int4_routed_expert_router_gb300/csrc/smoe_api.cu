@@ -138,7 +138,7 @@ Workspace workspace_layout(const smoe_shape &s, int T)
         const uint64_t umax = uint64_t(s.E < T * s.k ? s.E : T * s.k) + 1;
         w.ypair = o;     o = al(o + umax * T * s.H * 4);
     } else {
-        const uint64_t P = uint64_t(T) * s.k, nch = (uint64_t(T) + kBucketTok - 1) / kBucketTok;
+        const uint64_t P = uint64_t(T) * s.k, nch = (uint64_t(T) + bucket_tok(T) - 1) / bucket_tok(T);
         w.counts = o;     o = al(o + nch * s.E * 4);
         w.chunk_base = o; o = al(o + nch * s.E * 4);
         w.offsets = o;    o = al(o + (uint64_t(s.E) + 1) * 4);

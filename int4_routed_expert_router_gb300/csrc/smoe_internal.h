@@ -15,7 +15,11 @@ constexpr int kAtomBytes = 576;     // nibbles + 16 (s, b) fp16 pairs
 
 // Decode kernel (fused experts, T <= kDecodeMaxT).
 constexpr int kDecodeMaxT = 8;
-constexpr int kBucketTok = 32;     // tokens per bucketing chunk (T > kDecodeMaxT path)
+constexpr int kBucketTok = 32;     // most tokens per bucketing chunk (T > kDecodeMaxT path)
+// tokens per bucketing chunk for T tokens: small chunks (more warps in the
+// ordered scatter) when T is small
+inline __host__ __device__ int bucket_tok(int T) { return T <= 1024 ? 8 : kBucketTok; }
+constexpr int kRouteGemvMaxT = 512; // T > kDecodeMaxT up to this: logits by the GEMV kernel, else tcgen05
 constexpr int kSlice = 32;                        // intermediates per CTA
 constexpr int kChunkCols = 256;                   // H columns per streamed chunk
 constexpr int kRowBlocksA = kSlice / 8;           // gate/up row blocks per CTA
@@ -109,6 +113,7 @@ struct RouteParams {
     int32_t *err;
     int T, H, E, k;
     int fused_topk;
+    int gate_in_logits;     // logits[t][E] holds the shared-gate logit (GEMV path)
 };
 
 struct DecodeParams {
