@@ -192,6 +192,8 @@ __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + _
 
 __global__ void __launch_bounds__(256) bucket_count_kernel(const PrefillParams p)
 {
+    pdl_wait();                                   // the predecessor's writes are visible
+    pdl_trigger();
     __shared__ int cnt[1024];
     const int c = blockIdx.x, nch = gridDim.x, ct = bucket_tok(p.T);
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) cnt[e] = 0;
@@ -213,6 +215,8 @@ __global__ void __launch_bounds__(256) bucket_count_kernel(const PrefillParams p
 // most kXMaxN pairs of near-equal size; then the shared expert's runs over T.
 __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p)
 {
+    pdl_wait();                                   // the predecessor's writes are visible
+    pdl_trigger();
     __shared__ int buf[1024];
     __shared__ int tbuf[1024];
     __shared__ int last;
@@ -293,6 +297,8 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
 // memory first so the ordered loop only touches shared memory.
 __global__ void __launch_bounds__(32) bucket_scatter_kernel(const PrefillParams p)
 {
+    pdl_wait();                                   // the predecessor's writes are visible
+    pdl_trigger();
     __shared__ int base[1024];
     __shared__ int ids_s[kBucketTok * 16];
     const int c = blockIdx.x, nch = gridDim.x, lane = threadIdx.x;
@@ -327,6 +333,8 @@ __global__ void __launch_bounds__(32) bucket_scatter_kernel(const PrefillParams 
 // 2^-14, an absolute error under 3e-8); larger values set the error word.
 __global__ void __launch_bounds__(256) convert_x_kernel(const GemmParams g)
 {
+    pdl_wait();                                   // the predecessor's writes are visible
+    pdl_trigger();
     const int tok = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (tok >= g.T) return;
     const uint4 *src = reinterpret_cast<const uint4 *>(g.x_bf16 + size_t(tok) * g.H);
@@ -468,6 +476,8 @@ __device__ __forceinline__ void tma_raw(uint32_t dst, const CUtensorMap *map, in
 __global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmParams p,
                                                                     const __grid_constant__ CUtensorMap bmap)
 {
+    pdl_wait();                                   // the predecessor's writes are visible
+    pdl_trigger();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ab = smem;                                           // kPfAB x (A 16 KiB | B 32 KiB)
@@ -709,6 +719,8 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                                                                     const __grid_constant__ CUtensorMap amap,
                                                                     const __grid_constant__ CUtensorMap amap_shared)
 {
+    pdl_wait();                                   // the predecessor's writes are visible
+    pdl_trigger();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *bst = smem;                                          // kXStg x 24 KiB, 128-byte swizzled rows
@@ -956,6 +968,8 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
 // (+ residual), from the fp16 expert outputs, in fp32.
 __global__ void __launch_bounds__(256) combine_kernel(const PrefillParams p)
 {
+    pdl_wait();                                   // the predecessor's writes are visible
+    pdl_trigger();
     const int t = blockIdx.y;
     const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (c >= p.H) return;
@@ -1073,8 +1087,8 @@ cudaError_t launch_router_gemm(const RouteParams &r, cudaStream_t st)
     cudaError_t e = rows_map(&xmap, r.x, true, uint64_t(r.H), uint64_t(r.T));
     if (e != cudaSuccess) return e;
     const int ntile = (r.T + kPfMaxN - 1) / kPfMaxN;
-    router_gemm_kernel<<<persistent_grid(ntile * g.m_tiles), kPfThreads, kPfSmem, st>>>(g, xmap);
-    return cudaGetLastError();
+    return launch_pdl(router_gemm_kernel, dim3(persistent_grid(ntile * g.m_tiles)), dim3(kPfThreads), kPfSmem, st, g,
+                      xmap);
 }
 
 cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStream_t st, const cudaEvent_t *prof,
@@ -1093,23 +1107,26 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
     if ((e = atoms_map(&gu_shared, g0.shared_blob, p.H / kGroup, g0.I / 8, 1, g0.stride)) != cudaSuccess) return e;
     if ((e = atoms_map(&dn_pool, pool_down, g0.I / kGroup, p.H / 16, g0.n_slots, g0.stride)) != cudaSuccess) return e;
     if ((e = atoms_map(&dn_shared, shared_down, g0.I / kGroup, p.H / 16, 1, g0.stride)) != cudaSuccess) return e;
-    bucket_count_kernel<<<nch, 256, 0, st>>>(p);
-    bucket_scan_kernel<<<(p.E + 31) / 32, 1024, 0, st>>>(p);
-    bucket_scatter_kernel<<<nch, 32, 0, st>>>(p);
-    convert_x_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(g0);
+    if ((e = launch_pdl(bucket_count_kernel, dim3(nch), dim3(256), 0, st, p)) != cudaSuccess) return e;
+    if ((e = launch_pdl(bucket_scan_kernel, dim3((p.E + 31) / 32), dim3(1024), 0, st, p)) != cudaSuccess) return e;
+    if ((e = launch_pdl(bucket_scatter_kernel, dim3(nch), dim3(32), 0, st, p)) != cudaSuccess) return e;
+    if ((e = launch_pdl(convert_x_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, g0)) != cudaSuccess) return e;
     const int maxt = prefill_max_tiles(p.T, p.k, p.E);
     GemmParams g = g0;
     g.mode = 0;
     g.m_tiles = g.I / 64;
     if ((e = prof_record(nprof > 0 ? prof[0] : nullptr, st)) != cudaSuccess) return e;
-    expert_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kXThreads, kXSmem, st>>>(g, xmap, gu_pool, gu_shared);
+    if ((e = launch_pdl(expert_gemm_kernel, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), kXSmem, st, g, xmap,
+                        gu_pool, gu_shared)) != cudaSuccess)
+        return e;
     if ((e = prof_record(nprof > 1 ? prof[1] : nullptr, st)) != cudaSuccess) return e;
     g.mode = 1;
     g.m_tiles = p.H / kPfM;
-    expert_gemm_kernel<<<persistent_grid(maxt * g.m_tiles), kXThreads, kXSmem, st>>>(g, hmap, dn_pool, dn_shared);
+    if ((e = launch_pdl(expert_gemm_kernel, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), kXSmem, st, g, hmap,
+                        dn_pool, dn_shared)) != cudaSuccess)
+        return e;
     if ((e = prof_record(nprof > 2 ? prof[2] : nullptr, st)) != cudaSuccess) return e;
-    combine_kernel<<<dim3((p.H / 4 + 255) / 256, p.T), 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3((p.H / 4 + 255) / 256, p.T), dim3(256), 0, st, p);
 }
 
 }  // namespace smoe

@@ -174,8 +174,7 @@ cudaError_t launch_route(const RouteParams &p0, cudaStream_t st)
     if (p.T > kRouteGemvMaxT) {    // logits on tensor cores, then one warp per token
         cudaError_t e = launch_router_gemm(p, st);
         if (e != cudaSuccess) return e;
-        topk_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(topk_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, p);
     }
     // small T: the GEMV kernel over (row block, token block) CTAs; above kDecodeMaxT
     // it stops at the logits (row E: the shared-gate logit) and one warp per token
@@ -195,8 +194,7 @@ cudaError_t launch_route(const RouteParams &p0, cudaStream_t st)
     lc.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&lc, route_logits_kernel, p);
     if (e != cudaSuccess || p.fused_topk) return e;
-    topk_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, p);
 }
 
 }  // namespace smoe

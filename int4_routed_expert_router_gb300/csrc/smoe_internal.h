@@ -185,6 +185,26 @@ struct GemmParams {
     int m_tiles;
 };
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while its predecessor in the stream finishes; it calls pdl_wait (griddepcontrol.wait)
+// before touching global memory, so it still sees all of the predecessor's work.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args)
+{
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kern, static_cast<Args &&>(args)...);
+}
+
 // workspace carving (all offsets 256-byte aligned)
 struct Workspace {
     uint64_t route_counter, logits, fwd_counters, ypair, total;
