@@ -43,7 +43,7 @@ constexpr int kPfBoxRows = 64;     // B rows per TMA box
 constexpr int kPfWorkers = 8;      // warps: A (dequantisation, or router rows)
 constexpr int kPfEpi = 8;          // warps: epilogue (two per TMEM lane quadrant)
 constexpr int kPfRawWarp = kPfWorkers + kPfEpi;   // bulk copies of the raw atoms
-constexpr int kPfBWarp = kPfRawWarp + 1;          // TMA row gathers of B
+constexpr int kPfBWarp = kPfRawWarp + 1;          // B by TMA boxes (router tokens; the down GEMM's h rows)
 constexpr int kPfMma = kPfBWarp + 1;              // tcgen05.mma issuer
 constexpr int kPfThreads = (kPfMma + 1) * 32;
 constexpr int kPfRawBytes = 8 * kAtomBytes;         // 4608: 8 row blocks x one group
@@ -712,8 +712,12 @@ __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uin
 // the same K steps) for mode 0 (gate/up, K = H) and mode 1 (down, K = I), but
 // the eight dequantising warps write A straight into tensor memory
 // (tcgen05.st) and the MMAs read it there, so shared memory carries only the
-// raw atoms and B. Worker warp w writes atom a = 2 (w % 4) + w / 4 (rows
-// 16 a .. 16 a + 15, inside the lane quadrant w % 4 that the warp may access).
+// raw atoms and B. Roles: warps 0-7 dequantise (warp w writes atom a = 2 (w % 4)
+// + w / 4, rows 16 a .. 16 a + 15, inside the lane quadrant w % 4 that the warp
+// may access); warps 8-15 run the epilogue; warp 16 streams the raw atoms;
+// warp 17 loads B with TMA in the down GEMM; warp 18 issues the MMAs; warps
+// 19-22 gather B rows by token in the gate/up GEMM and join the epilogue in
+// the down GEMM. A and B of a K step share one stage of a 4-deep ring.
 __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmParams p,
                                                                     const __grid_constant__ CUtensorMap bmap,
                                                                     const __grid_constant__ CUtensorMap amap,

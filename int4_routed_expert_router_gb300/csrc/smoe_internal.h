@@ -139,7 +139,7 @@ struct PfTile {
     int32_t kind;     // 0: run of an expert's pairs; 1: run of tokens for the shared expert
     int32_t slot;     // pool slot of the expert (kind 0; -1 if the slot table entry is out of range), else 0
     int32_t p0;       // first pair (kind 0) or first token (kind 1)
-    int32_t n;        // rows in the run (<= 256)
+    int32_t n;        // rows in the run (1 .. 192)
 };
 
 // Token-bucketed path (T > 8): bucketing and combine.
