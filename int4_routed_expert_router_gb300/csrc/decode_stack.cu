@@ -53,7 +53,7 @@ __host__ __device__ inline StkSmem stk_smem(int H, int E, int I, int U, int nr, 
     L.hl = o;    o = align128(o + U * (I + 8) * 2);
     L.hsum = o;  o = align128(o + U * (I / kGroup) * kDecodeMaxT * 4);
     L.yp = o;    o = align128(o + U * 2 * 16 * 4);
-    L.red = o;   o = align128(o + kStkWarps * 32 * 16);
+    L.red = o;   o = align128(o + nu * kStkWarps * 8 * 8);
     L.cand = o;  o = align128(o + (2 * E + 2 * 16 + 2 * 16) * 4);
     L.ints = o;  o = align128(o + 64 * 4);
     L.bars = o;  o = align128(o + (nu + U + 3) * 8);
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
     uint16_t *hl = reinterpret_cast<uint16_t *>(smem + L.hl);
     float *hsum = reinterpret_cast<float *>(smem + L.hsum);
     float *yp = reinterpret_cast<float *>(smem + L.yp);
-    float4 *red = reinterpret_cast<float4 *>(smem + L.red);
+    float2 *red = reinterpret_cast<float2 *>(smem + L.red);     // [nu][warps][8] gate/up partial sums
     uint32_t *cand_k = reinterpret_cast<uint32_t *>(smem + L.cand);   // [E] candidates
     int32_t *cand_i = reinterpret_cast<int32_t *>(cand_k + E);
     uint32_t *mx_k = reinterpret_cast<uint32_t *>(cand_i + E);        // [16] slice maxima
@@ -329,10 +329,16 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
             }
         }
 
-        // ---- 4. gate/up units -> h
+        // ---- 4. gate/up units -> h. Each warp takes atoms kb = warp, warp + 16, ...
+        // of the CTA's units one after another, with no CTA barrier between units.
+        // The token is MMA column 0, so lanes 4 g (t4 = 0) hold the partial sums of
+        // rows g (gate) and g + 8 (up); they go to red[unit][warp][g]. After one
+        // barrier warp i reduces unit i over the warps in order.
+        int n_mine = 0;                                             // this CTA's units (uniform)
         for (int i = 0; i < p.nu; ++i) {
-            const int q = c + i * G, u = q / nrb, rb = q % nrb;
+            const int q = c + i * G, u = q / nrb;
             if (u >= U) break;                                      // uniform
+            ++n_mine;
             const bool valid = blob_of(u) != nullptr;               // uniform
             if (!bad && !mbar_wait(&ubar[i], par, p.err)) bad = true;
             float aG = 0.f, aU = 0.f;
@@ -365,34 +371,38 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                     aU += fmaf(su, acc[2] + acc2[2], bpu * xsum[kb]);
                 }
             }
-            red[warp * 32 + lane] = make_float4(aG, aU, 0.f, 0.f);
-            __syncthreads();
-            if (warp == 0) {
-#pragma unroll
-                for (int w = 1; w < kStkWarps; ++w) {
-                    const float4 v = red[w * 32 + lane];
-                    aG += v.x;
-                    aU += v.y;
-                }
-                // rows g (gate) and g + 8 (up) of the block are intermediate 8 rb + g; token =
-                // column 0. h goes out as bf16 hi and lo = bf16(h - hi), with the unit's
-                // sum of hi + lo over its 8 intermediates (the down rows' bias term)
-                const float hv = (valid && !bad) ? silu(aG) * aU : 0.f;
-                const uint16_t hi = f32_to_bf16_bits(hv);
-                const uint16_t lo = f32_to_bf16_bits(hv - __uint_as_float(uint32_t(hi) << 16));
-                float sum = __uint_as_float(uint32_t(hi) << 16) + __uint_as_float(uint32_t(lo) << 16);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-                uint16_t *hrow = p.h + (size_t(l) * 2 * U + u) * I;
-                if (t4 == 0) {
-                    __stcg(hrow + 8 * rb + g, hi);
-                    __stcg(hrow + size_t(U) * I + 8 * rb + g, lo);
-                }
-                if (lane == 0) __stcg(p.hps + (size_t(l) * U + u) * nrb + rb, sum);
-            }
-            __syncthreads();
+            if (t4 == 0) red[(i * kStkWarps + warp) * 8 + g] = make_float2(aG, aU);
         }
+        __syncthreads();
+        if (warp < n_mine) {
+            const int i = warp, q = c + i * G, u = q / nrb, rb = q % nrb;
+            const bool valid = blob_of(u) != nullptr;
+            const float2 *ri = red + i * kStkWarps * 8 + g;
+            float aG = ri[0].x, aU = ri[0].y;
+#pragma unroll
+            for (int w = 1; w < kStkWarps; ++w) {
+                const float2 v = ri[w * 8];
+                aG += v.x;
+                aU += v.y;
+            }
+            // intermediate 8 rb + g (the four lanes of a g hold the same sums). h goes
+            // out as bf16 hi and lo = bf16(h - hi), with the unit's sum of hi + lo over
+            // its 8 intermediates (the down rows' bias term)
+            const float hv = (valid && !bad) ? silu(aG) * aU : 0.f;
+            const uint16_t hi = f32_to_bf16_bits(hv);
+            const uint16_t lo = f32_to_bf16_bits(hv - __uint_as_float(uint32_t(hi) << 16));
+            float sum = __uint_as_float(uint32_t(hi) << 16) + __uint_as_float(uint32_t(lo) << 16);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+            uint16_t *hrow = p.h + (size_t(l) * 2 * U + u) * I;
+            if (t4 == 0) {
+                __stcg(hrow + 8 * rb + g, hi);
+                __stcg(hrow + size_t(U) * I + 8 * rb + g, lo);
+            }
+            if (lane == 0) __stcg(p.hps + (size_t(l) * U + u) * nrb + rb, sum);
+        }
+        __syncthreads();
         if (tid == 0) ticket_add(&cnt[1], 1u);
 
         // ---- 5. down rows of every expert for rows 16 c .. 16 c + 15, combine
@@ -471,7 +481,7 @@ cudaError_t stack_config(smoe_ctx *ctx)
     c.nr = (s.E + 1 + c.grid - 1) / c.grid;
     c.nu = (c.U * (s.I / 8) + c.grid - 1) / c.grid;
     c.smem = stk_smem(s.H, s.E, s.I, c.U, c.nr, c.nu).total;
-    c.ok = coop && c.grid >= s.H / 16 && s.E % 4 == 0 && c.smem <= max_smem;
+    c.ok = coop && c.grid >= s.H / 16 && s.E % 4 == 0 && c.nu <= kStkWarps && c.smem <= max_smem;
     if (!c.ok) return cudaSuccess;
     e = cudaFuncSetAttribute(decode_stack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, c.smem);
     if (e != cudaSuccess) return e;
