@@ -32,8 +32,6 @@ def tiny():
     return W.DevicePool(wl), W.LayerInputs(wl, 1)
 
 
-
-
 @pytest.mark.parametrize("T", [9, 64, 200, 600])
 def test_prefill_tiny_against_oracle(tiny, T):
     pool, inp = tiny
@@ -162,3 +160,25 @@ def test_token_limit_is_rejected_before_any_work(tiny):
     assert st == smoe.EINVAL
     torch.cuda.synchronize()
     assert smoe.check(err) == 0
+
+
+@pytest.mark.parametrize("name,lengths", [("tiny", (37, 9, 120, 300, 12)), ("decode35b", (9, 64, 200, 31))])
+def test_mixed_length_batch_equals_each_request(name, lengths):
+    """Requests of different lengths concatenated into one call: every token's
+    output is bit-identical to its own request's call (the same routing; all
+    calls on the token-bucketed path, T > 8). A token's rows meet the same
+    weights in the same K order whatever other tokens share its tiles."""
+    wl = synthetic.WORKLOADS[name]
+    pool, inp = W.DevicePool(wl, n_layers=1), W.LayerInputs(wl, 1)
+    xs = [synthetic.activations(wl.seed, T, wl.H, tag=7000 + i) for i, T in enumerate(lengths)]
+    x = np.concatenate(xs, 0)
+    ids, w, gate = gpu_route(pool, inp, 0, x)
+    full = gpu_forward(pool, 0, x, ids, w, gate)
+    o = 0
+    for T, xr in zip(lengths, xs):
+        part = gpu_forward(pool, 0, xr, ids[o:o + T], w[o:o + T], gate[o:o + T])
+        assert np.array_equal(part, full[o:o + T]), (T, o)
+        o += T
+    if name == "tiny":                                   # the whole batch against the oracle
+        ref = oracle_layer(wl, 0, x, inp)
+        assert_output_close(gpu_forward(pool, 0, x, ref["ids"], ref["w"], ref["gate"]), ref["out64"])
