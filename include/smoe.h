@@ -336,9 +336,10 @@ SMOE_API int smoe_cache_destroy(smoe_cache *cache);
 /* Makes experts ids[0..n) (host memory, any order, repeats allowed) of `layer`
  * resident. A miss takes a free slot, else evicts the resident expert used
  * least often, ties to the one used least recently, never one named by this
- * request; its blob is copied host -> device (one cudaMemcpyAsync per blob)
- * and the changed slot-table rows are rewritten, all asynchronously on
- * stream. The host mirror of the table is reused by the next call, so call
+ * request; its blob is copied host -> device (one cudaMemcpyAsync per blob,
+ * on up to four internal streams that start after the work already queued on
+ * stream and that stream waits for) and the changed slot-table rows are
+ * rewritten, all asynchronously with respect to the host. The host mirror of the table is reused by the next call, so call
  * again only after the stream has passed this call's copies (reading the next
  * layer's ids to the host ensures it). hits/misses (nullable): this call's
  * counts, one per entry of ids. Errors: SMOE_EINVAL (layer or an id out of

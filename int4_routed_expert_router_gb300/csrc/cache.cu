@@ -3,8 +3,10 @@
 // frequency-and-recency replacement: the xix.ai article, paragraphs on how it
 // works; the agentlenshq article, how expert streaming works). Host code only:
 // the policy decides which slot each (layer, expert) occupies; misses are
-// copied host -> device with one cudaMemcpyAsync per blob and the affected
-// rows of the context's slot table are rewritten, so the GPU kernels see only
+// copied host -> device with one cudaMemcpyAsync per blob (spread over a few
+// copy streams forked from and joined back to the caller's stream, so several
+// copy engines run at once) and the affected rows of the context's slot table
+// are rewritten, so the GPU kernels see only
 // resident experts through the same indirection as a fully resident pool.
 // Results do not depend on where an expert sits, so a cached run is
 // bit-identical to a fully resident one.
@@ -124,8 +126,12 @@ private:
 
 using smoe::SlotPolicy;
 
+constexpr int kCopyStreams = 4;
+
 struct smoe_cache {
     smoe_ctx *ctx;
+    cudaStream_t side[kCopyStreams];   // the blob copies of one call, forked from and joined to its stream
+    cudaEvent_t fork, join[kCopyStreams];
     const uint8_t *host_store;      // [n_layers][E][stride] packed blobs
     uint8_t *pool;                  // [n_slots][stride] device
     SlotPolicy *policy;
@@ -155,9 +161,25 @@ extern "C" int smoe_cache_create(smoe_ctx *ctx, const void *host_store, uint64_t
         return SMOE_ENOMEM;
     }
     for (uint64_t i = 0; i < n_experts; ++i) c->table_host[i] = -1;   // nothing resident yet
-    const cudaError_t e = cudaMemcpyAsync(ctx->table_dev, c->table_host, n_experts * 4, cudaMemcpyHostToDevice,
-                                          static_cast<cudaStream_t>(stream));
+    cudaError_t e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming);
+    int made = 0;                                                    // streams and join events created
+    for (; e == cudaSuccess && made < kCopyStreams; ++made) {
+        e = cudaStreamCreateWithFlags(&c->side[made], cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->join[made], cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            if (c->side[made]) cudaStreamDestroy(c->side[made]);
+            break;
+        }
+    }
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ctx->table_dev, c->table_host, n_experts * 4, cudaMemcpyHostToDevice,
+                            static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
+        for (int i = 0; i < made; ++i) {
+            cudaStreamDestroy(c->side[i]);
+            cudaEventDestroy(c->join[i]);
+        }
+        if (c->fork) cudaEventDestroy(c->fork);
         cudaFreeHost(c->table_host);
         delete c->policy;
         delete c;
@@ -170,6 +192,11 @@ extern "C" int smoe_cache_create(smoe_ctx *ctx, const void *host_store, uint64_t
 extern "C" int smoe_cache_destroy(smoe_cache *c)
 {
     if (!c) return SMOE_OK;
+    for (int i = 0; i < kCopyStreams; ++i) {          // released once their queued copies have run
+        cudaStreamDestroy(c->side[i]);
+        cudaEventDestroy(c->join[i]);
+    }
+    cudaEventDestroy(c->fork);
     cudaFreeHost(c->table_host);
     delete c->policy;
     delete c;
@@ -188,11 +215,25 @@ extern "C" int smoe_cache_prepare(smoe_cache *c, int32_t layer, const int32_t *i
     const uint64_t stride = ctx->layout.blob;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    for (const SlotPolicy::Fill &f : c->fills) {
-        const uint8_t *src = c->host_store + (uint64_t(f.layer) * E + f.expert) * stride;
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(c->pool + uint64_t(f.slot) * stride, src, stride, cudaMemcpyHostToDevice, st);
+    // The copies wait for everything queued on st before them (an evicted slot
+    // may still be read by an earlier forward), run on up to kCopyStreams
+    // streams, and st waits for all of them before the table rows change.
+    const int nside = int(c->fills.size() < size_t(kCopyStreams) ? c->fills.size() : size_t(kCopyStreams));
+    if (nside > 1) {
+        e = cudaEventRecord(c->fork, st);
+        for (int i = 0; i < nside && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(c->side[i], c->fork, 0);
     }
+    for (size_t j = 0; j < c->fills.size() && e == cudaSuccess; ++j) {
+        const SlotPolicy::Fill &f = c->fills[j];
+        const uint8_t *src = c->host_store + (uint64_t(f.layer) * E + f.expert) * stride;
+        e = cudaMemcpyAsync(c->pool + uint64_t(f.slot) * stride, src, stride, cudaMemcpyHostToDevice,
+                            nside > 1 ? c->side[j % size_t(nside)] : st);
+    }
+    if (nside > 1)
+        for (int i = 0; i < nside && e == cudaSuccess; ++i) {
+            e = cudaEventRecord(c->join[i], c->side[i]);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(st, c->join[i], 0);
+        }
     // the mirror, then the rows that changed: this layer's and those of evicted experts
     std::vector<int32_t> rows(1, layer);
     for (int64_t key : c->evicted) {
