@@ -64,7 +64,9 @@ extern "C" {
                                    65504 or beyond in fp16 (outside its fp16 intermediates) */
 
 /* Most tokens of one moe_route / moe_forward call (T); larger T is
- * SMOE_EINVAL and smoe_workspace_bytes returns 0. */
+ * SMOE_EINVAL and smoe_workspace_bytes returns 0. A call with T = 0 (any
+ * entry point taking T) returns SMOE_OK without touching a buffer, so its
+ * buffer pointers may be null (smoe_workspace_bytes(ctx, 0) is 0). */
 #define SMOE_MAX_TOKENS (1 << 20)
 
 /* ------------------------------------------------------------------ shapes */

@@ -118,10 +118,10 @@ extern "C" int moe_forward_debug(const smoe_ctx *ctx, int32_t layer, const uint1
                                  void *stream)
 {
     using namespace smoe;
-    if (!ctx || !x || !ids || !w || !gate || !pool || !shared_blob || !out || !err || T < 0 || T > SMOE_MAX_TOKENS)
-        return SMOE_EINVAL;
+    if (!ctx || T < 0 || T > SMOE_MAX_TOKENS) return SMOE_EINVAL;
     if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
-    if (T == 0) return SMOE_OK;
+    if (T == 0) return SMOE_OK;                      // nothing to do; the buffers may be null
+    if (!x || !ids || !w || !gate || !pool || !shared_blob || !out || !err) return SMOE_EINVAL;
     if (pool_bytes < uint64_t(ctx->n_slots) * ctx->layout.blob) return SMOE_ENOMEM;
     DebugParams p = {};
     p.x = x;

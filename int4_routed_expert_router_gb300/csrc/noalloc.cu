@@ -54,9 +54,10 @@ extern "C" int moe_forward_noalloc(const smoe_ctx *ctx, int32_t layer, const uin
                                    uint64_t pool_bytes, const void *shared_blob, const uint16_t *residual,
                                    uint16_t *out, int32_t *err, void *stream)
 {
-    if (!ctx || !x || !ids || !w || !gate || !pool || !shared_blob || !out || !err || T < 0) return SMOE_EINVAL;
+    if (!ctx || T < 0) return SMOE_EINVAL;
     if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
-    if (T == 0) return SMOE_OK;
+    if (T == 0) return SMOE_OK;                      // nothing to do; the buffers may be null
+    if (!x || !ids || !w || !gate || !pool || !shared_blob || !out || !err) return SMOE_EINVAL;
     if (T > kDecodeMaxT) return SMOE_ENOTSUP;
     if (!aligned16(x) || !aligned16(pool) || !aligned16(shared_blob)) return SMOE_EINVAL;
     if (pool_bytes < uint64_t(ctx->n_slots) * ctx->layout.blob) return SMOE_ENOMEM;

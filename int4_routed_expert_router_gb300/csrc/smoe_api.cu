@@ -285,9 +285,9 @@ extern "C" int moe_route(const smoe_ctx *ctx, const uint16_t *W_r, const uint16_
                          int32_t T, const float *logit_bias, int32_t *ids, float *w, float *gate, void *workspace,
                          uint64_t workspace_bytes, void *stream)
 {
-    if (!ctx || !W_r || !w_s || !x || !ids || !w || !gate || !workspace || T < 0 || T > SMOE_MAX_TOKENS)
-        return SMOE_EINVAL;
-    if (T == 0) return SMOE_OK;
+    if (!ctx || T < 0 || T > SMOE_MAX_TOKENS) return SMOE_EINVAL;
+    if (T == 0) return SMOE_OK;                      // nothing to do; the buffers may be null
+    if (!W_r || !w_s || !x || !ids || !w || !gate || !workspace) return SMOE_EINVAL;
     if (!aligned16(W_r) || !aligned16(w_s) || !aligned16(x) || !aligned16(workspace)) return SMOE_EINVAL;
     const Workspace W = workspace_layout(ctx->shape, T);
     if (workspace_bytes < W.total) return SMOE_ENOMEM;
@@ -315,11 +315,10 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
                            const void *shared_blob, const uint16_t *residual, uint16_t *out, void *workspace,
                            uint64_t workspace_bytes, int32_t *err, void *stream)
 {
-    if (!ctx || !x || !ids || !w || !gate || !pool || !shared_blob || !out || !workspace || !err || T < 0 ||
-        T > SMOE_MAX_TOKENS)
-        return SMOE_EINVAL;
+    if (!ctx || T < 0 || T > SMOE_MAX_TOKENS) return SMOE_EINVAL;
     if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
-    if (T == 0) return SMOE_OK;
+    if (T == 0) return SMOE_OK;                      // nothing to do; the buffers may be null
+    if (!x || !ids || !w || !gate || !pool || !shared_blob || !out || !workspace || !err) return SMOE_EINVAL;
     if (!aligned16(x) || !aligned16(pool) || !aligned16(shared_blob) || !aligned16(workspace) || !aligned16(out) ||
         (residual && !aligned16(residual)))
         return SMOE_EINVAL;

@@ -385,3 +385,45 @@ def test_host_side_validation(tiny):
     with pytest.raises(smoe.SmoeError) as ei:
         smoe.moe_route(pool.ctx, inp.Wr[0], inp.ws[0], x, ids, wt, gate, small)
     assert ei.value.status == smoe.ENOMEM
+
+
+# ------------------------------------------------------------- degenerate calls
+
+def test_empty_call_is_a_no_op(tiny):
+    """T = 0: every entry point returns OK without touching a buffer (the
+    workspace query gives 0 bytes, and null pointers are accepted)."""
+    pool, inp = tiny
+    wl = pool.wl
+    assert pool.ctx.workspace_bytes(0) == 0
+    x = torch.zeros((0, wl.H), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((0, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((0, wl.k), dtype=torch.float32, device="cuda")
+    gate = torch.zeros((0,), dtype=torch.float32, device="cuda")
+    out = torch.zeros((0, wl.H), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(0, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    smoe.moe_route(pool.ctx, inp.Wr[0], inp.ws[0], x, ids, w, gate, ws)
+    smoe.moe_forward(pool.ctx, 0, x, ids, w, gate, pool.pool, pool.shared[0], out, ws, err)
+    smoe.moe_forward_noalloc(pool.ctx, 0, x, ids, w, gate, pool.pool, pool.shared[0], out, err)
+    smoe.moe_forward_debug(pool.ctx, 0, x, ids, w, gate, pool.pool, pool.shared[0], out, err)
+    torch.cuda.synchronize()
+    assert smoe.check(err) == 0
+
+
+@pytest.mark.parametrize("T", [3, 40])
+def test_repeated_expert_within_a_token(tiny, T):
+    """A token that names the same expert twice (not what moe_route produces,
+    but moe_forward takes any ids): both pairs count, in route order, on the
+    decode path (T <= 8) and the bucketed path alike."""
+    pool, inp = tiny
+    wl = pool.wl
+    x = synthetic.activations(wl.seed, T, wl.H, tag=8800 + T)
+    rng = np.random.default_rng(T)
+    ids = np.stack([rng.choice(wl.E, wl.k, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[:, 1] = ids[:, 0]                               # every token repeats its first expert
+    w = rng.dirichlet(np.ones(wl.k), size=T).astype(np.float32)
+    gate = rng.uniform(0.2, 0.8, size=T).astype(np.float32)
+    experts = {int(e): synthetic.expert_triples(wl.seed, 0, int(e), wl.H, wl.I) for e in np.unique(ids)}
+    shared = synthetic.expert_triples(wl.seed, 0, None, wl.H, wl.I_shared)
+    y64, _ = oracle.combine(x, ids, w, gate, experts, shared, wl.E, wl.I, wl.I_shared)
+    assert_output_close(gpu_forward(pool, 0, x, ids, w, gate), y64)
