@@ -110,6 +110,31 @@ def _ptr(t) -> int | None:
     return t.data_ptr()
 
 
+def _dev(t, name: str, dtype=None, numel=None, min_bytes=None) -> int | None:
+    """Address of a contiguous CUDA tensor, after checking its dtype and
+    element count where given (None stays NULL). Anything else is refused
+    here, so a kernel is never handed a host address or a short buffer."""
+    if t is None:
+        return None
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s: expected a CUDA tensor, got %s" % (name, type(t).__name__ if not isinstance(
+            t, torch.Tensor) else "a tensor on " + str(t.device)))
+    if not t.is_contiguous():
+        raise ValueError("%s: must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s: expected %s, got %s" % (name, dtype, t.dtype))
+    if numel is not None and t.numel() != numel:
+        raise ValueError("%s: expected %d elements, got %d" % (name, numel, t.numel()))
+    if min_bytes is not None and t.numel() * t.element_size() < min_bytes:
+        raise ValueError("%s: expected at least %d bytes, got %d" % (name, min_bytes, t.numel() * t.element_size()))
+    return t.data_ptr()
+
+
+def _nbytes(t) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         try:
@@ -204,37 +229,52 @@ def set_slot_table(ctx: Context, layer: int, host_table: np.ndarray, stream=None
 
 
 def moe_route(ctx: Context, W_r, w_s, x, ids, w, gate, workspace, logit_bias=None, stream=None):
+    import torch
+    sh = ctx.shape
     T = x.shape[0]
-    _check(lib().moe_route(ctx.handle, _ptr(W_r), _ptr(w_s), _ptr(x), T, _ptr(logit_bias), _ptr(ids), _ptr(w),
-                           _ptr(gate), _ptr(workspace), workspace.numel() * workspace.element_size(),
+    _check(lib().moe_route(ctx.handle, _dev(W_r, "W_r", torch.bfloat16, sh.E * sh.H),
+                           _dev(w_s, "w_s", torch.bfloat16, sh.H), _dev(x, "x", torch.bfloat16, T * sh.H), T,
+                           _dev(logit_bias, "logit_bias", torch.float32, sh.E),
+                           _dev(ids, "ids", torch.int32, T * sh.k), _dev(w, "w", torch.float32, T * sh.k),
+                           _dev(gate, "gate", torch.float32, T), _dev(workspace, "workspace"), _nbytes(workspace),
                            _stream(stream)), "moe_route")
+
+
+def _forward_args(ctx: Context, x, ids, w, gate, pool, shared_blob, out, residual):
+    """Checked addresses of the arguments moe_forward and its variants share."""
+    import torch
+    sh = ctx.shape
+    T = x.shape[0]
+    return (_dev(x, "x", torch.bfloat16, T * sh.H), T, _dev(ids, "ids", torch.int32, T * sh.k),
+            _dev(w, "w", torch.float32, T * sh.k), _dev(gate, "gate", torch.float32, T),
+            _dev(pool, "pool"), _nbytes(pool),
+            _dev(shared_blob, "shared_blob", min_bytes=ctx.layout.blob_bytes),
+            _dev(residual, "residual", torch.bfloat16, T * sh.H), _dev(out, "out", torch.bfloat16, T * sh.H))
 
 
 def moe_forward(ctx: Context, layer: int, x, ids, w, gate, pool, shared_blob, out, workspace, err,
                 residual=None, stream=None):
-    T = x.shape[0]
-    _check(lib().moe_forward(ctx.handle, int(layer), _ptr(x), T, _ptr(ids), _ptr(w), _ptr(gate), _ptr(pool),
-                             pool.numel() * pool.element_size(), _ptr(shared_blob), _ptr(residual), _ptr(out),
-                             _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
-                             _stream(stream)), "moe_forward")
+    import torch
+    a = _forward_args(ctx, x, ids, w, gate, pool, shared_blob, out, residual)
+    _check(lib().moe_forward(ctx.handle, int(layer), *a, _dev(workspace, "workspace"), _nbytes(workspace),
+                             _dev(err, "err", torch.int32, 1), _stream(stream)), "moe_forward")
 
 
 def moe_forward_debug(ctx: Context, layer: int, x, ids, w, gate, pool, shared_blob, out, err, residual=None,
                       stream=None):
     """The plain per-token CUDA path (for checking the fast kernels)."""
-    T = x.shape[0]
-    _check(lib().moe_forward_debug(ctx.handle, int(layer), _ptr(x), T, _ptr(ids), _ptr(w), _ptr(gate), _ptr(pool),
-                                   pool.numel() * pool.element_size(), _ptr(shared_blob), _ptr(residual), _ptr(out),
-                                   _ptr(err), _stream(stream)), "moe_forward_debug")
+    import torch
+    a = _forward_args(ctx, x, ids, w, gate, pool, shared_blob, out, residual)
+    _check(lib().moe_forward_debug(ctx.handle, int(layer), *a, _dev(err, "err", torch.int32, 1), _stream(stream)),
+           "moe_forward_debug")
 
 
 def moe_forward_noalloc(ctx: Context, layer: int, x, ids, w, gate, pool, shared_blob, out, err,
                         residual=None, stream=None):
     """moe_forward without a workspace (scratch inside the library); T <= 8."""
-    T = x.shape[0]
-    _check(lib().moe_forward_noalloc(ctx.handle, int(layer), _ptr(x), T, _ptr(ids), _ptr(w), _ptr(gate),
-                                     _ptr(pool), pool.numel() * pool.element_size(), _ptr(shared_blob),
-                                     _ptr(residual), _ptr(out), _ptr(err), _stream(stream)),
+    import torch
+    a = _forward_args(ctx, x, ids, w, gate, pool, shared_blob, out, residual)
+    _check(lib().moe_forward_noalloc(ctx.handle, int(layer), *a, _dev(err, "err", torch.int32, 1), _stream(stream)),
            "moe_forward_noalloc")
 
 
@@ -243,12 +283,22 @@ def moe_decode_stack(ctx: Context, first_layer: int, Wr, ws, shared_blobs, xs, i
     """One token through len(Wr) layers in one launch. Wr, ws, shared_blobs:
     per-layer device tensors; xs bf16 [L + 1, H] (xs[0] the input); ids, w
     [L, k]; gate [L]."""
+    import torch
+    sh = ctx.shape
     n = len(Wr)
-    arr = lambda ts: (C.c_void_p * n)(*[_ptr(t) for t in ts])
-    _check(lib().moe_decode_stack(ctx.handle, int(first_layer), n, arr(Wr), arr(ws), arr(shared_blobs),
-                                  _ptr(logit_bias), _ptr(xs), _ptr(ids), _ptr(w), _ptr(gate), _ptr(pool),
-                                  pool.numel() * pool.element_size(), _ptr(workspace),
-                                  workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)),
+    if len(ws) != n or len(shared_blobs) != n:
+        raise ValueError("Wr, ws and shared_blobs must have one entry per layer")
+    arr = lambda ts: (C.c_void_p * n)(*ts)
+    _check(lib().moe_decode_stack(ctx.handle, int(first_layer), n,
+                                  arr([_dev(t, "Wr[%d]" % i, torch.bfloat16, sh.E * sh.H) for i, t in enumerate(Wr)]),
+                                  arr([_dev(t, "ws[%d]" % i, torch.bfloat16, sh.H) for i, t in enumerate(ws)]),
+                                  arr([_dev(t, "shared_blobs[%d]" % i, min_bytes=ctx.layout.blob_bytes)
+                                       for i, t in enumerate(shared_blobs)]),
+                                  _dev(logit_bias, "logit_bias", torch.float32, sh.E),
+                                  _dev(xs, "xs", torch.bfloat16, (n + 1) * sh.H), _dev(ids, "ids", torch.int32, n * sh.k),
+                                  _dev(w, "w", torch.float32, n * sh.k), _dev(gate, "gate", torch.float32, n),
+                                  _dev(pool, "pool"), _nbytes(pool), _dev(workspace, "workspace"), _nbytes(workspace),
+                                  _dev(err, "err", torch.int32, 1), _stream(stream)),
            "moe_decode_stack")
 
 

@@ -122,3 +122,26 @@ def test_oracle_pool_path_is_slot_permutation_invariant():
         assert np.array_equal(ob, direct["out_bf16"])
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
     assert np.array_equal(outs[0], direct["out64"])
+
+
+def test_binding_refuses_host_tensors_before_any_call():
+    """Device arguments must be CUDA tensors: a host tensor (or a numpy array)
+    is refused by the binding, so no kernel is ever handed a host address."""
+    import types
+
+    import torch
+    shape = smoe.make_shape(256, 16, 4, 64)
+    ctx = types.SimpleNamespace(handle=None, shape=shape, layout=smoe.layout_of(shape))
+    T, H, k = 2, 256, 4
+    x = torch.zeros((T, H), dtype=torch.bfloat16)
+    ids = torch.zeros((T, k), dtype=torch.int32)
+    w = torch.zeros((T, k), dtype=torch.float32)
+    gate = torch.zeros(T, dtype=torch.float32)
+    blob = torch.zeros(int(ctx.layout.blob_bytes), dtype=torch.uint8)
+    err = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="x: expected a CUDA tensor"):
+        smoe.moe_forward(ctx, 0, x, ids, w, gate, blob, blob, x, blob, err)
+    with pytest.raises(ValueError, match="W_r: expected a CUDA tensor"):
+        smoe.moe_route(ctx, np.zeros((16, H), np.uint16), x[0], x, ids, w, gate, blob)
+    with pytest.raises(ValueError, match="expected a CUDA tensor"):
+        smoe.moe_forward_noalloc(ctx, 0, x, ids, w, gate, blob, blob, x, err)

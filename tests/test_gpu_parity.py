@@ -385,6 +385,16 @@ def test_host_side_validation(tiny):
     with pytest.raises(smoe.SmoeError) as ei:
         smoe.moe_route(pool.ctx, inp.Wr[0], inp.ws[0], x, ids, wt, gate, small)
     assert ei.value.status == smoe.ENOMEM
+    # the binding checks dtypes, element counts and the shared blob's size
+    out = torch.zeros((1, wl.H), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = W.workspace(pool.ctx, 1)
+    with pytest.raises(ValueError, match="w: expected torch.float32"):
+        smoe.moe_forward(pool.ctx, 0, x, ids, wt.double(), gate, pool.pool, pool.shared[0], out, ws, err)
+    with pytest.raises(ValueError, match="ids: expected"):
+        smoe.moe_forward(pool.ctx, 0, x, ids[:, :2].contiguous(), wt, gate, pool.pool, pool.shared[0], out, ws, err)
+    with pytest.raises(ValueError, match="shared_blob: expected at least"):
+        smoe.moe_forward(pool.ctx, 0, x, ids, wt, gate, pool.pool, pool.shared[0][:64], out, ws, err)
 
 
 # ------------------------------------------------------------- degenerate calls

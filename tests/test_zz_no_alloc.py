@@ -74,7 +74,12 @@ def test_noalloc_rejects_calls_larger_than_its_scratch():
     with pytest.raises(smoe.SmoeError) as ei:
         smoe.moe_forward_noalloc(ctx, 0, x, ids, w, gate, pool, pool, out, err)
     assert ei.value.status == smoe.ENOMEM
-    x9 = torch.zeros((9, wl.H), dtype=torch.bfloat16, device="cuda")
+    T9 = 9                                 # above the decode path's 8 tokens
+    x9 = torch.zeros((T9, wl.H), dtype=torch.bfloat16, device="cuda")
+    ids9 = torch.zeros((T9, wl.k), dtype=torch.int32, device="cuda")
+    w9 = torch.zeros((T9, wl.k), dtype=torch.float32, device="cuda")
+    gate9 = torch.zeros((T9,), dtype=torch.float32, device="cuda")
+    out9 = torch.zeros((T9, wl.H), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(smoe.SmoeError) as ei:
-        smoe.moe_forward_noalloc(ctx, 0, x9, ids, w, gate, pool, pool, out, err)
+        smoe.moe_forward_noalloc(ctx, 0, x9, ids9, w9, gate9, pool, pool, out9, err)
     assert ei.value.status == smoe.ENOTSUP
