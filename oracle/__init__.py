@@ -65,6 +65,17 @@ def lib():
                                                            C.c_void_p, C.c_uint64, C.c_int64,
                                                            _i32p, C.c_void_p, _f64p, _u16p]
         L.orc_moe_combine_pool.restype = C.c_int
+        L.orc_dequant_mlx8.argtypes = [_u32p, _u16p, _u16p, C.c_int, C.c_int, _f64p]
+        L.orc_dequant_mlx8.restype = None
+        L.orc_quantize_mlx8.argtypes = [_f64p, C.c_int, C.c_int, _u32p, _u16p, _u16p]
+        L.orc_quantize_mlx8.restype = None
+        L.orc_moe_combine_dense.argtypes = [C.c_int] * 5 + [_u16p, _i32p, _f64p, _f64p] + [C.c_void_p] * 3 + \
+            [C.c_int] + [_f64p] * 3 + [_f64p, _u16p]
+        L.orc_moe_combine_dense.restype = C.c_int
+        L.orc_blob_bytes8.argtypes = [C.c_int, C.c_int]
+        L.orc_blob_bytes8.restype = C.c_uint64
+        L.orc_blob_to_mlx8.argtypes = [_u8p, C.c_int, C.c_int] + [_u32p, _u16p, _u16p] * 3
+        L.orc_blob_to_mlx8.restype = None
         _lib = L
     return _lib
 
@@ -202,6 +213,79 @@ def blob_to_mlx(blob: np.ndarray, H: int, I: int):
     ds = np.empty((H, I // 64), np.uint16); db = np.empty_like(ds)
     lib().orc_blob_to_mlx(np.ascontiguousarray(blob, np.uint8), H, I,
                           gq, gs, gb, uq, us, ub, dq, ds, db)
+    return [gq, gs, gb, uq, us, ub, dq, ds, db]
+
+
+# ------------------------------------------------------------ 8-bit experts
+
+def dequant8(q, s, b) -> np.ndarray:
+    """8-bit MLX triple (4 values per word) -> fp64 weights [rows, cols]."""
+    q = np.ascontiguousarray(q, np.uint32)
+    rows, cols = q.shape[0], q.shape[1] * 4
+    W = np.empty((rows, cols), np.float64)
+    lib().orc_dequant_mlx8(q, np.ascontiguousarray(s, np.uint16), np.ascontiguousarray(b, np.uint16), rows, cols, W)
+    return W
+
+
+def quantize8(W):
+    W = np.ascontiguousarray(W, np.float64)
+    rows, cols = W.shape
+    q = np.empty((rows, cols // 4), np.uint32)
+    s = np.empty((rows, cols // 64), np.uint16)
+    b = np.empty((rows, cols // 64), np.uint16)
+    lib().orc_quantize_mlx8(W, rows, cols, q, s, b)
+    return q, s, b
+
+
+def combine_dense(x, ids, w, gate, dense: dict, shared_dense, E: int, I: int, I_shared: int):
+    """Layer output given routing, for experts given as dense fp64 (G, U, D)
+    {e: (G [I,H], U [I,H], D [H,I])} and the shared expert's (G, U, D).
+
+    Returns (out64 [T,H] float64, out_bf16 [T,H] uint16 bits)."""
+    x = np.ascontiguousarray(x, np.uint16)
+    T, H = x.shape
+    k = ids.shape[1]
+    keep = {e: tuple(np.ascontiguousarray(m, np.float64) for m in gud) for e, gud in dense.items()}
+    ptrs = [(C.c_void_p * E)() for _ in range(3)]
+    for e, gud in keep.items():
+        for m in range(3):
+            ptrs[m][e] = gud[m].ctypes.data
+    Gs, Us, Ds = (np.ascontiguousarray(m, np.float64) for m in shared_dense)
+    out64 = np.empty((T, H), np.float64)
+    outb = np.empty((T, H), np.uint16)
+    rc = lib().orc_moe_combine_dense(T, H, k, I, I_shared, x, np.ascontiguousarray(ids, np.int32),
+                                     np.ascontiguousarray(w, np.float64), np.ascontiguousarray(gate, np.float64),
+                                     C.addressof(ptrs[0]), C.addressof(ptrs[1]), C.addressof(ptrs[2]), E,
+                                     Gs, Us, Ds, out64, outb)
+    if rc != 0:
+        raise ValueError("oracle: a routed expert was not provided")
+    return out64, outb
+
+
+def dense_of8(tr):
+    """(G, U, D) of an 8-bit ExpertTriples."""
+    return (dequant8(tr.gate_q, tr.gate_s, tr.gate_b), dequant8(tr.up_q, tr.up_s, tr.up_b),
+            dequant8(tr.down_q, tr.down_s, tr.down_b))
+
+
+def combine8(x, ids, w, gate, experts: dict, shared, E: int, I: int, I_shared: int):
+    """combine() for 8-bit experts: each one dequantised, then combine_dense."""
+    return combine_dense(x, ids, w, gate, {e: dense_of8(tr) for e, tr in experts.items()}, dense_of8(shared),
+                         E, I, I_shared)
+
+
+def blob_bytes8(H: int, I: int) -> int:
+    return int(lib().orc_blob_bytes8(H, I))
+
+
+def blob_to_mlx8(blob: np.ndarray, H: int, I: int):
+    """Parse one 8-bit expert blob -> list of 9 arrays in ExpertTriples order."""
+    gq = np.empty((I, H // 4), np.uint32); uq = np.empty_like(gq)
+    dq = np.empty((H, I // 4), np.uint32)
+    gs = np.empty((I, H // 64), np.uint16); gb = np.empty_like(gs)
+    us = np.empty_like(gs); ub = np.empty_like(gs)
+    ds = np.empty((H, I // 64), np.uint16); db = np.empty_like(ds)
+    lib().orc_blob_to_mlx8(np.ascontiguousarray(blob, np.uint8), H, I, gq, gs, gb, uq, us, ub, dq, ds, db)
     return [gq, gs, gb, uq, us, ub, dq, ds, db]
 
 

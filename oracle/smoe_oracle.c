@@ -477,3 +477,156 @@ int orc_moe_combine_pool(int T, int H, int k, int I, int E,
     free(ex);
     return rc;
 }
+
+/* ============================================================ 8-bit experts
+ * The pages name MLX-style int4/int8 group quantisation ("Swiftlet Packs 80B
+ * Qwen Into Mac...", last paragraph; agentlenshq article, relation to
+ * TurboFieldfare) and an 8-bit 80B run (paper-digest page, Core Mechanics).
+ * Reading taken: MLX's 8-bit affine format, the same group of 64 and fp16 s,
+ * b per group, w = s*q + b with q in 0..255, 4 values per uint32 (column c of
+ * a row in bits 8*(c%4)..8*(c%4)+7 of word c/4). s*q + b stays exact in fp64
+ * (an 11-bit significand times an 8-bit integer plus an 11-bit significand). */
+
+void orc_dequant_mlx8(const uint32_t *q, const uint16_t *s, const uint16_t *b,
+                      int rows, int cols, double *W)
+{
+    int wpr = cols / 4, gpr = cols / ORC_GROUP;
+    for (int r = 0; r < rows; r++)
+        for (int c = 0; c < cols; c++) {
+            uint32_t word = q[(size_t)r * wpr + c / 4];
+            unsigned byte = (word >> (8 * (c % 4))) & 255u;
+            double sc = orc_f16_to_f64(s[(size_t)r * gpr + c / ORC_GROUP]);
+            double bi = orc_f16_to_f64(b[(size_t)r * gpr + c / ORC_GROUP]);
+            W[(size_t)r * cols + c] = sc * (double)byte + bi;
+        }
+}
+
+/* The 4-bit quantiser's rule with 255 steps: b = fp16 rounded down of the
+ * group min, s = fp16 rounded up of (max - b)/255, q = clamp(round_half_even(
+ * (w - b)/s), 0, 255); so again |w - (s q + b)| <= s/2. */
+void orc_quantize_mlx8(const double *W, int rows, int cols,
+                       uint32_t *q, uint16_t *s, uint16_t *b)
+{
+    int wpr = cols / 4, gpr = cols / ORC_GROUP;
+    memset(q, 0, sizeof(uint32_t) * (size_t)rows * wpr);
+    for (int r = 0; r < rows; r++)
+        for (int g = 0; g < gpr; g++) {
+            const double *w = W + (size_t)r * cols + g * ORC_GROUP;
+            double lo = w[0], hi = w[0];
+            for (int c = 1; c < ORC_GROUP; c++) {
+                if (w[c] < lo) lo = w[c];
+                if (w[c] > hi) hi = w[c];
+            }
+            uint16_t bb = f16_round_dir(lo, 0);
+            double bv = orc_f16_to_f64(bb);
+            uint16_t ss = f16_round_dir((hi - bv) / 255.0, 1);
+            double sv = orc_f16_to_f64(ss);
+            s[(size_t)r * gpr + g] = ss;
+            b[(size_t)r * gpr + g] = bb;
+            for (int c = 0; c < ORC_GROUP; c++) {
+                double t = sv > 0 ? nearbyint((w[c] - bv) / sv) : 0.0;
+                if (t < 0) t = 0;
+                if (t > 255) t = 255;
+                int col = g * ORC_GROUP + c;
+                q[(size_t)r * wpr + col / 4] |= (uint32_t)t << (8 * (col % 4));
+            }
+        }
+}
+
+/* The layer given the routing, for experts given as dense fp64 weights (any
+ * width, already dequantised): the definition of orc_moe_combine, term for
+ * term. G[e], U[e]: [I][H]; D[e]: [H][I]; NULL for experts that ids does not
+ * name. Returns 0, or -1 if a needed expert is missing. */
+int orc_moe_combine_dense(int T, int H, int k, int I, int Is,
+                          const uint16_t *x, const int32_t *ids, const double *w,
+                          const double *gate, const double *const *G, const double *const *U,
+                          const double *const *D, int E, const double *Gs, const double *Us,
+                          const double *Ds, double *out64, uint16_t *out_bf16)
+{
+    double *xt = malloc(sizeof(double) * H);
+    double *y = malloc(sizeof(double) * H);
+    double *hb = malloc(sizeof(double) * (I > Is ? I : Is));
+    int rc = 0;
+    for (int t = 0; t < T && rc == 0; t++) {
+        for (int c = 0; c < H; c++)
+            xt[c] = orc_bf16_to_f64(x[(size_t)t * H + c]);
+        double *o = out64 + (size_t)t * H;
+        for (int c = 0; c < H; c++)
+            o[c] = 0.0;
+        for (int j = 0; j < k; j++) {
+            int e = ids[(size_t)t * k + j];
+            if (e < 0 || e >= E || !G[e] || !U[e] || !D[e]) { rc = -1; break; }
+            expert_mlp(G[e], U[e], D[e], H, I, xt, hb, y);
+            for (int c = 0; c < H; c++)
+                o[c] += w[(size_t)t * k + j] * y[c];
+        }
+        if (rc) break;
+        expert_mlp(Gs, Us, Ds, H, Is, xt, hb, y);
+        for (int c = 0; c < H; c++) {
+            o[c] += gate[t] * y[c];
+            if (out_bf16)
+                out_bf16[(size_t)t * H + c] = orc_f64_to_bf16(o[c]);
+        }
+    }
+    free(xt);
+    free(y);
+    free(hb);
+    return rc;
+}
+
+/* The oracle's reader of the library's 8-bit blob: the atoms keep the 4-bit
+ * atom's row and column order, but hold each value's low nibble in plane 0
+ * (bytes [0,512), the 4-bit lane layout) and its high nibble in plane 1
+ * (bytes [512,1024), the same layout), then the 64 bytes of fp16 (s, b) at
+ * [1024,1088) in the 4-bit atom's order. Atom order as for 4 bits. */
+#define ATOM8 1088
+
+static unsigned blob8_value(const uint8_t *atom, int row, int col)
+{
+    return blob_nibble(atom, row, col) | (blob_nibble(atom + 512, row, col) << 4);
+}
+
+uint64_t orc_blob_bytes8(int H, int I)
+{
+    return (uint64_t)(I / 8) * (H / ORC_GROUP) * ATOM8 +
+           (uint64_t)(H / 16) * (I / ORC_GROUP) * ATOM8;
+}
+
+/* Parse one 8-bit blob into 8-bit MLX triples (q words of 4 values). */
+void orc_blob_to_mlx8(const uint8_t *blob, int H, int I,
+                      uint32_t *gq, uint16_t *gs, uint16_t *gb,
+                      uint32_t *uq, uint16_t *us, uint16_t *ub,
+                      uint32_t *dq, uint16_t *ds, uint16_t *db)
+{
+    int kbH = H / ORC_GROUP, kbI = I / ORC_GROUP;
+    memset(gq, 0, sizeof(uint32_t) * (size_t)I * (H / 4));
+    memset(uq, 0, sizeof(uint32_t) * (size_t)I * (H / 4));
+    memset(dq, 0, sizeof(uint32_t) * (size_t)H * (I / 4));
+    for (int i = 0; i < I; i++)
+        for (int kb = 0; kb < kbH; kb++) {
+            const uint8_t *atom = blob + ((size_t)(i / 8) * kbH + kb) * ATOM8;
+            for (int which = 0; which < 2; which++) {
+                int row = (i % 8) + 8 * which;       /* gate: g, up: g+8 */
+                uint32_t *q = which ? uq : gq;
+                uint16_t *s = which ? us : gs, *b = which ? ub : gb;
+                for (int c = 0; c < ORC_GROUP; c++) {
+                    int col = kb * ORC_GROUP + c;
+                    q[(size_t)i * (H / 4) + col / 4] |=
+                        (uint32_t)blob8_value(atom, row, c) << (8 * (col % 4));
+                }
+                blob_sb(atom + 512, row, &s[(size_t)i * kbH + kb], &b[(size_t)i * kbH + kb]);
+            }
+        }
+    const uint8_t *down = blob + (size_t)(I / 8) * kbH * ATOM8;
+    for (int o = 0; o < H; o++)
+        for (int kb = 0; kb < kbI; kb++) {
+            const uint8_t *atom = down + ((size_t)(o / 16) * kbI + kb) * ATOM8;
+            int row = o % 16;
+            for (int c = 0; c < ORC_GROUP; c++) {
+                int col = kb * ORC_GROUP + c;
+                dq[(size_t)o * (I / 4) + col / 4] |=
+                    (uint32_t)blob8_value(atom, row, c) << (8 * (col % 4));
+            }
+            blob_sb(atom + 512, row, &ds[(size_t)o * kbI + kb], &db[(size_t)o * kbI + kb]);
+        }
+}

@@ -21,6 +21,9 @@ Distributions (the workloads of the Swiftlet pages, shapes of Qwen3.6-35B-A3B
 and Qwen3-Next-80B-A3B):
   q ~ U{0..15} (every bit of a q word is uniform, 8 nibbles per uint32)
   s ~ U[0.002, 0.006] rounded to fp16; b = fp16(-7.5 * s)
+  8-bit experts (MLX's 8-bit affine format, 4 values per uint32): q ~ U{0..255},
+  s ~ U[0.002, 0.006] / 17 rounded to fp16, b = fp16(-127.5 * s), so the
+  weights span the same range as the 4-bit recipe's
   router rows, shared-gate vector ~ N(0, 0.02) -> fp32 -> bf16 (RNE)
   activations ~ N(0, 1) -> fp32 -> bf16 (RNE)
 """
@@ -73,29 +76,44 @@ def q_words(key: np.uint64, rows: int, cols: int) -> np.ndarray:
     return out.astype(np.uint32).reshape(rows, cols // 8)
 
 
-def scale_bias(key: np.uint64, rows: int, cols: int):
-    """fp16 bits [rows, cols/64] of s ~ U[0.002, 0.006] and b = fp16(-7.5 s).
+def q_words8(key: np.uint64, rows: int, cols: int) -> np.ndarray:
+    """uint32 [rows, cols/4] of 8-bit values (column c of a row in bits
+    8*(c % 4) .. of word c/4): word w is half (w & 1) of value(key, w >> 1)."""
+    n = rows * (cols // 4)
+    w = np.arange(n, dtype=np.uint64)
+    v = stream_values(key, w >> np.uint64(1))
+    out = (v >> (np.uint64(32) * (w & np.uint64(1)))) & np.uint64(0xFFFFFFFF)
+    return out.astype(np.uint32).reshape(rows, cols // 4)
 
-    u = value >> 40 (24 uniform bits); s = fp16_rne(0.002 + 0.004 * (u / 2^24)),
-    with the two double operations rounded separately (no fused multiply-add).
+
+def scale_bias(key: np.uint64, rows: int, cols: int, bits: int = 4):
+    """fp16 bits [rows, cols/64] of s ~ U[0.002, 0.006] and b = fp16(-7.5 s)
+    (bits = 8: s ~ U[0.002, 0.006] / 17 and b = fp16(-127.5 s)).
+
+    u = value >> 40 (24 uniform bits); s = fp16_rne(0.002 + 0.004 * (u / 2^24))
+    (divided by 17 for 8 bits), with the double operations rounded separately
+    (no fused multiply-add).
     """
     n = rows * (cols // GROUP)
     v = stream_values(key, np.arange(n, dtype=np.uint64))
     u = (v >> np.uint64(40)).astype(np.float64) / 16777216.0
     t = np.multiply(0.004, u)
     s64 = np.add(0.002, t)
+    if bits == 8:
+        s64 = np.divide(s64, 17.0)
     s16 = s64.astype(np.float16)
-    b16 = np.multiply(-7.5, s16.astype(np.float64)).astype(np.float16)
+    b16 = np.multiply(-7.5 if bits == 4 else -127.5, s16.astype(np.float64)).astype(np.float16)
     return (s16.view(np.uint16).reshape(rows, cols // GROUP),
             b16.view(np.uint16).reshape(rows, cols // GROUP))
 
 
 @dataclasses.dataclass
 class ExpertTriples:
-    """MLX affine 4-bit triples of one expert (q uint32 words, s/b fp16 bits).
+    """MLX affine triples of one expert (q uint32 words, s/b fp16 bits).
 
-    gate, up: q [I, H/8], s/b [I, H/64]; down: q [H, I/8], s/b [H, I/64].
-    Within a word, column c of the row sits in bits 4*(c % 8) .. 4*(c % 8)+3.
+    4 bits: gate, up: q [I, H/8], s/b [I, H/64]; down: q [H, I/8], s/b [H, I/64];
+    within a word, column c of the row sits in bits 4*(c % 8) .. 4*(c % 8)+3.
+    8 bits: q [I, H/4] and [H, I/4], column c in bits 8*(c % 4) .. 8*(c % 4)+7.
     """
     gate_q: np.ndarray
     gate_s: np.ndarray
@@ -112,16 +130,19 @@ class ExpertTriples:
                 self.up_b, self.down_q, self.down_s, self.down_b]
 
 
-def expert_triples(seed: int, layer: int, expert: int | None, H: int, I: int) -> ExpertTriples:
-    """Triples of routed expert ``expert`` (or the shared expert if None)."""
+def expert_triples(seed: int, layer: int, expert: int | None, H: int, I: int, bits: int = 4) -> ExpertTriples:
+    """Triples of routed expert ``expert`` (or the shared expert if None), with
+    4-bit (default) or 8-bit q."""
+    assert bits in (4, 8)
     code = SHARED_EXPERT_CODE if expert is None else int(expert)
     k = lambda tid: stream_key(seed, tid, layer, code)
-    gs, gb = scale_bias(k(TID_GATE_S), I, H)
-    us, ub = scale_bias(k(TID_UP_S), I, H)
-    ds, db = scale_bias(k(TID_DOWN_S), H, I)
-    return ExpertTriples(q_words(k(TID_GATE_Q), I, H), gs, gb,
-                         q_words(k(TID_UP_Q), I, H), us, ub,
-                         q_words(k(TID_DOWN_Q), H, I), ds, db)
+    qw = q_words if bits == 4 else q_words8
+    gs, gb = scale_bias(k(TID_GATE_S), I, H, bits)
+    us, ub = scale_bias(k(TID_UP_S), I, H, bits)
+    ds, db = scale_bias(k(TID_DOWN_S), H, I, bits)
+    return ExpertTriples(qw(k(TID_GATE_Q), I, H), gs, gb,
+                         qw(k(TID_UP_Q), I, H), us, ub,
+                         qw(k(TID_DOWN_Q), H, I), ds, db)
 
 
 # ---------------------------------------------------------------- dense tensors

@@ -228,3 +228,68 @@ def test_oracle_reproduces_stored_tiny_fixture():
     got = mod.compute()
     for key in ref.files:
         assert np.array_equal(got[key], ref[key]), key
+
+
+# --------------------------------------------------------------- 8-bit experts
+
+def test_dequant8_matches_byte_view_unpack():
+    """8-bit MLX words: a second unpack that reads the words as little-endian
+    bytes (byte j of a word = column 4 w + j)."""
+    rng = np.random.default_rng(12)
+    rows, cols = 24, 192
+    q = rng.integers(0, 2 ** 32, size=(rows, cols // 4), dtype=np.uint64).astype(np.uint32)
+    s = oracle.f64_to_f16(rng.uniform(1e-4, 1e-2, size=(rows, cols // 64)))
+    b = oracle.f64_to_f16(rng.uniform(-1, 1, size=(rows, cols // 64)))
+    byte = q.view(np.uint8).reshape(rows, cols).astype(np.int64)
+    sc = torch_f16(s).double().numpy().repeat(64, axis=1)
+    bi = torch_f16(b).double().numpy().repeat(64, axis=1)
+    assert np.array_equal(oracle.dequant8(q, s, b), sc * byte + bi)
+
+
+@pytest.mark.parametrize("lo,hi", [(-0.05, 0.05), (0.0, 1.0), (-3.0, -2.5), (1e-4, 2e-4)])
+def test_quantize8_dequantize_error_at_most_half_scale(lo, hi):
+    rng = np.random.default_rng(int(1e4 * (hi - lo)) + 1)
+    W = rng.uniform(lo, hi, size=(16, 256))
+    W[3, 64:128] = W[3, 64]          # a constant group
+    q, s, b = oracle.quantize8(W)
+    Wd = oracle.dequant8(q, s, b)
+    sc = oracle.f16_to_f64(s).repeat(64, axis=1)
+    assert np.all(np.abs(Wd - W) <= sc / 2 * (1 + 1e-12) + 1e-300)
+    # 255 steps: about 17 times finer than the 4-bit quantiser on the same groups
+    s4 = oracle.f16_to_f64(oracle.quantize(W)[1])
+    assert np.median(s4 / np.maximum(oracle.f16_to_f64(s), 1e-300)) > 15
+
+
+def test_dense_combine_equals_the_4_bit_combine():
+    """combine_dense (experts given as fp64 weights) is the same definition as
+    the pinned 4-bit combine: fed the 4-bit experts' exact dequantisation, its
+    output is bit-identical, including a repeated expert within a token."""
+    x, Wr, ws = tiny_inputs(T=5)
+    ids, w, gate = oracle.route(x, Wr, ws, TINY.k)
+    ids[2, 1] = ids[2, 0]
+    experts = {int(e): synthetic.expert_triples(TINY.seed, 0, int(e), TINY.H, TINY.I) for e in np.unique(ids)}
+    shared = synthetic.expert_triples(TINY.seed, 0, None, TINY.H, TINY.I)
+    want, want_b = oracle.combine(x, ids, w, gate, experts, shared, TINY.E, TINY.I, TINY.I)
+    dq = lambda t: (oracle.dequant(t.gate_q, t.gate_s, t.gate_b), oracle.dequant(t.up_q, t.up_s, t.up_b),
+                    oracle.dequant(t.down_q, t.down_s, t.down_b))
+    got, got_b = oracle.combine_dense(x, ids, w, gate, {e: dq(t) for e, t in experts.items()}, dq(shared),
+                                      TINY.E, TINY.I, TINY.I)
+    assert np.array_equal(got, want) and np.array_equal(got_b, want_b)
+    with pytest.raises(ValueError):
+        oracle.combine_dense(x, ids, w, gate, {}, dq(shared), TINY.E, TINY.I, TINY.I)
+
+
+def test_8_bit_layer_one_hot_router_is_one_dense_swiglu_mlp():
+    """An 8-bit layer with k = 1 and the shared gate at 0 is one expert's
+    SwiGLU MLP on its dequantised weights (torch CPU fp64)."""
+    x, Wr, ws = tiny_inputs(T=3)
+    ids = np.full((3, 1), 5, np.int32)
+    w = np.ones((3, 1))
+    gate = np.zeros(3)
+    tr = synthetic.expert_triples(TINY.seed, 0, 5, TINY.H, TINY.I, bits=8)
+    sh = synthetic.expert_triples(TINY.seed, 0, None, TINY.H, TINY.I, bits=8)
+    out, _ = oracle.combine8(x, ids, w, gate, {5: tr}, sh, TINY.E, TINY.I, TINY.I)
+    G, U, D = (torch.from_numpy(m) for m in oracle.dense_of8(tr))
+    xt = torch_bf16(x).double()
+    ref = (F.silu(xt @ G.T) * (xt @ U.T)) @ D.T
+    assert np.allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)

@@ -39,3 +39,23 @@ def test_dense_tensors():
     assert sorted(tab.ravel().tolist()) == list(range(64))
     z = synthetic.zipf_bias(3, 16)
     assert np.isclose(np.sort(z)[::-1][0], 0.0) and np.isclose(z.min(), -1.1 * np.log(16))
+
+
+def test_expert_recipe_8_bit():
+    """8-bit triples: 4 values per word, every byte value equally likely,
+    s = the 4-bit recipe's / 17 and b = -127.5 s, so the weight range is the
+    4-bit recipe's; the 4-bit draw is unchanged by the option."""
+    t = synthetic.expert_triples(7, 3, 11, 512, 128, bits=8)
+    assert t.gate_q.shape == (128, 128) and t.down_q.shape == (512, 32) and t.down_s.shape == (512, 2)
+    q = np.stack([(t.gate_q >> np.uint32(8 * i)) & np.uint32(255) for i in range(4)]).ravel()
+    counts = np.bincount(q, minlength=256)
+    assert counts.min() > 0.75 * q.size / 256 and counts.max() < 1.25 * q.size / 256
+    s = t.gate_s.view(np.float16).astype(np.float64)
+    b = t.gate_b.view(np.float16).astype(np.float64)
+    assert s.min() >= 0.0019 / 17 and s.max() <= 0.00601 / 17
+    assert np.array_equal(b, (-127.5 * s).astype(np.float16).astype(np.float64))
+    t4 = synthetic.expert_triples(7, 3, 11, 512, 128)
+    assert np.array_equal(t4.gate_s, synthetic.expert_triples(7, 3, 11, 512, 128, bits=4).gate_s)
+    s4 = t4.gate_s.view(np.float16).astype(np.float64)
+    # both are one fp16 rounding of the same draw (divided by 17 for s): two half-ulps apart at most
+    assert np.all(np.abs(s - s4 / 17) <= 2 ** -10 * s4 / 17)
