@@ -495,9 +495,9 @@ void orc_dequant_mlx8(const uint32_t *q, const uint16_t *s, const uint16_t *b,
         for (int c = 0; c < cols; c++) {
             uint32_t word = q[(size_t)r * wpr + c / 4];
             unsigned byte = (word >> (8 * (c % 4))) & 255u;
-            double sc = orc_f16_to_f64(s[(size_t)r * gpr + c / ORC_GROUP]);
-            double bi = orc_f16_to_f64(b[(size_t)r * gpr + c / ORC_GROUP]);
-            W[(size_t)r * cols + c] = sc * (double)byte + bi;
+            double scale = orc_f16_to_f64(s[(size_t)r * gpr + c / ORC_GROUP]);
+            double bias = orc_f16_to_f64(b[(size_t)r * gpr + c / ORC_GROUP]);
+            W[(size_t)r * cols + c] = scale * (double)byte + bias;
         }
 }
 
@@ -563,7 +563,7 @@ int orc_moe_combine_dense(int T, int H, int k, int I, int Is,
         if (rc) break;
         expert_mlp(Gs, Us, Ds, H, Is, xt, hb, y);
         for (int c = 0; c < H; c++) {
-            o[c] += gate[t] * y[c];
+            o[c] += y[c] * gate[t];
             if (out_bf16)
                 out_bf16[(size_t)t * H + c] = orc_f64_to_bf16(o[c]);
         }

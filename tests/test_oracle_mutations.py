@@ -33,6 +33,9 @@ MUTATIONS = {
     "truncating_round": ("double r = nearbyint(v / quantum) * quantum;",
                          "double r = trunc(v / quantum) * quantum;"),
     "fp16_exponent_bias": ("v = ldexp(1.0 + m / 1024.0, e - 15);", "v = ldexp(1.0 + m / 1024.0, e - 16);"),
+    "byte_order_reversed_8_bit": ("unsigned byte = (word >> (8 * (c % 4))) & 255u;",
+                                  "unsigned byte = (word >> (8 * (3 - c % 4))) & 255u;"),
+    "dense_combine_shared_term_dropped": ("o[c] += y[c] * gate[t];", "o[c] += 0.0 * y[c] * gate[t];"),
     "router_row_col_swapped": ("acc += orc_bf16_to_f64(xt[h]) * orc_bf16_to_f64(Wr[(size_t)e * H + h]);",
                                "acc += orc_bf16_to_f64(xt[h]) * orc_bf16_to_f64(Wr[(size_t)h * E + e % E]);"),
 }
