@@ -72,7 +72,9 @@ extern "C" {
 /* ------------------------------------------------------------------ shapes */
 /* H: hidden size; E: routed experts per layer; k: experts per token;
  * I: routed expert intermediate size; I_shared: shared expert intermediate
- * size; group: quantisation group (must be 64); bits: 4.
+ * size; group: quantisation group (must be 64); bits: 4, or 8 for
+ * smoe_layout_of and host packing only (the kernels, and so smoe_ctx_create,
+ * take 4-bit experts; bits = 8 elsewhere is SMOE_ENOTSUP).
  * Supported: H % 256 == 0, H <= 2048, I % 64 == 0, 64 <= I <= 512, I_shared == I,
  * 1 <= k <= 16, k <= E <= 1024. Others return SMOE_ENOTSUP. */
 typedef struct smoe_shape {
@@ -111,13 +113,23 @@ typedef struct smoe_layout {
     uint32_t reserved;
 } smoe_layout;
 
+/* 8-bit experts (bits = 8): the same atoms of 16 rows x 64 columns in the
+ * same order, 1,088 bytes each: bytes [0,512) hold each value's low nibble
+ * and bytes [512,1024) its high nibble, each plane laid out exactly as the
+ * 4-bit atom's bytes [0,512) (so q = low + 16 * high), then the (s, b) bytes
+ * of the 4-bit atom at [1024,1088). 3,342,336 bytes per blob at H=2048, I=512.
+ * The pages name MLX int4/int8 group quantisation ("Swiftlet Packs 80B Qwen
+ * Into Mac...", last paragraph). */
+
 /* Fills *out for shape. Errors: SMOE_EINVAL (null), SMOE_ENOTSUP (shape). */
 SMOE_API int smoe_layout_of(const smoe_shape *shape, smoe_layout *out);
 
 /* ------------------------------------------------------------ pack_experts */
 /* MLX triples of one expert (as produced by MLX's affine quantisation):
  * q[0] gate uint32 [I][H/8], q[1] up [I][H/8], q[2] down [H][I/8], column c of
- * a row in bits 4*(c%8).. of word c/8; s[m], b[m] fp16 bits [rows][cols/64]. */
+ * a row in bits 4*(c%8).. of word c/8; s[m], b[m] fp16 bits [rows][cols/64].
+ * With bits = 8: q[0], q[1] [I][H/4], q[2] [H][I/4], column c in bits
+ * 8*(c%4).. of word c/4. */
 typedef struct smoe_expert_src {
     const uint32_t *q[3];
     const uint16_t *s[3];
@@ -135,6 +147,7 @@ typedef struct smoe_expert_src {
  * triples must stay valid until they complete. Corresponds to the pages'
  * repack step ("swiftlet-repack" builds fixed-stride containers from MLX
  * checkpoints), done in memory.
+ * 8-bit experts pack with SMOE_HOST only (SMOE_DEVICE: SMOE_ENOTSUP).
  * Errors: SMOE_EINVAL, SMOE_ENOTSUP, SMOE_ERANGE (slot < 0), SMOE_ENOMEM
  * (slot past pool_bytes), SMOE_ECUDA. */
 SMOE_API int pack_experts(const smoe_shape *shape, const smoe_expert_src *src, int32_t n,

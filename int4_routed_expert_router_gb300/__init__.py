@@ -149,8 +149,9 @@ def _stream(stream) -> int | None:
     return stream.cuda_stream
 
 
-def make_shape(H, E, k, I, I_shared=None) -> Shape:
-    return Shape(H, E, k, I, I if I_shared is None else I_shared, 64, 4)
+def make_shape(H, E, k, I, I_shared=None, bits=4) -> Shape:
+    """bits = 8: the 8-bit format, for layout_of and host packing only."""
+    return Shape(H, E, k, I, I if I_shared is None else I_shared, 64, bits)
 
 
 def layout_of(shape: Shape) -> Layout:

@@ -93,6 +93,81 @@ void pack_host(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst)
     }
 }
 
+// ------------------------------------------------------ 8-bit experts (host)
+// MLX's 8-bit affine format (4 values per uint32, column c of a row in bits
+// 8 (c % 4) ..) packs into atoms of the same 16 rows x 64 columns that hold
+// each value's low nibble in plane 0 and its high nibble in plane 1, each
+// plane in the 4-bit atom's lane order, then the same 64 bytes of (s, b): so
+// q = lo + 16 hi, and a kernel that reads 4-bit atoms reads each plane as
+// one. The pages name int4/int8 group quantisation ("Swiftlet Packs 80B Qwen
+// Into Mac...", last paragraph). Only the host packer and the layout exist;
+// the kernels take 4-bit experts.
+constexpr int kAtom8Bytes = 2 * kAtomQBytes + 64;    // 1088
+
+Layout layout8_of(int H, int I)
+{
+    Layout L;
+    L.gu_off = 0;
+    L.gu_bytes = uint64_t(I / 8) * (H / kGroup) * kAtom8Bytes;
+    L.down_off = L.gu_bytes;
+    L.down_bytes = uint64_t(H / 16) * (I / kGroup) * kAtom8Bytes;
+    L.blob = L.gu_bytes + L.down_bytes;
+    return L;
+}
+
+// The 4-bit-format word of 8 consecutive columns (column c0 + j in bits
+// 4j ..) made of one nibble plane of the 8-bit words w0 (columns c0 ..
+// c0 + 3) and w1 (c0 + 4 .. c0 + 7): plane 0 the low nibbles, plane 1 the high.
+inline uint32_t plane_word(uint32_t w0, uint32_t w1, int plane)
+{
+    uint32_t out = 0;
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t v = ((j < 4 ? w0 : w1) >> (8 * (j & 3))) & 0xFFu;
+        out |= ((v >> (4 * plane)) & 0xFu) << (4 * j);
+    }
+    return out;
+}
+
+// Lane L of nibble plane `plane` of 8-bit atom (part, rb, kb).
+inline uint4 atom_lane8(const smoe_expert_src &src, int H, int I, bool down, int rb, int kb, int L, int plane)
+{
+    const int g = L >> 2, t = L & 3;
+    const int wpr = down ? I / 4 : H / 4;
+    const int w0 = kb * 16 + 4 * t;    // 8-bit MLX word of columns kb*64 + 16t ..
+    uint32_t out[4];
+    for (int half = 0; half < 2; ++half) {     // row g, row g+8
+        int mat, row;
+        atom_row(down, rb, g + 8 * half, &mat, &row);
+        const uint32_t *q = src.q[mat] + size_t(row) * wpr;
+        out[2 * half] = blob_word(plane_word(q[w0], q[w0 + 1], plane));
+        out[2 * half + 1] = blob_word(plane_word(q[w0 + 2], q[w0 + 3], plane));
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+void pack_host8(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst)
+{
+    const Layout L = layout8_of(s.H, s.I);
+    for (int part = 0; part < 2; ++part) {
+        const bool down = part == 1;
+        const int nrb = down ? s.H / 16 : s.I / 8, nkb = down ? s.I / kGroup : s.H / kGroup;
+        uint8_t *base = dst + (down ? L.down_off : L.gu_off);
+        for (int rb = 0; rb < nrb; ++rb)
+            for (int kb = 0; kb < nkb; ++kb) {
+                uint8_t *atom = base + (size_t(rb) * nkb + kb) * kAtom8Bytes;
+                for (int plane = 0; plane < 2; ++plane)
+                    for (int lane = 0; lane < 32; ++lane) {
+                        const uint4 v = atom_lane8(src, s.H, s.I, down, rb, kb, lane, plane);
+                        std::memcpy(atom + kAtomQBytes * plane + 16 * lane, &v, 16);
+                    }
+                for (int g = 0; g < 8; ++g) {
+                    const uint2 v = atom_sb(src, s.H, s.I, down, rb, kb, g);
+                    std::memcpy(atom + 2 * kAtomQBytes + 8 * g, &v, 8);
+                }
+            }
+    }
+}
+
 // One thread per (atom, lane): 16 bytes of nibbles, and for lanes < 8 the 8
 // bytes of scales/biases.
 __global__ void pack_kernel(const smoe_expert_src src, int H, int I, uint8_t *dst, uint64_t down_off,
@@ -157,10 +232,12 @@ Workspace workspace_layout(const smoe_shape &s, int T)
 }  // namespace smoe
 
 // ====================================================================== C ABI
-static int shape_check(const smoe_shape *s)
+// allow8: the 8-bit format is accepted (layout and host packing only; the
+// kernels, the context and device packing take 4-bit experts)
+static int shape_check(const smoe_shape *s, bool allow8 = false)
 {
     if (!s) return SMOE_EINVAL;
-    if (s->group != 64 || s->bits != 4) return SMOE_ENOTSUP;
+    if (s->group != 64 || !(s->bits == 4 || (allow8 && s->bits == 8))) return SMOE_ENOTSUP;
     if (s->H <= 0 || s->E <= 0 || s->k <= 0 || s->I <= 0) return SMOE_EINVAL;
     if (s->H % 256 || s->H > 2048) return SMOE_ENOTSUP;
     if (s->I % 64 || s->I < 64 || s->I > 512 || s->I_shared != s->I) return SMOE_ENOTSUP;
@@ -172,16 +249,17 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SMOE_OK : SMOE
 
 extern "C" int smoe_layout_of(const smoe_shape *shape, smoe_layout *out)
 {
-    int rc = shape_check(shape);
+    int rc = shape_check(shape, true);
     if (rc) return rc;
     if (!out) return SMOE_EINVAL;
-    const Layout L = layout_of(shape->H, shape->I);
+    const bool b8 = shape->bits == 8;
+    const Layout L = b8 ? layout8_of(shape->H, shape->I) : layout_of(shape->H, shape->I);
     out->blob_bytes = L.blob;
     out->gu_offset = L.gu_off;
     out->gu_bytes = L.gu_bytes;
     out->down_offset = L.down_off;
     out->down_bytes = L.down_bytes;
-    out->atom_bytes = kAtomBytes;
+    out->atom_bytes = b8 ? kAtom8Bytes : kAtomBytes;
     out->atom_rows = kAtomRows;
     out->group = kGroup;
     out->reserved = 0;
@@ -192,11 +270,13 @@ extern "C" int pack_experts(const smoe_shape *shape, const smoe_expert_src *src,
                             const int64_t *dst_slots, void *pool, uint64_t pool_bytes, int32_t where,
                             void *stream)
 {
-    int rc = shape_check(shape);
+    int rc = shape_check(shape, true);
     if (rc) return rc;
     if (n < 0 || (n > 0 && (!src || !dst_slots || !pool))) return SMOE_EINVAL;
     if (where != SMOE_HOST && where != SMOE_DEVICE) return SMOE_EINVAL;
-    const Layout L = layout_of(shape->H, shape->I);
+    const bool b8 = shape->bits == 8;
+    if (b8 && where != SMOE_HOST) return SMOE_ENOTSUP;      // 8-bit: host packing only
+    const Layout L = b8 ? layout8_of(shape->H, shape->I) : layout_of(shape->H, shape->I);
     for (int i = 0; i < n; ++i) {
         for (int m = 0; m < 3; ++m)
             if (!src[i].q[m] || !src[i].s[m] || !src[i].b[m]) return SMOE_EINVAL;
@@ -207,7 +287,9 @@ extern "C" int pack_experts(const smoe_shape *shape, const smoe_expert_src *src,
     uint8_t *base = static_cast<uint8_t *>(pool);
     for (int i = 0; i < n; ++i) {
         uint8_t *dst = base + uint64_t(dst_slots[i]) * L.blob;
-        if (where == SMOE_HOST) {
+        if (b8) {
+            pack_host8(*shape, src[i], dst);
+        } else if (where == SMOE_HOST) {
             pack_host(*shape, src[i], dst);
         } else {
             cudaError_t e = launch_pack_device(*shape, src[i], dst, static_cast<cudaStream_t>(stream));

@@ -145,3 +145,60 @@ def test_binding_refuses_host_tensors_before_any_call():
         smoe.moe_route(ctx, np.zeros((16, H), np.uint16), x[0], x, ids, w, gate, blob)
     with pytest.raises(ValueError, match="expected a CUDA tensor"):
         smoe.moe_forward_noalloc(ctx, 0, x, ids, w, gate, blob, blob, x, err)
+
+
+# --------------------------------------------------------------- 8-bit experts
+
+def test_layout_8_bit():
+    lay = smoe.layout_of(smoe.make_shape(2048, 512, 10, 512, bits=8))
+    assert lay.atom_bytes == 1088 and lay.blob_bytes == 3342336 == oracle.blob_bytes8(2048, 512)
+    assert lay.down_offset == lay.gu_bytes == 64 * 32 * 1088 and lay.down_bytes == 128 * 8 * 1088
+    assert smoe.layout_of(smoe.make_shape(256, 16, 4, 64, bits=8)).blob_bytes == oracle.blob_bytes8(256, 64)
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.layout_of(smoe.make_shape(2048, 512, 10, 512, bits=6))
+    assert ei.value.status == smoe.ENOTSUP
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode80b"])
+def test_host_pack_8_bit_round_trips_through_oracle_reader(name):
+    """The library's 8-bit packer and the oracle's independently written
+    8-bit reader agree on every byte of the two-plane atoms."""
+    wl = synthetic.WORKLOADS[name]
+    shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I, bits=8)
+    stride = smoe.layout_of(shape).blob_bytes
+    srcs = [synthetic.expert_triples(wl.seed, 0, e, wl.H, wl.I, bits=8).arrays() for e in (3, 7)]
+    pool = np.zeros(3 * stride, np.uint8)
+    smoe.pack_experts(shape, srcs, [2, 0], pool, pool.size, smoe.HOST)
+    for src, slot in zip(srcs, [2, 0]):
+        back = oracle.blob_to_mlx8(pool[slot * stride:(slot + 1) * stride], wl.H, wl.I)
+        for a, b in zip(src, back):
+            assert np.array_equal(a, b)
+    assert not pool[stride:2 * stride].any()
+    # the low-nibble plane of an 8-bit blob is the 4-bit blob of the low nibbles
+    lo = [a & np.uint32(0x0F0F0F0F) if i % 3 == 0 else a for i, a in enumerate(srcs[0])]
+    lo4 = [_mlx8_to_4(a) if i % 3 == 0 else a for i, a in enumerate(lo)]
+    s4 = smoe.make_shape(wl.H, wl.E, wl.k, wl.I)
+    blob4 = np.zeros(smoe.layout_of(s4).blob_bytes, np.uint8)
+    smoe.pack_experts(s4, [lo4], [0], blob4, blob4.size, smoe.HOST)
+    atoms8 = pool[2 * stride:3 * stride].reshape(-1, 1088)
+    atoms4 = blob4.reshape(-1, 576)
+    assert np.array_equal(atoms8[:, :512], atoms4[:, :512]) and np.array_equal(atoms8[:, 1024:], atoms4[:, 512:])
+
+
+def _mlx8_to_4(q8):
+    """8-bit MLX words holding values 0..15 -> 4-bit MLX words (8 per word)."""
+    v = np.stack([(q8 >> np.uint32(8 * j)) & np.uint32(15) for j in range(4)], axis=-1).reshape(q8.shape[0], -1)
+    v = v.reshape(v.shape[0], -1, 8).astype(np.uint32)
+    return sum(v[:, :, j] << np.uint32(4 * j) for j in range(8)).astype(np.uint32)
+
+
+def test_8_bit_is_refused_where_the_kernels_would_run():
+    shape = smoe.make_shape(256, 16, 4, 64, bits=8)
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.Context(shape, 1, 16, np.zeros((1, 16), np.int32))
+    assert ei.value.status == smoe.ENOTSUP
+    src = synthetic.expert_triples(1, 0, 0, 256, 64, bits=8).arrays()
+    pool = np.zeros(smoe.layout_of(shape).blob_bytes, np.uint8)
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.pack_experts(shape, [src], [0], pool, pool.size, smoe.DEVICE)
+    assert ei.value.status == smoe.ENOTSUP
