@@ -21,15 +21,24 @@ constexpr int kDbgThreads = 256;
 // 16 t + 7), (g, 16 t + 8 ..), (g + 8, 16 t ..), (g + 8, 16 t + 8 ..); in a word
 // for columns c0 .. c0 + 7, column c0 + 2 m sits in bits 4 m .. 4 m + 3 and
 // column c0 + 2 m + 1 in bits 16 + 4 m ..; fp16 (s, b) of row g, then of row
-// g + 8, at byte 512 + 8 g.
-__device__ float atom_weight(const uint8_t *atom, int lr, int cc)
+// g + 8, at byte 512 + 8 g. An 8-bit atom holds two such 512-byte nibble
+// planes (low nibbles, then high nibbles: q = low + 16 high) and its (s, b)
+// at byte 1024 + 8 g.
+__device__ unsigned atom_nibble(const uint8_t *plane, int lr, int cc)
 {
     const int g = lr & 7, upper = lr >> 3, t = cc >> 4, half = (cc >> 3) & 1, cl = cc & 7;
-    const uint32_t word = *reinterpret_cast<const uint32_t *>(atom + 16 * (4 * g + t) + 4 * (2 * upper + half));
+    const uint32_t word = *reinterpret_cast<const uint32_t *>(plane + 16 * (4 * g + t) + 4 * (2 * upper + half));
     const int shift = (cl & 1) ? 16 + 4 * (cl >> 1) : 4 * (cl >> 1);
-    const float q = float((word >> shift) & 15u);
-    const uint16_t *sb = reinterpret_cast<const uint16_t *>(atom + kAtomQBytes + 8 * g + 4 * upper);
-    return __half2float(__ushort_as_half(sb[0])) * q + __half2float(__ushort_as_half(sb[1]));
+    return (word >> shift) & 15u;
+}
+
+__device__ float atom_weight(const uint8_t *atom, int lr, int cc, bool eight)
+{
+    const int g = lr & 7, upper = lr >> 3;
+    const unsigned q = eight ? atom_nibble(atom, lr, cc) + 16u * atom_nibble(atom + kAtomQBytes, lr, cc)
+                             : atom_nibble(atom, lr, cc);
+    const uint16_t *sb = reinterpret_cast<const uint16_t *>(atom + (eight ? 2 : 1) * kAtomQBytes + 8 * g + 4 * upper);
+    return __half2float(__ushort_as_half(sb[0])) * float(q) + __half2float(__ushort_as_half(sb[1]));
 }
 
 struct DebugParams {
@@ -42,6 +51,7 @@ struct DebugParams {
     const int32_t *table_row;
     uint64_t stride, down_off;
     int64_t n_slots;
+    int atom_bytes;                 // 576 (4-bit atoms) or 1088 (8-bit: two nibble planes)
     const uint16_t *residual;
     uint16_t *out;
     int32_t *err;
@@ -55,6 +65,8 @@ __global__ void __launch_bounds__(kDbgThreads) debug_forward_kernel(const DebugP
     float *hs = dsm + p.H;           // [I] h of the current expert
     const int t = blockIdx.x, tid = threadIdx.x;
     const int H = p.H, I = p.I, ngH = H / kGroup, ngI = I / kGroup;
+    const size_t ab = size_t(p.atom_bytes);
+    const bool eight = p.atom_bytes != kAtomBytes;
     for (int c = tid; c < H; c += kDbgThreads) xs[c] = __uint_as_float(uint32_t(p.x[size_t(t) * H + c]) << 16);
     constexpr int kRows = 2048 / kDbgThreads;                     // outputs per thread (H <= 2048)
     float acc[kRows];
@@ -79,12 +91,12 @@ __global__ void __launch_bounds__(kDbgThreads) debug_forward_kernel(const DebugP
         }
         __syncthreads();                                          // xs ready; hs free
         for (int i = tid; i < I; i += kDbgThreads) {              // gate row i and up row i
-            const uint8_t *row_atoms = blob + size_t(i / 8) * ngH * kAtomBytes;
+            const uint8_t *row_atoms = blob + size_t(i / 8) * ngH * ab;
             float gs = 0.f, us = 0.f;
             for (int c = 0; c < H; ++c) {
-                const uint8_t *atom = row_atoms + size_t(c / kGroup) * kAtomBytes;
-                gs = fmaf(atom_weight(atom, i % 8, c % kGroup), xs[c], gs);
-                us = fmaf(atom_weight(atom, 8 + i % 8, c % kGroup), xs[c], us);
+                const uint8_t *atom = row_atoms + size_t(c / kGroup) * ab;
+                gs = fmaf(atom_weight(atom, i % 8, c % kGroup, eight), xs[c], gs);
+                us = fmaf(atom_weight(atom, 8 + i % 8, c % kGroup, eight), xs[c], us);
             }
             hs[i] = gs / (1.f + expf(-gs)) * us;
         }
@@ -93,10 +105,10 @@ __global__ void __launch_bounds__(kDbgThreads) debug_forward_kernel(const DebugP
         for (int q = 0; q < kRows; ++q) {                         // down rows
             const int r = tid + q * kDbgThreads;
             if (r >= H) break;
-            const uint8_t *row_atoms = blob + p.down_off + size_t(r / 16) * ngI * kAtomBytes;
+            const uint8_t *row_atoms = blob + p.down_off + size_t(r / 16) * ngI * ab;
             float y = 0.f;
             for (int i = 0; i < I; ++i)
-                y = fmaf(atom_weight(row_atoms + size_t(i / kGroup) * kAtomBytes, r % 16, i % kGroup), hs[i], y);
+                y = fmaf(atom_weight(row_atoms + size_t(i / kGroup) * ab, r % 16, i % kGroup, eight), hs[i], y);
             acc[q] = fmaf(wt, y, acc[q]);
         }
     }
@@ -134,6 +146,7 @@ extern "C" int moe_forward_debug(const smoe_ctx *ctx, int32_t layer, const uint1
     p.stride = ctx->layout.blob;
     p.down_off = ctx->layout.down_off;
     p.n_slots = ctx->n_slots;
+    p.atom_bytes = ctx->shape.bits == 8 ? 2 * kAtomQBytes + 64 : kAtomBytes;
     p.residual = residual;
     p.out = out;
     p.err = err;

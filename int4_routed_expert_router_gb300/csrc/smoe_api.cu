@@ -302,14 +302,14 @@ extern "C" int pack_experts(const smoe_shape *shape, const smoe_expert_src *src,
 extern "C" int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_t n_slots, int32_t *table_dev,
                                smoe_ctx **out)
 {
-    int rc = shape_check(shape);
+    int rc = shape_check(shape, true);            // 8-bit: routing and the plain debug path only
     if (rc) return rc;
     if (!out || n_layers <= 0 || n_slots <= 0 || !table_dev) return SMOE_EINVAL;
     *out = nullptr;
     smoe_ctx *c = new (std::nothrow) smoe_ctx();
     if (!c) return SMOE_ENOMEM;
     c->shape = *shape;
-    c->layout = layout_of(shape->H, shape->I);
+    c->layout = shape->bits == 8 ? layout8_of(shape->H, shape->I) : layout_of(shape->H, shape->I);
     c->n_layers = n_layers;
     c->n_slots = n_slots;
     c->table_dev = table_dev;
@@ -399,6 +399,7 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
 {
     if (!ctx || T < 0 || T > SMOE_MAX_TOKENS) return SMOE_EINVAL;
     if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
+    if (ctx->shape.bits != 4) return SMOE_ENOTSUP;   // the expert kernels take 4-bit atoms
     if (T == 0) return SMOE_OK;                      // nothing to do; the buffers may be null
     if (!x || !ids || !w || !gate || !pool || !shared_blob || !out || !workspace || !err) return SMOE_EINVAL;
     if (!aligned16(x) || !aligned16(pool) || !aligned16(shared_blob) || !aligned16(workspace) || !aligned16(out) ||
@@ -524,7 +525,7 @@ static StackWs stack_ws(const smoe_ctx *ctx, int n)
 
 extern "C" uint64_t smoe_stack_workspace_bytes(const smoe_ctx *ctx, int32_t n_layers)
 {
-    if (!ctx || !ctx->stack.ok || n_layers < 1 || n_layers > kStackMaxLayers) return 0;
+    if (!ctx || !ctx->stack.ok || ctx->shape.bits != 4 || n_layers < 1 || n_layers > kStackMaxLayers) return 0;
     return stack_ws(ctx, n_layers).total;
 }
 
@@ -536,6 +537,7 @@ extern "C" int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_
 {
     if (!ctx || !W_r || !w_s || !shared_blobs || !xs || !ids || !w || !gate || !pool || !workspace || !err)
         return SMOE_EINVAL;
+    if (ctx->shape.bits != 4) return SMOE_ENOTSUP;   // the stack kernel takes 4-bit atoms
     if (n_layers < 1 || first_layer < 0 || first_layer + n_layers > ctx->n_layers) return SMOE_EINVAL;
     if (n_layers > kStackMaxLayers || !ctx->stack.ok) return SMOE_ENOTSUP;
     if (!aligned16(xs) || !aligned16(pool) || !aligned16(workspace)) return SMOE_EINVAL;

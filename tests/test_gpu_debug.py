@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import int4_routed_expert_router_gb300 as smoe
+import oracle
 import synthetic
 import workload as W
 from test_gpu_parity import assert_output_close, gpu_forward, oracle_layer
@@ -57,6 +58,47 @@ def test_debug_path_matches_oracle_and_fast_kernels(name, Ts):
         dres, _ = debug_forward(pool, 0, x, ref["ids"], ref["w"], ref["gate"], residual=True)
         xr = synthetic.bf16_bits_to_f32(x).astype(np.float64)
         assert_output_close(dres, xr + ref["out64"])
+
+
+def test_debug_path_8_bit_experts_match_oracle():
+    """8-bit experts (two-plane atoms, packed on the host) through the plain
+    CUDA path, against the oracle's 8-bit layer on the same routing; the fast
+    paths refuse an 8-bit context."""
+    wl = synthetic.WORKLOADS["tiny"]
+    shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I, bits=8)
+    stride = smoe.layout_of(shape).blob_bytes
+    trip = {e: synthetic.expert_triples(wl.seed, 0, e, wl.H, wl.I, bits=8) for e in range(wl.E)}
+    shared_t = synthetic.expert_triples(wl.seed, 0, None, wl.H, wl.I, bits=8)
+    host = np.zeros(wl.E * stride, np.uint8)
+    smoe.pack_experts(shape, [trip[e].arrays() for e in range(wl.E)], list(range(wl.E)), host, host.size, smoe.HOST)
+    sh = np.zeros(stride, np.uint8)
+    smoe.pack_experts(shape, [shared_t.arrays()], [0], sh, sh.size, smoe.HOST)
+    pool, shared = torch.from_numpy(host).cuda(), torch.from_numpy(sh).cuda()
+    table = torch.zeros((1, wl.E), dtype=torch.int32, device="cuda")
+    ctx = smoe.Context(shape, 1, wl.E, table)
+    smoe.set_slot_table(ctx, 0, np.arange(wl.E, dtype=np.int32))
+    inp = W.LayerInputs(wl, 1)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for T in (1, 5):
+        x = synthetic.activations(wl.seed, T, wl.H, tag=990 + T)
+        ids, w, gate = oracle.route(x, inp.Wr_bits[0], inp.ws_bits[0], wl.k)
+        ref, _ = oracle.combine8(x, ids, w, gate, {int(e): trip[int(e)] for e in np.unique(ids)}, shared_t,
+                                 wl.E, wl.I, wl.I)
+        dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dt)).cuda()
+        out = torch.zeros((T, wl.H), dtype=torch.bfloat16, device="cuda")
+        smoe.moe_forward_debug(ctx, 0, W.bf16_tensor(x), dev(ids, np.int32), dev(w, np.float32),
+                               dev(gate, np.float32), pool, shared, out, err)
+        assert smoe.check(err) == 0
+        assert_output_close(W.bits_of(out), ref)
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.moe_forward(ctx, 0, W.bf16_tensor(x), dev(ids, np.int32), dev(w, np.float32), dev(gate, np.float32),
+                         pool, shared, out, W.workspace(ctx, T), err)
+    assert ei.value.status == smoe.ENOTSUP
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.moe_forward_noalloc(ctx, 0, W.bf16_tensor(x), dev(ids, np.int32), dev(w, np.float32),
+                                 dev(gate, np.float32), pool, shared, out, err)
+    assert ei.value.status == smoe.ENOTSUP
+    assert ctx.stack_workspace_bytes(1) == 0
 
 
 def test_debug_path_bad_slot_sets_error_word():
