@@ -123,6 +123,7 @@ typedef struct smoe_layout {
 
 /* Fills *out for shape. Errors: SMOE_EINVAL (null), SMOE_ENOTSUP (shape). */
 SMOE_API int smoe_layout_of(const smoe_shape *shape, smoe_layout *out);
+/* (for bits = 8, atom_bytes is 1088 and the offsets count 8-bit atoms) */
 
 /* ------------------------------------------------------------ pack_experts */
 /* MLX triples of one expert (as produced by MLX's affine quantisation):
@@ -160,7 +161,10 @@ typedef struct smoe_ctx smoe_ctx;
 /* Creates a host-side context on the current CUDA device for shape, a stack
  * of n_layers layers and a pool of n_slots slots. table_dev is caller-owned
  * device memory of n_layers*E int32 (the slot table; filled by
- * set_slot_table). The context allocates no device memory.
+ * set_slot_table). The context allocates no device memory. A context of
+ * 8-bit experts (shape.bits = 8) serves moe_route and moe_forward_debug;
+ * moe_forward, moe_forward_noalloc and moe_decode_stack return SMOE_ENOTSUP
+ * for it (their kernels read 4-bit atoms).
  * Errors: SMOE_EINVAL, SMOE_ENOTSUP, SMOE_ECUDA. */
 SMOE_API int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_t n_slots,
                     int32_t *table_dev, smoe_ctx **out);
