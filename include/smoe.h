@@ -72,9 +72,9 @@ extern "C" {
 /* ------------------------------------------------------------------ shapes */
 /* H: hidden size; E: routed experts per layer; k: experts per token;
  * I: routed expert intermediate size; I_shared: shared expert intermediate
- * size; group: quantisation group (must be 64); bits: 4, or 8 for
- * smoe_layout_of and host packing only (the kernels, and so smoe_ctx_create,
- * take 4-bit experts; bits = 8 elsewhere is SMOE_ENOTSUP).
+ * size; group: quantisation group (must be 64); bits: 4, or 8 (layout,
+ * packing, routing and moe_forward_debug; the fast expert kernels take 4-bit
+ * experts, see smoe_ctx_create).
  * Supported: H % 256 == 0, H <= 2048, I % 64 == 0, 64 <= I <= 512, I_shared == I,
  * 1 <= k <= 16, k <= E <= 1024. Others return SMOE_ENOTSUP. */
 typedef struct smoe_shape {
@@ -148,7 +148,7 @@ typedef struct smoe_expert_src {
  * triples must stay valid until they complete. Corresponds to the pages'
  * repack step ("swiftlet-repack" builds fixed-stride containers from MLX
  * checkpoints), done in memory.
- * 8-bit experts pack with SMOE_HOST only (SMOE_DEVICE: SMOE_ENOTSUP).
+ * 8-bit experts pack with either kind.
  * Errors: SMOE_EINVAL, SMOE_ENOTSUP, SMOE_ERANGE (slot < 0), SMOE_ENOMEM
  * (slot past pool_bytes), SMOE_ECUDA. */
 SMOE_API int pack_experts(const smoe_shape *shape, const smoe_expert_src *src, int32_t n,

@@ -100,8 +100,8 @@ void pack_host(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst)
 // plane in the 4-bit atom's lane order, then the same 64 bytes of (s, b): so
 // q = lo + 16 hi, and a kernel that reads 4-bit atoms reads each plane as
 // one. The pages name int4/int8 group quantisation ("Swiftlet Packs 80B Qwen
-// Into Mac...", last paragraph). Only the host packer and the layout exist;
-// the kernels take 4-bit experts.
+// Into Mac...", last paragraph). The layout, the host and device packers and
+// the plain debug path take 8-bit experts; the fast expert kernels do not.
 constexpr int kAtom8Bytes = 2 * kAtomQBytes + 64;    // 1088
 
 Layout layout8_of(int H, int I)
@@ -118,7 +118,7 @@ Layout layout8_of(int H, int I)
 // The 4-bit-format word of 8 consecutive columns (column c0 + j in bits
 // 4j ..) made of one nibble plane of the 8-bit words w0 (columns c0 ..
 // c0 + 3) and w1 (c0 + 4 .. c0 + 7): plane 0 the low nibbles, plane 1 the high.
-inline uint32_t plane_word(uint32_t w0, uint32_t w1, int plane)
+__host__ __device__ inline uint32_t plane_word(uint32_t w0, uint32_t w1, int plane)
 {
     uint32_t out = 0;
     for (int j = 0; j < 8; ++j) {
@@ -129,7 +129,8 @@ inline uint32_t plane_word(uint32_t w0, uint32_t w1, int plane)
 }
 
 // Lane L of nibble plane `plane` of 8-bit atom (part, rb, kb).
-inline uint4 atom_lane8(const smoe_expert_src &src, int H, int I, bool down, int rb, int kb, int L, int plane)
+__host__ __device__ inline uint4 atom_lane8(const smoe_expert_src &src, int H, int I, bool down, int rb, int kb,
+                                            int L, int plane)
 {
     const int g = L >> 2, t = L & 3;
     const int wpr = down ? I / 4 : H / 4;
@@ -188,8 +189,40 @@ __global__ void pack_kernel(const smoe_expert_src src, int H, int I, uint8_t *ds
     }
 }
 
+// 8-bit: one thread per (atom, plane, lane): 16 bytes of that plane's
+// nibbles, and for plane 0, lanes < 8 the 8 bytes of scales/biases.
+__global__ void pack_kernel8(const smoe_expert_src src, int H, int I, uint8_t *dst, uint64_t down_off,
+                             long long n_gu_atoms, long long n_atoms)
+{
+    const long long total = n_atoms * 64;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long a = i >> 6;
+        const int plane = int((i >> 5) & 1), lane = int(i & 31);
+        const bool down = a >= n_gu_atoms;
+        const long long ai = down ? a - n_gu_atoms : a;
+        const int nkb = down ? I / kGroup : H / kGroup;
+        const int rb = int(ai / nkb), kb = int(ai % nkb);
+        uint8_t *atom = dst + (down ? down_off : 0) + ai * kAtom8Bytes;
+        *reinterpret_cast<uint4 *>(atom + kAtomQBytes * plane + 16 * lane) =
+            atom_lane8(src, H, I, down, rb, kb, lane, plane);
+        if (plane == 0 && lane < 8)
+            *reinterpret_cast<uint2 *>(atom + 2 * kAtomQBytes + 8 * lane) = atom_sb(src, H, I, down, rb, kb, lane);
+    }
+}
+
 cudaError_t launch_pack_device(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst, cudaStream_t st)
 {
+    if (s.bits == 8) {
+        const Layout L8 = layout8_of(s.H, s.I);
+        const long long ngu = (long long)(s.I / 8) * (s.H / kGroup);
+        const long long nd = (long long)(s.H / 16) * (s.I / kGroup);
+        const long long threads = (ngu + nd) * 64;
+        const long long grid = (threads + 255) / 256;
+        pack_kernel8<<<unsigned(grid < 65535 ? grid : 65535), 256, 0, st>>>(src, s.H, s.I, dst, L8.down_off, ngu,
+                                                                            ngu + nd);
+        return cudaGetLastError();
+    }
     const Layout L = layout_of(s.H, s.I);
     const long long ngu = (long long)(s.I / 8) * (s.H / kGroup);
     const long long nd = (long long)(s.H / 16) * (s.I / kGroup);
@@ -232,8 +265,8 @@ Workspace workspace_layout(const smoe_shape &s, int T)
 }  // namespace smoe
 
 // ====================================================================== C ABI
-// allow8: the 8-bit format is accepted (layout and host packing only; the
-// kernels, the context and device packing take 4-bit experts)
+// allow8: the 8-bit format is accepted (layout, packing, the context for
+// routing and the plain debug path; the fast expert kernels refuse it)
 static int shape_check(const smoe_shape *s, bool allow8 = false)
 {
     if (!s) return SMOE_EINVAL;
@@ -275,7 +308,6 @@ extern "C" int pack_experts(const smoe_shape *shape, const smoe_expert_src *src,
     if (n < 0 || (n > 0 && (!src || !dst_slots || !pool))) return SMOE_EINVAL;
     if (where != SMOE_HOST && where != SMOE_DEVICE) return SMOE_EINVAL;
     const bool b8 = shape->bits == 8;
-    if (b8 && where != SMOE_HOST) return SMOE_ENOTSUP;      // 8-bit: host packing only
     const Layout L = b8 ? layout8_of(shape->H, shape->I) : layout_of(shape->H, shape->I);
     for (int i = 0; i < n; ++i) {
         for (int m = 0; m < 3; ++m)
@@ -287,10 +319,9 @@ extern "C" int pack_experts(const smoe_shape *shape, const smoe_expert_src *src,
     uint8_t *base = static_cast<uint8_t *>(pool);
     for (int i = 0; i < n; ++i) {
         uint8_t *dst = base + uint64_t(dst_slots[i]) * L.blob;
-        if (b8) {
-            pack_host8(*shape, src[i], dst);
-        } else if (where == SMOE_HOST) {
-            pack_host(*shape, src[i], dst);
+        if (where == SMOE_HOST) {
+            if (b8) pack_host8(*shape, src[i], dst);
+            else pack_host(*shape, src[i], dst);
         } else {
             cudaError_t e = launch_pack_device(*shape, src[i], dst, static_cast<cudaStream_t>(stream));
             if (e != cudaSuccess) return SMOE_ECUDA;

@@ -1,6 +1,6 @@
 // synth.cu -- device side of the seeded input generator (see synthetic/__init__.py).
 //
-// Produces the MLX affine 4-bit triples of many experts directly in device
+// Produces the MLX affine 4-bit (or 8-bit) triples of many experts directly in device
 // memory with the same counter-based recipe as the numpy generator, so the
 // tens-of-GB expert pools never cross PCIe/C2C. Holds none of the MoE layer's
 // arithmetic: only the SplitMix64 output mix (Steele, Lea, Flood, OOPSLA 2014)
@@ -69,9 +69,10 @@ struct Job {
     uint16_t *b[3];
 };
 
-__global__ void q_kernel(uint64_t seed, int layer, int code0, int n, int H, int I, Job job)
+__global__ void q_kernel(uint64_t seed, int layer, int code0, int n, int H, int I, int bits, Job job)
 {
-    const int wq[3] = {I * (H / 8), I * (H / 8), H * (I / 8)};
+    const int per = 32 / bits;                       // values per word: 8 (4-bit) or 4 (8-bit)
+    const int wq[3] = {I * (H / per), I * (H / per), H * (I / per)};
     for (int ex = 0; ex < n; ++ex)
         for (int m = 0; m < 3; ++m) {
             const uint64_t key = stream_key(seed, 1 + 2 * m, layer, code0 + ex);
@@ -85,7 +86,7 @@ __global__ void q_kernel(uint64_t seed, int layer, int code0, int n, int H, int 
         }
 }
 
-__global__ void sb_kernel(uint64_t seed, int layer, int code0, int n, int H, int I, Job job)
+__global__ void sb_kernel(uint64_t seed, int layer, int code0, int n, int H, int I, int bits, Job job)
 {
     const int ng[3] = {I * (H / 64), I * (H / 64), H * (I / 64)};
     for (int ex = 0; ex < n; ++ex)
@@ -97,10 +98,11 @@ __global__ void sb_kernel(uint64_t seed, int layer, int code0, int n, int H, int
                  i += (long long)gridDim.x * blockDim.x) {
                 const uint64_t v = value(key, uint64_t(i));
                 const double u = double(v >> 40) / 16777216.0;
-                const double s64 = __dadd_rn(0.002, __dmul_rn(0.004, u));
+                double s64 = __dadd_rn(0.002, __dmul_rn(0.004, u));
+                if (bits == 8) s64 = __ddiv_rn(s64, 17.0);   // the 8-bit recipe's scale
                 const uint16_t sh = f64_to_f16(s64);
                 s[i] = sh;
-                b[i] = f64_to_f16(__dmul_rn(-7.5, f16_to_f64(sh)));
+                b[i] = f64_to_f16(__dmul_rn(bits == 8 ? -127.5 : -7.5, f16_to_f64(sh)));
             }
         }
 }
@@ -109,15 +111,23 @@ __global__ void sb_kernel(uint64_t seed, int layer, int code0, int n, int H, int
 
 // Triples of experts code0 .. code0+n-1 of `layer` (code 2^26-1 = shared
 // expert). Output arrays hold the n experts back to back, each in MLX layout:
-// q[0], q[1] [I][H/8], q[2] [H][I/8]; s/b[0..1] [I][H/64], s/b[2] [H][I/64].
-// Returns 0 or a cudaError_t.
+// q[0], q[1] [I][H/8], q[2] [H][I/8] (8 bits: [I][H/4], [H][I/4]);
+// s/b[0..1] [I][H/64], s/b[2] [H][I/64]. bits: 4 or 8. Returns 0 or a cudaError_t.
+extern "C" int synth_expert_triples_bits(uint64_t seed, int layer, int code0, int n, int H, int I, int bits,
+                                         uint32_t *gq, uint16_t *gs, uint16_t *gb, uint32_t *uq, uint16_t *us,
+                                         uint16_t *ub, uint32_t *dq, uint16_t *ds, uint16_t *db, void *stream)
+{
+    if (bits != 4 && bits != 8) return int(cudaErrorInvalidValue);
+    Job job = {{gq, uq, dq}, {gs, us, ds}, {gb, ub, db}};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    q_kernel<<<1024, 256, 0, st>>>(seed, layer, code0, n, H, I, bits, job);
+    sb_kernel<<<256, 256, 0, st>>>(seed, layer, code0, n, H, I, bits, job);
+    return int(cudaGetLastError());
+}
+
 extern "C" int synth_expert_triples(uint64_t seed, int layer, int code0, int n, int H, int I, uint32_t *gq,
                                     uint16_t *gs, uint16_t *gb, uint32_t *uq, uint16_t *us, uint16_t *ub,
                                     uint32_t *dq, uint16_t *ds, uint16_t *db, void *stream)
 {
-    Job job = {{gq, uq, dq}, {gs, us, ds}, {gb, ub, db}};
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    q_kernel<<<1024, 256, 0, st>>>(seed, layer, code0, n, H, I, job);
-    sb_kernel<<<256, 256, 0, st>>>(seed, layer, code0, n, H, I, job);
-    return int(cudaGetLastError());
+    return synth_expert_triples_bits(seed, layer, code0, n, H, I, 4, gq, gs, gb, uq, us, ub, dq, ds, db, stream);
 }

@@ -190,14 +190,3 @@ def _mlx8_to_4(q8):
     v = np.stack([(q8 >> np.uint32(8 * j)) & np.uint32(15) for j in range(4)], axis=-1).reshape(q8.shape[0], -1)
     v = v.reshape(v.shape[0], -1, 8).astype(np.uint32)
     return sum(v[:, :, j] << np.uint32(4 * j) for j in range(8)).astype(np.uint32)
-
-
-def test_8_bit_device_packing_is_refused():
-    """8-bit experts pack on the host only (the fast kernels' refusals of an
-    8-bit context are GPU tests)."""
-    shape = smoe.make_shape(256, 16, 4, 64, bits=8)
-    src = synthetic.expert_triples(1, 0, 0, 256, 64, bits=8).arrays()
-    pool = np.zeros(smoe.layout_of(shape).blob_bytes, np.uint8)
-    with pytest.raises(smoe.SmoeError) as ei:
-        smoe.pack_experts(shape, [src], [0], pool, pool.size, smoe.DEVICE)
-    assert ei.value.status == smoe.ENOTSUP

@@ -123,23 +123,23 @@ def oracle_layer(wl, layer, x_bits, inp):
 
 # ------------------------------------------------------------- generator/pack
 
-@pytest.mark.parametrize("name", ["tiny", "decode80b"])
-def test_device_generator_matches_host_generator(name):
+@pytest.mark.parametrize("name,bits", [("tiny", 4), ("decode80b", 4), ("tiny", 8), ("decode80b", 8)])
+def test_device_generator_matches_host_generator(name, bits):
     wl = synthetic.WORKLOADS[name]
     for layer, code in [(0, 0), (3, wl.E - 1), (1, synthetic.SHARED_EXPERT_CODE)]:
-        dev = [t[0].cpu().numpy() for t in W.device_triples(wl.seed, layer, code, 1, wl.H, wl.I)]
+        dev = [t[0].cpu().numpy() for t in W.device_triples(wl.seed, layer, code, 1, wl.H, wl.I, bits=bits)]
         host = synthetic.expert_triples(wl.seed, layer, None if code == synthetic.SHARED_EXPERT_CODE else code,
-                                        wl.H, wl.I).arrays()
+                                        wl.H, wl.I, bits=bits).arrays()
         for d, h in zip(dev, host):
             assert np.array_equal(d.view(h.dtype), h)
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode80b"])
-def test_device_pack_matches_host_pack(name):
+@pytest.mark.parametrize("name,bits", [("tiny", 4), ("decode80b", 4), ("tiny", 8), ("decode80b", 8)])
+def test_device_pack_matches_host_pack(name, bits):
     wl = synthetic.WORKLOADS[name]
-    shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I)
+    shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I, bits=bits)
     stride = smoe.layout_of(shape).blob_bytes
-    host = synthetic.expert_triples(wl.seed, 2, 5, wl.H, wl.I).arrays()
+    host = synthetic.expert_triples(wl.seed, 2, 5, wl.H, wl.I, bits=bits).arrays()
     hpool = np.zeros(2 * stride, np.uint8)
     smoe.pack_experts(shape, [host], [1], hpool, hpool.size, smoe.HOST)
     dev = [torch.from_numpy(a.view(np.int32 if a.dtype == np.uint32 else np.int16)).cuda() for a in host]

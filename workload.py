@@ -26,6 +26,8 @@ def synth_lib():
         L.synth_expert_triples.argtypes = [C.c_uint64, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int] + \
             [C.c_void_p] * 10
         L.synth_expert_triples.restype = C.c_int
+        L.synth_expert_triples_bits.argtypes = [C.c_uint64] + [C.c_int] * 6 + [C.c_void_p] * 10
+        L.synth_expert_triples_bits.restype = C.c_int
         _synth = L
     return _synth
 
@@ -38,15 +40,16 @@ def bits_of(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def device_triples(seed: int, layer: int, code0: int, n: int, H: int, I: int, stream=None):
+def device_triples(seed: int, layer: int, code0: int, n: int, H: int, I: int, stream=None, bits: int = 4):
     """Triples of n consecutive experts generated on the device: 9 tensors with
-    a leading expert dimension, in ExpertTriples order."""
+    a leading expert dimension, in ExpertTriples order (4-bit or 8-bit q)."""
     dev = torch.device("cuda")
-    shapes = [(I, H // 8), (I, H // 64), (I, H // 64)] * 2 + [(H, I // 8), (H, I // 64), (H, I // 64)]
+    per = 32 // bits
+    shapes = [(I, H // per), (I, H // 64), (I, H // 64)] * 2 + [(H, I // per), (H, I // 64), (H, I // 64)]
     dts = [torch.int32, torch.int16, torch.int16] * 3
     ts = [torch.empty((n,) + s, dtype=d, device=dev) for s, d in zip(shapes, dts)]
     st = torch.cuda.current_stream().cuda_stream if stream is None else stream.cuda_stream
-    rc = synth_lib().synth_expert_triples(seed, layer, code0, n, H, I, *[t.data_ptr() for t in ts], st)
+    rc = synth_lib().synth_expert_triples_bits(seed, layer, code0, n, H, I, bits, *[t.data_ptr() for t in ts], st)
     if rc != 0:
         raise RuntimeError("synth_expert_triples failed: %d" % rc)
     return ts
