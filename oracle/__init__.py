@@ -274,6 +274,25 @@ def combine8(x, ids, w, gate, experts: dict, shared, E: int, I: int, I_shared: i
                          E, I, I_shared)
 
 
+def combine_pool8(x, ids, w, gate, pool: np.ndarray, stride: int, n_slots: int, table_row: np.ndarray,
+                  shared_blob: np.ndarray, E: int, I: int):
+    """combine_pool() for 8-bit blobs: each named expert read from its slot's
+    blob bytes by the oracle's 8-bit reader, dequantised, then combine_dense."""
+    x = np.ascontiguousarray(x, np.uint16)
+    H = x.shape[1]
+
+    def dense_at(blob):
+        q = blob_to_mlx8(blob, H, I)
+        return dequant8(q[0], q[1], q[2]), dequant8(q[3], q[4], q[5]), dequant8(q[6], q[7], q[8])
+    dense = {}
+    for e in np.unique(ids):
+        slot = int(table_row[int(e)])
+        if not 0 <= slot < n_slots:
+            raise ValueError("oracle: invalid slot or expert id")
+        dense[int(e)] = dense_at(pool[slot * stride:(slot + 1) * stride])
+    return combine_dense(x, ids, w, gate, dense, dense_at(shared_blob), E, I, I)
+
+
 def blob_bytes8(H: int, I: int) -> int:
     return int(lib().orc_blob_bytes8(H, I))
 

@@ -190,3 +190,27 @@ def _mlx8_to_4(q8):
     v = np.stack([(q8 >> np.uint32(8 * j)) & np.uint32(15) for j in range(4)], axis=-1).reshape(q8.shape[0], -1)
     v = v.reshape(v.shape[0], -1, 8).astype(np.uint32)
     return sum(v[:, :, j] << np.uint32(4 * j) for j in range(8)).astype(np.uint32)
+
+
+def test_oracle_pool_path_8_bit_is_slot_permutation_invariant():
+    """Cache or disk, same answer, for 8-bit experts: read through any slot
+    permutation of an 8-bit pool (the library's packer, the oracle's reader),
+    the layer is bit-identical, and equal to the layer on the triples."""
+    wl = synthetic.WORKLOADS["tiny"]
+    shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I, bits=8)
+    stride = smoe.layout_of(shape).blob_bytes
+    x = synthetic.activations(wl.seed, wl.T, wl.H)
+    ids, w, gate = oracle.route(x, synthetic.router_weights(wl.seed, 0, wl.E, wl.H),
+                                synthetic.shared_gate_weights(wl.seed, 0, wl.H), wl.k)
+    trip = {e: synthetic.expert_triples(wl.seed, 0, e, wl.H, wl.I, bits=8) for e in range(wl.E)}
+    sh_t = synthetic.expert_triples(wl.seed, 0, None, wl.H, wl.I, bits=8)
+    direct, _ = oracle.combine8(x, ids, w, gate, trip, sh_t, wl.E, wl.I, wl.I)
+    shared = np.zeros(stride, np.uint8)
+    smoe.pack_experts(shape, [sh_t.arrays()], [0], shared, stride, smoe.HOST)
+    for seed in range(3):
+        table = np.random.default_rng(seed).permutation(2 * wl.E)[:wl.E].astype(np.int32)
+        pool = np.zeros(2 * wl.E * stride, np.uint8)
+        smoe.pack_experts(shape, [trip[e].arrays() for e in range(wl.E)], table.tolist(), pool, pool.size,
+                          smoe.HOST)
+        o64, _ = oracle.combine_pool8(x, ids, w, gate, pool, stride, 2 * wl.E, table, shared, wl.E, wl.I)
+        assert np.array_equal(o64, direct)
