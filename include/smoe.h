@@ -15,8 +15,9 @@
  *
  * The routed and shared experts hold MLX-style affine 4-bit weights: groups of
  * 64 along the input dimension, an fp16 scale s and bias b per group,
- * w = s*q + b (same xix.ai page, last paragraph: "MLX-style int4/int8 group
- * quantisation ... 64-bit offsets"). The routed experts of every layer live in
+ * w = s*q + b (the same xix.ai page, last paragraph, names MLX-style int4 and
+ * int8 group quantisation with 64-bit offsets). 8-bit experts are supported
+ * for packing, routing and the plain debug path (see smoe_ctx_create). The routed experts of every layer live in
  * one pool of fixed-stride blobs, one blob per expert, reached through a slot
  * table (same page, paragraph on how it works: fixed-stride blobs, one read
  * per expert, a bounded slot pool).
