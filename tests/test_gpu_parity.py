@@ -18,6 +18,7 @@ import int4_routed_expert_router_gb300 as smoe
 import oracle
 import synthetic
 import workload as W
+import oracle_shards
 
 pytestmark = pytest.mark.gpu
 
@@ -33,30 +34,44 @@ def built():
 # ------------------------------------------------------------------ helpers
 
 def routing_ok(ids_g, w_g, gate_g, ref, k, atol_w=2e-5, atol_gate=1e-5, gap=1e-4):
-    """Returns the tokens whose expert set matches the oracle's; asserts the
-    rule on every token where the oracle's decision is not a near-tie (the
-    probabilities differ by more than `gap`)."""
+    """Asserts the routing rule on every token and returns the oracle's
+    weights of the GPU's own choice, [T][k] fp64.
+
+    With p the oracle's probabilities, p_(k) and p_(k+1) its k-th and
+    (k+1)-th largest: the GPU's k ids are distinct, every chosen expert has
+    p >= p_(k) - gap and every other one p <= p_(k+1) + gap (so where the
+    two differ by more than gap the set is the oracle's exactly, and inside a
+    near-tie the choice is still a valid top-k); the ids come in descending p
+    within gap, and each position whose neighbours in the oracle's order
+    differ by more than gap holds the oracle's id. The GPU's weights equal
+    the renormalised oracle probabilities of its own choice within atol_w,
+    and the gate the oracle's within atol_gate."""
     probs = ref["probs"]
-    same = []
-    for t in range(ids_g.shape[0]):
+    T, E = probs.shape
+    assert ids_g.shape == (T, k)
+    w_own = oracle_shards.own_choice_weights(probs, np.clip(ids_g, 0, E - 1))
+    for t in range(T):
         p = probs[t]
-        order = np.argsort(-p, kind="stable")
-        ps = p[order]
-        gap_k = ps[k - 1] - ps[k] if k < len(p) else np.inf
-        if gap_k > gap:
-            assert set(ids_g[t].tolist()) == set(ref["ids"][t].tolist()), (t, ids_g[t], ref["ids"][t])
+        chosen = ids_g[t].astype(np.int64)
+        assert np.all((chosen >= 0) & (chosen < E)) and len(set(chosen.tolist())) == k, (t, chosen)
+        ps = np.sort(p)[::-1]
+        pk, pk1 = ps[k - 1], (ps[k] if k < E else -np.inf)
+        assert np.all(p[chosen] >= pk - gap), (t, chosen, p[chosen], pk)
+        others = np.ones(E, bool)
+        others[chosen] = False
+        if others.any():
+            assert p[others].max() <= pk1 + gap, (t, p[others].max(), pk1)
+        assert np.all(p[chosen][:-1] >= p[chosen][1:] - gap), (t, chosen)
+        if pk - pk1 > gap:
+            assert set(chosen.tolist()) == set(ref["ids"][t].tolist()), (t, chosen, ref["ids"][t])
         for j in range(k):
-            lo = ps[j] - ps[j + 1] if j + 1 < len(p) else np.inf
+            lo = ps[j] - ps[j + 1] if j + 1 < E else np.inf
             hi = ps[j - 1] - ps[j] if j > 0 else np.inf
             if lo > gap and hi > gap:
-                assert ids_g[t, j] == ref["ids"][t, j], (t, j)
-        if set(ids_g[t].tolist()) == set(ref["ids"][t].tolist()):
-            same.append(t)
-            pos = {e: j for j, e in enumerate(ref["ids"][t].tolist())}
-            for j, e in enumerate(ids_g[t].tolist()):
-                assert abs(w_g[t, j] - ref["w"][t, pos[e]]) <= atol_w, (t, j)
-        assert abs(gate_g[t] - ref["gate"][t]) <= atol_gate
-    return same
+                assert chosen[j] == ref["ids"][t, j], (t, j)
+        assert np.all(np.abs(w_g[t] - w_own[t]) <= atol_w), (t, w_g[t], w_own[t])
+        assert abs(gate_g[t] - ref["gate"][t]) <= atol_gate, (t, gate_g[t], ref["gate"][t])
+    return w_own
 
 
 def assert_output_close(gpu_bits, out64, ref_bf16=None, exact_frac=None):
@@ -72,19 +87,40 @@ def assert_output_close(gpu_bits, out64, ref_bf16=None, exact_frac=None):
     return rel
 
 
-def check_layer_on_own_input(wl, layer, x_bits, got_bits, ids, w, gate, inp):
-    """One layer of a GPU chain against the oracle run on the GPU's own input
-    to that layer: the routing rule with the layer margins, then, when the
-    expert set agrees, the output (residual included) within the layer
-    tolerance. Returns whether the output was compared (an exact near-tie can
-    legitimately pick a different set)."""
-    ref = oracle_layer(wl, layer, x_bits, inp)
-    same = routing_ok(ids, w, gate, ref, wl.k)
-    if not same:
-        return False
+def assert_residual_close(got_bits, x_bits, y64):
+    """A layer with the residual fused, got = bf16(x + y_gpu), against the
+    oracle's layer output y64 on the same x: the layer tolerance on x + y64
+    as a whole (relative L2 <= 5e-3, max abs <= 2e-2 rms), and per element
+    |got - (x + y64)| <= half a bf16 unit of the larger of the two values
+    (the output rounding) + 2e-2 rms(y64) (the layer tolerance on the layer
+    output alone)."""
     xr = synthetic.bf16_bits_to_f32(x_bits).astype(np.float64)
-    assert_output_close(got_bits, xr + ref["out64"])
-    return True
+    want = xr + y64
+    assert_output_close(got_bits, want)
+    g = synthetic.bf16_bits_to_f32(got_bits).astype(np.float64)
+    big = np.maximum(np.maximum(np.abs(want), np.abs(g)), 1e-30)
+    bound = 2.0 ** (np.floor(np.log2(big)) - 8) * (1 + 1e-9) + 2e-2 * np.sqrt(np.mean(y64 ** 2))
+    assert np.all(np.abs(g - want) <= bound), np.abs(g - want).max()
+
+
+def own_input_pieces(wl, layers, xs_bits, ids, inp):
+    """Work pieces for the oracle on the GPU's own input of each listed layer
+    and the GPU's own choice of experts there."""
+    return [(wl.name, l, xs_bits[i], ids[i], inp.Wr_bits[l], inp.ws_bits[l], inp.bias_np)
+            for i, l in enumerate(layers)]
+
+
+def check_chain_layers_on_own_input(wl, layers, xs_bits, ys_bits, ids, w, gate, inp):
+    """Every layer of a GPU chain held to the flat per-layer rule on its own
+    input: the oracle routes the GPU's input x_l to that layer (routing rule
+    with the layer margins) and combines the GPU's own choice of experts;
+    the GPU's x_{l+1} = bf16(x_l + y_l) must meet assert_residual_close.
+    xs_bits / ys_bits: per listed layer the [1][H] input and output bits;
+    ids, w, gate: per listed layer the GPU's [1][k], [1][k], [1]."""
+    refs = oracle_shards.run_pieces(own_input_pieces(wl, layers, xs_bits, ids, inp))
+    for i, ref in enumerate(refs):
+        routing_ok(ids[i], w[i], gate[i], ref, wl.k)
+        assert_residual_close(ys_bits[i], xs_bits[i], ref["out64"])
 
 
 def gpu_route(pool, inp, layer, x_bits):
@@ -173,23 +209,31 @@ def p80():
 
 @pytest.mark.parametrize("T", [1, 3, 4, 8, 64, 200])
 def test_route_tiny(tiny, T):
+    """16 experts, 4 chosen: near-ties are common, so the validity rule and
+    the output of the GPU's own choice are both exercised on every token."""
     pool, inp = tiny
-    x = synthetic.activations(pool.wl.seed, T, pool.wl.H, tag=T)
-    ref = oracle_layer(pool.wl, 0, x, inp)
+    wl = pool.wl
+    x = synthetic.activations(wl.seed, T, wl.H, tag=T)
     ids, w, gate = gpu_route(pool, inp, 0, x)
-    routing_ok(ids, w, gate, ref, pool.wl.k)
+    ref = oracle_shards.layer_piece((wl.name, 0, x, ids, inp.Wr_bits[0], inp.ws_bits[0], inp.bias_np))
+    routing_ok(ids, w, gate, ref, wl.k)
+    assert_output_close(gpu_forward(pool, 0, x, ids, w, gate), ref["out64"])
 
 
 @pytest.mark.parametrize("which,T", [("p35", 1), ("p80", 1), ("p80", 8), ("p80", 64)])
-def test_route_full_size(which, T, request):
+def test_route_and_forward_full_size(which, T, request):
+    """moe_route then moe_forward on the GPU's own routing, every token
+    checked: the routing rule (near-ties included: a valid top-k and the
+    weights of the GPU's own choice), and the output against the oracle's
+    combine of that same choice (T = 64 runs on the token-bucketed path)."""
     pool, inp = request.getfixturevalue(which)
     wl = pool.wl
     x = synthetic.activations(wl.seed, T, wl.H, tag=100 + T)
-    r = oracle.route(x, inp.Wr_bits[3], inp.ws_bits[3], wl.k, want_probs=True)
-    ref = dict(ids=r[0], w=r[1], gate=r[2], probs=r[3])
     ids, w, gate = gpu_route(pool, inp, 3, x)
-    same = routing_ok(ids, w, gate, ref, wl.k)
-    assert len(same) >= T - max(1, T // 20)
+    ref = oracle_shards.tokens_sharded(wl.name, 3, x, ids, inp.Wr_bits[3], inp.ws_bits[3], inp.bias_np)
+    routing_ok(ids, w, gate, ref, wl.k)
+    out = gpu_forward(pool, 3, x, ids, w, gate)
+    assert_output_close(out, ref["out64"])
 
 
 def test_route_zipf_t64():
@@ -245,26 +289,64 @@ def test_forward_residual_fused(tiny):
     assert_output_close(out, xr + ref["out64"], want, exact_frac=0.95)
 
 
+def check_chain(wl, inp, x0, xs_bits, ids, w, gate, first=0):
+    """A GPU chain of layers first .. first + n - 1 (xs_bits [n + 1][H]: the
+    input, then each layer's output x_{l+1} = bf16(x_l + y_l); ids, w [n][k],
+    gate [n]) against the oracle, in two ways.
+
+    1. Every layer on its own input, with the flat per-layer rule
+       (check_chain_layers_on_own_input): no layer escapes the layer
+       tolerance, wherever the two chains have drifted to.
+    2. The chain against the oracle's own chain from the same x0. Layer 0 sees
+       identical inputs and gets the layer tolerance (and >= 95% of the bf16
+       roundings). Deeper layers compare two chains that each round
+       x_{l+1} to bf16: where the two pre-rounding values straddle a rounding
+       boundary the chains differ by one bf16 unit, which then rides the
+       residual stream and moves the next router inputs. So layer l > 0 gets
+       the routing rule with a 1e-3 near-tie margin and weights and gate
+       within 2e-3 sqrt(l + 1); relative L2 of the stream <= 5e-3 sqrt(l + 1)
+       (independent per-layer disagreements add in quadrature); and per
+       element |gpu - oracle| <= the sum over the layers so far of one bf16
+       unit (of the larger binade of the two values at that layer) +
+       2e-2 rms(y). The comparison stops where the two chains pick different
+       experts inside the margin (both choices valid, the chains legitimately
+       part); part 1 has then already held every layer on its own input.
+    Returns the number of layers compared in part 2."""
+    n = ids.shape[0]
+    layers = list(range(first, first + n))
+    check_chain_layers_on_own_input(wl, layers, [xs_bits[i:i + 1] for i in range(n)],
+                                    [xs_bits[i + 1:i + 2] for i in range(n)], [ids[i:i + 1] for i in range(n)],
+                                    [w[i:i + 1] for i in range(n)], [gate[i:i + 1] for i in range(n)], inp)
+    x = x0
+    bound = np.zeros((1, wl.H))
+    for i, l in enumerate(layers):
+        ref = oracle_layer(wl, l, x, inp)
+        c = np.sqrt(i + 1)
+        tol = (2e-5, 1e-5, 1e-4) if i == 0 else (2e-3 * c, 2e-3 * c, 1e-3)
+        routing_ok(ids[i:i + 1], w[i:i + 1], gate[i:i + 1], ref, wl.k, *tol)
+        if set(ids[i].tolist()) != set(ref["ids"][0].tolist()):
+            return i                       # a near-tie: the chains part here
+        xr = synthetic.bf16_bits_to_f32(x).astype(np.float64)
+        want = oracle.residual(x, ref["out64"])
+        got = xs_bits[i + 1:i + 2]
+        g = synthetic.bf16_bits_to_f32(got).astype(np.float64)
+        o = synthetic.bf16_bits_to_f32(want).astype(np.float64)
+        big = np.maximum(np.maximum(np.abs(o), np.abs(g)), 1e-30)
+        bound += 2.0 ** (np.floor(np.log2(big)) - 7) + 2e-2 * np.sqrt(np.mean(ref["out64"] ** 2))
+        if i == 0:
+            assert_output_close(got, xr + ref["out64"], want, exact_frac=0.95)
+        else:
+            assert np.linalg.norm(g - o) <= 5e-3 * c * np.linalg.norm(o)
+            assert np.all(np.abs(g - o) <= bound)
+        x = want                      # continue the oracle's own chain
+    return n
+
+
 @pytest.mark.parametrize("which", ["p35", "p80"])
 def test_full_stack_in_cuda_graph(which, request):
     """The whole decode step (all layers, route + forward, residual chained) as
-    the benchmark runs it: captured in one CUDA graph and replayed.
-
-    Layer 0 sees identical inputs on both sides and gets the layer tolerance.
-    Deeper layers compare two chains: each side rounds x_{l+1} = x_l + y_l to
-    bf16, and where the two pre-rounding values straddle a rounding boundary
-    the chains differ by one bf16 unit, which then rides the residual stream.
-    So layer l > 0 gets: the routing rule with a 1e-3 near-tie margin (weights
-    and gate within 2e-3 sqrt(l + 1), since the router inputs drift apart by
-    such units layer after layer),
-    relative L2 of the stream <= 5e-3 sqrt(l + 1) (independent per-layer
-    disagreements add in quadrature), and
-    per element |gpu - oracle| <= the sum over layers so far of one bf16 unit
-    (of the larger binade of the two values at that layer) + 2e-2 rms(y).
-    Where the chains reach a near-tie and route differently, that layer and
-    every later one is checked on the GPU's own input to it (the oracle run on
-    the same bits, layer tolerance); at least half the layers must have had
-    their outputs compared."""
+    the benchmark's per-layer path runs it: captured in one CUDA graph and
+    replayed, then checked with check_chain."""
     pool, inp = request.getfixturevalue(which)
     wl = pool.wl
     st = W.Stack(pool, inp, 1)
@@ -274,43 +356,12 @@ def test_full_stack_in_cuda_graph(which, request):
     st.graph.replay()
     torch.cuda.synchronize()
     assert smoe.check(st.err) == 0
-    x = x0
-    bound = np.zeros((1, wl.H))
-    anchored, compared = False, 0      # after a near-tie: each layer on the GPU's own input
-    for l in range(pool.n_layers):
-        ids = st.ids[l].cpu().numpy()
-        if anchored:
-            compared += check_layer_on_own_input(wl, l, W.bits_of(st.xs[l]), W.bits_of(st.xs[l + 1]), ids,
-                                                 st.w[l].cpu().numpy(), st.gate[l].cpu().numpy(), inp)
-            continue
-        ref = oracle_layer(wl, l, x, inp)
-        # past layer 0 the router inputs differ by bf16 units: probabilities move
-        # by ~1e-4, so near-ties are judged with a 1e-3 margin there
-        c = np.sqrt(l + 1)
-        tol = (2e-5, 1e-5, 1e-4) if l == 0 else (2e-3 * c, 2e-3 * c, 1e-3)
-        same = routing_ok(ids, st.w[l].cpu().numpy(), st.gate[l].cpu().numpy(), ref, wl.k, *tol)
-        if not same:
-            # a near-tie: the two chains legitimately route differently from here
-            # on, so this and every later layer is checked on the GPU's own input
-            compared += check_layer_on_own_input(wl, l, W.bits_of(st.xs[l]), W.bits_of(st.xs[l + 1]), ids,
-                                                 st.w[l].cpu().numpy(), st.gate[l].cpu().numpy(), inp)
-            anchored = True
-            continue
-        xr = synthetic.bf16_bits_to_f32(x).astype(np.float64)
-        want = oracle.residual(x, ref["out64"])
-        got = W.bits_of(st.xs[l + 1])
-        g = synthetic.bf16_bits_to_f32(got).astype(np.float64)
-        o = synthetic.bf16_bits_to_f32(want).astype(np.float64)
-        big = np.maximum(np.maximum(np.abs(o), np.abs(g)), 1e-30)
-        bound += 2.0 ** (np.floor(np.log2(big)) - 7) + 2e-2 * np.sqrt(np.mean(ref["out64"] ** 2))
-        if l == 0:
-            assert_output_close(got, xr + ref["out64"], want, exact_frac=0.95)
-        else:
-            assert np.linalg.norm(g - o) <= 5e-3 * np.sqrt(l + 1) * np.linalg.norm(o)
-            assert np.all(np.abs(g - o) <= bound)
-        compared += 1
-        x = want                      # continue the oracle's own chain
-    assert compared >= pool.n_layers // 2, compared
+    L = pool.n_layers
+    xs = np.concatenate([W.bits_of(st.xs[l]) for l in range(L + 1)])
+    ids = np.concatenate([st.ids[l].cpu().numpy() for l in range(L)])
+    w = np.concatenate([st.w[l].cpu().numpy() for l in range(L)])
+    gate = np.concatenate([st.gate[l].cpu().numpy() for l in range(L)])
+    check_chain(wl, inp, x0, xs, ids, w, gate)
 
 
 # ----------------------------------------------- determinism and slot placement

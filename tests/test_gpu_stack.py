@@ -11,8 +11,7 @@ import int4_routed_expert_router_gb300 as smoe
 import oracle
 import synthetic
 import workload as W
-from test_gpu_parity import (assert_output_close, check_layer_on_own_input, gpu_forward, gpu_route, oracle_layer,
-                             routing_ok)
+from test_gpu_parity import assert_output_close, check_chain, gpu_forward, gpu_route
 
 pytestmark = pytest.mark.gpu
 
@@ -51,52 +50,6 @@ def run_stack(pool, inp, x0_bits, first=0, n=None, err=None):
     return xs, ids, w, gate, err
 
 
-def check_chain(pool, inp, x0, xs, ids, w, gate, first=0):
-    """The stack against the oracle's own chain, with the bounds of the
-    per-layer graph test: layer 0 the layer tolerance; later layers a 1e-3
-    near-tie margin, relative L2 <= 5e-3 sqrt(l + 1) and a per-element bound
-    that adds one bf16 unit per layer (the two chains round independently).
-    After a near-tie that sends the chains to different experts, each layer is
-    checked on the GPU's own input to it instead."""
-    wl = pool.wl
-    x = x0
-    bound = np.zeros((1, wl.H))
-    anchored, compared = False, 0      # after a near-tie: each layer on the GPU's own input
-    for i in range(ids.shape[0]):
-        l = first + i
-        args = (W.bits_of(xs[i:i + 1]), W.bits_of(xs[i + 1:i + 2]), ids[i:i + 1].cpu().numpy(),
-                w[i:i + 1].cpu().numpy(), gate[i:i + 1].cpu().numpy(), inp)
-        if anchored:
-            compared += check_layer_on_own_input(wl, l, *args)
-            continue
-        ref = oracle_layer(wl, l, x, inp)
-        c = np.sqrt(i + 1)
-        tol = (2e-5, 1e-5, 1e-4) if i == 0 else (2e-3 * c, 2e-3 * c, 1e-3)
-        same = routing_ok(ids[i:i + 1].cpu().numpy(), w[i:i + 1].cpu().numpy(), gate[i:i + 1].cpu().numpy(), ref,
-                          wl.k, *tol)
-        if not same:
-            # a near-tie: the two chains legitimately route differently from here
-            # on, so this and every later layer is checked on the GPU's own input
-            compared += check_layer_on_own_input(wl, l, *args)
-            anchored = True
-            continue
-        xr = synthetic.bf16_bits_to_f32(x).astype(np.float64)
-        want = oracle.residual(x, ref["out64"])
-        got = W.bits_of(xs[i + 1:i + 2])
-        g = synthetic.bf16_bits_to_f32(got).astype(np.float64)
-        o = synthetic.bf16_bits_to_f32(want).astype(np.float64)
-        big = np.maximum(np.maximum(np.abs(o), np.abs(g)), 1e-30)
-        bound += 2.0 ** (np.floor(np.log2(big)) - 7) + 2e-2 * np.sqrt(np.mean(ref["out64"] ** 2))
-        if i == 0:
-            assert_output_close(got, xr + ref["out64"], want, exact_frac=0.95)
-        else:
-            assert np.linalg.norm(g - o) <= 5e-3 * np.sqrt(i + 1) * np.linalg.norm(o)
-            assert np.all(np.abs(g - o) <= bound)
-        compared += 1
-        x = want
-    assert compared >= ids.shape[0] // 2, compared
-
-
 @pytest.mark.parametrize("name,n_layers,first", [("tiny", 3, 0), ("decode35b", 6, 0), ("decode80b", 6, 2)])
 def test_stack_against_oracle_chain(name, n_layers, first):
     pool, inp = make(name, n_layers)
@@ -104,7 +57,7 @@ def test_stack_against_oracle_chain(name, n_layers, first):
     x0 = synthetic.activations(wl.seed, 1, wl.H, tag=4242 + first)
     xs, ids, w, gate, err = run_stack(pool, inp, x0, first=first)
     assert smoe.check(err) == 0
-    check_chain(pool, inp, x0, xs, ids, w, gate, first=first)
+    check_chain(wl, inp, x0, W.bits_of(xs), ids.cpu().numpy(), w.cpu().numpy(), gate.cpu().numpy(), first=first)
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode80b"])
