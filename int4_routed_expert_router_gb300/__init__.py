@@ -150,7 +150,9 @@ def _stream(stream) -> int | None:
 
 
 def make_shape(H, E, k, I, I_shared=None, bits=4) -> Shape:
-    """bits = 8: the 8-bit format, for layout_of and host packing only."""
+    """bits = 8: MLX's 8-bit format, for the layout, host and device packing,
+    routing and moe_forward_debug; the fast expert kernels (moe_forward,
+    moe_forward_noalloc, moe_decode_stack) return ENOTSUP for it."""
     return Shape(H, E, k, I, I if I_shared is None else I_shared, 64, bits)
 
 

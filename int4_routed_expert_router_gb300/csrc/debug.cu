@@ -134,6 +134,8 @@ extern "C" int moe_forward_debug(const smoe_ctx *ctx, int32_t layer, const uint1
     if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
     if (T == 0) return SMOE_OK;                      // nothing to do; the buffers may be null
     if (!x || !ids || !w || !gate || !pool || !shared_blob || !out || !err) return SMOE_EINVAL;
+    auto a16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+    if (!a16(x) || !a16(pool) || !a16(shared_blob) || !a16(out) || (residual && !a16(residual))) return SMOE_EINVAL;
     if (pool_bytes < uint64_t(ctx->n_slots) * ctx->layout.blob) return SMOE_ENOMEM;
     DebugParams p = {};
     p.x = x;

@@ -60,7 +60,9 @@ extern "C" int moe_forward_noalloc(const smoe_ctx *ctx, int32_t layer, const uin
     if (T == 0) return SMOE_OK;                      // nothing to do; the buffers may be null
     if (!x || !ids || !w || !gate || !pool || !shared_blob || !out || !err) return SMOE_EINVAL;
     if (T > kDecodeMaxT) return SMOE_ENOTSUP;
-    if (!aligned16(x) || !aligned16(pool) || !aligned16(shared_blob)) return SMOE_EINVAL;
+    if (!aligned16(x) || !aligned16(pool) || !aligned16(shared_blob) || !aligned16(out) ||
+        (residual && !aligned16(residual)))
+        return SMOE_EINVAL;
     if (pool_bytes < uint64_t(ctx->n_slots) * ctx->layout.blob) return SMOE_ENOMEM;
     const smoe_shape &s = ctx->shape;
     const uint64_t umax = uint64_t(s.E < T * s.k ? s.E : T * s.k) + 1;

@@ -309,9 +309,16 @@ extern "C" int pack_experts(const smoe_shape *shape, const smoe_expert_src *src,
     if (where != SMOE_HOST && where != SMOE_DEVICE) return SMOE_EINVAL;
     const bool b8 = shape->bits == 8;
     const Layout L = b8 ? layout8_of(shape->H, shape->I) : layout_of(shape->H, shape->I);
+    // the device packer stores 16-byte lanes at pool + slot * stride (the stride is a
+    // whole number of 16-byte lanes); both packers read q as uint32 and s, b as fp16
+    if (where == SMOE_DEVICE && (reinterpret_cast<uintptr_t>(pool) & 15)) return SMOE_EINVAL;
     for (int i = 0; i < n; ++i) {
-        for (int m = 0; m < 3; ++m)
+        for (int m = 0; m < 3; ++m) {
             if (!src[i].q[m] || !src[i].s[m] || !src[i].b[m]) return SMOE_EINVAL;
+            if ((reinterpret_cast<uintptr_t>(src[i].q[m]) & 3) || (reinterpret_cast<uintptr_t>(src[i].s[m]) & 1) ||
+                (reinterpret_cast<uintptr_t>(src[i].b[m]) & 1))
+                return SMOE_EINVAL;
+        }
         if (dst_slots[i] < 0) return SMOE_ERANGE;
         const uint64_t end = (uint64_t(dst_slots[i]) + 1) * L.blob;
         if (end / L.blob != uint64_t(dst_slots[i]) + 1 || end > pool_bytes) return SMOE_ENOMEM;

@@ -214,3 +214,28 @@ def test_oracle_pool_path_8_bit_is_slot_permutation_invariant():
                           smoe.HOST)
         o64, _ = oracle.combine_pool8(x, ids, w, gate, pool, stride, 2 * wl.E, table, shared, wl.E, wl.I)
         assert np.array_equal(o64, direct)
+
+
+def test_pack_refuses_misaligned_buffers_before_any_work():
+    """A device pool that does not start on a 16-byte boundary (say an offset
+    view of a buffer) is refused with EINVAL before any copy or launch, as
+    are q words not on a 4-byte and s/b not on a 2-byte boundary (host or
+    device). The addresses are never dereferenced: the check comes first."""
+    wl = synthetic.WORKLOADS["tiny"]
+    shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I)
+    stride = smoe.layout_of(shape).blob_bytes
+    L = smoe.lib()
+
+    def call(pool_addr, q_off=0, s_off=0, where=smoe.DEVICE):
+        src = smoe.ExpertSrc()
+        for m in range(3):
+            src.q[m] = 0x100000 + 0x1000 * m + q_off
+            src.s[m] = 0x200000 + 0x1000 * m + s_off
+            src.b[m] = 0x300000 + 0x1000 * m
+        slots = (C.c_int64 * 1)(0)
+        return L.pack_experts(C.byref(shape), C.byref(src), 1, slots, pool_addr, 4 * stride, where, None)
+
+    assert call(0x400008) == smoe.EINVAL                    # device pool 8 bytes past a boundary
+    assert call(0x400010, q_off=2) == smoe.EINVAL           # q words not 4-byte aligned
+    assert call(0x400010, s_off=1) == smoe.EINVAL           # fp16 scales at an odd address
+    assert call(0x400010, q_off=2, where=smoe.HOST) == smoe.EINVAL

@@ -116,3 +116,35 @@ def test_debug_path_bad_slot_sets_error_word():
     finally:
         pool.table_dev[0, e] = saved
         torch.cuda.synchronize()
+
+
+def test_misaligned_buffers_are_refused_without_a_launch():
+    """An offset view (pool[8:], a shared blob or output 2 bytes in) is
+    contiguous and passes the binding, but the library refuses it with
+    EINVAL: the kernels read 16-byte lanes and 4-byte words. Checked through
+    the raw C ABI for moe_forward_debug and for device packing."""
+    wl = synthetic.WORKLOADS["tiny"]
+    pool, inp = W.DevicePool(wl, n_layers=1), W.LayerInputs(wl, 1)
+    T = 2
+    x = W.bf16_tensor(synthetic.activations(wl.seed, T, wl.H, tag=5))
+    ids = torch.zeros((T, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, wl.k), dtype=torch.float32, device="cuda")
+    gate = torch.zeros((T,), dtype=torch.float32, device="cuda")
+    out = torch.zeros((T * wl.H + 8,), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L, p = smoe.lib(), smoe._ptr
+    nbytes = pool.pool.numel()
+
+    def dbg(pool_p, shared_p, out_p):
+        return L.moe_forward_debug(pool.ctx.handle, 0, p(x), T, p(ids), p(w), p(gate), pool_p, nbytes, shared_p,
+                                   None, out_p, p(err), None)
+    assert dbg(p(pool.pool) + 8, p(pool.shared[0]), p(out)) == smoe.EINVAL
+    assert dbg(p(pool.pool), p(pool.shared[0]) + 4, p(out)) == smoe.EINVAL
+    assert dbg(p(pool.pool), p(pool.shared[0]), p(out) + 2) == smoe.EINVAL
+    shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I)
+    dev = [t[0] for t in W.device_triples(wl.seed, 0, 1, 1, wl.H, wl.I)]
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.pack_experts(shape, [dev], [0], pool.pool[8:], nbytes - 8, smoe.DEVICE)
+    assert ei.value.status == smoe.EINVAL
+    torch.cuda.synchronize()
+    assert smoe.check(err) == 0

@@ -83,3 +83,25 @@ def test_noalloc_rejects_calls_larger_than_its_scratch():
     with pytest.raises(smoe.SmoeError) as ei:
         smoe.moe_forward_noalloc(ctx, 0, x9, ids9, w9, gate9, pool, pool, out9, err)
     assert ei.value.status == smoe.ENOTSUP
+
+
+def test_noalloc_refuses_misaligned_output_or_residual():
+    """Like moe_forward, the output and the residual must start on a 16-byte
+    boundary; an offset view is refused with EINVAL before any launch."""
+    wl = synthetic.WORKLOADS["tiny"]
+    pool = W.DevicePool(wl, n_layers=1)
+    inp = W.LayerInputs(wl, 1)
+    T = 2
+    x, ids, w, gate = _inputs(pool, inp, T, tag=990)
+    out = torch.zeros((T * wl.H + 8,), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L, p = smoe.lib(), smoe._ptr
+    n = pool.pool.numel()
+    rc = L.moe_forward_noalloc(pool.ctx.handle, 0, p(x), T, p(ids), p(w), p(gate), p(pool.pool), n,
+                               p(pool.shared[0]), None, p(out) + 2, p(err), None)
+    assert rc == smoe.EINVAL
+    rc = L.moe_forward_noalloc(pool.ctx.handle, 0, p(x), T, p(ids), p(w), p(gate), p(pool.pool), n,
+                               p(pool.shared[0]), p(out) + 2, p(out), p(err), None)
+    assert rc == smoe.EINVAL
+    torch.cuda.synchronize()
+    assert smoe.check(err) == 0
