@@ -1,15 +1,20 @@
 #!/usr/bin/env python
 """Benchmark of the int4 routed-expert MoE layer on GB300.
 
-A step is one pass of the whole hot path over one batch: for the default
-workload (35B-A3B-shaped decode, T=1, a stack of 40 independent layers),
-per layer the router (moe_route) and the fused expert kernel (moe_forward,
-residual fused), all layers captured in one CUDA graph and replayed.
+A step is one pass of the whole hot path over one batch. For the default
+workload (Qwen3-Next-80B-A3B-shaped decode: H=2048, 10 of 512 experts, T=1,
+a stack of 48 independent layers, slot table a random permutation) a step is
+one moe_decode_stack launch (router, top-k, experts and the weighted combine
+of all 48 layers, residual chained), captured in a CUDA graph and replayed.
 
 Prints one JSON line. value = MoE-layer tokens/s = T * layers * steps / time
-(whole job: summed over ranks). The expert pool (18 GB at this shape) is far
-larger than the 129 MB L2 and each step streams 637 MB of distinct expert
-blobs, so no L2 flush is needed between steps.
+(whole job: summed over ranks). The expert pool (43.5 GB at this shape) is far
+larger than the 129 MB L2 and each step streams 934 MB of distinct expert
+blobs, so no L2 flush is needed between steps. After the headline the other
+target configurations (--extra: T=8192 prefill, Zipf-skewed T=64, 35B-shaped
+decode) are measured the same way and reported under "configs" in the same
+line; a configuration whose distinct blobs fit twice in L2 is timed step by
+step with a 256 MB write between steps.
 
 --impl reference times the CPU oracle (oracle/, one thread) on the same
 workload and metric, each step one layer for one token.
@@ -45,7 +50,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode35b")
+    ap.add_argument("--workload", default="decode80b")
+    ap.add_argument("--extra", default="prefill80b,zipf80b_t64,decode35b",
+                    help="comma-separated workloads measured after the headline, as sub-records of the same "
+                         "line (N = 1 only; empty: none)")
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (profiling of small cases)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -318,7 +326,12 @@ def run_reference(args, wl, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, wl, world, rank, dist):
+def measure(args, wl, dev, dist=None, e2e=False, cached_pool=None):
+    """Builds the workload on the device, captures one step in a CUDA graph
+    and times it: K replays after W warm-up replays (bracketed by a barrier
+    and synchronize), the dominant kernel(s) by event nodes inside an
+    instrumented copy of the graph, and optionally end to end (x from pinned
+    host memory, the step, the result back). Returns a dict of raw figures."""
     import numpy as np
     import torch
 
@@ -326,8 +339,6 @@ def run_ours(args, wl, world, rank, dist):
     import synthetic
     import workload as W
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
-    torch.cuda.set_device(dev)
     pool = W.DevicePool(wl)
     inp = W.LayerInputs(wl, wl.n_layers)
     # one-token steps run as one moe_decode_stack launch when the GPU supports it
@@ -344,7 +355,8 @@ def run_ours(args, wl, world, rank, dist):
         raise RuntimeError("device error word set during warm-up")
 
     # distinct expert blobs per step (the routing is the same every replay)
-    blobs = sum(len(np.unique(st.ids[l].cpu().numpy())) + 1 for l in range(wl.n_layers))
+    uniq = [len(np.unique((st.ids[l] if not stacked else st.ids[l]).cpu().numpy())) for l in range(wl.n_layers)]
+    blobs = sum(u + 1 for u in uniq)
     flush = blobs * int(pool.layout.blob_bytes) < 2 * L2_BYTES
 
     # ---- timed region: K replays of the whole step (each bracketed by its own
@@ -365,6 +377,7 @@ def run_ours(args, wl, world, rank, dist):
             b.record(stream)
         torch.cuda.synchronize()
         ms = float(sum(a.elapsed_time(b) for a, b in evs_t))
+        del scratch
     else:
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
@@ -379,8 +392,6 @@ def run_ours(args, wl, world, rank, dist):
     ms = max_over_ranks(ms, dist, dev)
     if smoe.check(st.err) != 0:
         raise RuntimeError("device error word set during the timed region")
-    step_s = ms / 1e3 / args.steps
-    value = world * wl.T * wl.n_layers / step_s
 
     # ---- the dominant kernel, bracketed by event nodes that the library's
     # profiling hook records inside an instrumented copy of the graph
@@ -397,7 +408,10 @@ def run_ours(args, wl, world, rank, dist):
         gi = st.capture(prof_events=evs[0] if stacked else evs)
         reps = max(3, min(args.steps, 100))
         tot, tot_down = [], []
+        scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
         for _ in range(reps):
+            if scratch is not None:
+                scratch.fill_(1)
             gi.replay()
             torch.cuda.synchronize()
             tot.extend(row[0].elapsed_time(row[1]) for row in evs)
@@ -405,71 +419,147 @@ def run_ours(args, wl, world, rank, dist):
                 tot_down.extend(row[1].elapsed_time(row[2]) for row in evs)
         kern_ms = float(np.mean(tot))
         down_ms = float(np.mean(tot_down)) if prefill else None
+        del gi, scratch
     except Exception as e:                               # noqa: BLE001
         print("kernel timing unavailable: %r" % (e,), file=sys.stderr)
 
+    out = dict(ms=ms, stacked=stacked, prefill=prefill, kern_ms=kern_ms, down_ms=down_ms, uniq=uniq, blobs=blobs,
+               flush=flush, blob=int(pool.layout.blob_bytes), clocks=sampler.summary())
+
     # ---- end to end: x from pinned host memory, the step, the result back
-    xh = torch.from_numpy(x0.view(np.int16)).view(torch.bfloat16).pin_memory()
-    oh = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if e2e:
+        xh = torch.from_numpy(x0.view(np.int16)).view(torch.bfloat16).pin_memory()
+        oh = torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            st.xs[0].copy_(xh, non_blocking=True)
+            g.replay()
+            oh.copy_(st.xs[wl.n_layers], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out["e2e_ms"] = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    del g, st, pool
     torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.steps):
-        st.xs[0].copy_(xh, non_blocking=True)
-        g.replay()
-        oh.copy_(st.xs[wl.n_layers], non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
-    e2e = {"value": round(world * wl.T * wl.n_layers * args.steps / (e2e_ms / 1e3), 1), "unit": UNIT,
+    torch.cuda.empty_cache()
+    return out
+
+
+def roofline_of(wl, m, pk, pk_src):
+    """The roofline record of one measurement. One-token and small batches
+    (T <= 64) are bounded by HBM: the algorithmic bytes are the distinct
+    routed experts' blobs plus the shared expert's, per layer; for the
+    one-launch stack the achieved rate uses that kernel's launch time, for a
+    T = 64 layer the whole layer's time (router, bucketing, GEMMs and
+    combine). T = 8192 prefill is a dense contraction bounded by the tensor
+    cores: gate/up 2 (2 I) H and down 2 I H FLOPs per (token, expert) pair,
+    pairs = T k routed + T shared, against the bf16 dense peak (the fp16
+    rate is the same)."""
+    import numpy as np
+    blob = m["blob"]
+    hbm = "MEASURED_PEAKS.json hbm_gbs (measured)" if pk_src == "measured" else "fallback 6.8 TB/s"
+    if wl.T <= 64:
+        per_layer = float(np.mean(m["uniq"]) + 1) * blob
+        if m["stacked"]:
+            alg, t_ms, kern = per_layer * wl.n_layers, m["kern_ms"], \
+                "decode_stack_kernel (moe_decode_stack: %d layers per launch)" % wl.n_layers
+        elif wl.T <= 8:
+            alg, t_ms, kern = per_layer, m["kern_ms"], "decode_kernel (moe_forward, T <= 8)"
+        else:
+            alg, t_ms = per_layer, m["ms"] / m.get("steps", 1) / wl.n_layers
+            kern = "whole layer (moe_route + moe_forward on the token-bucketed path)"
+        if not t_ms:
+            return None
+        ach = alg / (t_ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "kernel": kern, "bytes_per_launch": int(alg),
+                "us_per_launch": round(t_ms * 1e3, 3), "peak_source": hbm}
+    if not m["kern_ms"]:
+        return None
+    pairs = wl.T * wl.k + wl.T
+    f_gu = 2.0 * pairs * 2 * wl.I * wl.H
+    f_dn = 2.0 * pairs * wl.I * wl.H
+    peak = pk["bf16_tflops"]
+    t_gu, t_dn = m["kern_ms"] / 1e3, (m["down_ms"] or 0) / 1e3
+    comb = (f_gu + f_dn) / (t_gu + t_dn) / 1e12 if m["down_ms"] else None
+    return {"bound": "tensor", "achieved": round(comb or f_gu / t_gu / 1e12, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round((comb or f_gu / t_gu / 1e12) / peak, 4),
+            "kernel": "expert_gemm_kernel, gate/up and down launches together (fp16 operands, A in TMEM, fp32 "
+                      "accumulate)",
+            "flops_per_launch": f_gu + f_dn, "us_per_launch": round((t_gu + t_dn) * 1e6, 3),
+            "gate_up_us": round(t_gu * 1e6, 3), "gate_up_tflops": round(f_gu / t_gu / 1e12, 1),
+            "gate_up_frac": round(f_gu / t_gu / 1e12 / peak, 4),
+            "down_us": round(t_dn * 1e6, 3) if m["down_ms"] else None,
+            "down_tflops": round(f_dn / t_dn / 1e12, 1) if m["down_ms"] else None,
+            "layer_us": round(m["ms"] / m.get("steps", 1) / wl.n_layers * 1e3, 3),
+            "peak_source": "MEASURED_PEAKS.json bf16_tflops (measured; fp16 dense rate = bf16)"
+            if pk_src == "measured" else "fallback 1.9 PFLOP/s"}
+
+
+def traffic_of(wl, m):
+    if m["stacked"]:
+        t = stack_traffic(wl.name)
+        return t * wl.n_layers if t else None
+    if wl.T <= 8:
+        return recorded_traffic(wl.name)
+    if wl.T > 64:
+        return prefill_traffic(wl.name)
+    return None
+
+
+def run_ours(args, wl, world, rank, dist):
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    m = measure(args, wl, dev, dist, e2e=True)
+    m["steps"] = args.steps
+    ms = m["ms"]
+    step_s = ms / 1e3 / args.steps
+    value = world * wl.T * wl.n_layers / step_s
+    e2e = {"value": round(world * wl.T * wl.n_layers * args.steps / (m["e2e_ms"] / 1e3), 1), "unit": UNIT,
            "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2}
+    pk, pk_src = peaks()
+    roof = roofline_of(wl, m, pk, pk_src)
+    if roof is not None:
+        roof["traffic"] = traffic_of(wl, m)
+
+    # ---- the other target configurations, each measured the same way on this
+    # GPU after the headline (same steps and warm-up), as sub-records
+    extra = {}
+    if world == 1 and args.extra:
+        import synthetic
+        for name in [n for n in args.extra.split(",") if n and n != wl.name]:
+            w2 = synthetic.WORKLOADS[name]
+            m2 = measure(args, w2, dev)
+            m2["steps"] = args.steps
+            r2 = roofline_of(w2, m2, pk, pk_src)
+            if r2 is not None:
+                r2["traffic"] = traffic_of(w2, m2)
+            extra[name] = {"workload": w2.description, "value": round(w2.T * w2.n_layers * args.steps /
+                                                                        (m2["ms"] / 1e3), 1), "unit": UNIT,
+                           "us_per_layer": round(1e3 * m2["ms"] / args.steps / w2.n_layers, 3),
+                           "l2": "flushed between timed steps" if m2["flush"] else "no flush",
+                           "distinct_blobs_per_step": m2["blobs"], "roofline": r2, "clocks": m2["clocks"]}
 
     if rank != 0:
         return
-    pk, pk_src = peaks()
-    blob = int(pool.layout.blob_bytes)
-    roof = None
-    if kern_ms and not prefill:
-        # algorithmic bytes: every distinct routed expert of the step plus the shared expert
-        uniq = [len(np.unique(st.ids[l].cpu().numpy())) for l in range(wl.n_layers)]
-        alg_bytes = float(np.mean(uniq) + 1) * blob * (wl.n_layers if stacked else 1)
-        ach = alg_bytes / (kern_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / pk["hbm_gbs"], 4),
-                "traffic": (stack_traffic(wl.name) * wl.n_layers if stack_traffic(wl.name) else None) if stacked
-                else recorded_traffic(wl.name),
-                "kernel": ("decode_stack_kernel (moe_decode_stack: %d layers per launch)" % wl.n_layers) if stacked
-                else "decode_kernel (moe_forward, T <= 8)",
-                "bytes_per_launch": int(alg_bytes),
-                "us_per_launch": round(kern_ms * 1e3, 3),
-                "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk_src == "measured"
-                else "fallback 6.8 TB/s"}
-    elif kern_ms:
-        # gate/up grouped GEMM: 2 * (2 I) * H flops per (token, expert) pair, pairs = T*k routed + T shared
-        pairs = wl.T * wl.k + wl.T
-        flops = 2.0 * pairs * 2 * wl.I * wl.H
-        ach = flops / (kern_ms / 1e3) / 1e12
-        peak = pk["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4), "traffic": prefill_traffic(wl.name),
-                "kernel": "expert_gemm_kernel gate/up (fp16 operands, A in TMEM, fp32 accumulate)",
-                "flops_per_launch": flops, "us_per_launch": round(kern_ms * 1e3, 3),
-                "down_gemm_us": round(down_ms * 1e3, 3) if down_ms else None,
-                "down_gemm_tflops": round(2.0 * pairs * wl.I * wl.H / (down_ms / 1e3) / 1e12, 1) if down_ms else None,
-                "peak_source": "MEASURED_PEAKS.json bf16_tflops (measured; fp16 dense rate = bf16)"
-                if pk_src == "measured" else "fallback 1.9 PFLOP/s"}
+    stacked, prefill = m["stacked"], m["prefill"]
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp16" if prefill else "bf16", "data": "synthetic",
             "config": config_of(wl, ("CUDA graph of one moe_decode_stack call (%d layers in one launch); us per layer "
                                      "%.3f" if stacked else "CUDA graph of %d x (moe_route + moe_forward); us per "
-                                     "layer %.3f") % (wl.n_layers, 1e3 * ms / args.steps / wl.n_layers), blobs, flush),
+                                     "layer %.3f") % (wl.n_layers, 1e3 * ms / args.steps / wl.n_layers), m["blobs"],
+                                m["flush"]),
             "roofline": roof, "e2e": e2e,
             # per step: the one stack kernel; else per layer: decode = router + fused expert kernel;
             # bucketed path = router GEMM + top-k, 3 bucketing kernels, row gather, 2 grouped GEMMs, combine
             "gpu_launches": (1 if stacked else (9 if prefill else 2) * wl.n_layers) * args.steps,
-            "clocks": sampler.summary()}
+            "clocks": m["clocks"]}
+    if extra:
+        line["configs"] = extra
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     print(json.dumps(line), flush=True)

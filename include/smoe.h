@@ -149,7 +149,9 @@ typedef struct smoe_expert_src {
  * triples must stay valid until they complete. Corresponds to the pages'
  * repack step ("swiftlet-repack" builds fixed-stride containers from MLX
  * checkpoints), done in memory.
- * 8-bit experts pack with either kind.
+ * 8-bit experts pack with either kind. q words must start on a 4-byte and s,
+ * b on a 2-byte boundary, and a device pool on a 16-byte boundary (else
+ * SMOE_EINVAL before any work).
  * Errors: SMOE_EINVAL, SMOE_ENOTSUP, SMOE_ERANGE (slot < 0), SMOE_ENOMEM
  * (slot past pool_bytes), SMOE_ECUDA. */
 SMOE_API int pack_experts(const smoe_shape *shape, const smoe_expert_src *src, int32_t n,
@@ -189,6 +191,12 @@ SMOE_API uint64_t smoe_workspace_bytes(const smoe_ctx *ctx, int32_t T);
 /* --------------------------------------------------------------- moe_route */
 /* Router for T tokens: logits z = W_r x (+ logit_bias), softmax, top-k with
  * ties to the lower id, renormalised weights, and the shared-expert gate.
+ * The pages: every layer routes each token to 10 of 512 experts (80B model)
+ * or 8 of 256 (35B model), with the router kept resident (xix.ai article,
+ * paragraph on how it works; agentlenshq article, section on how expert
+ * streaming works). The softmax, the renormalisation over the chosen k, the
+ * tie rule and the sigmoid gate of the shared expert are this library's
+ * reading; the pages do not spell them out.
  *   W_r   bf16 [E][H] device   router rows
  *   w_s   bf16 [H]    device   shared-expert gate vector
  *   x     bf16 [T][H] device   token activations
@@ -204,7 +212,12 @@ SMOE_API int moe_route(const smoe_ctx *ctx, const uint16_t *W_r, const uint16_t 
               void *workspace, uint64_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------- moe_forward */
-/* The expert part of the layer for T tokens given their routing:
+/* The expert part of the layer for T tokens given their routing (the pages:
+ * each chosen routed expert is fetched whole from a fixed-size slot, one read
+ * per expert, while the shared experts stay resident; an expert read from the
+ * cache or from storage gives exactly the same answer -- xix.ai article,
+ * paragraphs on how it works and on correctness; agentlenshq article, section
+ * on how expert streaming works):
  *   out[t] = sum_{j<k} w[t][j] f_{ids[t][j]}(x_t) + gate[t] f_shared(x_t)
  *            (+ residual[t] if residual != NULL), rounded once to bf16.
  * Routed expert e of `layer` is read from pool + table[layer][e] * blob_bytes;
@@ -297,6 +310,19 @@ SMOE_API int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_t 
 /* Workspace bytes moe_decode_stack needs for n_layers layers (0 if the
  * context cannot run it). */
 SMOE_API uint64_t smoe_stack_workspace_bytes(const smoe_ctx *ctx, int32_t n_layers);
+
+/* Failure-detection hook (for tests; both settings are off by default).
+ * grid_wait_ns sets how long a grid-wide wait of moe_decode_stack on this
+ * context may last before it gives up (0: the default two seconds). With
+ * stall_layer >= 0, the first grid-wide wait of that layer (counted from the
+ * call's first_layer) waits for an arrival that never comes, so its limit
+ * runs out: the CTA that gives up first stores SMOE_DEV_TIMEOUT in the error
+ * word and raises the step's abort word, the other CTAs' waits end on it,
+ * every CTA still waits for its own bulk copies (their limit stays at two
+ * seconds) and the launch ends normally; the step's outputs from that layer
+ * on are undefined. stall_layer = -1 turns the stall off. Affects calls made
+ * after it. The pages describe no such hook. Errors: SMOE_EINVAL. */
+SMOE_API int smoe_set_stack_wait(smoe_ctx *ctx, uint64_t grid_wait_ns, int32_t stall_layer);
 
 /* Waits for stream, reads the error word (then clears it to 0) and returns
  * SMOE_OK, SMOE_EDEVICE if a kernel stored a code (copied to *code if

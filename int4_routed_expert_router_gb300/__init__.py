@@ -23,7 +23,7 @@ EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destro
            "smoe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_noalloc", "moe_decode_stack",
            "smoe_stack_workspace_bytes", "smoe_check", "smoe_ctx_describe", "smoe_set_profile_events",
            "smoe_status_string", "smoe_cache_create", "smoe_cache_destroy", "smoe_cache_prepare",
-           "smoe_cache_stats", "smoe_cache_simulate", "moe_forward_debug"]
+           "smoe_cache_stats", "smoe_cache_simulate", "moe_forward_debug", "smoe_set_stack_wait"]
 
 
 class SmoeError(RuntimeError):
@@ -83,6 +83,7 @@ def lib():
         L.smoe_check.argtypes = [vp, C.POINTER(C.c_int32), vp]
         L.smoe_ctx_describe.argtypes = [vp, C.c_char_p, i32]
         L.smoe_set_profile_events.argtypes = [vp, C.POINTER(vp), i32]
+        L.smoe_set_stack_wait.argtypes = [vp, u64, i32]
         L.smoe_status_string.argtypes = [C.c_int]
         L.smoe_status_string.restype = C.c_char_p
         for name in EXPORTS:
@@ -217,6 +218,12 @@ class Context:
         n = len(events)
         arr = (C.c_void_p * max(n, 1))(*[e.cuda_event for e in events])
         _check(lib().smoe_set_profile_events(self.handle, arr, n), "smoe_set_profile_events")
+
+    def set_stack_wait(self, grid_wait_ns: int = 0, stall_layer: int = -1):
+        """Failure-detection hook of moe_decode_stack (smoe_set_stack_wait):
+        the grid-wide wait limit (0: two seconds) and a layer whose first
+        grid-wide wait is made to run out (-1: none)."""
+        _check(lib().smoe_set_stack_wait(self.handle, int(grid_wait_ns), int(stall_layer)), "smoe_set_stack_wait")
 
     def stack_workspace_bytes(self, n_layers: int) -> int:
         """Workspace bytes of moe_decode_stack over n_layers layers (0: not available)."""

@@ -86,14 +86,15 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-// Thread 0 waits until *ctr >= target (two seconds at most, or until another
+// Thread 0 waits until *ctr >= target (limit_ns at most, two seconds by default, or until another
 // CTA raised the abort word), then the CTA synchronises. The counter is polled
 // with relaxed loads, one in flight at a time and spaced by a short sleep (the
 // abort word and the clock every 16 polls), and an acquire fence then orders what the arrivals
 // released before this CTA's reads. Returns false if the wait gave up; the
 // results of the step are then garbage and the error word says so, but every
 // CTA still runs to the end.
-__device__ bool grid_wait(const uint32_t *ctr, uint32_t target, uint32_t *abortw, int32_t *err, int *flag_s)
+__device__ bool grid_wait(const uint32_t *ctr, uint32_t target, uint32_t *abortw, int32_t *err, int *flag_s,
+                          uint64_t limit_ns)
 {
     if (threadIdx.x == 0) {
         int ok = 1;
@@ -102,7 +103,7 @@ __device__ bool grid_wait(const uint32_t *ctr, uint32_t target, uint32_t *abortw
             __nanosleep(32);                     // polls spaced out: the arrivals hit the same line
             if ((it & 15) == 0) {
                 if (ld_relaxed(abortw)) { ok = 0; break; }
-                if (global_ns() - t0 > 2000000000ull) {
+                if (global_ns() - t0 > limit_ns) {
                     atomicExch(abortw, 1u);
                     set_error(err, SMOE_DEV_TIMEOUT);
                     ok = 0;
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
         };
 
         // ---- 1. x_l, router rows, slot table row; logits of this CTA's rows
-        if (l > 0) grid_wait(p.sync + 3 * (l - 1) + 2, uint32_t(nrbB), abortw, p.err, flag_s);
+        if (l > 0) grid_wait(p.sync + 3 * (l - 1) + 2, uint32_t(nrbB), abortw, p.err, flag_s, p.wait_ns);
         if (tid == 0) {
             mbar_arrive_expect_tx(xbar, uint32_t(H * 2));
             bulk_nohint(x_s, p.xs + size_t(l) * H, uint32_t(H * 2), xbar);
@@ -218,7 +219,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
         // or above it can be chosen. Each such candidate's rank among the
         // candidates (larger key first, ties to the lower id) is its place in
         // route order.
-        grid_wait(&cnt[0], uint32_t(G), abortw, p.err, flag_s);
+        // (the failure-detection test hook asks for one arrival more than there are CTAs)
+        grid_wait(&cnt[0], uint32_t(G) + (l == p.stall_layer ? 1u : 0u), abortw, p.err, flag_s, p.wait_ns);
         for (int e = tid; e <= E; e += kStkThreads) zs[e] = __ldcg(p.logits + size_t(l) * (E + 1) + e);
         if (tid == 0) *ncand = 0;
         __syncthreads();
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
 
         // ---- 5. down rows of every expert for rows 16 c .. 16 c + 15, combine
         if (c < nrbB) {
-            grid_wait(&cnt[1], uint32_t(G), abortw, p.err, flag_s);
+            grid_wait(&cnt[1], uint32_t(G), abortw, p.err, flag_s, p.wait_ns);
             // h rows of every expert (hi, lo; padded rows), and the unit sums: one bulk
             // copy per lane of warp 0
             if (warp == 0) {

@@ -352,6 +352,8 @@ extern "C" int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_
     c->n_slots = n_slots;
     c->table_dev = table_dev;
     c->cs = shape->I / kSlice;
+    c->stack_wait_ns = 0;
+    c->stack_stall_layer = -1;
     cudaError_t e = cudaGetDevice(&c->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
     if (e == cudaSuccess) e = route_config();
@@ -605,6 +607,8 @@ extern "C" int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_
     p.hps = reinterpret_cast<float *>(ws + W.hps);
     p.sync = reinterpret_cast<uint32_t *>(ws + W.sync);
     p.err = err;
+    p.wait_ns = ctx->stack_wait_ns ? ctx->stack_wait_ns : kWaitLimitNs;
+    p.stall_layer = ctx->stack_stall_layer;
     p.n_layers = n_layers;
     p.H = ctx->shape.H;
     p.E = ctx->shape.E;
@@ -614,6 +618,14 @@ extern "C" int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_
     p.nr = ctx->stack.nr;
     p.nu = ctx->stack.nu;
     return cuda_status(launch_stack(ctx, p, static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int smoe_set_stack_wait(smoe_ctx *ctx, uint64_t grid_wait_ns, int32_t stall_layer)
+{
+    if (!ctx || stall_layer < -1 || stall_layer >= kStackMaxLayers) return SMOE_EINVAL;
+    ctx->stack_wait_ns = grid_wait_ns;
+    ctx->stack_stall_layer = stall_layer;
+    return SMOE_OK;
 }
 
 extern "C" int smoe_ctx_describe(const smoe_ctx *ctx, char *buf, int32_t len)

@@ -78,6 +78,8 @@ struct StackParams {
     float *hps;                                // [n_layers][U][I / 8] sum of hi + lo per 8-row unit
     uint32_t *sync;                            // [n_layers][3] arrival counters, then the abort word
     int32_t *err;
+    uint64_t wait_ns;                          // limit of a grid-wide wait
+    int stall_layer;                           // test hook: this layer's first grid-wide wait never completes (-1: off)
     int n_layers, H, E, k, I, U, nr, nu;
 };
 
@@ -96,6 +98,8 @@ struct smoe_ctx {
     int nprof;
     smoe::DecodeCfg decode[smoe::kDecodeMaxT + 1];
     smoe::StackCfg stack;
+    uint64_t stack_wait_ns;                  // grid-wide wait limit of moe_decode_stack (smoe_set_stack_wait)
+    int32_t stack_stall_layer;               // -1, or the layer whose first grid-wide wait is made to run out
 };
 
 namespace smoe {
