@@ -74,13 +74,28 @@ def routing_ok(ids_g, w_g, gate_g, ref, k, atol_w=2e-5, atol_gate=1e-5, gap=1e-4
     return w_own
 
 
+def half_bf16_unit(a):
+    """Half a bf16 unit in the last place at |a| (the largest error of a
+    round-to-nearest bf16 result), elementwise."""
+    big = np.maximum(np.abs(a), 1e-30)
+    return 2.0 ** (np.floor(np.log2(big)) - 8)
+
+
 def assert_output_close(gpu_bits, out64, ref_bf16=None, exact_frac=None):
+    """bf16 outputs against the oracle's fp64 result: relative L2 <= 5e-3, and
+    per element |gpu - oracle| <= 2e-2 rms(oracle) plus half a bf16 unit of
+    the larger of the two values. The half unit is the bf16 rounding of the
+    output itself: the oracle's own correctly rounded bf16 result is up to
+    half a unit from its fp64 value, which exceeds 2e-2 rms wherever an output
+    element is more than about 5 rms just above a power of two, so the bound
+    is read as holding before that final rounding."""
     g = synthetic.bf16_bits_to_f32(gpu_bits).astype(np.float64)
     err = g - out64
     rms = np.sqrt(np.mean(out64 ** 2))
     rel = np.linalg.norm(err) / np.linalg.norm(out64)
     assert rel <= 5e-3, rel
-    assert np.abs(err).max() <= 2e-2 * rms, (np.abs(err).max(), rms)
+    bound = 2e-2 * rms + half_bf16_unit(np.maximum(np.abs(g), np.abs(out64))) * (1 + 1e-9)
+    assert np.all(np.abs(err) <= bound), (np.abs(err).max(), rms)
     if exact_frac is not None:
         frac = np.mean(gpu_bits == ref_bf16)
         assert frac >= exact_frac, frac
@@ -98,8 +113,7 @@ def assert_residual_close(got_bits, x_bits, y64):
     want = xr + y64
     assert_output_close(got_bits, want)
     g = synthetic.bf16_bits_to_f32(got_bits).astype(np.float64)
-    big = np.maximum(np.maximum(np.abs(want), np.abs(g)), 1e-30)
-    bound = 2.0 ** (np.floor(np.log2(big)) - 8) * (1 + 1e-9) + 2e-2 * np.sqrt(np.mean(y64 ** 2))
+    bound = half_bf16_unit(np.maximum(np.abs(want), np.abs(g))) * (1 + 1e-9) + 2e-2 * np.sqrt(np.mean(y64 ** 2))
     assert np.all(np.abs(g - want) <= bound), np.abs(g - want).max()
 
 

@@ -7,7 +7,7 @@ import pytest
 import oracle
 import oracle_shards
 import synthetic
-from test_gpu_parity import assert_residual_close, routing_ok
+from test_gpu_parity import assert_output_close, assert_residual_close, routing_ok
 
 
 @pytest.fixture(scope="module")
@@ -79,3 +79,23 @@ def test_residual_rule_allows_the_output_rounding_only(tiny_ref):
     off[0, 0] += 3                                            # three bf16 units away
     with pytest.raises(AssertionError):
         assert_residual_close(off, x[:4], one["out64"])
+
+
+def test_exactly_rounded_output_passes_the_output_rule():
+    """The oracle's own round-to-nearest bf16 output must pass the output rule:
+    on this input its rounding alone is 1.15e-4 while 2e-2 rms is 1.11e-4 (an
+    element of 6.3 rms just above a power of two), which is why the rule adds
+    half a bf16 unit. Two units off still fails."""
+    wl = synthetic.WORKLOADS["tiny"]
+    x = synthetic.activations(wl.seed, 64, wl.H, tag=64)
+    one = oracle.layer(wl, 0, x, synthetic.router_weights(wl.seed, 0, wl.E, wl.H),
+                       synthetic.shared_gate_weights(wl.seed, 0, wl.H))
+    y, yb = one["out64"], one["out_bf16"]
+    rounding = np.abs(synthetic.bf16_bits_to_f32(yb).astype(np.float64) - y).max()
+    assert rounding > 2e-2 * np.sqrt(np.mean(y ** 2))
+    assert_output_close(yb, y)
+    i = np.unravel_index(np.abs(y).argmax(), y.shape)
+    off = yb.copy()
+    off[i] += 2
+    with pytest.raises(AssertionError):
+        assert_output_close(off, y)
