@@ -273,10 +273,12 @@ SMOE_API int moe_forward_noalloc(const smoe_ctx *ctx, int32_t layer, const uint1
  *   x_{l+1} = bf16(x_l + sum_j w_j f_{ids_j}(x_l) + gate f_shared(x_l)),
  * the residual stacking of a decode step (the layers run one after the
  * other for each new token: xix.ai article, paragraph on how it works). The
- * whole step is one persistent launch (one CTA per SM, cooperative), the
- * layers separated by grid-wide counters in the workspace instead of kernel
- * boundaries; the routing rule and its fp32 arithmetic are moe_route's, so
- * ids, w and gate equal what moe_route returns for the same x_l.
+ * whole step is one persistent launch (one CTA per SM, cooperative) instead of
+ * kernel boundaries: per layer the CTAs exchange the router logits, the
+ * SwiGLU values and the layer's output through the workspace, each value
+ * polled where it is needed. The routing rule and its fp32 arithmetic are
+ * moe_route's, so ids, w and gate equal what moe_route returns for the same
+ * x_l.
  *   W_r, w_s      HOST arrays of n_layers device pointers: each layer's router
  *                 rows (bf16 [E][H]) and shared-gate vector (bf16 [H]); the
  *                 pointers are copied into the launch, the arrays may be
@@ -290,13 +292,15 @@ SMOE_API int moe_forward_noalloc(const smoe_ctx *ctx, int32_t layer, const uint1
  *   gate          fp32 [n_layers] device, out
  *   pool          as for moe_forward
  *   workspace     device, >= smoe_stack_workspace_bytes(ctx, n_layers) bytes;
- *                 the call clears the part it needs (its counters) itself
- *   err           device error word as for moe_forward; a grid-wide wait
- *                 that gives up (2 s) stores SMOE_DEV_TIMEOUT
+ *                 the call initialises it itself (no clearing needed)
+ *   err           device error word as for moe_forward; a wait for other
+ *                 CTAs' results that gives up (2 s) stores SMOE_DEV_TIMEOUT
  * Expert arithmetic is the decode kernel's (exact weights, fp32 partials, h
  * as bf16 hi + lo); the partial sums are combined in a fixed order, so the
- * step is bit-identical across runs. Needs E % 4 == 0, 1 <= n_layers <= 64
- * and a GPU with cooperative launch and enough shared memory (see
+ * step is bit-identical across runs. A result whose bits are all ones (a
+ * NaN) is stored as the canonical NaN 0x7FFF. Needs E % 4 == 0, E <= 512,
+ * 1 <= n_layers <= 64 and a GPU with cooperative launch and enough shared
+ * memory (see
  * smoe_ctx_describe); otherwise SMOE_ENOTSUP. Errors: SMOE_EINVAL,
  * SMOE_ENOMEM, SMOE_ENOTSUP, SMOE_ECUDA. The pages describe one MoE layer at a
  * time; running a step's layers in one launch is this library's. */
@@ -312,16 +316,18 @@ SMOE_API int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_t 
 SMOE_API uint64_t smoe_stack_workspace_bytes(const smoe_ctx *ctx, int32_t n_layers);
 
 /* Failure-detection hook (for tests; both settings are off by default).
- * grid_wait_ns sets how long a grid-wide wait of moe_decode_stack on this
- * context may last before it gives up (0: the default two seconds). With
- * stall_layer >= 0, the first grid-wide wait of that layer (counted from the
- * call's first_layer) waits for an arrival that never comes, so its limit
- * runs out: the CTA that gives up first stores SMOE_DEV_TIMEOUT in the error
- * word and raises the step's abort word, the other CTAs' waits end on it,
- * every CTA still waits for its own bulk copies (their limit stays at two
- * seconds) and the launch ends normally; the step's outputs from that layer
- * on are undefined. stall_layer = -1 turns the stall off. Affects calls made
- * after it. The pages describe no such hook. Errors: SMOE_EINVAL. */
+ * grid_wait_ns sets how long a wait of moe_decode_stack for other CTAs'
+ * results (router logits, SwiGLU values, a layer's output) may last on this
+ * context before it gives up (0: the default two seconds). With
+ * stall_layer >= 0, the wait for that layer's router logits (the layer
+ * counted from the call's first_layer) also asks for a word that nothing
+ * writes, so its limit runs out: the CTA that gives up first stores
+ * SMOE_DEV_TIMEOUT in the error word and raises the step's abort word, the
+ * other CTAs' waits end on it, every CTA still waits for its own bulk copies
+ * (their limit stays at two seconds) and the launch ends normally; the
+ * step's outputs from that layer on are undefined. stall_layer = -1 turns
+ * the stall off. Affects calls made after it. The pages describe no such
+ * hook. Errors: SMOE_EINVAL. */
 SMOE_API int smoe_set_stack_wait(smoe_ctx *ctx, uint64_t grid_wait_ns, int32_t stall_layer);
 
 /* Waits for stream, reads the error word (then clears it to 0) and returns

@@ -1,30 +1,49 @@
 // decode_stack.cu -- one decode step (one token) through a stack of MoE
 // layers in a single persistent, cooperative launch: one CTA per SM for the
-// whole step, the layers separated by three grid-wide arrival counters each
-// instead of kernel boundaries. Per layer l:
-//   1. x_l and this CTA's router rows (rows c, c + G, ...; row E is the
-//      shared-gate vector) are bulk-copied into shared memory; the CTA's
-//      logits go to the workspace; counter A.
-//   2. Every CTA reads all E + 1 logits and computes the same top-k (by rank
-//      among the few logits that can be chosen), renormalised weights and
-//      shared gate (route_common.cuh's arithmetic); CTA 0 also writes them out.
-//   3. Gate/up: work units (expert u, 16-row block rb: intermediates
-//      8 rb .. 8 rb + 7, 32 contiguous atoms, one bulk copy) are spread over
-//      all CTAs; SwiGLU values go to the workspace as bf16 high and low
-//      parts with each unit's sum of them; counter B.
-//   4. Down and combine: CTA c < H/16 owns output rows 16 c .. 16 c + 15. Its
-//      down atoms of every expert were requested in step 3, so they stream in
-//      with the gate/up weights; after counter B it reads all h, computes the
-//      rows for every expert and writes x_{l+1} = bf16(x_l + sum_j w_j y_j
-//      (route order) + gate y_shared); counter C.
-// While layer l computes, layer l + 1's router rows and shared-expert blob
-// are prefetched into L2. The per-atom arithmetic is the decode kernel's
-// (bf16 (128 + q) fragments on m16n8k16 tensor-core steps, s and b - 128 s
-// per group, h as bf16 hi + lo). Every wait is bounded: a grid-wide wait gives
-// up after two seconds and raises an abort word that ends the others' waits.
-// Pages: the per-token expert stream of a decode step and its fixed-stride
-// blobs (xix.ai article, paragraphs on how it works); the shared expert and
-// its gate (agentlenshq article, how expert streaming works).
+// whole step.
+//
+// The CTAs exchange three things per layer -- the router logits, the SwiGLU
+// values h, and the layer's output x_{l+1} -- through buffers in the
+// workspace that the launch first fills with a sentinel bit pattern (all
+// ones: a NaN that the arithmetic never writes; a result with that pattern is
+// stored as the canonical NaN instead). A reader polls the words it needs
+// with relaxed loads until none holds the sentinel, so the data itself is the
+// signal: no arrival counter, no fence, one round trip to L2 per exchange.
+// Each word is written once per launch, and every value stands on its own, so
+// no ordering between words is needed.
+//
+// Per layer l, CTA c of G:
+//   A. x_l into shared memory (the caller's x_0 by a bulk copy; later layers
+//      polled from the exchange buffer).
+//   B. Router rows c, c + G, ... (row E is the shared-gate vector; loaded
+//      during the previous layer) dotted with x_l; the logits go out.
+//   C. CTAs c < I/8 compute the shared expert's gate/up unit c (intermediates
+//      8c .. 8c + 7; its weights were loaded during the previous layer) while
+//      the logits of the other CTAs arrive.
+//   D. One warp polls all E + 1 logits and picks the top k in registers
+//      (route_common.cuh's arithmetic, so ids, weights and gate equal
+//      moe_route's bit for bit); CTA 0 writes them out.
+//   E. The CTA requests its routed gate/up units (expert j in route order,
+//      row block rb: 32 contiguous atoms, one bulk copy each) and, for
+//      c < H/16, its down rows 16c .. 16c + 15 of every routed expert.
+//   F. Gate/up units as their bytes land -> h as bf16 high and low parts.
+//   G. CTAs c < H/16: poll all experts' h, down rows of every expert, combine
+//      in route order with the routing weights, + gate * shared expert +
+//      x_l, one bf16 rounding -> x_{l+1} (exchange buffer and the caller's
+//      xs).
+// The per-atom arithmetic is the decode kernel's: bf16 (128 + q) fragments on
+// m16n8k16 tensor-core steps, s and b - 128 s applied per group, fp32 sums.
+//
+// Every wait is bounded. A poll that runs past the limit (two seconds by
+// default) stores SMOE_DEV_TIMEOUT and raises the launch's abort word, which
+// ends the other CTAs' polls; the CTAs then run to the end on whatever the
+// buffers hold (every address stays in bounds). Waits for a CTA's own bulk
+// copies keep their own two-second limit, so no CTA leaves with a copy in
+// flight.
+// Pages: the per-token expert stream of a decode step, fixed-stride blobs and
+// one read per expert (xix.ai article, paragraph on how it works); the
+// resident router and shared experts (agentlenshq article, how expert
+// streaming works).
 #include "decode_common.cuh"
 #include "route_common.cuh"
 
@@ -32,31 +51,35 @@ namespace smoe {
 
 constexpr int kStkWarps = 16;
 constexpr int kStkThreads = kStkWarps * 32;
+constexpr uint32_t kSentinel32 = 0xFFFFFFFFu;
+constexpr uint16_t kSentinel16 = 0xFFFFu;
+constexpr int kStkMaxE = 512;           // experts per layer the one-launch step takes (larger E: per-layer calls)
 
 struct StkSmem {
-    int x_s, xsum, rows, zs, table, units, wdn, hps, hh, hl, hsum, yp, red, cand, ints, bars, total;
+    int x_s, xsum, rows, table, sunit, units, wdn, red, hh, yd, ysum, mx, cand, sel, ints, bars, total;
 };
 
 __host__ __device__ inline StkSmem stk_smem(int H, int E, int I, int U, int nr, int nu)
 {
+    const int ngH = H / kGroup, ngI = I / kGroup;
     StkSmem L;
     int o = 0;
     L.x_s = o;   o = align128(o + 2 * H + 16);
-    L.xsum = o;  o = align128(o + (H / kGroup) * 4);
-    L.rows = o;  o = align128(o + nr * H * 2);
-    L.zs = o;    o = align128(o + (E + 1) * 4);
-    L.table = o; o = align128(o + E * 4);
-    L.units = o; o = align128(o + nu * (H / kGroup) * kAtomBytes);
-    L.wdn = o;   o = align128(o + U * (I / kGroup) * kAtomBytes);
-    L.hps = o;   o = align128(o + U * (I / 8) * 4);
-    L.hh = o;    o = align128(o + U * (I + 8) * 2);
-    L.hl = o;    o = align128(o + U * (I + 8) * 2);
-    L.hsum = o;  o = align128(o + U * (I / kGroup) * kDecodeMaxT * 4);
-    L.yp = o;    o = align128(o + U * 2 * 16 * 4);
-    L.red = o;   o = align128(o + nu * kStkWarps * 8 * 8);
-    L.cand = o;  o = align128(o + (2 * E + 2 * 16 + 2 * 16) * 4);
+    L.xsum = o;  o = align128(o + ngH * 4);
+    L.rows = o;  o = align128(o + (nr > 0 ? nr : 1) * H * 2);
+    L.table = o; o = align128(o + 2 * E * 4);
+    L.sunit = o; o = align128(o + ngH * kAtomBytes);
+    L.units = o; o = align128(o + (nu > 0 ? nu : 1) * ngH * kAtomBytes);
+    L.wdn = o;   o = align128(o + U * ngI * kAtomBytes);
+    L.red = o;   o = align128(o + (nu + 1) * kStkWarps * 8 * 8);
+    L.hh = o;    o = align128(o + U * 2 * I * 2);
+    L.yd = o;    o = align128(o + U * ngI * 16 * 4);
+    L.ysum = o;  o = align128(o + U * 16 * 4);
+    L.mx = o;    o = align128(o + 2 * kStkWarps * 4);
+    L.cand = o;  o = align128(o + 2 * E * 4);
+    L.sel = o;   o = align128(o + 2 * 16 * 4);
     L.ints = o;  o = align128(o + 64 * 4);
-    L.bars = o;  o = align128(o + (nu + U + 3) * 8);
+    L.bars = o;  o = align128(o + (nu + U + 5) * 8);
     L.total = o;
     return L;
 }
@@ -67,9 +90,11 @@ __device__ __forceinline__ void bulk_nohint(void *dst, const void *src, uint32_t
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2_bytes(const void *p, uint32_t bytes)
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
 {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
@@ -79,44 +104,234 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
     return v;
 }
 
-__device__ __forceinline__ uint64_t global_ns()
+__device__ __forceinline__ uint2 ld_relaxed_v2(const void *p)
 {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
+    uint2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+    return v;
 }
 
-// Thread 0 waits until *ctr >= target (limit_ns at most, two seconds by default, or until another
-// CTA raised the abort word), then the CTA synchronises. The counter is polled
-// with relaxed loads, one in flight at a time and spaced by a short sleep (the
-// abort word and the clock every 16 polls), and an acquire fence then orders what the arrivals
-// released before this CTA's reads. Returns false if the wait gave up; the
-// results of the step are then garbage and the error word says so, but every
-// CTA still runs to the end.
-__device__ bool grid_wait(const uint32_t *ctr, uint32_t target, uint32_t *abortw, int32_t *err, int *flag_s,
-                          uint64_t limit_ns)
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void *p)
 {
-    if (threadIdx.x == 0) {
-        int ok = 1;
-        const uint64_t t0 = global_ns();
-        for (uint32_t it = 1; ld_relaxed(ctr) < target; ++it) {
-            __nanosleep(32);                     // polls spaced out: the arrivals hit the same line
-            if ((it & 15) == 0) {
-                if (ld_relaxed(abortw)) { ok = 0; break; }
-                if (global_ns() - t0 > limit_ns) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_u16(uint16_t *p, uint16_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_v4(void *p, uint4 v)
+{
+    asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// No half-word of v is the 16-bit sentinel.
+__device__ __forceinline__ bool ready16(uint32_t v)
+{
+    return (v & 0xFFFFu) != kSentinel16 && (v >> 16) != kSentinel16;
+}
+
+// A value that happens to carry the sentinel pattern (a NaN) is stored as the
+// canonical NaN of its width.
+__device__ __forceinline__ uint16_t canon16(uint16_t v) { return v == kSentinel16 ? uint16_t(0x7FFF) : v; }
+__device__ __forceinline__ uint32_t canon32(uint32_t v) { return v == kSentinel32 ? 0x7FFFFFFFu : v; }
+
+// Polls `load` (which re-reads the words it has not yet seen written and
+// returns true once all are) until it succeeds for every lane of `mask`, the
+// abort word is raised, or limit_ns pass; on the last, stores
+// SMOE_DEV_TIMEOUT and raises the abort word. Returns whether the data came.
+// All lanes of `mask` call it together and leave it together: every decision
+// is taken warp-wide, because a warp whose lanes had left a sleeping loop at
+// different times ran the code after it (the top-k, several times over)
+// unconverged, about four times slower. Only the words not yet seen written
+// are read again, after a short pause: every CTA polls the same few L2 lines
+// that the writers are storing to, and re-reading all of them in a tight loop
+// delayed those stores by microseconds.
+template <typename F>
+__device__ __forceinline__ bool poll_rounds(F load, uint32_t mask, uint32_t *abortw, int32_t *err, uint64_t limit_ns,
+                                            uint32_t pause)
+{
+    if (__all_sync(mask, load())) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(pause);                     // sleeps twice the request on this GPU
+        if (__all_sync(mask, load())) return true;
+        if ((it & 15) == 0) {
+            if (__any_sync(mask, ld_relaxed(abortw) != 0u)) return false;
+            if (__any_sync(mask, globaltimer_ns() - t0 > limit_ns)) {
+                if ((threadIdx.x & 31) == __ffs(mask) - 1) {
                     atomicExch(abortw, 1u);
                     set_error(err, SMOE_DEV_TIMEOUT);
-                    ok = 0;
-                    break;
                 }
+                return false;
             }
         }
+    }
+}
+
+// Even so, lanes that slept in the loop may wake at different times and stay
+// split into groups that the scheduler issues one after another (measured: a
+// warp's top-k afterwards took 20,000 cycles instead of 5,000). A warp
+// reduction after a __syncwarp merges them again; so every poll ends with one.
+template <typename F>
+__device__ __forceinline__ bool poll(F load, uint32_t mask, uint32_t *abortw, int32_t *err, uint64_t limit_ns,
+                                     uint32_t pause = 32)
+{
+    const bool ok = poll_rounds(load, mask, abortw, err, limit_ns, pause);
+    __syncwarp(mask);
+    (void)__reduce_or_sync(mask, 0u);
+    return ok;
+}
+
+// Thread 0 waits until *ctr >= target (bounded like poll), then an acquire
+// fence; the CTA synchronises. Used once, after the sentinel fill.
+__device__ void grid_wait(const uint32_t *ctr, uint32_t target, uint32_t *abortw, int32_t *err, uint64_t limit_ns)
+{
+    if (threadIdx.x == 0) {
+        poll([&] { return ld_relaxed(ctr) >= target; }, 1u, abortw, err, limit_ns);
         asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        asm volatile("fence.proxy.async.global;" ::: "memory");   // later bulk copies read what we acquired
-        *flag_s = ok;
     }
     __syncthreads();
-    return *flag_s != 0;
+}
+
+// The gate/up partial sums of one atom (16 rows x one 64-column group kb) for
+// the token (MMA column 0): lanes 4g (t4 = 0) get gate row g and up row g.
+__device__ __forceinline__ float2 gateup_atom(const uint8_t *atom, const uint16_t *x_s, float xs_kb, int kb, int lane)
+{
+    const int g = lane >> 2, t4 = lane & 3;
+    const uint4 A = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
+    const uint2 SB = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+    const int col = kb * kGroup + 16 * t4;
+    uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+    if (g == 0) {                                   // the token is MMA column 0
+        xa = *reinterpret_cast<const uint4 *>(x_s + col);
+        xb = *reinterpret_cast<const uint4 *>(x_s + col + 8);
+    }
+    const uint32_t xl[4] = {xa.x, xa.y, xa.z, xa.w}, xr[4] = {xb.x, xb.y, xb.z, xb.w};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < 4; m += 2) {
+        const uint32_t a0[4] = {nib_pair(A.x, m), nib_pair(A.z, m), nib_pair(A.y, m), nib_pair(A.w, m)};
+        const uint32_t a1[4] = {nib_pair(A.x, m + 1), nib_pair(A.z, m + 1), nib_pair(A.y, m + 1),
+                                nib_pair(A.w, m + 1)};
+        mma_bf16(acc, a0, xl[m], xr[m]);
+        mma_bf16(acc2, a1, xl[m + 1], xr[m + 1]);
+    }
+    float sg, bpg, su, bpu;
+    scale_bias(SB.x, sg, bpg);
+    scale_bias(SB.y, su, bpu);
+    return make_float2(fmaf(sg, acc[0] + acc2[0], bpg * xs_kb), fmaf(su, acc[2] + acc2[2], bpu * xs_kb));
+}
+
+// One warp's partial sums of a gate/up unit (H/64 atoms, one 64-column group
+// of x each) when nw warps share it: warp w takes atoms w, w + nw, ..., two at
+// a time so that their tensor-core chains overlap, and adds them in that order.
+__device__ __forceinline__ float2 gateup_partial(const uint8_t *ubase, const uint16_t *x_s, const float *xsum, int ngH,
+                                                 int warp, int nw, int lane)
+{
+    float aG = 0.f, aU = 0.f;
+    for (int kb = warp; kb < ngH; kb += 2 * nw) {
+        const int kb1 = kb + nw;
+        const float2 a = gateup_atom(ubase + kb * kAtomBytes, x_s, xsum[kb], kb, lane);
+        float2 b = make_float2(0.f, 0.f);
+        if (kb1 < ngH) b = gateup_atom(ubase + kb1 * kAtomBytes, x_s, xsum[kb1], kb1, lane);
+        aG += a.x;
+        aU += a.y;
+        aG += b.x;
+        aU += b.y;
+    }
+    return make_float2(aG, aU);
+}
+
+// Warp `warp` (whole warp) finishes a gate/up unit from the nw warps'
+// partials red[w * 8 + g] (summed in warp order): h of intermediates
+// 8 rb .. 8 rb + 7 as bf16 high parts and low parts (h - high), stored as one
+// 16-byte store each into the exchange rows hx_hi, hx_lo; then one release
+// add on the expert's arrival counter, so a reader that has acquired the
+// counter at I/8 sees every unit's h.
+__device__ __forceinline__ void finish_unit(const float2 *red, int nw, bool valid, uint16_t *hx_hi, uint16_t *hx_lo,
+                                            uint32_t *cnt, int lane)
+{
+    const int g = lane >> 2;
+    float aG = red[g].x, aU = red[g].y;
+    for (int w = 1; w < nw; ++w) {
+        const float2 v = red[w * 8 + g];
+        aG += v.x;
+        aU += v.y;
+    }
+    const float hv = valid ? silu(aG) * aU : 0.f;
+    const uint16_t hi = f32_to_bf16_bits(hv);
+    const uint16_t lo = f32_to_bf16_bits(hv - __uint_as_float(uint32_t(hi) << 16));
+    uint32_t phi[4], plo[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {                       // lanes 4g hold intermediate g
+        const uint32_t h0 = __shfl_sync(0xffffffffu, uint32_t(hi), 8 * q);
+        const uint32_t h1 = __shfl_sync(0xffffffffu, uint32_t(hi), 8 * q + 4);
+        const uint32_t l0 = __shfl_sync(0xffffffffu, uint32_t(lo), 8 * q);
+        const uint32_t l1 = __shfl_sync(0xffffffffu, uint32_t(lo), 8 * q + 4);
+        phi[q] = h0 | (h1 << 16);
+        plo[q] = l0 | (l1 << 16);
+    }
+    if (lane == 0) {
+        *reinterpret_cast<uint4 *>(hx_hi) = make_uint4(phi[0], phi[1], phi[2], phi[3]);
+        *reinterpret_cast<uint4 *>(hx_lo) = make_uint4(plo[0], plo[1], plo[2], plo[3]);
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
+    }
+}
+
+// Down rows 16 c .. 16 c + 15 of one expert over one 64-group of h, with h
+// split into bf16 high and low parts as MMA columns 0 and 1: lanes 0..3 (B
+// column 0) hold the group's high parts, lanes 4..7 (column 1) the low parts,
+// h0: columns 16 t4 .. +7 of the group, h1: +8 .. +15; other lanes hold zeros.
+// One m16n8k16 step per 16 columns yields both partial sums; gsum: the
+// group's sum of high + low parts. Lanes 4g (t4 = 0) return rows g and g + 8.
+__device__ __forceinline__ float2 down_atom(const uint8_t *atom, uint4 h0, uint4 h1, float gsum, int lane)
+{
+    const int g = lane >> 2;
+    const uint4 A = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
+    const uint2 SB = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+    const uint32_t ha_[4] = {h0.x, h0.y, h0.z, h0.w}, hb_[4] = {h1.x, h1.y, h1.z, h1.w};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < 4; m += 2) {
+        const uint32_t a0[4] = {nib_pair(A.x, m), nib_pair(A.z, m), nib_pair(A.y, m), nib_pair(A.w, m)};
+        const uint32_t a1[4] = {nib_pair(A.x, m + 1), nib_pair(A.z, m + 1), nib_pair(A.y, m + 1),
+                                nib_pair(A.w, m + 1)};
+        mma_bf16(acc, a0, ha_[m], hb_[m]);
+        mma_bf16(acc2, a1, ha_[m + 1], hb_[m + 1]);
+    }
+    float s0, bp0, s1, bp1;
+    scale_bias(SB.x, s0, bp0);
+    scale_bias(SB.y, s1, bp1);
+    // (row, column 0) + (row, column 1): the high and the low part's sums
+    return make_float2(fmaf(s0, (acc[0] + acc2[0]) + (acc[1] + acc2[1]), bp0 * gsum),
+                       fmaf(s1, (acc[2] + acc2[2]) + (acc[3] + acc2[3]), bp1 * gsum));
+}
+
+// Sum of the high + low parts of one 64-group held as down_atom's B columns
+// (lanes 0..3 the high parts, lanes 4..7 the low parts, 16 values each):
+// each lane sums its 16 in column order, then the eight lanes in a fixed
+// tree; every lane gets the sum.
+__device__ __forceinline__ float group_sum(uint4 h0, uint4 h1)
+{
+    const uint32_t v[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s += bf16lo(v[j]) + bf16hi(v[j]);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    return __shfl_sync(0xffffffffu, s, 0);
 }
 
 // Composite order of the routing keys: larger key first, equal keys by lower id.
@@ -125,190 +340,271 @@ __device__ __forceinline__ bool key_before(uint32_t ka, int32_t ia, uint32_t kb,
     return ka > kb || (ka == kb && ia < ib);
 }
 
+// The k largest of E <= 512 logits (plus the optional offsets), in route
+// order, by the whole CTA (thread t holds logit t): each warp's slice maximum;
+// the k-th largest of the 16 maxima bounds the k-th largest key from below
+// (k distinct keys reach it), so only the keys at or above it are
+// candidates (ties: the lower id first, a strict order); a candidate's rank
+// among the candidates is its place in route order. The same selection as
+// route_common.cuh's, so the ids are moe_route's. ncand must be zero on entry
+// and is zero again on return. Three CTA barriers.
+__device__ void block_topk(float z, const float *bias, int E, int k, uint32_t *mx_k, int32_t *mx_i, uint32_t *cand_k,
+                           int32_t *cand_i, int *ncand, uint32_t *sel_k, int32_t *sel_i)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t key = tid < E ? fkey(z + (bias ? bias[tid] : 0.f)) : 0u;
+    const int32_t id = tid < E ? tid : 0x7fffffff;
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
+    const int32_t mi = int32_t(__reduce_min_sync(0xffffffffu, key == mk ? uint32_t(id) : 0x7fffffffu));
+    if (lane == 0) {
+        mx_k[warp] = mk;
+        mx_i[warp] = mi;
+    }
+    __syncthreads();
+    const int j = lane & (kStkWarps - 1);
+    const uint32_t jk = mx_k[j];
+    const int32_t ji = mx_i[j];
+    int r = 0;
+#pragma unroll
+    for (int i = 0; i < kStkWarps; ++i) r += key_before(mx_k[i], mx_i[i], jk, ji);
+    const uint32_t b = __ballot_sync(0xffffffffu, lane < kStkWarps && r == k - 1);
+    const int src = b ? __ffs(b) - 1 : 0;
+    const uint32_t tk = b ? __shfl_sync(0xffffffffu, jk, src) : 0u;       // no such rank: every key qualifies
+    const int32_t ti = b ? __shfl_sync(0xffffffffu, ji, src) : 0x7fffffff;
+    const bool cand = key != 0u && !key_before(tk, ti, key, id);
+    const uint32_t cb = __ballot_sync(0xffffffffu, cand);
+    int base = 0;
+    if (lane == 0 && cb) base = atomicAdd(ncand, __popc(cb));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (cand) {
+        const int pos = base + __popc(cb & ((1u << lane) - 1u));
+        cand_k[pos] = key;
+        cand_i[pos] = id;
+    }
+    __syncthreads();
+    const int n = *ncand;
+    if (tid < n) {
+        const uint32_t ck = cand_k[tid];
+        const int32_t ci = cand_i[tid];
+        int rr = 0;
+        for (int q = 0; q < n; ++q) rr += key_before(cand_k[q], cand_i[q], ck, ci);
+        if (rr < k) {
+            sel_k[rr] = ck;
+            sel_i[rr] = ci;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) *ncand = 0;
+}
+
+// NGI = I / 64 (1, 2, 4 or 8) is a template parameter: the atom and unit
+// bookkeeping divides by it and by I / 8, and division by a value known only at
+// run time cost tens of instructions per atom.
+template <int NGI>
 __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __grid_constant__ StackParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int H = p.H, E = p.E, k = p.k, I = p.I, U = p.U;
-    const int ngH = H / kGroup, ngI = I / kGroup, nrb = I / 8, nrbB = H / 16;
+    constexpr int ngI = NGI, I = NGI * kGroup, nrb = I / 8;
+    const int H = p.H, E = p.E, k = p.k, U = p.U;
+    const int ngH = H / kGroup, nD = H / 16;
     const uint32_t ubytes = uint32_t(ngH * kAtomBytes), wbytes = uint32_t(ngI * kAtomBytes);
-    const uint64_t down_off = uint64_t(I / 8) * ngH * kAtomBytes;
+    const uint64_t down_off = uint64_t(nrb) * ngH * kAtomBytes;
     const StkSmem L = stk_smem(H, E, I, U, p.nr, p.nu);
     uint16_t *x_s = reinterpret_cast<uint16_t *>(smem + L.x_s);
     float *xsum = reinterpret_cast<float *>(smem + L.xsum);
     uint16_t *rows = reinterpret_cast<uint16_t *>(smem + L.rows);
-    float *zs = reinterpret_cast<float *>(smem + L.zs);
-    int *table = reinterpret_cast<int *>(smem + L.table);
+    int *tables = reinterpret_cast<int *>(smem + L.table);
+    uint8_t *sunit = smem + L.sunit;
     uint8_t *units = smem + L.units;
     uint8_t *wdn = smem + L.wdn;
-    float *hps = reinterpret_cast<float *>(smem + L.hps);
-    uint16_t *hh = reinterpret_cast<uint16_t *>(smem + L.hh);
-    uint16_t *hl = reinterpret_cast<uint16_t *>(smem + L.hl);
-    float *hsum = reinterpret_cast<float *>(smem + L.hsum);
-    float *yp = reinterpret_cast<float *>(smem + L.yp);
-    float2 *red = reinterpret_cast<float2 *>(smem + L.red);     // [nu][warps][8] gate/up partial sums
-    uint32_t *cand_k = reinterpret_cast<uint32_t *>(smem + L.cand);   // [E] candidates
+    float2 *red = reinterpret_cast<float2 *>(smem + L.red);          // [nu + 1][warps][8]
+    uint16_t *hh = reinterpret_cast<uint16_t *>(smem + L.hh);        // [hi, lo][U][I]: h of the layer
+    float *yd = reinterpret_cast<float *>(smem + L.yd);              // [U * ngI atoms][16 rows]
+    float *ysum = reinterpret_cast<float *>(smem + L.ysum);          // [U][16 rows]
+    uint32_t *mx_k = reinterpret_cast<uint32_t *>(smem + L.mx);      // [16] slice maxima
+    int32_t *mx_i = reinterpret_cast<int32_t *>(mx_k + kStkWarps);
+    uint32_t *cand_k = reinterpret_cast<uint32_t *>(smem + L.cand);  // [E] candidates
     int32_t *cand_i = reinterpret_cast<int32_t *>(cand_k + E);
-    uint32_t *mx_k = reinterpret_cast<uint32_t *>(cand_i + E);        // [16] slice maxima
-    int32_t *mx_i = reinterpret_cast<int32_t *>(mx_k + 16);
-    uint32_t *sel_k = reinterpret_cast<uint32_t *>(mx_i + 16);        // [16] chosen, in route order
-    int32_t *sel_i = reinterpret_cast<int32_t *>(sel_k + 16);
+    uint32_t *sel_k = reinterpret_cast<uint32_t *>(smem + L.sel);    // [16] chosen keys, route order
+    int32_t *ids_s = reinterpret_cast<int32_t *>(sel_k + 16);        // [16] chosen experts, route order
     int *ints = reinterpret_cast<int *>(smem + L.ints);
-    int *ids_s = ints;                  // [16] route order
-    float *w_s = reinterpret_cast<float *>(ints + 16);   // [16]
-    float *gate_s = reinterpret_cast<float *>(ints + 32);
-    int *flag_s = ints + 33;
-    int *ncand = ints + 34;
+    float *w_s = reinterpret_cast<float *>(ints);                    // [16]
+    float *gate_s = reinterpret_cast<float *>(ints + 16);
+    int *ncand = ints + 17;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *ubar = bars, *dbar = bars + p.nu, *xbar = dbar + U, *rbar = xbar + 1, *hbar = rbar + 1;
+    uint64_t *ubar = bars, *dbar = bars + p.nu, *xbar = dbar + U, *rbar = xbar + 1, *sbar = rbar + 1,
+             *hbar = sbar + 1;                                       // the layer's h has landed
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, t4 = lane & 3;
     const int G = int(gridDim.x), c = int(blockIdx.x);
-    uint32_t *abortw = p.sync + 3 * p.n_layers;
-    const int nr_mine = c <= E ? (E - c) / G + 1 : 0;           // router rows c, c + G, ... <= E
+    uint32_t *abortw = p.sync + 1;
+    const uint64_t lim = p.wait_ns;
+    const int nr_mine = c <= E ? (E - c) / G + 1 : 0;               // router rows c, c + G, ... <= E
+    const bool has_shared = c < nrb;                                 // the shared expert's unit rb = c
+    const bool has_down = c < nD;                                    // output rows 16 c .. 16 c + 15
+    const int R = k * nrb;                                           // routed units per layer
+    const int ord = c >= nD ? c - nD : c + (G - nD);                 // CTAs without down rows come first
+    const int n_mine = ord < R ? (R - 1 - ord) / G + 1 : 0;          // routed units r = ord + i G
+
+    auto issue_fixed = [&](int l) {                                  // thread 0: what layer l needs that is known early
+        mbar_arrive_expect_tx(rbar, uint32_t(nr_mine * H * 2 + E * 4));
+        for (int j = 0; j < nr_mine; ++j) {
+            const int r = c + j * G;
+            bulk_nohint(rows + size_t(j) * H, r < E ? p.Wr[l] + size_t(r) * H : p.ws[l], uint32_t(H * 2), rbar);
+        }
+        bulk_nohint(tables + (l & 1) * E, p.table + size_t(l) * E, uint32_t(E * 4), rbar);
+    };
+    auto issue_shared_unit = [&](int l) {
+        mbar_arrive_expect_tx(sbar, ubytes);
+        bulk_nohint(sunit, p.shared[l] + size_t(c) * ubytes, ubytes, sbar);
+    };
+    auto issue_shared_down = [&](int l) {
+        mbar_arrive_expect_tx(&dbar[0], wbytes);
+        bulk_nohint(wdn, p.shared[l] + down_off + size_t(c) * wbytes, wbytes, &dbar[0]);
+    };
 
     if (tid == 0) {
-        for (int i = 0; i < p.nu + U + 3; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < p.nu + U + 4; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
+        *ncand = 0;
     }
     __syncthreads();
+    if (tid == 0) {
+        mbar_arrive_expect_tx(xbar, uint32_t(H * 2));
+        bulk_nohint(x_s, p.xs, uint32_t(H * 2), xbar);
+        issue_fixed(0);
+        if (has_shared) issue_shared_unit(0);
+        if (has_down) issue_shared_down(0);
+    }
+    // ---- sentinel fill of the exchange buffers (16-byte stores over the grid),
+    // then one grid-wide arrival before any CTA writes a value
+    {
+        uint4 *xb = reinterpret_cast<uint4 *>(p.xbuf);
+        const uint4 ones = make_uint4(kSentinel32, kSentinel32, kSentinel32, kSentinel32);
+        for (uint64_t i = uint64_t(c) * kStkThreads + tid; i < p.xbuf_words16; i += uint64_t(G) * kStkThreads)
+            xb[i] = ones;
+        __syncthreads();
+        if (tid == 0) ticket_add(&p.sync[0], 1u);
+        grid_wait(&p.sync[0], uint32_t(G), abortw, p.err, lim);
+    }
     const uint64_t pol = policy_evict_first();
-    bool bad = false;                    // this thread's bounded mbarrier wait gave up
+    bool bad = false;                                 // a bounded wait for this CTA's own copies gave up
 
     for (int l = 0; l < p.n_layers; ++l) {
         const uint32_t par = uint32_t(l & 1);
-        uint32_t *cnt = p.sync + 3 * l;
-        const uint8_t *shared = p.shared[l];
-        auto blob_of = [&](int u) -> const uint8_t * {
-            if (u == 0) return shared;
+        const int *table = tables + (l & 1) * E;
+        float *zl = p.zl + size_t(l) * (E + kStackZPad);
+        uint16_t *hx_hi = p.hx + size_t(l) * 2 * U * I, *hx_lo = hx_hi + size_t(U) * I;
+        uint32_t *hcnt = p.hcnt + size_t(l) * U * kStackCntStride;   // expert u's counter at u * stride
+        auto blob_of = [&](int u) -> const uint8_t * {              // u = 0: shared; u >= 1: route position u - 1
+            if (u == 0) return p.shared[l];
             const int64_t slot = table[ids_s[u - 1]];
             if (slot < 0 || slot >= p.n_slots) return nullptr;
             return p.pool + uint64_t(slot) * p.stride;
         };
 
-        // ---- 1. x_l, router rows, slot table row; logits of this CTA's rows
-        if (l > 0) grid_wait(p.sync + 3 * (l - 1) + 2, uint32_t(nrbB), abortw, p.err, flag_s, p.wait_ns);
-        if (tid == 0) {
-            mbar_arrive_expect_tx(xbar, uint32_t(H * 2));
-            bulk_nohint(x_s, p.xs + size_t(l) * H, uint32_t(H * 2), xbar);
-            mbar_arrive_expect_tx(rbar, uint32_t(nr_mine * H * 2 + E * 4));
-            for (int j = 0; j < nr_mine; ++j) {
-                const int r = c + j * G;
-                bulk_nohint(rows + size_t(j) * H, r < E ? p.Wr[l] + size_t(r) * H : p.ws[l], uint32_t(H * 2), rbar);
-            }
-            bulk_nohint(table, p.table + size_t(l) * E, uint32_t(E * 4), rbar);
+        // ---- A. x_l
+        if (l == 0) {
+            if (!bad && !mbar_wait(xbar, 0, p.err)) bad = true;
+        } else if (tid < H / 4) {
+            // H / 4 (a multiple of 64, at most 512) chunks of 8 bytes: whole warps poll
+            const uint16_t *src = p.xe + size_t(l) * H;
+            uint2 v;
+            bool seen = false;
+            poll([&] {
+                if (!seen) {
+                    v = ld_relaxed_v2(src + 4 * tid);
+                    seen = ready16(v.x) && ready16(v.y);
+                }
+                return seen;
+            }, 0xffffffffu, abortw, p.err, lim);
+            *reinterpret_cast<uint2 *>(x_s + 4 * tid) = v;
         }
-        if (!bad && !mbar_wait(xbar, par, p.err)) bad = true;
         if (!bad && !mbar_wait(rbar, par, p.err)) bad = true;
+        __syncthreads();
+
+        // ---- B. logits of this CTA's router rows; per-group sums of x (bias term)
         for (int j = warp; j < nr_mine; j += kStkWarps) {
             const float z = router_dot(rows + size_t(j) * H, x_s, H, lane);
-            if (lane == 0) __stcg(p.logits + size_t(l) * (E + 1) + c + j * G, z);
+            if (lane == 0) st_relaxed(reinterpret_cast<uint32_t *>(zl + c + j * G), canon32(__float_as_uint(z)));
         }
-        for (int grp = warp; grp < ngH; grp += kStkWarps) {          // per-group sums of x (bias term)
+        for (int grp = warp; grp < ngH; grp += kStkWarps) {
             const uint32_t v = *reinterpret_cast<const uint32_t *>(x_s + grp * kGroup + 2 * lane);
             float s = bf16lo(v) + bf16hi(v);
             for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
             if (lane == 0) xsum[grp] = s;
         }
         __syncthreads();
-        if (tid == 0) ticket_add(&cnt[0], 1u);
-
-        // ---- 2. routing, redundantly in every CTA. Warp w holds the keys of slice
-        // w (E / 16 logits); the k-th largest of the 16 slice maxima bounds the
-        // k-th largest key from below (k distinct keys reach it), so only keys at
-        // or above it can be chosen. Each such candidate's rank among the
-        // candidates (larger key first, ties to the lower id) is its place in
-        // route order.
-        // (the failure-detection test hook asks for one arrival more than there are CTAs)
-        grid_wait(&cnt[0], uint32_t(G) + (l == p.stall_layer ? 1u : 0u), abortw, p.err, flag_s, p.wait_ns);
-        for (int e = tid; e <= E; e += kStkThreads) zs[e] = __ldcg(p.logits + size_t(l) * (E + 1) + e);
-        if (tid == 0) *ncand = 0;
-        __syncthreads();
-        {
-            const int spw = (E + kStkWarps - 1) / kStkWarps;        // keys per slice (<= 64)
-            uint32_t kk[2];
-            int32_t ki[2];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int j = lane + 32 * h2, e = warp * spw + j;
-                const bool in = j < spw && e < E;
-                kk[h2] = in ? fkey(zs[e] + (p.bias ? p.bias[e] : 0.f)) : 0u;
-                ki[h2] = in ? e : 0x7fffffff;
-            }
-            const bool second = key_before(kk[1], ki[1], kk[0], ki[0]);
-            const uint32_t bk = second ? kk[1] : kk[0];
-            const int32_t bi = second ? ki[1] : ki[0];
-            const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
-            const int32_t mi = int32_t(__reduce_min_sync(0xffffffffu, uint32_t(bk == mk ? bi : 0x7fffffff)));
-            if (lane == 0) {
-                mx_k[warp] = mk;
-                mx_i[warp] = mi;
-            }
-            __syncthreads();
-            // the k-th largest slice maximum (k <= 16 slices): the one with rank k - 1
-            int rank = 0;
-            if (lane < kStkWarps)
-                for (int j = 0; j < kStkWarps; ++j) rank += key_before(mx_k[j], mx_i[j], mx_k[lane], mx_i[lane]);
-            // (fewer than k slices with keys: no such rank; then every key is a candidate)
-            const int tl = __ffs(__ballot_sync(0xffffffffu, lane < kStkWarps && rank == k - 1)) - 1;
-            const uint32_t t_k = tl >= 0 ? mx_k[tl] : 0u;
-            const int32_t t_i = tl >= 0 ? mx_i[tl] : 0x7fffffff;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
-                if (kk[h2] != 0u && !key_before(t_k, t_i, kk[h2], ki[h2])) {
-                    const int pos = atomicAdd(ncand, 1);
-                    cand_k[pos] = kk[h2];
-                    cand_i[pos] = ki[h2];
-                }
-            __syncthreads();
-            const int n = *ncand;
-            for (int q = tid; q < n; q += kStkThreads) {
-                const uint32_t ck = cand_k[q];
-                const int32_t ci = cand_i[q];
-                int r = 0;
-                for (int j = 0; j < n; ++j) r += key_before(cand_k[j], cand_i[j], ck, ci);
-                if (r < k) {
-                    sel_k[r] = ck;
-                    sel_i[r] = ci;
-                }
-            }
-            __syncthreads();
+        if (tid == 0 && l + 1 < p.n_layers) {                       // the rows are read; the other table is free
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue_fixed(l + 1);
         }
-        if (warp == 0) {
-            const float wl = choice_weight(sel_k, k, lane);
-            if (lane < k) {
-                ids_s[lane] = sel_i[lane];
-                w_s[lane] = wl;
-                if (c == 0) {
-                    p.ids[size_t(l) * k + lane] = sel_i[lane];
-                    p.w[size_t(l) * k + lane] = wl;
-                }
+
+        // ---- C. the shared expert's unit c, while the other CTAs' logits arrive
+        if (has_shared) {
+            if (!bad && !mbar_wait(sbar, par, p.err)) bad = true;
+            const float2 a = gateup_partial(sunit, x_s, xsum, ngH, warp, kStkWarps, lane);
+            if ((lane & 3) == 0) red[(p.nu * kStkWarps + warp) * 8 + (lane >> 2)] = a;
+            __syncthreads();
+            if (warp == 0)
+                finish_unit(red + p.nu * kStkWarps * 8, kStkWarps, true, hx_hi + 8 * c, hx_lo + 8 * c, hcnt, lane);
+            if (tid == 32 && l + 1 < p.n_layers) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_shared_unit(l + 1);
             }
-            if (lane == 0) {
-                *gate_s = shared_gate(zs[E]);
+        }
+
+        // ---- D. every thread polls its logit (thread 0 also the shared-gate
+        // logit, word E, and under the stall hook word E + 1, which nothing
+        // writes), then the CTA's top-k
+        {
+            const int nz = tid == 0 ? (l == p.stall_layer ? 3 : 2) : (tid < E ? 1 : 0);
+            uint32_t zv[3] = {0u, 0u, 0u};
+            uint32_t pend = (1u << nz) - 1u;
+            poll([&] {
+#pragma unroll
+                for (int q = 0; q < 3; ++q)
+                    if (pend >> q & 1u) zv[q] = ld_relaxed(reinterpret_cast<const uint32_t *>(zl + (q == 0 ? tid : E + q - 1)));
+#pragma unroll
+                for (int q = 0; q < 3; ++q)
+                    if ((pend >> q & 1u) && zv[q] != kSentinel32) pend &= ~(1u << q);
+                return pend == 0;
+            }, 0xffffffffu, abortw, p.err, lim);
+            if (tid == 0) {
+                *gate_s = shared_gate(__uint_as_float(zv[1]));
                 if (c == 0) p.gate[l] = *gate_s;
             }
+            block_topk(__uint_as_float(zv[0]), p.bias, E, k, mx_k, mx_i, cand_k, cand_i, ncand, sel_k, ids_s);
+            if (warp == kStkWarps - 1) {                             // weights: needed only by the combine
+                const float wl = choice_weight(sel_k, k, lane);
+                if (lane < k) {
+                    w_s[lane] = wl;
+                    if (c == 0) {
+                        p.ids[size_t(l) * k + lane] = ids_s[lane];
+                        p.w[size_t(l) * k + lane] = wl;
+                    }
+                }
+            }
         }
-        __syncthreads();
 
-        // ---- 3. request this layer's weights (one bulk copy per lane 0 of a warp,
-        // so the copies issue in parallel); prefetch the next layer's fixed ones into L2
+        // ---- E. request the routed units and (CTAs with output rows) the down rows of
+        // every routed expert: lane 0 of warp w issues copy w, w + 16, ... (units
+        // first), so the copies go out in parallel
         if (lane == 0) {
-            const int nd = c < nrbB ? U : 0;
-            for (int it = warp; it < p.nu + nd; it += kStkWarps) {
-                if (it < p.nu) {
-                    const int q = c + it * G, u = q / nrb;
-                    if (u >= U) continue;
+            const int nd = has_down ? k : 0;
+            for (int it = warp; it < n_mine + nd; it += kStkWarps) {
+                if (it < n_mine) {
+                    const int r = ord + it * G, u = 1 + r / nrb, rb = r % nrb;
                     const uint8_t *blob = blob_of(u);
                     if (blob) {
                         mbar_arrive_expect_tx(&ubar[it], ubytes);
-                        bulk_g2s(units + size_t(it) * ubytes, blob + size_t(q % nrb) * ubytes, ubytes, &ubar[it], pol);
+                        bulk_g2s(units + size_t(it) * ubytes, blob + size_t(rb) * ubytes, ubytes, &ubar[it], pol);
                     } else {
                         set_error(p.err, SMOE_DEV_BAD_SLOT);
                         mbar_arrive(&ubar[it]);
                     }
                 } else {
-                    const int u = it - p.nu;
+                    const int u = 1 + (it - n_mine);
                     const uint8_t *blob = blob_of(u);
                     if (blob) {
                         mbar_arrive_expect_tx(&dbar[u], wbytes);
@@ -318,156 +614,125 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                     }
                 }
             }
-            if (warp == kStkWarps - 1 && l + 1 < p.n_layers) {
-                for (int j = 0; j < nr_mine; ++j) {
-                    const int r = c + j * G;
-                    prefetch_l2_bytes(r < E ? p.Wr[l + 1] + size_t(r) * H : p.ws[l + 1], uint32_t(H * 2));
-                }
-                for (int i = 0; i < p.nu; ++i) {
-                    const int q = c + i * G;
-                    if (q < nrb) prefetch_l2_bytes(p.shared[l + 1] + size_t(q) * ubytes, ubytes);
-                }
-                if (c < nrbB) prefetch_l2_bytes(p.shared[l + 1] + down_off + size_t(c) * wbytes, wbytes);
-            }
         }
 
-        // ---- 4. gate/up units -> h. Each warp takes atoms kb = warp, warp + 16, ...
-        // of the CTA's units one after another, with no CTA barrier between units.
-        // The token is MMA column 0, so lanes 4 g (t4 = 0) hold the partial sums of
-        // rows g (gate) and g + 8 (up); they go to red[unit][warp][g]. After one
-        // barrier warp i reduces unit i over the warps in order.
-        int n_mine = 0;                                             // this CTA's units (uniform)
-        for (int i = 0; i < p.nu; ++i) {
-            const int q = c + i * G, u = q / nrb;
-            if (u >= U) break;                                      // uniform
-            ++n_mine;
-            const bool valid = blob_of(u) != nullptr;               // uniform
+        // ---- F. routed gate/up units as they land; then warp i finishes unit i
+        for (int i = 0; i < n_mine; ++i) {
+            const int r = ord + i * G;
+            const bool valid = blob_of(1 + r / nrb) != nullptr;     // uniform
             if (!bad && !mbar_wait(&ubar[i], par, p.err)) bad = true;
-            float aG = 0.f, aU = 0.f;
-            if (valid && !bad) {
-                const uint8_t *ubase = units + size_t(i) * ubytes;
-                for (int kb = warp; kb < ngH; kb += kStkWarps) {
-                    const uint8_t *atom = ubase + kb * kAtomBytes;
-                    const uint4 A = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
-                    const uint2 SB = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
-                    const int col = kb * kGroup + 16 * t4;
-                    uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
-                    if (g == 0) {                                   // the token is MMA column 0
-                        xa = *reinterpret_cast<const uint4 *>(x_s + col);
-                        xb = *reinterpret_cast<const uint4 *>(x_s + col + 8);
-                    }
-                    const uint32_t xl[4] = {xa.x, xa.y, xa.z, xa.w}, xr[4] = {xb.x, xb.y, xb.z, xb.w};
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int m = 0; m < 4; m += 2) {
-                        const uint32_t a0[4] = {nib_pair(A.x, m), nib_pair(A.z, m), nib_pair(A.y, m), nib_pair(A.w, m)};
-                        const uint32_t a1[4] = {nib_pair(A.x, m + 1), nib_pair(A.z, m + 1), nib_pair(A.y, m + 1),
-                                                nib_pair(A.w, m + 1)};
-                        mma_bf16(acc, a0, xl[m], xr[m]);
-                        mma_bf16(acc2, a1, xl[m + 1], xr[m + 1]);
-                    }
-                    float sg, bpg, su, bpu;
-                    scale_bias(SB.x, sg, bpg);
-                    scale_bias(SB.y, su, bpu);
-                    aG += fmaf(sg, acc[0] + acc2[0], bpg * xsum[kb]);
-                    aU += fmaf(su, acc[2] + acc2[2], bpu * xsum[kb]);
-                }
-            }
-            if (t4 == 0) red[(i * kStkWarps + warp) * 8 + g] = make_float2(aG, aU);
+            float2 a = make_float2(0.f, 0.f);
+            if (valid && !bad) a = gateup_partial(units + size_t(i) * ubytes, x_s, xsum, ngH, warp, kStkWarps, lane);
+            if ((lane & 3) == 0) red[(i * kStkWarps + warp) * 8 + (lane >> 2)] = a;
         }
         __syncthreads();
-        if (warp < n_mine) {
-            const int i = warp, q = c + i * G, u = q / nrb, rb = q % nrb;
-            const bool valid = blob_of(u) != nullptr;
-            const float2 *ri = red + i * kStkWarps * 8 + g;
-            float aG = ri[0].x, aU = ri[0].y;
-#pragma unroll
-            for (int w = 1; w < kStkWarps; ++w) {
-                const float2 v = ri[w * 8];
-                aG += v.x;
-                aU += v.y;
-            }
-            // intermediate 8 rb + g (the four lanes of a g hold the same sums). h goes
-            // out as bf16 hi and lo = bf16(h - hi), with the unit's sum of hi + lo over
-            // its 8 intermediates (the down rows' bias term)
-            const float hv = (valid && !bad) ? silu(aG) * aU : 0.f;
-            const uint16_t hi = f32_to_bf16_bits(hv);
-            const uint16_t lo = f32_to_bf16_bits(hv - __uint_as_float(uint32_t(hi) << 16));
-            float sum = __uint_as_float(uint32_t(hi) << 16) + __uint_as_float(uint32_t(lo) << 16);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-            uint16_t *hrow = p.h + (size_t(l) * 2 * U + u) * I;
-            if (t4 == 0) {
-                __stcg(hrow + 8 * rb + g, hi);
-                __stcg(hrow + size_t(U) * I + 8 * rb + g, lo);
-            }
-            if (lane == 0) __stcg(p.hps + (size_t(l) * U + u) * nrb + rb, sum);
+        for (int i = warp; i < n_mine; i += kStkWarps) {
+            const int r = ord + i * G, u = 1 + r / nrb, rb = r % nrb;
+            finish_unit(red + i * kStkWarps * 8, kStkWarps, blob_of(u) != nullptr && !bad,
+                        hx_hi + size_t(u) * I + 8 * rb, hx_lo + size_t(u) * I + 8 * rb,
+                        hcnt + size_t(u) * kStackCntStride, lane);
         }
-        __syncthreads();
-        if (tid == 0) ticket_add(&cnt[1], 1u);
 
-        // ---- 5. down rows of every expert for rows 16 c .. 16 c + 15, combine
-        if (c < nrbB) {
-            grid_wait(&cnt[1], uint32_t(G), abortw, p.err, flag_s, p.wait_ns);
-            // h rows of every expert (hi, lo; padded rows), and the unit sums: one bulk
-            // copy per lane of warp 0
+        // ---- G. down rows 16 c .. 16 c + 15 of every expert, combine -> x_{l+1}.
+        // Warp 0 polls the U experts' arrival counters (one per 128-byte line)
+        // until every unit's h is in, then bulk-copies the layer's h into shared
+        // memory; warp w takes atoms a = w, w + 16, ... (expert u = a / (I/64),
+        // group kb = a % (I/64)), two at a time.
+        if (has_down) {
             if (warp == 0) {
-                if (lane == 0) mbar_arrive_expect_tx(hbar, uint32_t(U * I * 4 + U * nrb * 4));
-                __syncwarp();
-                const uint16_t *hl_src = p.h + size_t(l) * 2 * U * I;
-                for (int j = lane; j < 2 * U + 1; j += 32) {
-                    if (j < U)
-                        bulk_nohint(hh + j * (I + 8), hl_src + size_t(j) * I, uint32_t(I * 2), hbar);
-                    else if (j < 2 * U)
-                        bulk_nohint(hl + (j - U) * (I + 8), hl_src + size_t(U + (j - U)) * I, uint32_t(I * 2), hbar);
-                    else
-                        bulk_nohint(hps, p.hps + size_t(l) * U * nrb, uint32_t(U * nrb * 4), hbar);
+                uint32_t pend = lane < U ? 1u : 0u;
+                poll([&] {
+                    if (pend && ld_acquire(hcnt + size_t(lane) * kStackCntStride) >= uint32_t(nrb)) pend = 0;
+                    return pend == 0;
+                }, 0xffffffffu, abortw, p.err, lim);
+                // h ([hi, lo][U][I]) by two bulk copies: whole lines, so each L2 line
+                // is requested once per CTA, not once per 16 bytes; the proxy fence
+                // makes what the acquire saw visible to the copies
+                if (lane == 0) {
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    const uint32_t hb = uint32_t(U * I * 2);
+                    mbar_arrive_expect_tx(hbar, 2 * hb);
+                    bulk_nohint(hh, hx_hi, hb, hbar);
+                    bulk_nohint(hh + size_t(U) * I, hx_lo, hb, hbar);
                 }
             }
             if (!bad && !mbar_wait(hbar, par, p.err)) bad = true;
-            for (int it = tid; it < U * ngI; it += kStkThreads) {   // group sums: the 8 unit sums in order
-                const float *ps = hps + it * 8;
-                float s2 = 0.f;
+            const int na = U * ngI, nj = (na - warp + kStkWarps - 1) / kStkWarps;   // this warp's atoms
+            for (int j = 0; j < nj; j += 2) {
+                const bool two = j + 1 < nj;
+                const int a0 = warp + kStkWarps * j, a1 = a0 + kStkWarps;
+                const int u0 = a0 / ngI, u1 = two ? a1 / ngI : u0;
+                if (!bad && !mbar_wait(&dbar[u0], par, p.err)) bad = true;
+                if (two && !bad && !mbar_wait(&dbar[u1], par, p.err)) bad = true;
+                uint4 h[4];                                          // atom 0: h0 h1, atom 1: h0 h1
 #pragma unroll
-                for (int j = 0; j < 8; ++j) s2 += ps[j];
-                hsum[it * kDecodeMaxT] = s2;
-            }
-            __syncthreads();
-            const int nkh = ngI >= 2 ? 2 : 1;
-            for (int it = warp; it < U * nkh; it += kStkWarps) {
-                const int u = it / nkh, kh = it % nkh;
-                const int kbeg = kh * (ngI / nkh), kend = kh + 1 == nkh ? ngI : kbeg + ngI / nkh;
-                const bool valid = blob_of(u) != nullptr;
-                float y[4] = {0.f, 0.f, 0.f, 0.f};
-                if (!bad && !mbar_wait(&dbar[u], par, p.err)) bad = true;
-                if (valid && !bad)
-                    down_rows(wdn + size_t(u) * wbytes, 0, ngI, kbeg, kend, hh + u * (I + 8), hl + u * (I + 8),
-                              hsum + u * ngI * kDecodeMaxT, I, 1, lane, y);
-                if (t4 == 0) {                                       // token = column 0
-                    yp[(u * 2 + kh) * 16 + g] = y[0];
-                    yp[(u * 2 + kh) * 16 + g + 8] = y[2];
+                for (int q = 0; q < 4; ++q) h[q] = make_uint4(0, 0, 0, 0);
+                if (lane < 8) {                  // B columns 0 (high parts, lanes 0..3) and 1 (low parts, 4..7)
+                    const int part = lane >> 2, t4 = lane & 3;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q < 2 || two) {
+                            const int a = q < 2 ? a0 : a1;
+                            h[q] = *reinterpret_cast<const uint4 *>(hh + (size_t(part) * U + a / ngI) * I +
+                                                                    (a % ngI) * kGroup + 16 * t4 + 8 * (q & 1));
+                        }
+                }
+                const float gs0 = group_sum(h[0], h[1]);
+                const float gs1 = group_sum(h[2], h[3]);
+                float2 y0 = make_float2(0.f, 0.f), y1 = y0;
+                if (blob_of(u0) != nullptr && !bad)
+                    y0 = down_atom(wdn + size_t(u0) * wbytes + (a0 % ngI) * kAtomBytes, h[0], h[1], gs0, lane);
+                if (two && blob_of(u1) != nullptr && !bad)
+                    y1 = down_atom(wdn + size_t(u1) * wbytes + (a1 % ngI) * kAtomBytes, h[2], h[3], gs1, lane);
+                if ((lane & 3) == 0) {
+                    yd[a0 * 16 + (lane >> 2)] = y0.x;
+                    yd[a0 * 16 + (lane >> 2) + 8] = y0.y;
+                    if (two) {
+                        yd[a1 * 16 + (lane >> 2)] = y1.x;
+                        yd[a1 * 16 + (lane >> 2) + 8] = y1.y;
+                    }
                 }
             }
-            if (nkh == 1)
-                for (int i = tid; i < U * 16; i += kStkThreads) yp[((i / 16) * 2 + 1) * 16 + i % 16] = 0.f;
+            __syncthreads();
+            if (tid == 0 && l + 1 < p.n_layers) {                   // the shared down rows are read
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_shared_down(l + 1);
+            }
+            if (tid < U * 16) {                                      // expert u, row r: its groups in order
+                const int u = tid >> 4, r = tid & 15;
+                float s = 0.f;
+                for (int kb = 0; kb < ngI; ++kb) s += yd[(u * ngI + kb) * 16 + r];
+                ysum[tid] = s;
+            }
             __syncthreads();
             if (tid < 16) {
                 const int row = 16 * c + tid;
-                auto yv = [&](int u) { return yp[(u * 2) * 16 + tid] + yp[(u * 2 + 1) * 16 + tid]; };
                 float acc = 0.f;
-                for (int j = 0; j < k; ++j) acc = fmaf(w_s[j], yv(j + 1), acc);
-                acc = fmaf(*gate_s, yv(0), acc);
+                for (int j = 0; j < k; ++j) acc = fmaf(w_s[j], ysum[(j + 1) * 16 + tid], acc);
+                acc = fmaf(*gate_s, ysum[tid], acc);
                 acc += __uint_as_float(uint32_t(x_s[row]) << 16);
-                p.xs[size_t(l + 1) * H + row] = f32_to_bf16_bits(acc);
+                const uint16_t o = f32_to_bf16_bits(acc);
+                p.xs[size_t(l + 1) * H + row] = o;
+                st_relaxed_u16(p.xe + size_t(l + 1) * H + row, canon16(o));
             }
-            __syncthreads();
-            if (tid == 0) ticket_add(&cnt[2], 1u);
         }
+        // the next layer's copies overwrite regions read through the generic proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
     }
 }
 
 // ---------------------------------------------------------------------- host
+
+static const void *stack_kernel_for(int ngI)
+{
+    switch (ngI) {
+    case 1: return reinterpret_cast<const void *>(&decode_stack_kernel<1>);
+    case 2: return reinterpret_cast<const void *>(&decode_stack_kernel<2>);
+    case 4: return reinterpret_cast<const void *>(&decode_stack_kernel<4>);
+    default: return reinterpret_cast<const void *>(&decode_stack_kernel<8>);
+    }
+}
 
 cudaError_t stack_config(smoe_ctx *ctx)
 {
@@ -481,14 +746,18 @@ cudaError_t stack_config(smoe_ctx *ctx)
     c.grid = ctx->num_sms;
     c.U = s.k + 1;
     c.nr = (s.E + 1 + c.grid - 1) / c.grid;
-    c.nu = (c.U * (s.I / 8) + c.grid - 1) / c.grid;
+    c.nu = (s.k * (s.I / 8) + c.grid - 1) / c.grid;
     c.smem = stk_smem(s.H, s.E, s.I, c.U, c.nr, c.nu).total;
-    c.ok = coop && c.grid >= s.H / 16 && s.E % 4 == 0 && c.nu <= kStkWarps && c.smem <= max_smem;
+    const int ngI = s.I / kGroup;
+    const bool ngi_ok = ngI == 1 || ngI == 2 || ngI == 4 || ngI == 8;
+    c.ok = coop && ngi_ok && c.grid >= s.H / 16 && c.grid >= s.I / 8 && s.E % 4 == 0 && s.E <= kStkMaxE &&
+           c.nu <= kStkWarps && c.smem <= max_smem;
     if (!c.ok) return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_stack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, c.smem);
+    const void *kern = stack_kernel_for(ngI);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, c.smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stack_kernel, kStkThreads, c.smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kStkThreads, c.smem);
     if (e != cudaSuccess) return e;
     c.ok = per_sm >= 1;
     return cudaSuccess;
@@ -496,7 +765,7 @@ cudaError_t stack_config(smoe_ctx *ctx)
 
 cudaError_t launch_stack(const smoe_ctx *ctx, const StackParams &p, cudaStream_t st)
 {
-    cudaError_t e = cudaMemsetAsync(p.sync, 0, size_t(3 * p.n_layers + 1) * 4, st);
+    cudaError_t e = cudaMemsetAsync(p.sync, 0, p.sync_bytes, st);
     if (e == cudaSuccess) e = prof_record(ctx->nprof > 0 ? ctx->prof[0] : nullptr, st);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute at[1];
@@ -509,7 +778,11 @@ cudaError_t launch_stack(const smoe_ctx *ctx, const StackParams &p, cudaStream_t
     lc.stream = st;
     lc.attrs = at;
     lc.numAttrs = 1;
-    e = cudaLaunchKernelEx(&lc, decode_stack_kernel, p);
+    const int ngI = p.I / kGroup;
+    if (ngI == 1) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<1>, p);
+    else if (ngI == 2) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<2>, p);
+    else if (ngI == 4) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<4>, p);
+    else e = cudaLaunchKernelEx(&lc, decode_stack_kernel<8>, p);
     if (e == cudaSuccess) e = prof_record(ctx->nprof > 1 ? ctx->prof[1] : nullptr, st);
     return e;
 }

@@ -14,23 +14,26 @@
 namespace smoe {
 
 // One router row (bf16 [H]) dotted with one token (bf16 [H]) by a warp: lane l
-// takes columns 8 l .. 8 l + 7 of every 256, fp32 fused multiply-adds in that
-// order, then a butterfly sum. Every lane returns the total.
+// takes columns 8 l .. 8 l + 7 of every 256; within them column 8 l + j goes
+// to partial sum j % 4 (four independent fp32 chains of fused multiply-adds,
+// in column order), the four are added as (s0 + s1) + (s2 + s3), then a
+// butterfly sum over the lanes. Every lane returns the total.
 __device__ __forceinline__ float router_dot(const uint16_t *row, const uint16_t *x, int H, int lane)
 {
-    float acc = 0.f;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
     for (int c = 8 * lane; c < H; c += 256) {
         const uint4 wv = *reinterpret_cast<const uint4 *>(row + c);
         const uint4 xv = *reinterpret_cast<const uint4 *>(x + c);
-        acc = fmaf(bf16lo(wv.x), bf16lo(xv.x), acc);
-        acc = fmaf(bf16hi(wv.x), bf16hi(xv.x), acc);
-        acc = fmaf(bf16lo(wv.y), bf16lo(xv.y), acc);
-        acc = fmaf(bf16hi(wv.y), bf16hi(xv.y), acc);
-        acc = fmaf(bf16lo(wv.z), bf16lo(xv.z), acc);
-        acc = fmaf(bf16hi(wv.z), bf16hi(xv.z), acc);
-        acc = fmaf(bf16lo(wv.w), bf16lo(xv.w), acc);
-        acc = fmaf(bf16hi(wv.w), bf16hi(xv.w), acc);
+        s0 = fmaf(bf16lo(wv.x), bf16lo(xv.x), s0);
+        s1 = fmaf(bf16hi(wv.x), bf16hi(xv.x), s1);
+        s2 = fmaf(bf16lo(wv.y), bf16lo(xv.y), s2);
+        s3 = fmaf(bf16hi(wv.y), bf16hi(xv.y), s3);
+        s0 = fmaf(bf16lo(wv.z), bf16lo(xv.z), s0);
+        s1 = fmaf(bf16hi(wv.z), bf16hi(xv.z), s1);
+        s2 = fmaf(bf16lo(wv.w), bf16lo(xv.w), s2);
+        s3 = fmaf(bf16hi(wv.w), bf16hi(xv.w), s3);
     }
+    float acc = (s0 + s1) + (s2 + s3);
     for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     return acc;
 }

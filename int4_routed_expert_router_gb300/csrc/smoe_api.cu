@@ -544,9 +544,12 @@ extern "C" int smoe_set_profile_events(smoe_ctx *ctx, void *const *events, int32
     return SMOE_OK;
 }
 
-// Workspace of moe_decode_stack: logits [n][E + 1], h [n][U][I] fp32, counters.
+// Workspace of moe_decode_stack: the arrival words and h's per-expert
+// counters (zeroed at launch), the exchange region the kernel fills with its
+// sentinel (logits [n][E + kStackZPad] fp32, x [n + 1][H] bf16), then h
+// [n][2][U][I] bf16 (read only after its counter says it is complete).
 struct StackWs {
-    uint64_t logits, h, hps, sync, total;
+    uint64_t sync, hcnt, zl, xe, xend, hx, total;
 };
 
 static StackWs stack_ws(const smoe_ctx *ctx, int n)
@@ -555,10 +558,12 @@ static StackWs stack_ws(const smoe_ctx *ctx, int n)
     const smoe_shape &s = ctx->shape;
     StackWs w = {};
     uint64_t o = 0;
-    w.logits = o; o = al(o + uint64_t(n) * (s.E + 1) * 4);
-    w.h = o;      o = al(o + uint64_t(n) * ctx->stack.U * s.I * 4);
-    w.hps = o;    o = al(o + uint64_t(n) * ctx->stack.U * (s.I / 8) * 4);
-    w.sync = o;   o = al(o + (3 * uint64_t(n) + 1) * 4);
+    w.sync = o;   o = al(o + kStackSyncBytes);
+    w.hcnt = o;   o = al(o + uint64_t(n) * ctx->stack.U * kStackCntStride * 4);
+    w.zl = o;     o = al(o + uint64_t(n) * (s.E + kStackZPad) * 4);
+    w.xe = o;     o = al(o + (uint64_t(n) + 1) * s.H * 2);
+    w.xend = o;
+    w.hx = o;     o = al(o + uint64_t(n) * 2 * ctx->stack.U * s.I * 2);
     w.total = o;
     return w;
 }
@@ -602,10 +607,14 @@ extern "C" int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_
     p.table = ctx->table_dev + size_t(first_layer) * ctx->shape.E;
     p.stride = ctx->layout.blob;
     p.n_slots = ctx->n_slots;
-    p.logits = reinterpret_cast<float *>(ws + W.logits);
-    p.h = reinterpret_cast<uint16_t *>(ws + W.h);
-    p.hps = reinterpret_cast<float *>(ws + W.hps);
+    p.zl = reinterpret_cast<float *>(ws + W.zl);
+    p.hx = reinterpret_cast<uint16_t *>(ws + W.hx);
+    p.xe = reinterpret_cast<uint16_t *>(ws + W.xe);
+    p.xbuf = ws + W.zl;
+    p.xbuf_words16 = (W.xend - W.zl) / 16;
     p.sync = reinterpret_cast<uint32_t *>(ws + W.sync);
+    p.hcnt = reinterpret_cast<uint32_t *>(ws + W.hcnt);
+    p.sync_bytes = W.zl;                           // the counters and arrival words, zeroed per launch
     p.err = err;
     p.wait_ns = ctx->stack_wait_ns ? ctx->stack_wait_ns : kWaitLimitNs;
     p.stall_layer = ctx->stack_stall_layer;

@@ -50,6 +50,9 @@ struct DecodeCfg {
 
 // Multi-layer decode step (decode_stack.cu), one token.
 constexpr int kStackMaxLayers = 64;
+constexpr int kStackSyncBytes = 64;         // start-of-launch arrival counter, abort word
+constexpr int kStackCntStride = 32;         // words between two experts' arrival counters (one 128-byte line)
+constexpr int kStackZPad = 8;               // a logit row holds E + kStackZPad words (E % 4 == 0)
 
 struct StackCfg {
     bool ok = false;          // cooperative launch available and the shared memory fits
@@ -73,10 +76,16 @@ struct StackParams {
     const int32_t *table;                      // slot table rows of the layers [n_layers][E]
     uint64_t stride;
     int64_t n_slots;
-    float *logits;                             // [n_layers][E + 1]
-    uint16_t *h;                               // [n_layers][2][U][I] bf16: h's high part, then h - high
-    float *hps;                                // [n_layers][U][I / 8] sum of hi + lo per 8-row unit
-    uint32_t *sync;                            // [n_layers][3] arrival counters, then the abort word
+    // exchange buffers, one region filled with the all-ones sentinel at launch:
+    float *zl;                                 // [n_layers][E + kStackZPad] logits (word E: shared gate)
+    uint16_t *hx;                              // [n_layers][2][U][I] bf16: h's high part, then h - high
+                                               // (not part of the filled region: guarded by hcnt)
+    uint16_t *xe;                              // [n_layers + 1][H] bf16: each layer's output
+    void *xbuf;                                // the region (16-byte aligned)
+    uint64_t xbuf_words16;                     // its size in 16-byte words
+    uint32_t *sync;                            // kStackSyncBytes: [0] start arrivals, [1] abort word
+    uint32_t *hcnt;                            // [n_layers][U][kStackCntStride] arrival counters of h (zeroed)
+    uint64_t sync_bytes;                       // bytes from sync zeroed at launch (sync and hcnt)
     int32_t *err;
     uint64_t wait_ns;                          // limit of a grid-wide wait
     int stall_layer;                           // test hook: this layer's first grid-wide wait never completes (-1: off)
