@@ -17,7 +17,8 @@
  * 64 along the input dimension, an fp16 scale s and bias b per group,
  * w = s*q + b (the same xix.ai page, last paragraph, names MLX-style int4 and
  * int8 group quantisation with 64-bit offsets). 8-bit experts are supported
- * for packing, routing and the plain debug path (see smoe_ctx_create). The routed experts of every layer live in
+ * for packing, routing, the T <= 8 expert kernel and the plain debug path
+ * (see smoe_ctx_create). The routed experts of every layer live in
  * one pool of fixed-stride blobs, one blob per expert, reached through a slot
  * table (same page, paragraph on how it works: fixed-stride blobs, one read
  * per expert, a bounded slot pool).
@@ -74,8 +75,8 @@ extern "C" {
 /* H: hidden size; E: routed experts per layer; k: experts per token;
  * I: routed expert intermediate size; I_shared: shared expert intermediate
  * size; group: quantisation group (must be 64); bits: 4, or 8 (layout,
- * packing, routing and moe_forward_debug; the fast expert kernels take 4-bit
- * experts, see smoe_ctx_create).
+ * packing, routing, moe_forward for T <= 8 and moe_forward_debug; see
+ * smoe_ctx_create).
  * Supported: H % 256 == 0, H <= 2048, I % 64 == 0, 64 <= I <= 512, I_shared == I,
  * 1 <= k <= 16, k <= E <= 1024. Others return SMOE_ENOTSUP. */
 typedef struct smoe_shape {
@@ -165,9 +166,10 @@ typedef struct smoe_ctx smoe_ctx;
  * of n_layers layers and a pool of n_slots slots. table_dev is caller-owned
  * device memory of n_layers*E int32 (the slot table; filled by
  * set_slot_table). The context allocates no device memory. A context of
- * 8-bit experts (shape.bits = 8) serves moe_route and moe_forward_debug;
- * moe_forward, moe_forward_noalloc and moe_decode_stack return SMOE_ENOTSUP
- * for it (their kernels read 4-bit atoms).
+ * 8-bit experts (shape.bits = 8) serves moe_route, moe_forward for T <= 8
+ * (the fused decode kernel reads both nibble planes) and moe_forward_debug;
+ * moe_forward for T > 8, moe_forward_noalloc and moe_decode_stack return
+ * SMOE_ENOTSUP for it (their kernels read 4-bit atoms).
  * Errors: SMOE_EINVAL, SMOE_ENOTSUP, SMOE_ECUDA. */
 SMOE_API int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_t n_slots,
                     int32_t *table_dev, smoe_ctx **out);

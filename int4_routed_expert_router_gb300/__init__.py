@@ -152,8 +152,8 @@ def _stream(stream) -> int | None:
 
 def make_shape(H, E, k, I, I_shared=None, bits=4) -> Shape:
     """bits = 8: MLX's 8-bit format, for the layout, host and device packing,
-    routing and moe_forward_debug; the fast expert kernels (moe_forward,
-    moe_forward_noalloc, moe_decode_stack) return ENOTSUP for it."""
+    routing, moe_forward with T <= 8 and moe_forward_debug; moe_forward with
+    T > 8, moe_forward_noalloc and moe_decode_stack return ENOTSUP for it."""
     return Shape(H, E, k, I, I if I_shared is None else I_shared, 64, bits)
 
 

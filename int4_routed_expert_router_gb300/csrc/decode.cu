@@ -43,14 +43,21 @@ __host__ __device__ inline int red_entries(int ncw, int H, int cs)
     return m > 1 ? m : 1;
 }
 
-__host__ __device__ inline DecodeSmem decode_smem(int T, int H, int I, int cs, int ncw)
+// Bytes of one ring slot (one 256-column chunk of a CTA's gate/up rows) for
+// BITS-bit atoms.
+__host__ __device__ constexpr int chunk_bytes(int bits)
+{
+    return kRowBlocksA * (kChunkCols / kGroup) * (bits == 8 ? kAtom8Bytes : kAtomBytes);
+}
+
+__host__ __device__ inline DecodeSmem decode_smem(int T, int H, int I, int cs, int ncw, int bits)
 {
     DecodeSmem L;
     L.nst = H / kChunkCols;
     int o = 0;
     L.x_s = o;    o = align128(o + T * (2 * H + 16));
     L.xsum = o;   o = align128(o + (H / kGroup) * kDecodeMaxT * 4);
-    L.ring = o;   o = align128(o + L.nst * kChunkBytes);
+    L.ring = o;   o = align128(o + L.nst * chunk_bytes(bits));
     L.hslice = o; o = align128(o + kDecodeMaxT * kSlice * 4);
     L.hhi = o;    o = align128(o + T * (I + 8) * 2);
     L.hlo = o;    o = align128(o + T * (I + 8) * 2);
@@ -68,15 +75,20 @@ __device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint3
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-template <int NCW>
+// BITS: 4, or 8 for MLX 8-bit experts (two-plane atoms; each plane runs the
+// 4-bit fragment path and the group epilogue weights the high plane by 16).
+template <int NCW, int BITS>
 __global__ void __launch_bounds__((NCW + 1) * 32, 16 / NCW) decode_kernel(const DecodeParams p)
 {
+    using Fmt = AtomFmt<BITS>;
+    constexpr int NP = BITS == 8 ? 2 : 1;           // nibble planes per atom
+    constexpr int kCB = chunk_bytes(BITS);          // ring slot bytes
     constexpr int kCons = NCW * 32;                 // consumer threads (named barrier 1)
     constexpr int kGQ = NCW / 4;                    // warps sharing one gate/up row block
     constexpr int kGPW = (kChunkCols / kGroup) / kGQ;   // groups per chunk per warp
     extern __shared__ __align__(1024) uint8_t smem[];
     const int T = p.T, H = p.H, I = p.I, k = p.k;
-    const DecodeSmem L = decode_smem(T, H, I, p.cs, NCW);
+    const DecodeSmem L = decode_smem(T, H, I, p.cs, NCW, BITS);
     const int nst = L.nst;
     uint16_t *x_s = reinterpret_cast<uint16_t *>(smem + L.x_s);
     float *xsum = reinterpret_cast<float *>(smem + L.xsum);      // [H/64][8]
@@ -103,9 +115,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 16 / NCW) decode_kernel(const 
     const int rowsB = H / p.cs;
     const int nrbB = rowsB / 16;
     const int splitB = NCW > nrbB ? NCW / nrbB : 1;      // NCW, nrbB powers of two
-    const uint32_t wB_bytes = uint32_t(nrbB * ngI * kAtomBytes);
-    const int nB = int((wB_bytes + kChunkBytes - 1) / kChunkBytes);   // phase B slots (<= nst)
-    const uint64_t down_off = uint64_t(I / 8) * ngH * kAtomBytes;
+    const uint32_t wB_bytes = uint32_t(nrbB * ngI * Fmt::bytes);
+    const int nB = int((wB_bytes + kCB - 1) / kCB);      // phase B slots (<= nst)
+    const uint64_t down_off = uint64_t(I / 8) * ngH * Fmt::bytes;
     const bool producer = warp == NCW;
     const int xstride = H + 8;
 
@@ -131,17 +143,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 16 / NCW) decode_kernel(const 
     // producer: fill f of slot s (waits for the consumers to free the previous fill)
     auto fill_slot = [&](int s, uint32_t f, const uint8_t *blob, bool phaseA) {
         if (f >= 1 && !mbar_wait(&empty[s], (f - 1) & 1, p.err)) return false;
-        uint8_t *dst = ring + s * kChunkBytes;
+        uint8_t *dst = ring + s * kCB;
         if (phaseA) {
-            mbar_arrive_expect_tx(&full[s], kChunkBytes);
-            const int per_rb = (kChunkCols / kGroup) * kAtomBytes;
+            mbar_arrive_expect_tx(&full[s], kCB);
+            const int per_rb = (kChunkCols / kGroup) * Fmt::bytes;
             for (int rb = 0; rb < kRowBlocksA; ++rb) {
                 const uint64_t atom = uint64_t(rank * kRowBlocksA + rb) * ngH + uint64_t(s) * (kChunkCols / kGroup);
-                bulk_g2s(dst + rb * per_rb, blob + atom * kAtomBytes, per_rb, &full[s], pol_stream);
+                bulk_g2s(dst + rb * per_rb, blob + atom * Fmt::bytes, per_rb, &full[s], pol_stream);
             }
         } else {
-            const uint32_t off = uint32_t(s) * kChunkBytes;
-            const uint32_t bytes = wB_bytes - off < uint32_t(kChunkBytes) ? wB_bytes - off : uint32_t(kChunkBytes);
+            const uint32_t off = uint32_t(s) * kCB;
+            const uint32_t bytes = wB_bytes - off < uint32_t(kCB) ? wB_bytes - off : uint32_t(kCB);
             mbar_arrive_expect_tx(&full[s], bytes);
             bulk_g2s(dst, blob + down_off + uint64_t(rank) * wB_bytes + off, bytes, &full[s], pol_stream);
         }
@@ -214,13 +226,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 16 / NCW) decode_kernel(const 
                 }
                 for (int c = 0; c < nst; ++c) {
                     if (!bad && !mbar_wait(&full[c], fills(vit, c) & 1, p.err)) bad = true;
-                    const uint8_t *base = ring + c * kChunkBytes + rb * (kChunkCols / kGroup) * kAtomBytes;
+                    const uint8_t *base = ring + c * kCB + rb * (kChunkCols / kGroup) * Fmt::bytes;
 #pragma unroll
                     for (int gg = 0; gg < kGPW; ++gg) {
                         const int gl = gq * kGPW + gg;
-                        const uint8_t *atom = base + gl * kAtomBytes;
-                        const uint4 A = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
-                        const uint2 SB = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+                        const uint8_t *atom = base + gl * Fmt::bytes;
+                        const uint2 SB = *reinterpret_cast<const uint2 *>(atom + Fmt::sb + 8 * g);
                         const int grp = c * (kChunkCols / kGroup) + gl;
                         const int col = grp * kGroup + 16 * t4;
                         uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
@@ -230,24 +241,37 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 16 / NCW) decode_kernel(const 
                         }
                         const uint32_t xl[4] = {xa.x, xa.y, xa.z, xa.w};
                         const uint32_t xh4[4] = {xb.x, xb.y, xb.z, xb.w};
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+                        float v[4];
 #pragma unroll
-                        for (int m = 0; m < 4; m += 2) {   // two independent chains of two
-                            const uint32_t a0[4] = {nib_pair(A.x, m), nib_pair(A.z, m), nib_pair(A.y, m),
-                                                    nib_pair(A.w, m)};
-                            const uint32_t a1[4] = {nib_pair(A.x, m + 1), nib_pair(A.z, m + 1),
-                                                    nib_pair(A.y, m + 1), nib_pair(A.w, m + 1)};
-                            mma_bf16(acc, a0, xl[m], xh4[m]);
-                            mma_bf16(acc2, a1, xl[m + 1], xh4[m + 1]);
+                        for (int pl = 0; pl < NP; ++pl) {         // nibble planes (8-bit: low, then high)
+                            const uint4 A = *reinterpret_cast<const uint4 *>(atom + pl * kAtomQBytes + 16 * lane);
+                            float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int m = 0; m < 4; m += 2) {   // two independent chains of two
+                                const uint32_t a0[4] = {nib_pair(A.x, m), nib_pair(A.z, m), nib_pair(A.y, m),
+                                                        nib_pair(A.w, m)};
+                                const uint32_t a1[4] = {nib_pair(A.x, m + 1), nib_pair(A.z, m + 1),
+                                                        nib_pair(A.y, m + 1), nib_pair(A.w, m + 1)};
+                                mma_bf16(acc, a0, xl[m], xh4[m]);
+                                mma_bf16(acc2, a1, xl[m + 1], xh4[m + 1]);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                v[i] = pl == 0 ? acc[i] + acc2[i] : fmaf(16.f, acc[i] + acc2[i], v[i]);
                         }
                         const float2 X = *reinterpret_cast<const float2 *>(xsum + grp * kDecodeMaxT + 2 * t4);
                         float sg, bpg, su, bpu;
-                        scale_bias(SB.x, sg, bpg);
-                        scale_bias(SB.y, su, bpu);
-                        aG0 += fmaf(sg, acc[0] + acc2[0], bpg * X.x);
-                        aG1 += fmaf(sg, acc[1] + acc2[1], bpg * X.y);
-                        aU0 += fmaf(su, acc[2] + acc2[2], bpu * X.x);
-                        aU1 += fmaf(su, acc[3] + acc2[3], bpu * X.y);
+                        if (BITS == 8) {
+                            scale_bias8(SB.x, sg, bpg);
+                            scale_bias8(SB.y, su, bpu);
+                        } else {
+                            scale_bias(SB.x, sg, bpg);
+                            scale_bias(SB.y, su, bpu);
+                        }
+                        aG0 += fmaf(sg, v[0], bpg * X.x);
+                        aG1 += fmaf(sg, v[1], bpg * X.y);
+                        aU0 += fmaf(su, v[2], bpu * X.x);
+                        aU1 += fmaf(su, v[3], bpu * X.y);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[c]);
@@ -319,7 +343,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 16 / NCW) decode_kernel(const 
                 const int kbeg = sp * kb_per < ngI ? sp * kb_per : ngI;
                 const int kend = kbeg + kb_per < ngI ? kbeg + kb_per : ngI;
                 float y[4] = {0.f, 0.f, 0.f, 0.f};
-                if (valid && !bad) down_rows(ring, rbB, ngI, kbeg, kend, hhi, hlo, xh, I, T, lane, y);
+                if (valid && !bad) down_rows<BITS>(ring, rbB, ngI, kbeg, kend, hhi, hlo, xh, I, T, lane, y);
                 if (valid) {
                     __syncwarp();
                     if (lane == 0)
@@ -337,7 +361,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 16 / NCW) decode_kernel(const 
             } else {
                 for (int rbB = warp; rbB < nrbB; rbB += NCW) {
                     float y[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (valid && !bad) down_rows(ring, rbB, ngI, 0, ngI, hhi, hlo, xh, I, T, lane, y);
+                    if (valid && !bad) down_rows<BITS>(ring, rbB, ngI, 0, ngI, hhi, hlo, xh, I, T, lane, y);
                     store(rbB, y);
                 }
                 if (valid) {
@@ -396,20 +420,20 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 16 / NCW) decode_kernel(const 
     }
 }
 
-template <int NCW>
+template <int NCW, int BITS>
 static cudaError_t config_one(smoe_ctx *ctx, int max_smem_optin, int *smem_out, int *clusters_out)
 {
     const smoe_shape &s = ctx->shape;
     int worst = 0;
     for (int T = 1; T <= kDecodeMaxT; ++T) {
-        const int sm = decode_smem(T, s.H, s.I, ctx->cs, NCW).total;
+        const int sm = decode_smem(T, s.H, s.I, ctx->cs, NCW, BITS).total;
         smem_out[T] = sm;
         if (sm > worst) worst = sm;
     }
     if (worst > max_smem_optin) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<NCW>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<NCW, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
     if (e == cudaSuccess && ctx->cs > 8)
-        e = cudaFuncSetAttribute(decode_kernel<NCW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(decode_kernel<NCW, BITS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     for (int T = 1; T <= kDecodeMaxT; ++T) {
         cudaLaunchConfig_t lc = {};
@@ -424,22 +448,23 @@ static cudaError_t config_one(smoe_ctx *ctx, int max_smem_optin, int *smem_out, 
         lc.attrs = at;
         lc.numAttrs = 1;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, decode_kernel<NCW>, &lc);
+        e = cudaOccupancyMaxActiveClusters(&n, decode_kernel<NCW, BITS>, &lc);
         if (e != cudaSuccess) return e;
         clusters_out[T] = n;
     }
     return cudaSuccess;
 }
 
-cudaError_t decode_config(smoe_ctx *ctx)
+template <int BITS>
+static cudaError_t decode_config_bits(smoe_ctx *ctx)
 {
     int max_smem_optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device);
     if (e != cudaSuccess) return e;
     int sm8[kDecodeMaxT + 1], cl8[kDecodeMaxT + 1], sm16[kDecodeMaxT + 1], cl16[kDecodeMaxT + 1];
-    e = config_one<8>(ctx, max_smem_optin, sm8, cl8);
+    e = config_one<8, BITS>(ctx, max_smem_optin, sm8, cl8);
     if (e != cudaSuccess) return e;
-    e = config_one<16>(ctx, max_smem_optin, sm16, cl16);
+    e = config_one<16, BITS>(ctx, max_smem_optin, sm16, cl16);
     if (e != cudaSuccess) return e;
     for (int T = 1; T <= kDecodeMaxT; ++T) {
         if (cl8[T] < 1) return cudaErrorInvalidConfiguration;
@@ -450,6 +475,26 @@ cudaError_t decode_config(smoe_ctx *ctx)
         ctx->decode[T].max_clusters16 = cl16[T];
     }
     return cudaSuccess;
+}
+
+cudaError_t decode_config(smoe_ctx *ctx)
+{
+    ctx->decode_ok = false;
+    if (ctx->shape.bits == 8) {
+        // 8-bit contexts also serve routing and the plain path, so a shape whose
+        // 8-bit ring does not fit leaves the fast kernel unavailable (ENOTSUP)
+        // instead of failing the context
+        const cudaError_t e = decode_config_bits<8>(ctx);
+        if (e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration) {
+            cudaGetLastError();
+            return cudaSuccess;
+        }
+        if (e == cudaSuccess) ctx->decode_ok = true;
+        return e;
+    }
+    const cudaError_t e = decode_config_bits<4>(ctx);
+    if (e == cudaSuccess) ctx->decode_ok = true;
+    return e;
 }
 
 cudaError_t launch_decode(const smoe_ctx *ctx, const DecodeParams &p0, cudaStream_t st)
@@ -477,7 +522,9 @@ cudaError_t launch_decode(const smoe_ctx *ctx, const DecodeParams &p0, cudaStrea
     at[1].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = at;
     lc.numAttrs = 2;
-    return wide ? cudaLaunchKernelEx(&lc, decode_kernel<16>, p) : cudaLaunchKernelEx(&lc, decode_kernel<8>, p);
+    if (ctx->shape.bits == 8)
+        return wide ? cudaLaunchKernelEx(&lc, decode_kernel<16, 8>, p) : cudaLaunchKernelEx(&lc, decode_kernel<8, 8>, p);
+    return wide ? cudaLaunchKernelEx(&lc, decode_kernel<16, 4>, p) : cudaLaunchKernelEx(&lc, decode_kernel<8, 4>, p);
 }
 
 }  // namespace smoe

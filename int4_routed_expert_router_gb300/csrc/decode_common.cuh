@@ -18,28 +18,52 @@ __device__ __forceinline__ void scale_bias(uint32_t sb, float &s, float &bp)
     bp = fmaf(-128.f, s, half_bits_to_f32(uint16_t(sb >> 16)));
 }
 
+// s (low half) and b (high half) of one fp16 pair for an 8-bit atom: s and
+// b - 2176 s. With q = lo + 16 hi and the (128 + nibble) fragments of the two
+// planes, sum_c (s q_c + b) x_c = s (acc_lo + 16 acc_hi) + (b - 2176 s) sum_c x_c
+// (128 + 16 * 128 = 2176).
+__device__ __forceinline__ void scale_bias8(uint32_t sb, float &s, float &bp)
+{
+    s = half_bits_to_f32(uint16_t(sb & 0xffff));
+    bp = fmaf(-2176.f, s, half_bits_to_f32(uint16_t(sb >> 16)));
+}
+
+// Atom geometry of a BITS-bit blob: bytes per atom and the offset of its
+// (s, b) pairs; an 8-bit atom holds the low-nibble plane at 0 and the
+// high-nibble plane at kAtomQBytes, each in the 4-bit lane layout.
+template <int BITS> struct AtomFmt {
+    static constexpr int bytes = BITS == 8 ? kAtom8Bytes : kAtomBytes;
+    static constexpr int sb = BITS == 8 ? 2 * kAtomQBytes : kAtomQBytes;
+};
+
 // Down rows of one 16-row block over groups [kbeg, kend) of h, h given as bf16
 // hi + lo parts ([T][I + 8] each) and per-group sums xh[group][8] of hi + lo.
 // wB: the block's atoms, rbB * ngI + kb indexing. y = rows (g, g+8) x tokens
 // (2 t4, 2 t4 + 1). Groups two at a time; per group the hi and lo halves of h
-// accumulate in separate chains.
+// accumulate in separate chains (for 8-bit atoms, per nibble plane as well).
+template <int BITS>
 __device__ __forceinline__ void down_rows(const uint8_t *wB, int rbB, int ngI, int kbeg, int kend,
                                           const uint16_t *hhi, const uint16_t *hlo, const float *xh, int I,
                                           int T, int lane, float (&y)[4])
 {
+    using F = AtomFmt<BITS>;
+    constexpr int NP = BITS == 8 ? 2 : 1;                 // nibble planes
     const int g = lane >> 2, t4 = lane & 3;
     for (int kb0 = kbeg; kb0 < kend; kb0 += 2) {
-        float acc[2][2][4];
-        uint4 A[2];
+        float acc[2][NP][2][4];
+        uint4 A[2][NP];
         uint2 SB[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int kb = kb0 + q < kend ? kb0 + q : kb0;
-            const uint8_t *atom = wB + (rbB * ngI + kb) * kAtomBytes;
-            A[q] = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
-            SB[q] = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+            const uint8_t *atom = wB + (rbB * ngI + kb) * F::bytes;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[q][0][i] = acc[q][1][i] = 0.f;
+            for (int pl = 0; pl < NP; ++pl) {
+                A[q][pl] = *reinterpret_cast<const uint4 *>(atom + pl * kAtomQBytes + 16 * lane);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[q][pl][0][i] = acc[q][pl][1][i] = 0.f;
+            }
+            SB[q] = *reinterpret_cast<const uint2 *>(atom + F::sb + 8 * g);
         }
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -55,12 +79,14 @@ __device__ __forceinline__ void down_rows(const uint8_t *wB, int rbB, int ngI, i
             const uint32_t ha_[4] = {ha.x, ha.y, ha.z, ha.w}, hb_[4] = {hb.x, hb.y, hb.z, hb.w};
             const uint32_t la_[4] = {la.x, la.y, la.z, la.w}, lb_[4] = {lb.x, lb.y, lb.z, lb.w};
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t a[4] = {nib_pair(A[q].x, m), nib_pair(A[q].z, m), nib_pair(A[q].y, m),
-                                       nib_pair(A[q].w, m)};
-                mma_bf16(acc[q][0], a, ha_[m], hb_[m]);
-                mma_bf16(acc[q][1], a, la_[m], lb_[m]);
-            }
+            for (int pl = 0; pl < NP; ++pl)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint4 Ap = A[q][pl];
+                    const uint32_t a[4] = {nib_pair(Ap.x, m), nib_pair(Ap.z, m), nib_pair(Ap.y, m), nib_pair(Ap.w, m)};
+                    mma_bf16(acc[q][pl][0], a, ha_[m], hb_[m]);
+                    mma_bf16(acc[q][pl][1], a, la_[m], lb_[m]);
+                }
         }
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -68,12 +94,23 @@ __device__ __forceinline__ void down_rows(const uint8_t *wB, int rbB, int ngI, i
             const int kb = kb0 + q;
             const float2 X = *reinterpret_cast<const float2 *>(xh + kb * kDecodeMaxT + 2 * t4);
             float s0, bp0, s1, bp1;
-            scale_bias(SB[q].x, s0, bp0);
-            scale_bias(SB[q].y, s1, bp1);
-            y[0] += fmaf(s0, acc[q][0][0] + acc[q][1][0], bp0 * X.x);
-            y[1] += fmaf(s0, acc[q][0][1] + acc[q][1][1], bp0 * X.y);
-            y[2] += fmaf(s1, acc[q][0][2] + acc[q][1][2], bp1 * X.x);
-            y[3] += fmaf(s1, acc[q][0][3] + acc[q][1][3], bp1 * X.y);
+            if (BITS == 8) {
+                scale_bias8(SB[q].x, s0, bp0);
+                scale_bias8(SB[q].y, s1, bp1);
+            } else {
+                scale_bias(SB[q].x, s0, bp0);
+                scale_bias(SB[q].y, s1, bp1);
+            }
+            float v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[i] = acc[q][0][0][i] + acc[q][0][1][i];
+                if (NP == 2) v[i] = fmaf(16.f, acc[q][NP - 1][0][i] + acc[q][NP - 1][1][i], v[i]);
+            }
+            y[0] += fmaf(s0, v[0], bp0 * X.x);
+            y[1] += fmaf(s0, v[1], bp0 * X.y);
+            y[2] += fmaf(s1, v[2], bp1 * X.x);
+            y[3] += fmaf(s1, v[3], bp1 * X.y);
         }
     }
 }

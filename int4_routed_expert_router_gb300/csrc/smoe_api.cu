@@ -102,7 +102,6 @@ void pack_host(const smoe_shape &s, const smoe_expert_src &src, uint8_t *dst)
 // one. The pages name int4/int8 group quantisation ("Swiftlet Packs 80B Qwen
 // Into Mac...", last paragraph). The layout, the host and device packers and
 // the plain debug path take 8-bit experts; the fast expert kernels do not.
-constexpr int kAtom8Bytes = 2 * kAtomQBytes + 64;    // 1088
 
 Layout layout8_of(int H, int I)
 {
@@ -439,7 +438,8 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
 {
     if (!ctx || T < 0 || T > SMOE_MAX_TOKENS) return SMOE_EINVAL;
     if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
-    if (ctx->shape.bits != 4) return SMOE_ENOTSUP;   // the expert kernels take 4-bit atoms
+    // 8-bit experts: the T <= 8 kernel only (the bucketed path takes 4-bit atoms)
+    if (ctx->shape.bits != 4 && (T > kDecodeMaxT || !ctx->decode_ok)) return SMOE_ENOTSUP;
     if (T == 0) return SMOE_OK;                      // nothing to do; the buffers may be null
     if (!x || !ids || !w || !gate || !pool || !shared_blob || !out || !workspace || !err) return SMOE_EINVAL;
     if (!aligned16(x) || !aligned16(pool) || !aligned16(shared_blob) || !aligned16(workspace) || !aligned16(out) ||

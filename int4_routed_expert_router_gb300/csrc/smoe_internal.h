@@ -12,6 +12,7 @@ constexpr int kGroup = 64;          // quantisation group along the input dim
 constexpr int kAtomRows = 16;       // rows per atom
 constexpr int kAtomQBytes = 512;    // packed nibbles of one atom
 constexpr int kAtomBytes = 576;     // nibbles + 16 (s, b) fp16 pairs
+constexpr int kAtom8Bytes = 2 * kAtomQBytes + 64;   // 8-bit atom: two nibble planes, then the (s, b) pairs
 
 // Decode kernel (fused experts, T <= kDecodeMaxT).
 constexpr int kDecodeMaxT = 8;
@@ -107,6 +108,7 @@ struct smoe_ctx {
     int nprof;
     smoe::DecodeCfg decode[smoe::kDecodeMaxT + 1];
     smoe::StackCfg stack;
+    bool decode_ok;                          // the T <= 8 expert kernel runs this shape's experts
     uint64_t stack_wait_ns;                  // grid-wide wait limit of moe_decode_stack (smoe_set_stack_wait)
     int32_t stack_stall_layer;               // -1, or the layer whose first grid-wide wait is made to run out
 };

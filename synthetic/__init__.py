@@ -222,6 +222,7 @@ class Workload:
     zipf: bool
     seed: int
     description: str
+    bits: int = 4          # expert weights: MLX 4-bit or 8-bit affine
 
 
 WORKLOADS = {
@@ -238,5 +239,8 @@ WORKLOADS = {
                  "80B-shaped prefill: T=8192, uniform router"),
         Workload("prefill35b", 2048, 256, 8, 512, 512, 8192, 1, False, False, 3592,
                  "35B-shaped prefill: T=8192, uniform router"),
+        Workload("decode80b_int8", 2048, 512, 10, 512, 512, 1, 48, True, False, 8008,
+                 "80B-A3B-shaped decode with MLX 8-bit experts: H=2048, E=512, k=10, I=512, T=1, 48 layers, "
+                 "permuted slots", bits=8),
     ]
 }

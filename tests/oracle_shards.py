@@ -11,7 +11,8 @@ rows, shared-gate vector, logit offsets or None). A worker routes x with the
 oracle (keeping the probabilities) and combines the experts named by ``ids``
 (the GPU's choice) with the weights the method gives that choice: the oracle's
 probabilities of those experts, renormalised over them. With ids=None it
-combines the oracle's own choice.
+combines the oracle's own choice. 8-bit workloads use the oracle's 8-bit
+combine.
 """
 from __future__ import annotations
 
@@ -40,9 +41,11 @@ def layer_piece(args):
     r_ids, r_w, r_gate, probs = oracle.route(x, Wr, ws, wl.k, bias=bias, want_probs=True)
     use = r_ids if ids is None else np.ascontiguousarray(ids, np.int32)
     w_used = r_w if ids is None else own_choice_weights(probs, use)
-    experts = {int(e): synthetic.expert_triples(wl.seed, layer, int(e), wl.H, wl.I) for e in np.unique(use)}
-    shared = synthetic.expert_triples(wl.seed, layer, None, wl.H, wl.I_shared)
-    out64, outb = oracle.combine(x, use, w_used, r_gate, experts, shared, wl.E, wl.I, wl.I_shared)
+    bits = wl.bits
+    experts = {int(e): synthetic.expert_triples(wl.seed, layer, int(e), wl.H, wl.I, bits=bits) for e in np.unique(use)}
+    shared = synthetic.expert_triples(wl.seed, layer, None, wl.H, wl.I_shared, bits=bits)
+    combine = oracle.combine8 if bits == 8 else oracle.combine
+    out64, outb = combine(x, use, w_used, r_gate, experts, shared, wl.E, wl.I, wl.I_shared)
     return dict(ids=r_ids, w=r_w, gate=r_gate, probs=probs, out64=out64, out_bf16=outb, w_used=w_used)
 
 

@@ -1,0 +1,100 @@
+"""GPU: MLX 8-bit experts through the fused decode kernel (moe_forward,
+T <= 8), against the oracle's 8-bit layer, element by element: the 80B shape
+at T = 1 and 8 on the GPU's own routing, bit-identity across reruns and slot
+permutations, agreement with the plain CUDA path, and the calls that still
+take only 4-bit experts."""
+import numpy as np
+import pytest
+import torch
+
+import int4_routed_expert_router_gb300 as smoe
+import oracle_shards
+import synthetic
+import workload as W
+from test_gpu_parity import assert_output_close, gpu_forward, gpu_route, routing_ok
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from int4_routed_expert_router_gb300 import _build
+    from synthetic import _build as sb
+    _build.build()
+    sb.build()
+
+
+@pytest.fixture(scope="module")
+def p80_8():
+    wl = synthetic.WORKLOADS["decode80b_int8"]
+    return W.DevicePool(wl, n_layers=2), W.LayerInputs(wl, 2)
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_8bit_decode_against_oracle(p80_8, T):
+    pool, inp = p80_8
+    wl = pool.wl
+    for layer in (0, 1):
+        x = synthetic.activations(wl.seed, T, wl.H, tag=300 + 10 * layer + T)
+        ids, w, gate = gpu_route(pool, inp, layer, x)
+        ref = oracle_shards.tokens_sharded(wl.name, layer, x, ids, inp.Wr_bits[layer], inp.ws_bits[layer])
+        routing_ok(ids, w, gate, ref, wl.k)
+        out = gpu_forward(pool, layer, x, ids, w, gate)
+        assert_output_close(out, ref["out64"])
+        res = gpu_forward(pool, layer, x, ids, w, gate, residual=True)
+        xr = synthetic.bf16_bits_to_f32(x).astype(np.float64)
+        assert_output_close(res, xr + ref["out64"])
+
+
+def test_8bit_bit_identical_across_runs_and_slot_permutations(p80_8):
+    pool, inp = p80_8
+    wl = pool.wl
+    perm = np.random.default_rng(21).permutation(2 * wl.E).astype(np.int32).reshape(2, wl.E)
+    other = W.DevicePool(wl, n_layers=2, table=perm)
+    for T in (1, 4):
+        x = synthetic.activations(wl.seed, T, wl.H, tag=700 + T)
+        ids, w, gate = gpu_route(pool, inp, 1, x)
+        a = gpu_forward(pool, 1, x, ids, w, gate)
+        assert np.array_equal(a, gpu_forward(pool, 1, x, ids, w, gate))
+        assert np.array_equal(a, gpu_forward(other, 1, x, ids, w, gate))
+
+
+def test_8bit_fast_and_plain_paths_agree(p80_8):
+    """Two approximations of the oracle's layer: within twice the layer bounds
+    of each other, and each within the bounds of the oracle."""
+    pool, inp = p80_8
+    wl = pool.wl
+    T = 3
+    x = synthetic.activations(wl.seed, T, wl.H, tag=777)
+    ids, w, gate = gpu_route(pool, inp, 0, x)
+    fast = gpu_forward(pool, 0, x, ids, w, gate)
+    out = torch.zeros((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, dt)).cuda()
+    smoe.moe_forward_debug(pool.ctx, 0, W.bf16_tensor(x), dev(ids, np.int32), dev(w, np.float32),
+                           dev(gate, np.float32), pool.pool, pool.shared[0], out, err)
+    assert smoe.check(err) == 0
+    ref = oracle_shards.tokens_sharded(wl.name, 0, x, ids, inp.Wr_bits[0], inp.ws_bits[0])
+    f = synthetic.bf16_bits_to_f32(fast).astype(np.float64)
+    d = synthetic.bf16_bits_to_f32(W.bits_of(out)).astype(np.float64)
+    assert_output_close(W.bits_of(out), ref["out64"])
+    assert np.linalg.norm(f - d) <= 2 * 5e-3 * np.linalg.norm(ref["out64"])
+
+
+def test_8bit_calls_that_take_only_4bit_experts(p80_8):
+    pool, inp = p80_8
+    wl = pool.wl
+    T = 9                                                 # the token-bucketed path reads 4-bit atoms
+    x = W.bf16_tensor(synthetic.activations(wl.seed, T, wl.H, tag=5))
+    ids = torch.zeros((T, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, wl.k), dtype=torch.float32, device="cuda")
+    gate = torch.zeros((T,), dtype=torch.float32, device="cuda")
+    out = torch.zeros((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.moe_forward(pool.ctx, 0, x, ids, w, gate, pool.pool, pool.shared[0], out, W.workspace(pool.ctx, T), err)
+    assert ei.value.status == smoe.ENOTSUP
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.moe_forward_noalloc(pool.ctx, 0, x[:2], ids[:2], w[:2], gate[:2], pool.pool, pool.shared[0], out[:2], err)
+    assert ei.value.status == smoe.ENOTSUP
+    assert pool.ctx.stack_workspace_bytes(2) == 0

@@ -62,8 +62,9 @@ def test_debug_path_matches_oracle_and_fast_kernels(name, Ts):
 
 def test_debug_path_8_bit_experts_match_oracle():
     """8-bit experts (two-plane atoms, packed on the host) through the plain
-    CUDA path, against the oracle's 8-bit layer on the same routing; the fast
-    paths refuse an 8-bit context."""
+    CUDA path and the fused decode kernel, against the oracle's 8-bit layer
+    on the same routing; moe_forward_noalloc and the stack refuse an 8-bit
+    context."""
     wl = synthetic.WORKLOADS["tiny"]
     shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I, bits=8)
     stride = smoe.layout_of(shape).blob_bytes
@@ -90,10 +91,12 @@ def test_debug_path_8_bit_experts_match_oracle():
                                dev(gate, np.float32), pool, shared, out, err)
         assert smoe.check(err) == 0
         assert_output_close(W.bits_of(out), ref)
-    with pytest.raises(smoe.SmoeError) as ei:
-        smoe.moe_forward(ctx, 0, W.bf16_tensor(x), dev(ids, np.int32), dev(w, np.float32), dev(gate, np.float32),
-                         pool, shared, out, W.workspace(ctx, T), err)
-    assert ei.value.status == smoe.ENOTSUP
+    # the fused decode kernel reads 8-bit atoms too (T <= 8): the same layer
+    fast = torch.zeros((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    smoe.moe_forward(ctx, 0, W.bf16_tensor(x), dev(ids, np.int32), dev(w, np.float32), dev(gate, np.float32),
+                     pool, shared, fast, W.workspace(ctx, T), err)
+    assert smoe.check(err) == 0
+    assert_output_close(W.bits_of(fast), ref)
     with pytest.raises(smoe.SmoeError) as ei:
         smoe.moe_forward_noalloc(ctx, 0, W.bf16_tensor(x), dev(ids, np.int32), dev(w, np.float32),
                                  dev(gate, np.float32), pool, shared, out, err)

@@ -62,7 +62,7 @@ class DevicePool:
         self.wl = wl
         L = wl.n_layers if n_layers is None else n_layers
         self.n_layers = L
-        self.shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I, wl.I_shared)
+        self.shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I, wl.I_shared, bits=wl.bits)
         self.layout = smoe.layout_of(self.shape)
         self.stride = int(self.layout.blob_bytes)
         self.table = synthetic.slot_table(wl.seed, L, wl.E, wl.permuted_slots) if table is None else table
@@ -81,12 +81,12 @@ class DevicePool:
         chunk = 128
         for e0 in range(0, wl.E, chunk):
             n = min(chunk, wl.E - e0)
-            ts = device_triples(wl.seed, layer, e0, n, wl.H, wl.I)
+            ts = device_triples(wl.seed, layer, e0, n, wl.H, wl.I, bits=wl.bits)
             experts = [[t[i] for t in ts] for i in range(n)]
             slots = [int(self.table[layer, e0 + i]) for i in range(n)]
             smoe.pack_experts(self.shape, experts, slots, self.pool, self.pool.numel(), smoe.DEVICE)
             torch.cuda.synchronize()
-        ts = device_triples(wl.seed, layer, synthetic.SHARED_EXPERT_CODE, 1, wl.H, wl.I_shared)
+        ts = device_triples(wl.seed, layer, synthetic.SHARED_EXPERT_CODE, 1, wl.H, wl.I_shared, bits=wl.bits)
         smoe.pack_experts(self.shape, [[t[0] for t in ts]], [0], self.shared[layer],
                           self.stride, smoe.DEVICE)
 
