@@ -6,7 +6,8 @@ CUDA library never imports, links or calls it, and it never imports the CUDA
 library. All arithmetic lives in the C file; this wrapper only marshals numpy
 arrays (inputs come from ``synthetic``).
 
-Functions and the passages they follow are documented in ``smoe_oracle.c``.
+Functions and the passages they follow are documented in ``smoe_oracle.c``
+and ``gdn_oracle.c`` (the Gated DeltaNet recurrence step).
 """
 from __future__ import annotations
 
@@ -76,6 +77,8 @@ def lib():
         L.orc_blob_bytes8.restype = C.c_uint64
         L.orc_blob_to_mlx8.argtypes = [_u8p, C.c_int, C.c_int] + [_u32p, _u16p, _u16p] * 3
         L.orc_blob_to_mlx8.restype = None
+        L.orc_gdn_step.argtypes = [C.c_int] * 6 + [_u16p, _u16p, _u16p, _f64p, _f64p, C.c_double, _f64p, _f64p]
+        L.orc_gdn_step.restype = C.c_int
         _lib = L
     return _lib
 
@@ -329,3 +332,25 @@ def layer(wl, seed_layer: int, x, Wr, ws, bias=None, want_probs=False):
     out64, outb = combine(x, ids, w, gate, experts, shared, wl.E, wl.I, wl.I_shared)
     return dict(ids=ids, w=w, gate=gate, out64=out64, out_bf16=outb,
                 probs=(r[3] if want_probs else None))
+
+
+# ------------------------------------------------------- Gated DeltaNet step
+
+def gdn_step(q, k, v, g, beta, state, scale=None):
+    """One Gated DeltaNet recurrence step per token (gdn_oracle.c): q, k bf16
+    bits [T][B][n_k][d_k], v [T][B][n_v][d_v], g, beta [T][B][n_v] (float),
+    state [B][n_v][d_v][d_k] float64 (not modified). scale defaults to
+    d_k ** -0.5. Returns (new state, out [T][B][n_v][d_v] float64)."""
+    q = np.ascontiguousarray(q, np.uint16)
+    k = np.ascontiguousarray(k, np.uint16)
+    v = np.ascontiguousarray(v, np.uint16)
+    T, B, nk, dk = q.shape
+    nv, dv = v.shape[2], v.shape[3]
+    S = np.array(state, dtype=np.float64, copy=True, order="C")
+    out = np.empty((T, B, nv, dv), np.float64)
+    sc = dk ** -0.5 if scale is None else float(scale)
+    rc = lib().orc_gdn_step(T, B, nk, nv, dk, dv, q, k, v, np.ascontiguousarray(g, np.float64),
+                            np.ascontiguousarray(beta, np.float64), sc, S, out)
+    if rc != 0:
+        raise ValueError("oracle: bad Gated DeltaNet shape")
+    return S, out

@@ -8,16 +8,16 @@ import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SRC = os.path.join(HERE, "smoe_oracle.c")
+SRCS = [os.path.join(HERE, "smoe_oracle.c"), os.path.join(HERE, "gdn_oracle.c")]
 LIB = os.path.join(HERE, "liboracle.so")
 
 
 def build(force: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
+    if not force and os.path.exists(LIB) and all(os.path.getmtime(LIB) >= os.path.getmtime(s) for s in SRCS):
         return LIB
     tmp = LIB + ".tmp%d" % os.getpid()
     cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-           "-shared", "-Wall", "-Wextra", "-Wno-unused-parameter", "-o", tmp, SRC, "-lm"]
+           "-shared", "-Wall", "-Wextra", "-Wno-unused-parameter", "-o", tmp] + SRCS + ["-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

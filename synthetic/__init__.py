@@ -244,3 +244,46 @@ WORKLOADS = {
                  "permuted slots", bits=8),
     ]
 }
+
+
+# ------------------------------------------------- Gated DeltaNet step inputs
+
+@dataclasses.dataclass(frozen=True)
+class GdnShape:
+    """One Gated DeltaNet layer's recurrence shape: n_k query/key heads, n_v
+    value heads (n_v / n_k value heads share a query/key head), head dims
+    d_k, d_v; B sequences; T tokens per call."""
+    name: str
+    nk: int
+    nv: int
+    dk: int
+    dv: int
+    B: int
+    T: int
+    seed: int
+    description: str
+
+
+GDN_WORKLOADS = {
+    w.name: w for w in [
+        GdnShape("gdn_tiny", 2, 4, 32, 32, 3, 2, 501, "tiny Gated DeltaNet: 2 key heads, 4 value heads, d=32"),
+        GdnShape("gdn80b", 16, 32, 128, 128, 128, 1, 502,
+                 "Qwen3-Next-80B-shaped Gated DeltaNet decode step: 16 key heads, 32 value heads, d_k = d_v = 128, "
+                 "128 sequences, one token each"),
+    ]
+}
+
+
+def gdn_inputs(seed: int, T: int, B: int, nk: int, nv: int, dk: int, dv: int, tag: int = 0):
+    """Seeded inputs of T Gated DeltaNet steps: q, k bf16 bits [T][B][nk][dk]
+    and v [T][B][nv][dv] ~ N(0, 1); the gate's log decay g ~ U[-2, -0.01] and
+    the write strength beta ~ U[0.05, 0.95], fp32 [T][B][nv]; a starting
+    state ~ N(0, 0.1), fp32 [B][nv][dv][dk] (a state in mid-sequence)."""
+    q = normal_bf16(seed, 7000 + 16 * tag + 1, (T, B, nk, dk), 1.0)
+    k = normal_bf16(seed, 7000 + 16 * tag + 2, (T, B, nk, dk), 1.0)
+    v = normal_bf16(seed, 7000 + 16 * tag + 3, (T, B, nv, dv), 1.0)
+    rng = _philox(seed, 7000 + 16 * tag + 4)
+    g = rng.uniform(-2.0, -0.01, size=(T, B, nv)).astype(np.float32)
+    beta = rng.uniform(0.05, 0.95, size=(T, B, nv)).astype(np.float32)
+    state = (rng.standard_normal((B, nv, dv, dk)) * 0.1).astype(np.float32)
+    return q, k, v, g, beta, state

@@ -11,7 +11,8 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SRC = os.path.join(ROOT, "oracle", "smoe_oracle.c")
+SRCS = {"smoe": os.path.join(ROOT, "oracle", "smoe_oracle.c"), "gdn": os.path.join(ROOT, "oracle", "gdn_oracle.c")}
+PINS = [os.path.join(ROOT, "tests", "test_oracle_pins.py"), os.path.join(ROOT, "tests", "test_oracle_gdn.py")]
 
 MUTATIONS = {
     "gate_up_swapped": ("hbuf[i] = silu(g) * u;", "hbuf[i] = silu(u) * g;"),
@@ -38,21 +39,34 @@ MUTATIONS = {
     "dense_combine_shared_term_dropped": ("o[c] += y[c] * gate[t];", "o[c] += 0.0 * y[c] * gate[t];"),
     "router_row_col_swapped": ("acc += orc_bf16_to_f64(xt[h]) * orc_bf16_to_f64(Wr[(size_t)e * H + h]);",
                                "acc += orc_bf16_to_f64(xt[h]) * orc_bf16_to_f64(Wr[(size_t)h * E + e % E]);"),
+    # the Gated DeltaNet step (gdn_oracle.c)
+    "gdn_decay_missing_on_read": ("double c = bt * (orc_bf16_to_f64(vv[i]) - alpha * u);",
+                                  "double c = bt * (orc_bf16_to_f64(vv[i]) - u);"),
+    "gdn_output_before_update": ("row[j] = alpha * row[j] + c * kn[j];\n                        oi += row[j] * qn[j];",
+                                 "oi += row[j] * qn[j];\n                        row[j] = alpha * row[j] + c * kn[j];"),
+    "gdn_key_not_unit": ("normalise(k + kq, dk, 1.0, kn);", "normalise(k + kq, dk, 2.0, kn);"),
+    "gdn_query_is_key": ("normalise(q + kq, dk, scale, qn);", "normalise(k + kq, dk, scale, qn);"),
+    "gdn_head_grouping": ("int hk = h / (nv / nk);", "int hk = h % nk;"),
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pins_catch_planted_mistake(name, tmp_path):
     old, new = MUTATIONS[name]
-    src = open(SRC).read()
-    assert src.count(old) == 1, "mutation anchor not found: " + name
-    mutated = tmp_path / "mutant.c"
-    mutated.write_text(src.replace(old, new))
+    which = "gdn" if name.startswith("gdn_") else "smoe"
+    srcs = []
+    for key, path in SRCS.items():
+        src = open(path).read()
+        if key == which:
+            assert src.count(old) == 1, "mutation anchor not found: " + name
+            src = src.replace(old, new)
+        out = tmp_path / (key + ".c")
+        out.write_text(src)
+        srcs.append(str(out))
     lib = tmp_path / "libmutant.so"
     subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
-                    "-o", str(lib), str(mutated), "-lm"], check=True)
+                    "-o", str(lib)] + srcs + ["-lm"], check=True)
     env = dict(os.environ, SMOE_ORACLE_LIB=str(lib))
-    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider"] + PINS,
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, "pins did not catch mutation %s:\n%s" % (name, r.stdout[-2000:])
