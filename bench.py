@@ -12,9 +12,10 @@ Prints one JSON line. value = MoE-layer tokens/s = T * layers * steps / time
 larger than the 129 MB L2 and each step streams 934 MB of distinct expert
 blobs, so no L2 flush is needed between steps. After the headline the other
 target configurations (--extra: T=8192 prefill, Zipf-skewed T=64, 35B-shaped
-decode) are measured the same way and reported under "configs" in the same
-line; a configuration whose distinct blobs fit twice in L2 is timed step by
-step with a 256 MB write between steps.
+decode, 8-bit experts, and the 80B Gated DeltaNet recurrence step) are
+measured the same way and reported under "configs" in the same line; a
+configuration whose distinct blobs fit twice in L2 is timed step by step with
+a 256 MB write between steps.
 
 --impl reference times the CPU oracle (oracle/, one thread) on the same
 workload and metric, each step one layer for one token.
@@ -51,7 +52,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode80b")
-    ap.add_argument("--extra", default="prefill80b,zipf80b_t64,decode35b,decode80b_int8",
+    ap.add_argument("--extra", default="prefill80b,zipf80b_t64,decode35b,decode80b_int8,gdn80b",
                     help="comma-separated workloads measured after the headline, as sub-records of the same "
                          "line (N = 1 only; empty: none)")
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (profiling of small cases)")
@@ -497,6 +498,64 @@ def roofline_of(wl, m, pk, pk_src):
             if pk_src == "measured" else "fallback 1.9 PFLOP/s"}
 
 
+def measure_gdn(args, gs, dev, pk, pk_src):
+    """The Gated DeltaNet recurrence step of one layer (gdn_step) on the
+    state of gs.B sequences: K launches after W warm-up launches, timed with
+    events on the launching stream; the state (far larger than L2 at the 80B
+    shape) is updated in place by every launch. HBM-bound: the algorithmic
+    bytes are the fp32 state read and written once, plus q, k, v, the gates
+    and the bf16 output."""
+    import torch
+
+    import int4_routed_expert_router_gb300 as smoe
+    import synthetic
+    from workload import bf16_tensor
+
+    q, k, v, g, beta, S0 = synthetic.gdn_inputs(gs.seed, gs.T, gs.B, gs.nk, gs.nv, gs.dk, gs.dv, tag=11)
+    qd, kd, vd = bf16_tensor(q), bf16_tensor(k), bf16_tensor(v)
+    gd, bd = torch.from_numpy(g).to(dev), torch.from_numpy(beta).to(dev)
+    S = torch.from_numpy(S0).to(dev)
+    out = torch.empty((gs.T, gs.B, gs.nv, gs.dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        smoe.gdn_step(gs.nk, gs.nv, qd, kd, vd, gd, bd, S, out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    state_bytes = S.numel() * 4
+    flush = 2 * state_bytes < 2 * L2_BYTES
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
+    sampler = ClockSampler()
+    sampler.start()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in evs:
+        if scratch is not None:
+            scratch.fill_(1)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    ms = float(sum(a.elapsed_time(b) for a, b in evs))
+    alg = 2 * state_bytes + (q.nbytes + k.nbytes + v.nbytes) + g.nbytes + beta.nbytes + out.numel() * 2
+    t = ms / 1e3 / args.steps
+    ach = alg / t / 1e9
+    del S, out, scratch
+    torch.cuda.empty_cache()
+    return {"workload": gs.description, "value": round(gs.B * gs.T * args.steps / (ms / 1e3), 1),
+            "unit": "DeltaNet-layer tokens/s", "us_per_launch": round(t * 1e6, 3),
+            "l2": "flushed between timed steps" if flush else "no flush (state larger than L2)",
+            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(ach / pk["hbm_gbs"], 4), "kernel": "gdn_step_kernel (gdn_step)",
+                         "bytes_per_launch": int(alg), "us_per_launch": round(t * 1e6, 3),
+                         "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk_src == "measured"
+                         else "fallback 6.8 TB/s", "traffic": None},
+            "clocks": sampler.summary()}
+
+
 def traffic_of(wl, m):
     if m["stacked"]:
         t = stack_traffic(wl.name)
@@ -531,6 +590,9 @@ def run_ours(args, wl, world, rank, dist):
     if world == 1 and args.extra:
         import synthetic
         for name in [n for n in args.extra.split(",") if n and n != wl.name]:
+            if name in synthetic.GDN_WORKLOADS:
+                extra[name] = measure_gdn(args, synthetic.GDN_WORKLOADS[name], dev, pk, pk_src)
+                continue
             w2 = synthetic.WORKLOADS[name]
             m2 = measure(args, w2, dev)
             m2["steps"] = args.steps

@@ -412,6 +412,35 @@ SMOE_API int smoe_cache_stats(const smoe_cache *cache, uint64_t *hits, uint64_t 
 SMOE_API int smoe_cache_simulate(int32_t n_layers, int32_t E, int64_t n_slots, const int32_t *requests,
                                  int32_t n_requests, int32_t *out_slots, int64_t *hits, int64_t *misses);
 
+/* Shape of a Gated DeltaNet layer: n_k query/key heads and n_v value heads
+ * (n_v a multiple of n_k; value head h reads query/key head h / (n_v / n_k)),
+ * key width d_k and value width d_v. */
+typedef struct smoe_gdn_shape {
+    int32_t nk, nv, dk, dv;
+} smoe_gdn_shape;
+
+/* T recurrence steps of a Gated DeltaNet layer for B sequences, in order,
+ * on a state held in device memory (the linear-attention layers that make up
+ * three quarters of the hybrid model and keep a fixed-size state instead of a
+ * growing KV cache: xix.ai article, paragraph on the forward pass; agentlenshq
+ * article, section on how expert streaming works). The pages do not spell the
+ * rule out; this is the gated delta rule with L2-normalised q and k. Per
+ * sequence b, value head h, token t, with S = state[b][h] (d_v x d_k):
+ *   k^ = k / sqrt(sum k^2 + 1e-6),  q^ = scale * q / sqrt(sum q^2 + 1e-6),
+ *   S <- exp(g) S + beta (v - exp(g) S k^) k^T,  o = S q^.
+ * All device pointers, 16-byte aligned, row-major:
+ *   q, k  bf16 [T][B][n_k][d_k];   v, out  bf16 [T][B][n_v][d_v];
+ *   g, beta  fp32 [T][B][n_v] (g the log decay, beta the write strength);
+ *   state  fp32 [B][n_v][d_v][d_k], read and updated in place (caller-owned).
+ * scale <= 0 means 1 / sqrt(d_k). Arithmetic is fp32; out is rounded to bf16.
+ * Supported: d_k in {32, 64, 128}, d_v a multiple of 4 up to 1024; others
+ * return SMOE_ENOTSUP. B = 0 or T = 0 does nothing. Asynchronous on stream.
+ * Errors: SMOE_EINVAL (null, misaligned, n_v not a multiple of n_k),
+ * SMOE_ENOTSUP, SMOE_ECUDA. */
+SMOE_API int gdn_step(const smoe_gdn_shape *shape, int32_t B, int32_t T, const uint16_t *q, const uint16_t *k,
+                      const uint16_t *v, const float *g, const float *beta, float scale, float *state,
+                      uint16_t *out, void *stream);
+
 /* Short English text for a status code (static storage). */
 SMOE_API const char *smoe_status_string(int status);
 

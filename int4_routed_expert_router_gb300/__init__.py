@@ -23,7 +23,7 @@ EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destro
            "smoe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_noalloc", "moe_decode_stack",
            "smoe_stack_workspace_bytes", "smoe_check", "smoe_ctx_describe", "smoe_set_profile_events",
            "smoe_status_string", "smoe_cache_create", "smoe_cache_destroy", "smoe_cache_prepare",
-           "smoe_cache_stats", "smoe_cache_simulate", "moe_forward_debug", "smoe_set_stack_wait"]
+           "smoe_cache_stats", "smoe_cache_simulate", "moe_forward_debug", "smoe_set_stack_wait", "gdn_step"]
 
 
 class SmoeError(RuntimeError):
@@ -41,6 +41,10 @@ class Layout(C.Structure):
     _fields_ = [("blob_bytes", C.c_uint64), ("gu_offset", C.c_uint64), ("gu_bytes", C.c_uint64),
                 ("down_offset", C.c_uint64), ("down_bytes", C.c_uint64), ("atom_bytes", C.c_uint32),
                 ("atom_rows", C.c_uint32), ("group", C.c_uint32), ("reserved", C.c_uint32)]
+
+
+class GdnShape(C.Structure):
+    _fields_ = [("nk", C.c_int32), ("nv", C.c_int32), ("dk", C.c_int32), ("dv", C.c_int32)]
 
 
 class ExpertSrc(C.Structure):
@@ -85,6 +89,7 @@ def lib():
         L.smoe_set_profile_events.argtypes = [vp, C.POINTER(vp), i32]
         L.smoe_set_stack_wait.argtypes = [vp, u64, i32]
         L.smoe_status_string.argtypes = [C.c_int]
+        L.gdn_step.argtypes = [C.POINTER(GdnShape), i32, i32, vp, vp, vp, vp, vp, C.c_float, vp, vp, vp]
         L.smoe_status_string.restype = C.c_char_p
         for name in EXPORTS:
             if name not in ("smoe_workspace_bytes", "smoe_status_string"):
@@ -366,6 +371,23 @@ def cache_simulate(n_layers: int, E: int, n_slots: int, requests) -> tuple[np.nd
     _check(lib().smoe_cache_simulate(int(n_layers), int(E), int(n_slots), req.ctypes.data, len(requests),
                                      out.ctypes.data, C.byref(h), C.byref(m)), "smoe_cache_simulate")
     return out, int(h.value), int(m.value)
+
+
+def gdn_step(nk: int, nv: int, q, k, v, g, beta, state, out, scale: float = 0.0, stream=None):
+    """T Gated DeltaNet recurrence steps on `state` in place. q, k bf16
+    [T, B, nk, dk]; v, out bf16 [T, B, nv, dv]; g, beta fp32 [T, B, nv];
+    state fp32 [B, nv, dv, dk]. scale <= 0 means 1 / sqrt(dk)."""
+    import torch
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v: expected [T, B, heads, width]")
+    T, B, _, dk = q.shape
+    dv = v.shape[3]
+    sh = GdnShape(int(nk), int(nv), int(dk), int(dv))
+    _check(lib().gdn_step(C.byref(sh), int(B), int(T), _dev(q, "q", torch.bfloat16, T * B * nk * dk),
+                          _dev(k, "k", torch.bfloat16, T * B * nk * dk), _dev(v, "v", torch.bfloat16, T * B * nv * dv),
+                          _dev(g, "g", torch.float32, T * B * nv), _dev(beta, "beta", torch.float32, T * B * nv),
+                          float(scale), _dev(state, "state", torch.float32, B * nv * dv * dk),
+                          _dev(out, "out", torch.bfloat16, T * B * nv * dv), _stream(stream)), "gdn_step")
 
 
 def check(err, stream=None) -> int:

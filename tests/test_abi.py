@@ -239,3 +239,25 @@ def test_pack_refuses_misaligned_buffers_before_any_work():
     assert call(0x400010, q_off=2) == smoe.EINVAL           # q words not 4-byte aligned
     assert call(0x400010, s_off=1) == smoe.EINVAL           # fp16 scales at an odd address
     assert call(0x400010, q_off=2, where=smoe.HOST) == smoe.EINVAL
+
+
+def test_gdn_step_checks_shapes_before_any_work():
+    """gdn_step refuses bad shapes and null buffers without touching memory or
+    the device (the checks come before any launch), and does nothing for B = 0
+    or T = 0."""
+    L = smoe.lib()
+
+    def call(nk, nv, dk, dv, B=1, T=1, ptr=None):
+        sh = smoe.GdnShape(nk, nv, dk, dv)
+        return L.gdn_step(C.byref(sh), B, T, ptr, ptr, ptr, ptr, ptr, 0.0, ptr, ptr, None)
+
+    assert call(2, 3, 128, 128) == smoe.EINVAL          # n_v not a multiple of n_k
+    assert call(0, 4, 128, 128) == smoe.EINVAL
+    assert call(2, 4, 96, 128) == smoe.ENOTSUP          # d_k outside {32, 64, 128}
+    assert call(2, 4, 128, 130) == smoe.ENOTSUP         # d_v not a multiple of 4
+    assert call(2, 4, 128, 2048) == smoe.ENOTSUP        # d_v above 1024
+    assert call(2, 4, 128, 128, B=-1) == smoe.EINVAL
+    assert call(2, 4, 128, 128) == smoe.EINVAL          # null buffers
+    assert call(2, 4, 128, 128, ptr=0x100008) == smoe.EINVAL   # not 16-byte aligned
+    assert call(2, 4, 128, 128, B=0) == smoe.OK
+    assert call(2, 4, 128, 128, T=0) == smoe.OK
