@@ -498,6 +498,24 @@ def roofline_of(wl, m, pk, pk_src):
             if pk_src == "measured" else "fallback 1.9 PFLOP/s"}
 
 
+GDN_SOURCES = ["int4_routed_expert_router_gb300/csrc/deltanet.cu",
+               "int4_routed_expert_router_gb300/csrc/smoe_dev.cuh",
+               "int4_routed_expert_router_gb300/csrc/smoe_internal.h"]
+
+
+def gdn_traffic(workload: str):
+    """DRAM bytes per launch of the DeltaNet step kernel from the committed
+    ncu summary, only if its sources are unchanged since it was taken."""
+    p = os.path.join(ROOT, "profiles", "gdn_step_kernel_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_sha256") != src_hash(GDN_SOURCES) or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
 def measure_gdn(args, gs, dev, pk, pk_src):
     """The Gated DeltaNet recurrence step of one layer (gdn_step) on the
     state of gs.B sequences: K launches after W warm-up launches, timed with
@@ -552,7 +570,7 @@ def measure_gdn(args, gs, dev, pk, pk_src):
                          "frac": round(ach / pk["hbm_gbs"], 4), "kernel": "gdn_step_kernel (gdn_step)",
                          "bytes_per_launch": int(alg), "us_per_launch": round(t * 1e6, 3),
                          "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if pk_src == "measured"
-                         else "fallback 6.8 TB/s", "traffic": None},
+                         else "fallback 6.8 TB/s", "traffic": gdn_traffic(gs.name)},
             "clocks": sampler.summary()}
 
 
