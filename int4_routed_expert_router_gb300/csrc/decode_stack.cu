@@ -17,15 +17,17 @@
 //      polled from the exchange buffer).
 //   B. Router rows c, c + G, ... (row E is the shared-gate vector; loaded
 //      during the previous layer) dotted with x_l; the logits go out.
-//   C. CTAs c < I/8 compute the shared expert's gate/up unit c (intermediates
-//      8c .. 8c + 7; its weights were loaded during the previous layer) while
-//      the logits of the other CTAs arrive.
 //   D. One warp polls all E + 1 logits and picks the top k in registers
 //      (route_common.cuh's arithmetic, so ids, weights and gate equal
 //      moe_route's bit for bit); CTA 0 writes them out.
 //   E. The CTA requests its routed gate/up units (expert j in route order,
 //      row block rb: 32 contiguous atoms, one bulk copy each) and, for
 //      c < H/16, its down rows 16c .. 16c + 15 of every routed expert.
+//   C. CTAs c < I/8 compute the shared expert's gate/up unit c (intermediates
+//      8c .. 8c + 7; its weights were loaded during the previous layer) while
+//      the routed units' first bytes are on their way: done before the
+//      top-k, it delayed these CTAs' requests, and the slowest CTA's h gates
+//      every output CTA.
 //   F. Gate/up units as their bytes land -> h as bf16 high and low parts.
 //   G. CTAs c < H/16: poll all experts' h, down rows of every expert, combine
 //      in route order with the routing weights, + gate * shared expert +
@@ -56,7 +58,7 @@ constexpr uint16_t kSentinel16 = 0xFFFFu;
 constexpr int kStkMaxE = 512;           // experts per layer the one-launch step takes (larger E: per-layer calls)
 
 struct StkSmem {
-    int x_s, xsum, rows, table, sunit, units, wdn, red, hh, yd, ysum, mx, cand, sel, ints, bars, total;
+    int x_s, xsum, rows, table, sunit, units, wdn, red, hh, gsum, yd, ysum, mx, cand, sel, ints, bars, total;
 };
 
 __host__ __device__ inline StkSmem stk_smem(int H, int E, int I, int U, int nr, int nu)
@@ -73,6 +75,7 @@ __host__ __device__ inline StkSmem stk_smem(int H, int E, int I, int U, int nr, 
     L.wdn = o;   o = align128(o + U * ngI * kAtomBytes);
     L.red = o;   o = align128(o + (nu + 1) * kStkWarps * 8 * 8);
     L.hh = o;    o = align128(o + U * 2 * I * 2);
+    L.gsum = o;  o = align128(o + U * ngI * 4);
     L.yd = o;    o = align128(o + U * ngI * 16 * 4);
     L.ysum = o;  o = align128(o + U * 16 * 4);
     L.mx = o;    o = align128(o + 2 * kStkWarps * 4);
@@ -88,13 +91,6 @@ __device__ __forceinline__ void bulk_nohint(void *dst, const void *src, uint32_t
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
 }
 
 __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
@@ -204,20 +200,41 @@ __device__ void grid_wait(const uint32_t *ctr, uint32_t target, uint32_t *abortw
     __syncthreads();
 }
 
-// The gate/up partial sums of one atom (16 rows x one 64-column group kb) for
-// the token (MMA column 0): lanes 4g (t4 = 0) get gate row g and up row g.
-__device__ __forceinline__ float2 gateup_atom(const uint8_t *atom, const uint16_t *x_s, float xs_kb, int kb, int lane)
+// The token's B fragment of one 64-column group kb of x (the token is MMA
+// column 0: lanes 0..3 hold columns 16 t4 .. 16 t4 + 15, the others zeros) and
+// the group's sum of x. A warp always works on the same one or two groups, so
+// it loads them once per layer.
+struct XFrag {
+    uint4 xa, xb;
+    float xs;
+};
+
+__device__ __forceinline__ XFrag load_xfrag(const uint16_t *x_s, const float *xsum, int kb, int ngH, int lane)
 {
-    const int g = lane >> 2, t4 = lane & 3;
+    XFrag f;
+    f.xa = make_uint4(0, 0, 0, 0);
+    f.xb = f.xa;
+    f.xs = 0.f;
+    if (kb < ngH) {
+        if (lane < 4) {
+            const int col = kb * kGroup + 16 * lane;
+            f.xa = *reinterpret_cast<const uint4 *>(x_s + col);
+            f.xb = *reinterpret_cast<const uint4 *>(x_s + col + 8);
+        }
+        f.xs = xsum[kb];
+    }
+    return f;
+}
+
+// The gate/up partial sums of one atom (16 rows x one 64-column group) for
+// the token (MMA column 0): lanes 4g (t4 = 0) get gate row g and up row g.
+__device__ __forceinline__ float2 gateup_atom(const uint8_t *atom, const XFrag &f, int lane)
+{
+    const int g = lane >> 2;
     const uint4 A = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
     const uint2 SB = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
-    const int col = kb * kGroup + 16 * t4;
-    uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
-    if (g == 0) {                                   // the token is MMA column 0
-        xa = *reinterpret_cast<const uint4 *>(x_s + col);
-        xb = *reinterpret_cast<const uint4 *>(x_s + col + 8);
-    }
-    const uint32_t xl[4] = {xa.x, xa.y, xa.z, xa.w}, xr[4] = {xb.x, xb.y, xb.z, xb.w};
+    const float xs_kb = f.xs;
+    const uint32_t xl[4] = {f.xa.x, f.xa.y, f.xa.z, f.xa.w}, xr[4] = {f.xb.x, f.xb.y, f.xb.z, f.xb.w};
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int m = 0; m < 4; m += 2) {
@@ -233,18 +250,19 @@ __device__ __forceinline__ float2 gateup_atom(const uint8_t *atom, const uint16_
     return make_float2(fmaf(sg, acc[0] + acc2[0], bpg * xs_kb), fmaf(su, acc[2] + acc2[2], bpu * xs_kb));
 }
 
-// One warp's partial sums of a gate/up unit (H/64 atoms, one 64-column group
-// of x each) when nw warps share it: warp w takes atoms w, w + nw, ..., two at
-// a time so that their tensor-core chains overlap, and adds them in that order.
-__device__ __forceinline__ float2 gateup_partial(const uint8_t *ubase, const uint16_t *x_s, const float *xsum, int ngH,
-                                                 int warp, int nw, int lane)
+// One warp's partial sums of a gate/up unit (H/64 <= 32 atoms, one 64-column
+// group of x each) when the 16 warps share it: warp w takes atoms w and
+// w + 16 (f0, f1: their x fragments), whose tensor-core chains overlap, and
+// adds them in that order.
+__device__ __forceinline__ float2 gateup_partial(const uint8_t *ubase, const XFrag &f0, const XFrag &f1, int ngH,
+                                                 int warp, int lane)
 {
     float aG = 0.f, aU = 0.f;
-    for (int kb = warp; kb < ngH; kb += 2 * nw) {
-        const int kb1 = kb + nw;
-        const float2 a = gateup_atom(ubase + kb * kAtomBytes, x_s, xsum[kb], kb, lane);
+    if (warp < ngH) {
+        const int kb1 = warp + kStkWarps;
+        const float2 a = gateup_atom(ubase + warp * kAtomBytes, f0, lane);
         float2 b = make_float2(0.f, 0.f);
-        if (kb1 < ngH) b = gateup_atom(ubase + kb1 * kAtomBytes, x_s, xsum[kb1], kb1, lane);
+        if (kb1 < ngH) b = gateup_atom(ubase + kb1 * kAtomBytes, f1, lane);
         aG += a.x;
         aU += a.y;
         aG += b.x;
@@ -256,9 +274,12 @@ __device__ __forceinline__ float2 gateup_partial(const uint8_t *ubase, const uin
 // Warp `warp` (whole warp) finishes a gate/up unit from the nw warps'
 // partials red[w * 8 + g] (summed in warp order): h of intermediates
 // 8 rb .. 8 rb + 7 as bf16 high parts and low parts (h - high), stored as one
-// 16-byte store each into the exchange rows hx_hi, hx_lo; then one release
-// add on the expert's arrival counter, so a reader that has acquired the
-// counter at I/8 sees every unit's h.
+// 16-byte store each into the exchange rows hx_hi, hx_lo (a value with the
+// sentinel pattern as the canonical NaN); then one relaxed add on the
+// expert's arrival counter. The add may become visible before the stores (a
+// release would hold the warp until they are acknowledged, about a microsecond
+// on the layer's critical path), so a reader that sees the counter at I/8
+// checks the copied h for sentinels and copies again if one is left.
 __device__ __forceinline__ void finish_unit(const float2 *red, int nw, bool valid, uint16_t *hx_hi, uint16_t *hx_lo,
                                             uint32_t *cnt, int lane)
 {
@@ -270,8 +291,8 @@ __device__ __forceinline__ void finish_unit(const float2 *red, int nw, bool vali
         aU += v.y;
     }
     const float hv = valid ? silu(aG) * aU : 0.f;
-    const uint16_t hi = f32_to_bf16_bits(hv);
-    const uint16_t lo = f32_to_bf16_bits(hv - __uint_as_float(uint32_t(hi) << 16));
+    const uint16_t hi = canon16(f32_to_bf16_bits(hv));
+    const uint16_t lo = canon16(f32_to_bf16_bits(hv - __uint_as_float(uint32_t(hi) << 16)));
     uint32_t phi[4], plo[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {                       // lanes 4g hold intermediate g
@@ -285,7 +306,7 @@ __device__ __forceinline__ void finish_unit(const float2 *red, int nw, bool vali
     if (lane == 0) {
         *reinterpret_cast<uint4 *>(hx_hi) = make_uint4(phi[0], phi[1], phi[2], phi[3]);
         *reinterpret_cast<uint4 *>(hx_lo) = make_uint4(plo[0], plo[1], plo[2], plo[3]);
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
+        asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
     }
 }
 
@@ -318,20 +339,37 @@ __device__ __forceinline__ float2 down_atom(const uint8_t *atom, uint4 h0, uint4
                        fmaf(s1, (acc[2] + acc2[2]) + (acc[3] + acc2[3]), bp1 * gsum));
 }
 
-// Sum of the high + low parts of one 64-group held as down_atom's B columns
-// (lanes 0..3 the high parts, lanes 4..7 the low parts, 16 values each):
-// each lane sums its 16 in column order, then the eight lanes in a fixed
-// tree; every lane gets the sum.
-__device__ __forceinline__ float group_sum(uint4 h0, uint4 h1)
+// Every (expert u, group kb) sum of h's high + low parts, gsum[u * ngI + kb]
+// (the bias term of down_atom), in a fixed order: eight threads per group,
+// thread q of them holding the high (q < 4) or low parts of columns
+// 16 (q % 4) .. + 15, each sums its 16 values in column order, then the eight
+// partial sums combine in a fixed tree (pairs, then quads, then the halves).
+// The whole CTA calls it; each group is summed once per layer. It reads every
+// half-word of h once, so it also returns whether this thread met the
+// sentinel (a value not yet written when h was copied).
+__device__ __forceinline__ bool group_sums(const uint16_t *hh, int U, int I, int ngI, float *gsum)
 {
-    const uint32_t v[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-    float s = 0.f;
+    const int tid = threadIdx.x, q = tid & 7, part = q >> 2, t4 = q & 3;
+    bool miss = false;
+    for (int gi = tid >> 3; gi < ((U * ngI + 3) & ~3); gi += kStkThreads / 8) {   // whole warps per round
+        float s = 0.f;
+        if (gi < U * ngI) {
+            const int u = gi / ngI, kb = gi - u * ngI;
+            const uint16_t *src = hh + (size_t(part) * U + u) * I + kb * kGroup + 16 * t4;
+            const uint4 h0 = *reinterpret_cast<const uint4 *>(src), h1 = *reinterpret_cast<const uint4 *>(src + 8);
+            const uint32_t v[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s += bf16lo(v[j]) + bf16hi(v[j]);
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    s += __shfl_xor_sync(0xffffffffu, s, 4);
-    return __shfl_sync(0xffffffffu, s, 0);
+            for (int j = 0; j < 8; ++j) {
+                s += bf16lo(v[j]) + bf16hi(v[j]);
+                miss |= !ready16(v[j]);
+            }
+        }
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        s += __shfl_xor_sync(0xffffffffu, s, 4);
+        if (q == 0 && gi < U * ngI) gsum[gi] = s;
+    }
+    return miss;
 }
 
 // Composite order of the routing keys: larger key first, equal keys by lower id.
@@ -419,6 +457,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
     uint8_t *wdn = smem + L.wdn;
     float2 *red = reinterpret_cast<float2 *>(smem + L.red);          // [nu + 1][warps][8]
     uint16_t *hh = reinterpret_cast<uint16_t *>(smem + L.hh);        // [hi, lo][U][I]: h of the layer
+    float *gsum_s = reinterpret_cast<float *>(smem + L.gsum);        // [U * ngI] group sums of h
     float *yd = reinterpret_cast<float *>(smem + L.yd);              // [U * ngI atoms][16 rows]
     float *ysum = reinterpret_cast<float *>(smem + L.ysum);          // [U][16 rows]
     uint32_t *mx_k = reinterpret_cast<uint32_t *>(smem + L.mx);      // [16] slice maxima
@@ -431,6 +470,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
     float *w_s = reinterpret_cast<float *>(ints);                    // [16]
     float *gate_s = reinterpret_cast<float *>(ints + 16);
     int *ncand = ints + 17;
+    uint32_t *vmask_s = reinterpret_cast<uint32_t *>(ints + 18);     // bit u: expert u's blob is in the pool
+    int *giveup_s = ints + 19;                                        // the h copy's retries ran out
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *ubar = bars, *dbar = bars + p.nu, *xbar = dbar + U, *rbar = xbar + 1, *sbar = rbar + 1,
              *hbar = sbar + 1;                                       // the layer's h has landed
@@ -443,7 +484,10 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
     const bool has_shared = c < nrb;                                 // the shared expert's unit rb = c
     const bool has_down = c < nD;                                    // output rows 16 c .. 16 c + 15
     const int R = k * nrb;                                           // routed units per layer
-    const int ord = c >= nD ? c - nD : c + (G - nD);                 // CTAs without down rows come first
+    // routed unit order: the CTAs without down rows first, then the others from
+    // the highest index down, so the CTAs that also take a shared unit (c < I/8)
+    // are the last to get a fifth routed unit
+    const int ord = c >= nD ? c - nD : (nD - 1 - c) + (G - nD);
     const int n_mine = ord < R ? (R - 1 - ord) / G + 1 : 0;          // routed units r = ord + i G
 
     auto issue_fixed = [&](int l) {                                  // thread 0: what layer l needs that is known early
@@ -467,6 +511,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
         for (int i = 0; i < p.nu + U + 4; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         *ncand = 0;
+        *giveup_s = 0;
     }
     __syncthreads();
     if (tid == 0) {
@@ -489,6 +534,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
     }
     const uint64_t pol = policy_evict_first();
     bool bad = false;                                 // a bounded wait for this CTA's own copies gave up
+    uint32_t hpar = 0;                                // phase parity of the next wait on hbar
 
     for (int l = 0; l < p.n_layers; ++l) {
         const uint32_t par = uint32_t(l & 1);
@@ -539,20 +585,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue_fixed(l + 1);
         }
-
-        // ---- C. the shared expert's unit c, while the other CTAs' logits arrive
-        if (has_shared) {
-            if (!bad && !mbar_wait(sbar, par, p.err)) bad = true;
-            const float2 a = gateup_partial(sunit, x_s, xsum, ngH, warp, kStkWarps, lane);
-            if ((lane & 3) == 0) red[(p.nu * kStkWarps + warp) * 8 + (lane >> 2)] = a;
-            __syncthreads();
-            if (warp == 0)
-                finish_unit(red + p.nu * kStkWarps * 8, kStkWarps, true, hx_hi + 8 * c, hx_lo + 8 * c, hcnt, lane);
-            if (tid == 32 && l + 1 < p.n_layers) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue_shared_unit(l + 1);
-            }
-        }
+        const XFrag f0 = load_xfrag(x_s, xsum, warp, ngH, lane), f1 = load_xfrag(x_s, xsum, warp + kStkWarps, ngH, lane);
 
         // ---- D. every thread polls its logit (thread 0 also the shared-gate
         // logit, word E, and under the stall hook word E + 1, which nothing
@@ -616,13 +649,28 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
             }
         }
 
+        // ---- C. the shared expert's unit c (its weights are in shared memory), while
+        // the routed units' first bytes are on their way
+        if (has_shared) {
+            if (!bad && !mbar_wait(sbar, par, p.err)) bad = true;
+            const float2 a = gateup_partial(sunit, f0, f1, ngH, warp, lane);
+            if ((lane & 3) == 0) red[(p.nu * kStkWarps + warp) * 8 + (lane >> 2)] = a;
+            __syncthreads();
+            if (warp == kStkWarps - 1)
+                finish_unit(red + p.nu * kStkWarps * 8, kStkWarps, true, hx_hi + 8 * c, hx_lo + 8 * c, hcnt, lane);
+            if (tid == 32 && l + 1 < p.n_layers) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_shared_unit(l + 1);
+            }
+        }
+
         // ---- F. routed gate/up units as they land; then warp i finishes unit i
         for (int i = 0; i < n_mine; ++i) {
             const int r = ord + i * G;
             const bool valid = blob_of(1 + r / nrb) != nullptr;     // uniform
             if (!bad && !mbar_wait(&ubar[i], par, p.err)) bad = true;
             float2 a = make_float2(0.f, 0.f);
-            if (valid && !bad) a = gateup_partial(units + size_t(i) * ubytes, x_s, xsum, ngH, warp, kStkWarps, lane);
+            if (valid && !bad) a = gateup_partial(units + size_t(i) * ubytes, f0, f1, ngH, warp, lane);
             if ((lane & 3) == 0) red[(i * kStkWarps + warp) * 8 + (lane >> 2)] = a;
         }
         __syncthreads();
@@ -635,28 +683,61 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
 
         // ---- G. down rows 16 c .. 16 c + 15 of every expert, combine -> x_{l+1}.
         // Warp 0 polls the U experts' arrival counters (one per 128-byte line)
-        // until every unit's h is in, then bulk-copies the layer's h into shared
-        // memory; warp w takes atoms a = w, w + 16, ... (expert u = a / (I/64),
-        // group kb = a % (I/64)), two at a time.
+        // until every unit has reported, then bulk-copies the layer's h into
+        // shared memory (whole lines, so each L2 line is requested once per CTA,
+        // not once per 16 bytes). The group sums read every half-word of it; if
+        // one still holds the sentinel (its store was overtaken by the relaxed
+        // counter add), h is copied again. Then warp w takes atoms
+        // a = w, w + 16, ... (expert u = a / (I/64), group kb = a % (I/64)),
+        // two at a time.
         if (has_down) {
+            const uint32_t hb = uint32_t(U * I * 2);
+            auto copy_h = [&] {                                     // one thread
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                mbar_arrive_expect_tx(hbar, 2 * hb);
+                bulk_nohint(hh, hx_hi, hb, hbar);
+                bulk_nohint(hh + size_t(U) * I, hx_lo, hb, hbar);
+            };
             if (warp == 0) {
                 uint32_t pend = lane < U ? 1u : 0u;
                 poll([&] {
-                    if (pend && ld_acquire(hcnt + size_t(lane) * kStackCntStride) >= uint32_t(nrb)) pend = 0;
+                    if (pend && ld_relaxed(hcnt + size_t(lane) * kStackCntStride) >= uint32_t(nrb)) pend = 0;
                     return pend == 0;
                 }, 0xffffffffu, abortw, p.err, lim);
-                // h ([hi, lo][U][I]) by two bulk copies: whole lines, so each L2 line
-                // is requested once per CTA, not once per 16 bytes; the proxy fence
-                // makes what the acquire saw visible to the copies
+                const uint32_t vm = __ballot_sync(0xffffffffu, lane < U && blob_of(lane) != nullptr);
                 if (lane == 0) {
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    const uint32_t hb = uint32_t(U * I * 2);
-                    mbar_arrive_expect_tx(hbar, 2 * hb);
-                    bulk_nohint(hh, hx_hi, hb, hbar);
-                    bulk_nohint(hh + size_t(U) * I, hx_lo, hb, hbar);
+                    *vmask_s = vm;                                   // read after the barrier below
+                    copy_h();
                 }
             }
-            if (!bad && !mbar_wait(hbar, par, p.err)) bad = true;
+            uint64_t t_retry = 0;
+            for (;;) {
+                if (!bad && !mbar_wait(hbar, hpar, p.err)) bad = true;
+                hpar ^= 1u;
+                const bool miss = group_sums(hh, U, I, ngI, gsum_s) && !bad;
+                if (!__syncthreads_or(miss)) break;
+                // rare: copy again (bounded like every wait; the generic reads of
+                // the old copy are ordered before it by the barrier above)
+                if (tid == 0) {
+                    const uint64_t now = globaltimer_ns();
+                    if (t_retry == 0) t_retry = now;
+                    if (now - t_retry > lim || ld_relaxed(abortw) != 0u) {
+                        atomicExch(abortw, 1u);
+                        set_error(p.err, SMOE_DEV_TIMEOUT);
+                        *giveup_s = 1;
+                    } else {
+                        __nanosleep(100);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        copy_h();
+                    }
+                }
+                __syncthreads();
+                if (*giveup_s) {
+                    bad = true;
+                    break;
+                }
+            }
+            const uint32_t vmask = *vmask_s;
             const int na = U * ngI, nj = (na - warp + kStkWarps - 1) / kStkWarps;   // this warp's atoms
             for (int j = 0; j < nj; j += 2) {
                 const bool two = j + 1 < nj;
@@ -677,12 +758,12 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                                                                     (a % ngI) * kGroup + 16 * t4 + 8 * (q & 1));
                         }
                 }
-                const float gs0 = group_sum(h[0], h[1]);
-                const float gs1 = group_sum(h[2], h[3]);
+                const float gs0 = gsum_s[a0];
+                const float gs1 = two ? gsum_s[a1] : 0.f;
                 float2 y0 = make_float2(0.f, 0.f), y1 = y0;
-                if (blob_of(u0) != nullptr && !bad)
+                if ((vmask >> u0 & 1u) && !bad)
                     y0 = down_atom(wdn + size_t(u0) * wbytes + (a0 % ngI) * kAtomBytes, h[0], h[1], gs0, lane);
-                if (two && blob_of(u1) != nullptr && !bad)
+                if (two && (vmask >> u1 & 1u) && !bad)
                     y1 = down_atom(wdn + size_t(u1) * wbytes + (a1 % ngI) * kAtomBytes, h[2], h[3], gs1, lane);
                 if ((lane & 3) == 0) {
                     yd[a0 * 16 + (lane >> 2)] = y0.x;

@@ -611,7 +611,7 @@ extern "C" int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_
     p.hx = reinterpret_cast<uint16_t *>(ws + W.hx);
     p.xe = reinterpret_cast<uint16_t *>(ws + W.xe);
     p.xbuf = ws + W.zl;
-    p.xbuf_words16 = (W.xend - W.zl) / 16;
+    p.xbuf_words16 = (W.total - W.zl) / 16;       // logits, layer outputs and h
     p.sync = reinterpret_cast<uint32_t *>(ws + W.sync);
     p.hcnt = reinterpret_cast<uint32_t *>(ws + W.hcnt);
     p.sync_bytes = W.zl;                           // the counters and arrival words, zeroed per launch
