@@ -60,8 +60,9 @@ static_assert(kPfSmem <= 232448, "shared memory per CTA");
 constexpr int kXMaxN = 192;        // tokens per expert tile
 constexpr int kXRaw = 16;          // raw atom slots
 constexpr int kXStg = 4;           // operand stages: A in TMEM + B in shared memory, one barrier pair each
+constexpr int kXAcc = 2;           // accumulator buffers in TMEM (the epilogue of a tile overlaps the next)
 constexpr int kXBBytes = kXMaxN * kPfK * 2;                 // 24 KiB
-constexpr uint32_t kXACol0 = 2 * kXMaxN;                    // first A column (384)
+constexpr uint32_t kXACol0 = kXAcc * kXMaxN;                // first A column
 constexpr int kXSmem = kXStg * kXBBytes + kXRaw * kPfRawBytes + 1024 /*align*/ + 512 /*barriers*/;
 static_assert(kXSmem <= 232448, "shared memory per CTA");
 static_assert(kXACol0 + kXStg * 32 <= 512, "TMEM columns");
@@ -187,6 +188,11 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // ---------------------------------------------------------------- bucketing
+constexpr int kBucketSmallT = 256;   // up to this T: one CTA buckets (at most 32 chunks of 8 tokens)
+
+// Dynamic shared memory of bucket_small_kernel's bucketing CTA for E experts.
+__host__ __device__ inline int bucket_small_smem(int E) { return (32 * E + 2 * 1024 + kBucketSmallT * 16) * 4; }
+
 // counts and chunk_base are [E][chunks] (chunks of bucket_tok(T) tokens): the
 // scan's warps (one per expert) read and write an expert's row coalesced.
 
@@ -206,6 +212,48 @@ __global__ void __launch_bounds__(256) bucket_count_kernel(const PrefillParams p
     }
     __syncthreads();
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) p.counts[size_t(e) * nch + c] = cnt[e];
+}
+
+// Thread e of a 1024-thread CTA (e < E: its expert, with `total` pairs from
+// pair row `start` and nt tiles from tile tstart; ntr: all routed tiles):
+// the expert's tiles, runs of at most kXMaxN pairs of near-equal size, its
+// slot resolved; then the shared expert's runs over T and the tile count.
+__device__ void write_tiles(const PrefillParams &p, int e, int total, int nt, int start, int tstart, int ntr)
+{
+    if (e < p.E) {
+        const int64_t slot = p.table_row[e];
+        for (int i = 0; i < nt; ++i) {
+            PfTile tl;
+            tl.kind = 0;
+            tl.slot = (slot < 0 || slot >= p.n_slots) ? -1 : int(slot);
+            tl.p0 = start + int((int64_t(i) * total) / nt);               // runs of near-equal size
+            tl.n = int((int64_t(i + 1) * total) / nt) - int((int64_t(i) * total) / nt);
+            p.tiles[tstart + i] = tl;
+        }
+    }
+    const int nts = (p.T + kXMaxN - 1) / kXMaxN;
+    for (int i = e; i < nts; i += blockDim.x) {       // the shared expert: runs of near-equal size over T
+        PfTile tl;
+        tl.kind = 1;
+        tl.slot = 0;
+        tl.p0 = int((int64_t(i) * p.T) / nts);
+        tl.n = int((int64_t(i + 1) * p.T) / nts) - tl.p0;
+        p.tiles[ntr + i] = tl;
+    }
+    if (e == 0) *p.ntiles = ntr + nts;
+}
+
+// Inclusive scans over the 1024 threads of a CTA of a[] and b[] (in place).
+__device__ void block_scan2(int *a, int *b)
+{
+    const int e = threadIdx.x;
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int x = e >= off ? a[e - off] : 0, y = e >= off ? b[e - off] : 0;
+        __syncthreads();
+        a[e] += x;
+        b[e] += y;
+        __syncthreads();
+    }
 }
 
 // One warp per expert: chunk_base[e][c] = pairs of expert e in chunks before
@@ -254,40 +302,12 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(const PrefillParams p
     buf[e] = total;
     tbuf[e] = nt;
     __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {       // inclusive scans of totals and tile counts
-        const int a = e >= off ? buf[e - off] : 0, b = e >= off ? tbuf[e - off] : 0;
-        __syncthreads();
-        buf[e] += a;
-        tbuf[e] += b;
-        __syncthreads();
-    }
+    block_scan2(buf, tbuf);                           // inclusive scans of totals and tile counts
     const int start = buf[e] - total;                 // exclusive
-    const int tstart = tbuf[e] - nt;
-    if (e < p.E) {
-        p.offsets[e] = start;                         // the scatter adds it to the chunk prefixes
-        const int64_t slot = p.table_row[e];
-        for (int i = 0; i < nt; ++i) {
-            PfTile tl;
-            tl.kind = 0;
-            tl.slot = (slot < 0 || slot >= p.n_slots) ? -1 : int(slot);
-            tl.p0 = start + int((int64_t(i) * total) / nt);               // runs of near-equal size
-            tl.n = int((int64_t(i + 1) * total) / nt) - int((int64_t(i) * total) / nt);
-            p.tiles[tstart + i] = tl;
-        }
-    }
-    const int ntr = tbuf[1023];
-    const int nts = (p.T + kXMaxN - 1) / kXMaxN;
-    for (int i = e; i < nts; i += blockDim.x) {       // the shared expert: runs of near-equal size over T
-        PfTile tl;
-        tl.kind = 1;
-        tl.slot = 0;
-        tl.p0 = int((int64_t(i) * p.T) / nts);
-        tl.n = int((int64_t(i + 1) * p.T) / nts) - tl.p0;
-        p.tiles[ntr + i] = tl;
-    }
+    if (e < p.E) p.offsets[e] = start;                // the scatter adds it to the chunk prefixes
+    write_tiles(p, e, total, nt, start, tbuf[e] - nt, tbuf[1023]);
     if (e == 0) {
         p.offsets[p.E] = buf[1023];
-        *p.ntiles = ntr + nts;
         atomicExch(p.ticket, 0u);                     // ready for the next call
     }
 }
@@ -331,12 +351,8 @@ __global__ void __launch_bounds__(32) bucket_scatter_kernel(const PrefillParams 
 // GEMMs' K order (perm64 inside each 64-column group); the gate/up GEMM gathers
 // its B rows from xt by token. fp16 is exact for |x| < 65504 (subnormal below
 // 2^-14, an absolute error under 3e-8); larger values set the error word.
-__global__ void __launch_bounds__(256) convert_x_kernel(const GemmParams g)
+__device__ void convert_x_token(const GemmParams &g, int tok, int lane)
 {
-    pdl_wait();                                   // the predecessor's writes are visible
-    pdl_trigger();
-    const int tok = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (tok >= g.T) return;
     const uint4 *src = reinterpret_cast<const uint4 *>(g.x_bf16 + size_t(tok) * g.H);
     uint2 *dst2 = reinterpret_cast<uint2 *>(const_cast<uint16_t *>(g.x) + size_t(tok) * g.H);
     bool bad = false;
@@ -356,6 +372,88 @@ __global__ void __launch_bounds__(256) convert_x_kernel(const GemmParams g)
         dst2[(base + perm64((c0 & 63) + 4)) / 4] = make_uint2(o[2], o[3]);
     }
     if (bad) set_error(g.err, SMOE_DEV_RANGE);
+}
+
+__global__ void __launch_bounds__(256) convert_x_kernel(const GemmParams g)
+{
+    pdl_wait();                                   // the predecessor's writes are visible
+    pdl_trigger();
+    const int tok = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (tok < g.T) convert_x_token(g, tok, lane);
+}
+
+// -------------------------------------------- bucketing of a small batch
+// T <= kBucketSmallT (chunks of bucket_tok(T) = 8 tokens, at most 32): CTA 0
+// runs the three bucketing steps above in shared memory, warp c taking chunk
+// c, with the same results (pairs by expert, then by token; the same tile
+// list); the other CTAs convert x, one warp per token. A small batch then
+// costs one launch instead of four, each of which was mostly launch and
+// serial latency at T = 64.
+__global__ void __launch_bounds__(1024) bucket_small_kernel(const PrefillParams p, const GemmParams g)
+{
+    pdl_wait();                                   // the predecessor's writes are visible
+    pdl_trigger();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (blockIdx.x > 0) {
+        const int tok = (int(blockIdx.x) - 1) * 32 + warp;
+        if (tok < g.T) convert_x_token(g, tok, lane);
+        return;
+    }
+    extern __shared__ int sm[];
+    const int E = p.E, k = p.k, ct = bucket_tok(p.T), nch = (p.T + ct - 1) / ct;
+    int *cnt = sm;                                // [32 chunks][E]: counts, then the chunk's next slot per expert
+    int *buf = sm + 32 * E, *tbuf = buf + 1024;
+    int *ids_s = tbuf + 1024;                     // [T * k] (k <= 16): the batch's expert ids
+    for (int i = tid; i < 32 * E; i += 1024) cnt[i] = 0;
+    for (int q = tid; q < p.T * k; q += 1024) ids_s[q] = p.ids[q];
+    __syncthreads();
+    if (warp < nch) {
+        const int t0 = warp * ct, t1 = min(p.T, t0 + ct);
+        for (int q = t0 * k + lane; q < t1 * k; q += 32) {
+            const int e = ids_s[q];
+            if (e >= 0 && e < E) atomicAdd(&cnt[warp * E + e], 1);
+            else set_error(p.err, SMOE_DEV_BAD_EXPERT);
+        }
+    }
+    __syncthreads();
+    const int e = tid;
+    int total = 0;
+    if (e < E)
+        for (int c = 0; c < nch; ++c) {            // chunk prefixes of expert e
+            const int v = cnt[c * E + e];
+            cnt[c * E + e] = total;
+            total += v;
+        }
+    const int nt = (total + kXMaxN - 1) / kXMaxN;
+    buf[e] = total;
+    tbuf[e] = nt;
+    __syncthreads();
+    block_scan2(buf, tbuf);
+    const int start = buf[e] - total;
+    write_tiles(p, e, total, nt, start, tbuf[e] - nt, tbuf[1023]);
+    if (e < E)
+        for (int c = 0; c < nch; ++c) cnt[c * E + e] += start;
+    __syncthreads();
+    if (warp < nch) {                             // warp c: chunk c's pairs in token order
+        int *base = cnt + warp * E;
+        const int t0 = warp * ct, t1 = min(p.T, t0 + ct);
+        for (int t = t0; t < t1; ++t) {
+            const int q = t * k + lane;
+            const bool act = lane < k;
+            const int ex = act ? ids_s[q] : -1;
+            const bool ok = act && ex >= 0 && ex < E;
+            // lanes naming the same expert take consecutive slots in lane order
+            const uint32_t same = __match_any_sync(0xffffffffu, ok ? ex : -1 - lane);
+            const int rank = __popc(same & ((1u << lane) - 1u));
+            int pos = -1;
+            if (ok) pos = base[ex] + rank;
+            __syncwarp();
+            if (ok && rank == __popc(same) - 1) base[ex] = pos + 1;
+            if (ok) p.pair_token[pos] = t;
+            if (act) p.pair_pos[q] = pos;
+            __syncwarp();
+        }
+    }
 }
 
 // ---------------------------------------------------------- grouped GEMM
@@ -641,11 +739,11 @@ __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uin
     uint32_t ymax = 0;                                            // largest |fp16| bits stored, per half
     TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
     for (int i = 0; i < my_tiles; ++i) {
-        const int b = i & 1;
+        const int b = i % kXAcc;
         const TileInfo ti = tnext;
         const int mt = tile_of(i) % p.m_tiles;
         if (i + 1 < my_tiles) tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
-        pf_wait(&accfull[b], (i / 2) & 1, p.err, abort);
+        pf_wait(&accfull[b], (i / kXAcc) & 1, p.err, abort);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (!ti.valid) set_error(p.err, SMOE_DEV_BAD_SLOT);       // and the tile's outputs are zeros
         if (p.mode == 0) {
@@ -732,8 +830,8 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     uint64_t *bars = reinterpret_cast<uint64_t *>(raw + kXRaw * kPfRawBytes);
     uint64_t *rawfull = bars, *rawempty = bars + kXRaw;
     uint64_t *full = bars + 2 * kXRaw, *empty = full + kXStg;     // stage s: A (TMEM) + B (smem)
-    uint64_t *accfull = empty + kXStg, *accempty = accfull + 2;
-    uint64_t *bfull = accempty + 2;                               // down: B copies of stage s (TMA)
+    uint64_t *accfull = empty + kXStg, *accempty = accfull + kXAcc;
+    uint64_t *bfull = accempty + kXAcc;                           // down: B copies of stage s (TMA)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bfull + kXStg);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -757,7 +855,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             mbar_init(&empty[s], 1);
             mbar_init(&bfull[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kXAcc; ++b) {
             mbar_init(&accfull[b], 1);
             mbar_init(&accempty[b], (p.mode == 1 ? kPfEpi + kXGatherWarps : kPfEpi) * 32);   // epilogue threads
         }
@@ -900,10 +998,10 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             uint32_t ph = 0;
             int nextN = tile_info(p, tile_of(0) / p.m_tiles).N;
             for (int i = 0; i < my_tiles; ++i) {
-                const int b = i & 1;
+                const int b = i % kXAcc;
                 const uint32_t idesc = umma_idesc(nextN, false);
                 if (i + 1 < my_tiles) nextN = tile_info(p, tile_of(i + 1) / p.m_tiles).N;   // used one tile later
-                pf_wait(&accempty[b], ((i >> 1) & 1) ^ 1u, p.err, abort);
+                pf_wait(&accempty[b], ((i / kXAcc) & 1) ^ 1u, p.err, abort);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t acc_t = tmem + uint32_t(b * kXMaxN);
                 for (int kb = 0; kb < nk; ++kb) {
@@ -922,7 +1020,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                 umma_commit(&accfull[b]);
             }
             // the tensor cores are done with TMEM and shared memory before the CTA exits
-            mbar_wait(&accfull[(my_tiles - 1) & 1], ((my_tiles - 1) >> 1) & 1, p.err);
+            mbar_wait(&accfull[(my_tiles - 1) % kXAcc], ((my_tiles - 1) / kXAcc) & 1, p.err);
         }
     } else if (warp < kPfWorkers) {
         // ---- A: dequantise atom a of each K step into the fragment order of the
@@ -1006,6 +1104,9 @@ cudaError_t prefill_config()
 {
     cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bucket_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 bucket_small_smem(1024));
     return e;
 }
 
@@ -1111,10 +1212,16 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
     if ((e = atoms_map(&gu_shared, g0.shared_blob, p.H / kGroup, g0.I / 8, 1, g0.stride)) != cudaSuccess) return e;
     if ((e = atoms_map(&dn_pool, pool_down, g0.I / kGroup, p.H / 16, g0.n_slots, g0.stride)) != cudaSuccess) return e;
     if ((e = atoms_map(&dn_shared, shared_down, g0.I / kGroup, p.H / 16, 1, g0.stride)) != cudaSuccess) return e;
-    if ((e = launch_pdl(bucket_count_kernel, dim3(nch), dim3(256), 0, st, p)) != cudaSuccess) return e;
-    if ((e = launch_pdl(bucket_scan_kernel, dim3((p.E + 31) / 32), dim3(1024), 0, st, p)) != cudaSuccess) return e;
-    if ((e = launch_pdl(bucket_scatter_kernel, dim3(nch), dim3(32), 0, st, p)) != cudaSuccess) return e;
-    if ((e = launch_pdl(convert_x_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, g0)) != cudaSuccess) return e;
+    if (p.T <= kBucketSmallT) {
+        if ((e = launch_pdl(bucket_small_kernel, dim3(1 + (p.T + 31) / 32), dim3(1024), bucket_small_smem(p.E), st, p,
+                            g0)) != cudaSuccess)
+            return e;
+    } else {
+        if ((e = launch_pdl(bucket_count_kernel, dim3(nch), dim3(256), 0, st, p)) != cudaSuccess) return e;
+        if ((e = launch_pdl(bucket_scan_kernel, dim3((p.E + 31) / 32), dim3(1024), 0, st, p)) != cudaSuccess) return e;
+        if ((e = launch_pdl(bucket_scatter_kernel, dim3(nch), dim3(32), 0, st, p)) != cudaSuccess) return e;
+        if ((e = launch_pdl(convert_x_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, g0)) != cudaSuccess) return e;
+    }
     const int maxt = prefill_max_tiles(p.T, p.k, p.E);
     GemmParams g = g0;
     g.mode = 0;

@@ -120,9 +120,13 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const RouteParams p)
 
     if (warp < nrows && ok) {
         const int row = row0 + warp;
-        for (int t = 0; t < ntok; ++t) {
-            const float acc = router_dot(wrow + warp * H, xs + t * H, H, lane);
-            if (lane == 0) p.logits[size_t(tok0 + t) * (E + 1) + row] = acc;
+        float acc[kRouteToks];
+        router_dot_multi<kRouteToks>(wrow + warp * H, xs, H, ntok, lane, acc);
+        if (lane < ntok) {
+            float z = acc[0];
+#pragma unroll
+            for (int t = 1; t < kRouteToks; ++t) z = lane == t ? acc[t] : z;
+            p.logits[size_t(tok0 + lane) * (E + 1) + row] = z;
         }
     }
     if (!p.fused_topk) return;

@@ -38,6 +38,44 @@ __device__ __forceinline__ float router_dot(const uint16_t *row, const uint16_t 
     return acc;
 }
 
+// One router row dotted with ntok <= NT tokens (rows t of xs, H apart): each
+// result in router_dot's order (per lane four interleaved partial sums over
+// the lane's 8-element chunks, then (s0 + s1) + (s2 + s3), then the
+// butterfly), so out[t] equals router_dot(row, xs + t H) bit for bit; each
+// chunk of the row is loaded once for all tokens, and the tokens' chains are
+// independent, so their latencies overlap.
+template <int NT>
+__device__ __forceinline__ void router_dot_multi(const uint16_t *row, const uint16_t *xs, int H, int ntok, int lane,
+                                                 float (&out)[NT])
+{
+    float s[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+    for (int c = 8 * lane; c < H; c += 256) {
+        const uint4 wv = *reinterpret_cast<const uint4 *>(row + c);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t < ntok) {
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xs + size_t(t) * H + c);
+                s[t][0] = fmaf(bf16lo(wv.x), bf16lo(xv.x), s[t][0]);
+                s[t][1] = fmaf(bf16hi(wv.x), bf16hi(xv.x), s[t][1]);
+                s[t][2] = fmaf(bf16lo(wv.y), bf16lo(xv.y), s[t][2]);
+                s[t][3] = fmaf(bf16hi(wv.y), bf16hi(xv.y), s[t][3]);
+                s[t][0] = fmaf(bf16lo(wv.z), bf16lo(xv.z), s[t][0]);
+                s[t][1] = fmaf(bf16hi(wv.z), bf16hi(xv.z), s[t][1]);
+                s[t][2] = fmaf(bf16lo(wv.w), bf16lo(xv.w), s[t][2]);
+                s[t][3] = fmaf(bf16hi(wv.w), bf16hi(xv.w), s[t][3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        float acc = (s[t][0] + s[t][1]) + (s[t][2] + s[t][3]);
+        for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        out[t] = acc;
+    }
+}
+
 // Order-preserving map float -> uint32 (larger float, larger key); key 0 is
 // reserved for "taken / empty" (no finite or infinite float maps to it).
 __device__ __forceinline__ uint32_t fkey(float f)
