@@ -359,10 +359,12 @@ __device__ __forceinline__ bool group_sums(const uint16_t *hh, int U, int I, int
             const uint4 h0 = *reinterpret_cast<const uint4 *>(src), h1 = *reinterpret_cast<const uint4 *>(src + 8);
             const uint32_t v[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                s += bf16lo(v[j]) + bf16hi(v[j]);
-                miss |= !ready16(v[j]);
-            }
+            for (int j = 0; j < 8; ++j) s += bf16lo(v[j]) + bf16hi(v[j]);
+            // the sentinel is a NaN, so only a non-finite partial sum can hide one:
+            // then (rarely: NaN or infinite data) check the half-words themselves
+            if (!(fabsf(s) <= 3.402823466e38f))
+#pragma unroll
+                for (int j = 0; j < 8; ++j) miss |= !ready16(v[j]);
         }
         s += __shfl_xor_sync(0xffffffffu, s, 1);
         s += __shfl_xor_sync(0xffffffffu, s, 2);
@@ -620,24 +622,26 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
             }
         }
 
-        // ---- E. request the routed units and (CTAs with output rows) the down rows of
-        // every routed expert: lane 0 of warp w issues copy w, w + 16, ... (units
-        // first), so the copies go out in parallel
-        if (lane == 0) {
-            const int nd = has_down ? k : 0;
-            for (int it = warp; it < n_mine + nd; it += kStkWarps) {
-                if (it < n_mine) {
-                    const int r = ord + it * G, u = 1 + r / nrb, rb = r % nrb;
-                    const uint8_t *blob = blob_of(u);
-                    if (blob) {
-                        mbar_arrive_expect_tx(&ubar[it], ubytes);
-                        bulk_g2s(units + size_t(it) * ubytes, blob + size_t(rb) * ubytes, ubytes, &ubar[it], pol);
-                    } else {
-                        set_error(p.err, SMOE_DEV_BAD_SLOT);
-                        mbar_arrive(&ubar[it]);
-                    }
+        // ---- E. request the routed units: lane 0 of warp w issues unit w, w + 16, ...
+        // so the copies go out in parallel. The CTAs with output rows request the
+        // down rows of every routed expert only once their first unit has landed
+        // (in F): they are needed last, and requested with the units they delayed
+        // the units' first bytes.
+        if (lane == 0)
+            for (int it = warp; it < n_mine; it += kStkWarps) {
+                const int r = ord + it * G, u = 1 + r / nrb, rb = r % nrb;
+                const uint8_t *blob = blob_of(u);
+                if (blob) {
+                    mbar_arrive_expect_tx(&ubar[it], ubytes);
+                    bulk_g2s(units + size_t(it) * ubytes, blob + size_t(rb) * ubytes, ubytes, &ubar[it], pol);
                 } else {
-                    const int u = 1 + (it - n_mine);
+                    set_error(p.err, SMOE_DEV_BAD_SLOT);
+                    mbar_arrive(&ubar[it]);
+                }
+            }
+        auto issue_down = [&] {                                      // lane 0 of warp w: expert 1 + w
+            if (has_down && lane == 0)
+                for (int u = 1 + warp; u <= k; u += kStkWarps) {
                     const uint8_t *blob = blob_of(u);
                     if (blob) {
                         mbar_arrive_expect_tx(&dbar[u], wbytes);
@@ -646,8 +650,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                         mbar_arrive(&dbar[u]);
                     }
                 }
-            }
-        }
+        };
+        if (n_mine == 0) issue_down();
 
         // ---- C. the shared expert's unit c (its weights are in shared memory), while
         // the routed units' first bytes are on their way
@@ -669,6 +673,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
             const int r = ord + i * G;
             const bool valid = blob_of(1 + r / nrb) != nullptr;     // uniform
             if (!bad && !mbar_wait(&ubar[i], par, p.err)) bad = true;
+            if (i == 0) issue_down();
             float2 a = make_float2(0.f, 0.f);
             if (valid && !bad) a = gateup_partial(units + size_t(i) * ubytes, f0, f1, ngH, warp, lane);
             if ((lane & 3) == 0) red[(i * kStkWarps + warp) * 8 + (lane >> 2)] = a;
