@@ -340,35 +340,35 @@ __device__ __forceinline__ float2 down_atom(const uint8_t *atom, uint4 h0, uint4
 }
 
 // Every (expert u, group kb) sum of h's high + low parts, gsum[u * ngI + kb]
-// (the bias term of down_atom), in a fixed order: eight threads per group,
-// thread q of them holding the high (q < 4) or low parts of columns
-// 16 (q % 4) .. + 15, each sums its 16 values in column order, then the eight
-// partial sums combine in a fixed tree (pairs, then quads, then the halves).
-// The whole CTA calls it; each group is summed once per layer. It reads every
-// half-word of h once, so it also returns whether this thread met the
-// sentinel (a value not yet written when h was copied).
+// (the bias term of down_atom), in a fixed order: four threads per group,
+// thread q of them summing the high then the low parts of columns
+// 16 q .. 16 q + 15 in column order, then the four partial sums in a fixed
+// tree (pairs, then the halves). The whole CTA calls it; each group is summed
+// once per layer (4 U I/64 <= 512 threads: one round at the 80B shape). It
+// reads every half-word of h once, so it also returns whether this thread met
+// the sentinel (a value not yet written when h was copied).
 __device__ __forceinline__ bool group_sums(const uint16_t *hh, int U, int I, int ngI, float *gsum)
 {
-    const int tid = threadIdx.x, q = tid & 7, part = q >> 2, t4 = q & 3;
+    const int tid = threadIdx.x, q = tid & 3;
     bool miss = false;
-    for (int gi = tid >> 3; gi < ((U * ngI + 3) & ~3); gi += kStkThreads / 8) {   // whole warps per round
+    for (int gi = tid >> 2; gi < ((U * ngI + 7) & ~7); gi += kStkThreads / 4) {   // whole warps per round
         float s = 0.f;
         if (gi < U * ngI) {
             const int u = gi / ngI, kb = gi - u * ngI;
-            const uint16_t *src = hh + (size_t(part) * U + u) * I + kb * kGroup + 16 * t4;
-            const uint4 h0 = *reinterpret_cast<const uint4 *>(src), h1 = *reinterpret_cast<const uint4 *>(src + 8);
-            const uint32_t v[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+            const uint16_t *hi = hh + size_t(u) * I + kb * kGroup + 16 * q, *lo = hi + size_t(U) * I;
+            const uint4 a = *reinterpret_cast<const uint4 *>(hi), b = *reinterpret_cast<const uint4 *>(hi + 8);
+            const uint4 c = *reinterpret_cast<const uint4 *>(lo), d = *reinterpret_cast<const uint4 *>(lo + 8);
+            const uint32_t v[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s += bf16lo(v[j]) + bf16hi(v[j]);
+            for (int j = 0; j < 16; ++j) s += bf16lo(v[j]) + bf16hi(v[j]);
             // the sentinel is a NaN, so only a non-finite partial sum can hide one:
             // then (rarely: NaN or infinite data) check the half-words themselves
             if (!(fabsf(s) <= 3.402823466e38f))
 #pragma unroll
-                for (int j = 0; j < 8; ++j) miss |= !ready16(v[j]);
+                for (int j = 0; j < 16; ++j) miss |= !ready16(v[j]);
         }
         s += __shfl_xor_sync(0xffffffffu, s, 1);
         s += __shfl_xor_sync(0xffffffffu, s, 2);
-        s += __shfl_xor_sync(0xffffffffu, s, 4);
         if (q == 0 && gi < U * ngI) gsum[gi] = s;
     }
     return miss;
