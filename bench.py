@@ -155,31 +155,29 @@ STACK_SOURCES = ["int4_routed_expert_router_gb300/csrc/decode_stack.cu",
                  "int4_routed_expert_router_gb300/csrc/smoe_internal.h"]
 
 
-def stack_traffic(workload: str):
-    """DRAM bytes per layer of the stack kernel from the committed ncu summary
-    (captured on a shorter stack; the traffic is per layer), only if its
-    sources are unchanged since it was taken."""
-    p = os.path.join(ROOT, "profiles", "decode_stack_kernel_traffic.json")
+def _traffic_record(name: str, sources, workload: str, key: str):
+    """Field `key` of workload's record in profiles/<name> (a committed ncu
+    capture: {"source_sha256": ..., "records": {workload: {...}}}), only if
+    the kernel's sources are unchanged since it was taken."""
+    p = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("source_sha256") != src_hash(STACK_SOURCES) or d.get("workload") != workload:
+    if d.get("source_sha256") != src_hash(sources):
         return None
-    return d.get("dram_bytes_per_layer")
+    return d.get("records", {}).get(workload, {}).get(key)
+
+
+def stack_traffic(workload: str):
+    """DRAM bytes per layer of the stack kernel (captured on a shorter stack;
+    the traffic is per layer)."""
+    return _traffic_record("decode_stack_kernel_traffic.json", STACK_SOURCES, workload, "dram_bytes_per_layer")
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, only if the kernel sources are unchanged since it was taken."""
-    p = os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")
-    if not os.path.exists(p):
-        return None
-    with open(p) as f:
-        d = json.load(f)
-    if d.get("source_sha256") != src_hash(DECODE_SOURCES) or d.get("workload") != workload:
-        return None
-    return d.get("dram_bytes_per_launch")
+    """DRAM bytes per launch (one layer) of the decode kernel."""
+    return _traffic_record("decode_kernel_traffic.json", DECODE_SOURCES, workload, "dram_bytes_per_launch")
 
 
 PREFILL_SOURCES = ["int4_routed_expert_router_gb300/csrc/prefill.cu",
@@ -188,16 +186,8 @@ PREFILL_SOURCES = ["int4_routed_expert_router_gb300/csrc/prefill.cu",
 
 
 def prefill_traffic(workload: str):
-    """DRAM bytes per launch of the gate/up expert GEMM from the committed ncu
-    summary, only if the prefill sources are unchanged since it was taken."""
-    p = os.path.join(ROOT, "profiles", "expert_gemm_traffic.json")
-    if not os.path.exists(p):
-        return None
-    with open(p) as f:
-        d = json.load(f)
-    if d.get("source_sha256") != src_hash(PREFILL_SOURCES) or d.get("workload") != workload:
-        return None
-    return d.get("dram_bytes_per_launch")
+    """DRAM bytes per launch of the gate/up expert GEMM."""
+    return _traffic_record("expert_gemm_traffic.json", PREFILL_SOURCES, workload, "dram_bytes_per_launch")
 
 
 L2_BYTES = 129 * 10**6
@@ -504,16 +494,8 @@ GDN_SOURCES = ["int4_routed_expert_router_gb300/csrc/deltanet.cu",
 
 
 def gdn_traffic(workload: str):
-    """DRAM bytes per launch of the DeltaNet step kernel from the committed
-    ncu summary, only if its sources are unchanged since it was taken."""
-    p = os.path.join(ROOT, "profiles", "gdn_step_kernel_traffic.json")
-    if not os.path.exists(p):
-        return None
-    with open(p) as f:
-        d = json.load(f)
-    if d.get("source_sha256") != src_hash(GDN_SOURCES) or d.get("workload") != workload:
-        return None
-    return d.get("dram_bytes_per_launch")
+    """DRAM bytes per launch of the DeltaNet step kernel."""
+    return _traffic_record("gdn_step_kernel_traffic.json", GDN_SOURCES, workload, "dram_bytes_per_launch")
 
 
 def measure_gdn(args, gs, dev, pk, pk_src):
