@@ -17,7 +17,7 @@
  * 64 along the input dimension, an fp16 scale s and bias b per group,
  * w = s*q + b (the same xix.ai page, last paragraph, names MLX-style int4 and
  * int8 group quantisation with 64-bit offsets). 8-bit experts are supported
- * for packing, routing, the T <= 8 expert kernel and the plain debug path
+ * for packing, routing, moe_forward at every T and the plain debug path
  * (see smoe_ctx_create). The routed experts of every layer live in
  * one pool of fixed-stride blobs, one blob per expert, reached through a slot
  * table (same page, paragraph on how it works: fixed-stride blobs, one read
@@ -166,9 +166,9 @@ typedef struct smoe_ctx smoe_ctx;
  * of n_layers layers and a pool of n_slots slots. table_dev is caller-owned
  * device memory of n_layers*E int32 (the slot table; filled by
  * set_slot_table). The context allocates no device memory. A context of
- * 8-bit experts (shape.bits = 8) serves moe_route, moe_forward for T <= 8
- * (the fused decode kernel reads both nibble planes) and moe_forward_debug;
- * moe_forward for T > 8, moe_forward_noalloc and moe_decode_stack return
+ * 8-bit experts (shape.bits = 8) serves moe_route, moe_forward (the T <= 8
+ * kernel and the bucketed expert GEMMs both read the two nibble planes) and
+ * moe_forward_debug; moe_forward_noalloc and moe_decode_stack return
  * SMOE_ENOTSUP for it (their kernels read 4-bit atoms).
  * Errors: SMOE_EINVAL, SMOE_ENOTSUP, SMOE_ECUDA. */
 SMOE_API int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_t n_slots,

@@ -46,7 +46,6 @@ constexpr int kPfRawWarp = kPfWorkers + kPfEpi;   // bulk copies of the raw atom
 constexpr int kPfBWarp = kPfRawWarp + 1;          // B by TMA boxes (router tokens; the down GEMM's h rows)
 constexpr int kPfMma = kPfBWarp + 1;              // tcgen05.mma issuer
 constexpr int kPfThreads = (kPfMma + 1) * 32;
-constexpr int kPfRawBytes = 8 * kAtomBytes;         // 4608: 8 row blocks x one group
 constexpr int kPfABytes = kPfM * kPfK * 2;          // 16 KiB
 constexpr int kPfBBytes = kPfMaxN * kPfK * 2;       // 32 KiB
 constexpr int kPfStageBytes = kPfABytes + kPfBBytes;
@@ -63,8 +62,18 @@ constexpr int kXStg = 4;           // operand stages: A in TMEM + B in shared me
 constexpr int kXAcc = 2;           // accumulator buffers in TMEM (the epilogue of a tile overlaps the next)
 constexpr int kXBBytes = kXMaxN * kPfK * 2;                 // 24 KiB
 constexpr uint32_t kXACol0 = kXAcc * kXMaxN;                // first A column
-constexpr int kXSmem = kXStg * kXBBytes + kXRaw * kPfRawBytes + 1024 /*align*/ + 512 /*barriers*/;
-static_assert(kXSmem <= 232448, "shared memory per CTA");
+
+// The raw-atom ring of the expert GEMMs for BITS-bit experts: bytes per atom,
+// slots, bytes per K step (8 atoms), and the CTA's shared memory.
+template <int BITS>
+struct XRaw {
+    static constexpr int AB = BITS == 8 ? kAtom8Bytes : kAtomBytes;
+    static constexpr int Slots = BITS == 8 ? 12 : kXRaw;
+    static constexpr int Step = 8 * AB;
+    static constexpr int Smem = kXStg * kXBBytes + Slots * Step + 1024 /*align*/ + 512 /*barriers*/;
+};
+static_assert(XRaw<8>::Smem <= 232448, "shared memory per CTA");
+static_assert(XRaw<4>::Smem <= 232448, "shared memory per CTA");
 static_assert(kXACol0 + kXStg * 32 <= 512, "TMEM columns");
 constexpr int kXGatherW0 = 19;     // gate/up: warps 19 .. 22 gather the B rows (cp.async)
 constexpr int kXGatherWarps = 4;
@@ -483,6 +492,15 @@ __device__ __forceinline__ uint32_t nib_pair_f16(uint32_t w, int m)
     return hsub2(r, 0x64006400u);
 }
 
+// fp16x2 (q_even, q_odd) of value pair m of an 8-bit atom's two nibble planes
+// (wl: the low nibbles, wh: the high nibbles, each in the 4-bit word layout):
+// 1024 + lo + 16 hi is exact in fp16 for q <= 255, and subtracting 1024 too.
+__device__ __forceinline__ uint32_t byte_pair_f16(uint32_t wl, uint32_t wh, int m)
+{
+    const uint32_t lo = (wl >> (4 * m)) & 0x000F000Fu, hi = (wh >> (4 * m)) & 0x000F000Fu;
+    return hsub2(lo | (hi << 4) | 0x64006400u, 0x64006400u);
+}
+
 // Bounded wait for the persistent GEMM: gives up after kWaitLimitNs of
 // global time, and once any wait of the CTA has given up (*abort set) every
 // later wait returns at once, so a failed CTA drains in bounded time.
@@ -547,6 +565,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
                  " [%0], [%1, {%2, %3}], [%4];"
                  ::"r"(dst), "l"(map), "r"(col), "r"(row), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// The raw 8-bit atoms of one K step (8 row blocks x one group, 8704 bytes) as
+// one box {136 words, 2 halves, 8 row blocks, 1 slot} of the 4-D map
+// [slot][row block][group x 2 halves][136 words]: a 1088-byte atom is 272
+// words, more than a box dimension may hold, so each atom is two halves.
+__device__ __forceinline__ void tma_raw8(uint32_t dst, const CUtensorMap *map, int kb, int mt, int slot, uint64_t *bar,
+                                         uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+                 ::"r"(dst), "l"(map), "r"(0), "r"(2 * kb), "r"(8 * mt), "r"(slot), "r"(smem_u32(bar)), "l"(policy)
                  : "memory");
 }
 
@@ -816,6 +847,7 @@ __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uin
 // warp 17 loads B with TMA in the down GEMM; warp 18 issues the MMAs; warps
 // 19-22 gather B rows by token in the gate/up GEMM and join the epilogue in
 // the down GEMM. A and B of a K step share one stage of a 4-deep ring.
+template <int BITS>
 __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmParams p,
                                                                     const __grid_constant__ CUtensorMap bmap,
                                                                     const __grid_constant__ CUtensorMap amap,
@@ -826,10 +858,11 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *bst = smem;                                          // kXStg x 24 KiB, 128-byte swizzled rows
-    uint8_t *raw = smem + kXStg * kXBBytes;                       // kXRaw x 4608 B
-    uint64_t *bars = reinterpret_cast<uint64_t *>(raw + kXRaw * kPfRawBytes);
-    uint64_t *rawfull = bars, *rawempty = bars + kXRaw;
-    uint64_t *full = bars + 2 * kXRaw, *empty = full + kXStg;     // stage s: A (TMEM) + B (smem)
+    using RW = XRaw<BITS>;
+    uint8_t *raw = smem + kXStg * kXBBytes;                       // RW::Slots x RW::Step bytes
+    uint64_t *bars = reinterpret_cast<uint64_t *>(raw + RW::Slots * RW::Step);
+    uint64_t *rawfull = bars, *rawempty = bars + RW::Slots;
+    uint64_t *full = bars + 2 * RW::Slots, *empty = full + kXStg;     // stage s: A (TMEM) + B (smem)
     uint64_t *accfull = empty + kXStg, *accempty = accfull + kXAcc;
     uint64_t *bfull = accempty + kXAcc;                           // down: B copies of stage s (TMA)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bfull + kXStg);
@@ -844,7 +877,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     auto tile_of = [&](int i) { return int(blockIdx.x) + i * int(gridDim.x); };
 
     if (tid == 0) {
-        for (int r = 0; r < kXRaw; ++r) {
+        for (int r = 0; r < RW::Slots; ++r) {
             mbar_init(&rawfull[r], 1);
             mbar_init(&rawempty[r], kPfWorkers);
         }
@@ -879,7 +912,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     if (epi_role) {
         epilogue(p, tmem, accfull, accempty, abort, warp, lane, my_tiles, tile_of);
     } else if (warp == kPfRawWarp) {
-        // ---- raw int4 atoms (8 row blocks x one group) per K step: one TMA box each
+        // ---- raw atoms (8 row blocks x one group) per K step: one TMA box each
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&amap) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(&amap_shared) : "memory");
@@ -894,18 +927,19 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!pf_wait(&rawempty[r], ph ^ 1u, p.err, abort)) { ok = false; break; }
                     if (ti.valid) {
-                        mbar_arrive_expect_tx(&rawfull[r], kPfRawBytes);
-                        tma_raw(smem_u32(raw + r * kPfRawBytes), map, kb, mt, ti.slot, &rawfull[r], pol);
+                        mbar_arrive_expect_tx(&rawfull[r], RW::Step);
+                        if constexpr (BITS == 8) tma_raw8(smem_u32(raw + r * RW::Step), map, kb, mt, ti.slot, &rawfull[r], pol);
+                        else tma_raw(smem_u32(raw + r * RW::Step), map, kb, mt, ti.slot, &rawfull[r], pol);
                     } else {
                         mbar_arrive(&rawfull[r]);              // nothing to load; the epilogue writes zeros
                     }
                     ++done;
-                    if (++r == kXRaw) { r = 0; ph ^= 1u; }
+                    if (++r == RW::Slots) { r = 0; ph ^= 1u; }
                 }
             }
             // let the last copy into each slot land before the CTA can exit
-            for (int g2 = done - 1; g2 >= 0 && g2 >= done - kXRaw; --g2)
-                mbar_wait(&rawfull[g2 % kXRaw], (g2 / kXRaw) & 1, p.err);
+            for (int g2 = done - 1; g2 >= 0 && g2 >= done - RW::Slots; --g2)
+                mbar_wait(&rawfull[g2 % RW::Slots], (g2 / RW::Slots) & 1, p.err);
         }
     } else if (warp >= kXGatherW0) {
         if (p.mode == 0) {
@@ -1032,23 +1066,33 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
         uint32_t phr = 0, pha = 0;                                // raw ring, operand ring
         for (int gk = 0; gk < total; ++gk) {
             pf_wait(&rawfull[r], phr, p.err, abort);
-            const uint8_t *atom = raw + r * kPfRawBytes + a * kAtomBytes;
-            const uint4 q = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
-            const uint2 sbp = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+            const uint8_t *atom = raw + r * RW::Step + a * RW::AB;
+            const uint4 q = *reinterpret_cast<const uint4 *>(atom + 16 * lane);   // (low nibbles, 8-bit)
+            uint4 qh = make_uint4(0u, 0u, 0u, 0u);                                // 8-bit: the high nibbles
+            if constexpr (BITS == 8) qh = *reinterpret_cast<const uint4 *>(atom + kAtomQBytes + 16 * lane);
+            const uint2 sbp = *reinterpret_cast<const uint2 *>(atom + (BITS == 8 ? 2 : 1) * kAtomQBytes + 8 * g);
             __syncwarp();
             if (lane == 0) mbar_arrive(&rawempty[r]);
-            if (++r == kXRaw) { r = 0; phr ^= 1u; }
+            if (++r == RW::Slots) { r = 0; phr ^= 1u; }
             const uint32_t s0 = __byte_perm(sbp.x, 0, 0x1010), b0 = __byte_perm(sbp.x, 0, 0x3232);   // row g
             const uint32_t s1 = __byte_perm(sbp.y, 0, 0x1010), b1 = __byte_perm(sbp.y, 0, 0x3232);   // row g + 8
             const uint32_t wg[2] = {q.x, q.y}, wh[2] = {q.z, q.w};
+            const uint32_t wg8[2] = {qh.x, qh.y}, wh8[2] = {qh.z, qh.w};
             uint32_t v[16];
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
                 const int m0 = 2 * (rr & 1);
-                v[4 * rr + 0] = hfma2(nib_pair_f16(wg[rr >> 1], m0), s0, b0);
-                v[4 * rr + 1] = hfma2(nib_pair_f16(wg[rr >> 1], m0 + 1), s0, b0);
-                v[4 * rr + 2] = hfma2(nib_pair_f16(wh[rr >> 1], m0), s1, b1);
-                v[4 * rr + 3] = hfma2(nib_pair_f16(wh[rr >> 1], m0 + 1), s1, b1);
+                if constexpr (BITS == 8) {
+                    v[4 * rr + 0] = hfma2(byte_pair_f16(wg[rr >> 1], wg8[rr >> 1], m0), s0, b0);
+                    v[4 * rr + 1] = hfma2(byte_pair_f16(wg[rr >> 1], wg8[rr >> 1], m0 + 1), s0, b0);
+                    v[4 * rr + 2] = hfma2(byte_pair_f16(wh[rr >> 1], wh8[rr >> 1], m0), s1, b1);
+                    v[4 * rr + 3] = hfma2(byte_pair_f16(wh[rr >> 1], wh8[rr >> 1], m0 + 1), s1, b1);
+                } else {
+                    v[4 * rr + 0] = hfma2(nib_pair_f16(wg[rr >> 1], m0), s0, b0);
+                    v[4 * rr + 1] = hfma2(nib_pair_f16(wg[rr >> 1], m0 + 1), s0, b0);
+                    v[4 * rr + 2] = hfma2(nib_pair_f16(wh[rr >> 1], m0), s1, b1);
+                    v[4 * rr + 3] = hfma2(nib_pair_f16(wh[rr >> 1], m0 + 1), s1, b1);
+                }
             }
             pf_wait(&empty[sa], pha ^ 1u, p.err, abort);
             tmem_st16x256x4(tmem + lane_base + kXACol0 + uint32_t(32 * sa), v);
@@ -1103,7 +1147,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const PrefillParams p)
 cudaError_t prefill_config()
 {
     cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(expert_gemm_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, XRaw<4>::Smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(expert_gemm_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, XRaw<8>::Smem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bucket_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  bucket_small_smem(1024));
@@ -1160,6 +1207,25 @@ static cudaError_t atoms_map(CUtensorMap *m, const void *base, int groups, int r
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The same for 8-bit atoms (1088 bytes = 272 words, above the 256 a box
+// dimension may hold): [slot][row block][group x 2 halves][136 words], one
+// box {136 words, 2 halves, 8 row blocks, 1 slot} = 8 whole atoms per K step.
+static cudaError_t atoms_map8(CUtensorMap *m, const void *base, int groups, int row_blocks, int64_t n_slots,
+                              uint64_t stride)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    constexpr int kHalfWords = kAtom8Bytes / 8;                  // 136
+    const cuuint64_t dims[4] = {uint64_t(kHalfWords), uint64_t(groups) * 2, uint64_t(row_blocks), uint64_t(n_slots)};
+    const cuuint64_t strides[3] = {uint64_t(kAtom8Bytes / 2), uint64_t(groups) * kAtom8Bytes, stride};
+    const cuuint32_t box[4] = {uint32_t(kHalfWords), 2, 8, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void *>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 static cudaError_t rows_map(CUtensorMap *m, const void *base, bool bf16, uint64_t cols, uint64_t rows)
 {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -1205,13 +1271,15 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
     if (e != cudaSuccess) return e;
     if ((e = rows_map(&hmap, g0.hbuf, false, uint64_t(g0.I), uint64_t(p.P + p.T))) != cudaSuccess) return e;
     // raw atoms: gate/up region [I/8 row blocks][H/64 groups], down region [H/16][I/64] at I/8 x H/64 atoms
-    const uint64_t down_off = uint64_t(g0.I / 8) * (p.H / kGroup) * kAtomBytes;
+    const bool b8 = g0.bits == 8;
+    const uint64_t down_off = uint64_t(g0.I / 8) * (p.H / kGroup) * (b8 ? kAtom8Bytes : kAtomBytes);
     const uint8_t *shared_down = g0.shared_blob + down_off, *pool_down = g0.pool + down_off;
+    auto amap = b8 ? atoms_map8 : atoms_map;
     CUtensorMap gu_pool, gu_shared, dn_pool, dn_shared;
-    if ((e = atoms_map(&gu_pool, g0.pool, p.H / kGroup, g0.I / 8, g0.n_slots, g0.stride)) != cudaSuccess) return e;
-    if ((e = atoms_map(&gu_shared, g0.shared_blob, p.H / kGroup, g0.I / 8, 1, g0.stride)) != cudaSuccess) return e;
-    if ((e = atoms_map(&dn_pool, pool_down, g0.I / kGroup, p.H / 16, g0.n_slots, g0.stride)) != cudaSuccess) return e;
-    if ((e = atoms_map(&dn_shared, shared_down, g0.I / kGroup, p.H / 16, 1, g0.stride)) != cudaSuccess) return e;
+    if ((e = amap(&gu_pool, g0.pool, p.H / kGroup, g0.I / 8, g0.n_slots, g0.stride)) != cudaSuccess) return e;
+    if ((e = amap(&gu_shared, g0.shared_blob, p.H / kGroup, g0.I / 8, 1, g0.stride)) != cudaSuccess) return e;
+    if ((e = amap(&dn_pool, pool_down, g0.I / kGroup, p.H / 16, g0.n_slots, g0.stride)) != cudaSuccess) return e;
+    if ((e = amap(&dn_shared, shared_down, g0.I / kGroup, p.H / 16, 1, g0.stride)) != cudaSuccess) return e;
     if (p.T <= kBucketSmallT) {
         if ((e = launch_pdl(bucket_small_kernel, dim3(1 + (p.T + 31) / 32), dim3(1024), bucket_small_smem(p.E), st, p,
                             g0)) != cudaSuccess)
@@ -1227,14 +1295,16 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
     g.mode = 0;
     g.m_tiles = g.I / 64;
     if ((e = prof_record(nprof > 0 ? prof[0] : nullptr, st)) != cudaSuccess) return e;
-    if ((e = launch_pdl(expert_gemm_kernel, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), kXSmem, st, g, xmap,
-                        gu_pool, gu_shared)) != cudaSuccess)
+    auto kern = b8 ? expert_gemm_kernel<8> : expert_gemm_kernel<4>;
+    const int xsmem = b8 ? XRaw<8>::Smem : XRaw<4>::Smem;
+    if ((e = launch_pdl(kern, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), xsmem, st, g, xmap, gu_pool,
+                        gu_shared)) != cudaSuccess)
         return e;
     if ((e = prof_record(nprof > 1 ? prof[1] : nullptr, st)) != cudaSuccess) return e;
     g.mode = 1;
     g.m_tiles = p.H / kPfM;
-    if ((e = launch_pdl(expert_gemm_kernel, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), kXSmem, st, g, hmap,
-                        dn_pool, dn_shared)) != cudaSuccess)
+    if ((e = launch_pdl(kern, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), xsmem, st, g, hmap, dn_pool,
+                        dn_shared)) != cudaSuccess)
         return e;
     if ((e = prof_record(nprof > 2 ? prof[2] : nullptr, st)) != cudaSuccess) return e;
     return launch_pdl(combine_kernel, dim3((p.H / 4 + 255) / 256, p.T), dim3(256), 0, st, p);

@@ -438,8 +438,8 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
 {
     if (!ctx || T < 0 || T > SMOE_MAX_TOKENS) return SMOE_EINVAL;
     if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
-    // 8-bit experts: the T <= 8 kernel only (the bucketed path takes 4-bit atoms)
-    if (ctx->shape.bits != 4 && (T > kDecodeMaxT || !ctx->decode_ok)) return SMOE_ENOTSUP;
+    // 8-bit experts: the bucketed path for T > 8, the T <= 8 kernel where it fits
+    if (ctx->shape.bits != 4 && T <= kDecodeMaxT && !ctx->decode_ok) return SMOE_ENOTSUP;
     if (T == 0) return SMOE_OK;                      // nothing to do; the buffers may be null
     if (!x || !ids || !w || !gate || !pool || !shared_blob || !out || !workspace || !err) return SMOE_EINVAL;
     if (!aligned16(x) || !aligned16(pool) || !aligned16(shared_blob) || !aligned16(workspace) || !aligned16(out) ||
@@ -494,6 +494,7 @@ extern "C" int moe_forward(const smoe_ctx *ctx, int32_t layer, const uint16_t *x
         g.k = q.k;
         g.I = ctx->shape.I;
         g.P = q.P;
+        g.bits = ctx->shape.bits;
         return cuda_status(launch_prefill(q, g, st, ctx->prof, ctx->nprof));
     }
     DecodeParams p = {};

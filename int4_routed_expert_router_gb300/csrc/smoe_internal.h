@@ -198,6 +198,7 @@ struct GemmParams {
     int32_t *err;
     int T, H, E, k, I, P;
     int m_tiles;
+    int bits;              // expert GEMMs: 4 or 8 (the atom format of pool and shared_blob)
 };
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled

@@ -1,6 +1,8 @@
-"""GPU: MLX 8-bit experts through the fused decode kernel (moe_forward,
-T <= 8), against the oracle's 8-bit layer, element by element: the 80B shape
-at T = 1 and 8 on the GPU's own routing, bit-identity across reruns and slot
+"""GPU: MLX 8-bit experts through moe_forward, against the oracle's 8-bit
+layer, element by element: the fused decode kernel (T <= 8) at T = 1 and 8
+and the token-bucketed grouped GEMMs (T > 8) at T = 9 and 64 on the GPU's
+own routing, and at T = 600 with every token routed among 12 experts (three
+tiles per expert, the last one ragged); bit-identity across reruns and slot
 permutations, agreement with the plain CUDA path, and the calls that still
 take only 4-bit experts."""
 import numpy as np
@@ -30,7 +32,7 @@ def p80_8():
     return W.DevicePool(wl, n_layers=2), W.LayerInputs(wl, 2)
 
 
-@pytest.mark.parametrize("T", [1, 8])
+@pytest.mark.parametrize("T", [1, 8, 9, 64])
 def test_8bit_decode_against_oracle(p80_8, T):
     pool, inp = p80_8
     wl = pool.wl
@@ -51,7 +53,7 @@ def test_8bit_bit_identical_across_runs_and_slot_permutations(p80_8):
     wl = pool.wl
     perm = np.random.default_rng(21).permutation(2 * wl.E).astype(np.int32).reshape(2, wl.E)
     other = W.DevicePool(wl, n_layers=2, table=perm)
-    for T in (1, 4):
+    for T in (1, 4, 40):
         x = synthetic.activations(wl.seed, T, wl.H, tag=700 + T)
         ids, w, gate = gpu_route(pool, inp, 1, x)
         a = gpu_forward(pool, 1, x, ids, w, gate)
@@ -81,10 +83,28 @@ def test_8bit_fast_and_plain_paths_agree(p80_8):
     assert np.linalg.norm(f - d) <= 2 * 5e-3 * np.linalg.norm(ref["out64"])
 
 
+def test_8bit_bucketed_multi_tile_experts(p80_8):
+    """600 tokens, each routed to 10 of the same 12 experts (about 500 pairs
+    per expert: three tiles of at most 192 tokens, the last one ragged),
+    through the large-T bucketing; weights are the oracle's probabilities
+    renormalised over that choice. A rerun is bit-identical."""
+    pool, inp = p80_8
+    wl = pool.wl
+    T = 600
+    x = synthetic.activations(wl.seed, T, wl.H, tag=901)
+    rng = np.random.default_rng(33)
+    hot = rng.choice(wl.E, 12, replace=False)
+    ids = np.stack([rng.choice(hot, wl.k, replace=False) for _ in range(T)]).astype(np.int32)
+    ref = oracle_shards.tokens_sharded(wl.name, 1, x, ids, inp.Wr_bits[1], inp.ws_bits[1])
+    out = gpu_forward(pool, 1, x, ids, ref["w_used"], ref["gate"])
+    assert_output_close(out, ref["out64"])
+    assert np.array_equal(out, gpu_forward(pool, 1, x, ids, ref["w_used"], ref["gate"]))
+
+
 def test_8bit_calls_that_take_only_4bit_experts(p80_8):
     pool, inp = p80_8
     wl = pool.wl
-    T = 9                                                 # the token-bucketed path reads 4-bit atoms
+    T = 2
     x = W.bf16_tensor(synthetic.activations(wl.seed, T, wl.H, tag=5))
     ids = torch.zeros((T, wl.k), dtype=torch.int32, device="cuda")
     w = torch.zeros((T, wl.k), dtype=torch.float32, device="cuda")
@@ -92,9 +112,6 @@ def test_8bit_calls_that_take_only_4bit_experts(p80_8):
     out = torch.zeros((T, wl.H), dtype=torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(smoe.SmoeError) as ei:
-        smoe.moe_forward(pool.ctx, 0, x, ids, w, gate, pool.pool, pool.shared[0], out, W.workspace(pool.ctx, T), err)
-    assert ei.value.status == smoe.ENOTSUP
-    with pytest.raises(smoe.SmoeError) as ei:
-        smoe.moe_forward_noalloc(pool.ctx, 0, x[:2], ids[:2], w[:2], gate[:2], pool.pool, pool.shared[0], out[:2], err)
+        smoe.moe_forward_noalloc(pool.ctx, 0, x, ids, w, gate, pool.pool, pool.shared[0], out, err)
     assert ei.value.status == smoe.ENOTSUP
     assert pool.ctx.stack_workspace_bytes(2) == 0
