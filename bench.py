@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode80b")
-    ap.add_argument("--extra", default="prefill80b,zipf80b_t64,decode35b,decode80b_int8,gdn80b",
+    ap.add_argument("--extra", default="prefill80b,zipf80b_t64,decode35b,decode80b_int8,prefill80b_int8,gdn80b",
                     help="comma-separated workloads measured after the headline, as sub-records of the same "
                          "line (N = 1 only; empty: none)")
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (profiling of small cases)")

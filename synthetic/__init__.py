@@ -242,6 +242,8 @@ WORKLOADS = {
         Workload("decode80b_int8", 2048, 512, 10, 512, 512, 1, 48, True, False, 8008,
                  "80B-A3B-shaped decode with MLX 8-bit experts: H=2048, E=512, k=10, I=512, T=1, 48 layers, "
                  "permuted slots", bits=8),
+        Workload("prefill80b_int8", 2048, 512, 10, 512, 512, 8192, 1, False, False, 8208,
+                 "80B-shaped prefill with MLX 8-bit experts: T=8192, uniform router", bits=8),
     ]
 }
 
