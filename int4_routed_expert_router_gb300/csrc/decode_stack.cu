@@ -28,7 +28,8 @@
 //      the routed units' first bytes are on their way: done before the
 //      top-k, it delayed these CTAs' requests, and the slowest CTA's h gates
 //      every output CTA.
-//   F. Gate/up units as their bytes land -> h as bf16 high and low parts.
+//   F. Gate/up units, a batch at a time once the batch has landed -> h as
+//      bf16 high and low parts.
 //   G. CTAs c < H/16: poll all experts' h, down rows of every expert, combine
 //      in route order with the routing weights, + gate * shared expert +
 //      x_l, one bf16 rounding -> x_{l+1} (exchange buffer and the caller's
@@ -53,6 +54,7 @@ namespace smoe {
 
 constexpr int kStkWarps = 16;
 constexpr int kStkThreads = kStkWarps * 32;
+constexpr int kStkUnitBatch = 5;       // routed gate/up units a warp works on at once (80B: all of a CTA's)
 constexpr uint32_t kSentinel32 = 0xFFFFFFFFu;
 constexpr uint16_t kSentinel16 = 0xFFFFu;
 constexpr int kStkMaxE = 512;           // experts per layer the one-launch step takes (larger E: per-layer calls)
@@ -668,15 +670,32 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
             }
         }
 
-        // ---- F. routed gate/up units as they land; then warp i finishes unit i
-        for (int i = 0; i < n_mine; ++i) {
-            const int r = ord + i * G;
-            const bool valid = blob_of(1 + r / nrb) != nullptr;     // uniform
-            if (!bad && !mbar_wait(&ubar[i], par, p.err)) bad = true;
+        // ---- F. routed gate/up units; then warp i finishes unit i
+        // Up to kStkUnitBatch units at a time, once all of them have landed: the
+        // atoms of several units in flight per warp overlap their tensor-core and
+        // load latencies, which bound this phase more than the bytes' arrival.
+        for (int i = 0; i < n_mine; i += kStkUnitBatch) {
+            bool on[kStkUnitBatch], ok[kStkUnitBatch];
+#pragma unroll
+            for (int q = 0; q < kStkUnitBatch; ++q) {
+                on[q] = i + q < n_mine;
+                ok[q] = on[q] && blob_of(1 + (ord + (i + q) * G) / nrb) != nullptr;     // uniform
+            }
+#pragma unroll
+            for (int q = 0; q < kStkUnitBatch; ++q)
+                if (on[q] && !bad && !mbar_wait(&ubar[i + q], par, p.err)) bad = true;
             if (i == 0) issue_down();
-            float2 a = make_float2(0.f, 0.f);
-            if (valid && !bad) a = gateup_partial(units + size_t(i) * ubytes, f0, f1, ngH, warp, lane);
-            if ((lane & 3) == 0) red[(i * kStkWarps + warp) * 8 + (lane >> 2)] = a;
+            float2 a[kStkUnitBatch];
+#pragma unroll
+            for (int q = 0; q < kStkUnitBatch; ++q) {
+                a[q] = make_float2(0.f, 0.f);
+                if (ok[q] && !bad) a[q] = gateup_partial(units + size_t(i + q) * ubytes, f0, f1, ngH, warp, lane);
+            }
+            if ((lane & 3) == 0) {
+#pragma unroll
+                for (int q = 0; q < kStkUnitBatch; ++q)
+                    if (on[q]) red[((i + q) * kStkWarps + warp) * 8 + (lane >> 2)] = a[q];
+            }
         }
         __syncthreads();
         for (int i = warp; i < n_mine; i += kStkWarps) {
@@ -746,8 +765,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
             const int na = U * ngI, nj = (na - warp + kStkWarps - 1) / kStkWarps;   // this warp's atoms
             for (int j = 0; j < nj; j += 2) {
                 const bool two = j + 1 < nj;
-                const int a0 = warp + kStkWarps * j, a1 = a0 + kStkWarps;
-                const int u0 = a0 / ngI, u1 = two ? a1 / ngI : u0;
+                const int a0 = warp + kStkWarps * j, a1 = two ? a0 + kStkWarps : a0;
+                const int u0 = a0 / ngI, u1 = a1 / ngI;
                 if (!bad && !mbar_wait(&dbar[u0], par, p.err)) bad = true;
                 if (two && !bad && !mbar_wait(&dbar[u1], par, p.err)) bad = true;
                 uint4 h[4];                                          // atom 0: h0 h1, atom 1: h0 h1
@@ -756,20 +775,19 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                 if (lane < 8) {                  // B columns 0 (high parts, lanes 0..3) and 1 (low parts, 4..7)
                     const int part = lane >> 2, t4 = lane & 3;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (q < 2 || two) {
-                            const int a = q < 2 ? a0 : a1;
-                            h[q] = *reinterpret_cast<const uint4 *>(hh + (size_t(part) * U + a / ngI) * I +
-                                                                    (a % ngI) * kGroup + 16 * t4 + 8 * (q & 1));
-                        }
+                    for (int q = 0; q < 4; ++q) {
+                        const int a = q < 2 ? a0 : a1;
+                        h[q] = *reinterpret_cast<const uint4 *>(hh + (size_t(part) * U + a / ngI) * I +
+                                                                (a % ngI) * kGroup + 16 * t4 + 8 * (q & 1));
+                    }
                 }
-                const float gs0 = gsum_s[a0];
-                const float gs1 = two ? gsum_s[a1] : 0.f;
-                float2 y0 = make_float2(0.f, 0.f), y1 = y0;
-                if ((vmask >> u0 & 1u) && !bad)
-                    y0 = down_atom(wdn + size_t(u0) * wbytes + (a0 % ngI) * kAtomBytes, h[0], h[1], gs0, lane);
-                if (two && (vmask >> u1 & 1u) && !bad)
-                    y1 = down_atom(wdn + size_t(u1) * wbytes + (a1 % ngI) * kAtomBytes, h[2], h[3], gs1, lane);
+                // both atoms unconditionally (the second repeats the first when this
+                // warp has an odd count; a result not needed is dropped), so the two
+                // chains always overlap
+                float2 y0 = down_atom(wdn + size_t(u0) * wbytes + (a0 % ngI) * kAtomBytes, h[0], h[1], gsum_s[a0], lane);
+                float2 y1 = down_atom(wdn + size_t(u1) * wbytes + (a1 % ngI) * kAtomBytes, h[2], h[3], gsum_s[a1], lane);
+                if (!(vmask >> u0 & 1u) || bad) y0 = make_float2(0.f, 0.f);
+                if (!(vmask >> u1 & 1u) || bad) y1 = make_float2(0.f, 0.f);
                 if ((lane & 3) == 0) {
                     yd[a0 * 16 + (lane >> 2)] = y0.x;
                     yd[a0 * 16 + (lane >> 2) + 8] = y0.y;
