@@ -17,9 +17,9 @@
 //      polled from the exchange buffer).
 //   B. Router rows c, c + G, ... (row E is the shared-gate vector; loaded
 //      during the previous layer) dotted with x_l; the logits go out.
-//   D. One warp polls all E + 1 logits and picks the top k in registers
-//      (route_common.cuh's arithmetic, so ids, weights and gate equal
-//      moe_route's bit for bit); CTA 0 writes them out.
+//   D. Every thread polls its logit and the CTA picks the top k (the same
+//      selection and weights as route_common.cuh's, so ids, weights and
+//      gate equal moe_route's bit for bit); CTA 0 writes them out.
 //   E. The CTA requests its routed gate/up units (expert j in route order,
 //      row block rb: 32 contiguous atoms, one bulk copy each) and, for
 //      c < H/16, its down rows 16c .. 16c + 15 of every routed expert.

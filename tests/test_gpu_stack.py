@@ -82,6 +82,25 @@ def test_stack_routing_equals_moe_route_and_layers_match_moe_forward(name):
         assert_output_close(got, synthetic.bf16_bits_to_f32(ref_fwd).astype(np.float64))
 
 
+def test_stack_top_k_of_equal_logits():
+    """A layer whose router rows are all zero: every logit is 0, so the top-k
+    is decided by the tie rule alone (the lowest ids first) and the candidate
+    set is far wider than one warp (the slow ranking path). The ids and
+    weights equal moe_route's and the rule's: experts 0 .. k-1, each 1/k."""
+    pool, inp = make("decode80b", 2)
+    wl = pool.wl
+    inp.Wr[1].zero_()
+    x0 = synthetic.activations(wl.seed, 1, wl.H, tag=31)
+    xs, ids, w, gate, err = run_stack(pool, inp, x0)
+    assert smoe.check(err) == 0
+    xl = W.bits_of(xs[1:2])
+    ids_r, w_r, gate_r = gpu_route(pool, inp, 1, xl)
+    assert np.array_equal(ids[1].cpu().numpy(), ids_r[0])
+    assert np.array_equal(w[1].cpu().numpy(), w_r[0])
+    assert np.array_equal(ids_r[0], np.arange(wl.k))
+    assert np.allclose(w_r[0], 1.0 / wl.k, rtol=0, atol=1e-7)
+
+
 def test_stack_bit_identical_across_runs_slot_permutations_and_graph_replay():
     wl = synthetic.WORKLOADS["decode80b"]
     L = 3
