@@ -167,9 +167,9 @@ typedef struct smoe_ctx smoe_ctx;
  * device memory of n_layers*E int32 (the slot table; filled by
  * set_slot_table). The context allocates no device memory. A context of
  * 8-bit experts (shape.bits = 8) serves moe_route, moe_forward (the T <= 8
- * kernel and the bucketed expert GEMMs both read the two nibble planes) and
- * moe_forward_debug; moe_forward_noalloc and moe_decode_stack return
- * SMOE_ENOTSUP for it (their kernels read 4-bit atoms).
+ * kernel and the bucketed expert GEMMs both read the two nibble planes),
+ * moe_decode_stack and moe_forward_debug; moe_forward_noalloc returns
+ * SMOE_ENOTSUP for it (its kernel reads 4-bit atoms).
  * Errors: SMOE_EINVAL, SMOE_ENOTSUP, SMOE_ECUDA. */
 SMOE_API int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_t n_slots,
                     int32_t *table_dev, smoe_ctx **out);

@@ -63,22 +63,43 @@ struct StkSmem {
     int x_s, xsum, rows, table, sunit, units, wdn, red, hh, gsum, yd, ysum, mx, cand, sel, ints, bars, total;
 };
 
-__host__ __device__ inline StkSmem stk_smem(int H, int E, int I, int U, int nr, int nu)
+// Shared memory of the stack kernel. 4-bit atoms: the shared expert's unit,
+// nu routed units and the down rows of every expert each have a region of
+// their own, so the next layer's shared unit and shared down rows load during
+// this layer. 8-bit atoms (twice the bytes): one ring of nslot unit slots
+// (the shared unit, if the CTA has one, in slot 0, then the routed units);
+// once the units are read, the down rows, h, its group sums and the down
+// partial sums reuse the ring.
+__host__ __device__ inline StkSmem stk_smem(int H, int E, int I, int U, int nr, int nu, int bits, int nslot)
 {
     const int ngH = H / kGroup, ngI = I / kGroup;
+    const int AB = bits == 8 ? kAtom8Bytes : kAtomBytes;
     StkSmem L;
     int o = 0;
     L.x_s = o;   o = align128(o + 2 * H + 16);
     L.xsum = o;  o = align128(o + ngH * 4);
     L.rows = o;  o = align128(o + (nr > 0 ? nr : 1) * H * 2);
     L.table = o; o = align128(o + 2 * E * 4);
-    L.sunit = o; o = align128(o + ngH * kAtomBytes);
-    L.units = o; o = align128(o + (nu > 0 ? nu : 1) * ngH * kAtomBytes);
-    L.wdn = o;   o = align128(o + U * ngI * kAtomBytes);
-    L.red = o;   o = align128(o + (nu + 1) * kStkWarps * 8 * 8);
-    L.hh = o;    o = align128(o + U * 2 * I * 2);
-    L.gsum = o;  o = align128(o + U * ngI * 4);
-    L.yd = o;    o = align128(o + U * ngI * 16 * 4);
+    if (bits == 8) {
+        const int ring = (nslot > 0 ? nslot : 1) * ngH * AB;
+        L.sunit = o;
+        L.units = o;                                 // + one slot where the CTA has a shared unit
+        L.wdn = o;
+        L.hh = align128(L.wdn + U * ngI * AB);
+        L.gsum = align128(L.hh + U * 2 * I * 2);
+        L.yd = align128(L.gsum + U * ngI * 4);
+        const int reuse = align128(L.yd + U * ngI * 16 * 4) - o;
+        o = align128(o + (ring > reuse ? ring : reuse));
+        L.red = o;   o = align128(o + (nu + 1) * kStkWarps * 8 * 8);
+    } else {
+        L.sunit = o; o = align128(o + ngH * AB);
+        L.units = o; o = align128(o + (nu > 0 ? nu : 1) * ngH * AB);
+        L.wdn = o;   o = align128(o + U * ngI * AB);
+        L.red = o;   o = align128(o + (nu + 1) * kStkWarps * 8 * 8);
+        L.hh = o;    o = align128(o + U * 2 * I * 2);
+        L.gsum = o;  o = align128(o + U * ngI * 4);
+        L.yd = o;    o = align128(o + U * ngI * 16 * 4);
+    }
     L.ysum = o;  o = align128(o + U * 16 * 4);
     L.mx = o;    o = align128(o + 2 * kStkWarps * 4);
     L.cand = o;  o = align128(o + 2 * E * 4);
@@ -230,14 +251,20 @@ __device__ __forceinline__ XFrag load_xfrag(const uint16_t *x_s, const float *xs
 
 // The gate/up partial sums of one atom (16 rows x one 64-column group) for
 // the token (MMA column 0): lanes 4g (t4 = 0) get gate row g and up row g.
+// 8-bit atoms: each nibble plane runs the 4-bit fragments through its own
+// tensor-core chains and the epilogue weights the high plane by 16.
+template <int BITS>
 __device__ __forceinline__ float2 gateup_atom(const uint8_t *atom, const XFrag &f, int lane)
 {
     const int g = lane >> 2;
     const uint4 A = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
-    const uint2 SB = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+    uint4 Ah = A;
+    if constexpr (BITS == 8) Ah = *reinterpret_cast<const uint4 *>(atom + kAtomQBytes + 16 * lane);
+    const uint2 SB = *reinterpret_cast<const uint2 *>(atom + AtomFmt<BITS>::sb + 8 * g);
     const float xs_kb = f.xs;
     const uint32_t xl[4] = {f.xa.x, f.xa.y, f.xa.z, f.xa.w}, xr[4] = {f.xb.x, f.xb.y, f.xb.z, f.xb.w};
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    float hcc[4] = {0.f, 0.f, 0.f, 0.f}, hcc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int m = 0; m < 4; m += 2) {
         const uint32_t a0[4] = {nib_pair(A.x, m), nib_pair(A.z, m), nib_pair(A.y, m), nib_pair(A.w, m)};
@@ -245,26 +272,41 @@ __device__ __forceinline__ float2 gateup_atom(const uint8_t *atom, const XFrag &
                                 nib_pair(A.w, m + 1)};
         mma_bf16(acc, a0, xl[m], xr[m]);
         mma_bf16(acc2, a1, xl[m + 1], xr[m + 1]);
+        if constexpr (BITS == 8) {
+            const uint32_t b0[4] = {nib_pair(Ah.x, m), nib_pair(Ah.z, m), nib_pair(Ah.y, m), nib_pair(Ah.w, m)};
+            const uint32_t b1[4] = {nib_pair(Ah.x, m + 1), nib_pair(Ah.z, m + 1), nib_pair(Ah.y, m + 1),
+                                    nib_pair(Ah.w, m + 1)};
+            mma_bf16(hcc, b0, xl[m], xr[m]);
+            mma_bf16(hcc2, b1, xl[m + 1], xr[m + 1]);
+        }
     }
     float sg, bpg, su, bpu;
-    scale_bias(SB.x, sg, bpg);
-    scale_bias(SB.y, su, bpu);
-    return make_float2(fmaf(sg, acc[0] + acc2[0], bpg * xs_kb), fmaf(su, acc[2] + acc2[2], bpu * xs_kb));
+    if constexpr (BITS == 8) {
+        scale_bias8(SB.x, sg, bpg);
+        scale_bias8(SB.y, su, bpu);
+        return make_float2(fmaf(sg, fmaf(16.f, hcc[0] + hcc2[0], acc[0] + acc2[0]), bpg * xs_kb),
+                           fmaf(su, fmaf(16.f, hcc[2] + hcc2[2], acc[2] + acc2[2]), bpu * xs_kb));
+    } else {
+        scale_bias(SB.x, sg, bpg);
+        scale_bias(SB.y, su, bpu);
+        return make_float2(fmaf(sg, acc[0] + acc2[0], bpg * xs_kb), fmaf(su, acc[2] + acc2[2], bpu * xs_kb));
+    }
 }
 
 // One warp's partial sums of a gate/up unit (H/64 <= 32 atoms, one 64-column
 // group of x each) when the 16 warps share it: warp w takes atoms w and
 // w + 16 (f0, f1: their x fragments), whose tensor-core chains overlap, and
 // adds them in that order.
+template <int BITS>
 __device__ __forceinline__ float2 gateup_partial(const uint8_t *ubase, const XFrag &f0, const XFrag &f1, int ngH,
                                                  int warp, int lane)
 {
     float aG = 0.f, aU = 0.f;
     if (warp < ngH) {
         const int kb1 = warp + kStkWarps;
-        const float2 a = gateup_atom(ubase + warp * kAtomBytes, f0, lane);
+        const float2 a = gateup_atom<BITS>(ubase + warp * AtomFmt<BITS>::bytes, f0, lane);
         float2 b = make_float2(0.f, 0.f);
-        if (kb1 < ngH) b = gateup_atom(ubase + kb1 * kAtomBytes, f1, lane);
+        if (kb1 < ngH) b = gateup_atom<BITS>(ubase + kb1 * AtomFmt<BITS>::bytes, f1, lane);
         aG += a.x;
         aU += a.y;
         aG += b.x;
@@ -316,15 +358,20 @@ __device__ __forceinline__ void finish_unit(const float2 *red, int nw, bool vali
 // split into bf16 high and low parts as MMA columns 0 and 1: lanes 0..3 (B
 // column 0) hold the group's high parts, lanes 4..7 (column 1) the low parts,
 // h0: columns 16 t4 .. +7 of the group, h1: +8 .. +15; other lanes hold zeros.
-// One m16n8k16 step per 16 columns yields both partial sums; gsum: the
-// group's sum of high + low parts. Lanes 4g (t4 = 0) return rows g and g + 8.
+// One m16n8k16 step per 16 columns yields both partial sums (per nibble
+// plane for 8-bit atoms); gsum: the group's sum of high + low parts. Lanes 4g
+// (t4 = 0) return rows g and g + 8.
+template <int BITS>
 __device__ __forceinline__ float2 down_atom(const uint8_t *atom, uint4 h0, uint4 h1, float gsum, int lane)
 {
     const int g = lane >> 2;
     const uint4 A = *reinterpret_cast<const uint4 *>(atom + 16 * lane);
-    const uint2 SB = *reinterpret_cast<const uint2 *>(atom + kAtomQBytes + 8 * g);
+    uint4 Ah = A;
+    if constexpr (BITS == 8) Ah = *reinterpret_cast<const uint4 *>(atom + kAtomQBytes + 16 * lane);
+    const uint2 SB = *reinterpret_cast<const uint2 *>(atom + AtomFmt<BITS>::sb + 8 * g);
     const uint32_t ha_[4] = {h0.x, h0.y, h0.z, h0.w}, hb_[4] = {h1.x, h1.y, h1.z, h1.w};
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    float hcc[4] = {0.f, 0.f, 0.f, 0.f}, hcc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int m = 0; m < 4; m += 2) {
         const uint32_t a0[4] = {nib_pair(A.x, m), nib_pair(A.z, m), nib_pair(A.y, m), nib_pair(A.w, m)};
@@ -332,13 +379,29 @@ __device__ __forceinline__ float2 down_atom(const uint8_t *atom, uint4 h0, uint4
                                 nib_pair(A.w, m + 1)};
         mma_bf16(acc, a0, ha_[m], hb_[m]);
         mma_bf16(acc2, a1, ha_[m + 1], hb_[m + 1]);
+        if constexpr (BITS == 8) {
+            const uint32_t b0[4] = {nib_pair(Ah.x, m), nib_pair(Ah.z, m), nib_pair(Ah.y, m), nib_pair(Ah.w, m)};
+            const uint32_t b1[4] = {nib_pair(Ah.x, m + 1), nib_pair(Ah.z, m + 1), nib_pair(Ah.y, m + 1),
+                                    nib_pair(Ah.w, m + 1)};
+            mma_bf16(hcc, b0, ha_[m], hb_[m]);
+            mma_bf16(hcc2, b1, ha_[m + 1], hb_[m + 1]);
+        }
     }
     float s0, bp0, s1, bp1;
-    scale_bias(SB.x, s0, bp0);
-    scale_bias(SB.y, s1, bp1);
     // (row, column 0) + (row, column 1): the high and the low part's sums
-    return make_float2(fmaf(s0, (acc[0] + acc2[0]) + (acc[1] + acc2[1]), bp0 * gsum),
-                       fmaf(s1, (acc[2] + acc2[2]) + (acc[3] + acc2[3]), bp1 * gsum));
+    if constexpr (BITS == 8) {
+        scale_bias8(SB.x, s0, bp0);
+        scale_bias8(SB.y, s1, bp1);
+        return make_float2(fmaf(s0, fmaf(16.f, (hcc[0] + hcc2[0]) + (hcc[1] + hcc2[1]),
+                                         (acc[0] + acc2[0]) + (acc[1] + acc2[1])), bp0 * gsum),
+                           fmaf(s1, fmaf(16.f, (hcc[2] + hcc2[2]) + (hcc[3] + hcc2[3]),
+                                         (acc[2] + acc2[2]) + (acc[3] + acc2[3])), bp1 * gsum));
+    } else {
+        scale_bias(SB.x, s0, bp0);
+        scale_bias(SB.y, s1, bp1);
+        return make_float2(fmaf(s0, (acc[0] + acc2[0]) + (acc[1] + acc2[1]), bp0 * gsum),
+                           fmaf(s1, (acc[2] + acc2[2]) + (acc[3] + acc2[3]), bp1 * gsum));
+    }
 }
 
 // Every (expert u, group kb) sum of h's high + low parts, gsum[u * ngI + kb]
@@ -441,23 +504,27 @@ __device__ void block_topk(float z, const float *bias, int E, int k, uint32_t *m
 
 // NGI = I / 64 (1, 2, 4 or 8) is a template parameter: the atom and unit
 // bookkeeping divides by it and by I / 8, and division by a value known only at
-// run time cost tens of instructions per atom.
-template <int NGI>
+// run time cost tens of instructions per atom. BITS: 4, or 8 for MLX 8-bit
+// experts (two-plane atoms, the ring plan of stk_smem).
+template <int NGI, int BITS>
 __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __grid_constant__ StackParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int ngI = NGI, I = NGI * kGroup, nrb = I / 8;
+    constexpr int AB = AtomFmt<BITS>::bytes;
+    constexpr bool kRing = BITS == 8;                 // units, then down rows and h, share one ring
     const int H = p.H, E = p.E, k = p.k, U = p.U;
     const int ngH = H / kGroup, nD = H / 16;
-    const uint32_t ubytes = uint32_t(ngH * kAtomBytes), wbytes = uint32_t(ngI * kAtomBytes);
-    const uint64_t down_off = uint64_t(nrb) * ngH * kAtomBytes;
-    const StkSmem L = stk_smem(H, E, I, U, p.nr, p.nu);
+    const uint32_t ubytes = uint32_t(ngH * AB), wbytes = uint32_t(ngI * AB);
+    const uint64_t down_off = uint64_t(nrb) * ngH * AB;
+    const StkSmem L = stk_smem(H, E, I, U, p.nr, p.nu, BITS, p.nslot);
     uint16_t *x_s = reinterpret_cast<uint16_t *>(smem + L.x_s);
     float *xsum = reinterpret_cast<float *>(smem + L.xsum);
     uint16_t *rows = reinterpret_cast<uint16_t *>(smem + L.rows);
     int *tables = reinterpret_cast<int *>(smem + L.table);
+    const int c_ = int(blockIdx.x);
     uint8_t *sunit = smem + L.sunit;
-    uint8_t *units = smem + L.units;
+    uint8_t *units = smem + L.units + (kRing && c_ < nrb ? ubytes : 0u);   // ring: after the shared unit
     uint8_t *wdn = smem + L.wdn;
     float2 *red = reinterpret_cast<float2 *>(smem + L.red);          // [nu + 1][warps][8]
     uint16_t *hh = reinterpret_cast<uint16_t *>(smem + L.hh);        // [hi, lo][U][I]: h of the layer
@@ -523,7 +590,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
         bulk_nohint(x_s, p.xs, uint32_t(H * 2), xbar);
         issue_fixed(0);
         if (has_shared) issue_shared_unit(0);
-        if (has_down) issue_shared_down(0);
+        if (has_down && !kRing) issue_shared_down(0);
     }
     // ---- sentinel fill of the exchange buffers (16-byte stores over the grid),
     // then one grid-wide arrival before any CTA writes a value
@@ -552,6 +619,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
             if (slot < 0 || slot >= p.n_slots) return nullptr;
             return p.pool + uint64_t(slot) * p.stride;
         };
+
+        if (kRing && l > 0 && has_shared && tid == 0) issue_shared_unit(l);   // the ring is free again
 
         // ---- A. x_l
         if (l == 0) {
@@ -653,18 +722,18 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                     }
                 }
         };
-        if (n_mine == 0) issue_down();
+        if (n_mine == 0 && !kRing) issue_down();
 
         // ---- C. the shared expert's unit c (its weights are in shared memory), while
         // the routed units' first bytes are on their way
         if (has_shared) {
             if (!bad && !mbar_wait(sbar, par, p.err)) bad = true;
-            const float2 a = gateup_partial(sunit, f0, f1, ngH, warp, lane);
+            const float2 a = gateup_partial<BITS>(sunit, f0, f1, ngH, warp, lane);
             if ((lane & 3) == 0) red[(p.nu * kStkWarps + warp) * 8 + (lane >> 2)] = a;
             __syncthreads();
             if (warp == kStkWarps - 1)
                 finish_unit(red + p.nu * kStkWarps * 8, kStkWarps, true, hx_hi + 8 * c, hx_lo + 8 * c, hcnt, lane);
-            if (tid == 32 && l + 1 < p.n_layers) {
+            if (!kRing && tid == 32 && l + 1 < p.n_layers) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 issue_shared_unit(l + 1);
             }
@@ -684,12 +753,12 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
 #pragma unroll
             for (int q = 0; q < kStkUnitBatch; ++q)
                 if (on[q] && !bad && !mbar_wait(&ubar[i + q], par, p.err)) bad = true;
-            if (i == 0) issue_down();
+            if (i == 0 && !kRing) issue_down();
             float2 a[kStkUnitBatch];
 #pragma unroll
             for (int q = 0; q < kStkUnitBatch; ++q) {
                 a[q] = make_float2(0.f, 0.f);
-                if (ok[q] && !bad) a[q] = gateup_partial(units + size_t(i + q) * ubytes, f0, f1, ngH, warp, lane);
+                if (ok[q] && !bad) a[q] = gateup_partial<BITS>(units + size_t(i + q) * ubytes, f0, f1, ngH, warp, lane);
             }
             if ((lane & 3) == 0) {
 #pragma unroll
@@ -697,7 +766,13 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                     if (on[q]) red[((i + q) * kStkWarps + warp) * 8 + (lane >> 2)] = a[q];
             }
         }
+        // ring plan: the units are read, so the down rows may overwrite them
+        if (kRing) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
+        if (kRing) {
+            issue_down();
+            if (tid == 0 && has_down) issue_shared_down(l);
+        }
         for (int i = warp; i < n_mine; i += kStkWarps) {
             const int r = ord + i * G, u = 1 + r / nrb, rb = r % nrb;
             finish_unit(red + i * kStkWarps * 8, kStkWarps, blob_of(u) != nullptr && !bad,
@@ -784,8 +859,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                 // both atoms unconditionally (the second repeats the first when this
                 // warp has an odd count; a result not needed is dropped), so the two
                 // chains always overlap
-                float2 y0 = down_atom(wdn + size_t(u0) * wbytes + (a0 % ngI) * kAtomBytes, h[0], h[1], gsum_s[a0], lane);
-                float2 y1 = down_atom(wdn + size_t(u1) * wbytes + (a1 % ngI) * kAtomBytes, h[2], h[3], gsum_s[a1], lane);
+                float2 y0 = down_atom<BITS>(wdn + size_t(u0) * wbytes + (a0 % ngI) * AB, h[0], h[1], gsum_s[a0], lane);
+                float2 y1 = down_atom<BITS>(wdn + size_t(u1) * wbytes + (a1 % ngI) * AB, h[2], h[3], gsum_s[a1], lane);
                 if (!(vmask >> u0 & 1u) || bad) y0 = make_float2(0.f, 0.f);
                 if (!(vmask >> u1 & 1u) || bad) y1 = make_float2(0.f, 0.f);
                 if ((lane & 3) == 0) {
@@ -798,7 +873,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                 }
             }
             __syncthreads();
-            if (tid == 0 && l + 1 < p.n_layers) {                   // the shared down rows are read
+            if (!kRing && tid == 0 && l + 1 < p.n_layers) {         // the shared down rows are read
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 issue_shared_down(l + 1);
             }
@@ -828,13 +903,14 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
 
 // ---------------------------------------------------------------------- host
 
+template <int BITS>
 static const void *stack_kernel_for(int ngI)
 {
     switch (ngI) {
-    case 1: return reinterpret_cast<const void *>(&decode_stack_kernel<1>);
-    case 2: return reinterpret_cast<const void *>(&decode_stack_kernel<2>);
-    case 4: return reinterpret_cast<const void *>(&decode_stack_kernel<4>);
-    default: return reinterpret_cast<const void *>(&decode_stack_kernel<8>);
+    case 1: return reinterpret_cast<const void *>(&decode_stack_kernel<1, BITS>);
+    case 2: return reinterpret_cast<const void *>(&decode_stack_kernel<2, BITS>);
+    case 4: return reinterpret_cast<const void *>(&decode_stack_kernel<4, BITS>);
+    default: return reinterpret_cast<const void *>(&decode_stack_kernel<8, BITS>);
     }
 }
 
@@ -851,13 +927,22 @@ cudaError_t stack_config(smoe_ctx *ctx)
     c.U = s.k + 1;
     c.nr = (s.E + 1 + c.grid - 1) / c.grid;
     c.nu = (s.k * (s.I / 8) + c.grid - 1) / c.grid;
-    c.smem = stk_smem(s.H, s.E, s.I, c.U, c.nr, c.nu).total;
+    // most units (routed, plus the shared one where the CTA has it) of one CTA,
+    // with the kernel's order of the routed units
+    const int nD = s.H / 16, nrb = s.I / 8, R = s.k * nrb;
+    c.nslot = 0;
+    for (int b = 0; b < c.grid; ++b) {
+        const int ord = b >= nD ? b - nD : (nD - 1 - b) + (c.grid - nD);
+        const int n = (ord < R ? (R - 1 - ord) / c.grid + 1 : 0) + (b < nrb ? 1 : 0);
+        if (n > c.nslot) c.nslot = n;
+    }
+    c.smem = stk_smem(s.H, s.E, s.I, c.U, c.nr, c.nu, s.bits, c.nslot).total;
     const int ngI = s.I / kGroup;
     const bool ngi_ok = ngI == 1 || ngI == 2 || ngI == 4 || ngI == 8;
     c.ok = coop && ngi_ok && c.grid >= s.H / 16 && c.grid >= s.I / 8 && s.E % 4 == 0 && s.E <= kStkMaxE &&
-           c.nu <= kStkWarps && c.smem <= max_smem;
+           c.nu <= kStkWarps && c.smem <= max_smem && (s.bits == 4 || s.bits == 8);
     if (!c.ok) return cudaSuccess;
-    const void *kern = stack_kernel_for(ngI);
+    const void *kern = s.bits == 8 ? stack_kernel_for<8>(ngI) : stack_kernel_for<4>(ngI);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, c.smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -883,10 +968,17 @@ cudaError_t launch_stack(const smoe_ctx *ctx, const StackParams &p, cudaStream_t
     lc.attrs = at;
     lc.numAttrs = 1;
     const int ngI = p.I / kGroup;
-    if (ngI == 1) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<1>, p);
-    else if (ngI == 2) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<2>, p);
-    else if (ngI == 4) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<4>, p);
-    else e = cudaLaunchKernelEx(&lc, decode_stack_kernel<8>, p);
+    if (ctx->shape.bits == 8) {
+        if (ngI == 1) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<1, 8>, p);
+        else if (ngI == 2) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<2, 8>, p);
+        else if (ngI == 4) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<4, 8>, p);
+        else e = cudaLaunchKernelEx(&lc, decode_stack_kernel<8, 8>, p);
+    } else {
+        if (ngI == 1) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<1, 4>, p);
+        else if (ngI == 2) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<2, 4>, p);
+        else if (ngI == 4) e = cudaLaunchKernelEx(&lc, decode_stack_kernel<4, 4>, p);
+        else e = cudaLaunchKernelEx(&lc, decode_stack_kernel<8, 4>, p);
+    }
     if (e == cudaSuccess) e = prof_record(ctx->nprof > 1 ? ctx->prof[1] : nullptr, st);
     return e;
 }

@@ -571,7 +571,7 @@ static StackWs stack_ws(const smoe_ctx *ctx, int n)
 
 extern "C" uint64_t smoe_stack_workspace_bytes(const smoe_ctx *ctx, int32_t n_layers)
 {
-    if (!ctx || !ctx->stack.ok || ctx->shape.bits != 4 || n_layers < 1 || n_layers > kStackMaxLayers) return 0;
+    if (!ctx || !ctx->stack.ok || n_layers < 1 || n_layers > kStackMaxLayers) return 0;
     return stack_ws(ctx, n_layers).total;
 }
 
@@ -583,7 +583,6 @@ extern "C" int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_
 {
     if (!ctx || !W_r || !w_s || !shared_blobs || !xs || !ids || !w || !gate || !pool || !workspace || !err)
         return SMOE_EINVAL;
-    if (ctx->shape.bits != 4) return SMOE_ENOTSUP;   // the stack kernel takes 4-bit atoms
     if (n_layers < 1 || first_layer < 0 || first_layer + n_layers > ctx->n_layers) return SMOE_EINVAL;
     if (n_layers > kStackMaxLayers || !ctx->stack.ok) return SMOE_ENOTSUP;
     if (!aligned16(xs) || !aligned16(pool) || !aligned16(workspace)) return SMOE_EINVAL;
@@ -627,6 +626,7 @@ extern "C" int moe_decode_stack(const smoe_ctx *ctx, int32_t first_layer, int32_
     p.U = ctx->stack.U;
     p.nr = ctx->stack.nr;
     p.nu = ctx->stack.nu;
+    p.nslot = ctx->stack.nslot;
     return cuda_status(launch_stack(ctx, p, static_cast<cudaStream_t>(stream)));
 }
 

@@ -60,7 +60,8 @@ struct StackCfg {
     int grid = 0;             // CTAs (one per SM)
     int U = 0;                // experts per layer: k routed + the shared expert
     int nr = 0;               // most router rows of one CTA
-    int nu = 0;               // most gate/up units of one CTA
+    int nu = 0;               // most routed gate/up units of one CTA
+    int nslot = 0;            // most gate/up units (routed + shared) of one CTA: 8-bit ring slots
     int smem = 0;
 };
 
@@ -90,7 +91,7 @@ struct StackParams {
     int32_t *err;
     uint64_t wait_ns;                          // limit of a grid-wide wait
     int stall_layer;                           // test hook: this layer's first grid-wide wait never completes (-1: off)
-    int n_layers, H, E, k, I, U, nr, nu;
+    int n_layers, H, E, k, I, U, nr, nu, nslot;
 };
 
 }  // namespace smoe

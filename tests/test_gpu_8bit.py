@@ -3,8 +3,9 @@ layer, element by element: the fused decode kernel (T <= 8) at T = 1 and 8
 and the token-bucketed grouped GEMMs (T > 8) at T = 9 and 64 on the GPU's
 own routing, and at T = 600 with every token routed among 12 experts (three
 tiles per expert, the last one ragged); bit-identity across reruns and slot
-permutations, agreement with the plain CUDA path, and the calls that still
-take only 4-bit experts."""
+permutations, agreement with the plain CUDA path, the one-launch decode
+stack (moe_decode_stack) on 8-bit experts, and the call that still takes only
+4-bit experts."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +14,8 @@ import int4_routed_expert_router_gb300 as smoe
 import oracle_shards
 import synthetic
 import workload as W
-from test_gpu_parity import assert_output_close, gpu_forward, gpu_route, routing_ok
+from test_gpu_parity import assert_output_close, check_chain_layers_on_own_input, gpu_forward, gpu_route, routing_ok
+from test_gpu_stack import run_stack
 
 pytestmark = pytest.mark.gpu
 
@@ -101,6 +103,35 @@ def test_8bit_bucketed_multi_tile_experts(p80_8):
     assert np.array_equal(out, gpu_forward(pool, 1, x, ids, ref["w_used"], ref["gate"]))
 
 
+def test_8bit_stack_against_oracle_and_per_layer_path(p80_8):
+    """moe_decode_stack on 8-bit experts (two layers of the 80B shape): each
+    layer on its own input against the oracle's 8-bit combine of the GPU's
+    choice (the flat per-layer rule), routing bit-identical to moe_route on
+    that input, output within the layer tolerance of moe_forward's; a rerun
+    and a permuted slot placement give the same bits."""
+    pool, inp = p80_8
+    wl = pool.wl
+    x0 = synthetic.activations(wl.seed, 1, wl.H, tag=808)
+    xs, ids, w, gate, err = run_stack(pool, inp, x0)
+    assert smoe.check(err) == 0
+    xb = W.bits_of(xs)
+    idn, wn, gn = ids.cpu().numpy(), w.cpu().numpy(), gate.cpu().numpy()
+    check_chain_layers_on_own_input(wl, [0, 1], [xb[l:l + 1] for l in range(2)], [xb[l + 1:l + 2] for l in range(2)],
+                                    [idn[l:l + 1] for l in range(2)], [wn[l:l + 1] for l in range(2)],
+                                    [gn[l:l + 1] for l in range(2)], inp)
+    for l in range(2):
+        ids_r, w_r, gate_r = gpu_route(pool, inp, l, xb[l:l + 1])
+        assert np.array_equal(idn[l], ids_r[0]) and np.array_equal(wn[l], w_r[0])
+        assert np.array_equal(gn[l:l + 1], gate_r)
+        ref_fwd = gpu_forward(pool, l, xb[l:l + 1], ids_r, w_r, gate_r, residual=True)
+        assert_output_close(xb[l + 1:l + 2], synthetic.bf16_bits_to_f32(ref_fwd).astype(np.float64))
+    again = run_stack(pool, inp, x0)
+    perm = np.random.default_rng(23).permutation(2 * wl.E).astype(np.int32).reshape(2, wl.E)
+    other = run_stack(W.DevicePool(wl, n_layers=2, table=perm), inp, x0)
+    for a, b, c in zip((xs, ids, w, gate), again[:4], other[:4]):
+        assert torch.equal(a, b) and torch.equal(a, c)
+
+
 def test_8bit_calls_that_take_only_4bit_experts(p80_8):
     pool, inp = p80_8
     wl = pool.wl
@@ -114,4 +145,3 @@ def test_8bit_calls_that_take_only_4bit_experts(p80_8):
     with pytest.raises(smoe.SmoeError) as ei:
         smoe.moe_forward_noalloc(pool.ctx, 0, x, ids, w, gate, pool.pool, pool.shared[0], out, err)
     assert ei.value.status == smoe.ENOTSUP
-    assert pool.ctx.stack_workspace_bytes(2) == 0
