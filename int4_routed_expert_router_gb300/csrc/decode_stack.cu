@@ -101,7 +101,7 @@ __host__ __device__ inline StkSmem stk_smem(int H, int E, int I, int U, int nr, 
         L.yd = o;    o = align128(o + U * ngI * 16 * 4);
     }
     L.ysum = o;  o = align128(o + U * 16 * 4);
-    L.mx = o;    o = align128(o + 2 * kStkWarps * 4);
+    L.mx = o;    o = align128(o + 2 * kStkWarps * 4 + 8);
     L.cand = o;  o = align128(o + 2 * E * 4);
     L.sel = o;   o = align128(o + 2 * 16 * 4);
     L.ints = o;  o = align128(o + 64 * 4);
@@ -452,9 +452,9 @@ __device__ __forceinline__ bool key_before(uint32_t ka, int32_t ia, uint32_t kb,
 // candidates (ties: the lower id first, a strict order); a candidate's rank
 // among the candidates is its place in route order. The same selection as
 // route_common.cuh's, so the ids are moe_route's. ncand must be zero on entry
-// and is zero again on return. Three CTA barriers.
-__device__ void block_topk(float z, const float *bias, int E, int k, uint32_t *mx_k, int32_t *mx_i, uint32_t *cand_k,
-                           int32_t *cand_i, int *ncand, uint32_t *sel_k, int32_t *sel_i)
+// and is zero again on return. thr: two words of scratch. Four CTA barriers.
+__device__ void block_topk(float z, const float *bias, int E, int k, uint32_t *mx_k, int32_t *mx_i, uint32_t *thr,
+                           uint32_t *cand_k, int32_t *cand_i, int *ncand, uint32_t *sel_k, int32_t *sel_i)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t key = tid < E ? fkey(z + (bias ? bias[tid] : 0.f)) : 0u;
@@ -466,16 +466,27 @@ __device__ void block_topk(float z, const float *bias, int E, int k, uint32_t *m
         mx_i[warp] = mi;
     }
     __syncthreads();
-    const int j = lane & (kStkWarps - 1);
-    const uint32_t jk = mx_k[j];
-    const int32_t ji = mx_i[j];
-    int r = 0;
+    // warp 0 finds the bound (each warp doing it was 16 times the issued work
+    // for one more barrier's worth of time) and passes it through thr
+    if (warp == 0) {
+        const int j = lane & (kStkWarps - 1);
+        const uint32_t jk = mx_k[j];
+        const int32_t ji = mx_i[j];
+        int r = 0;
 #pragma unroll
-    for (int i = 0; i < kStkWarps; ++i) r += key_before(mx_k[i], mx_i[i], jk, ji);
-    const uint32_t b = __ballot_sync(0xffffffffu, lane < kStkWarps && r == k - 1);
-    const int src = b ? __ffs(b) - 1 : 0;
-    const uint32_t tk = b ? __shfl_sync(0xffffffffu, jk, src) : 0u;       // no such rank: every key qualifies
-    const int32_t ti = b ? __shfl_sync(0xffffffffu, ji, src) : 0x7fffffff;
+        for (int i = 0; i < kStkWarps; ++i) r += key_before(mx_k[i], mx_i[i], jk, ji);
+        const uint32_t b = __ballot_sync(0xffffffffu, lane < kStkWarps && r == k - 1);
+        const int src = b ? __ffs(b) - 1 : 0;
+        const uint32_t tk0 = b ? __shfl_sync(0xffffffffu, jk, src) : 0u;   // no such rank: every key qualifies
+        const int32_t ti0 = b ? __shfl_sync(0xffffffffu, ji, src) : 0x7fffffff;
+        if (lane == 0) {
+            thr[0] = tk0;
+            thr[1] = uint32_t(ti0);
+        }
+    }
+    __syncthreads();
+    const uint32_t tk = thr[0];
+    const int32_t ti = int32_t(thr[1]);
     const bool cand = key != 0u && !key_before(tk, ti, key, id);
     const uint32_t cb = __ballot_sync(0xffffffffu, cand);
     int base = 0;
@@ -533,6 +544,7 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
     float *ysum = reinterpret_cast<float *>(smem + L.ysum);          // [U][16 rows]
     uint32_t *mx_k = reinterpret_cast<uint32_t *>(smem + L.mx);      // [16] slice maxima
     int32_t *mx_i = reinterpret_cast<int32_t *>(mx_k + kStkWarps);
+    uint32_t *thr = mx_k + 2 * kStkWarps;                            // [2] the top-k's bound
     uint32_t *cand_k = reinterpret_cast<uint32_t *>(smem + L.cand);  // [E] candidates
     int32_t *cand_i = reinterpret_cast<int32_t *>(cand_k + E);
     uint32_t *sel_k = reinterpret_cast<uint32_t *>(smem + L.sel);    // [16] chosen keys, route order
@@ -680,7 +692,8 @@ __global__ void __launch_bounds__(kStkThreads, 1) decode_stack_kernel(const __gr
                 *gate_s = shared_gate(__uint_as_float(zv[1]));
                 if (c == 0) p.gate[l] = *gate_s;
             }
-            block_topk(__uint_as_float(zv[0]), p.bias, E, k, mx_k, mx_i, cand_k, cand_i, ncand, sel_k, ids_s);
+            block_topk(__uint_as_float(zv[0]), p.bias, E, k, mx_k, mx_i, thr, cand_k, cand_i, ncand, sel_k,
+                       ids_s);
             if (warp == kStkWarps - 1) {                             // weights: needed only by the combine
                 const float wl = choice_weight(sel_k, k, lane);
                 if (lane < k) {
