@@ -10,7 +10,7 @@ import int4_routed_expert_router_gb300 as smoe
 import oracle
 import synthetic
 import workload as W
-from test_gpu_parity import assert_output_close, gpu_forward, oracle_layer
+from test_gpu_parity import assert_output_close, gpu_forward, oracle_layer, routing_ok
 
 pytestmark = pytest.mark.gpu
 
@@ -62,9 +62,8 @@ def test_debug_path_matches_oracle_and_fast_kernels(name, Ts):
 
 def test_debug_path_8_bit_experts_match_oracle():
     """8-bit experts (two-plane atoms, packed on the host) through the plain
-    CUDA path and the fused decode kernel, against the oracle's 8-bit layer
-    on the same routing; moe_forward_noalloc and the stack refuse an 8-bit
-    context."""
+    CUDA path, the fused decode kernel and the one-launch stack, against the
+    oracle's 8-bit layer; moe_forward_noalloc refuses an 8-bit context."""
     wl = synthetic.WORKLOADS["tiny"]
     shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I, bits=8)
     stride = smoe.layout_of(shape).blob_bytes
@@ -101,7 +100,26 @@ def test_debug_path_8_bit_experts_match_oracle():
         smoe.moe_forward_noalloc(ctx, 0, W.bf16_tensor(x), dev(ids, np.int32), dev(w, np.float32),
                                  dev(gate, np.float32), pool, shared, out, err)
     assert ei.value.status == smoe.ENOTSUP
-    assert ctx.stack_workspace_bytes(1) == 0
+    # the stack on the same layer: its own routing (moe_route's rule) and x + the layer
+    nb = ctx.stack_workspace_bytes(1)
+    assert nb > 0
+    x1 = synthetic.activations(wl.seed, 1, wl.H, tag=997)
+    xs = torch.zeros((2, wl.H), dtype=torch.bfloat16, device="cuda")
+    xs[0].copy_(W.bf16_tensor(x1)[0])
+    sid = torch.zeros((1, wl.k), dtype=torch.int32, device="cuda")
+    sw = torch.zeros((1, wl.k), dtype=torch.float32, device="cuda")
+    sg = torch.zeros((1,), dtype=torch.float32, device="cuda")
+    ws = torch.zeros((nb + 15) // 16 * 16, dtype=torch.uint8, device="cuda")
+    smoe.moe_decode_stack(ctx, 0, [inp.Wr[0]], [inp.ws[0]], [shared], xs, sid, sw, sg, pool, ws, err)
+    torch.cuda.synchronize()
+    assert smoe.check(err) == 0
+    r = oracle.route(x1, inp.Wr_bits[0], inp.ws_bits[0], wl.k, want_probs=True)
+    gids = sid.cpu().numpy()
+    w_own = routing_ok(gids, sw.cpu().numpy(), sg.cpu().numpy(), dict(ids=r[0], probs=r[3], gate=r[2]), wl.k)
+    ref1, _ = oracle.combine8(x1, gids, w_own, r[2], {int(e): trip[int(e)] for e in np.unique(gids)}, shared_t,
+                              wl.E, wl.I, wl.I)
+    xr = synthetic.bf16_bits_to_f32(x1).astype(np.float64)
+    assert_output_close(W.bits_of(xs[1:2]), xr + ref1)
 
 
 def test_debug_path_bad_slot_sets_error_word():
