@@ -166,10 +166,10 @@ typedef struct smoe_ctx smoe_ctx;
  * of n_layers layers and a pool of n_slots slots. table_dev is caller-owned
  * device memory of n_layers*E int32 (the slot table; filled by
  * set_slot_table). The context allocates no device memory. A context of
- * 8-bit experts (shape.bits = 8) serves moe_route, moe_forward (the T <= 8
- * kernel and the bucketed expert GEMMs both read the two nibble planes),
- * moe_decode_stack and moe_forward_debug; moe_forward_noalloc returns
- * SMOE_ENOTSUP for it (its kernel reads 4-bit atoms).
+ * 8-bit experts (shape.bits = 8) serves every call (the T <= 8 kernel, the
+ * bucketed expert GEMMs and the stack kernel all read the two nibble
+ * planes); a shape whose 8-bit T <= 8 kernel does not fit the GPU makes
+ * moe_forward (T <= 8) and moe_forward_noalloc return SMOE_ENOTSUP.
  * Errors: SMOE_EINVAL, SMOE_ENOTSUP, SMOE_ECUDA. */
 SMOE_API int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_t n_slots,
                     int32_t *table_dev, smoe_ctx **out);

@@ -56,7 +56,7 @@ extern "C" int moe_forward_noalloc(const smoe_ctx *ctx, int32_t layer, const uin
 {
     if (!ctx || T < 0) return SMOE_EINVAL;
     if (layer < 0 || layer >= ctx->n_layers) return SMOE_EINVAL;
-    if (ctx->shape.bits != 4) return SMOE_ENOTSUP;   // the decode kernel takes 4-bit atoms
+    if (!ctx->decode_ok) return SMOE_ENOTSUP;        // no T <= 8 kernel for this shape's atoms
     if (T == 0) return SMOE_OK;                      // nothing to do; the buffers may be null
     if (!x || !ids || !w || !gate || !pool || !shared_blob || !out || !err) return SMOE_EINVAL;
     if (T > kDecodeMaxT) return SMOE_ENOTSUP;

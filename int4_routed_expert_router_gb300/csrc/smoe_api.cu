@@ -264,8 +264,7 @@ Workspace workspace_layout(const smoe_shape &s, int T)
 }  // namespace smoe
 
 // ====================================================================== C ABI
-// allow8: the 8-bit format is accepted (layout, packing, the context for
-// routing and the plain debug path; the fast expert kernels refuse it)
+// allow8: the 8-bit format is accepted (layout, packing and contexts)
 static int shape_check(const smoe_shape *s, bool allow8 = false)
 {
     if (!s) return SMOE_EINVAL;
@@ -339,7 +338,7 @@ extern "C" int pack_experts(const smoe_shape *shape, const smoe_expert_src *src,
 extern "C" int smoe_ctx_create(const smoe_shape *shape, int32_t n_layers, int64_t n_slots, int32_t *table_dev,
                                smoe_ctx **out)
 {
-    int rc = shape_check(shape, true);            // 8-bit: routing and the plain debug path only
+    int rc = shape_check(shape, true);
     if (rc) return rc;
     if (!out || n_layers <= 0 || n_slots <= 0 || !table_dev) return SMOE_EINVAL;
     *out = nullptr;

@@ -3,9 +3,9 @@ layer, element by element: the fused decode kernel (T <= 8) at T = 1 and 8
 and the token-bucketed grouped GEMMs (T > 8) at T = 9 and 64 on the GPU's
 own routing, and at T = 600 with every token routed among 12 experts (three
 tiles per expert, the last one ragged); bit-identity across reruns and slot
-permutations, agreement with the plain CUDA path, the one-launch decode
-stack (moe_decode_stack) on 8-bit experts, and the call that still takes only
-4-bit experts."""
+permutations, agreement with the plain CUDA path, and the one-launch decode
+stack (moe_decode_stack) on 8-bit experts (moe_forward_noalloc on 8-bit
+experts: test_zz_no_alloc.py)."""
 import numpy as np
 import pytest
 import torch
@@ -130,18 +130,3 @@ def test_8bit_stack_against_oracle_and_per_layer_path(p80_8):
     other = run_stack(W.DevicePool(wl, n_layers=2, table=perm), inp, x0)
     for a, b, c in zip((xs, ids, w, gate), again[:4], other[:4]):
         assert torch.equal(a, b) and torch.equal(a, c)
-
-
-def test_8bit_calls_that_take_only_4bit_experts(p80_8):
-    pool, inp = p80_8
-    wl = pool.wl
-    T = 2
-    x = W.bf16_tensor(synthetic.activations(wl.seed, T, wl.H, tag=5))
-    ids = torch.zeros((T, wl.k), dtype=torch.int32, device="cuda")
-    w = torch.zeros((T, wl.k), dtype=torch.float32, device="cuda")
-    gate = torch.zeros((T,), dtype=torch.float32, device="cuda")
-    out = torch.zeros((T, wl.H), dtype=torch.bfloat16, device="cuda")
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    with pytest.raises(smoe.SmoeError) as ei:
-        smoe.moe_forward_noalloc(pool.ctx, 0, x, ids, w, gate, pool.pool, pool.shared[0], out, err)
-    assert ei.value.status == smoe.ENOTSUP

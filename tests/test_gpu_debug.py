@@ -62,8 +62,8 @@ def test_debug_path_matches_oracle_and_fast_kernels(name, Ts):
 
 def test_debug_path_8_bit_experts_match_oracle():
     """8-bit experts (two-plane atoms, packed on the host) through the plain
-    CUDA path, the fused decode kernel and the one-launch stack, against the
-    oracle's 8-bit layer; moe_forward_noalloc refuses an 8-bit context."""
+    CUDA path, the fused decode kernel (moe_forward and moe_forward_noalloc)
+    and the one-launch stack, against the oracle's 8-bit layer."""
     wl = synthetic.WORKLOADS["tiny"]
     shape = smoe.make_shape(wl.H, wl.E, wl.k, wl.I, bits=8)
     stride = smoe.layout_of(shape).blob_bytes
@@ -96,10 +96,12 @@ def test_debug_path_8_bit_experts_match_oracle():
                      pool, shared, fast, W.workspace(ctx, T), err)
     assert smoe.check(err) == 0
     assert_output_close(W.bits_of(fast), ref)
-    with pytest.raises(smoe.SmoeError) as ei:
-        smoe.moe_forward_noalloc(ctx, 0, W.bf16_tensor(x), dev(ids, np.int32), dev(w, np.float32),
-                                 dev(gate, np.float32), pool, shared, out, err)
-    assert ei.value.status == smoe.ENOTSUP
+    # moe_forward_noalloc runs the same kernel: the same bits
+    na = torch.zeros((T, wl.H), dtype=torch.bfloat16, device="cuda")
+    smoe.moe_forward_noalloc(ctx, 0, W.bf16_tensor(x), dev(ids, np.int32), dev(w, np.float32),
+                             dev(gate, np.float32), pool, shared, na, err)
+    assert smoe.check(err) == 0
+    assert torch.equal(na, fast)
     # the stack on the same layer: its own routing (moe_route's rule) and x + the layer
     nb = ctx.stack_workspace_bytes(1)
     assert nb > 0

@@ -35,7 +35,8 @@ def _inputs(pool, inp, T, tag):
     return W.bf16_tensor(x_bits), dev(r[0], np.int32), dev(r[1], np.float32), dev(r[2], np.float32)
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 4), ("decode80b", 1), ("decode80b", 8)])
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("decode80b", 1), ("decode80b", 8), ("decode80b_int8", 1),
+                                    ("decode80b_int8", 8)])
 def test_noalloc_matches_moe_forward_twice(name, T):
     wl = synthetic.WORKLOADS[name]
     pool = W.DevicePool(wl, n_layers=1)
