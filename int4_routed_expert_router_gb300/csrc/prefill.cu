@@ -53,33 +53,48 @@ constexpr int kPfSmem = kPfAB * kPfStageBytes + 1024 /*align*/ + 512 /*barriers*
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
 
 // Expert GEMMs (gate/up, down): A (the dequantised weights) lives in tensor
-// memory. TMEM columns: two accumulators of kXMaxN columns, then kXStg A
-// stages of 32 columns (128 rows x 64 fp16 K values). Shared memory holds only
-// the B stages and the raw atoms.
-constexpr int kXMaxN = 192;        // tokens per expert tile
+// memory. TMEM columns: two accumulators of MaxN columns, then Stg A stages of
+// 32 columns (128 rows x 64 fp16 K values). Shared memory holds only the B
+// stages and the raw atoms.
+constexpr int kXMaxN = 192;        // tokens per expert tile (the bucketing's bound)
 constexpr int kXRaw = 16;          // raw atom slots
-constexpr int kXStg = 4;           // operand stages: A in TMEM + B in shared memory, one barrier pair each
 constexpr int kXAcc = 2;           // accumulator buffers in TMEM (the epilogue of a tile overlaps the next)
-constexpr int kXBBytes = kXMaxN * kPfK * 2;                 // 24 KiB
-constexpr uint32_t kXACol0 = kXAcc * kXMaxN;                // first A column
+constexpr int kXGatherW0 = 19;     // gate/up: warps 19 .. 22 gather the B rows (cp.async)
+constexpr int kXGatherWarps = 4;
+constexpr int kXThreads = (kXGatherW0 + kXGatherWarps) * 32;
+
+// Ring shape of the expert GEMMs: MAXN tokens per tile (the accumulators' and
+// B stages' width), STG operand stages (A in TMEM and B in shared memory, one
+// barrier pair each), GDEPTH K steps a gather thread keeps in flight past the
+// one it signals (at most STG - 2, or the gather and the MMAs take turns).
+// Wide takes any tile. Narrow serves T <= kXNarrowT, where a tile holds at most
+// T tokens: its narrower accumulators leave tensor memory for 8 stages, so the
+// gathered rows (about a microsecond from request to landing) are asked for 6
+// steps ahead instead of 2.
+template <int MAXN, int STG, int GDEPTH>
+struct XCfg {
+    static constexpr int MaxN = MAXN, Stg = STG, GDepth = GDEPTH;
+    static constexpr int BBytes = MAXN * kPfK * 2;                   // one B stage
+    static constexpr uint32_t ACol0 = kXAcc * MAXN;                  // first A column
+    static constexpr int GRows = MAXN / (kXGatherWarps * 32 / 8);    // rows per gather thread per K step
+    static_assert(ACol0 + STG * 32 <= 512, "TMEM columns");
+    static_assert(GDEPTH <= STG - 2 && MAXN % 64 == 0, "ring shape");
+};
+using XWide = XCfg<kXMaxN, 4, 2>;
+using XNarrow = XCfg<64, 8, 6>;
+constexpr int kXNarrowT = 64;
 
 // The raw-atom ring of the expert GEMMs for BITS-bit experts: bytes per atom,
 // slots, bytes per K step (8 atoms), and the CTA's shared memory.
-template <int BITS>
+template <int BITS, typename CFG>
 struct XRaw {
     static constexpr int AB = BITS == 8 ? kAtom8Bytes : kAtomBytes;
     static constexpr int Slots = BITS == 8 ? 12 : kXRaw;
     static constexpr int Step = 8 * AB;
-    static constexpr int Smem = kXStg * kXBBytes + Slots * Step + 1024 /*align*/ + 512 /*barriers*/;
+    static constexpr int Smem = CFG::Stg * CFG::BBytes + Slots * Step + 1024 /*align*/ + 1024 /*barriers*/;
 };
-static_assert(XRaw<8>::Smem <= 232448, "shared memory per CTA");
-static_assert(XRaw<4>::Smem <= 232448, "shared memory per CTA");
-static_assert(kXACol0 + kXStg * 32 <= 512, "TMEM columns");
-constexpr int kXGatherW0 = 19;     // gate/up: warps 19 .. 22 gather the B rows (cp.async)
-constexpr int kXGatherWarps = 4;
-constexpr int kXThreads = (kXGatherW0 + kXGatherWarps) * 32;
-constexpr int kXGRows = kXMaxN / (kXGatherWarps * 32 / 8);   // rows per gather thread per K step (12)
-constexpr int kXGDepth = 2;        // K steps a gather thread keeps in flight past the one it signals
+static_assert(XRaw<8, XWide>::Smem <= 232448 && XRaw<4, XWide>::Smem <= 232448, "shared memory per CTA");
+static_assert(XRaw<8, XNarrow>::Smem <= 232448 && XRaw<4, XNarrow>::Smem <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t sw128(int r, int c)   // byte offset of (row, col) in a 64-col bf16 tile
 {
@@ -761,7 +776,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmPa
 // h in the down GEMM's K order) share a 4-byte store.
 // Down: 12 warps, 3 per quadrant, chunks of 32 tokens; each pair's fp16
 // output, two rows per 4-byte store (neighbouring lanes swap halves).
-template <typename TileOf>
+template <int MAXN, typename TileOf>
 __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uint64_t *accfull, uint64_t *accempty,
                                          volatile int *abort, int warp, int lane, int my_tiles, TileOf tile_of)
 {
@@ -787,7 +802,7 @@ __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uin
             const uint32_t sel = godd ? 0x3276u : 0x5410u;
             for (int cc = 0; 64 * cc < ti.N; ++cc) {                    // uniform over the warp
                 uint32_t v[32];
-                tmem_ld16x256x8(tmem + (uint32_t(32 * q + 16 * h) << 16) + uint32_t(b * kXMaxN + 64 * cc), v);
+                tmem_ld16x256x8(tmem + (uint32_t(32 * q + 16 * h) << 16) + uint32_t(b * MAXN + 64 * cc), v);
                 const int c0 = 64 * cc + 2 * t + godd;                  // this thread's token, + 8 r
                 uint32_t *hp = reinterpret_cast<uint32_t *>(p.hbuf + size_t(ti.rowbase + c0) * p.I + hcol);
 #pragma unroll
@@ -813,7 +828,7 @@ __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uin
             const uint32_t sel = odd ? 0x3276u : 0x5410u;
             for (int j = h; 32 * j < ti.N; j += 3) {                    // uniform over the warp
                 uint32_t v[32];
-                tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(b * kXMaxN + 32 * j), v);
+                tmem_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(b * MAXN + 32 * j), v);
                 uint32_t *y = reinterpret_cast<uint32_t *>(p.ypair + size_t(ti.rowbase + 32 * j + odd) * p.H + R0);
                 const int nc = ti.n - 32 * j - odd;                     // stored when 2 m < nc
 #pragma unroll
@@ -846,8 +861,8 @@ __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uin
 // may access); warps 8-15 run the epilogue; warp 16 streams the raw atoms;
 // warp 17 loads B with TMA in the down GEMM; warp 18 issues the MMAs; warps
 // 19-22 gather B rows by token in the gate/up GEMM and join the epilogue in
-// the down GEMM. A and B of a K step share one stage of a 4-deep ring.
-template <int BITS>
+// the down GEMM. A and B of a K step share one stage of a CFG::Stg-deep ring.
+template <int BITS, typename CFG>
 __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmParams p,
                                                                     const __grid_constant__ CUtensorMap bmap,
                                                                     const __grid_constant__ CUtensorMap amap,
@@ -857,15 +872,15 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     pdl_trigger();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *bst = smem;                                          // kXStg x 24 KiB, 128-byte swizzled rows
-    using RW = XRaw<BITS>;
-    uint8_t *raw = smem + kXStg * kXBBytes;                       // RW::Slots x RW::Step bytes
+    uint8_t *bst = smem;                                          // CFG::Stg x 24 KiB, 128-byte swizzled rows
+    using RW = XRaw<BITS, CFG>;
+    uint8_t *raw = smem + CFG::Stg * CFG::BBytes;                       // RW::Slots x RW::Step bytes
     uint64_t *bars = reinterpret_cast<uint64_t *>(raw + RW::Slots * RW::Step);
     uint64_t *rawfull = bars, *rawempty = bars + RW::Slots;
-    uint64_t *full = bars + 2 * RW::Slots, *empty = full + kXStg;     // stage s: A (TMEM) + B (smem)
-    uint64_t *accfull = empty + kXStg, *accempty = accfull + kXAcc;
+    uint64_t *full = bars + 2 * RW::Slots, *empty = full + CFG::Stg;     // stage s: A (TMEM) + B (smem)
+    uint64_t *accfull = empty + CFG::Stg, *accempty = accfull + kXAcc;
     uint64_t *bfull = accempty + kXAcc;                           // down: B copies of stage s (TMA)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bfull + kXStg);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bfull + CFG::Stg);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -881,7 +896,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             mbar_init(&rawfull[r], 1);
             mbar_init(&rawempty[r], kPfWorkers);
         }
-        for (int s = 0; s < kXStg; ++s) {
+        for (int s = 0; s < CFG::Stg; ++s) {
             // the A threads, plus in gate/up the 128 gathering threads (the down
             // GEMM's B copies complete on bfull instead)
             mbar_init(&full[s], kPfWorkers * 32 + (p.mode == 0 ? kXGatherWarps * 32 : 0));
@@ -910,7 +925,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     // epilogue warps: 8..15, and in the down GEMM also the gather warps (idle there)
     const bool epi_role = (warp >= kPfWorkers && warp < kPfWorkers + kPfEpi) || (p.mode == 1 && warp >= kXGatherW0);
     if (epi_role) {
-        epilogue(p, tmem, accfull, accempty, abort, warp, lane, my_tiles, tile_of);
+        epilogue<CFG::MaxN>(p, tmem, accfull, accempty, abort, warp, lane, my_tiles, tile_of);
     } else if (warp == kPfRawWarp) {
         // ---- raw atoms (8 row blocks x one group) per K step: one TMA box each
         if (lane == 0) {
@@ -946,14 +961,14 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             // ---- B (gate/up): the tile's N token rows of xt, one 16-byte chunk per
             // thread and row: thread g takes chunk g % 8 of rows g / 8 + 16 u. Rows
             // n .. N - 1 repeat row n - 1 (their accumulator columns are never
-            // stored). A step is signalled once its copies have landed, kXGDepth
+            // stored). A step is signalled once its copies have landed, CFG::GDepth
             // steps later (cp.async groups), after a proxy fence for the MMA.
             const int gt = tid - kXGatherW0 * 32, c8 = gt & 7, r0 = gt >> 3;
             // byte offsets: source row u = token row start + chunk; destination row
             // r0 + 16 u = sw128(r0, 8 c8) + 2048 u (16 u keeps the row's swizzle phase)
-            auto rows_of = [&](const TileInfo &t, uint32_t (&off)[kXGRows]) {
+            auto rows_of = [&](const TileInfo &t, uint32_t (&off)[CFG::GRows]) {
 #pragma unroll
-                for (int u = 0; u < kXGRows; ++u) {
+                for (int u = 0; u < CFG::GRows; ++u) {
                     const int rr = min(r0 + 16 * u, t.n - 1);
                     const int tok = t.kind == 1 ? t.p0 + rr : p.pair_token[t.p0 + rr];
                     off[u] = uint32_t(tok) * uint32_t(2 * p.H) + uint32_t(16 * c8);   // < 2^32: T <= SMOE_MAX_TOKENS, H <= 2048
@@ -961,7 +976,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             };
             const char *xt = reinterpret_cast<const char *>(p.x);
             const uint32_t dst0 = smem_u32(bst) + sw128(r0, 8 * c8);
-            uint32_t cur[kXGRows], nxt[kXGRows];
+            uint32_t cur[CFG::GRows], nxt[CFG::GRows];
             TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
             rows_of(tnext, nxt);
             int sb = 0, sd = 0, issued = 0;
@@ -969,7 +984,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             for (int i = 0; i < my_tiles; ++i) {
                 const TileInfo ti = tnext;
 #pragma unroll
-                for (int u = 0; u < kXGRows; ++u) cur[u] = nxt[u];
+                for (int u = 0; u < CFG::GRows; ++u) cur[u] = nxt[u];
                 if (i + 1 < my_tiles) {
                     tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
                     rows_of(tnext, nxt);
@@ -977,26 +992,26 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                 const int urows = (ti.N - r0 + 15) / 16;              // rows r0 + 16 u < N
                 for (int kb = 0; kb < nk; ++kb) {
                     pf_wait(&empty[sb], ph ^ 1u, p.err, abort);
-                    const uint32_t dst = dst0 + uint32_t(sb * kXBBytes);
+                    const uint32_t dst = dst0 + uint32_t(sb * CFG::BBytes);
                     const char *src = xt + kb * (kPfK * 2);
 #pragma unroll
-                    for (int u = 0; u < kXGRows; ++u)
+                    for (int u = 0; u < CFG::GRows; ++u)
                         if (u < urows) cp_async16(dst + uint32_t(2048 * u), src + cur[u], 16u);
                     asm volatile("cp.async.commit_group;" ::: "memory");
-                    if (++sb == kXStg) { sb = 0; ph ^= 1u; }
-                    if (++issued > kXGDepth) {
-                        asm volatile("cp.async.wait_group %0;" ::"n"(kXGDepth) : "memory");
+                    if (++sb == CFG::Stg) { sb = 0; ph ^= 1u; }
+                    if (++issued > CFG::GDepth) {
+                        asm volatile("cp.async.wait_group %0;" ::"n"(CFG::GDepth) : "memory");
                         fence_async_smem();
                         mbar_arrive(&full[sd]);
-                        if (++sd == kXStg) sd = 0;
+                        if (++sd == CFG::Stg) sd = 0;
                     }
                 }
             }
             asm volatile("cp.async.wait_group 0;" ::: "memory");
             fence_async_smem();
-            for (int j = 0; j < min(issued, kXGDepth); ++j) {
+            for (int j = 0; j < min(issued, CFG::GDepth); ++j) {
                 mbar_arrive(&full[sd]);
-                if (++sd == kXStg) sd = 0;
+                if (++sd == CFG::Stg) sd = 0;
             }
         }
     } else if (warp == kPfBWarp) {
@@ -1013,20 +1028,20 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!pf_wait(&empty[sb], ph ^ 1u, p.err, abort)) { ok = false; break; }
                     mbar_arrive_expect_tx(&bfull[sb], bytes);
-                    const uint32_t dst = smem_u32(bst + sb * kXBBytes);
+                    const uint32_t dst = smem_u32(bst + sb * CFG::BBytes);
                     for (int j = 0; j < nbox; ++j)
                         tma_load_2d(dst + j * (kPfBoxRows * kPfK * 2), &bmap, kb * kPfK, ti.rowbase + j * kPfBoxRows,
                                     &bfull[sb]);
                     ++issued;
-                    if (++sb == kXStg) { sb = 0; ph ^= 1u; }
+                    if (++sb == CFG::Stg) { sb = 0; ph ^= 1u; }
                 }
             }
             // the last copy into each stage lands before the CTA can exit (also after an abort)
-            for (int g2 = issued - 1; g2 >= 0 && g2 >= issued - kXStg; --g2)
-                mbar_wait(&bfull[g2 % kXStg], (g2 / kXStg) & 1, p.err);
+            for (int g2 = issued - 1; g2 >= 0 && g2 >= issued - CFG::Stg; --g2)
+                mbar_wait(&bfull[g2 % CFG::Stg], (g2 / CFG::Stg) & 1, p.err);
         }
     } else if (warp == kPfMma) {
-        // ---- MMA issuer: tile i accumulates in TMEM columns (i % 2) * kXMaxN ..
+        // ---- MMA issuer: tile i accumulates in TMEM columns (i % 2) * MaxN ..
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0;
@@ -1037,19 +1052,19 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                 if (i + 1 < my_tiles) nextN = tile_info(p, tile_of(i + 1) / p.m_tiles).N;   // used one tile later
                 pf_wait(&accempty[b], ((i / kXAcc) & 1) ^ 1u, p.err, abort);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t acc_t = tmem + uint32_t(b * kXMaxN);
+                const uint32_t acc_t = tmem + uint32_t(b * CFG::MaxN);
                 for (int kb = 0; kb < nk; ++kb) {
                     pf_wait_fast(&full[s], ph, p.err, abort);
                     if (p.mode == 1) pf_wait_fast(&bfull[s], ph, p.err, abort);
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint64_t bd = umma_desc(smem_u32(bst + s * kXBBytes));
-                    const uint32_t a_t = tmem + kXACol0 + uint32_t(32 * s);
+                    const uint64_t bd = umma_desc(smem_u32(bst + s * CFG::BBytes));
+                    const uint32_t a_t = tmem + CFG::ACol0 + uint32_t(32 * s);
                     umma_ts(acc_t, a_t, bd, idesc, kb ? 1u : 0u);
 #pragma unroll
                     for (int k4 = 1; k4 < kPfK / 16; ++k4)
                         umma_ts(acc_t, a_t + uint32_t(8 * k4), bd + uint64_t(k4 * 2), idesc, 1u);
                     umma_commit(&empty[s]);
-                    if (++s == kXStg) { s = 0; ph ^= 1u; }
+                    if (++s == CFG::Stg) { s = 0; ph ^= 1u; }
                 }
                 umma_commit(&accfull[b]);
             }
@@ -1095,11 +1110,11 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                 }
             }
             pf_wait(&empty[sa], pha ^ 1u, p.err, abort);
-            tmem_st16x256x4(tmem + lane_base + kXACol0 + uint32_t(32 * sa), v);
+            tmem_st16x256x4(tmem + lane_base + CFG::ACol0 + uint32_t(32 * sa), v);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&full[sa]);
-            if (++sa == kXStg) { sa = 0; pha ^= 1u; }
+            if (++sa == CFG::Stg) { sa = 0; pha ^= 1u; }
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -1148,9 +1163,17 @@ cudaError_t prefill_config()
 {
     cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(expert_gemm_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, XRaw<4>::Smem);
+        e = cudaFuncSetAttribute(expert_gemm_kernel<4, XWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 XRaw<4, XWide>::Smem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(expert_gemm_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, XRaw<8>::Smem);
+        e = cudaFuncSetAttribute(expert_gemm_kernel<8, XWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 XRaw<8, XWide>::Smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(expert_gemm_kernel<4, XNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 XRaw<4, XNarrow>::Smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(expert_gemm_kernel<8, XNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 XRaw<8, XNarrow>::Smem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bucket_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  bucket_small_smem(1024));
@@ -1295,8 +1318,12 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
     g.mode = 0;
     g.m_tiles = g.I / 64;
     if ((e = prof_record(nprof > 0 ? prof[0] : nullptr, st)) != cudaSuccess) return e;
-    auto kern = b8 ? expert_gemm_kernel<8> : expert_gemm_kernel<4>;
-    const int xsmem = b8 ? XRaw<8>::Smem : XRaw<4>::Smem;
+    // T <= kXNarrowT: every tile holds at most T tokens, so the narrow ring shape fits
+    const bool narrow = p.T <= kXNarrowT;
+    auto kern = narrow ? (b8 ? expert_gemm_kernel<8, XNarrow> : expert_gemm_kernel<4, XNarrow>)
+                       : (b8 ? expert_gemm_kernel<8, XWide> : expert_gemm_kernel<4, XWide>);
+    const int xsmem = narrow ? (b8 ? XRaw<8, XNarrow>::Smem : XRaw<4, XNarrow>::Smem)
+                             : (b8 ? XRaw<8, XWide>::Smem : XRaw<4, XWide>::Smem);
     if ((e = launch_pdl(kern, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), xsmem, st, g, xmap, gu_pool,
                         gu_shared)) != cudaSuccess)
         return e;
