@@ -156,9 +156,9 @@ def _stream(stream) -> int | None:
 
 
 def make_shape(H, E, k, I, I_shared=None, bits=4) -> Shape:
-    """bits = 8: MLX's 8-bit format, for the layout, host and device packing,
-    routing, moe_forward with T <= 8 and moe_forward_debug; moe_forward with
-    T > 8, moe_forward_noalloc and moe_decode_stack return ENOTSUP for it."""
+    """bits = 8: MLX's 8-bit format (two-plane atoms), taken by every call:
+    layout, host and device packing, routing, moe_forward at any T,
+    moe_forward_noalloc, moe_decode_stack and moe_forward_debug."""
     return Shape(H, E, k, I, I if I_shared is None else I_shared, 64, bits)
 
 
