@@ -45,6 +45,22 @@ def test_prefill_tiny_against_oracle(tiny, T):
     assert_output_close(out2, xr + ref["out64"])
 
 
+@pytest.mark.parametrize("name", ["tiny", "zipf80b_t64"])
+def test_prefill_t64_full_width_tiles(name):
+    """T = 64 with every token routed to the same k experts: each of them gets
+    a full 64-token tile, the widest the T <= 64 ring shape takes (the
+    weights are the oracle's probabilities renormalised over that choice)."""
+    wl = synthetic.WORKLOADS[name]
+    pool, inp = W.DevicePool(wl, n_layers=1), W.LayerInputs(wl, 1)
+    T = 64
+    x = synthetic.activations(wl.seed, T, wl.H, tag=6464)
+    hot = np.random.default_rng(64).choice(wl.E, wl.k, replace=False).astype(np.int32)
+    ids = np.stack([np.random.default_rng(t).permutation(hot) for t in range(T)]).astype(np.int32)
+    ref = oracle_shards.tokens_sharded(wl.name, 0, x, ids, inp.Wr_bits[0], inp.ws_bits[0])
+    out = gpu_forward(pool, 0, x, ids, ref["w_used"], ref["gate"])
+    assert_output_close(out, ref["out64"])
+
+
 def test_prefill_zipf_t64_full_layer():
     """The skewed T = 64 layer through moe_route and moe_forward on the GPU's
     own routing: every token's routing and output against the oracle's
