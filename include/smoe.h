@@ -127,6 +127,24 @@ typedef struct smoe_layout {
 SMOE_API int smoe_layout_of(const smoe_shape *shape, smoe_layout *out);
 /* (for bits = 8, atom_bytes is 1088 and the offsets count 8-bit atoms) */
 
+/* ------------------------------------------------------- smoe_quantize_mlx */
+/* MLX-style affine quantisation of one float32 matrix w [rows][cols]
+ * (row-major, host memory) into the triples pack_experts reads: per group of
+ * 64 columns of a row, b = the group minimum rounded down to fp16, s = (max -
+ * b) / (2^bits - 1) rounded up to fp16, q = round-half-even((w - b) / s)
+ * clamped to [0, 2^bits - 1] (q = 0 where s = 0), all in double precision, so
+ * |w - (s q + b)| <= s / 2. Outputs (host, caller-owned): q uint32
+ * [rows][cols * bits / 32] (column c in bits bits*(c % (32/bits)).. of word
+ * c / (32/bits)), s and b fp16 bits [rows][cols / 64]. The pages name MLX
+ * int4/int8 group quantisation with a scale and bias per group of 64 (xix.ai
+ * article, last paragraph) but not the quantiser; the rounding directions are
+ * this library's reading, and bit parity with MLX's own quantiser is not
+ * claimed. Errors: SMOE_EINVAL (negative sizes, null buffers), SMOE_ENOTSUP
+ * (bits not 4 or 8, cols % 64), SMOE_ERANGE (a value or a group's span that
+ * fp16 cannot hold: non-finite or above 65504). */
+SMOE_API int smoe_quantize_mlx(const float *w, int32_t rows, int32_t cols, int32_t bits, uint32_t *q,
+                               uint16_t *s, uint16_t *b);
+
 /* ------------------------------------------------------------ pack_experts */
 /* MLX triples of one expert (as produced by MLX's affine quantisation):
  * q[0] gate uint32 [I][H/8], q[1] up [I][H/8], q[2] down [H][I/8], column c of

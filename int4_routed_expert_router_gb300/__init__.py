@@ -23,7 +23,8 @@ EXPORTS = ["smoe_layout_of", "pack_experts", "smoe_ctx_create", "smoe_ctx_destro
            "smoe_workspace_bytes", "moe_route", "moe_forward", "moe_forward_noalloc", "moe_decode_stack",
            "smoe_stack_workspace_bytes", "smoe_check", "smoe_ctx_describe", "smoe_set_profile_events",
            "smoe_status_string", "smoe_cache_create", "smoe_cache_destroy", "smoe_cache_prepare",
-           "smoe_cache_stats", "smoe_cache_simulate", "moe_forward_debug", "smoe_set_stack_wait", "gdn_step"]
+           "smoe_cache_stats", "smoe_cache_simulate", "moe_forward_debug", "smoe_set_stack_wait", "gdn_step",
+           "smoe_quantize_mlx"]
 
 
 class SmoeError(RuntimeError):
@@ -90,6 +91,7 @@ def lib():
         L.smoe_set_stack_wait.argtypes = [vp, u64, i32]
         L.smoe_status_string.argtypes = [C.c_int]
         L.gdn_step.argtypes = [C.POINTER(GdnShape), i32, i32, vp, vp, vp, vp, vp, C.c_float, vp, vp, vp]
+        L.smoe_quantize_mlx.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.smoe_status_string.restype = C.c_char_p
         for name in EXPORTS:
             if name not in ("smoe_workspace_bytes", "smoe_status_string"):
@@ -176,6 +178,21 @@ def expert_src(arrays) -> ExpertSrc:
         st.s[m] = _ptr(arrays[3 * m + 1])
         st.b[m] = _ptr(arrays[3 * m + 2])
     return st
+
+
+def quantize_mlx(w, bits: int = 4):
+    """MLX-style affine triples of a float32 matrix [rows][cols] (host numpy,
+    cols a multiple of 64): (q uint32 [rows][cols*bits/32], s, b fp16 bits
+    [rows][cols/64]), by the library's smoe_quantize_mlx."""
+    import numpy as np
+    w = np.ascontiguousarray(w, np.float32)
+    rows, cols = w.shape
+    q = np.zeros((rows, cols * bits // 32), np.uint32)
+    s = np.zeros((rows, cols // 64), np.uint16)
+    b = np.zeros((rows, cols // 64), np.uint16)
+    _check(lib().smoe_quantize_mlx(w.ctypes.data, rows, cols, bits, q.ctypes.data, s.ctypes.data, b.ctypes.data),
+           "smoe_quantize_mlx")
+    return q, s, b
 
 
 def pack_experts(shape: Shape, experts, slots, pool, pool_bytes: int, where: int, stream=None):

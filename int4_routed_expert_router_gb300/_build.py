@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libsmoe.so")
 SOURCES = ["smoe_api.cu", "route.cu", "decode.cu", "decode_stack.cu", "prefill.cu", "noalloc.cu", "cache.cu", "debug.cu",
-           "deltanet.cu"]
+           "deltanet.cu", "quant.cu"]
 HEADERS = ["smoe_dev.cuh", "smoe_internal.h", "decode_common.cuh", "route_common.cuh"]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
