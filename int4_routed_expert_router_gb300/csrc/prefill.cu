@@ -71,30 +71,56 @@ constexpr int kXThreads = (kXGatherW0 + kXGatherWarps) * 32;
 // T tokens: its narrower accumulators leave tensor memory for 8 stages, so the
 // gathered rows (about a microsecond from request to landing) are asked for 6
 // steps ahead instead of 2.
-template <int MAXN, int STG, int GDEPTH>
+// KS: K columns per step (64 or 128; a step's B stage is KS / 64 panels of
+// MAXN rows x 128 bytes, its A stage KS / 2 tensor-memory columns).
+template <int MAXN, int STG, int GDEPTH, int KS = 64, int ACC = kXAcc>
 struct XCfg {
-    static constexpr int MaxN = MAXN, Stg = STG, GDepth = GDEPTH;
-    static constexpr int BBytes = MAXN * kPfK * 2;                   // one B stage
-    static constexpr uint32_t ACol0 = kXAcc * MAXN;                  // first A column
-    static constexpr int GRows = MAXN / (kXGatherWarps * 32 / 8);    // rows per gather thread per K step
-    static_assert(ACol0 + STG * 32 <= 512, "TMEM columns");
-    static_assert(GDEPTH <= STG - 2 && MAXN % 64 == 0, "ring shape");
+    static constexpr int MaxN = MAXN, Stg = STG, GDepth = GDEPTH, Ks = KS, Acc = ACC;
+    static constexpr int Panels = KS / 64;                             // 64-column K panels per step
+    static constexpr int PanelBytes = MAXN * 128;
+    static constexpr int BBytes = Panels * PanelBytes;                 // one B stage
+    static constexpr uint32_t ACol0 = ACC * MAXN;                      // first A column
+    static constexpr int ACols = KS / 2;                               // A stage columns
+    static constexpr int GChunks = KS / 8;                             // 16-byte pieces of a row per step
+    static constexpr int GRStep = kXGatherWarps * 32 / GChunks;        // rows between one thread's pieces
+    static constexpr int GRows = MAXN / GRStep;                        // rows per gather thread per K step
+    static_assert(ACol0 + STG * ACols <= 512, "TMEM columns");
+    static_assert(GDEPTH <= STG - 2 && MAXN % 64 == 0 && (KS == 64 || KS == 128 || KS == 256) && ACC >= 1,
+                  "ring shape");
 };
-using XWide = XCfg<kXMaxN, 4, 2>;
-using XNarrow = XCfg<64, 8, 6>;
+// The shapes in use. A step's fixed cost (the operand ring's waits and
+// arrivals, the gather's round trip, the MMA thread's commit) is paid per K
+// step, so the largest K step that tensor and shared memory allow wins:
+// wide tiles take 128 columns per step with one accumulator (three stages),
+// narrow ones 256 (their accumulators are a third as wide). K (H for gate/up,
+// I for down) must be a multiple of the step; I that is not falls back to
+// 64-column steps for the down GEMM.
+using XWide = XCfg<kXMaxN, 3, 1, 128, 1>;
+using XWide64 = XCfg<kXMaxN, 4, 2, 64, 2>;
+using XNarrow = XCfg<64, 3, 1, 256>;
+using XNarrow64 = XCfg<64, 8, 6, 64>;
 constexpr int kXNarrowT = 64;
 
 // The raw-atom ring of the expert GEMMs for BITS-bit experts: bytes per atom,
-// slots, bytes per K step (8 atoms), and the CTA's shared memory.
+// bytes per K step (8 atoms per 64 columns), slots (the K lead of 16 or 12
+// 64-column steps where shared memory allows, else what fits), and the CTA's
+// shared memory.
 template <int BITS, typename CFG>
 struct XRaw {
     static constexpr int AB = BITS == 8 ? kAtom8Bytes : kAtomBytes;
-    static constexpr int Slots = BITS == 8 ? 12 : kXRaw;
-    static constexpr int Step = 8 * AB;
+    static constexpr int Step = 8 * AB * CFG::Panels;
+    static constexpr int Budget = 232448 - 2048 - CFG::Stg * CFG::BBytes;
+    static constexpr int Want = (BITS == 8 ? 12 : kXRaw) / CFG::Panels;
+    static constexpr int Slots = Want * Step <= Budget ? Want : Budget / Step;
     static constexpr int Smem = CFG::Stg * CFG::BBytes + Slots * Step + 1024 /*align*/ + 1024 /*barriers*/;
+    static_assert(Slots >= 2 && Smem <= 232448, "shared memory per CTA");
 };
-static_assert(XRaw<8, XWide>::Smem <= 232448 && XRaw<4, XWide>::Smem <= 232448, "shared memory per CTA");
-static_assert(XRaw<8, XNarrow>::Smem <= 232448 && XRaw<4, XNarrow>::Smem <= 232448, "shared memory per CTA");
+
+// The kernel and its shared memory for one launch.
+struct XLaunch {
+    void (*kern)(const GemmParams, const CUtensorMap, const CUtensorMap, const CUtensorMap);
+    int smem;
+};
 
 __device__ __forceinline__ uint32_t sw128(int r, int c)   // byte offset of (row, col) in a 64-col bf16 tile
 {
@@ -776,7 +802,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) router_gemm_kernel(const GemmPa
 // h in the down GEMM's K order) share a 4-byte store.
 // Down: 12 warps, 3 per quadrant, chunks of 32 tokens; each pair's fp16
 // output, two rows per 4-byte store (neighbouring lanes swap halves).
-template <int MAXN, typename TileOf>
+template <int MAXN, int ACC, typename TileOf>
 __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uint64_t *accfull, uint64_t *accempty,
                                          volatile int *abort, int warp, int lane, int my_tiles, TileOf tile_of)
 {
@@ -785,11 +811,11 @@ __device__ __forceinline__ void epilogue(const GemmParams &p, uint32_t tmem, uin
     uint32_t ymax = 0;                                            // largest |fp16| bits stored, per half
     TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
     for (int i = 0; i < my_tiles; ++i) {
-        const int b = i % kXAcc;
+        const int b = i % ACC;
         const TileInfo ti = tnext;
         const int mt = tile_of(i) % p.m_tiles;
         if (i + 1 < my_tiles) tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
-        pf_wait(&accfull[b], (i / kXAcc) & 1, p.err, abort);
+        pf_wait(&accfull[b], (i / ACC) & 1, p.err, abort);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (!ti.valid) set_error(p.err, SMOE_DEV_BAD_SLOT);       // and the tile's outputs are zeros
         if (p.mode == 0) {
@@ -878,8 +904,8 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     uint64_t *bars = reinterpret_cast<uint64_t *>(raw + RW::Slots * RW::Step);
     uint64_t *rawfull = bars, *rawempty = bars + RW::Slots;
     uint64_t *full = bars + 2 * RW::Slots, *empty = full + CFG::Stg;     // stage s: A (TMEM) + B (smem)
-    uint64_t *accfull = empty + CFG::Stg, *accempty = accfull + kXAcc;
-    uint64_t *bfull = accempty + kXAcc;                           // down: B copies of stage s (TMA)
+    uint64_t *accfull = empty + CFG::Stg, *accempty = accfull + CFG::Acc;
+    uint64_t *bfull = accempty + CFG::Acc;                           // down: B copies of stage s (TMA)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bfull + CFG::Stg);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -887,7 +913,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     const int ntiles = *p.ntiles * p.m_tiles;
     const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
     if (my_tiles == 0) return;                                    // uniform
-    const int nk = (p.mode == 1 ? p.I : p.H) / kPfK;
+    const int nk = (p.mode == 1 ? p.I : p.H) / CFG::Ks;
     const int total = my_tiles * nk;
     auto tile_of = [&](int i) { return int(blockIdx.x) + i * int(gridDim.x); };
 
@@ -903,7 +929,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             mbar_init(&empty[s], 1);
             mbar_init(&bfull[s], 1);
         }
-        for (int b = 0; b < kXAcc; ++b) {
+        for (int b = 0; b < CFG::Acc; ++b) {
             mbar_init(&accfull[b], 1);
             mbar_init(&accempty[b], (p.mode == 1 ? kPfEpi + kXGatherWarps : kPfEpi) * 32);   // epilogue threads
         }
@@ -925,7 +951,7 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
     // epilogue warps: 8..15, and in the down GEMM also the gather warps (idle there)
     const bool epi_role = (warp >= kPfWorkers && warp < kPfWorkers + kPfEpi) || (p.mode == 1 && warp >= kXGatherW0);
     if (epi_role) {
-        epilogue<CFG::MaxN>(p, tmem, accfull, accempty, abort, warp, lane, my_tiles, tile_of);
+        epilogue<CFG::MaxN, CFG::Acc>(p, tmem, accfull, accempty, abort, warp, lane, my_tiles, tile_of);
     } else if (warp == kPfRawWarp) {
         // ---- raw atoms (8 row blocks x one group) per K step: one TMA box each
         if (lane == 0) {
@@ -943,8 +969,12 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                     if (!pf_wait(&rawempty[r], ph ^ 1u, p.err, abort)) { ok = false; break; }
                     if (ti.valid) {
                         mbar_arrive_expect_tx(&rawfull[r], RW::Step);
-                        if constexpr (BITS == 8) tma_raw8(smem_u32(raw + r * RW::Step), map, kb, mt, ti.slot, &rawfull[r], pol);
-                        else tma_raw(smem_u32(raw + r * RW::Step), map, kb, mt, ti.slot, &rawfull[r], pol);
+#pragma unroll
+                        for (int j = 0; j < CFG::Panels; ++j) {            // one box per 64-column group
+                            const uint32_t dst = smem_u32(raw + r * RW::Step + j * 8 * RW::AB);
+                            if constexpr (BITS == 8) tma_raw8(dst, map, kb * CFG::Panels + j, mt, ti.slot, &rawfull[r], pol);
+                            else tma_raw(dst, map, kb * CFG::Panels + j, mt, ti.slot, &rawfull[r], pol);
+                        }
                     } else {
                         mbar_arrive(&rawfull[r]);              // nothing to load; the epilogue writes zeros
                     }
@@ -963,19 +993,23 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             // n .. N - 1 repeat row n - 1 (their accumulator columns are never
             // stored). A step is signalled once its copies have landed, CFG::GDepth
             // steps later (cp.async groups), after a proxy fence for the MMA.
-            const int gt = tid - kXGatherW0 * 32, c8 = gt & 7, r0 = gt >> 3;
-            // byte offsets: source row u = token row start + chunk; destination row
-            // r0 + 16 u = sw128(r0, 8 c8) + 2048 u (16 u keeps the row's swizzle phase)
+            // (KS = 128: thread g takes piece g % 16 of rows g / 16 + 8 u, the
+            // pieces 8 .. 15 going to the step's second panel)
+            const int gt = tid - kXGatherW0 * 32, c = gt % CFG::GChunks, r0 = gt / CFG::GChunks;
+            const int c8 = c & 7, pan = c >> 3;
+            // byte offsets: source row u = token row start + piece; destination row
+            // r0 + GRStep u at sw128(r0 + GRStep u, 8 c8) of the piece's panel (with
+            // KS = 256 the step is 4 rows, so the row's swizzle phase changes with u)
             auto rows_of = [&](const TileInfo &t, uint32_t (&off)[CFG::GRows]) {
 #pragma unroll
                 for (int u = 0; u < CFG::GRows; ++u) {
-                    const int rr = min(r0 + 16 * u, t.n - 1);
+                    const int rr = min(r0 + CFG::GRStep * u, t.n - 1);
                     const int tok = t.kind == 1 ? t.p0 + rr : p.pair_token[t.p0 + rr];
-                    off[u] = uint32_t(tok) * uint32_t(2 * p.H) + uint32_t(16 * c8);   // < 2^32: T <= SMOE_MAX_TOKENS, H <= 2048
+                    off[u] = uint32_t(tok) * uint32_t(2 * p.H) + uint32_t(16 * c);   // < 2^32: T <= SMOE_MAX_TOKENS, H <= 2048
                 }
             };
             const char *xt = reinterpret_cast<const char *>(p.x);
-            const uint32_t dst0 = smem_u32(bst) + sw128(r0, 8 * c8);
+            const uint32_t dst0 = smem_u32(bst) + uint32_t(pan * CFG::PanelBytes);
             uint32_t cur[CFG::GRows], nxt[CFG::GRows];
             TileInfo tnext = tile_info(p, tile_of(0) / p.m_tiles);
             rows_of(tnext, nxt);
@@ -989,14 +1023,14 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
                     tnext = tile_info(p, tile_of(i + 1) / p.m_tiles);
                     rows_of(tnext, nxt);
                 }
-                const int urows = (ti.N - r0 + 15) / 16;              // rows r0 + 16 u < N
+                const int urows = (ti.N - r0 + CFG::GRStep - 1) / CFG::GRStep;   // rows r0 + GRStep u < N
                 for (int kb = 0; kb < nk; ++kb) {
                     pf_wait(&empty[sb], ph ^ 1u, p.err, abort);
                     const uint32_t dst = dst0 + uint32_t(sb * CFG::BBytes);
-                    const char *src = xt + kb * (kPfK * 2);
+                    const char *src = xt + kb * (CFG::Ks * 2);
 #pragma unroll
                     for (int u = 0; u < CFG::GRows; ++u)
-                        if (u < urows) cp_async16(dst + uint32_t(2048 * u), src + cur[u], 16u);
+                        if (u < urows) cp_async16(dst + sw128(r0 + CFG::GRStep * u, 8 * c8), src + cur[u], 16u);
                     asm volatile("cp.async.commit_group;" ::: "memory");
                     if (++sb == CFG::Stg) { sb = 0; ph ^= 1u; }
                     if (++issued > CFG::GDepth) {
@@ -1024,14 +1058,15 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             for (int i = 0; i < my_tiles && ok; ++i) {
                 const TileInfo ti = tile_info(p, tile_of(i) / p.m_tiles);
                 const int nbox = (ti.N + kPfBoxRows - 1) / kPfBoxRows;
-                const uint32_t bytes = uint32_t(nbox) * kPfBoxRows * (kPfK * 2);
+                const uint32_t bytes = uint32_t(CFG::Panels * nbox) * kPfBoxRows * (kPfK * 2);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!pf_wait(&empty[sb], ph ^ 1u, p.err, abort)) { ok = false; break; }
                     mbar_arrive_expect_tx(&bfull[sb], bytes);
                     const uint32_t dst = smem_u32(bst + sb * CFG::BBytes);
-                    for (int j = 0; j < nbox; ++j)
-                        tma_load_2d(dst + j * (kPfBoxRows * kPfK * 2), &bmap, kb * kPfK, ti.rowbase + j * kPfBoxRows,
-                                    &bfull[sb]);
+                    for (int pn = 0; pn < CFG::Panels; ++pn)
+                        for (int j = 0; j < nbox; ++j)
+                            tma_load_2d(dst + pn * CFG::PanelBytes + j * (kPfBoxRows * kPfK * 2), &bmap,
+                                        kb * CFG::Ks + pn * kPfK, ti.rowbase + j * kPfBoxRows, &bfull[sb]);
                     ++issued;
                     if (++sb == CFG::Stg) { sb = 0; ph ^= 1u; }
                 }
@@ -1047,29 +1082,30 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
             uint32_t ph = 0;
             int nextN = tile_info(p, tile_of(0) / p.m_tiles).N;
             for (int i = 0; i < my_tiles; ++i) {
-                const int b = i % kXAcc;
+                const int b = i % CFG::Acc;
                 const uint32_t idesc = umma_idesc(nextN, false);
                 if (i + 1 < my_tiles) nextN = tile_info(p, tile_of(i + 1) / p.m_tiles).N;   // used one tile later
-                pf_wait(&accempty[b], ((i / kXAcc) & 1) ^ 1u, p.err, abort);
+                pf_wait(&accempty[b], ((i / CFG::Acc) & 1) ^ 1u, p.err, abort);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t acc_t = tmem + uint32_t(b * CFG::MaxN);
                 for (int kb = 0; kb < nk; ++kb) {
                     pf_wait_fast(&full[s], ph, p.err, abort);
                     if (p.mode == 1) pf_wait_fast(&bfull[s], ph, p.err, abort);
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint64_t bd = umma_desc(smem_u32(bst + s * CFG::BBytes));
-                    const uint32_t a_t = tmem + CFG::ACol0 + uint32_t(32 * s);
-                    umma_ts(acc_t, a_t, bd, idesc, kb ? 1u : 0u);
+                    const uint32_t bs = smem_u32(bst + s * CFG::BBytes);
+                    const uint32_t a_t = tmem + CFG::ACol0 + uint32_t(CFG::ACols * s);
 #pragma unroll
-                    for (int k4 = 1; k4 < kPfK / 16; ++k4)
-                        umma_ts(acc_t, a_t + uint32_t(8 * k4), bd + uint64_t(k4 * 2), idesc, 1u);
+                    for (int k4 = 0; k4 < CFG::Ks / 16; ++k4) {
+                        const uint64_t bd = umma_desc(bs + uint32_t((k4 >> 2) * CFG::PanelBytes));
+                        umma_ts(acc_t, a_t + uint32_t(8 * k4), bd + uint64_t((k4 & 3) * 2), idesc, (kb | k4) ? 1u : 0u);
+                    }
                     umma_commit(&empty[s]);
                     if (++s == CFG::Stg) { s = 0; ph ^= 1u; }
                 }
                 umma_commit(&accfull[b]);
             }
             // the tensor cores are done with TMEM and shared memory before the CTA exits
-            mbar_wait(&accfull[(my_tiles - 1) % kXAcc], ((my_tiles - 1) / kXAcc) & 1, p.err);
+            mbar_wait(&accfull[(my_tiles - 1) % CFG::Acc], ((my_tiles - 1) / CFG::Acc) & 1, p.err);
         }
     } else if (warp < kPfWorkers) {
         // ---- A: dequantise atom a of each K step into the fragment order of the
@@ -1081,36 +1117,44 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
         uint32_t phr = 0, pha = 0;                                // raw ring, operand ring
         for (int gk = 0; gk < total; ++gk) {
             pf_wait(&rawfull[r], phr, p.err, abort);
-            const uint8_t *atom = raw + r * RW::Step + a * RW::AB;
-            const uint4 q = *reinterpret_cast<const uint4 *>(atom + 16 * lane);   // (low nibbles, 8-bit)
-            uint4 qh = make_uint4(0u, 0u, 0u, 0u);                                // 8-bit: the high nibbles
-            if constexpr (BITS == 8) qh = *reinterpret_cast<const uint4 *>(atom + kAtomQBytes + 16 * lane);
-            const uint2 sbp = *reinterpret_cast<const uint2 *>(atom + (BITS == 8 ? 2 : 1) * kAtomQBytes + 8 * g);
+            uint4 q[CFG::Panels], qh[CFG::Panels];
+            uint2 sbp[CFG::Panels];
+#pragma unroll
+            for (int j = 0; j < CFG::Panels; ++j) {                    // group j of the step
+                const uint8_t *atom = raw + r * RW::Step + j * 8 * RW::AB + a * RW::AB;
+                q[j] = *reinterpret_cast<const uint4 *>(atom + 16 * lane);          // (low nibbles, 8-bit)
+                qh[j] = make_uint4(0u, 0u, 0u, 0u);                                 // 8-bit: the high nibbles
+                if constexpr (BITS == 8) qh[j] = *reinterpret_cast<const uint4 *>(atom + kAtomQBytes + 16 * lane);
+                sbp[j] = *reinterpret_cast<const uint2 *>(atom + (BITS == 8 ? 2 : 1) * kAtomQBytes + 8 * g);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&rawempty[r]);
             if (++r == RW::Slots) { r = 0; phr ^= 1u; }
-            const uint32_t s0 = __byte_perm(sbp.x, 0, 0x1010), b0 = __byte_perm(sbp.x, 0, 0x3232);   // row g
-            const uint32_t s1 = __byte_perm(sbp.y, 0, 0x1010), b1 = __byte_perm(sbp.y, 0, 0x3232);   // row g + 8
-            const uint32_t wg[2] = {q.x, q.y}, wh[2] = {q.z, q.w};
-            const uint32_t wg8[2] = {qh.x, qh.y}, wh8[2] = {qh.z, qh.w};
-            uint32_t v[16];
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                const int m0 = 2 * (rr & 1);
-                if constexpr (BITS == 8) {
-                    v[4 * rr + 0] = hfma2(byte_pair_f16(wg[rr >> 1], wg8[rr >> 1], m0), s0, b0);
-                    v[4 * rr + 1] = hfma2(byte_pair_f16(wg[rr >> 1], wg8[rr >> 1], m0 + 1), s0, b0);
-                    v[4 * rr + 2] = hfma2(byte_pair_f16(wh[rr >> 1], wh8[rr >> 1], m0), s1, b1);
-                    v[4 * rr + 3] = hfma2(byte_pair_f16(wh[rr >> 1], wh8[rr >> 1], m0 + 1), s1, b1);
-                } else {
-                    v[4 * rr + 0] = hfma2(nib_pair_f16(wg[rr >> 1], m0), s0, b0);
-                    v[4 * rr + 1] = hfma2(nib_pair_f16(wg[rr >> 1], m0 + 1), s0, b0);
-                    v[4 * rr + 2] = hfma2(nib_pair_f16(wh[rr >> 1], m0), s1, b1);
-                    v[4 * rr + 3] = hfma2(nib_pair_f16(wh[rr >> 1], m0 + 1), s1, b1);
-                }
-            }
             pf_wait(&empty[sa], pha ^ 1u, p.err, abort);
-            tmem_st16x256x4(tmem + lane_base + CFG::ACol0 + uint32_t(32 * sa), v);
+#pragma unroll
+            for (int j = 0; j < CFG::Panels; ++j) {
+                const uint32_t s0 = __byte_perm(sbp[j].x, 0, 0x1010), b0 = __byte_perm(sbp[j].x, 0, 0x3232);   // row g
+                const uint32_t s1 = __byte_perm(sbp[j].y, 0, 0x1010), b1 = __byte_perm(sbp[j].y, 0, 0x3232);   // row g + 8
+                const uint32_t wg[2] = {q[j].x, q[j].y}, wh[2] = {q[j].z, q[j].w};
+                const uint32_t wg8[2] = {qh[j].x, qh[j].y}, wh8[2] = {qh[j].z, qh[j].w};
+                uint32_t v[16];
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int m0 = 2 * (rr & 1);
+                    if constexpr (BITS == 8) {
+                        v[4 * rr + 0] = hfma2(byte_pair_f16(wg[rr >> 1], wg8[rr >> 1], m0), s0, b0);
+                        v[4 * rr + 1] = hfma2(byte_pair_f16(wg[rr >> 1], wg8[rr >> 1], m0 + 1), s0, b0);
+                        v[4 * rr + 2] = hfma2(byte_pair_f16(wh[rr >> 1], wh8[rr >> 1], m0), s1, b1);
+                        v[4 * rr + 3] = hfma2(byte_pair_f16(wh[rr >> 1], wh8[rr >> 1], m0 + 1), s1, b1);
+                    } else {
+                        v[4 * rr + 0] = hfma2(nib_pair_f16(wg[rr >> 1], m0), s0, b0);
+                        v[4 * rr + 1] = hfma2(nib_pair_f16(wg[rr >> 1], m0 + 1), s0, b0);
+                        v[4 * rr + 2] = hfma2(nib_pair_f16(wh[rr >> 1], m0), s1, b1);
+                        v[4 * rr + 3] = hfma2(nib_pair_f16(wh[rr >> 1], m0 + 1), s1, b1);
+                    }
+                }
+                tmem_st16x256x4(tmem + lane_base + CFG::ACol0 + uint32_t(CFG::ACols * sa + 32 * j), v);
+            }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             mbar_arrive(&full[sa]);
@@ -1159,21 +1203,32 @@ __global__ void __launch_bounds__(256) combine_kernel(const PrefillParams p)
 
 // ------------------------------------------------------------------ host
 
+template <int BITS, typename CFG>
+static XLaunch xlaunch()
+{
+    return {expert_gemm_kernel<BITS, CFG>, XRaw<BITS, CFG>::Smem};
+}
+
+// The shape for one expert GEMM launch: narrow for T <= kXNarrowT, wide above;
+// the 64-column variant where K is not a multiple of the shape's step.
+static XLaunch pick_gemm(bool b8, bool narrow, int K)
+{
+    if (narrow) {
+        if (K % XNarrow::Ks == 0) return b8 ? xlaunch<8, XNarrow>() : xlaunch<4, XNarrow>();
+        return b8 ? xlaunch<8, XNarrow64>() : xlaunch<4, XNarrow64>();
+    }
+    if (K % XWide::Ks == 0) return b8 ? xlaunch<8, XWide>() : xlaunch<4, XWide>();
+    return b8 ? xlaunch<8, XWide64>() : xlaunch<4, XWide64>();
+}
+
 cudaError_t prefill_config()
 {
     cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(expert_gemm_kernel<4, XWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 XRaw<4, XWide>::Smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(expert_gemm_kernel<8, XWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 XRaw<8, XWide>::Smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(expert_gemm_kernel<4, XNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 XRaw<4, XNarrow>::Smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(expert_gemm_kernel<8, XNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 XRaw<8, XNarrow>::Smem);
+    const XLaunch all[8] = {xlaunch<4, XWide>(), xlaunch<8, XWide>(), xlaunch<4, XWide64>(), xlaunch<8, XWide64>(),
+                            xlaunch<4, XNarrow>(), xlaunch<8, XNarrow>(), xlaunch<4, XNarrow64>(),
+                            xlaunch<8, XNarrow64>()};
+    for (const XLaunch &x : all)
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(x.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, x.smem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bucket_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  bucket_small_smem(1024));
@@ -1318,20 +1373,18 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
     g.mode = 0;
     g.m_tiles = g.I / 64;
     if ((e = prof_record(nprof > 0 ? prof[0] : nullptr, st)) != cudaSuccess) return e;
-    // T <= kXNarrowT: every tile holds at most T tokens, so the narrow ring shape fits
+    // T <= kXNarrowT: every tile holds at most T tokens, so the narrow ring shape fits;
+    // its 128-column K steps need K (H for gate/up, I for down) a multiple of 128
     const bool narrow = p.T <= kXNarrowT;
-    auto kern = narrow ? (b8 ? expert_gemm_kernel<8, XNarrow> : expert_gemm_kernel<4, XNarrow>)
-                       : (b8 ? expert_gemm_kernel<8, XWide> : expert_gemm_kernel<4, XWide>);
-    const int xsmem = narrow ? (b8 ? XRaw<8, XNarrow>::Smem : XRaw<4, XNarrow>::Smem)
-                             : (b8 ? XRaw<8, XWide>::Smem : XRaw<4, XWide>::Smem);
-    if ((e = launch_pdl(kern, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), xsmem, st, g, xmap, gu_pool,
-                        gu_shared)) != cudaSuccess)
+    const XLaunch gu = pick_gemm(b8, narrow, p.H), dn = pick_gemm(b8, narrow, g0.I);
+    if ((e = launch_pdl(gu.kern, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), gu.smem, st, g, xmap,
+                        gu_pool, gu_shared)) != cudaSuccess)
         return e;
     if ((e = prof_record(nprof > 1 ? prof[1] : nullptr, st)) != cudaSuccess) return e;
     g.mode = 1;
     g.m_tiles = p.H / kPfM;
-    if ((e = launch_pdl(kern, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), xsmem, st, g, hmap, dn_pool,
-                        dn_shared)) != cudaSuccess)
+    if ((e = launch_pdl(dn.kern, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), dn.smem, st, g, hmap,
+                        dn_pool, dn_shared)) != cudaSuccess)
         return e;
     if ((e = prof_record(nprof > 2 ? prof[2] : nullptr, st)) != cudaSuccess) return e;
     return launch_pdl(combine_kernel, dim3((p.H / 4 + 255) / 256, p.T), dim3(256), 0, st, p);
