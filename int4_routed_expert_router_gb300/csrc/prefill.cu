@@ -10,8 +10,9 @@
 //     the int4 atoms are dequantised to fp16 straight into tensor memory, the
 //     tile's token rows are gathered into 128-byte-swizzled shared memory, and
 //     tcgen05 tensor cores multiply them (A from TMEM, B from shared memory)
-//     into an accumulator in TMEM; the epilogue applies SwiGLU and writes h in
-//     expert order;
+//     into an accumulator in TMEM, 128 K columns per pipeline step (256 for
+//     T <= 64, whose tiles are narrower); the epilogue applies SwiGLU and
+//     writes h in expert order;
 //   down GEMM: per tile, 128 down rows x its pairs, K = I, B = h rows; the
 //     epilogue stores each pair's expert output;
 //   combine: per token, the k pair outputs times their routing weights in route
@@ -36,7 +37,7 @@
 namespace smoe {
 
 constexpr int kPfM = 128;          // weight rows per tile
-constexpr int kPfK = 64;           // K per pipeline step (one quantisation group)
+constexpr int kPfK = 64;           // K of one quantisation group (a 128-byte swizzled panel of 16-bit values)
 constexpr int kPfMaxN = 256;       // tokens per tile
 constexpr int kPfAB = 4;           // router GEMM: A/B operand stages
 constexpr int kPfBoxRows = 64;     // B rows per TMA box
@@ -53,9 +54,9 @@ constexpr int kPfSmem = kPfAB * kPfStageBytes + 1024 /*align*/ + 512 /*barriers*
 static_assert(kPfSmem <= 232448, "shared memory per CTA");
 
 // Expert GEMMs (gate/up, down): A (the dequantised weights) lives in tensor
-// memory. TMEM columns: two accumulators of MaxN columns, then Stg A stages of
-// 32 columns (128 rows x 64 fp16 K values). Shared memory holds only the B
-// stages and the raw atoms.
+// memory. TMEM columns: Acc accumulators of MaxN columns, then Stg A stages of
+// Ks / 2 columns (128 rows x Ks fp16 K values). Shared memory holds only the
+// B stages and the raw atoms.
 constexpr int kXMaxN = 192;        // tokens per expert tile (the bucketing's bound)
 constexpr int kXRaw = 16;          // raw atom slots
 constexpr int kXAcc = 2;           // accumulator buffers in TMEM (the epilogue of a tile overlaps the next)
