@@ -11,10 +11,12 @@
 // route_logits_kernel: CTA (row block, token block) of 8 rows x 8 tokens; the
 // rows (router rows, plus the shared-gate vector as row E) and the tokens are
 // bulk-copied into shared memory, one warp per row forms the fp32 dot products.
-// With fused_topk the last CTA to finish (arrival ticket) then runs the top-k
-// for every token with all its warps (two levels of warp max-reductions over
-// order-preserving integer keys), so a decode step costs one launch;
-// otherwise topk_kernel runs one warp per token.
+// With fused_topk (T <= 8) the last CTA to finish (arrival ticket) then runs
+// the top-k for every token with all its warps (two levels of warp
+// max-reductions over order-preserving integer keys), so a decode step costs
+// one launch; up to kRouteGemvMaxT tokens topk_cta_kernel then ranks each
+// token with a CTA the same way; above it the logits come from the
+// tensor-core kernel and topk_kernel runs one warp per token.
 #include "route_common.cuh"
 
 namespace smoe {
@@ -48,17 +50,18 @@ __device__ void write_choice(const RouteParams &p, int t, const uint32_t *fk, co
     if (lane == 0) p.gate[t] = shared_gate(zs);
 }
 
-// Top-k of T <= 8 tokens by the 8 warps of a CTA (the CTA that finishes the
-// logits last). The T x (E + 1) logits are first copied to shared memory by
-// all threads (one round trip to L2). Each token gets 8/T' warps (T' = T
-// rounded up to a power of two); each of them takes a slice of the experts
-// (level 1), then one warp merges the slices' candidates (level 2).
-// ckey/cid: 2 * 8 * 16 entries; zsm: T * (E + 1) floats.
-__device__ void block_topk(const RouteParams &p, uint32_t *ckey, int32_t *cid, float *zsm)
+// Top-k of tokens tok0 .. tok0 + T - 1 (T <= 8) by the 8 warps of a CTA. The
+// T x (E + 1) logits are first copied to shared memory by all threads (one
+// round trip to L2). Each token gets 8/T' warps (T' = T rounded up to a power
+// of two); each of them takes a slice of the experts (level 1), then one warp
+// merges the slices' candidates (level 2). ckey/cid: 2 * 8 * 16 entries; zsm:
+// T * (E + 1) floats.
+__device__ void block_topk(const RouteParams &p, int tok0, int T, uint32_t *ckey, int32_t *cid, float *zsm)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int T = p.T, E = p.E, k = p.k;
-    for (int i = threadIdx.x; i < T * (E + 1); i += blockDim.x) zsm[i] = __ldcg(p.logits + i);
+    const int E = p.E, k = p.k;
+    const float *lg = p.logits + size_t(tok0) * (E + 1);
+    for (int i = threadIdx.x; i < T * (E + 1); i += blockDim.x) zsm[i] = __ldcg(lg + i);
     __syncthreads();
     int tp = 1;
     while (tp < T) tp <<= 1;
@@ -76,7 +79,7 @@ __device__ void block_topk(const RouteParams &p, uint32_t *ckey, int32_t *cid, f
         int32_t *fi = cid + 8 * 16 + warp * 16;
         topk_merge(ckey + warp * 16, cid + warp * 16, wpt, k, fk, fi, lane);
         __syncwarp();
-        write_choice(p, t, fk, fi, zsm[t * (E + 1) + E], lane);
+        write_choice(p, tok0 + t, fk, fi, zsm[t * (E + 1) + E], lane);
     }
 }
 
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const RouteParams p)
     if (!last) return;
     __shared__ uint32_t ckey[2 * 8 * 16];
     __shared__ int32_t cid[2 * 8 * 16];
-    block_topk(p, ckey, cid, reinterpret_cast<float *>(wrow));   // the router rows are no longer needed
+    block_topk(p, 0, T, ckey, cid, reinterpret_cast<float *>(wrow));   // the router rows are no longer needed
     if (tid == 0) atomicExch(p.counter, 0u);
 }
 
@@ -164,6 +167,20 @@ __global__ void __launch_bounds__(256) topk_kernel(const RouteParams p)
                                       : router_dot(p.ws, p.x + size_t(t) * p.H, p.H, lane);
     __syncwarp();
     write_choice(p, t, ckey + warp * 16, cid + warp * 16, zs, lane);
+}
+
+// One token per CTA (8 < T <= kRouteGemvMaxT, after the GEMV kernel): the
+// token's 8 warps each rank a slice of the experts and warp 0 merges them, as
+// the fused top-k does for T <= 8, so a token's top-k takes one warp's share
+// of E / 8 experts instead of all E.
+__global__ void __launch_bounds__(256) topk_cta_kernel(const RouteParams p)
+{
+    __shared__ uint32_t ckey[2 * 8 * 16];
+    __shared__ int32_t cid[2 * 8 * 16];
+    __shared__ float zsm[1024 + 1];
+    pdl_wait();
+    pdl_trigger();
+    block_topk(p, int(blockIdx.x), 1, ckey, cid, zsm);
 }
 
 cudaError_t route_config()
@@ -198,7 +215,7 @@ cudaError_t launch_route(const RouteParams &p0, cudaStream_t st)
     lc.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&lc, route_logits_kernel, p);
     if (e != cudaSuccess || p.fused_topk) return e;
-    return launch_pdl(topk_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, p);
+    return launch_pdl(topk_cta_kernel, dim3(p.T), dim3(256), 0, st, p);
 }
 
 }  // namespace smoe
