@@ -95,8 +95,11 @@ struct XCfg {
 // wide tiles take 128 columns per step with one accumulator (three stages),
 // narrow ones 256 (their accumulators are a third as wide). K (H for gate/up,
 // I for down) must be a multiple of the step; I that is not falls back to
-// 64-column steps for the down GEMM.
+// 64-column steps for the down GEMM. The wide down GEMM loads B by TMA (no
+// gather to run ahead), so it trades the third stage for a second accumulator
+// and its epilogue overlaps the next tile's MMAs.
 using XWide = XCfg<kXMaxN, 3, 1, 128, 1>;
+using XWideDown = XCfg<kXMaxN, 2, 0, 128, 2>;
 using XWide64 = XCfg<kXMaxN, 4, 2, 64, 2>;
 using XNarrow = XCfg<64, 3, 1, 256>;
 using XNarrow64 = XCfg<64, 8, 6, 64>;
@@ -1212,12 +1215,13 @@ static XLaunch xlaunch()
 
 // The shape for one expert GEMM launch: narrow for T <= kXNarrowT, wide above;
 // the 64-column variant where K is not a multiple of the shape's step.
-static XLaunch pick_gemm(bool b8, bool narrow, int K)
+static XLaunch pick_gemm(bool b8, bool narrow, bool down, int K)
 {
     if (narrow) {
         if (K % XNarrow::Ks == 0) return b8 ? xlaunch<8, XNarrow>() : xlaunch<4, XNarrow>();
         return b8 ? xlaunch<8, XNarrow64>() : xlaunch<4, XNarrow64>();
     }
+    if (down && K % XWideDown::Ks == 0) return b8 ? xlaunch<8, XWideDown>() : xlaunch<4, XWideDown>();
     if (K % XWide::Ks == 0) return b8 ? xlaunch<8, XWide>() : xlaunch<4, XWide>();
     return b8 ? xlaunch<8, XWide64>() : xlaunch<4, XWide64>();
 }
@@ -1225,9 +1229,9 @@ static XLaunch pick_gemm(bool b8, bool narrow, int K)
 cudaError_t prefill_config()
 {
     cudaError_t e = cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
-    const XLaunch all[8] = {xlaunch<4, XWide>(), xlaunch<8, XWide>(), xlaunch<4, XWide64>(), xlaunch<8, XWide64>(),
-                            xlaunch<4, XNarrow>(), xlaunch<8, XNarrow>(), xlaunch<4, XNarrow64>(),
-                            xlaunch<8, XNarrow64>()};
+    const XLaunch all[10] = {xlaunch<4, XWide>(), xlaunch<8, XWide>(), xlaunch<4, XWideDown>(), xlaunch<8, XWideDown>(),
+                             xlaunch<4, XWide64>(), xlaunch<8, XWide64>(), xlaunch<4, XNarrow>(), xlaunch<8, XNarrow>(),
+                             xlaunch<4, XNarrow64>(), xlaunch<8, XNarrow64>()};
     for (const XLaunch &x : all)
         if (e == cudaSuccess) e = cudaFuncSetAttribute(x.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, x.smem);
     if (e == cudaSuccess)
@@ -1377,7 +1381,7 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
     // T <= kXNarrowT: every tile holds at most T tokens, so the narrow ring shape fits;
     // its 128-column K steps need K (H for gate/up, I for down) a multiple of 128
     const bool narrow = p.T <= kXNarrowT;
-    const XLaunch gu = pick_gemm(b8, narrow, p.H), dn = pick_gemm(b8, narrow, g0.I);
+    const XLaunch gu = pick_gemm(b8, narrow, false, p.H), dn = pick_gemm(b8, narrow, true, g0.I);
     if ((e = launch_pdl(gu.kern, dim3(persistent_grid(maxt * g.m_tiles)), dim3(kXThreads), gu.smem, st, g, xmap,
                         gu_pool, gu_shared)) != cudaSuccess)
         return e;
