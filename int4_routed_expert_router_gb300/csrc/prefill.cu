@@ -1174,13 +1174,16 @@ __global__ void __launch_bounds__(kXThreads, 1) expert_gemm_kernel(const GemmPar
 // ---------------------------------------------------------------- combine
 
 // out[t] = sum_j w[t][j] ypair[pos(t, j)] (route order) + gate[t] ypair[P + t]
-// (+ residual), from the fp16 expert outputs, in fp32.
+// (+ residual), from the fp16 expert outputs, in fp32. Block b: token b / nxb,
+// columns 1024 (b % nxb) .. + 1023 (nxb = H / 1024 rounded up; the token
+// index is in x, whose range covers SMOE_MAX_TOKENS, unlike y's 65,535).
 __global__ void __launch_bounds__(256) combine_kernel(const PrefillParams p)
 {
     pdl_wait();                                   // the predecessor's writes are visible
     pdl_trigger();
-    const int t = blockIdx.y;
-    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    const int nxb = (p.H / 4 + 255) / 256;
+    const int t = int(blockIdx.x) / nxb;
+    const int c = ((int(blockIdx.x) - t * nxb) * blockDim.x + threadIdx.x) * 4;
     if (c >= p.H) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     auto add = [&](int row, float wt) {
@@ -1392,7 +1395,7 @@ cudaError_t launch_prefill(const PrefillParams &p, const GemmParams &g0, cudaStr
                         dn_pool, dn_shared)) != cudaSuccess)
         return e;
     if ((e = prof_record(nprof > 2 ? prof[2] : nullptr, st)) != cudaSuccess) return e;
-    return launch_pdl(combine_kernel, dim3((p.H / 4 + 255) / 256, p.T), dim3(256), 0, st, p);
+    return launch_pdl(combine_kernel, dim3(unsigned((p.H / 4 + 255) / 256) * unsigned(p.T)), dim3(256), 0, st, p);
 }
 
 }  // namespace smoe

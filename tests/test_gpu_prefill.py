@@ -120,6 +120,30 @@ def test_prefill_8192_tokens_sampled(name):
     assert np.array_equal(out, gpu_forward(pool, 0, x, ids, w, gate))
 
 
+def test_prefill_at_the_token_limit():
+    """T = SMOE_MAX_TOKENS (2^20 tokens, the largest call the boundary takes)
+    on the tiny shape: about 262,000 pairs per expert (some 1,400 tiles each),
+    the bucketed path's row offsets and the gather's byte offsets near their
+    32-bit bounds. x is 16 seeded blocks of 65,536 tokens. The routing and
+    outputs of a seeded sample that holds the first and last tokens, a token of
+    every block and a token of every expert, against the oracle; every output
+    finite."""
+    wl = synthetic.WORKLOADS["tiny"]
+    pool, inp = W.DevicePool(wl, n_layers=1), W.LayerInputs(wl, 1)
+    T, blk = smoe.MAX_TOKENS, 1 << 16
+    x = np.concatenate([synthetic.activations(wl.seed, blk, wl.H, tag=5000 + j) for j in range(T // blk)])
+    ids, w, gate = gpu_route(pool, inp, 0, x)
+    out = gpu_forward(pool, 0, x, ids, w, gate)
+    assert np.isfinite(synthetic.bf16_bits_to_f32(out)).all()
+    counts = np.bincount(ids.ravel(), minlength=wl.E)
+    assert counts.sum() == T * wl.k and counts.min() > 0
+    edges = [0, 1, T - 2, T - 1] + [j * blk + 7 for j in range(T // blk)]
+    sample = np.union1d(covering_sample(ids, 48, wl.E), edges)
+    ref = oracle_shards.tokens_sharded(wl.name, 0, x[sample], ids[sample], inp.Wr_bits[0], inp.ws_bits[0])
+    routing_ok(ids[sample], w[sample], gate[sample], ref, wl.k)
+    assert_output_close(out[sample], ref["out64"])
+
+
 def test_decode_and_prefill_agree(tiny):
     """Each token decoded alone (T = 1) equals the same tokens run as one
     batch through the bucketed path, within the layer tolerance."""
