@@ -244,6 +244,10 @@ WORKLOADS = {
                  "permuted slots", bits=8),
         Workload("prefill80b_int8", 2048, 512, 10, 512, 512, 8192, 1, False, False, 8208,
                  "80B-shaped prefill with MLX 8-bit experts: T=8192, uniform router", bits=8),
+        Workload("limits_e1024_k16", 2048, 1024, 16, 512, 512, 64, 2, False, False, 10016,
+                 "the boundary's largest router: H=2048, E=1024, k=16, I=512, T=64"),
+        Workload("limits_k1", 512, 8, 1, 128, 128, 64, 2, False, False, 1008,
+                 "top-1 routing: H=512, E=8, k=1, I=128, T=64"),
     ]
 }
 
